@@ -1,0 +1,202 @@
+"""fp64 CPU attention oracle -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline / reference
+legs of ``bench.py`` may import this module.  The product path (the CUDA
+library ``libfa_gb300.so`` and its Python binding) never imports it, and the
+two share no code.
+
+The arithmetic lives in ``attn_oracle.c`` (plain C, IEEE double); this file
+builds that library with gcc on first use, converts the fp16 / bf16 input bit
+patterns to exact doubles, and loops over (batch, head).  It computes the
+textbook definition of scaled-dot-product attention described in the
+flash-attention-cuda README ("What is Attention?", "The Problem", and the
+causal row of the "Kernel design" table): explicit scores, max-subtracted
+softmax, weighted sum of the value rows.
+
+Every function here is pinned by ``tests/test_oracle_pins.py``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+from concurrent.futures import ThreadPoolExecutor
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "attn_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile attn_oracle.c into a shared library (gcc, -O2, no fast-math)."""
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c99", "-fPIC", "-shared", "-fno-fast-math",
+           "-ffp-contract=off", _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            dp = ctypes.POINTER(ctypes.c_double)
+            lp = ctypes.POINTER(ctypes.c_long)
+            lib.oracle_attention_head.argtypes = [
+                dp, dp, dp, dp, ctypes.c_long, ctypes.c_long, ctypes.c_int,
+                ctypes.c_int, ctypes.c_double, lp, ctypes.c_long, dp]
+            lib.oracle_attention_head.restype = ctypes.c_int
+            lib.oracle_decode_head.argtypes = [
+                dp, dp, dp, ctypes.c_long, ctypes.c_long, ctypes.c_int,
+                ctypes.c_double, dp]
+            lib.oracle_decode_head.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def _dptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+# --------------------------------------------------------------------------
+# Exact decoding of the 16-bit input formats into float64.
+# --------------------------------------------------------------------------
+def f16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
+    """IEEE binary16 bit patterns (uint16) -> exact float64 values."""
+    return np.asarray(bits, dtype=np.uint16).view(np.float16).astype(np.float64)
+
+
+def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
+    """bfloat16 bit patterns (uint16) -> exact float64 values.
+
+    bfloat16 is the upper half of an IEEE binary32, so shifting the pattern
+    left by 16 bits gives the binary32 with the same value.
+    """
+    b32 = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)
+    return b32.view(np.float32).astype(np.float64)
+
+
+def bits_to_f64(bits: np.ndarray, dtype: str) -> np.ndarray:
+    if dtype == "f16":
+        return f16_bits_to_f64(bits)
+    if dtype == "bf16":
+        return bf16_bits_to_f64(bits)
+    raise ValueError(f"unknown 16-bit dtype {dtype!r}")
+
+
+# --------------------------------------------------------------------------
+# Prefill (batched, multi-head) and decode.
+# --------------------------------------------------------------------------
+def attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, causal: bool,
+              scale: float, rows=None, threads: int = 1) -> np.ndarray:
+    """O = softmax(scale * Q K^T [causal mask]) V for every (batch, head).
+
+    q, k, v: float64 arrays [B, H, N, d] (or [N, d] for one head).
+    rows: None (all rows) or a sequence of query indices, the same for every
+    head; the result then has shape [B, H, len(rows), d].
+    threads: heads are independent, so they may be spread over host threads.
+    """
+    single = q.ndim == 2
+    if single:
+        q, k, v = q[None, None], k[None, None], v[None, None]
+    q = np.ascontiguousarray(q, dtype=np.float64)
+    k = np.ascontiguousarray(k, dtype=np.float64)
+    v = np.ascontiguousarray(v, dtype=np.float64)
+    B, H, n_q, d = q.shape
+    n_k = k.shape[2]
+    if rows is None:
+        row_arr = None
+        n_rows = n_q
+    else:
+        row_arr = np.ascontiguousarray(np.asarray(rows, dtype=np.int64)).astype(np.int_)
+        n_rows = len(row_arr)
+    out = np.zeros((B, H, n_rows, d), dtype=np.float64)
+    lib = _load()
+    rows_ptr = (row_arr.ctypes.data_as(ctypes.POINTER(ctypes.c_long))
+                if row_arr is not None else None)
+
+    def one(bh):
+        b, h = divmod(bh, H)
+        o = np.zeros((n_rows, d), dtype=np.float64)
+        rc = lib.oracle_attention_head(
+            _dptr(q[b, h]), _dptr(k[b, h]), _dptr(v[b, h]), _dptr(o),
+            n_q, n_k, d, int(bool(causal)), float(scale), rows_ptr, n_rows, None)
+        if rc != 0:
+            raise RuntimeError("oracle_attention_head failed")
+        out[b, h] = o
+
+    if threads > 1 and B * H > 1:
+        with ThreadPoolExecutor(max_workers=threads) as ex:
+            list(ex.map(one, range(B * H)))
+    else:
+        for bh in range(B * H):
+            one(bh)
+    return out[0, 0] if single else out
+
+
+def attention_weights(q: np.ndarray, k: np.ndarray, causal: bool, scale: float,
+                      rows=None) -> np.ndarray:
+    """The softmax weight rows P[i, :] of one head (zero where masked)."""
+    q = np.ascontiguousarray(q, dtype=np.float64)
+    k = np.ascontiguousarray(k, dtype=np.float64)
+    n_q, d = q.shape
+    n_k = k.shape[0]
+    if rows is None:
+        rows = np.arange(n_q)
+    row_arr = np.ascontiguousarray(np.asarray(rows, dtype=np.int64)).astype(np.int_)
+    n_rows = len(row_arr)
+    v = np.zeros((n_k, d), dtype=np.float64)
+    o = np.zeros((n_rows, d), dtype=np.float64)
+    p = np.zeros((n_rows, n_k), dtype=np.float64)
+    rc = _load().oracle_attention_head(
+        _dptr(q), _dptr(k), _dptr(v), _dptr(o), n_q, n_k, d, int(bool(causal)),
+        float(scale), row_arr.ctypes.data_as(ctypes.POINTER(ctypes.c_long)),
+        n_rows, _dptr(p))
+    if rc != 0:
+        raise RuntimeError("oracle_attention_head failed")
+    return p
+
+
+def decode(q: np.ndarray, k_cache: np.ndarray, v_cache: np.ndarray,
+           seq_lens, scale: float, threads: int = 1) -> np.ndarray:
+    """Decode: each (b, h) query row attends over cache rows [0, seq_lens[b]).
+
+    q: [B, H, 1, d] (or [B, H, d]); caches: [B, H, max_len, d]; returns [B, H, 1, d].
+    """
+    q = np.ascontiguousarray(q, dtype=np.float64).reshape(k_cache.shape[0], k_cache.shape[1], -1)
+    k_cache = np.ascontiguousarray(k_cache, dtype=np.float64)
+    v_cache = np.ascontiguousarray(v_cache, dtype=np.float64)
+    B, H, max_len, d = k_cache.shape
+    lens = np.asarray(seq_lens, dtype=np.int64).reshape(-1)
+    out = np.zeros((B, H, 1, d), dtype=np.float64)
+    lib = _load()
+
+    def one(bh):
+        b, h = divmod(bh, H)
+        o = np.zeros(d, dtype=np.float64)
+        rc = lib.oracle_decode_head(_dptr(q[b, h]), _dptr(k_cache[b, h]),
+                                    _dptr(v_cache[b, h]), int(lens[b]), max_len,
+                                    d, float(scale), _dptr(o))
+        if rc != 0:
+            raise RuntimeError("oracle_decode_head failed")
+        out[b, h, 0] = o
+
+    if threads > 1 and B * H > 1:
+        with ThreadPoolExecutor(max_workers=threads) as ex:
+            list(ex.map(one, range(B * H)))
+    else:
+        for bh in range(B * H):
+            one(bh)
+    return out
