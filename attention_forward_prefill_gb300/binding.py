@@ -1,0 +1,230 @@
+"""ctypes binding over libfa_gb300.so (C ABI declared in include/fa.h).
+
+The ``fa_*`` functions mirror the C entry points one to one (pointers as
+Python ints, streams as ints).  ``prefill`` / ``decode`` are the two calls of
+the flash-attention-cuda README's usage section, taking torch tensors: they
+only check and marshal arguments, allocate the output, and call the library.
+Every step of the computation runs in the library's CUDA kernels; if the
+library is missing this module raises -- there is no CPU fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+from . import build as _build
+
+FA_F16, FA_BF16, FA_F32 = 0, 1, 2
+FA_FLAG_NONE, FA_FLAG_NO_CAUSAL_SKIP = 0, 1
+FA_OK = 0
+STATUS_NAMES = {
+    0: "FA_OK", 1: "FA_ERR_NULL", 2: "FA_ERR_SHAPE", 3: "FA_ERR_HEAD_DIM",
+    4: "FA_ERR_DTYPE", 5: "FA_ERR_ALIGN", 6: "FA_ERR_SCALE", 7: "FA_ERR_ARCH",
+    8: "FA_ERR_WORKSPACE", 9: "FA_ERR_CUDA", 10: "FA_ERR_WATCHDOG",
+    11: "FA_ERR_ALIAS", 12: "FA_ERR_SPLITS",
+}
+
+_lock = threading.Lock()
+_lib = None
+
+_vp, _i, _f, _u, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_uint, ctypes.c_size_t
+_SIGNATURES = {
+    "fa_prefill": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp]),
+    "fa_prefill_ex": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _i, _u, _vp]),
+    "fa_decode": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _vp]),
+    "fa_decode_ex": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _i, _i, _vp, _sz, _vp]),
+    "fa_decode_choose_splits": (_i, [_i, _i, _i, _i]),
+    "fa_decode_chunk_len": (_i, [_i, _i]),
+    "fa_decode_workspace_bytes": (_sz, [_i, _i, _i, _i, _i]),
+    "fa_status_string": (ctypes.c_char_p, [_i]),
+    "fa_last_cuda_error": (_i, []),
+    "fa_device_status": (_i, [_i]),
+    "fa_version": (_i, []),
+}
+
+
+class FaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS_NAMES.get(status, status)} "
+                         f"({status_string(status)})")
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load(build_if_missing: bool = False):
+    """Load libfa_gb300.so (building it first only if asked)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.LIB_PATH
+            if not os.path.exists(path):
+                if not build_if_missing:
+                    raise RuntimeError(
+                        f"{path} is missing: build it with attention_forward_prefill_gb300.build"
+                        ".build() (there is no CPU fallback)")
+                _build.build()
+            lib = ctypes.CDLL(path)
+            for name, (res, args) in _SIGNATURES.items():
+                fn = getattr(lib, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = lib
+    return _lib
+
+
+# ---------------------------------------------------------------- raw C ABI
+def fa_prefill(q, k, v, out, B, H, N, d, causal, scale, stream=0) -> int:
+    return load().fa_prefill(q, k, v, out, B, H, N, d, int(causal), float(scale), stream)
+
+
+def fa_prefill_ex(q, k, v, out, B, H, N, d, causal, scale, in_dtype, out_dtype, flags=0,
+                  stream=0) -> int:
+    return load().fa_prefill_ex(q, k, v, out, B, H, N, d, int(causal), float(scale),
+                                in_dtype, out_dtype, flags, stream)
+
+
+def fa_decode(q, k_cache, v_cache, seq_lens, out, B, H, max_len, d, scale, stream=0) -> int:
+    return load().fa_decode(q, k_cache, v_cache, seq_lens, out, B, H, max_len, d,
+                            float(scale), stream)
+
+
+def fa_decode_ex(q, k_cache, v_cache, seq_lens, out, B, H, max_len, d, scale, in_dtype,
+                 out_dtype, num_splits=0, workspace=None, workspace_bytes=0, stream=0) -> int:
+    return load().fa_decode_ex(q, k_cache, v_cache, seq_lens, out, B, H, max_len, d,
+                               float(scale), in_dtype, out_dtype, num_splits, workspace,
+                               workspace_bytes, stream)
+
+
+def fa_decode_choose_splits(B, H, max_len, num_sms=0) -> int:
+    return load().fa_decode_choose_splits(B, H, max_len, num_sms)
+
+
+def fa_decode_chunk_len(max_len, num_splits) -> int:
+    return load().fa_decode_chunk_len(max_len, num_splits)
+
+
+def fa_decode_workspace_bytes(B, H, max_len, d, num_splits) -> int:
+    return load().fa_decode_workspace_bytes(B, H, max_len, d, num_splits)
+
+
+def status_string(status: int) -> str:
+    return load().fa_status_string(status).decode()
+
+
+def fa_last_cuda_error() -> int:
+    return load().fa_last_cuda_error()
+
+
+def fa_device_status(reset: bool = False) -> int:
+    return load().fa_device_status(int(reset))
+
+
+def fa_version() -> int:
+    return load().fa_version()
+
+
+# ---------------------------------------------------------------- torch calls
+def _torch():
+    import torch
+    return torch
+
+
+def dtype_code(dt) -> int:
+    torch = _torch()
+    if dt == torch.float16:
+        return FA_F16
+    if dt == torch.bfloat16:
+        return FA_BF16
+    if dt == torch.float32:
+        return FA_F32
+    raise TypeError(f"unsupported dtype {dt}")
+
+
+def _check_cuda(name, t, shape=None, dtype=None):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} has dtype {t.dtype}, expected {dtype}")
+
+
+def _stream_handle(device) -> int:
+    torch = _torch()
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def prefill(q, k, v, causal: bool = False, scale: float | None = None, out_dtype=None,
+            flags: int = 0, out=None):
+    """out = softmax(scale * q k^T [causal]) v for tensors [B, H, N, d] (fp16/bf16).
+
+    CUDA inputs run on the current stream and return a CUDA tensor.  Host
+    inputs are copied to the current device first and the result is copied
+    back to host memory (the end-to-end form of the same call).
+    """
+    torch = _torch()
+    host = not q.is_cuda
+    if host:
+        dev = torch.device("cuda", torch.cuda.current_device())
+        res = prefill(q.to(dev, non_blocking=True), k.to(dev, non_blocking=True),
+                      v.to(dev, non_blocking=True), causal, scale, out_dtype, flags)
+        dst = torch.empty(res.shape, dtype=res.dtype, pin_memory=q.is_pinned())
+        dst.copy_(res, non_blocking=False)
+        return dst
+    B, H, N, d = q.shape
+    _check_cuda("q", q)
+    _check_cuda("k", k, q.shape, q.dtype)
+    _check_cuda("v", v, q.shape, q.dtype)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    out_dtype = q.dtype if out_dtype is None else out_dtype
+    if out is None:
+        out = torch.empty(q.shape, dtype=out_dtype, device=q.device)
+    else:
+        _check_cuda("out", out, q.shape, out_dtype)
+    rc = fa_prefill_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, H, N, d,
+                       causal, scale, dtype_code(q.dtype), dtype_code(out_dtype), flags,
+                       _stream_handle(q.device))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_prefill_ex")
+    return out
+
+
+def decode(q, k_cache, v_cache, seq_lens, scale: float | None = None, out_dtype=None,
+           num_splits: int = 0, workspace=None, out=None):
+    """One query row per (b, h) over the first seq_lens[b] rows of the cache.
+
+    q: [B, H, 1, d]; caches: [B, H, max_len, d]; seq_lens: int32 [B] on the
+    same device.  Returns [B, H, 1, d].
+    """
+    torch = _torch()
+    B, H, max_len, d = k_cache.shape
+    _check_cuda("k_cache", k_cache)
+    _check_cuda("v_cache", v_cache, k_cache.shape, k_cache.dtype)
+    _check_cuda("q", q, (B, H, 1, d), k_cache.dtype)
+    _check_cuda("seq_lens", seq_lens, (B,), torch.int32)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    out_dtype = q.dtype if out_dtype is None else out_dtype
+    if out is None:
+        out = torch.empty((B, H, 1, d), dtype=out_dtype, device=q.device)
+    else:
+        _check_cuda("out", out, (B, H, 1, d), out_dtype)
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        _check_cuda("workspace", workspace)
+        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    rc = fa_decode_ex(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), seq_lens.data_ptr(),
+                      out.data_ptr(), B, H, max_len, d, scale, dtype_code(q.dtype),
+                      dtype_code(out_dtype), num_splits, ws_ptr, ws_bytes,
+                      _stream_handle(q.device))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_decode_ex")
+    return out

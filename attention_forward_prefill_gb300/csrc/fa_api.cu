@@ -1,0 +1,271 @@
+// fa_api.cu -- the extern "C" boundary of libfa_gb300.so (declared in
+// include/fa.h).  Argument validation happens before any CUDA call, so every
+// argument error is reported without touching a device.  The interface
+// follows the two calls of the flash-attention-cuda README ("Installation"
+// usage: prefill(q, k, v, causal, scale) and decode(q, k_cache, v_cache,
+// seq_lens, scale)) with the validation its bindings layer performs
+// ("Project structure": bindings.cpp, "input validation").
+#include <climits>
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "fa_internal.h"
+
+namespace fa {
+
+namespace {
+thread_local int t_last_cuda_error = 0;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_dev_mu;
+DeviceInfo g_dev_cache[kMaxDevices];
+bool g_dev_have[kMaxDevices] = {};
+
+constexpr int kDecodeRowAlign = 64;       // chunk lengths are multiples of this
+constexpr int kDecodeAutoMaxChunk = 4096; // automatic choice keeps scores <= 16 KB
+constexpr int kDecodeMaxChunk = 48 * 1024;// explicit choice: scores <= 192 KB smem
+
+bool misaligned(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; }
+
+bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+    return a0 < b0 + nb && b0 < a0 + na;
+}
+
+size_t dtype_size(int dt) { return dt == FA_F32 ? 4 : 2; }
+
+long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
+
+int decode_effective_splits(int max_len, int splits, int *chunk_out) {
+    const long long chunk =
+        ceil_div(ceil_div(max_len, splits), kDecodeRowAlign) * kDecodeRowAlign;
+    if (chunk_out) *chunk_out = static_cast<int>(chunk);
+    return static_cast<int>(ceil_div(max_len, chunk));
+}
+
+size_t ws_ml_bytes(long long bh, int splits) {
+    return static_cast<size_t>((bh * splits * 2 * 4 + 255) / 256 * 256);
+}
+}  // namespace
+
+int cuda_fail(cudaError_t e) {
+    t_last_cuda_error = static_cast<int>(e);
+    return FA_ERR_CUDA;
+}
+
+int current_device_info(DeviceInfo *out) {
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (dev < 0 || dev >= kMaxDevices) return cuda_fail(cudaErrorInvalidDevice);
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    if (!g_dev_have[dev]) {
+        DeviceInfo d;
+        d.device = dev;
+        int v = 0;
+        if ((e = cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev)) ||
+            (e = cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev)) ||
+            (e = cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev)) ||
+            (e = cudaDeviceGetAttribute(&d.l2_bytes, cudaDevAttrL2CacheSize, dev)) ||
+            (e = cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)))
+            return cuda_fail(e);
+        d.max_smem_optin = static_cast<size_t>(v);
+        g_dev_cache[dev] = d;
+        g_dev_have[dev] = true;
+    }
+    *out = g_dev_cache[dev];
+    if (!(out->cc_major == 10 && out->cc_minor == 3)) return FA_ERR_ARCH;
+    return FA_OK;
+}
+
+}  // namespace fa
+
+using namespace fa;
+
+extern "C" {
+
+int fa_version(void) { return 1 * 10000 + 0 * 100 + 0; }
+
+const char *fa_status_string(int status) {
+    switch (status) {
+        case FA_OK: return "ok";
+        case FA_ERR_NULL: return "a required pointer is NULL";
+        case FA_ERR_SHAPE: return "bad shape: sizes must be >= 1 and fit in int32";
+        case FA_ERR_HEAD_DIM: return "unsupported head dimension (64 or 128)";
+        case FA_ERR_DTYPE: return "unsupported dtype combination";
+        case FA_ERR_ALIGN: return "a pointer is not 16-byte aligned";
+        case FA_ERR_SCALE: return "scale is not finite";
+        case FA_ERR_ARCH: return "device is not compute capability 10.3 (sm_103a)";
+        case FA_ERR_WORKSPACE: return "workspace too small or allocation failed";
+        case FA_ERR_CUDA: return "CUDA runtime error (see fa_last_cuda_error)";
+        case FA_ERR_WATCHDOG: return "a device-side wait ran out of time";
+        case FA_ERR_ALIAS: return "output overlaps an input";
+        case FA_ERR_SPLITS: return "num_splits out of range";
+        default: return "unknown status";
+    }
+}
+
+int fa_last_cuda_error(void) { return t_last_cuda_error; }
+
+int fa_device_status(int reset) {
+    if (cudaDeviceSynchronize() != cudaSuccess) return -1;
+    return read_prefill_status(reset);
+}
+
+int fa_prefill_ex(const void *q, const void *k, const void *v, void *out, int B, int H, int N,
+                  int d, int causal, float scale, fa_dtype in_dtype, fa_dtype out_dtype,
+                  unsigned flags, void *stream) {
+    if (!q || !k || !v || !out) return FA_ERR_NULL;
+    if (B < 1 || H < 1 || N < 1) return FA_ERR_SHAPE;
+    if (static_cast<long long>(B) * H * N > INT_MAX) return FA_ERR_SHAPE;
+    if (d != 64 && d != 128) return FA_ERR_HEAD_DIM;
+    if (in_dtype != FA_F16 && in_dtype != FA_BF16) return FA_ERR_DTYPE;
+    if (out_dtype != FA_F16 && out_dtype != FA_BF16 && out_dtype != FA_F32) return FA_ERR_DTYPE;
+    if (misaligned(q) || misaligned(k) || misaligned(v) || misaligned(out)) return FA_ERR_ALIGN;
+    if (!std::isfinite(scale)) return FA_ERR_SCALE;
+    const size_t elems = static_cast<size_t>(B) * H * N * d;
+    const size_t in_bytes = elems * 2, out_bytes = elems * dtype_size(out_dtype);
+    if (overlaps(out, out_bytes, q, in_bytes) || overlaps(out, out_bytes, k, in_bytes) ||
+        overlaps(out, out_bytes, v, in_bytes))
+        return FA_ERR_ALIAS;
+    DeviceInfo dev;
+    int rc = current_device_info(&dev);
+    if (rc != FA_OK) return rc;
+    PrefillLaunch a;
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.out = out;
+    a.B = B;
+    a.H = H;
+    a.N = N;
+    a.d = d;
+    a.causal = causal ? 1 : 0;
+    a.no_skip = (flags & FA_FLAG_NO_CAUSAL_SKIP) ? 1 : 0;
+    a.scale = scale;
+    a.in_bf16 = in_dtype == FA_BF16 ? 1 : 0;
+    a.out_dtype = out_dtype;
+    return launch_prefill(a, dev, static_cast<cudaStream_t>(stream));
+}
+
+int fa_prefill(const void *q, const void *k, const void *v, void *out, int B, int H, int N, int d,
+               int causal, float scale, void *stream) {
+    return fa_prefill_ex(q, k, v, out, B, H, N, d, causal, scale, FA_F16, FA_F16, FA_FLAG_NONE,
+                         stream);
+}
+
+int fa_decode_chunk_len(int max_len, int num_splits) {
+    if (max_len < 1 || num_splits < 1) return -FA_ERR_SHAPE;
+    int chunk = 0;
+    decode_effective_splits(max_len, num_splits, &chunk);
+    return chunk;
+}
+
+int fa_decode_choose_splits(int B, int H, int max_len, int num_sms) {
+    if (B < 1 || H < 1 || max_len < 1) return -FA_ERR_SHAPE;
+    if (num_sms <= 0) {
+        DeviceInfo dev;
+        int rc = current_device_info(&dev);
+        if (rc != FA_OK) return -rc;
+        num_sms = dev.num_sms;
+    }
+    const long long bh = static_cast<long long>(B) * H;
+    // About two CTAs per SM, counting every (b, h, chunk) CTA of the grid.
+    long long splits = ceil_div(2LL * num_sms, bh);
+    const long long max_splits = ceil_div(max_len, kDecodeRowAlign);
+    const long long min_splits = ceil_div(max_len, kDecodeAutoMaxChunk);
+    if (splits > max_splits) splits = max_splits;
+    if (splits < min_splits) splits = min_splits;
+    if (splits < 1) splits = 1;
+    return decode_effective_splits(max_len, static_cast<int>(splits), nullptr);
+}
+
+size_t fa_decode_workspace_bytes(int B, int H, int max_len, int d, int num_splits) {
+    if (B < 1 || H < 1 || max_len < 1 || num_splits < 1) return 0;
+    if (d != 64 && d != 128) return 0;
+    const int splits = decode_effective_splits(max_len, num_splits, nullptr);
+    const long long bh = static_cast<long long>(B) * H;
+    return ws_ml_bytes(bh, splits) + static_cast<size_t>(bh) * splits * d * 4;
+}
+
+int fa_decode_ex(const void *q, const void *k_cache, const void *v_cache, const int32_t *seq_lens,
+                 void *out, int B, int H, int max_len, int d, float scale, fa_dtype in_dtype,
+                 fa_dtype out_dtype, int num_splits, void *workspace, size_t workspace_bytes,
+                 void *stream) {
+    if (!q || !k_cache || !v_cache || !seq_lens || !out) return FA_ERR_NULL;
+    if (B < 1 || H < 1 || max_len < 1) return FA_ERR_SHAPE;
+    if (static_cast<long long>(B) * H * max_len > INT_MAX) return FA_ERR_SHAPE;
+    if (d != 64 && d != 128) return FA_ERR_HEAD_DIM;
+    if (in_dtype != FA_F16 && in_dtype != FA_BF16) return FA_ERR_DTYPE;
+    if (out_dtype != FA_F16 && out_dtype != FA_BF16 && out_dtype != FA_F32) return FA_ERR_DTYPE;
+    if (misaligned(q) || misaligned(k_cache) || misaligned(v_cache) || misaligned(out) ||
+        (reinterpret_cast<uintptr_t>(seq_lens) & 3u) != 0 || (workspace && misaligned(workspace)))
+        return FA_ERR_ALIGN;
+    if (!std::isfinite(scale)) return FA_ERR_SCALE;
+    const long long max_splits = ceil_div(max_len, kDecodeRowAlign);
+    if (num_splits < 0 || num_splits > max_splits) return FA_ERR_SPLITS;
+    const size_t bh = static_cast<size_t>(B) * H;
+    const size_t out_bytes = bh * d * dtype_size(out_dtype);
+    const size_t cache_bytes = bh * static_cast<size_t>(max_len) * d * 2;
+    if (overlaps(out, out_bytes, q, bh * d * 2) || overlaps(out, out_bytes, k_cache, cache_bytes) ||
+        overlaps(out, out_bytes, v_cache, cache_bytes) ||
+        overlaps(out, out_bytes, seq_lens, static_cast<size_t>(B) * 4))
+        return FA_ERR_ALIAS;
+
+    int splits = num_splits;
+    if (splits == 0) {
+        splits = fa_decode_choose_splits(B, H, max_len, 0);
+        if (splits < 0) return -splits;
+    }
+    int chunk = 0;
+    splits = decode_effective_splits(max_len, splits, &chunk);
+    if (chunk > kDecodeMaxChunk) return FA_ERR_SPLITS;
+    const size_t need = fa_decode_workspace_bytes(B, H, max_len, d, splits);
+    if (workspace && workspace_bytes < need) return FA_ERR_WORKSPACE;
+
+    DeviceInfo dev;
+    int rc = current_device_info(&dev);
+    if (rc != FA_OK) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    void *ws = workspace;
+    if (!ws) {
+        cudaError_t e = cudaMallocAsync(&ws, need, st);
+        if (e != cudaSuccess) {
+            cuda_fail(e);
+            return FA_ERR_WORKSPACE;
+        }
+    }
+    DecodeLaunch a;
+    a.q = q;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.seq_lens = seq_lens;
+    a.out = out;
+    a.B = B;
+    a.H = H;
+    a.max_len = max_len;
+    a.d = d;
+    a.scale = scale;
+    a.in_bf16 = in_dtype == FA_BF16 ? 1 : 0;
+    a.out_dtype = out_dtype;
+    a.num_splits = splits;
+    a.chunk = chunk;
+    a.partial_ml = static_cast<float *>(ws);
+    a.partial_acc = reinterpret_cast<float *>(static_cast<char *>(ws) +
+                                              ws_ml_bytes(static_cast<long long>(bh), splits));
+    rc = launch_decode(a, dev, st);
+    if (!workspace) {
+        cudaError_t e = cudaFreeAsync(ws, st);
+        if (rc == FA_OK && e != cudaSuccess) rc = cuda_fail(e);
+    }
+    return rc;
+}
+
+int fa_decode(const void *q, const void *k_cache, const void *v_cache, const int32_t *seq_lens,
+              void *out, int B, int H, int max_len, int d, float scale, void *stream) {
+    return fa_decode_ex(q, k_cache, v_cache, seq_lens, out, B, H, max_len, d, scale, FA_F16,
+                        FA_F16, 0, nullptr, 0, stream);
+}
+
+}  // extern "C"

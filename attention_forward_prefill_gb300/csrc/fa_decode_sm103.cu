@@ -1,0 +1,288 @@
+// fa_decode_sm103.cu -- split-K decode: one query row per (b, h) over a ragged
+// KV cache (flash-attention-cuda README, "What did I implement?" generation
+// phase, and the "Kernel design" rows "Split-K decode + adaptive chunk" and
+// "Two-pass merge, no atomics").
+//
+// Kernel 1 (split): CTA (s, h, b) covers cache rows
+//   [s * chunk, min((s + 1) * chunk, len_b))
+// and writes the partial (m_s, l_s, acc_s) with scores kept in the exp2 domain
+// (c = scale * log2 e):  x_j = c * q.k_j,  m_s = max_j x_j,
+//   l_s = sum_j 2^(x_j - m_s),  acc_s = sum_j 2^(x_j - m_s) v_j.
+// A CTA whose chunk starts at or past len_b does nothing.
+// Kernel 2 (merge): one warp per (b, h), splits combined in index order:
+//   M = max_s m_s,  w_s = 2^(m_s - M),  O = sum_s w_s acc_s / sum_s w_s l_s.
+// Every reduction runs in a fixed order, so a given split count gives the
+// same bits on every run; there are no atomics.
+//
+// The split kernel is HBM-bound (about one FLOP per byte): it streams each K
+// row and each V row once with 16-byte loads, eight in flight per thread,
+// lanes of a warp covering whole rows so that every load is coalesced.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "fa_internal.h"
+#include "sm103_ptx.cuh"
+
+namespace fa {
+
+namespace {
+
+constexpr int kSplitThreads = 128;
+constexpr int kSplitWarps = kSplitThreads / 32;
+constexpr int kUnroll = 8;
+constexpr int kMergeWarps = 4;
+
+struct DParams {
+    const uint16_t *q;
+    const uint16_t *k;
+    const uint16_t *v;
+    const int32_t *seq_lens;
+    void *out;
+    float *ml;
+    float *acc;
+    int H;
+    int BH;
+    int max_len;
+    int chunk;
+    int splits;
+    int in_bf16;
+    int out_dtype;
+    float scale_log2;
+};
+
+__device__ __forceinline__ int clamp_len(int len, int max_len) {
+    return len < 0 ? 0 : (len > max_len ? max_len : len);
+}
+
+__device__ __forceinline__ void unpack8(const uint4 &w, int bf16, float (&f)[8]) {
+    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        float2 t;
+        if (bf16) {
+            t = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u[i]));
+        } else {
+            t = __half22float2(*reinterpret_cast<const __half2 *>(&u[i]));
+        }
+        f[2 * i] = t.x;
+        f[2 * i + 1] = t.y;
+    }
+}
+
+__device__ __forceinline__ uint4 ldg_stream(const uint16_t *p) {
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kSplitThreads)
+    decode_split_kernel(const DParams p) {
+    constexpr int LPK = D * 2 / 16;          // lanes per cache row (16 bytes each)
+    constexpr int KPW = 32 / LPK;            // rows per warp per step
+    constexpr int KPC = KPW * kSplitWarps;   // rows per CTA per step
+    extern __shared__ float sh[];            // [chunk] scores, then reduction scratch
+    __shared__ float red[kSplitWarps][D];
+    __shared__ float red1[kSplitWarps];
+
+    const int s = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int len = clamp_len(p.seq_lens[b], p.max_len);
+    const int start = s * p.chunk;
+    if (start >= len) return;
+    const int n = min(start + p.chunk, len) - start;
+    const size_t bh = static_cast<size_t>(b) * p.H + h;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int sub = lane % LPK, kw = lane / LPK;
+
+    float qf[8];
+    unpack8(*reinterpret_cast<const uint4 *>(p.q + bh * D + sub * 8), p.in_bf16, qf);
+    const uint16_t *kbase = p.k + (bh * p.max_len + start) * D + sub * 8;
+    const uint16_t *vbase = p.v + (bh * p.max_len + start) * D + sub * 8;
+    float *sc = sh;
+
+    // ---- scores x_j = c * q.k_j
+    // The loop bound is warp-uniform (base0); each lane's row is base0 + kw.
+    for (int base0 = warp * KPW; base0 < n; base0 += KPC * kUnroll) {
+        const int base = base0 + kw;
+        uint4 kr[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int key = base + u * KPC;
+            kr[u] = key < n ? ldg_stream(kbase + static_cast<size_t>(key) * D) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            float kf[8];
+            unpack8(kr[u], p.in_bf16, kf);
+            float dot = 0.f;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) dot = fmaf(qf[e], kf[e], dot);
+#pragma unroll
+            for (int off = 1; off < LPK; off <<= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
+            const int key = base + u * KPC;
+            if (sub == 0 && key < n) sc[key] = dot * p.scale_log2;
+        }
+    }
+    __syncthreads();
+
+    // ---- chunk maximum
+    float mx = -INFINITY;
+    for (int i = threadIdx.x; i < n; i += kSplitThreads) mx = fmaxf(mx, sc[i]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    if (lane == 0) red1[warp] = mx;
+    __syncthreads();
+    float m = red1[0];
+#pragma unroll
+    for (int w = 1; w < kSplitWarps; ++w) m = fmaxf(m, red1[w]);
+    __syncthreads();
+
+    // ---- weights 2^(x_j - m) and their sum
+    float sum = 0.f;
+    for (int i = threadIdx.x; i < n; i += kSplitThreads) {
+        const float e = ex2_approx(sc[i] - m);
+        sc[i] = e;
+        sum += e;
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+    if (lane == 0) red1[warp] = sum;
+    __syncthreads();
+    float l = red1[0];
+#pragma unroll
+    for (int w = 1; w < kSplitWarps; ++w) l += red1[w];
+
+    // ---- acc = sum_j w_j v_j
+    float acc[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+    for (int base0 = warp * KPW; base0 < n; base0 += KPC * kUnroll) {
+        const int base = base0 + kw;
+        uint4 vr[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int key = base + u * KPC;
+            vr[u] = key < n ? ldg_stream(vbase + static_cast<size_t>(key) * D) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int key = base + u * KPC;
+            const float w = key < n ? sc[key] : 0.f;
+            float vf[8];
+            unpack8(vr[u], p.in_bf16, vf);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[e] = fmaf(w, vf[e], acc[e]);
+        }
+    }
+#pragma unroll
+    for (int off = LPK; off < 32; off <<= 1)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], off);
+    if (kw == 0)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) red[warp][sub * 8 + e] = acc[e];
+    __syncthreads();
+
+    const size_t part = bh * p.splits + s;
+    for (int c = threadIdx.x; c < D; c += kSplitThreads) {
+        float a = red[0][c];
+#pragma unroll
+        for (int w = 1; w < kSplitWarps; ++w) a += red[w][c];
+        p.acc[part * D + c] = a;
+    }
+    if (threadIdx.x == 0) {
+        p.ml[part * 2 + 0] = m;
+        p.ml[part * 2 + 1] = l;
+    }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kMergeWarps * 32)
+    decode_merge_kernel(const DParams p) {
+    constexpr int EPL = D / 32;  // output elements per lane
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int gw = blockIdx.x * kMergeWarps + warp;
+    if (gw >= p.BH) return;
+    const int b = gw / p.H;
+    const int len = clamp_len(p.seq_lens[b], p.max_len);
+    const int n_act = (len + p.chunk - 1) / p.chunk;
+    float o[EPL];
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) o[e] = 0.f;
+    if (n_act > 0) {
+        const float *ml = p.ml + static_cast<size_t>(gw) * p.splits * 2;
+        const float *acc = p.acc + static_cast<size_t>(gw) * p.splits * D + lane * EPL;
+        float M = ml[0];
+        for (int s = 1; s < n_act; ++s) M = fmaxf(M, ml[2 * s]);
+        float L = 0.f;
+        for (int s = 0; s < n_act; ++s) {
+            const float w = ex2_approx(ml[2 * s] - M);
+            L = fmaf(w, ml[2 * s + 1], L);
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) o[e] = fmaf(w, acc[static_cast<size_t>(s) * D + e], o[e]);
+        }
+        const float inv = 1.0f / L;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) o[e] *= inv;
+    }
+    const size_t off = static_cast<size_t>(gw) * D + lane * EPL;
+    if (p.out_dtype == FA_F32) {
+        float *out = reinterpret_cast<float *>(p.out) + off;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) out[e] = o[e];
+    } else if (p.out_dtype == FA_BF16) {
+        __nv_bfloat16 *out = reinterpret_cast<__nv_bfloat16 *>(p.out) + off;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) out[e] = __float2bfloat16_rn(o[e]);
+    } else {
+        __half *out = reinterpret_cast<__half *>(p.out) + off;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) out[e] = __float2half_rn(o[e]);
+    }
+}
+
+template <int D>
+int launch_decode_d(const DecodeLaunch &a, cudaStream_t stream) {
+    DParams p;
+    p.q = static_cast<const uint16_t *>(a.q);
+    p.k = static_cast<const uint16_t *>(a.k_cache);
+    p.v = static_cast<const uint16_t *>(a.v_cache);
+    p.seq_lens = a.seq_lens;
+    p.out = a.out;
+    p.ml = a.partial_ml;
+    p.acc = a.partial_acc;
+    p.H = a.H;
+    p.BH = a.B * a.H;
+    p.max_len = a.max_len;
+    p.chunk = a.chunk;
+    p.splits = a.num_splits;
+    p.in_bf16 = a.in_bf16;
+    p.out_dtype = a.out_dtype;
+    p.scale_log2 = a.scale * 1.4426950408889634f;
+    const size_t smem = static_cast<size_t>(a.chunk) * sizeof(float);
+    cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<D>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return cuda_fail(e);
+    dim3 grid(a.num_splits, a.H, a.B);
+    decode_split_kernel<D><<<grid, kSplitThreads, smem, stream>>>(p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e);
+    const int mblocks = (p.BH + kMergeWarps - 1) / kMergeWarps;
+    decode_merge_kernel<D><<<mblocks, kMergeWarps * 32, 0, stream>>>(p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e);
+    return FA_OK;
+}
+
+}  // namespace
+
+int launch_decode(const DecodeLaunch &a, const DeviceInfo &dev, cudaStream_t stream) {
+    (void)dev;
+    if (a.d == 64) return launch_decode_d<64>(a, stream);
+    if (a.d == 128) return launch_decode_d<128>(a, stream);
+    return FA_ERR_HEAD_DIM;
+}
+
+}  // namespace fa

@@ -1,0 +1,61 @@
+// fa_internal.h -- declarations shared between the C-ABI layer (fa_api.cu)
+// and the kernel translation units.  Not part of the public interface.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/fa.h"
+
+namespace fa {
+
+struct DeviceInfo {
+    int device = -1;
+    int num_sms = 0;
+    int cc_major = 0;
+    int cc_minor = 0;
+    int l2_bytes = 0;
+    size_t max_smem_optin = 0;
+};
+
+// Cached attributes of the current device; returns FA_OK / FA_ERR_CUDA / FA_ERR_ARCH.
+int current_device_info(DeviceInfo *out);
+
+// Record a CUDA error for fa_last_cuda_error() and return FA_ERR_CUDA.
+int cuda_fail(cudaError_t e);
+
+struct PrefillLaunch {
+    const void *q, *k, *v;
+    void *out;
+    int B, H, N, d;
+    int causal;
+    int no_skip;
+    float scale;
+    int in_bf16;    // 1: bf16 inputs, 0: fp16
+    int out_dtype;  // fa_dtype
+};
+
+// Validated arguments -> encode tensor maps, launch the persistent kernel.
+int launch_prefill(const PrefillLaunch &a, const DeviceInfo &dev, cudaStream_t stream);
+
+struct DecodeLaunch {
+    const void *q, *k_cache, *v_cache;
+    const int32_t *seq_lens;
+    void *out;
+    int B, H, max_len, d;
+    float scale;
+    int in_bf16;
+    int out_dtype;
+    int num_splits;
+    int chunk;
+    float *partial_ml;   // [B][H][splits][2]  (m, l)
+    float *partial_acc;  // [B][H][splits][d]
+};
+
+int launch_decode(const DecodeLaunch &a, const DeviceInfo &dev, cudaStream_t stream);
+
+// Device-side watchdog words (one per kernel translation unit).
+int read_prefill_status(int reset);
+
+}  // namespace fa

@@ -1,0 +1,608 @@
+// fa_prefill_sm103.cu -- fused attention forward, prefill, for sm_103a.
+//
+// Method (flash-attention-cuda README, "What is Flash Attention?" and the
+// "Kernel design" table; "B200 attention kernel from scratch to near-SOTA in
+// 60 diagrams" for the Blackwell setting): the keys and values are streamed
+// through on-chip memory one 128-row tile at a time, each query row keeps a
+// running maximum m and a running denominator l in fp32, the fp32 output
+// accumulator is rescaled when m moves, and the N x N score table never
+// reaches HBM.  Tiles wholly above the causal diagonal are never visited.
+//
+// GB300 mapping (one persistent CTA per SM, 12 warps = 3 warpgroups):
+//   warps 0-3  softmax for query tile 0 (thread = row; TMEM lanes 0..127)
+//   warps 4-7  softmax for query tile 1
+//   warp  8    TMA producer: Q tiles, then K_j / V_j into a shared-memory ring
+//   warp  9    tcgen05 MMA issuer (one thread) and TMEM owner
+//   warps 10-11 idle
+// The softmax warpgroups hold a whole 128-key score row per thread, so they
+// take registers from the producer/MMA warpgroup with setmaxnreg.
+// TMEM (512 columns): S0 | S1 (128 fp32 columns each) | O0 | O1 (d columns
+// each).  P (16-bit) overwrites the first 64 columns of its S tile and feeds
+// the PV product straight from TMEM.  The two query tiles ping-pong: while
+// the softmax warps of one tile work on exponentials, the tensor core runs
+// the other tile's products.
+//
+// Softmax in the exp2 domain: with c = scale * log2(e), p = 2^(s*c - m_ref).
+// Rescaling is lazy: m_ref only moves when the tile maximum exceeds it by more
+// than TAU (log2 units), so p <= 2^TAU; O and l share m_ref, so the final O/l
+// is unchanged.
+#include <cfloat>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "fa_internal.h"
+#include "sm103_ptx.cuh"
+
+namespace fa {
+
+namespace {
+
+constexpr int kThreads = 384;
+// setmaxnreg split: 2 x 128 threads x kRegsSoftmax + 128 x kRegsOther must not
+// exceed kThreads x (registers at launch); the host checks the launch count.
+constexpr int kRegsSoftmax = 200;
+constexpr int kRegsOther = 104;
+constexpr int kMinLaunchRegs = (2 * 128 * kRegsSoftmax + 128 * kRegsOther + kThreads - 1) / kThreads;
+constexpr int kTmaWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kBlockM = 128;   // query rows per tile
+constexpr int kBlockN = 128;   // keys per tile
+constexpr int kRowsPerUnit = 2 * kBlockM;
+constexpr float kTau = 8.0f;   // lazy-rescale threshold, log2 units
+constexpr uint64_t kWatchdogNs = 1500ull * 1000ull * 1000ull;
+constexpr uint32_t kTmemCols = 512;
+
+__device__ int g_prefill_status = 0;
+
+template <int D>
+struct Layout {
+    static constexpr int kChunkBytes = kBlockM * 128;  // 128 rows x 64 16-bit columns
+    static constexpr int kChunks = D / 64;
+    static constexpr int kTileBytes = kChunks * kChunkBytes;
+    static constexpr int kStages = (D == 128) ? 4 : 8;
+    static constexpr int kQOff = 0;
+    static constexpr int kRingOff = 2 * kTileBytes;
+    static constexpr int kBarOff = kRingOff + kStages * kTileBytes;
+    // q_full, q_empty, s_full[2], p_full[2], o_done[2], drain, kv_full[S], kv_empty[S]
+    static constexpr int kNumBars = 9 + 2 * kStages;
+    static constexpr int kMiscOff = kBarOff + kNumBars * 8;
+    static constexpr int kSmemBytes = kMiscOff + 16 + 1024;  // + alignment slack
+    static constexpr uint32_t kSCol0 = 0, kSCol1 = 128;
+    static constexpr uint32_t kOCol0 = 256, kOCol1 = 256 + D;
+};
+
+struct Params {
+    void *out;
+    int N;
+    int BH;
+    int n_qb;      // 256-row query blocks per head
+    int n_units;   // BH * n_qb
+    int causal;
+    int no_skip;
+    int in_bf16;
+    int out_dtype;
+    int scale_neg;
+    float scale_log2;  // scale * log2(e)
+};
+
+__device__ __forceinline__ void unit_coords(const Params &p, int u, int &bh, int &qb) {
+    if (p.causal) {  // heaviest query blocks first
+        qb = p.n_qb - 1 - u / p.BH;
+        bh = u % p.BH;
+    } else {         // neighbouring CTAs share a head's K/V in L2
+        bh = u / p.n_qb;
+        qb = u % p.n_qb;
+    }
+}
+
+// Key tiles a 128-row query tile starting at row0 must visit (0 = no rows).
+__device__ __forceinline__ int kv_tiles(const Params &p, int row0) {
+    if (row0 >= p.N) return 0;
+    const int nk = (p.N + kBlockN - 1) / kBlockN;
+    if (!p.causal || p.no_skip) return nk;
+    const int last = min(row0 + kBlockM - 1, p.N - 1);
+    return last / kBlockN + 1;
+}
+
+// Warp-uniform bounded wait: lane 0 polls, the verdict is broadcast.
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag) {
+    int ok = 1;
+    if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort_flag, kWatchdogNs) ? 1 : 0;
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    return ok != 0;
+}
+
+template <int D>
+__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_addr, uint32_t k_addr,
+                                         uint32_t idesc) {
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = (kk >> 2) * Layout<D>::kChunkBytes + (kk & 3) * 32;
+        umma_ss(d_tmem, sdesc_sw128(q_addr + off, 16, 1024), sdesc_sw128(k_addr + off, 16, 1024),
+                idesc, kk > 0 ? 1u : 0u);
+    }
+}
+
+template <int D>
+__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_addr,
+                                         uint32_t idesc, bool accumulate) {
+#pragma unroll
+    for (int kk = 0; kk < kBlockN / 16; ++kk) {
+        // V tile is [key][d] with d contiguous: an MN-major B operand.  16 keys
+        // per step = two 8-key groups (SBO apart); 64-column slabs LBO apart.
+        umma_ts(d_tmem, p_tmem + kk * 8,
+                sdesc_sw128(v_addr + kk * 16 * 128, Layout<D>::kChunkBytes, 1024), idesc,
+                (accumulate || kk > 0) ? 1u : 0u);
+    }
+}
+
+__device__ __forceinline__ uint32_t pack2(float lo, float hi, int bf16) {
+    if (bf16) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+        return *reinterpret_cast<uint32_t *>(&h);
+    }
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+// One 32-column slice of a finished output row: O * inv_l -> out dtype.
+__device__ __forceinline__ void store_out32(void *dst, const uint32_t (&r)[32], float inv,
+                                            int out_dtype) {
+    if (out_dtype == FA_F32) {
+        uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+        for (int v = 0; v < 8; ++v) {
+            uint4 w;
+            w.x = __float_as_uint(__uint_as_float(r[4 * v + 0]) * inv);
+            w.y = __float_as_uint(__uint_as_float(r[4 * v + 1]) * inv);
+            w.z = __float_as_uint(__uint_as_float(r[4 * v + 2]) * inv);
+            w.w = __float_as_uint(__uint_as_float(r[4 * v + 3]) * inv);
+            d4[v] = w;
+        }
+    } else {
+        const int bf = out_dtype == FA_BF16;
+        uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+            uint4 w;
+            w.x = pack2(__uint_as_float(r[8 * v + 0]) * inv, __uint_as_float(r[8 * v + 1]) * inv, bf);
+            w.y = pack2(__uint_as_float(r[8 * v + 2]) * inv, __uint_as_float(r[8 * v + 3]) * inv, bf);
+            w.z = pack2(__uint_as_float(r[8 * v + 4]) * inv, __uint_as_float(r[8 * v + 5]) * inv, bf);
+            w.w = pack2(__uint_as_float(r[8 * v + 6]) * inv, __uint_as_float(r[8 * v + 7]) * inv, bf);
+            d4[v] = w;
+        }
+    }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_kernel(const __grid_constant__ CUtensorMap map_q,
+                   const __grid_constant__ CUtensorMap map_k,
+                   const __grid_constant__ CUtensorMap map_v, const Params p) {
+    using L = Layout<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kBarOff);
+    uint64_t *q_full = bars + 0;
+    uint64_t *q_empty = bars + 1;
+    uint64_t *s_full = bars + 2;   // [2]
+    uint64_t *p_full = bars + 4;   // [2]
+    uint64_t *o_done = bars + 6;   // [2]
+    uint64_t *drain = bars + 8;
+    uint64_t *kv_full = bars + 9;
+    uint64_t *kv_empty = bars + 9 + L::kStages;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kMiscOff);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kMiscOff + 4);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        mbar_init(q_full, 1);
+        mbar_init(q_empty, 1);
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(s_full + t, 1);
+            mbar_init(p_full + t, 128);
+            mbar_init(o_done + t, 1);
+        }
+        mbar_init(drain, 1);
+        for (int s = 0; s < L::kStages; ++s) {
+            mbar_init(kv_full + s, 1);
+            mbar_init(kv_empty + s, 1);
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == kMmaWarp) {
+        tmem_alloc(tmem_slot, kTmemCols);
+        tmem_relinquish();
+    }
+    if (warp == kTmaWarp && lane == 0) {
+        prefetch_tensormap(&map_q);
+        prefetch_tensormap(&map_k);
+        prefetch_tensormap(&map_v);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == kTmaWarp) {
+        // ------------------------------------------------------------ producer
+        regs_shrink<kRegsOther>();
+        if (lane == 0) {
+            const uint64_t pol_kv = l2_policy_evict_last();
+            const uint64_t pol_q = l2_policy_evict_first();
+            uint8_t *q_smem = smem + L::kQOff;
+            uint8_t *ring = smem + L::kRingOff;
+            uint32_t qc = 0, rc = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; u < p.n_units && ok; u += gridDim.x) {
+                int bh, qb;
+                unit_coords(p, u, bh, qb);
+                const int q0 = qb * kRowsPerUnit;
+                const int n0 = kv_tiles(p, q0), n1 = kv_tiles(p, q0 + kBlockM);
+                const int n = max(n0, n1);
+                if (qc > 0 && !mbar_wait(q_empty, (qc - 1) & 1, abort_flag, kWatchdogNs)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(q_full, (n1 > 0 ? 2 : 1) * L::kTileBytes);
+                for (int t = 0; t < (n1 > 0 ? 2 : 1); ++t)
+                    for (int c = 0; c < L::kChunks; ++c)
+                        tma_load_3d(q_smem + t * L::kTileBytes + c * L::kChunkBytes, &map_q, q_full,
+                                    c * 64, q0 + t * kBlockM, bh, pol_q);
+                ++qc;
+                for (int j = 0; j < n && ok; ++j) {
+                    for (int kv = 0; kv < 2; ++kv) {
+                        const uint32_t slot = rc % L::kStages;
+                        if (rc >= (uint32_t)L::kStages &&
+                            !mbar_wait(kv_empty + slot, ((rc / L::kStages) - 1) & 1, abort_flag,
+                                       kWatchdogNs)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(kv_full + slot, L::kTileBytes);
+                        for (int c = 0; c < L::kChunks; ++c)
+                            tma_load_3d(ring + slot * L::kTileBytes + c * L::kChunkBytes,
+                                        kv ? &map_v : &map_k, kv_full + slot, c * 64, j * kBlockN,
+                                        bh, pol_kv);
+                        ++rc;
+                    }
+                }
+            }
+            if (!ok) {
+                // Let every copy already issued land before the CTA goes away.
+                constexpr uint64_t kDrainNs = 200ull * 1000ull * 1000ull;
+                int dummy = 0;
+                if (qc > 0) mbar_wait(q_full, (qc - 1) & 1, &dummy, kDrainNs);
+                for (uint32_t i = (rc > (uint32_t)L::kStages ? rc - L::kStages : 0); i < rc; ++i)
+                    mbar_wait(kv_full + (i % L::kStages), (i / L::kStages) & 1, &dummy, kDrainNs);
+            }
+        }
+        __syncwarp();
+    } else if (warp == kMmaWarp) {
+        // ------------------------------------------------------------ MMA issuer
+        regs_shrink<kRegsOther>();
+        if (lane == 0) {
+            const uint32_t idesc_qk = idesc_f16(p.in_bf16 != 0, kBlockM, kBlockN, false, false);
+            const uint32_t idesc_pv = idesc_f16(p.in_bf16 != 0, kBlockM, D, false, true);
+            const uint32_t q_addr = smem_u32(smem + L::kQOff);
+            const uint32_t ring_addr = smem_u32(smem + L::kRingOff);
+            const uint32_t s_tmem0 = tmem + L::kSCol0, s_tmem1 = tmem + L::kSCol1;
+            const uint32_t o_tmem0 = tmem + L::kOCol0, o_tmem1 = tmem + L::kOCol1;
+            uint32_t qc = 0, rc = 0, pc0 = 0, pc1 = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; u < p.n_units && ok; u += gridDim.x) {
+                int bh, qb;
+                unit_coords(p, u, bh, qb);
+                const int q0 = qb * kRowsPerUnit;
+                const int n0 = kv_tiles(p, q0), n1 = kv_tiles(p, q0 + kBlockM);
+                const int n = max(n0, n1);
+                if (!mbar_wait(q_full, qc & 1, abort_flag, kWatchdogNs)) { ok = false; break; }
+                ++qc;
+                tc_fence_after();
+                {   // S_t = Q_t K_0^T
+                    const uint32_t slot = rc % L::kStages;
+                    if (!mbar_wait(kv_full + slot, (rc / L::kStages) & 1, abort_flag, kWatchdogNs)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t k_addr = ring_addr + slot * L::kTileBytes;
+                    if (n0 > 0) {
+                        issue_qk<D>(s_tmem0, q_addr, k_addr, idesc_qk);
+                        umma_commit(s_full + 0);
+                    }
+                    if (n1 > 0) {
+                        issue_qk<D>(s_tmem1, q_addr + L::kTileBytes, k_addr, idesc_qk);
+                        umma_commit(s_full + 1);
+                    }
+                    umma_commit(kv_empty + slot);
+                    ++rc;
+                    if (n == 1) umma_commit(q_empty);
+                }
+                for (int j = 0; j < n && ok; ++j) {
+                    const uint32_t slot_v = rc % L::kStages;
+                    if (!mbar_wait(kv_full + slot_v, (rc / L::kStages) & 1, abort_flag, kWatchdogNs)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    ++rc;
+                    const uint32_t v_addr = ring_addr + slot_v * L::kTileBytes;
+                    const uint32_t slot_k = rc % L::kStages;
+                    const uint32_t k_addr = ring_addr + slot_k * L::kTileBytes;
+                    const uint32_t k_parity = (rc / L::kStages) & 1;
+                    bool k_ready = false;
+                    // One query tile's step: wait for P_t, O_t (+)= P_t V_j, then
+                    // S_t = Q_t K_{j+1}^T (issued after the PV product that reads P_t).
+                    auto tile_step = [&](int nt, uint64_t *pf, uint32_t &pc, uint32_t s_t,
+                                         uint32_t o_t, uint32_t q_t, uint64_t *sf, uint64_t *od) {
+                        if (j >= nt) return true;
+                        if (!mbar_wait(pf, pc & 1, abort_flag, kWatchdogNs)) return false;
+                        ++pc;
+                        tc_fence_after();
+                        issue_pv<D>(o_t, s_t, v_addr, idesc_pv, j > 0);
+                        if (j == nt - 1) umma_commit(od);
+                        if (j + 1 < nt) {
+                            if (!k_ready) {
+                                if (!mbar_wait(kv_full + slot_k, k_parity, abort_flag, kWatchdogNs))
+                                    return false;
+                                tc_fence_after();
+                                k_ready = true;
+                            }
+                            issue_qk<D>(s_t, q_t, k_addr, idesc_qk);
+                            umma_commit(sf);
+                        }
+                        return true;
+                    };
+                    ok = tile_step(n0, p_full + 0, pc0, s_tmem0, o_tmem0, q_addr, s_full + 0, o_done + 0) &&
+                         tile_step(n1, p_full + 1, pc1, s_tmem1, o_tmem1, q_addr + L::kTileBytes,
+                                   s_full + 1, o_done + 1);
+                    if (!ok) break;
+                    umma_commit(kv_empty + slot_v);
+                    if (j + 1 < n) {
+                        umma_commit(kv_empty + slot_k);
+                        ++rc;
+                        if (j + 1 == n - 1) umma_commit(q_empty);
+                    }
+                }
+            }
+            // Nothing may still be running on the tensor core at teardown.
+            umma_commit(drain);
+            int dummy = 0;
+            mbar_wait(drain, 0, &dummy, kWatchdogNs);
+        }
+        __syncwarp();
+    } else if (warp < 8) {
+        // ------------------------------------------------------------ softmax
+        regs_grow<kRegsSoftmax>();
+        const int t = warp >> 2;
+        const int wq = warp & 3;
+        const int r = wq * 32 + lane;
+        const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+        const uint32_t s_addr = tmem + lane_off + (t ? L::kSCol1 : L::kSCol0);
+        const uint32_t o_addr = tmem + lane_off + (t ? L::kOCol1 : L::kOCol0);
+        const float cexp = p.scale_log2;
+        uint32_t sc = 0, oc = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; u < p.n_units && ok; u += gridDim.x) {
+            int bh, qb;
+            unit_coords(p, u, bh, qb);
+            const int tile_row0 = qb * kRowsPerUnit + t * kBlockM;
+            const int ntile = kv_tiles(p, tile_row0);
+            if (ntile == 0) continue;
+            const int row = tile_row0 + r;
+            const int lim = p.causal ? min(row, p.N - 1) : p.N - 1;  // last visible key
+            float m_ref = -INFINITY;
+            float l = 0.f;
+            for (int j = 0; j < ntile; ++j) {
+                if (!warp_wait(s_full + t, sc & 1, abort_flag)) { ok = false; break; }
+                ++sc;
+                tc_fence_after();
+                uint32_t sr[4][32];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) tmem_ld32(s_addr + q * 32, sr[q]);
+                tmem_ld_wait();
+#pragma unroll
+                for (int q = 0; q < 4; ++q) reg_fence32(sr[q]);
+
+                const int cmax = lim - j * kBlockN;  // columns > cmax are masked
+                const bool masked = cmax < kBlockN - 1;
+                float m_tile;
+                if (!p.scale_neg) {
+                    float mx = -INFINITY;
+                    if (masked) {
+#pragma unroll
+                        for (int c = 0; c < 128; ++c)
+                            mx = fmaxf(mx, c > cmax ? -INFINITY : __uint_as_float(sr[c >> 5][c & 31]));
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < 128; ++c) mx = fmaxf(mx, __uint_as_float(sr[c >> 5][c & 31]));
+                    }
+                    m_tile = (mx == -INFINITY) ? -INFINITY : mx * cexp;
+                } else {
+                    float mn = INFINITY;
+#pragma unroll
+                    for (int c = 0; c < 128; ++c)
+                        mn = fminf(mn, (masked && c > cmax) ? INFINITY : __uint_as_float(sr[c >> 5][c & 31]));
+                    m_tile = (mn == INFINITY) ? -INFINITY : mn * cexp;
+                }
+                __syncwarp();  // the masked branches above may diverge per lane
+                const bool need = m_tile > m_ref + kTau;
+                float alpha = 1.f;
+                if (need) {
+                    alpha = ex2_approx(m_ref - m_tile);  // 0 on the first tile
+                    l *= alpha;
+                    m_ref = m_tile;
+                }
+                const float negm = -m_ref;
+                float sum[4] = {0.f, 0.f, 0.f, 0.f};
+                // P in 32-key quarters: 16 packed registers per TMEM store.
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int c2 = 0; c2 < 16; ++c2) {
+                        const int c = q * 32 + 2 * c2;
+                        float p0 = ex2_approx(fmaf(__uint_as_float(sr[q][2 * c2]), cexp, negm));
+                        float p1 = ex2_approx(fmaf(__uint_as_float(sr[q][2 * c2 + 1]), cexp, negm));
+                        if (masked) {
+                            p0 = c > cmax ? 0.f : p0;
+                            p1 = c + 1 > cmax ? 0.f : p1;
+                        }
+                        sum[c2 & 3] += p0 + p1;
+                        pk[c2] = pack2(p0, p1, p.in_bf16);
+                    }
+                    tmem_st16(s_addr + q * 16, pk);
+                }
+                l += (sum[0] + sum[1]) + (sum[2] + sum[3]);
+                if (j > 0 && __any_sync(0xffffffffu, need)) {
+                    // O rows are complete up to tile j-1: the commit that
+                    // signalled S_t(j) also covers the earlier PV product.
+                    // Done after P is written so the score registers are free.
+#pragma unroll
+                    for (int q = 0; q < D / 32; ++q) {
+                        uint32_t o[32];
+                        tmem_ld32(o_addr + q * 32, o);
+                        tmem_ld_wait();
+                        reg_fence32(o);
+#pragma unroll
+                        for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+                        tmem_st32(o_addr + q * 32, o);
+                    }
+                    tmem_st_wait();
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(p_full + t);
+            }
+            if (!ok) break;
+            // ---- epilogue: O / l -> out
+            if (!warp_wait(o_done + t, oc & 1, abort_flag)) { ok = false; break; }
+            ++oc;
+            tc_fence_after();
+            const float inv = 1.0f / l;
+            const int osize = p.out_dtype == FA_F32 ? 4 : 2;
+            uint8_t *orow = reinterpret_cast<uint8_t *>(p.out) +
+                            ((static_cast<size_t>(bh) * p.N + row) * D) * osize;
+#pragma unroll
+            for (int q = 0; q < D / 32; ++q) {
+                uint32_t o[32];
+                tmem_ld32(o_addr + q * 32, o);
+                tmem_ld_wait();
+                reg_fence32(o);
+                if (row < p.N) store_out32(orow + q * 32 * osize, o, inv, p.out_dtype);
+            }
+            tc_fence_before();
+        }
+    } else {
+        regs_shrink<kRegsOther>();  // idle warps 10-11
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+    if (threadIdx.x == 0 && *abort_flag) atomicCAS(&g_prefill_status, 0, (int)FA_ERR_WATCHDOG);
+}
+
+// ---------------------------------------------------------------- host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult qres;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                             &qres) != cudaSuccess ||
+            qres != cudaDriverEntryPointSuccess)
+            ptr = nullptr;
+        return reinterpret_cast<EncodeTiledFn>(ptr);
+    }();
+    return fn;
+}
+
+// [BH][N][d] 16-bit tensor viewed as 3-D (d, N, BH); 64 x 128 x 1 boxes,
+// 128-byte swizzle.  Rows past N read as zero, per head.
+int make_map(CUtensorMap *map, const void *base, int d, int N, int BH, int bf16) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return cuda_fail(cudaErrorNotSupported);
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
+    cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)d * 2 * (cuuint64_t)N};
+    cuuint32_t box[3] = {64, 128, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+                     const_cast<void *>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cuda_fail(cudaErrorInvalidValue);
+    return FA_OK;
+}
+
+template <int D>
+int launch_d(const PrefillLaunch &a, const DeviceInfo &dev, cudaStream_t stream) {
+    using L = Layout<D>;
+    static_assert(L::kSmemBytes <= 227 * 1024, "shared memory budget");
+    CUtensorMap mq, mk, mv;
+    const int BH = a.B * a.H;
+    int rc;
+    if ((rc = make_map(&mq, a.q, D, a.N, BH, a.in_bf16)) != FA_OK) return rc;
+    if ((rc = make_map(&mk, a.k, D, a.N, BH, a.in_bf16)) != FA_OK) return rc;
+    if ((rc = make_map(&mv, a.v, D, a.N, BH, a.in_bf16)) != FA_OK) return rc;
+    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
+    if (e != cudaSuccess) return cuda_fail(e);
+    // The setmaxnreg split inside the kernel draws on the launch allocation:
+    // refuse to launch a build whose register count would make it wait forever.
+    cudaFuncAttributes fattr;
+    e = cudaFuncGetAttributes(&fattr, prefill_kernel<D>);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (fattr.numRegs < kMinLaunchRegs) return cuda_fail(cudaErrorInvalidConfiguration);
+
+    Params p;
+    p.out = a.out;
+    p.N = a.N;
+    p.BH = BH;
+    p.n_qb = (a.N + kRowsPerUnit - 1) / kRowsPerUnit;
+    p.n_units = BH * p.n_qb;
+    p.causal = a.causal ? 1 : 0;
+    p.no_skip = a.no_skip ? 1 : 0;
+    p.in_bf16 = a.in_bf16;
+    p.out_dtype = a.out_dtype;
+    p.scale_neg = a.scale < 0.f ? 1 : 0;
+    p.scale_log2 = a.scale * 1.4426950408889634f;
+    const int grid = p.n_units < dev.num_sms ? p.n_units : dev.num_sms;
+    prefill_kernel<D><<<grid, kThreads, L::kSmemBytes, stream>>>(mq, mk, mv, p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e);
+    return FA_OK;
+}
+
+}  // namespace
+
+int launch_prefill(const PrefillLaunch &a, const DeviceInfo &dev, cudaStream_t stream) {
+    if (a.d == 64) return launch_d<64>(a, dev, stream);
+    if (a.d == 128) return launch_d<128>(a, dev, stream);
+    return FA_ERR_HEAD_DIM;
+}
+
+int read_prefill_status(int reset) {
+    int v = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&v, g_prefill_status, sizeof(int));
+    if (e != cudaSuccess) return -1;
+    if (reset && v) {
+        int z = 0;
+        if (cudaMemcpyToSymbol(g_prefill_status, &z, sizeof(int)) != cudaSuccess) return -1;
+    }
+    return v;
+}
+
+}  // namespace fa

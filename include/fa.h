@@ -1,0 +1,168 @@
+/*
+ * fa.h -- C ABI of libfa_gb300.so: fused scaled-dot-product attention forward
+ * (prefill and split-K decode) for one NVIDIA GB300 (sm_103a).
+ *
+ * What is computed (flash-attention-cuda README, "What is Attention?", "What is
+ * Flash Attention?" and the "Kernel design" table):
+ *     O = softmax(scale * Q K^T [+ causal mask]) V
+ * row by row, tile by tile, with the online-softmax recurrence (a running row
+ * maximum m, a running denominator l and a rescaled fp32 accumulator), so the
+ * N x N score table is never written to memory.  Inputs are fp16 or bf16, all
+ * sums are fp32 ("fp16 in, fp32 accumulate" row of the "Kernel design" table).
+ *
+ * Conventions shared by every entry point
+ *   - Tensors are dense, row-major, head dimension innermost:
+ *       prefill q, k, v, out : [B][H][N][d]
+ *       decode  q, out       : [B][H][1][d]
+ *       decode  caches       : [B][H][max_len][d]
+ *   - Every pointer is a device pointer owned by the caller, 16-byte aligned.
+ *     The library keeps no pointer after the call returns.  Work is enqueued on
+ *     `stream` (a cudaStream_t passed as void*; NULL = the legacy default
+ *     stream) and runs asynchronously: inputs must stay alive and unmodified,
+ *     and `out` untouched, until that stream work has completed.
+ *   - `out` must not overlap any input.
+ *   - Status: FA_OK (0) or an fa_status code, returned synchronously for bad
+ *     arguments and for launch failures.  A fault during execution surfaces at
+ *     the caller's next synchronisation, as for any CUDA call.  Nothing throws
+ *     across this ABI.  On any non-zero status no work was enqueued.
+ *   - The library runs only on compute capability 10.3 (sm_103a); any other
+ *     device returns FA_ERR_ARCH.  There is no fallback path.
+ *   - All entry points are thread-safe; the only global state is a per-device
+ *     attribute cache and a device-side watchdog status word.
+ */
+#ifndef FA_GB300_H
+#define FA_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { FA_F16 = 0, FA_BF16 = 1, FA_F32 = 2 } fa_dtype;
+
+typedef enum {
+    FA_OK = 0,
+    FA_ERR_NULL = 1,       /* a required pointer is NULL                          */
+    FA_ERR_SHAPE = 2,      /* B, H, N or max_len < 1, or a size overflows int32   */
+    FA_ERR_HEAD_DIM = 3,   /* d is not a supported head dimension                 */
+    FA_ERR_DTYPE = 4,      /* unsupported input/output dtype combination          */
+    FA_ERR_ALIGN = 5,      /* a pointer is not 16-byte aligned                    */
+    FA_ERR_SCALE = 6,      /* scale is NaN or infinite                            */
+    FA_ERR_ARCH = 7,       /* current device is not compute capability 10.3       */
+    FA_ERR_WORKSPACE = 8,  /* caller workspace too small, or allocation failed    */
+    FA_ERR_CUDA = 9,       /* a CUDA runtime call failed: see fa_last_cuda_error  */
+    FA_ERR_WATCHDOG = 10,  /* a device-side wait ran out (see fa_device_status)   */
+    FA_ERR_ALIAS = 11,     /* out overlaps an input                               */
+    FA_ERR_SPLITS = 12     /* num_splits outside [0, ceil(max_len / 64)]          */
+} fa_status;
+
+/* Flags for fa_prefill_ex. */
+#define FA_FLAG_NONE 0u
+/* Causal only: run the key-tile loop over every tile instead of stopping at
+ * the diagonal (tiles above it are then fully masked).  The result must be
+ * bit-identical to the default ("Kernel design" table, causal tile skipping,
+ * "verified bit-identical"); the flag exists so that tests can check that. */
+#define FA_FLAG_NO_CAUSAL_SKIP 1u
+
+/*
+ * Prefill (flash-attention-cuda README, "What did I implement?" prompt phase,
+ * and "Installation" usage `prefill(q, k, v, causal, scale)`): batched,
+ * multi-head attention of N queries over the same N keys.
+ *   q, k, v : fp16 inputs [B][H][N][d]
+ *   out     : fp16 output [B][H][N][d]
+ *   d       : 64 or 128
+ *   causal  : nonzero -> key j is visible to query i iff j <= i; tiles wholly
+ *             above the diagonal are skipped by loop bounds.
+ *   scale   : finite float multiplying Q K^T (0 gives the mean of the visible
+ *             value rows; negative values are allowed).
+ */
+int fa_prefill(const void *q, const void *k, const void *v, void *out,
+               int B, int H, int N, int d, int causal, float scale,
+               void *stream);
+
+/*
+ * Prefill with explicit dtypes and flags.
+ *   in_dtype  : FA_F16 or FA_BF16 (q, k and v share it)
+ *   out_dtype : FA_F16, FA_BF16 or FA_F32 (rounded to nearest even)
+ *   flags     : FA_FLAG_* bits
+ */
+int fa_prefill_ex(const void *q, const void *k, const void *v, void *out,
+                  int B, int H, int N, int d, int causal, float scale,
+                  fa_dtype in_dtype, fa_dtype out_dtype, unsigned flags,
+                  void *stream);
+
+/*
+ * Split-K decode (flash-attention-cuda README, "What did I implement?"
+ * generation phase; "Kernel design" rows "Split-K decode + adaptive chunk"
+ * and "Two-pass merge, no atomics"): one query row per (b, h) attends over
+ * the first seq_lens[b] rows of its KV cache.  The cache is split into
+ * chunks, each chunk yields a partial (m, l, acc), and a second kernel merges
+ * the partials in a fixed order, without atomics.
+ *   q        : fp16 [B][H][1][d]
+ *   k_cache, v_cache : fp16 [B][H][max_len][d]
+ *   seq_lens : int32 device array [B]; precondition 1 <= seq_lens[b] <= max_len.
+ *              Values are clamped to [0, max_len]; a length of 0 yields a zero
+ *              output row.
+ *   out      : fp16 [B][H][1][d]
+ *   d        : 64 or 128
+ * The split count is chosen from (B, H, max_len, SM count) only, never from
+ * the device-resident lengths, so it needs no device-to-host copy and gives
+ * bit-identical results run to run.  The partials workspace is allocated
+ * stream-ordered (cudaMallocAsync / cudaFreeAsync on `stream`).
+ */
+int fa_decode(const void *q, const void *k_cache, const void *v_cache,
+              const int32_t *seq_lens, void *out,
+              int B, int H, int max_len, int d, float scale, void *stream);
+
+/*
+ * Decode with explicit dtypes, split count and workspace.
+ *   in_dtype / out_dtype : as for fa_prefill_ex
+ *   num_splits : 0 = automatic (fa_decode_choose_splits), else the number of
+ *                key chunks per (b, h), 1 <= num_splits <= ceil(max_len / 64)
+ *   workspace  : NULL -> allocated stream-ordered; else a device buffer of at
+ *                least fa_decode_workspace_bytes(B, H, max_len, d, splits)
+ *                bytes, 16-byte aligned, owned by the caller, not used by any
+ *                other work running at the same time.
+ */
+int fa_decode_ex(const void *q, const void *k_cache, const void *v_cache,
+                 const int32_t *seq_lens, void *out,
+                 int B, int H, int max_len, int d, float scale,
+                 fa_dtype in_dtype, fa_dtype out_dtype, int num_splits,
+                 void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * The automatic split count ("Kernel design" table: choose_decode_split
+ * targets about two resident blocks per SM).  Pure host arithmetic on its
+ * arguments; num_sms <= 0 means "the current device's SM count".
+ * Returns the split count (>= 1), or a negative fa_status on bad arguments.
+ */
+int fa_decode_choose_splits(int B, int H, int max_len, int num_sms);
+
+/* Keys per chunk for a given split count: round_up(ceil(max_len/splits), 64). */
+int fa_decode_chunk_len(int max_len, int num_splits);
+
+/* Workspace bytes needed by fa_decode_ex for this problem (0 on bad args). */
+size_t fa_decode_workspace_bytes(int B, int H, int max_len, int d,
+                                 int num_splits);
+
+/* Static text for a status code ("unknown status" for other values). */
+const char *fa_status_string(int status);
+
+/* The cudaError_t behind the calling thread's last FA_ERR_CUDA (0 if none). */
+int fa_last_cuda_error(void);
+
+/* Device-side status word of the current device: 0 or FA_ERR_WATCHDOG after a
+ * kernel's bounded wait ran out.  Synchronises the device.  If reset is
+ * nonzero the word is cleared.  Returns a negative value if it cannot be read. */
+int fa_device_status(int reset);
+
+/* ABI version: major * 10000 + minor * 100 + patch. */
+int fa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_H */

@@ -1,0 +1,137 @@
+"""GPU parity of split-K decode against the fp64 oracle (through the C ABI).
+
+Ragged-decode configuration: B in {1, 8, 32}, H in {14, 12}, d = 64, fp16
+caches [B, H, 4096, 64], per-sequence lengths uniform on [1, 4096], scale 1/8.
+Every output is checked (decode is cheap for the oracle).  Also: decode of
+token t equals row t of causal prefill, invariance over every split count,
+bit-identical reruns for a fixed split, lengths at chunk edges.
+"""
+import numpy as np
+import pytest
+
+from attention_forward_prefill_gb300 import inputs
+from tests import gpu_util as G
+
+pytestmark = pytest.mark.gpu
+CFG_DECODE = 3
+
+
+@pytest.fixture(scope="module")
+def fa():
+    import torch
+    from attention_forward_prefill_gb300 import binding, build
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    assert torch.cuda.get_device_capability() == (10, 3), "libfa_gb300 targets sm_103a"
+    build.build()
+    binding.load()
+    return binding
+
+
+def make_decode(B, H, L, d, dtype, cfg, lens=None):
+    q = inputs.normal_bits((B, H, 1, d), inputs.seed_for(cfg, inputs.TENSOR_Q) + 1000 * H, dtype)
+    kc = inputs.normal_bits((B, H, L, d), inputs.seed_for(cfg, inputs.TENSOR_K) + 1000 * H, dtype)
+    vc = inputs.normal_bits((B, H, L, d), inputs.seed_for(cfg, inputs.TENSOR_V) + 1000 * H, dtype)
+    if lens is None:
+        lens = inputs.seq_lens(inputs.seed_for(cfg, inputs.TENSOR_SEQLEN) + B, B, L)
+    return q, kc, vc, np.asarray(lens, dtype=np.int32)
+
+
+def run_decode(fa, q, kc, vc, lens, dtype, scale, out_dtype="f16", num_splits=0, workspace=None):
+    import torch
+    out = fa.decode(G.bits_to_device(q, dtype), G.bits_to_device(kc, dtype),
+                    G.bits_to_device(vc, dtype), torch.from_numpy(lens).cuda(), scale=scale,
+                    out_dtype=G.torch_dtype(out_dtype), num_splits=num_splits,
+                    workspace=workspace)
+    torch.cuda.synchronize()
+    return out
+
+
+def oracle_decode(oracle_mod, q, kc, vc, lens, dtype, scale):
+    return oracle_mod.decode(oracle_mod.bits_to_f64(q, dtype), oracle_mod.bits_to_f64(kc, dtype),
+                             oracle_mod.bits_to_f64(vc, dtype), lens, scale, threads=G.THREADS)
+
+
+@pytest.mark.parametrize("B", [1, 8, 32])
+@pytest.mark.parametrize("H", [14, 12])
+def test_ragged_decode_config(fa, oracle_mod, B, H):
+    q, kc, vc, lens = make_decode(B, H, 4096, 64, "f16", CFG_DECODE)
+    got = G.device_to_f64(run_decode(fa, q, kc, vc, lens, "f16", 0.125))
+    want = oracle_decode(oracle_mod, q, kc, vc, lens, "f16", 0.125)
+    G.assert_close(got, want, "f16", "f16", f"decode B={B} H={H}")
+
+
+def test_lengths_at_chunk_edges(fa, oracle_mod):
+    L, B, H = 4096, 11, 3
+    splits = fa.fa_decode_choose_splits(B, H, L, 0)
+    chunk = fa.fa_decode_chunk_len(L, splits)
+    lens = [1, 2, chunk - 1, chunk, chunk + 1, 2 * chunk, 2 * chunk + 1, L - 1, L, 63, 65]
+    lens = [min(max(x, 1), L) for x in lens]
+    q, kc, vc, lens = make_decode(B, H, L, 64, "f16", 300, lens)
+    got = G.device_to_f64(run_decode(fa, q, kc, vc, lens, "f16", 0.125, "f32"))
+    want = oracle_decode(oracle_mod, q, kc, vc, lens, "f16", 0.125)
+    G.assert_close(got, want, "f16", "f32", "decode chunk edges")
+
+
+def test_every_split_count_agrees(fa, oracle_mod):
+    L, B, H = 1000, 3, 2
+    q, kc, vc, lens = make_decode(B, H, L, 64, "f16", 301, [1000, 517, 64])
+    want = oracle_decode(oracle_mod, q, kc, vc, lens, "f16", 0.125)
+    max_splits = (L + 63) // 64
+    first = None
+    for s in range(1, max_splits + 1):
+        got = G.device_to_f64(run_decode(fa, q, kc, vc, lens, "f16", 0.125, "f32", num_splits=s))
+        G.assert_close(got, want, "f16", "f32", f"decode splits={s}")
+        if first is None:
+            first = got
+        assert np.abs(got - first).max() <= 2e-3
+
+
+def test_fixed_split_is_bit_identical_and_workspace_paths_agree(fa):
+    import torch
+    B, H, L = 8, 14, 4096
+    q, kc, vc, lens = make_decode(B, H, L, 64, "f16", CFG_DECODE)
+    a = run_decode(fa, q, kc, vc, lens, "f16", 0.125)
+    b = run_decode(fa, q, kc, vc, lens, "f16", 0.125)
+    splits = fa.fa_decode_choose_splits(B, H, L, 0)
+    nbytes = fa.fa_decode_workspace_bytes(B, H, L, 64, splits)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    c = run_decode(fa, q, kc, vc, lens, "f16", 0.125, workspace=ws)
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    assert torch.equal(a.view(torch.int16), c.view(torch.int16))
+
+
+def test_decode_of_token_t_equals_causal_prefill_row_t(fa):
+    import torch
+    B, H, N, d = 2, 12, 1024, 64
+    q = inputs.normal_bits((B, H, N, d), 11, "f16")
+    k = inputs.normal_bits((B, H, N, d), 12, "f16")
+    v = inputs.normal_bits((B, H, N, d), 13, "f16")
+    qd, kd, vd = (G.bits_to_device(x, "f16") for x in (q, k, v))
+    pre = fa.prefill(qd, kd, vd, causal=True, scale=0.125, out_dtype=torch.float32)
+    for t in [0, 1, 63, 64, 500, N - 1]:
+        lens = torch.full((B,), t + 1, dtype=torch.int32, device="cuda")
+        dec = fa.decode(qd[:, :, t:t + 1].contiguous(), kd, vd, lens, scale=0.125,
+                        out_dtype=torch.float32)
+        torch.cuda.synchronize()
+        diff = (dec[:, :, 0] - pre[:, :, t]).abs().max().item()
+        assert diff <= 2e-3, (t, diff)
+
+
+def test_length_clamping_and_zero_length(fa, oracle_mod):
+    B, H, L = 4, 2, 300
+    q, kc, vc, _ = make_decode(B, H, L, 64, "f16", 302, [1, 1, 1, 1])
+    lens = np.array([0, 300, 5000, -7], dtype=np.int32)
+    got = G.device_to_f64(run_decode(fa, q, kc, vc, lens, "f16", 0.125, "f32"))
+    want = oracle_decode(oracle_mod, q, kc, vc, np.clip(lens, 0, L), "f16", 0.125)
+    assert np.array_equal(got[0], np.zeros_like(got[0]))
+    assert np.array_equal(got[3], np.zeros_like(got[3]))
+    G.assert_close(got, want, "f16", "f32", "decode clamped lengths")
+
+
+@pytest.mark.parametrize("d,dtype", [(128, "bf16"), (64, "bf16"), (128, "f16")])
+def test_other_head_dims_and_dtypes(fa, oracle_mod, d, dtype):
+    B, H, L = 5, 4, 2000
+    q, kc, vc, lens = make_decode(B, H, L, d, dtype, 303)
+    got = G.device_to_f64(run_decode(fa, q, kc, vc, lens, dtype, 1.0 / np.sqrt(d), "f32"))
+    want = oracle_decode(oracle_mod, q, kc, vc, lens, dtype, 1.0 / np.sqrt(d))
+    G.assert_close(got, want, dtype, "f32", f"decode d={d} {dtype}")
