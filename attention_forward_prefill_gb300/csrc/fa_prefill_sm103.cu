@@ -136,6 +136,12 @@ __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint3
     }
 }
 
+// The two 16-bit values of a packed pair, back in fp32 (exact).
+__device__ __forceinline__ float2 unpack2(uint32_t w, int bf16) {
+    if (bf16) return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+    return __half22float2(*reinterpret_cast<const __half2 *>(&w));
+}
+
 __device__ __forceinline__ uint32_t pack2(float lo, float hi, int bf16) {
     if (bf16) {
         __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
@@ -453,8 +459,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                             p0 = c > cmax ? 0.f : p0;
                             p1 = c + 1 > cmax ? 0.f : p1;
                         }
-                        sum[c2 & 3] += p0 + p1;
                         pk[c2] = pack2(p0, p1, p.in_bf16);
+                        // l sums the same rounded weights the PV product uses,
+                        // so a row dominated by one key returns that value row.
+                        const float2 r = unpack2(pk[c2], p.in_bf16);
+                        sum[c2 & 3] += r.x + r.y;
                     }
                     tmem_st16(s_addr + q * 16, pk);
                 }

@@ -1,0 +1,461 @@
+"""Benchmark: fused attention forward on GB300 (prefill + split-K decode).
+
+One step = one pass of the whole path over one batch of synthetic input:
+  * dense non-causal prefill, B=1, H=16, d=128, bf16 in/out, fp32 accumulate,
+    scale = 1/sqrt(128), at N = 4096, 8192 and 16384 (one launch each);
+  * ragged split-K decode, B=32, H=14, d=64, fp16, KV caches [32,14,4096,64],
+    seq_lens uniform on [1, 4096], scale = 1/8 (split kernel + merge kernel).
+`value` is prefill TFLOP/s (4*B*H*N^2*d FLOPs per launch) over the device time
+of the prefill launches; decode GB/s (K+V bytes of the visible cache rows)
+is reported beside it.  L2 is flushed (a 2 x L2 buffer is written) before
+every timed kernel, outside its CUDA-event pair.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+Under torchrun (N > 1) every rank runs the same step on its own GPU with its
+own seed (no data-path collective: weak scaling); rank 0 prints the line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "prefill TFLOP/s (% BF16 TC peak) d=128 N=4K–16K; decode HBM GB/s (% peak)"
+PREFILL_B, PREFILL_H, PREFILL_D = 1, 16, 128
+PREFILL_NS = (4096, 8192, 16384)
+DECODE_B, DECODE_H, DECODE_L, DECODE_D = 32, 14, 4096, 64
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+# DRAM traffic per launch from an ncu capture, valid only for the kernel source
+# it was taken on (sha256 of the .cu file, first 16 hex digits).
+NCU_TRAFFIC = {
+    # "prefill": {"src_sha": "...", "bytes_per_launch": {"16384": ...}},
+}
+
+
+def prefill_flops(B, H, N, d, causal=False):
+    f = 4.0 * B * H * N * N * d
+    return f / 2 if causal else f
+
+
+def decode_bytes(lens, H, d):
+    return 2.0 * H * float(sum(int(x) for x in lens)) * d * 2  # K and V rows, 16-bit
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {k: float(p[k]) for k in FALLBACK_PEAKS}, "measured"
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def src_sha(name):
+    path = os.path.join(ROOT, "attention_forward_prefill_gb300", "csrc", name)
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+# ------------------------------------------------------------------ ranks
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def aggregate(local_seconds: float, local_units: float, world: int, device=None):
+    """Max elapsed time and summed work over ranks (both via all_reduce)."""
+    if world == 1:
+        return local_seconds, local_units
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([local_seconds], dtype=torch.float64, device=device)
+    u = torch.tensor([local_units], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", str(self.index)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+                power.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[4:8]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------ our path
+def make_inputs(torch, device, rank):
+    """Synthetic N(0,1) inputs generated on the device (seeded per rank)."""
+    from attention_forward_prefill_gb300 import inputs as fin
+    g = torch.Generator(device=device)
+    g.manual_seed(0xFA000000 + 97 * rank)
+    pre = {}
+    for N in PREFILL_NS:
+        shape = (PREFILL_B, PREFILL_H, N, PREFILL_D)
+        pre[N] = [torch.randn(shape, generator=g, device=device, dtype=torch.float32)
+                  .to(torch.bfloat16) for _ in range(3)]
+    shp = (DECODE_B, DECODE_H, DECODE_L, DECODE_D)
+    dq = torch.randn((DECODE_B, DECODE_H, 1, DECODE_D), generator=g, device=device).half()
+    dk = torch.randn(shp, generator=g, device=device).half()
+    dv = torch.randn(shp, generator=g, device=device).half()
+    lens_np = fin.seq_lens(fin.seed_for(3, fin.TENSOR_SEQLEN) + rank, DECODE_B, DECODE_L)
+    lens = torch.from_numpy(lens_np).to(device)
+    return pre, (dq, dk, dv, lens, lens_np)
+
+
+def run_ours(args):
+    import torch
+
+    from attention_forward_prefill_gb300 import binding
+    from attention_forward_prefill_gb300 import build as fa_build
+
+    world, rank, local = dist_env()
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+    if rank == 0 or not os.path.exists(fa_build.LIB_PATH):
+        fa_build.build()
+    if world > 1:
+        dist.barrier()
+    binding.load()
+    scale_p = float(1.0 / math.sqrt(PREFILL_D))
+    scale_d = 0.125
+    pre, (dq, dk, dv, lens, lens_np) = make_inputs(torch, device, rank)
+    outs = {N: torch.empty_like(pre[N][0]) for N in PREFILL_NS}
+    dout = torch.empty_like(dq)
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+    splits = binding.fa_decode_choose_splits(DECODE_B, DECODE_H, DECODE_L, 0)
+    ws = torch.empty(binding.fa_decode_workspace_bytes(DECODE_B, DECODE_H, DECODE_L, DECODE_D,
+                                                       splits), dtype=torch.uint8, device=device)
+    cases = args.case.split(",") if args.case else None
+    do_pre = [N for N in PREFILL_NS if cases is None or f"prefill:{N}" in cases]
+    do_dec = cases is None or "decode" in cases
+
+    def step(record):
+        ev = []
+        for N in do_pre:
+            q, k, v = pre[N]
+            flush.zero_()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            binding.prefill(q, k, v, causal=False, scale=scale_p, out=outs[N])
+            e1.record(stream)
+            ev.append(("prefill", N, e0, e1))
+        if do_dec:
+            flush.zero_()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            binding.decode(dq, dk, dv, lens, scale=scale_d, num_splits=splits, workspace=ws,
+                           out=dout)
+            e1.record(stream)
+            ev.append(("decode", 0, e0, e1))
+        if record is not None:
+            record.append(ev)
+
+    for _ in range(args.warmup):
+        step(None)
+    torch.cuda.synchronize()
+    assert binding.fa_device_status(False) == 0
+
+    sampler = ClockSampler(local) if not args.no_clocks else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    records = []
+    t_start.record(stream)
+    for _ in range(args.steps):
+        step(records)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop() if sampler else None
+    step_ms = t_start.elapsed_time(t_end) / args.steps
+
+    pre_ms = {N: [] for N in do_pre}
+    dec_ms = []
+    for ev in records:
+        for kind, N, e0, e1 in ev:
+            (pre_ms[N] if kind == "prefill" else dec_ms).append(e0.elapsed_time(e1))
+    pre_time_s = sum(sum(v) for v in pre_ms.values()) / 1e3
+    pre_flops = sum(prefill_flops(PREFILL_B, PREFILL_H, N, PREFILL_D) for N in do_pre) * args.steps
+    dec_time_s = sum(dec_ms) / 1e3
+    dec_bytes = decode_bytes(lens_np, DECODE_H, DECODE_D) * (args.steps if do_dec else 0)
+
+    # ---- end to end through the public call with pinned host buffers
+    e2e = None
+    if not args.no_e2e and do_pre:
+        host = {N: [x.cpu().pin_memory() for x in pre[N]] for N in do_pre}
+        h2d = sum(x.numel() * x.element_size() for N in do_pre for x in host[N])
+        d2h = sum(outs[N].numel() * outs[N].element_size() for N in do_pre)
+        for N in do_pre:  # warm the host path once
+            binding.prefill(*host[N], causal=False, scale=scale_p)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            for N in do_pre:
+                binding.prefill(*host[N], causal=False, scale=scale_p)
+        torch.cuda.synchronize()
+        e2e_s = time.perf_counter() - t0
+        e2e_s, e2e_flops = aggregate(e2e_s, pre_flops, world, device)
+        e2e = {"value": e2e_flops / e2e_s / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+    tot_s, tot_flops = aggregate(pre_time_s, pre_flops, world, device)
+    _, tot_dec_bytes = aggregate(dec_time_s, dec_bytes, world, device)
+    dec_s_max, _ = aggregate(dec_time_s, 0.0, world, device)
+    step_ms_max, _ = aggregate(step_ms, 0.0, world, device)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        cpu = cpu_baseline(args.cpu_seconds)
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return None
+
+    peaks, peak_src = load_peaks()
+    value = tot_flops / tot_s / 1e12 if do_pre else None
+    n_launch = len(do_pre) * args.steps + (2 * args.steps if do_dec else 0)
+    detail = {}
+    for N in do_pre:
+        ms = statistics.median(pre_ms[N])
+        tf = prefill_flops(PREFILL_B, PREFILL_H, N, PREFILL_D) / (ms / 1e3) / 1e12
+        detail[f"prefill_N{N}"] = {"median_ms": round(ms, 4), "min_ms": round(min(pre_ms[N]), 4),
+                                   "tflops": round(tf, 1)}
+    traffic = None
+    rec = NCU_TRAFFIC.get("prefill")
+    if rec and rec.get("src_sha") == src_sha("fa_prefill_sm103.cu") and do_pre:
+        per = [rec["bytes_per_launch"].get(str(N)) for N in do_pre]
+        if all(x is not None for x in per):
+            traffic = sum(per) / len(per)
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2) if value is not None else None,
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(step_ms_max, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {
+            "workload": ("dense non-causal prefill B=1 H=16 d=128 bf16 N=4096,8192,16384 "
+                         "+ ragged split-K decode B=32 H=14 d=64 fp16 max_len=4096"),
+            "prefill_shapes": [[PREFILL_B, PREFILL_H, N, PREFILL_D] for N in do_pre],
+            "decode_shape": [DECODE_B, DECODE_H, DECODE_L, DECODE_D] if do_dec else None,
+            "decode_splits": splits,
+            "l2": "flushed before every timed kernel (2 x L2 buffer written, outside the events)",
+            "ms_per_step_includes": "L2 flushes between kernels",
+        },
+        "roofline": {
+            "bound": "tensor",
+            "achieved": round(value, 2) if value is not None else None,
+            "peak": peaks["bf16_tflops"],
+            "unit": "TFLOP/s",
+            "frac": round(value / peaks["bf16_tflops"], 4) if value is not None else None,
+            "traffic": traffic,
+            "peak_source": f"{peak_src} bf16 dense burst (kernels timed alone)",
+            "frac_of_sustained": (round(value / peaks["bf16_tflops_sustained"], 4)
+                                  if value is not None else None),
+            "kernel": "fa::prefill_kernel<128>",
+        },
+        "decode": None,
+        "detail": detail,
+        "e2e": e2e,
+        "gpu_launches": n_launch,
+        "clocks": clocks,
+        "cpu_baseline": cpu,
+    }
+    if do_dec:
+        gbs = tot_dec_bytes / dec_s_max / 1e9
+        line["decode"] = {
+            "value": round(gbs, 1), "unit": "GB/s", "dtype": "f16",
+            "median_us": round(statistics.median(dec_ms) * 1e3, 2),
+            "kv_bytes_per_step": decode_bytes(lens_np, DECODE_H, DECODE_D),
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
+                         "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4),
+                         "traffic": None, "peak_source": f"{peak_src} copy bandwidth"},
+        }
+    if world > 1:
+        dist.destroy_process_group()
+    return line
+
+
+# ------------------------------------------------------------------ oracle legs
+def oracle_sample(seconds: float, N: int = 16384):
+    """Time the fp64 oracle on whole rows of the N-length prefill (one head)."""
+    import numpy as np
+
+    from attention_forward_prefill_gb300 import inputs as fin
+    from oracle import oracle
+
+    d = PREFILL_D
+    rows_per_call = 8
+    k = oracle.bf16_bits_to_f64(fin.normal_bits((N, d), fin.seed_for(2, 1), "bf16"))
+    v = oracle.bf16_bits_to_f64(fin.normal_bits((N, d), fin.seed_for(2, 2), "bf16"))
+    q = oracle.bf16_bits_to_f64(fin.normal_bits((N, d), fin.seed_for(2, 0), "bf16"))
+    scale = float(np.float32(1.0 / math.sqrt(d)))
+    oracle.attention(q, k, v, False, scale, rows=[0])  # load / build
+    done = 0
+    t0 = time.perf_counter()
+    while time.perf_counter() - t0 < seconds:
+        rows = np.arange(done, done + rows_per_call) % N
+        oracle.attention(q, k, v, False, scale, rows=rows, threads=1)
+        done += rows_per_call
+    dt = time.perf_counter() - t0
+    flops = 4.0 * N * d * done
+    return flops / dt / 1e12, done, dt
+
+
+def cpu_baseline(seconds: float):
+    value, rows, dt = oracle_sample(seconds)
+    return {"value": value, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+            "sample": (f"{rows} query rows of one head of the N=16384 d=128 dense prefill "
+                       f"({dt:.1f} s single-threaded fp64 C oracle); FLOPs counted as 4*N*d "
+                       "per row")}
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return None
+    per_step = max(0.5, args.cpu_seconds / max(1, args.steps))
+    for _ in range(args.warmup):
+        oracle_sample(min(0.5, per_step))
+    vals, rows_total, t_total = [], 0, 0.0
+    for _ in range(args.steps):
+        v, rows, dt = oracle_sample(per_step)
+        vals.append(v)
+        rows_total += rows
+        t_total += dt
+    value = 4.0 * 16384 * PREFILL_D * rows_total / t_total / 1e12
+    sample = (f"{rows_total} query rows of one head of the N=16384 d=128 dense prefill over "
+              f"{args.steps} steps of ~{per_step:.1f} s (single-threaded fp64 C oracle)")
+    return {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": value,
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": t_total / args.steps * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": ("dense non-causal prefill B=1 H=16 d=128 bf16 N=4096,8192,16384 "
+                                "+ ragged split-K decode B=32 H=14 d=64 fp16 max_len=4096"),
+                   "reference": "the fp64 CPU oracle, as it stands, on sampled rows"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--case", default="", help="subset, e.g. prefill:8192 or decode")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3 and args.impl == "ours" and not args.case:
+        ap.error("--warmup must be >= 3")
+    line = run_reference(args) if args.impl == "reference" else run_ours(args)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,129 @@
+"""The C-ABI library without a GPU: it loads, exports every symbol that
+include/fa.h declares, rejects bad arguments with the documented status codes
+before touching any device, and its host-side split arithmetic is consistent.
+"""
+import os
+import re
+
+import pytest
+
+from attention_forward_prefill_gb300 import binding, build
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                      "include", "fa.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return binding.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fa_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert "fa_prefill" in names and "fa_decode" in names
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(binding._SIGNATURES) >= set(names)
+
+
+def test_status_strings_and_version(lib):
+    for code in range(13):
+        assert binding.status_string(code) != "unknown status"
+    assert binding.status_string(999) == "unknown status"
+    assert binding.fa_version() >= 10000
+
+
+A = 1 << 20   # an aligned fake address: validation must reject before using it
+B_ = 1 << 28
+
+
+@pytest.mark.parametrize("args,status", [
+    ((None, A, A, B_, 1, 1, 1, 64, 0, 1.0, 0, 0, 0), 1),
+    ((A, A, A, B_, 0, 1, 1, 64, 0, 1.0, 0, 0, 0), 2),
+    ((A, A, A, B_, 1, 1, -3, 64, 0, 1.0, 0, 0, 0), 2),
+    ((A, A, A, B_, 65536, 65536, 2, 64, 0, 1.0, 0, 0, 0), 2),
+    ((A, A, A, B_, 1, 1, 1, 96, 0, 1.0, 0, 0, 0), 3),
+    ((A, A, A, B_, 1, 1, 1, 64, 0, 1.0, 2, 0, 0), 4),
+    ((A, A, A, B_, 1, 1, 1, 64, 0, 1.0, 0, 7, 0), 4),
+    ((A + 8, A, A, B_, 1, 1, 1, 64, 0, 1.0, 0, 0, 0), 5),
+    ((A, A, A, B_ + 2, 1, 1, 1, 64, 0, 1.0, 0, 0, 0), 5),
+    ((A, A, A, B_, 1, 1, 1, 64, 0, float("nan"), 0, 0, 0), 6),
+    ((A, A, A, B_, 1, 1, 1, 64, 0, float("inf"), 0, 0, 0), 6),
+    ((A, A, A, A, 1, 1, 1, 64, 0, 1.0, 0, 0, 0), 11),
+    ((A, A, A, A + 64, 1, 2, 8, 64, 0, 1.0, 0, 0, 0), 11),
+])
+def test_prefill_argument_errors(lib, args, status):
+    q, k, v, out, B, H, N, d, causal, scale, it, ot, fl = args
+    assert binding.fa_prefill_ex(q, k, v, out, B, H, N, d, causal, scale, it, ot, fl, None) == status
+
+
+def test_plain_prefill_checks_too(lib):
+    assert binding.fa_prefill(None, A, A, B_, 1, 1, 1, 64, 0, 1.0, None) == 1
+    assert binding.fa_prefill(A, A, A, B_, 1, 1, 1, 80, 0, 1.0, None) == 3
+
+
+S = 1 << 24  # seq_lens
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(seq_lens=None), 1),
+    (dict(B=0), 2),
+    (dict(d=32), 3),
+    (dict(in_dtype=2), 4),
+    (dict(q=A + 4), 5),
+    (dict(seq_lens=S + 2), 5),
+    (dict(workspace=A + 8, workspace_bytes=1 << 20), 5),
+    (dict(scale=float("nan")), 6),
+    (dict(num_splits=-1), 12),
+    (dict(num_splits=65), 12),
+    (dict(num_splits=4, workspace=1 << 30, workspace_bytes=16), 8),
+    (dict(out=S), 11),
+])
+def test_decode_argument_errors(lib, kw, status):
+    a = dict(q=A, k=1 << 26, v=1 << 27, seq_lens=S, out=B_, B=2, H=3, max_len=4096, d=64,
+             scale=0.125, in_dtype=0, out_dtype=0, num_splits=0, workspace=None,
+             workspace_bytes=0)
+    a.update(kw)
+    got = binding.fa_decode_ex(a["q"], a["k"], a["v"], a["seq_lens"], a["out"], a["B"], a["H"],
+                               a["max_len"], a["d"], a["scale"], a["in_dtype"], a["out_dtype"],
+                               a["num_splits"], a["workspace"], a["workspace_bytes"], None)
+    assert got == status
+
+
+@pytest.mark.parametrize("B,H,L,sms", [(1, 14, 4096, 152), (8, 14, 4096, 152), (32, 14, 4096, 152),
+                                       (1, 12, 4096, 148), (3, 2, 1000, 152), (1, 1, 1, 152),
+                                       (2, 2, 100000, 152), (64, 64, 4096, 152)])
+def test_split_choice_host_logic(lib, B, H, L, sms):
+    s = binding.fa_decode_choose_splits(B, H, L, sms)
+    assert s >= 1
+    chunk = binding.fa_decode_chunk_len(L, s)
+    assert chunk % 64 == 0
+    assert chunk * s >= L and (s - 1) * chunk < L          # every row in exactly one chunk
+    assert chunk <= 4096                                    # scores fit the kernel's buffer
+    # target: about two CTAs per SM over the whole (b, h, chunk) grid, at
+    # least one chunk per 4096 rows, at most one per 64 rows
+    target = min(max(-(-2 * sms // (B * H)), -(-L // 4096), 1), -(-L // 64))
+    assert s <= target
+    assert chunk == 64 or -(-L // (chunk - 64)) > target    # chunk is the smallest that fits
+    ws = binding.fa_decode_workspace_bytes(B, H, L, 64, s)
+    assert ws >= B * H * s * (64 + 2) * 4
+
+
+def test_split_choice_bad_args(lib):
+    assert binding.fa_decode_choose_splits(0, 1, 10, 152) < 0
+    assert binding.fa_decode_chunk_len(0, 1) < 0
+    assert binding.fa_decode_workspace_bytes(1, 1, 10, 48, 1) == 0
+
+
+def test_product_path_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(binding, "_lib", None)
+    monkeypatch.setattr(build, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="no CPU fallback"):
+        binding.load()
