@@ -35,6 +35,8 @@ _SIGNATURES = {
     "fa_prefill_ex": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _i, _u, _vp]),
     "fa_decode": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _vp]),
     "fa_decode_ex": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _i, _i, _vp, _sz, _vp]),
+    "fa_decode_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _i, _i, _vp]),
+    "fa_decode_noalloc_max_bytes": (_sz, []),
     "fa_decode_choose_splits": (_i, [_i, _i, _i, _i]),
     "fa_decode_chunk_len": (_i, [_i, _i]),
     "fa_decode_workspace_bytes": (_sz, [_i, _i, _i, _i, _i]),
@@ -98,6 +100,17 @@ def fa_decode_ex(q, k_cache, v_cache, seq_lens, out, B, H, max_len, d, scale, in
     return load().fa_decode_ex(q, k_cache, v_cache, seq_lens, out, B, H, max_len, d,
                                float(scale), in_dtype, out_dtype, num_splits, workspace,
                                workspace_bytes, stream)
+
+
+def fa_decode_noalloc(q, k_cache, v_cache, seq_lens, out, B, H, max_len, d, scale, in_dtype,
+                      out_dtype, num_splits=0, stream=0) -> int:
+    """Decode with the library's static scratch: allocates no device memory."""
+    return load().fa_decode_noalloc(q, k_cache, v_cache, seq_lens, out, B, H, max_len, d,
+                                    float(scale), in_dtype, out_dtype, num_splits, stream)
+
+
+def fa_decode_noalloc_max_bytes() -> int:
+    return load().fa_decode_noalloc_max_bytes()
 
 
 def fa_decode_choose_splits(B, H, max_len, num_sms=0) -> int:

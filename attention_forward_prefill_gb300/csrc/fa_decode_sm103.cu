@@ -286,3 +286,70 @@ int launch_decode(const DecodeLaunch &a, const DeviceInfo &dev, cudaStream_t str
 }
 
 }  // namespace fa
+
+// ---------------------------------------------------------------------------
+// Decode without any allocation.  The split partials live in a fixed
+// file-scope device array instead of a cudaMallocAsync'd or caller-provided
+// buffer.  Every GPU that loads this library reserves the array until the
+// process exits.  Host code may not pass the array's name to a kernel (on the
+// host it is only a stand-in for the device symbol): its device address is
+// looked up once per device with cudaGetSymbolAddress.
+// ---------------------------------------------------------------------------
+#include <mutex>
+
+namespace fa {
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(4) << 20;  // 4 MiB
+static __device__ __align__(256) unsigned char g_decode_scratch[kNoAllocScratchBytes];
+
+constexpr int kMaxScratchDevices = 64;
+std::mutex g_scratch_mu;
+void *g_scratch_addr[kMaxScratchDevices] = {};
+
+// Device address of the static scratch on the current device (set up on the
+// first call per device, with that device current).
+int noalloc_scratch(void **out) {
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (dev < 0 || dev >= kMaxScratchDevices) return cuda_fail(cudaErrorInvalidDevice);
+    std::lock_guard<std::mutex> lk(g_scratch_mu);
+    if (!g_scratch_addr[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_decode_scratch);
+        if (e != cudaSuccess) return cuda_fail(e);
+        g_scratch_addr[dev] = p;
+    }
+    *out = g_scratch_addr[dev];
+    return FA_OK;
+}
+
+}  // namespace
+}  // namespace fa
+
+extern "C" size_t fa_decode_noalloc_max_bytes(void) { return fa::kNoAllocScratchBytes; }
+
+extern "C" int fa_decode_noalloc(const void *q, const void *k_cache, const void *v_cache,
+                                 const int32_t *seq_lens, void *out, int B, int H, int max_len,
+                                 int d, float scale, fa_dtype in_dtype, fa_dtype out_dtype,
+                                 int num_splits, void *stream) {
+    // Pointer and size checks first (host arithmetic once the split count is
+    // known); every other argument error is left to fa_decode_ex.
+    if (!q || !k_cache || !v_cache || !seq_lens || !out) return FA_ERR_NULL;
+    if (B >= 1 && H >= 1 && max_len >= 1 && (d == 64 || d == 128) && num_splits >= 0) {
+        int splits = num_splits;
+        if (splits == 0) {
+            splits = fa_decode_choose_splits(B, H, max_len, 0);
+            if (splits < 0) return -splits;
+        }
+        if (fa_decode_workspace_bytes(B, H, max_len, d, splits) > fa::kNoAllocScratchBytes)
+            return FA_ERR_WORKSPACE;
+    }
+    void *scratch = nullptr;
+    int rc = fa::noalloc_scratch(&scratch);
+    if (rc != FA_OK) return rc;
+    // With a workspace supplied, fa_decode_ex allocates nothing.
+    return fa_decode_ex(q, k_cache, v_cache, seq_lens, out, B, H, max_len, d, scale, in_dtype,
+                        out_dtype, num_splits, scratch, fa::kNoAllocScratchBytes, stream);
+}

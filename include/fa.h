@@ -147,6 +147,37 @@ int fa_decode_chunk_len(int max_len, int num_splits);
 size_t fa_decode_workspace_bytes(int B, int H, int max_len, int d,
                                  int num_splits);
 
+/*
+ * Decode that allocates nothing.  The pages have no counterpart: this entry
+ * point exists for callers that cannot allocate device memory while they run
+ * -- for example a host that reserves the whole device up front for its own
+ * memory pool, a latency-critical serving loop where an allocation may block
+ * or synchronise, or a deployment that forbids allocation after start-up.
+ * It computes exactly what fa_decode_ex computes (same kernels, same split
+ * choice), with the split partials kept in a fixed 4 MiB device array built
+ * into the library (fa_decode_noalloc_max_bytes()); every GPU that loads the
+ * library holds that array until the process exits.
+ *   - Arguments are those of fa_decode_ex, without the workspace.
+ *   - A problem whose partials need more than the array holds
+ *     (fa_decode_workspace_bytes(...) > fa_decode_noalloc_max_bytes())
+ *     returns FA_ERR_WORKSPACE and enqueues nothing.
+ *   - The first call on each device looks up the array's device address with
+ *     that device current; make that first call before any stream capture.
+ *   - All calls share the one array and it keeps the last call's contents.
+ *     Nothing in it needs to start at zero (each call writes every partial it
+ *     reads), but two calls whose work overlaps on the GPU -- different
+ *     streams, or different host threads -- race on it and give wrong results.
+ *     Serialise them, e.g. on one stream.
+ */
+int fa_decode_noalloc(const void *q, const void *k_cache, const void *v_cache,
+                      const int32_t *seq_lens, void *out,
+                      int B, int H, int max_len, int d, float scale,
+                      fa_dtype in_dtype, fa_dtype out_dtype, int num_splits,
+                      void *stream);
+
+/* Bytes of the static scratch array behind fa_decode_noalloc. */
+size_t fa_decode_noalloc_max_bytes(void);
+
 /* Static text for a status code ("unknown status" for other values). */
 const char *fa_status_string(int status);
 
