@@ -82,7 +82,8 @@ struct Params {
     int in_bf16;
     int out_dtype;
     int scale_neg;
-    float scale_log2;  // scale * log2(e)
+    float scale_log2;      // c = scale * log2(e)
+    float scale_log2_abs;  // |c|
 };
 
 __device__ __forceinline__ void unit_coords(const Params &p, int u, int &bh, int &qb) {
@@ -136,10 +137,49 @@ __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint3
     }
 }
 
-// The two 16-bit values of a packed pair, back in fp32 (exact).
-__device__ __forceinline__ float2 unpack2(uint32_t w, int bf16) {
-    if (bf16) return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
-    return __half22float2(*reinterpret_cast<const __half2 *>(&w));
+// The two 16-bit values of a packed pair, back in fp32 (exact), as an f32x2.
+template <bool BF16>
+__device__ __forceinline__ uint64_t unpack2(uint32_t w) {
+    if constexpr (BF16) {
+        return f2_pack(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+    } else {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&w));
+        return f2_pack(f.x, f.y);
+    }
+}
+
+template <bool BF16>
+__device__ __forceinline__ uint32_t pack2t(float lo, float hi) {
+    if constexpr (BF16) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+        return *reinterpret_cast<uint32_t *>(&h);
+    } else {
+        __half2 h = __floats2half2_rn(lo, hi);
+        return *reinterpret_cast<uint32_t *>(&h);
+    }
+}
+
+// Row maximum of 128 scores: eight independent chains of 3-input maxima.
+template <bool NEG>
+__device__ __forceinline__ float row_max128(const uint32_t (&sr)[4][32]) {
+    float m[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const float a = __uint_as_float(sr[i >> 1][(i & 1) * 16 + 0]);
+        m[i] = NEG ? -a : a;
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        // chain i covers columns [16 i, 16 i + 16)
+#pragma unroll
+        for (int c = 1; c < 16; c += 2) {
+            const int col = 16 * i + c;
+            const float a = __uint_as_float(sr[col >> 5][col & 31]);
+            const float b = (c + 1 < 16) ? __uint_as_float(sr[(col + 1) >> 5][(col + 1) & 31]) : a;
+            m[i] = NEG ? fmax3(m[i], -a, -b) : fmax3(m[i], a, b);
+        }
+    }
+    return fmaxf(fmax3(m[0], m[1], m[2]), fmax3(fmax3(m[3], m[4], m[5]), m[6], m[7]));
 }
 
 __device__ __forceinline__ uint32_t pack2(float lo, float hi, int bf16) {
@@ -180,7 +220,7 @@ __device__ __forceinline__ void store_out32(void *dst, const uint32_t (&r)[32], 
     }
 }
 
-template <int D>
+template <int D, bool BF16>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap map_q,
                    const __grid_constant__ CUtensorMap map_k,
@@ -292,8 +332,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------------ MMA issuer
         regs_shrink<kRegsOther>();
         if (lane == 0) {
-            const uint32_t idesc_qk = idesc_f16(p.in_bf16 != 0, kBlockM, kBlockN, false, false);
-            const uint32_t idesc_pv = idesc_f16(p.in_bf16 != 0, kBlockM, D, false, true);
+            const uint32_t idesc_qk = idesc_f16(BF16, kBlockM, kBlockN, false, false);
+            const uint32_t idesc_pv = idesc_f16(BF16, kBlockM, D, false, true);
             const uint32_t q_addr = smem_u32(smem + L::kQOff);
             const uint32_t ring_addr = smem_u32(smem + L::kRingOff);
             const uint32_t s_tmem0 = tmem + L::kSCol0, s_tmem1 = tmem + L::kSCol1;
@@ -416,27 +456,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int q = 0; q < 4; ++q) reg_fence32(sr[q]);
 
                 const int cmax = lim - j * kBlockN;  // columns > cmax are masked
-                const bool masked = cmax < kBlockN - 1;
-                float m_tile;
-                if (!p.scale_neg) {
-                    float mx = -INFINITY;
-                    if (masked) {
-#pragma unroll
-                        for (int c = 0; c < 128; ++c)
-                            mx = fmaxf(mx, c > cmax ? -INFINITY : __uint_as_float(sr[c >> 5][c & 31]));
-                    } else {
-#pragma unroll
-                        for (int c = 0; c < 128; ++c) mx = fmaxf(mx, __uint_as_float(sr[c >> 5][c & 31]));
-                    }
-                    m_tile = (mx == -INFINITY) ? -INFINITY : mx * cexp;
-                } else {
-                    float mn = INFINITY;
+                if (cmax < kBlockN - 1) {
+                    // Masked columns get the score that the exponent maps to 0.
+                    const uint32_t fill = __float_as_uint(p.scale_neg ? INFINITY : -INFINITY);
 #pragma unroll
                     for (int c = 0; c < 128; ++c)
-                        mn = fminf(mn, (masked && c > cmax) ? INFINITY : __uint_as_float(sr[c >> 5][c & 31]));
-                    m_tile = (mn == INFINITY) ? -INFINITY : mn * cexp;
+                        sr[c >> 5][c & 31] = c > cmax ? fill : sr[c >> 5][c & 31];
                 }
-                __syncwarp();  // the masked branches above may diverge per lane
+                // m_tile = max_c (s_c * cexp), via max(+-s) * |cexp|
+                const float mx = p.scale_neg ? row_max128<true>(sr) : row_max128<false>(sr);
+                const float m_tile = (mx == -INFINITY) ? -INFINITY : mx * p.scale_log2_abs;
+                __syncwarp();  // the masked branch above may diverge per lane
                 const bool need = m_tile > m_ref + kTau;
                 float alpha = 1.f;
                 if (need) {
@@ -444,30 +474,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                     l *= alpha;
                     m_ref = m_tile;
                 }
-                const float negm = -m_ref;
-                float sum[4] = {0.f, 0.f, 0.f, 0.f};
+                const uint64_t c2 = f2_pack(cexp, cexp);
+                const uint64_t nm2 = f2_pack(-m_ref, -m_ref);
+                uint64_t sum2[4] = {0, 0, 0, 0};
                 // P in 32-key quarters: 16 packed registers per TMEM store.
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     uint32_t pk[16];
 #pragma unroll
-                    for (int c2 = 0; c2 < 16; ++c2) {
-                        const int c = q * 32 + 2 * c2;
-                        float p0 = ex2_approx(fmaf(__uint_as_float(sr[q][2 * c2]), cexp, negm));
-                        float p1 = ex2_approx(fmaf(__uint_as_float(sr[q][2 * c2 + 1]), cexp, negm));
-                        if (masked) {
-                            p0 = c > cmax ? 0.f : p0;
-                            p1 = c + 1 > cmax ? 0.f : p1;
-                        }
-                        pk[c2] = pack2(p0, p1, p.in_bf16);
+                    for (int c2i = 0; c2i < 16; ++c2i) {
+                        const uint64_t x = ffma2(f2_pack(__uint_as_float(sr[q][2 * c2i]),
+                                                         __uint_as_float(sr[q][2 * c2i + 1])),
+                                                 c2, nm2);
+                        pk[c2i] = pack2t<BF16>(ex2_approx(f2_lo(x)), ex2_approx(f2_hi(x)));
                         // l sums the same rounded weights the PV product uses,
                         // so a row dominated by one key returns that value row.
-                        const float2 r = unpack2(pk[c2], p.in_bf16);
-                        sum[c2 & 3] += r.x + r.y;
+                        sum2[c2i & 3] = fadd2(sum2[c2i & 3], unpack2<BF16>(pk[c2i]));
                     }
                     tmem_st16(s_addr + q * 16, pk);
                 }
-                l += (sum[0] + sum[1]) + (sum[2] + sum[3]);
+                const uint64_t s01 = fadd2(sum2[0], sum2[1]), s23 = fadd2(sum2[2], sum2[3]);
+                const uint64_t st = fadd2(s01, s23);
+                l += f2_lo(st) + f2_hi(st);
                 if (j > 0 && __any_sync(0xffffffffu, need)) {
                     // O rows are complete up to tile j-1: the commit that
                     // signalled S_t(j) also covers the earlier PV product.
@@ -556,7 +584,7 @@ int make_map(CUtensorMap *map, const void *base, int d, int N, int BH, int bf16)
     return FA_OK;
 }
 
-template <int D>
+template <int D, bool BF16>
 int launch_d(const PrefillLaunch &a, const DeviceInfo &dev, cudaStream_t stream) {
     using L = Layout<D>;
     static_assert(L::kSmemBytes <= 227 * 1024, "shared memory budget");
@@ -566,13 +594,13 @@ int launch_d(const PrefillLaunch &a, const DeviceInfo &dev, cudaStream_t stream)
     if ((rc = make_map(&mq, a.q, D, a.N, BH, a.in_bf16)) != FA_OK) return rc;
     if ((rc = make_map(&mk, a.k, D, a.N, BH, a.in_bf16)) != FA_OK) return rc;
     if ((rc = make_map(&mv, a.v, D, a.N, BH, a.in_bf16)) != FA_OK) return rc;
-    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D>,
+    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D, BF16>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
     if (e != cudaSuccess) return cuda_fail(e);
     // The setmaxnreg split inside the kernel draws on the launch allocation:
     // refuse to launch a build whose register count would make it wait forever.
     cudaFuncAttributes fattr;
-    e = cudaFuncGetAttributes(&fattr, prefill_kernel<D>);
+    e = cudaFuncGetAttributes(&fattr, prefill_kernel<D, BF16>);
     if (e != cudaSuccess) return cuda_fail(e);
     if (fattr.numRegs < kMinLaunchRegs) return cuda_fail(cudaErrorInvalidConfiguration);
 
@@ -586,10 +614,14 @@ int launch_d(const PrefillLaunch &a, const DeviceInfo &dev, cudaStream_t stream)
     p.no_skip = a.no_skip ? 1 : 0;
     p.in_bf16 = a.in_bf16;
     p.out_dtype = a.out_dtype;
-    p.scale_neg = a.scale < 0.f ? 1 : 0;
-    p.scale_log2 = a.scale * 1.4426950408889634f;
+    // scale == 0 runs as 2^-100: every weight is then exactly 1 as well, and
+    // masked scores (+-inf) never meet a zero multiplier.
+    const float scale = a.scale == 0.f ? 0x1p-100f : a.scale;
+    p.scale_neg = scale < 0.f ? 1 : 0;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.scale_log2_abs = fabsf(p.scale_log2);
     const int grid = p.n_units < dev.num_sms ? p.n_units : dev.num_sms;
-    prefill_kernel<D><<<grid, kThreads, L::kSmemBytes, stream>>>(mq, mk, mv, p);
+    prefill_kernel<D, BF16><<<grid, kThreads, L::kSmemBytes, stream>>>(mq, mk, mv, p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e);
     return FA_OK;
@@ -598,8 +630,8 @@ int launch_d(const PrefillLaunch &a, const DeviceInfo &dev, cudaStream_t stream)
 }  // namespace
 
 int launch_prefill(const PrefillLaunch &a, const DeviceInfo &dev, cudaStream_t stream) {
-    if (a.d == 64) return launch_d<64>(a, dev, stream);
-    if (a.d == 128) return launch_d<128>(a, dev, stream);
+    if (a.d == 64) return a.in_bf16 ? launch_d<64, true>(a, dev, stream) : launch_d<64, false>(a, dev, stream);
+    if (a.d == 128) return a.in_bf16 ? launch_d<128, true>(a, dev, stream) : launch_d<128, false>(a, dev, stream);
     return FA_ERR_HEAD_DIM;
 }
 
