@@ -40,8 +40,8 @@ namespace {
 constexpr int kThreads = 384;
 // setmaxnreg split: 2 x 128 threads x kRegsSoftmax + 128 x kRegsOther must not
 // exceed kThreads x (registers at launch); the host checks the launch count.
-constexpr int kRegsSoftmax = 200;
-constexpr int kRegsOther = 104;
+constexpr int kRegsSoftmax = 176;
+constexpr int kRegsOther = 152;
 constexpr int kMinLaunchRegs = (2 * 128 * kRegsSoftmax + 128 * kRegsOther + kThreads - 1) / kThreads;
 constexpr int kTmaWarp = 8;
 constexpr int kMmaWarp = 9;
@@ -113,28 +113,30 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volati
     return ok != 0;
 }
 
+// S (+)= Q K^T over d: a_desc / b_desc describe the Q and K tiles at K-step 0;
+// step kk moves (kk / 4) 64-column slabs and (kk % 4) 32-byte atoms along d.
+// Descriptors are built once per tile; each step only adds a constant to the
+// start-address field (shared addresses stay below 256 KB, so it cannot carry).
 template <int D>
-__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_addr, uint32_t k_addr,
+__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                          uint32_t idesc) {
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t off = (kk >> 2) * Layout<D>::kChunkBytes + (kk & 3) * 32;
-        umma_ss(d_tmem, sdesc_sw128(q_addr + off, 16, 1024), sdesc_sw128(k_addr + off, 16, 1024),
-                idesc, kk > 0 ? 1u : 0u);
+        const uint64_t off = ((kk >> 2) * Layout<D>::kChunkBytes + (kk & 3) * 32) >> 4;
+        umma_ss(d_tmem, a_desc + off, b_desc + off, idesc, kk > 0 ? 1u : 0u);
     }
 }
 
+// O (+)= P V: P from TMEM (16 keys = 8 columns per step), V tile [key][d] with d
+// contiguous is an MN-major B operand: 16 keys per step = two 8-key groups
+// (SBO apart), 64-column slabs of d LBO apart.
 template <int D>
-__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_addr,
+__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint64_t v_desc,
                                          uint32_t idesc, bool accumulate) {
 #pragma unroll
-    for (int kk = 0; kk < kBlockN / 16; ++kk) {
-        // V tile is [key][d] with d contiguous: an MN-major B operand.  16 keys
-        // per step = two 8-key groups (SBO apart); 64-column slabs LBO apart.
-        umma_ts(d_tmem, p_tmem + kk * 8,
-                sdesc_sw128(v_addr + kk * 16 * 128, Layout<D>::kChunkBytes, 1024), idesc,
+    for (int kk = 0; kk < kBlockN / 16; ++kk)
+        umma_ts(d_tmem, p_tmem + kk * 8, v_desc + ((kk * 16 * 128) >> 4), idesc,
                 (accumulate || kk > 0) ? 1u : 0u);
-    }
 }
 
 // The two 16-bit values of a packed pair, back in fp32 (exact), as an f32x2.
@@ -335,6 +337,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t idesc_qk = idesc_f16(BF16, kBlockM, kBlockN, false, false);
             const uint32_t idesc_pv = idesc_f16(BF16, kBlockM, D, false, true);
             const uint32_t q_addr = smem_u32(smem + L::kQOff);
+            const uint64_t q_desc0 = sdesc_sw128(q_addr, 16, 1024);
+            const uint64_t q_desc1 = sdesc_sw128(q_addr + L::kTileBytes, 16, 1024);
             const uint32_t ring_addr = smem_u32(smem + L::kRingOff);
             const uint32_t s_tmem0 = tmem + L::kSCol0, s_tmem1 = tmem + L::kSCol1;
             const uint32_t o_tmem0 = tmem + L::kOCol0, o_tmem1 = tmem + L::kOCol1;
@@ -356,13 +360,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t k_addr = ring_addr + slot * L::kTileBytes;
+                    const uint64_t k_desc = sdesc_sw128(ring_addr + slot * L::kTileBytes, 16, 1024);
                     if (n0 > 0) {
-                        issue_qk<D>(s_tmem0, q_addr, k_addr, idesc_qk);
+                        issue_qk<D>(s_tmem0, q_desc0, k_desc, idesc_qk);
                         umma_commit(s_full + 0);
                     }
                     if (n1 > 0) {
-                        issue_qk<D>(s_tmem1, q_addr + L::kTileBytes, k_addr, idesc_qk);
+                        issue_qk<D>(s_tmem1, q_desc1, k_desc, idesc_qk);
                         umma_commit(s_full + 1);
                     }
                     umma_commit(kv_empty + slot);
@@ -377,20 +381,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     tc_fence_after();
                     ++rc;
-                    const uint32_t v_addr = ring_addr + slot_v * L::kTileBytes;
+                    const uint64_t v_desc =
+                        sdesc_sw128(ring_addr + slot_v * L::kTileBytes, L::kChunkBytes, 1024);
                     const uint32_t slot_k = rc % L::kStages;
-                    const uint32_t k_addr = ring_addr + slot_k * L::kTileBytes;
+                    const uint64_t k_desc = sdesc_sw128(ring_addr + slot_k * L::kTileBytes, 16, 1024);
                     const uint32_t k_parity = (rc / L::kStages) & 1;
                     bool k_ready = false;
                     // One query tile's step: wait for P_t, O_t (+)= P_t V_j, then
                     // S_t = Q_t K_{j+1}^T (issued after the PV product that reads P_t).
                     auto tile_step = [&](int nt, uint64_t *pf, uint32_t &pc, uint32_t s_t,
-                                         uint32_t o_t, uint32_t q_t, uint64_t *sf, uint64_t *od) {
+                                         uint32_t o_t, uint64_t q_desc, uint64_t *sf, uint64_t *od) {
                         if (j >= nt) return true;
                         if (!mbar_wait(pf, pc & 1, abort_flag, kWatchdogNs)) return false;
                         ++pc;
                         tc_fence_after();
-                        issue_pv<D>(o_t, s_t, v_addr, idesc_pv, j > 0);
+                        issue_pv<D>(o_t, s_t, v_desc, idesc_pv, j > 0);
                         if (j == nt - 1) umma_commit(od);
                         if (j + 1 < nt) {
                             if (!k_ready) {
@@ -399,14 +404,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 tc_fence_after();
                                 k_ready = true;
                             }
-                            issue_qk<D>(s_t, q_t, k_addr, idesc_qk);
+                            issue_qk<D>(s_t, q_desc, k_desc, idesc_qk);
                             umma_commit(sf);
                         }
                         return true;
                     };
-                    ok = tile_step(n0, p_full + 0, pc0, s_tmem0, o_tmem0, q_addr, s_full + 0, o_done + 0) &&
-                         tile_step(n1, p_full + 1, pc1, s_tmem1, o_tmem1, q_addr + L::kTileBytes,
-                                   s_full + 1, o_done + 1);
+                    ok = tile_step(n0, p_full + 0, pc0, s_tmem0, o_tmem0, q_desc0, s_full + 0, o_done + 0) &&
+                         tile_step(n1, p_full + 1, pc1, s_tmem1, o_tmem1, q_desc1, s_full + 1,
+                                   o_done + 1);
                     if (!ok) break;
                     umma_commit(kv_empty + slot_v);
                     if (j + 1 < n) {
