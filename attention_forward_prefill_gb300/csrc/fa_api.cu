@@ -22,9 +22,9 @@ std::mutex g_dev_mu;
 DeviceInfo g_dev_cache[kMaxDevices];
 bool g_dev_have[kMaxDevices] = {};
 
-constexpr int kDecodeRowAlign = 64;       // chunk lengths are multiples of this
-constexpr int kDecodeAutoMaxChunk = 4096; // automatic choice keeps scores <= 16 KB
-constexpr int kDecodeMaxChunk = 48 * 1024;// explicit choice: scores <= 192 KB smem
+constexpr int kDecodeRowAlign = 64;      // chunk lengths are multiples of this
+constexpr int kDecodeAutoMaxChunk = 512;  // automatic choice: at most 512 rows per CTA
+constexpr int kDecodeMaxChunk = 48 * 1024; // any choice: scores of a chunk <= 192 KB smem
 
 bool misaligned(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; }
 
@@ -110,7 +110,9 @@ int fa_last_cuda_error(void) { return t_last_cuda_error; }
 
 int fa_device_status(int reset) {
     if (cudaDeviceSynchronize() != cudaSuccess) return -1;
-    return read_prefill_status(reset);
+    const int a = read_prefill_status(reset), b = read_decode_status(reset);
+    if (a < 0 || b < 0) return -1;
+    return a ? a : b;
 }
 
 int fa_prefill_ex(const void *q, const void *k, const void *v, void *out, int B, int H, int N,
@@ -171,7 +173,9 @@ int fa_decode_choose_splits(int B, int H, int max_len, int num_sms) {
         num_sms = dev.num_sms;
     }
     const long long bh = static_cast<long long>(B) * H;
-    // About two CTAs per SM, counting every (b, h, chunk) CTA of the grid.
+    // About two CTAs per SM over the whole (b, h, chunk) grid, and no CTA
+    // longer than 512 rows, so that ragged lengths do not leave a few long
+    // CTAs running alone at the end.
     long long splits = ceil_div(2LL * num_sms, bh);
     const long long max_splits = ceil_div(max_len, kDecodeRowAlign);
     const long long min_splits = ceil_div(max_len, kDecodeAutoMaxChunk);

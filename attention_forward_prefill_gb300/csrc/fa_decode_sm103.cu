@@ -32,6 +32,8 @@ constexpr int kSplitWarps = kSplitThreads / 32;
 constexpr int kUnroll = 8;
 constexpr int kMergeWarps = 4;
 
+__device__ int g_decode_status = 0;  // reserved for device-side waits; the decode kernels have none
+
 struct DParams {
     const uint16_t *q;
     const uint16_t *k;
@@ -87,6 +89,9 @@ __global__ void __launch_bounds__(kSplitThreads)
     __shared__ float red[kSplitWarps][D];
     __shared__ float red1[kSplitWarps];
 
+    // Let the merge kernel (launched with programmatic dependent launch) get
+    // scheduled early; it still waits for this whole grid before reading.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int s = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int len = clamp_len(p.seq_lens[b], p.max_len);
     const int start = s * p.chunk;
@@ -204,6 +209,8 @@ __global__ void __launch_bounds__(kMergeWarps * 32)
     constexpr int EPL = D / 32;  // output elements per lane
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int gw = blockIdx.x * kMergeWarps + warp;
+    // Wait until the split kernel has completed and its partials are visible.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     if (gw >= p.BH) return;
     const int b = gw / p.H;
     const int len = clamp_len(p.seq_lens[b], p.max_len);
@@ -269,14 +276,33 @@ int launch_decode_d(const DecodeLaunch &a, cudaStream_t stream) {
     decode_split_kernel<D><<<grid, kSplitThreads, smem, stream>>>(p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e);
-    const int mblocks = (p.BH + kMergeWarps - 1) / kMergeWarps;
-    decode_merge_kernel<D><<<mblocks, kMergeWarps * 32, 0, stream>>>(p);
-    e = cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((p.BH + kMergeWarps - 1) / kMergeWarps);
+    cfg.blockDim = dim3(kMergeWarps * 32);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, decode_merge_kernel<D>, p);
+    if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e);
     return FA_OK;
 }
 
 }  // namespace
+
+int read_decode_status(int reset) {
+    int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_decode_status, sizeof(int)) != cudaSuccess) return -1;
+    if (reset && v) {
+        int z = 0;
+        if (cudaMemcpyToSymbol(g_decode_status, &z, sizeof(int)) != cudaSuccess) return -1;
+    }
+    return v;
+}
 
 int launch_decode(const DecodeLaunch &a, const DeviceInfo &dev, cudaStream_t stream) {
     (void)dev;

@@ -57,5 +57,6 @@ int launch_decode(const DecodeLaunch &a, const DeviceInfo &dev, cudaStream_t str
 
 // Device-side watchdog words (one per kernel translation unit).
 int read_prefill_status(int reset);
+int read_decode_status(int reset);
 
 }  // namespace fa

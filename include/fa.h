@@ -134,7 +134,9 @@ int fa_decode_ex(const void *q, const void *k_cache, const void *v_cache,
 
 /*
  * The automatic split count ("Kernel design" table: choose_decode_split
- * targets about two resident blocks per SM).  Pure host arithmetic on its
+ * targets about two resident blocks per SM): enough (b, h, chunk) CTAs for
+ * two per SM, and chunks of at most 512 rows so that ragged lengths do not
+ * leave a few long CTAs running alone.  Pure host arithmetic on its
  * arguments; num_sms <= 0 means "the current device's SM count".
  * Returns the split count (>= 1), or a negative fa_status on bad arguments.
  */
