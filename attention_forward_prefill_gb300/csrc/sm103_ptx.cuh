@@ -85,14 +85,20 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t by
                  : "memory");
 }
 
+// Test for completion of the phase with the given parity.  The suspend-time
+// hint lets the hardware park the waiting thread until the phase completes
+// (or the hint expires) instead of returning at once: a waiting warp then
+// takes no issue slots from the warps that do the work on its SMSP.
+constexpr uint32_t kSuspendHintNs = 100000;
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendHintNs)
         : "memory");
     return ok != 0;
 }
@@ -106,7 +112,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 63u) == 0u) {
+        if ((it & 3u) == 0u) {
             if (*abort_flag) return false;
             if (globaltimer_ns() - t0 > limit_ns) {
                 *abort_flag = 1;
