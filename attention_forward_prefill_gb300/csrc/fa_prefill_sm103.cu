@@ -251,7 +251,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(q_empty, 1);
         for (int t = 0; t < 2; ++t) {
             mbar_init(s_full + t, 1);
-            mbar_init(p_full + t, 128);
+            mbar_init(p_full + t, 4);  // one arrival per softmax warp
             mbar_init(o_done + t, 1);
         }
         mbar_init(drain, 1);
@@ -519,7 +519,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tmem_st_wait();
                 tc_fence_before();
-                mbar_arrive(p_full + t);
+                // Every lane's TMEM stores are ordered before the warp sync;
+                // one arrival per warp keeps traffic on the barrier low.
+                __syncwarp();
+                if (lane == 0) mbar_arrive(p_full + t);
             }
             if (!ok) break;
             // ---- epilogue: O / l -> out
