@@ -84,7 +84,29 @@ struct Params {
     int scale_neg;
     float scale_log2;      // c = scale * log2(e)
     float scale_log2_abs;  // |c|
+    // Stream-K (non-causal only): the W = n_units * T (unit, key tile) steps
+    // are cut into gridDim.x equal contiguous ranges; a unit cut between two
+    // CTAs is finished by the fixup kernel from the partials in ws_o / ws_ml.
+    int stream_k;
+    int T;                 // key tiles per unit
+    long long W;           // n_units * T
+    float *ws_o;           // [gridDim.x][2 slots][256 rows][D]  unnormalised O
+    float *ws_ml;          // [gridDim.x][2 slots][256 rows][2]  (m_ref, l)
 };
+
+// The CTA's next piece of work: unit u, key tiles [j0, j1), and the key-tile
+// counts n0, n1 of its two query tiles (0 = no rows).  Every role of a CTA
+// walks the same sequence.
+struct SegCursor {
+    long long s, s_end;  // stream-K step range
+    int u;               // unit-granular schedule
+};
+
+__device__ __forceinline__ void seg_begin(const Params &p, SegCursor &c) {
+    c.s = static_cast<long long>(blockIdx.x) * p.W / gridDim.x;
+    c.s_end = static_cast<long long>(blockIdx.x + 1) * p.W / gridDim.x;
+    c.u = blockIdx.x;
+}
 
 __device__ __forceinline__ void unit_coords(const Params &p, int u, int &bh, int &qb) {
     if (p.causal) {  // heaviest query blocks first
@@ -103,6 +125,31 @@ __device__ __forceinline__ int kv_tiles(const Params &p, int row0) {
     if (!p.causal || p.no_skip) return nk;
     const int last = min(row0 + kBlockM - 1, p.N - 1);
     return last / kBlockN + 1;
+}
+
+__device__ __forceinline__ bool seg_next(const Params &p, SegCursor &c, int &u, int &bh, int &q0,
+                                         int &j0, int &j1, int &n0, int &n1) {
+    int qb;
+    if (p.stream_k) {
+        if (c.s >= c.s_end) return false;
+        u = static_cast<int>(c.s / p.T);
+        j0 = static_cast<int>(c.s % p.T);
+        const long long left = c.s_end - c.s;
+        j1 = static_cast<int>(left < p.T - j0 ? j0 + left : p.T);
+        c.s += j1 - j0;
+    } else {
+        if (c.u >= p.n_units) return false;
+        u = c.u;
+        c.u += gridDim.x;
+        j0 = 0;
+        j1 = -1;
+    }
+    unit_coords(p, u, bh, qb);
+    q0 = qb * kRowsPerUnit;
+    n0 = kv_tiles(p, q0);
+    n1 = kv_tiles(p, q0 + kBlockM);
+    if (j1 < 0) j1 = max(n0, n1);
+    return true;
 }
 
 // Warp-uniform bounded wait: lane 0 polls, the verdict is broadcast.
@@ -286,12 +333,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint8_t *ring = smem + L::kRingOff;
             uint32_t qc = 0, rc = 0;
             bool ok = true;
-            for (int u = blockIdx.x; u < p.n_units && ok; u += gridDim.x) {
-                int bh, qb;
-                unit_coords(p, u, bh, qb);
-                const int q0 = qb * kRowsPerUnit;
-                const int n0 = kv_tiles(p, q0), n1 = kv_tiles(p, q0 + kBlockM);
-                const int n = max(n0, n1);
+            SegCursor cur;
+            seg_begin(p, cur);
+            int u, bh, q0, j0, j1, n0, n1;
+            while (ok && seg_next(p, cur, u, bh, q0, j0, j1, n0, n1)) {
                 if (qc > 0 && !mbar_wait(q_empty, (qc - 1) & 1, abort_flag, kWatchdogNs)) {
                     ok = false;
                     break;
@@ -302,7 +347,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tma_load_3d(q_smem + t * L::kTileBytes + c * L::kChunkBytes, &map_q, q_full,
                                     c * 64, q0 + t * kBlockM, bh, pol_q);
                 ++qc;
-                for (int j = 0; j < n && ok; ++j) {
+                for (int j = j0; j < j1 && ok; ++j) {
                     for (int kv = 0; kv < 2; ++kv) {
                         const uint32_t slot = rc % L::kStages;
                         if (rc >= (uint32_t)L::kStages &&
@@ -344,12 +389,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t o_tmem0 = tmem + L::kOCol0, o_tmem1 = tmem + L::kOCol1;
             uint32_t qc = 0, rc = 0, pc0 = 0, pc1 = 0;
             bool ok = true;
-            for (int u = blockIdx.x; u < p.n_units && ok; u += gridDim.x) {
-                int bh, qb;
-                unit_coords(p, u, bh, qb);
-                const int q0 = qb * kRowsPerUnit;
-                const int n0 = kv_tiles(p, q0), n1 = kv_tiles(p, q0 + kBlockM);
-                const int n = max(n0, n1);
+            SegCursor cur;
+            seg_begin(p, cur);
+            int u, bh, q0, j0, j1, nk0, nk1;
+            while (ok && seg_next(p, cur, u, bh, q0, j0, j1, nk0, nk1)) {
+                // key tiles [j0, e_t) for query tile t (empty when e_t <= j0)
+                const int n0 = min(nk0, j1), n1 = min(nk1, j1);
                 if (!mbar_wait(q_full, qc & 1, abort_flag, kWatchdogNs)) { ok = false; break; }
                 ++qc;
                 tc_fence_after();
@@ -361,19 +406,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     tc_fence_after();
                     const uint64_t k_desc = sdesc_sw128(ring_addr + slot * L::kTileBytes, 16, 1024);
-                    if (n0 > 0) {
+                    if (n0 > j0) {
                         issue_qk<D>(s_tmem0, q_desc0, k_desc, idesc_qk);
                         umma_commit(s_full + 0);
                     }
-                    if (n1 > 0) {
+                    if (n1 > j0) {
                         issue_qk<D>(s_tmem1, q_desc1, k_desc, idesc_qk);
                         umma_commit(s_full + 1);
                     }
                     umma_commit(kv_empty + slot);
                     ++rc;
-                    if (n == 1) umma_commit(q_empty);
+                    if (j1 - j0 == 1) umma_commit(q_empty);
                 }
-                for (int j = 0; j < n && ok; ++j) {
+                for (int j = j0; j < j1 && ok; ++j) {
                     const uint32_t slot_v = rc % L::kStages;
                     if (!mbar_wait(kv_full + slot_v, (rc / L::kStages) & 1, abort_flag, kWatchdogNs)) {
                         ok = false;
@@ -395,7 +440,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (!mbar_wait(pf, pc & 1, abort_flag, kWatchdogNs)) return false;
                         ++pc;
                         tc_fence_after();
-                        issue_pv<D>(o_t, s_t, v_desc, idesc_pv, j > 0);
+                        issue_pv<D>(o_t, s_t, v_desc, idesc_pv, j > j0);
                         if (j == nt - 1) umma_commit(od);
                         if (j + 1 < nt) {
                             if (!k_ready) {
@@ -414,10 +459,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                                    o_done + 1);
                     if (!ok) break;
                     umma_commit(kv_empty + slot_v);
-                    if (j + 1 < n) {
+                    if (j + 1 < j1) {
                         umma_commit(kv_empty + slot_k);
                         ++rc;
-                        if (j + 1 == n - 1) umma_commit(q_empty);
+                        if (j + 1 == j1 - 1) umma_commit(q_empty);
                     }
                 }
             }
@@ -439,17 +484,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float cexp = p.scale_log2;
         uint32_t sc = 0, oc = 0;
         bool ok = true;
-        for (int u = blockIdx.x; u < p.n_units && ok; u += gridDim.x) {
-            int bh, qb;
-            unit_coords(p, u, bh, qb);
-            const int tile_row0 = qb * kRowsPerUnit + t * kBlockM;
-            const int ntile = kv_tiles(p, tile_row0);
-            if (ntile == 0) continue;
+        SegCursor cur;
+        seg_begin(p, cur);
+        int u, bh, q0, j0, j1, nk0, nk1;
+        for (int seg = 0; ok && seg_next(p, cur, u, bh, q0, j0, j1, nk0, nk1); ++seg) {
+            const int ntile = min(t ? nk1 : nk0, j1);  // this tile's key tiles: [j0, ntile)
+            if (ntile <= j0) continue;
+            const int tile_row0 = q0 + t * kBlockM;
             const int row = tile_row0 + r;
             const int lim = p.causal ? min(row, p.N - 1) : p.N - 1;  // last visible key
             float m_ref = -INFINITY;
             float l = 0.f;
-            for (int j = 0; j < ntile; ++j) {
+            for (int j = j0; j < ntile; ++j) {
                 if (!warp_wait(s_full + t, sc & 1, abort_flag)) { ok = false; break; }
                 ++sc;
                 tc_fence_after();
@@ -529,6 +575,28 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!warp_wait(o_done + t, oc & 1, abort_flag)) { ok = false; break; }
             ++oc;
             tc_fence_after();
+            if (p.stream_k && !(j0 == 0 && j1 == p.T)) {
+                // Part of a unit: keep O unnormalised with its (m_ref, l) for the
+                // fixup kernel.  Slot 0 = the CTA's first piece, 1 = its last.
+                const size_t rec = (static_cast<size_t>(blockIdx.x) * 2 + (seg == 0 ? 0 : 1)) * kRowsPerUnit +
+                                   t * kBlockM + r;
+                float *wo = p.ws_o + rec * D;
+#pragma unroll
+                for (int q = 0; q < D / 32; ++q) {
+                    uint32_t o[32];
+                    tmem_ld32(o_addr + q * 32, o);
+                    tmem_ld_wait();
+                    reg_fence32(o);
+                    uint4 *d4 = reinterpret_cast<uint4 *>(wo + q * 32);
+#pragma unroll
+                    for (int v = 0; v < 8; ++v)
+                        d4[v] = make_uint4(o[4 * v], o[4 * v + 1], o[4 * v + 2], o[4 * v + 3]);
+                }
+                p.ws_ml[rec * 2 + 0] = m_ref;
+                p.ws_ml[rec * 2 + 1] = l;
+                tc_fence_before();
+                continue;
+            }
             const float inv = 1.0f / l;
             const int osize = p.out_dtype == FA_F32 ? 4 : 2;
             uint8_t *orow = reinterpret_cast<uint8_t *>(p.out) +
@@ -554,6 +622,88 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_dealloc(tmem, kTmemCols);
     }
     if (threadIdx.x == 0 && *abort_flag) atomicCAS(&g_prefill_status, 0, (int)FA_ERR_WATCHDOG);
+}
+
+// ---------------------------------------------------------------- stream-K fixup
+// Units cut between CTAs: merge the partial (O, m_ref, l) of every piece in CTA
+// order, O = sum_k 2^(m_k - M) O_k / sum_k 2^(m_k - M) l_k, and write the rows.
+constexpr int kMaxSplit = 192;
+
+struct FixupParams {
+    void *out;
+    const float *ws_o;
+    const float *ws_ml;
+    int N;
+    int n_qb;
+    int T;
+    int G;
+    long long W;
+    int out_dtype;
+    int n_split;
+    int4 item[kMaxSplit];  // (unit, first CTA, last CTA, unused)
+};
+
+template <int D>
+__global__ void __launch_bounds__(256) prefill_fixup(const __grid_constant__ FixupParams f) {
+    constexpr int EPL = D / 32;  // columns per lane
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // Launched with programmatic dependent launch: wait until the main kernel
+    // has completed and its partials are visible.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int4 it = f.item[blockIdx.x];
+    const int u = it.x;
+    const int rrow = blockIdx.y * 8 + warp;  // row within the 256-row unit
+    const int bh = u / f.n_qb, qb = u % f.n_qb;
+    const int row = qb * kRowsPerUnit + rrow;
+    if (row >= f.N) return;
+    const long long ustart = static_cast<long long>(u) * f.T;
+    auto rec_of = [&](int c) {
+        const long long first = static_cast<long long>(c) * f.W / f.G;
+        return (static_cast<size_t>(c) * 2 + (first >= ustart ? 0 : 1)) * kRowsPerUnit + rrow;
+    };
+    float M = -INFINITY;
+    for (int c = it.y; c <= it.z; ++c) M = fmaxf(M, f.ws_ml[rec_of(c) * 2]);
+    float L = 0.f, o[EPL];
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) o[e] = 0.f;
+    for (int c = it.y; c <= it.z; ++c) {
+        const size_t rec = rec_of(c);
+        const float w = ex2_approx(f.ws_ml[rec * 2] - M);
+        L = fmaf(w, f.ws_ml[rec * 2 + 1], L);
+        const float *src = f.ws_o + rec * D + lane * EPL;
+#pragma unroll
+        for (int e = 0; e < EPL; e += 2) {
+            float2 x;
+            if constexpr (EPL % 4 == 0) {
+                if (e % 4 == 0) {
+                    const float4 y = *reinterpret_cast<const float4 *>(src + e);
+                    o[e] = fmaf(w, y.x, o[e]);
+                    o[e + 1] = fmaf(w, y.y, o[e + 1]);
+                    o[e + 2] = fmaf(w, y.z, o[e + 2]);
+                    o[e + 3] = fmaf(w, y.w, o[e + 3]);
+                }
+                continue;
+            }
+            x = *reinterpret_cast<const float2 *>(src + e);
+            o[e] = fmaf(w, x.x, o[e]);
+            o[e + 1] = fmaf(w, x.y, o[e + 1]);
+        }
+    }
+    const float inv = 1.0f / L;
+    const size_t off = (static_cast<size_t>(bh) * f.N + row) * D + lane * EPL;
+    if (f.out_dtype == FA_F32) {
+        float *dst = reinterpret_cast<float *>(f.out) + off;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) dst[e] = o[e] * inv;
+    } else if (f.out_dtype == FA_BF16) {
+        __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(f.out) + off;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) dst[e] = __float2bfloat16_rn(o[e] * inv);
+    } else {
+        __half *dst = reinterpret_cast<__half *>(f.out) + off;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) dst[e] = __float2half_rn(o[e] * inv);
+    }
 }
 
 // ---------------------------------------------------------------- host side
@@ -628,9 +778,83 @@ int launch_d(const PrefillLaunch &a, const DeviceInfo &dev, cudaStream_t stream)
     p.scale_neg = scale < 0.f ? 1 : 0;
     p.scale_log2 = scale * 1.4426950408889634f;
     p.scale_log2_abs = fabsf(p.scale_log2);
-    const int grid = p.n_units < dev.num_sms ? p.n_units : dev.num_sms;
+    p.T = (a.N + kBlockN - 1) / kBlockN;
+    p.W = static_cast<long long>(p.n_units) * p.T;
+    p.ws_o = nullptr;
+    p.ws_ml = nullptr;
+    // Non-causal units all cost T key-tile steps.  Unit by unit, the busiest
+    // CTA does ceil(U / G) * T steps; cut into equal ranges (stream-K) it does
+    // ceil(W / G) plus the cost of merging the cut units (a fixup pass over
+    // their partials and shorter pieces), measured at about 24 steps.  Take
+    // the cheaper of the two.
+    const int sms = dev.num_sms < kMaxSplit ? dev.num_sms : kMaxSplit;
+    constexpr long long kMergeCostSteps = 24;
+    const long long unit_steps = static_cast<long long>((p.n_units + sms - 1) / sms) * p.T;
+    const long long sk_steps = (p.W + sms - 1) / sms + kMergeCostSteps;
+    p.stream_k = (!p.causal && p.n_units > sms && sk_steps < unit_steps) ? 1 : 0;
+    int grid = p.n_units < dev.num_sms ? p.n_units : dev.num_sms;
+    FixupParams f;
+    f.n_split = 0;
+    void *ws = nullptr;
+    if (p.stream_k) {
+        grid = sms;
+        f.out = a.out;
+        f.N = a.N;
+        f.n_qb = p.n_qb;
+        f.T = p.T;
+        f.G = grid;
+        f.W = p.W;
+        f.out_dtype = a.out_dtype;
+        auto first_step = [&](long long c) { return c * p.W / grid; };
+        auto cta_of = [&](long long step) {  // c with first_step(c) <= step < first_step(c + 1)
+            long long c = (step + 1) * grid / p.W;
+            while (c > 0 && first_step(c) > step) --c;
+            while (c + 1 < grid && first_step(c + 1) <= step) ++c;
+            return static_cast<int>(c);
+        };
+        int last_u = -1;
+        for (int c = 1; c < grid; ++c) {
+            const long long b = first_step(c);
+            if (b % p.T == 0) continue;  // boundary between units: nothing to merge
+            const int u = static_cast<int>(b / p.T);
+            if (u == last_u) continue;
+            last_u = u;
+            f.item[f.n_split++] = make_int4(u, cta_of(static_cast<long long>(u) * p.T),
+                                            cta_of(static_cast<long long>(u + 1) * p.T - 1), 0);
+        }
+        if (f.n_split > 0) {
+            const size_t o_bytes = static_cast<size_t>(grid) * 2 * kRowsPerUnit * D * sizeof(float);
+            const size_t ml_bytes = static_cast<size_t>(grid) * 2 * kRowsPerUnit * 2 * sizeof(float);
+            e = cudaMallocAsync(&ws, o_bytes + ml_bytes, stream);
+            if (e != cudaSuccess) {
+                cuda_fail(e);
+                return FA_ERR_WORKSPACE;
+            }
+            p.ws_o = static_cast<float *>(ws);
+            p.ws_ml = reinterpret_cast<float *>(static_cast<char *>(ws) + o_bytes);
+            f.ws_o = p.ws_o;
+            f.ws_ml = p.ws_ml;
+        }
+    }
     prefill_kernel<D, BF16><<<grid, kThreads, L::kSmemBytes, stream>>>(mq, mk, mv, p);
     e = cudaGetLastError();
+    if (e == cudaSuccess && f.n_split > 0) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(f.n_split, kRowsPerUnit / 8);
+        cfg.blockDim = dim3(256);
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, prefill_fixup<D>, f);
+        if (e == cudaSuccess) e = cudaGetLastError();
+    }
+    if (ws) {
+        const cudaError_t e2 = cudaFreeAsync(ws, stream);
+        if (e == cudaSuccess) e = e2;
+    }
     if (e != cudaSuccess) return cuda_fail(e);
     return FA_OK;
 }

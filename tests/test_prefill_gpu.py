@@ -169,12 +169,25 @@ def test_identical_value_rows(fa):
 
 
 # ------------------------------------------------------------ determinism
-def test_run_to_run_bit_identical(fa):
+@pytest.mark.parametrize("causal", [True, False])
+def test_run_to_run_bit_identical(fa, causal):
     import torch
     q, k, v, _ = make_qkv((4, 12, 2048, 64), "f16", CFG_GPT2)
-    outs = [run_prefill(fa, q, k, v, "f16", c, 0.125, "f16") for c in (True, True, True)]
+    outs = [run_prefill(fa, q, k, v, "f16", causal, 0.125, "f16") for _ in range(3)]
     for o in outs[1:]:
         assert torch.equal(o.view(torch.int16), outs[0].view(torch.int16))
+
+
+@pytest.mark.parametrize("shape", [(1, 24, 8192, 64), (1, 3, 1000, 64), (2, 5, 4100, 128)])
+def test_units_cut_across_ctas(fa, oracle_mod, shape):
+    # When the last wave of 256-row units would leave most SMs idle, the
+    # non-causal work is spread over all SMs in equal step ranges, so a unit
+    # can be cut between CTAs and merged afterwards (768 and 170 units here on
+    # ~150 SMs); the small shape keeps the unit-per-CTA schedule.
+    B, H, N, d = shape
+    dtype = "bf16" if d == 128 else "f16"
+    check(fa, oracle_mod, shape, dtype, "f32", False, 1.0 / np.sqrt(d), 210 + N,
+          rows=G.sample_rows(N, 7) if N > 2048 else None)
 
 
 @pytest.mark.parametrize("N,d", [(2048, 64), (1000, 128), (4096, 128)])
