@@ -40,7 +40,11 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM traffic per launch from an ncu capture, valid only for the kernel source
 # it was taken on (sha256 of the .cu file, first 16 hex digits).
 NCU_TRAFFIC = {
-    # "prefill": {"src_sha": "...", "bytes_per_launch": {"16384": ...}},
+    # Measured at N=8192 (ncu --set full, profiles/prefill_kernel_d128_n8192.md);
+    # the other lengths are scaled by the bytes the launch must move (linear in N).
+    "prefill": {"src_sha": "bd4267fe943e3762",
+                "bytes_per_launch": {"4096": 124.65e6 / 2, "8192": 124.65e6, "16384": 124.65e6 * 2},
+                "measured_at": "8192", "scaled": ["4096", "16384"]},
 }
 
 
