@@ -18,6 +18,11 @@
  *   - same README, "What did I implement?" (generation phase): a decode query
  *     attends over the first seq_len rows of its KV cache;
  *   - "Kernel design" table, causal row: key j is visible to query i iff j <= i.
+ *     When there are fewer queries than keys (a new chunk of a prompt over
+ *     keys that already include earlier tokens) the queries are the LAST n_q
+ *     positions: key j is visible to query i iff j <= i + (n_k - n_q).  This
+ *     is the reading under which a decode row (n_q = 1) sees its whole cache,
+ *     as "What did I implement?" describes; for n_q == n_k it is j <= i.
  *
  * For query row i with visible key set J:
  *     s_j  = scale * sum_c Q[i,c] * K[j,c]            (j in J)
@@ -77,7 +82,8 @@ static void weighted_values(const double *p, const double *v, long n, int d,
  * One attention head, a chosen subset of query rows.
  *   q: [n_q][d], k, v: [n_k][d], out: [n_rows][d]
  *   rows: the query indices to compute (NULL = all n_q rows, in order)
- *   causal: key j visible to query i iff j <= i (square problems: n_q == n_k)
+ *   causal: key j visible to query i iff j <= i + (n_k - n_q)  (j <= i when
+ *           n_q == n_k); a row with no visible key is a zero row
  *   p_out: optional [n_rows][n_k] softmax weights (zero for masked keys)
  * Returns 0 on success, -1 on bad arguments or allocation failure.
  */
@@ -93,7 +99,11 @@ int oracle_attention_head(const double *q, const double *k, const double *v,
         long i = rows ? rows[r] : r;
         if (i < 0 || i >= n_q) { free(s); return -1; }
         long n_vis = n_k;
-        if (causal) n_vis = (i + 1 < n_k) ? i + 1 : n_k;
+        if (causal) {
+            n_vis = i + 1 + (n_k - n_q);
+            if (n_vis > n_k) n_vis = n_k;
+            if (n_vis < 0) n_vis = 0;
+        }
         double *o = out + r * (long)d;
         if (p_out)
             for (long j = 0; j < n_k; ++j) p_out[r * n_k + j] = 0.0;

@@ -103,9 +103,14 @@ def attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, causal: bool,
               scale: float, rows=None, threads: int = 1) -> np.ndarray:
     """O = softmax(scale * Q K^T [causal mask]) V for every (batch, head).
 
-    q, k, v: float64 arrays [B, H, N, d] (or [N, d] for one head).
+    q: float64 [B, Hq, Nq, d]; k, v: [B, Hkv, Nk, d] (or [N, d] for one head).
+    Grouped heads: Hq must be a multiple of Hkv, and query head h reads key /
+    value head h // (Hq // Hkv) -- the result equals repeating every key /
+    value head Hq // Hkv times in place, the host-side repeat that the
+    flash-attention-cuda README's "Future work" (kernel-side GQA) refers to.
+    Causal with Nq != Nk: query i sees key j iff j <= i + (Nk - Nq).
     rows: None (all rows) or a sequence of query indices, the same for every
-    head; the result then has shape [B, H, len(rows), d].
+    head; the result then has shape [B, Hq, len(rows), d].
     threads: heads are independent, so they may be spread over host threads.
     """
     single = q.ndim == 2
@@ -115,7 +120,10 @@ def attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, causal: bool,
     k = np.ascontiguousarray(k, dtype=np.float64)
     v = np.ascontiguousarray(v, dtype=np.float64)
     B, H, n_q, d = q.shape
-    n_k = k.shape[2]
+    h_kv, n_k = k.shape[1], k.shape[2]
+    if H % h_kv != 0 or v.shape[:3] != k.shape[:3] or k.shape[0] != B:
+        raise ValueError("bad shapes: q [B,Hq,Nq,d], k/v [B,Hkv,Nk,d] with Hkv | Hq")
+    group = H // h_kv
     if rows is None:
         row_arr = None
         n_rows = n_q
@@ -130,8 +138,9 @@ def attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, causal: bool,
     def one(bh):
         b, h = divmod(bh, H)
         o = np.zeros((n_rows, d), dtype=np.float64)
+        hk = h // group
         rc = lib.oracle_attention_head(
-            _dptr(q[b, h]), _dptr(k[b, h]), _dptr(v[b, h]), _dptr(o),
+            _dptr(q[b, h]), _dptr(k[b, hk]), _dptr(v[b, hk]), _dptr(o),
             n_q, n_k, d, int(bool(causal)), float(scale), rows_ptr, n_rows, None)
         if rc != 0:
             raise RuntimeError("oracle_attention_head failed")
@@ -144,6 +153,37 @@ def attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, causal: bool,
         for bh in range(B * H):
             one(bh)
     return out[0, 0] if single else out
+
+
+def attention_varlen(q: np.ndarray, k: np.ndarray, v: np.ndarray, cu_seqlens_q,
+                     cu_seqlens_k, causal: bool, scale: float, threads: int = 1) -> np.ndarray:
+    """Packed variable-length batch: sequence b owns query tokens
+    [cu_q[b], cu_q[b+1]) and key tokens [cu_k[b], cu_k[b+1]).
+
+    q: float64 [total_q, Hq, d]; k, v: [total_k, Hkv, d]; returns [total_q, Hq, d].
+    Each sequence is an independent problem with its own lengths (causal
+    alignment and grouped heads as in ``attention``); sequences never see
+    each other's keys.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    cq = [int(x) for x in cu_seqlens_q]
+    ck = [int(x) for x in cu_seqlens_k]
+    if len(cq) != len(ck) or cq[0] != 0 or ck[0] != 0:
+        raise ValueError("cu_seqlens must start at 0 and have B + 1 entries each")
+    out = np.zeros(q.shape, dtype=np.float64)
+    for b in range(len(cq) - 1):
+        if cq[b + 1] == cq[b]:
+            continue
+        qs = q[cq[b]:cq[b + 1]].transpose(1, 0, 2)[None]      # [1, Hq, nq, d]
+        ks = k[ck[b]:ck[b + 1]].transpose(1, 0, 2)[None]
+        vs = v[ck[b]:ck[b + 1]].transpose(1, 0, 2)[None]
+        if ks.shape[2] == 0:
+            continue                                           # no keys: zero rows
+        o = attention(qs, ks, vs, causal, scale, threads=threads)
+        out[cq[b]:cq[b + 1]] = o[0].transpose(1, 0, 2)
+    return out
 
 
 def attention_weights(q: np.ndarray, k: np.ndarray, causal: bool, scale: float,

@@ -256,3 +256,104 @@ def test_decode_matches_torch_sdpa_on_truncated_cache(oracle_mod):
             torch.from_numpy(q[b:b + 1]), torch.from_numpy(kc[b:b + 1, :, :n]),
             torch.from_numpy(vc[b:b + 1, :, :n]), scale=0.125).numpy()
         assert np.max(np.abs(got[b:b + 1] - want)) < 1e-12
+
+
+# ------------------------------- chunked prefill, grouped heads, packed batches
+def test_chunk_rows_equal_the_tail_of_the_square_causal_problem(oracle_mod):
+    # a prompt chunk of the last Nq positions over all Nk keys is the last Nq
+    # rows of the square causal problem (same visible sets, row by row)
+    r = rng(20)
+    Nk, Nq, d = 40, 15, 8
+    q, k, v = r.normal(size=(3, Nk, d))
+    square = oracle_mod.attention(q, k, v, True, 0.3)
+    chunk = oracle_mod.attention(q[Nk - Nq:], k, v, True, 0.3)
+    assert np.array_equal(chunk, square[Nk - Nq:])
+    # the last query row sees every key, and a one-row chunk is a decode step
+    full = oracle_mod.attention(q[Nk - Nq:], k, v, False, 0.3)
+    assert np.array_equal(chunk[-1], full[-1])
+    dec = oracle_mod.decode(q[None, None, -1:], k[None, None], v[None, None], [Nk], 0.3)
+    one = oracle_mod.attention(q[-1:], k, v, True, 0.3)
+    assert np.max(np.abs(dec[0, 0, 0] - one[0])) < 1e-15
+
+
+def test_more_queries_than_keys_leaves_leading_rows_empty(oracle_mod):
+    # Nq > Nk: query i sees keys j <= i - (Nq - Nk); the first Nq - Nk rows
+    # see nothing (zero rows), the next sees key 0 alone
+    r = rng(21)
+    q = r.normal(size=(10, 6))
+    k, v = r.normal(size=(2, 4, 6))
+    out = oracle_mod.attention(q, k, v, True, 0.5)
+    assert np.array_equal(out[:6], np.zeros((6, 6)))
+    assert np.array_equal(out[6], v[0])
+    full = oracle_mod.attention(q, k, v, False, 0.5)
+    assert np.max(np.abs(out[-1] - full[-1])) < 1e-15
+
+
+def test_chunk_matches_an_explicit_library_mask(oracle_mod):
+    torch = pytest.importorskip("torch")
+    r = rng(22)
+    Nq, Nk, d = 23, 57, 16
+    q = r.normal(size=(1, 2, Nq, d))
+    k, v = r.normal(size=(2, 1, 2, Nk, d))
+    i = np.arange(Nq)[:, None]
+    j = np.arange(Nk)[None, :]
+    mask = torch.from_numpy(j <= i + (Nk - Nq))
+    want = torch.nn.functional.scaled_dot_product_attention(
+        torch.from_numpy(q), torch.from_numpy(k), torch.from_numpy(v), attn_mask=mask,
+        scale=0.2).numpy()
+    got = oracle_mod.attention(q, k, v, True, 0.2)
+    assert np.max(np.abs(got - want)) < 1e-12
+
+
+def test_grouped_heads_equal_repeated_kv_heads(oracle_mod):
+    r = rng(23)
+    B, Hq, Hkv, N, d = 2, 6, 2, 19, 8
+    q = r.normal(size=(B, Hq, N, d))
+    k, v = r.normal(size=(2, B, Hkv, N, d))
+    got = oracle_mod.attention(q, k, v, True, 0.4)
+    rep = oracle_mod.attention(q, np.repeat(k, 3, axis=1), np.repeat(v, 3, axis=1), True, 0.4)
+    assert np.array_equal(got, rep)
+    # consecutive query heads share a kv head (h // 3), not h % 2
+    alt = oracle_mod.attention(q, np.tile(k, (1, 3, 1, 1)), np.tile(v, (1, 3, 1, 1)), True, 0.4)
+    assert np.max(np.abs(got - alt)) > 1e-3
+
+
+def test_grouped_heads_match_library_gqa(oracle_mod):
+    torch = pytest.importorskip("torch")
+    r = rng(24)
+    B, Hq, Hkv, N, d = 1, 14, 2, 21, 16
+    q = r.normal(size=(B, Hq, N, d))
+    k, v = r.normal(size=(2, B, Hkv, N, d))
+    want = torch.nn.functional.scaled_dot_product_attention(
+        torch.from_numpy(q), torch.from_numpy(k), torch.from_numpy(v), is_causal=True,
+        scale=0.25, enable_gqa=True).numpy()
+    got = oracle_mod.attention(q, k, v, True, 0.25)
+    assert np.max(np.abs(got - want)) < 1e-12
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_packed_batch_equals_each_sequence_alone(oracle_mod, causal):
+    r = rng(25)
+    Hq, Hkv, d = 4, 2, 8
+    lens_q = [5, 17, 1, 0, 12]
+    lens_k = [5, 30, 9, 4, 12]
+    cu_q = np.concatenate([[0], np.cumsum(lens_q)])
+    cu_k = np.concatenate([[0], np.cumsum(lens_k)])
+    q = r.normal(size=(cu_q[-1], Hq, d))
+    k, v = r.normal(size=(2, cu_k[-1], Hkv, d))
+    got = oracle_mod.attention_varlen(q, k, v, cu_q, cu_k, causal, 0.35)
+    for b in range(len(lens_q)):
+        if lens_q[b] == 0:
+            continue
+        qs = q[cu_q[b]:cu_q[b + 1]].transpose(1, 0, 2)[None]
+        ks = k[cu_k[b]:cu_k[b + 1]].transpose(1, 0, 2)[None]
+        vs = v[cu_k[b]:cu_k[b + 1]].transpose(1, 0, 2)[None]
+        want = oracle_mod.attention(qs, ks, vs, causal, 0.35)[0].transpose(1, 0, 2)
+        assert np.array_equal(got[cu_q[b]:cu_q[b + 1]], want)
+    # keys of other sequences are never seen: changing them changes nothing
+    k2 = k.copy()
+    k2[cu_k[1]:cu_k[2]] *= 3.0   # (a shift would cancel in the softmax)
+    got2 = oracle_mod.attention_varlen(q, k2, v, cu_q, cu_k, causal, 0.35)
+    assert np.array_equal(got2[cu_q[0]:cu_q[1]], got[cu_q[0]:cu_q[1]])
+    assert np.array_equal(got2[cu_q[2]:], got[cu_q[2]:])
+    assert np.max(np.abs(got2[cu_q[1]:cu_q[2]] - got[cu_q[1]:cu_q[2]])) > 1e-3
