@@ -18,6 +18,7 @@ from . import build as _build
 
 FA_F16, FA_BF16, FA_F32 = 0, 1, 2
 FA_FLAG_NONE, FA_FLAG_NO_CAUSAL_SKIP = 0, 1
+FA_FLAG_SCHEDULE_UNITS, FA_FLAG_SCHEDULE_STREAM_K = 2, 4
 FA_OK = 0
 STATUS_NAMES = {
     0: "FA_OK", 1: "FA_ERR_NULL", 2: "FA_ERR_SHAPE", 3: "FA_ERR_HEAD_DIM",
@@ -33,6 +34,9 @@ _vp, _i, _f, _u, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_u
 _SIGNATURES = {
     "fa_prefill": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp]),
     "fa_prefill_ex": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _i, _u, _vp]),
+    "fa_prefill_gqa": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _f, _i, _i, _u, _vp]),
+    "fa_prefill_varlen": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _i,
+                               _f, _i, _i, _u, _vp]),
     "fa_decode": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _vp]),
     "fa_decode_ex": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _i, _i, _vp, _sz, _vp]),
     "fa_decode_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _i, _i, _vp]),
@@ -88,6 +92,20 @@ def fa_prefill_ex(q, k, v, out, B, H, N, d, causal, scale, in_dtype, out_dtype, 
                   stream=0) -> int:
     return load().fa_prefill_ex(q, k, v, out, B, H, N, d, int(causal), float(scale),
                                 in_dtype, out_dtype, flags, stream)
+
+
+def fa_prefill_gqa(q, k, v, out, B, Hq, Hkv, Nq, Nk, d, causal, scale, in_dtype, out_dtype,
+                   flags=0, stream=0) -> int:
+    return load().fa_prefill_gqa(q, k, v, out, B, Hq, Hkv, Nq, Nk, d, int(causal), float(scale),
+                                 in_dtype, out_dtype, flags, stream)
+
+
+def fa_prefill_varlen(q, k, v, out, cu_seqlens_q, cu_seqlens_k, B, Hq, Hkv, total_q, total_k,
+                      max_seqlen_q, max_seqlen_k, d, causal, scale, in_dtype, out_dtype, flags=0,
+                      stream=0) -> int:
+    return load().fa_prefill_varlen(q, k, v, out, cu_seqlens_q, cu_seqlens_k, B, Hq, Hkv, total_q,
+                                    total_k, max_seqlen_q, max_seqlen_k, d, int(causal),
+                                    float(scale), in_dtype, out_dtype, flags, stream)
 
 
 def fa_decode(q, k_cache, v_cache, seq_lens, out, B, H, max_len, d, scale, stream=0) -> int:
@@ -176,7 +194,9 @@ def _stream_handle(device) -> int:
 
 def prefill(q, k, v, causal: bool = False, scale: float | None = None, out_dtype=None,
             flags: int = 0, out=None):
-    """out = softmax(scale * q k^T [causal]) v for tensors [B, H, N, d] (fp16/bf16).
+    """out = softmax(scale * q k^T [causal]) v for q [B, Hq, Nq, d] and k, v
+    [B, Hkv, Nk, d] (fp16/bf16; Hq a multiple of Hkv; causal queries are the
+    last Nq positions).
 
     CUDA inputs run on the current stream and return a CUDA tensor.  Host
     inputs are copied to the current device first and the result is copied
@@ -191,10 +211,13 @@ def prefill(q, k, v, causal: bool = False, scale: float | None = None, out_dtype
         dst = torch.empty(res.shape, dtype=res.dtype, pin_memory=q.is_pinned())
         dst.copy_(res, non_blocking=False)
         return dst
-    B, H, N, d = q.shape
+    B, Hq, Nq, d = q.shape
     _check_cuda("q", q)
-    _check_cuda("k", k, q.shape, q.dtype)
-    _check_cuda("v", v, q.shape, q.dtype)
+    _check_cuda("k", k, None, q.dtype)
+    if k.dim() != 4 or k.shape[0] != B or k.shape[3] != d:
+        raise ValueError(f"k has shape {tuple(k.shape)}, expected [{B}, Hkv, Nk, {d}]")
+    Hkv, Nk = k.shape[1], k.shape[2]
+    _check_cuda("v", v, k.shape, q.dtype)
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     out_dtype = q.dtype if out_dtype is None else out_dtype
@@ -202,11 +225,44 @@ def prefill(q, k, v, causal: bool = False, scale: float | None = None, out_dtype
         out = torch.empty(q.shape, dtype=out_dtype, device=q.device)
     else:
         _check_cuda("out", out, q.shape, out_dtype)
-    rc = fa_prefill_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, H, N, d,
-                       causal, scale, dtype_code(q.dtype), dtype_code(out_dtype), flags,
-                       _stream_handle(q.device))
+    rc = fa_prefill_gqa(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, Hq, Hkv, Nq,
+                        Nk, d, causal, scale, dtype_code(q.dtype), dtype_code(out_dtype), flags,
+                        _stream_handle(q.device))
     if rc != FA_OK:
-        raise FaError(rc, "fa_prefill_ex")
+        raise FaError(rc, "fa_prefill_gqa")
+    return out
+
+
+def prefill_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, max_seqlen_k: int,
+                   causal: bool = False, scale: float | None = None, out_dtype=None,
+                   flags: int = 0, out=None):
+    """Packed variable-length prefill: q [total_q, Hq, d], k, v [total_k, Hkv, d],
+    cu_seqlens_* int32 [B + 1] on the same device.  Returns [total_q, Hq, d]."""
+    torch = _torch()
+    _check_cuda("q", q)
+    if q.dim() != 3 or k.dim() != 3:
+        raise ValueError("q and k must be [tokens, heads, d]")
+    total_q, Hq, d = q.shape
+    total_k, Hkv = k.shape[0], k.shape[1]
+    _check_cuda("k", k, (total_k, Hkv, d), q.dtype)
+    _check_cuda("v", v, k.shape, q.dtype)
+    B = cu_seqlens_q.shape[0] - 1
+    _check_cuda("cu_seqlens_q", cu_seqlens_q, (B + 1,), torch.int32)
+    _check_cuda("cu_seqlens_k", cu_seqlens_k, (B + 1,), torch.int32)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    out_dtype = q.dtype if out_dtype is None else out_dtype
+    if out is None:
+        out = torch.empty(q.shape, dtype=out_dtype, device=q.device)
+    else:
+        _check_cuda("out", out, q.shape, out_dtype)
+    rc = fa_prefill_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                           cu_seqlens_q.data_ptr(), cu_seqlens_k.data_ptr(), B, Hq, Hkv, total_q,
+                           total_k, int(max_seqlen_q), int(max_seqlen_k), d, causal, scale,
+                           dtype_code(q.dtype), dtype_code(out_dtype), flags,
+                           _stream_handle(q.device))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_prefill_varlen")
     return out
 
 

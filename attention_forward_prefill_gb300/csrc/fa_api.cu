@@ -22,6 +22,9 @@ std::mutex g_dev_mu;
 DeviceInfo g_dev_cache[kMaxDevices];
 bool g_dev_have[kMaxDevices] = {};
 
+cudaMemPool_t g_pool[kMaxDevices] = {};
+constexpr uint64_t kPoolKeepBytes = 256ull << 20;  // freed scratch kept mapped
+
 constexpr int kDecodeRowAlign = 64;      // chunk lengths are multiples of this
 constexpr int kDecodeAutoMaxChunk = 512;  // automatic choice: at most 512 rows per CTA
 constexpr int kDecodeMaxChunk = 48 * 1024; // any choice: scores of a chunk <= 192 KB smem
@@ -79,13 +82,43 @@ int current_device_info(DeviceInfo *out) {
     return FA_OK;
 }
 
+cudaError_t scratch_alloc(void **ptr, size_t bytes, cudaStream_t stream) {
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    cudaMemPool_t pool;
+    {
+        std::lock_guard<std::mutex> lk(g_dev_mu);
+        if (!g_pool[dev]) {
+            cudaMemPoolProps props = {};
+            props.allocType = cudaMemAllocationTypePinned;
+            props.location.type = cudaMemLocationTypeDevice;
+            props.location.id = dev;
+            cudaMemPool_t created;
+            if ((e = cudaMemPoolCreate(&created, &props)) != cudaSuccess) return e;
+            uint64_t keep = kPoolKeepBytes;
+            if ((e = cudaMemPoolSetAttribute(created, cudaMemPoolAttrReleaseThreshold, &keep)) !=
+                cudaSuccess) {
+                cudaMemPoolDestroy(created);
+                return e;
+            }
+            g_pool[dev] = created;
+        }
+        pool = g_pool[dev];
+    }
+    return cudaMallocFromPoolAsync(ptr, bytes, pool, stream);
+}
+
+cudaError_t scratch_free(void *ptr, cudaStream_t stream) { return cudaFreeAsync(ptr, stream); }
+
 }  // namespace fa
 
 using namespace fa;
 
 extern "C" {
 
-int fa_version(void) { return 1 * 10000 + 0 * 100 + 0; }
+int fa_version(void) { return 1 * 10000 + 1 * 100 + 0; }
 
 const char *fa_status_string(int status) {
     switch (status) {
@@ -115,40 +148,122 @@ int fa_device_status(int reset) {
     return a ? a : b;
 }
 
-int fa_prefill_ex(const void *q, const void *k, const void *v, void *out, int B, int H, int N,
-                  int d, int causal, float scale, fa_dtype in_dtype, fa_dtype out_dtype,
-                  unsigned flags, void *stream) {
+namespace {
+int prefill_common_checks(const void *q, const void *k, const void *v, void *out, int d,
+                          fa_dtype in_dtype, fa_dtype out_dtype, float scale) {
     if (!q || !k || !v || !out) return FA_ERR_NULL;
-    if (B < 1 || H < 1 || N < 1) return FA_ERR_SHAPE;
-    if (static_cast<long long>(B) * H * N > INT_MAX) return FA_ERR_SHAPE;
     if (d != 64 && d != 128) return FA_ERR_HEAD_DIM;
     if (in_dtype != FA_F16 && in_dtype != FA_BF16) return FA_ERR_DTYPE;
     if (out_dtype != FA_F16 && out_dtype != FA_BF16 && out_dtype != FA_F32) return FA_ERR_DTYPE;
     if (misaligned(q) || misaligned(k) || misaligned(v) || misaligned(out)) return FA_ERR_ALIGN;
     if (!std::isfinite(scale)) return FA_ERR_SCALE;
-    const size_t elems = static_cast<size_t>(B) * H * N * d;
-    const size_t in_bytes = elems * 2, out_bytes = elems * dtype_size(out_dtype);
-    if (overlaps(out, out_bytes, q, in_bytes) || overlaps(out, out_bytes, k, in_bytes) ||
-        overlaps(out, out_bytes, v, in_bytes))
+    return FA_OK;
+}
+
+int schedule_of(unsigned flags) {
+    if (flags & FA_FLAG_SCHEDULE_UNITS) return 1;
+    if (flags & FA_FLAG_SCHEDULE_STREAM_K) return 2;
+    return 0;
+}
+}  // namespace
+
+int fa_prefill_gqa(const void *q, const void *k, const void *v, void *out, int B, int Hq, int Hkv,
+                   int Nq, int Nk, int d, int causal, float scale, fa_dtype in_dtype,
+                   fa_dtype out_dtype, unsigned flags, void *stream) {
+    int rc = prefill_common_checks(q, k, v, out, d, in_dtype, out_dtype, scale);
+    if (rc != FA_OK) return rc;
+    if (B < 1 || Hq < 1 || Hkv < 1 || Nq < 1 || Nk < 1) return FA_ERR_SHAPE;
+    if (Hq % Hkv != 0) return FA_ERR_SHAPE;
+    if (static_cast<long long>(B) * Hq * Nq > INT_MAX || static_cast<long long>(B) * Hkv * Nk > INT_MAX)
+        return FA_ERR_SHAPE;
+    const size_t q_bytes = static_cast<size_t>(B) * Hq * Nq * d * 2;
+    const size_t kv_bytes = static_cast<size_t>(B) * Hkv * Nk * d * 2;
+    const size_t out_bytes = static_cast<size_t>(B) * Hq * Nq * d * dtype_size(out_dtype);
+    if (overlaps(out, out_bytes, q, q_bytes) || overlaps(out, out_bytes, k, kv_bytes) ||
+        overlaps(out, out_bytes, v, kv_bytes))
         return FA_ERR_ALIAS;
     DeviceInfo dev;
-    int rc = current_device_info(&dev);
+    rc = current_device_info(&dev);
     if (rc != FA_OK) return rc;
     PrefillLaunch a;
     a.q = q;
     a.k = k;
     a.v = v;
     a.out = out;
+    a.cu_q = nullptr;
+    a.cu_k = nullptr;
     a.B = B;
-    a.H = H;
-    a.N = N;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.Nq = Nq;
+    a.Nk = Nk;
+    a.total_q = 0;
+    a.total_k = 0;
     a.d = d;
     a.causal = causal ? 1 : 0;
     a.no_skip = (flags & FA_FLAG_NO_CAUSAL_SKIP) ? 1 : 0;
     a.scale = scale;
     a.in_bf16 = in_dtype == FA_BF16 ? 1 : 0;
     a.out_dtype = out_dtype;
+    a.schedule = schedule_of(flags);
     return launch_prefill(a, dev, static_cast<cudaStream_t>(stream));
+}
+
+int fa_prefill_varlen(const void *q, const void *k, const void *v, void *out,
+                      const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k, int B, int Hq,
+                      int Hkv, int total_q, int total_k, int max_seqlen_q, int max_seqlen_k, int d,
+                      int causal, float scale, fa_dtype in_dtype, fa_dtype out_dtype,
+                      unsigned flags, void *stream) {
+    int rc = prefill_common_checks(q, k, v, out, d, in_dtype, out_dtype, scale);
+    if (rc != FA_OK) return rc;
+    if (!cu_seqlens_q || !cu_seqlens_k) return FA_ERR_NULL;
+    if ((reinterpret_cast<uintptr_t>(cu_seqlens_q) & 3u) || (reinterpret_cast<uintptr_t>(cu_seqlens_k) & 3u))
+        return FA_ERR_ALIGN;
+    if (B < 1 || Hq < 1 || Hkv < 1 || total_q < 0 || total_k < 0 || max_seqlen_q < 0 ||
+        max_seqlen_k < 0)
+        return FA_ERR_SHAPE;
+    if (Hq % Hkv != 0) return FA_ERR_SHAPE;
+    if (static_cast<long long>(B) * Hq * ((static_cast<long long>(max_seqlen_q) + 255) / 256) > INT_MAX)
+        return FA_ERR_SHAPE;
+    if (total_q == 0 || max_seqlen_q == 0) return FA_OK;  // no query rows
+    const size_t q_bytes = static_cast<size_t>(total_q) * Hq * d * 2;
+    const size_t kv_bytes = static_cast<size_t>(total_k) * Hkv * d * 2;
+    const size_t out_bytes = static_cast<size_t>(total_q) * Hq * d * dtype_size(out_dtype);
+    if (overlaps(out, out_bytes, q, q_bytes) || overlaps(out, out_bytes, k, kv_bytes) ||
+        overlaps(out, out_bytes, v, kv_bytes))
+        return FA_ERR_ALIAS;
+    DeviceInfo dev;
+    rc = current_device_info(&dev);
+    if (rc != FA_OK) return rc;
+    PrefillLaunch a;
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.out = out;
+    a.cu_q = cu_seqlens_q;
+    a.cu_k = cu_seqlens_k;
+    a.B = B;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.Nq = max_seqlen_q;
+    a.Nk = max_seqlen_k;
+    a.total_q = total_q;
+    a.total_k = total_k;
+    a.d = d;
+    a.causal = causal ? 1 : 0;
+    a.no_skip = (flags & FA_FLAG_NO_CAUSAL_SKIP) ? 1 : 0;
+    a.scale = scale;
+    a.in_bf16 = in_dtype == FA_BF16 ? 1 : 0;
+    a.out_dtype = out_dtype;
+    a.schedule = 1;
+    return launch_prefill(a, dev, static_cast<cudaStream_t>(stream));
+}
+
+int fa_prefill_ex(const void *q, const void *k, const void *v, void *out, int B, int H, int N,
+                  int d, int causal, float scale, fa_dtype in_dtype, fa_dtype out_dtype,
+                  unsigned flags, void *stream) {
+    return fa_prefill_gqa(q, k, v, out, B, H, H, N, N, d, causal, scale, in_dtype, out_dtype, flags,
+                          stream);
 }
 
 int fa_prefill(const void *q, const void *k, const void *v, void *out, int B, int H, int N, int d,
@@ -234,7 +349,7 @@ int fa_decode_ex(const void *q, const void *k_cache, const void *v_cache, const 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     void *ws = workspace;
     if (!ws) {
-        cudaError_t e = cudaMallocAsync(&ws, need, st);
+        cudaError_t e = scratch_alloc(&ws, need, st);
         if (e != cudaSuccess) {
             cuda_fail(e);
             return FA_ERR_WORKSPACE;
@@ -260,7 +375,7 @@ int fa_decode_ex(const void *q, const void *k_cache, const void *v_cache, const 
                                               ws_ml_bytes(static_cast<long long>(bh), splits));
     rc = launch_decode(a, dev, st);
     if (!workspace) {
-        cudaError_t e = cudaFreeAsync(ws, st);
+        cudaError_t e = scratch_free(ws, st);
         if (rc == FA_OK && e != cudaSuccess) rc = cuda_fail(e);
     }
     return rc;

@@ -25,15 +25,26 @@ int current_device_info(DeviceInfo *out);
 // Record a CUDA error for fa_last_cuda_error() and return FA_ERR_CUDA.
 int cuda_fail(cudaError_t e);
 
+// Stream-ordered scratch memory from a pool the library owns on the current
+// device.  The pool keeps freed memory mapped (up to a threshold), so a call
+// made after a stream synchronisation does not pay to map its workspace again.
+cudaError_t scratch_alloc(void **ptr, size_t bytes, cudaStream_t stream);
+cudaError_t scratch_free(void *ptr, cudaStream_t stream);
+
 struct PrefillLaunch {
     const void *q, *k, *v;
     void *out;
-    int B, H, N, d;
+    const int32_t *cu_q, *cu_k;  // packed batch: [B+1] token offsets (device); null when dense
+    int B, Hq, Hkv;
+    int Nq, Nk;                  // dense: lengths; packed: max_seqlen_q / max_seqlen_k
+    int total_q, total_k;        // packed: token counts
+    int d;
     int causal;
     int no_skip;
     float scale;
     int in_bf16;    // 1: bf16 inputs, 0: fp16
     int out_dtype;  // fa_dtype
+    int schedule;   // 0: choose, 1: unit by unit, 2: stream-K where possible
 };
 
 // Validated arguments -> encode tensor maps, launch the persistent kernel.

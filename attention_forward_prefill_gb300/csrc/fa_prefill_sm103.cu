@@ -26,6 +26,7 @@
 // Rescaling is lazy: m_ref only moves when the tile maximum exceeds it by more
 // than TAU (log2 units), so p <= 2^TAU; O and l share m_ref, so the final O/l
 // is unchanged.
+#include <algorithm>
 #include <cfloat>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -71,32 +72,49 @@ struct Layout {
     static constexpr uint32_t kOCol0 = 256, kOCol1 = 256 + D;
 };
 
+constexpr int kMaxPre = 1024;  // stream-K: query blocks per head with a step table
+
 struct Params {
     void *out;
-    int N;
-    int BH;
-    int n_qb;      // 256-row query blocks per head
-    int n_units;   // BH * n_qb
-    int causal;
+    // A packed batch (variable lengths) keeps tokens [cu_q[b], cu_q[b+1]) of
+    // sequence b in a [tokens][H][d] tensor; a dense batch is [B][H][N][d].
+    const int *cu_q;       // packed: [B+1] query-token offsets (device); null when dense
+    const int *cu_k;       // packed: [B+1] key-token offsets
+    int B, Hq, Hkv, group; // query head h reads key/value head h / group
+    int Nq, Nk;            // dense: every sequence's lengths; packed: the maxima
+    int total_q, total_k;  // packed: tokens in q and in k/v
+    int BH;                // B * Hq
+    int n_qb;              // 256-row query blocks per (sequence, query head)
+    int n_units;           // BH * n_qb
+    int causal;            // bottom-right aligned: query i sees keys j <= i + Nk - Nq
     int no_skip;
     int in_bf16;
     int out_dtype;
     int scale_neg;
     float scale_log2;      // c = scale * log2(e)
     float scale_log2_abs;  // |c|
-    // Stream-K (non-causal only): the W = n_units * T (unit, key tile) steps
-    // are cut into gridDim.x equal contiguous ranges; a unit cut between two
-    // CTAs is finished by the fixup kernel from the partials in ws_o / ws_ml.
+    // Stream-K (dense batches): the W = BH * HT (unit, key tile) steps are cut
+    // into gridDim.x equal contiguous ranges; a unit cut between two CTAs is
+    // finished by the fixup kernel from the partials in ws_o / ws_ml.
     int stream_k;
-    int T;                 // key tiles per unit
-    long long W;           // n_units * T
+    int HT;                // key-tile steps per (sequence, head) = pre[n_qb]
+    long long W;           // BH * HT
     float *ws_o;           // [gridDim.x][2 slots][256 rows][D]  unnormalised O
     float *ws_ml;          // [gridDim.x][2 slots][256 rows][2]  (m_ref, l)
+    int pre[kMaxPre + 1];  // steps of a head before query block qb
 };
 
-// The CTA's next piece of work: unit u, key tiles [j0, j1), and the key-tile
-// counts n0, n1 of its two query tiles (0 = no rows).  Every role of a CTA
-// walks the same sequence.
+// One piece of work: unit u = (sequence b, query head h, query block) and its
+// key tiles [j0, j1).  n0 / n1: key tiles the two 128-row query tiles need
+// (0 = none: no rows, or rows that see no key).
+struct Work {
+    int u, b, h, hk;
+    int q0;                // first query row of the unit, within the sequence
+    int nq, nk, off;       // the sequence's lengths; off = nk - nq (causal alignment)
+    long long qt0, kt0;    // packed: first query / key token of the sequence
+    int j0, j1, n0, n1;
+};
+
 struct SegCursor {
     long long s, s_end;  // stream-K step range
     int u;               // unit-granular schedule
@@ -108,47 +126,76 @@ __device__ __forceinline__ void seg_begin(const Params &p, SegCursor &c) {
     c.u = blockIdx.x;
 }
 
-__device__ __forceinline__ void unit_coords(const Params &p, int u, int &bh, int &qb) {
-    if (p.causal) {  // heaviest query blocks first
-        qb = p.n_qb - 1 - u / p.BH;
-        bh = u % p.BH;
-    } else {         // neighbouring CTAs share a head's K/V in L2
-        bh = u / p.n_qb;
-        qb = u % p.n_qb;
+// Key tiles a 128-row query tile starting at row0 must visit.
+__device__ __forceinline__ int kv_tiles(int causal, int no_skip, int nq, int nk, int off, int row0) {
+    if (row0 >= nq) return 0;
+    const int tk = (nk + kBlockN - 1) / kBlockN;
+    if (!causal || no_skip) return tk;
+    const int last = min(row0 + kBlockM - 1, nq - 1) + off;
+    if (last < 0) return 0;
+    return min(tk, last / kBlockN + 1);
+}
+
+// Fill sequence fields of w from (b, h).
+__device__ __forceinline__ void load_seq(const Params &p, Work &w) {
+    w.hk = w.h / p.group;
+    if (p.cu_q) {
+        const int q_lo = min(max(__ldg(p.cu_q + w.b), 0), p.total_q);
+        const int q_hi = min(max(__ldg(p.cu_q + w.b + 1), q_lo), p.total_q);
+        const int k_lo = min(max(__ldg(p.cu_k + w.b), 0), p.total_k);
+        const int k_hi = min(max(__ldg(p.cu_k + w.b + 1), k_lo), p.total_k);
+        w.qt0 = q_lo;
+        w.kt0 = k_lo;
+        w.nq = min(q_hi - q_lo, p.Nq);
+        w.nk = min(k_hi - k_lo, p.Nk);
+    } else {
+        w.qt0 = 0;
+        w.kt0 = 0;
+        w.nq = p.Nq;
+        w.nk = p.Nk;
     }
+    w.off = w.nk - w.nq;
 }
 
-// Key tiles a 128-row query tile starting at row0 must visit (0 = no rows).
-__device__ __forceinline__ int kv_tiles(const Params &p, int row0) {
-    if (row0 >= p.N) return 0;
-    const int nk = (p.N + kBlockN - 1) / kBlockN;
-    if (!p.causal || p.no_skip) return nk;
-    const int last = min(row0 + kBlockM - 1, p.N - 1);
-    return last / kBlockN + 1;
-}
-
-__device__ __forceinline__ bool seg_next(const Params &p, SegCursor &c, int &u, int &bh, int &q0,
-                                         int &j0, int &j1, int &n0, int &n1) {
-    int qb;
+__device__ __forceinline__ bool seg_next(const Params &p, SegCursor &c, Work &w) {
+    int bh, qb;
     if (p.stream_k) {
         if (c.s >= c.s_end) return false;
-        u = static_cast<int>(c.s / p.T);
-        j0 = static_cast<int>(c.s % p.T);
+        bh = static_cast<int>(c.s / p.HT);
+        const int rem = static_cast<int>(c.s - static_cast<long long>(bh) * p.HT);
+        int lo = 0, hi = p.n_qb - 1;  // last qb with pre[qb] <= rem
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (p.pre[mid] <= rem) lo = mid; else hi = mid - 1;
+        }
+        qb = lo;
+        w.j0 = rem - p.pre[qb];
+        const int cost = p.pre[qb + 1] - p.pre[qb];
         const long long left = c.s_end - c.s;
-        j1 = static_cast<int>(left < p.T - j0 ? j0 + left : p.T);
-        c.s += j1 - j0;
+        w.j1 = static_cast<int>(left < cost - w.j0 ? w.j0 + left : cost);
+        c.s += w.j1 - w.j0;
+        w.u = bh * p.n_qb + qb;
     } else {
         if (c.u >= p.n_units) return false;
-        u = c.u;
+        w.u = c.u;
         c.u += gridDim.x;
-        j0 = 0;
-        j1 = -1;
+        if (p.causal) {  // heaviest query blocks first
+            qb = p.n_qb - 1 - w.u / p.BH;
+            bh = w.u % p.BH;
+        } else {         // neighbouring CTAs share a head's K/V in L2
+            bh = w.u / p.n_qb;
+            qb = w.u % p.n_qb;
+        }
+        w.j0 = 0;
+        w.j1 = -1;
     }
-    unit_coords(p, u, bh, qb);
-    q0 = qb * kRowsPerUnit;
-    n0 = kv_tiles(p, q0);
-    n1 = kv_tiles(p, q0 + kBlockM);
-    if (j1 < 0) j1 = max(n0, n1);
+    w.b = bh / p.Hq;
+    w.h = bh % p.Hq;
+    load_seq(p, w);
+    w.q0 = qb * kRowsPerUnit;
+    w.n0 = kv_tiles(p.causal, p.no_skip, w.nq, w.nk, w.off, w.q0);
+    w.n1 = kv_tiles(p.causal, p.no_skip, w.nq, w.nk, w.off, w.q0 + kBlockM);
+    if (w.j1 < 0) w.j1 = max(w.n0, w.n1);
     return true;
 }
 
@@ -273,7 +320,7 @@ template <int D, bool BF16>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap map_q,
                    const __grid_constant__ CUtensorMap map_k,
-                   const __grid_constant__ CUtensorMap map_v, const Params p) {
+                   const __grid_constant__ CUtensorMap map_v, const __grid_constant__ Params p) {
     using L = Layout<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -335,19 +382,31 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = true;
             SegCursor cur;
             seg_begin(p, cur);
-            int u, bh, q0, j0, j1, n0, n1;
-            while (ok && seg_next(p, cur, u, bh, q0, j0, j1, n0, n1)) {
+            Work w;
+            const bool packed = p.cu_q != nullptr;
+            while (ok && seg_next(p, cur, w)) {
+                if (w.j1 <= w.j0) continue;  // no key tiles: the softmax warps write zeros
+                // query tile t is loaded when it has key tiles in [j0, j1)
+                const bool need0 = min(w.n0, w.j1) > w.j0, need1 = min(w.n1, w.j1) > w.j0;
                 if (qc > 0 && !mbar_wait(q_empty, (qc - 1) & 1, abort_flag, kWatchdogNs)) {
                     ok = false;
                     break;
                 }
-                mbar_arrive_expect_tx(q_full, (n1 > 0 ? 2 : 1) * L::kTileBytes);
-                for (int t = 0; t < (n1 > 0 ? 2 : 1); ++t)
-                    for (int c = 0; c < L::kChunks; ++c)
-                        tma_load_3d(q_smem + t * L::kTileBytes + c * L::kChunkBytes, &map_q, q_full,
-                                    c * 64, q0 + t * kBlockM, bh, pol_q);
+                mbar_arrive_expect_tx(q_full, ((need0 ? 1 : 0) + (need1 ? 1 : 0)) * L::kTileBytes);
+                for (int t = 0; t < 2; ++t) {
+                    if (!(t ? need1 : need0)) continue;
+                    const int row = w.q0 + t * kBlockM;
+                    for (int c = 0; c < L::kChunks; ++c) {
+                        if (packed)
+                            tma_load_3d(q_smem + t * L::kTileBytes + c * L::kChunkBytes, &map_q, q_full,
+                                        c * 64, w.h, static_cast<int>(w.qt0 + row), pol_q);
+                        else
+                            tma_load_3d(q_smem + t * L::kTileBytes + c * L::kChunkBytes, &map_q, q_full,
+                                        c * 64, row, w.b * p.Hq + w.h, pol_q);
+                    }
+                }
                 ++qc;
-                for (int j = j0; j < j1 && ok; ++j) {
+                for (int j = w.j0; j < w.j1 && ok; ++j) {
                     for (int kv = 0; kv < 2; ++kv) {
                         const uint32_t slot = rc % L::kStages;
                         if (rc >= (uint32_t)L::kStages &&
@@ -357,10 +416,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                             break;
                         }
                         mbar_arrive_expect_tx(kv_full + slot, L::kTileBytes);
-                        for (int c = 0; c < L::kChunks; ++c)
-                            tma_load_3d(ring + slot * L::kTileBytes + c * L::kChunkBytes,
-                                        kv ? &map_v : &map_k, kv_full + slot, c * 64, j * kBlockN,
-                                        bh, pol_kv);
+                        const CUtensorMap *m = kv ? &map_v : &map_k;
+                        for (int c = 0; c < L::kChunks; ++c) {
+                            if (packed)
+                                tma_load_3d(ring + slot * L::kTileBytes + c * L::kChunkBytes, m,
+                                            kv_full + slot, c * 64, w.hk,
+                                            static_cast<int>(w.kt0 + j * kBlockN), pol_kv);
+                            else
+                                tma_load_3d(ring + slot * L::kTileBytes + c * L::kChunkBytes, m,
+                                            kv_full + slot, c * 64, j * kBlockN, w.b * p.Hkv + w.hk,
+                                            pol_kv);
+                        }
                         ++rc;
                     }
                 }
@@ -391,10 +457,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = true;
             SegCursor cur;
             seg_begin(p, cur);
-            int u, bh, q0, j0, j1, nk0, nk1;
-            while (ok && seg_next(p, cur, u, bh, q0, j0, j1, nk0, nk1)) {
+            Work w;
+            while (ok && seg_next(p, cur, w)) {
+                const int j0 = w.j0, j1 = w.j1;
+                if (j1 <= j0) continue;  // no key tiles: nothing to multiply
                 // key tiles [j0, e_t) for query tile t (empty when e_t <= j0)
-                const int n0 = min(nk0, j1), n1 = min(nk1, j1);
+                const int n0 = min(w.n0, j1), n1 = min(w.n1, j1);
                 if (!mbar_wait(q_full, qc & 1, abort_flag, kWatchdogNs)) { ok = false; break; }
                 ++qc;
                 tc_fence_after();
@@ -482,17 +550,37 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t s_addr = tmem + lane_off + (t ? L::kSCol1 : L::kSCol0);
         const uint32_t o_addr = tmem + lane_off + (t ? L::kOCol1 : L::kOCol0);
         const float cexp = p.scale_log2;
+        const int osize = p.out_dtype == FA_F32 ? 4 : 2;
         uint32_t sc = 0, oc = 0;
         bool ok = true;
         SegCursor cur;
         seg_begin(p, cur);
-        int u, bh, q0, j0, j1, nk0, nk1;
-        for (int seg = 0; ok && seg_next(p, cur, u, bh, q0, j0, j1, nk0, nk1); ++seg) {
-            const int ntile = min(t ? nk1 : nk0, j1);  // this tile's key tiles: [j0, ntile)
-            if (ntile <= j0) continue;
-            const int tile_row0 = q0 + t * kBlockM;
-            const int row = tile_row0 + r;
-            const int lim = p.causal ? min(row, p.N - 1) : p.N - 1;  // last visible key
+        Work w;
+        for (int seg = 0; ok && seg_next(p, cur, w); ++seg) {
+            const int j0 = w.j0, j1 = w.j1;
+            const int tile_row0 = w.q0 + t * kBlockM;
+            const int row = tile_row0 + r;  // query index within the sequence
+            // Output row: dense [B][Hq][Nq][d], packed [tokens][Hq][d].
+            uint8_t *const orow = reinterpret_cast<uint8_t *>(p.out) +
+                                  (p.cu_q ? ((w.qt0 + row) * p.Hq + w.h) * D
+                                          : ((static_cast<long long>(w.b) * p.Hq + w.h) * p.Nq + row) * D) *
+                                      osize;
+            const bool row_ok = row < w.nq;
+            // A stream-K piece of a unit keeps its partial state for the fixup.
+            const bool partial = p.stream_k && !(j0 == 0 && j1 == max(w.n0, w.n1));
+            const int ntile = min(t ? w.n1 : w.n0, j1);  // this tile's key tiles: [j0, ntile)
+            if (ntile <= j0) {
+                // Rows that see no key at all are zero rows.  (A stream-K piece
+                // that only lacks this tile's keys leaves it to the other pieces.)
+                if (!p.stream_k && row_ok) {
+                    const uint32_t zero[32] = {};
+#pragma unroll
+                    for (int q = 0; q < D / 32; ++q) store_out32(orow + q * 32 * osize, zero, 0.f, p.out_dtype);
+                }
+                continue;
+            }
+            // last visible key of this row (< 0: none)
+            const int lim = p.causal ? min(row + w.off, w.nk - 1) : w.nk - 1;
             float m_ref = -INFINITY;
             float l = 0.f;
             for (int j = j0; j < ntile; ++j) {
@@ -525,8 +613,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     l *= alpha;
                     m_ref = m_tile;
                 }
+                // A row with nothing visible yet keeps m_ref = -inf: its masked
+                // scores still map to exactly 0 with a zero offset.
+                const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
                 const uint64_t c2 = f2_pack(cexp, cexp);
-                const uint64_t nm2 = f2_pack(-m_ref, -m_ref);
+                const uint64_t nm2 = f2_pack(-m_use, -m_use);
                 uint64_t sum2[4] = {0, 0, 0, 0};
                 // P in 32-key quarters: 16 packed registers per TMEM store.
 #pragma unroll
@@ -547,7 +638,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint64_t s01 = fadd2(sum2[0], sum2[1]), s23 = fadd2(sum2[2], sum2[3]);
                 const uint64_t st = fadd2(s01, s23);
                 l += f2_lo(st) + f2_hi(st);
-                if (j > 0 && __any_sync(0xffffffffu, need)) {
+                if (j > j0 && __any_sync(0xffffffffu, need)) {
                     // O rows are complete up to tile j-1: the commit that
                     // signalled S_t(j) also covers the earlier PV product.
                     // Done after P is written so the score registers are free.
@@ -575,7 +666,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!warp_wait(o_done + t, oc & 1, abort_flag)) { ok = false; break; }
             ++oc;
             tc_fence_after();
-            if (p.stream_k && !(j0 == 0 && j1 == p.T)) {
+            if (partial) {
                 // Part of a unit: keep O unnormalised with its (m_ref, l) for the
                 // fixup kernel.  Slot 0 = the CTA's first piece, 1 = its last.
                 const size_t rec = (static_cast<size_t>(blockIdx.x) * 2 + (seg == 0 ? 0 : 1)) * kRowsPerUnit +
@@ -597,17 +688,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_before();
                 continue;
             }
-            const float inv = 1.0f / l;
-            const int osize = p.out_dtype == FA_F32 ? 4 : 2;
-            uint8_t *orow = reinterpret_cast<uint8_t *>(p.out) +
-                            ((static_cast<size_t>(bh) * p.N + row) * D) * osize;
+            const float inv = l > 0.f ? 1.0f / l : 0.f;  // l = 0: no visible key
 #pragma unroll
             for (int q = 0; q < D / 32; ++q) {
                 uint32_t o[32];
                 tmem_ld32(o_addr + q * 32, o);
                 tmem_ld_wait();
                 reg_fence32(o);
-                if (row < p.N) store_out32(orow + q * 32 * osize, o, inv, p.out_dtype);
+                if (row_ok) store_out32(orow + q * 32 * osize, o, inv, p.out_dtype);
             }
             tc_fence_before();
         }
@@ -627,20 +715,23 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ---------------------------------------------------------------- stream-K fixup
 // Units cut between CTAs: merge the partial (O, m_ref, l) of every piece in CTA
 // order, O = sum_k 2^(m_k - M) O_k / sum_k 2^(m_k - M) l_k, and write the rows.
+// A piece holds a partial for a query tile only if its key range starts before
+// the tile's last key tile (a causal unit's first tile ends one key tile early).
 constexpr int kMaxSplit = 192;
 
 struct FixupParams {
     void *out;
     const float *ws_o;
     const float *ws_ml;
-    int N;
+    int Hq, Nq, Nk;
     int n_qb;
-    int T;
+    int causal, no_skip;
     int G;
     long long W;
     int out_dtype;
     int n_split;
-    int4 item[kMaxSplit];  // (unit, first CTA, last CTA, unused)
+    int4 item[kMaxSplit];            // (unit, first CTA, last CTA, unit's key-tile steps)
+    long long ustart[kMaxSplit];     // first step of the unit
 };
 
 template <int D>
@@ -655,25 +746,39 @@ __global__ void __launch_bounds__(256) prefill_fixup(const __grid_constant__ Fix
     const int rrow = blockIdx.y * 8 + warp;  // row within the 256-row unit
     const int bh = u / f.n_qb, qb = u % f.n_qb;
     const int row = qb * kRowsPerUnit + rrow;
-    if (row >= f.N) return;
-    const long long ustart = static_cast<long long>(u) * f.T;
-    auto rec_of = [&](int c) {
-        const long long first = static_cast<long long>(c) * f.W / f.G;
+    if (row >= f.Nq) return;
+    const int tile_row0 = qb * kRowsPerUnit + (rrow / kBlockM) * kBlockM;
+    const int n_t = kv_tiles(f.causal, f.no_skip, f.Nq, f.Nk, f.Nk - f.Nq, tile_row0);
+    const long long ustart = f.ustart[blockIdx.x];
+    auto first_of = [&](int c) { return static_cast<long long>(c) * f.W / f.G; };
+    // piece of CTA c: (record, first key tile of the piece within the unit)
+    auto piece = [&](int c, int &j_first) {
+        const long long first = first_of(c);
+        j_first = first > ustart ? static_cast<int>(first - ustart) : 0;
         return (static_cast<size_t>(c) * 2 + (first >= ustart ? 0 : 1)) * kRowsPerUnit + rrow;
     };
     float M = -INFINITY;
-    for (int c = it.y; c <= it.z; ++c) M = fmaxf(M, f.ws_ml[rec_of(c) * 2]);
+    // CTAs with an empty step range (more CTAs than steps) hold no piece.
+    auto empty = [&](int c) { return first_of(c + 1) <= first_of(c); };
+    for (int c = it.y; c <= it.z; ++c) {
+        int jf;
+        const size_t rec = piece(c, jf);
+        if (!empty(c) && jf < n_t) M = fmaxf(M, f.ws_ml[rec * 2]);
+    }
     float L = 0.f, o[EPL];
 #pragma unroll
     for (int e = 0; e < EPL; ++e) o[e] = 0.f;
     for (int c = it.y; c <= it.z; ++c) {
-        const size_t rec = rec_of(c);
-        const float w = ex2_approx(f.ws_ml[rec * 2] - M);
+        int jf;
+        const size_t rec = piece(c, jf);
+        if (empty(c) || jf >= n_t) continue;  // no keys of this row in the piece
+        const float m = f.ws_ml[rec * 2];
+        if (m == -INFINITY) continue;
+        const float w = ex2_approx(m - M);
         L = fmaf(w, f.ws_ml[rec * 2 + 1], L);
         const float *src = f.ws_o + rec * D + lane * EPL;
 #pragma unroll
         for (int e = 0; e < EPL; e += 2) {
-            float2 x;
             if constexpr (EPL % 4 == 0) {
                 if (e % 4 == 0) {
                     const float4 y = *reinterpret_cast<const float4 *>(src + e);
@@ -684,13 +789,13 @@ __global__ void __launch_bounds__(256) prefill_fixup(const __grid_constant__ Fix
                 }
                 continue;
             }
-            x = *reinterpret_cast<const float2 *>(src + e);
+            const float2 x = *reinterpret_cast<const float2 *>(src + e);
             o[e] = fmaf(w, x.x, o[e]);
             o[e + 1] = fmaf(w, x.y, o[e + 1]);
         }
     }
-    const float inv = 1.0f / L;
-    const size_t off = (static_cast<size_t>(bh) * f.N + row) * D + lane * EPL;
+    const float inv = L > 0.f ? 1.0f / L : 0.f;
+    const size_t off = (static_cast<size_t>(bh) * f.Nq + row) * D + lane * EPL;
     if (f.out_dtype == FA_F32) {
         float *dst = reinterpret_cast<float *>(f.out) + off;
 #pragma unroll
@@ -725,14 +830,27 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// [BH][N][d] 16-bit tensor viewed as 3-D (d, N, BH); 64 x 128 x 1 boxes,
-// 128-byte swizzle.  Rows past N read as zero, per head.
-int make_map(CUtensorMap *map, const void *base, int d, int N, int BH, int bf16) {
+// A dense [BH][N][d] tensor is viewed as (d, N, BH) with 64 x 128 x 1 boxes; a
+// packed [tokens][H][d] tensor as (d, H, tokens) with 64 x 1 x 128 boxes.  Both
+// land in shared memory as 128 rows of 128 bytes, 128-byte swizzled.  Rows past
+// the end of the tensor read as zero.
+int make_map(CUtensorMap *map, const void *base, int d, bool packed, long long rows, long long outer,
+             int bf16) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return cuda_fail(cudaErrorNotSupported);
-    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
-    cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)d * 2 * (cuuint64_t)N};
-    cuuint32_t box[3] = {64, 128, 1};
+    cuuint64_t dims[3], strides[2];
+    cuuint32_t box[3];
+    if (packed) {  // rows = tokens, outer = heads
+        dims[0] = d; dims[1] = (cuuint64_t)outer; dims[2] = (cuuint64_t)(rows > 0 ? rows : 1);
+        strides[0] = (cuuint64_t)d * 2;
+        strides[1] = (cuuint64_t)d * 2 * (cuuint64_t)outer;
+        box[0] = 64; box[1] = 1; box[2] = 128;
+    } else {       // rows = sequence length, outer = batch x heads
+        dims[0] = d; dims[1] = (cuuint64_t)rows; dims[2] = (cuuint64_t)outer;
+        strides[0] = (cuuint64_t)d * 2;
+        strides[1] = (cuuint64_t)d * 2 * (cuuint64_t)rows;
+        box[0] = 64; box[1] = 128; box[2] = 1;
+    }
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = enc(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
                      const_cast<void *>(base), dims, strides, box, estr,
@@ -742,16 +860,38 @@ int make_map(CUtensorMap *map, const void *base, int d, int N, int BH, int bf16)
     return FA_OK;
 }
 
+int host_kv_tiles(int causal, int no_skip, int nq, int nk, int row0) {
+    if (row0 >= nq) return 0;
+    const int tk = (nk + kBlockN - 1) / kBlockN;
+    if (!causal || no_skip) return tk;
+    const int last = std::min(row0 + kBlockM - 1, nq - 1) + (nk - nq);
+    if (last < 0) return 0;
+    return std::min(tk, last / kBlockN + 1);
+}
+
+// Stream-K costs, in key-tile steps, fitted to measured launch times on GB300
+// (d = 64 and 128, dense and causal): cutting units between CTAs costs about
+// 20 steps (partial writes, extra pipeline fills, the fixup pass), and a causal
+// stream-K step runs about 8% slower than a step of the unit schedule.
+constexpr long long kMergeCostSteps = 20;
+constexpr long long kCausalStepPct = 108;
+
 template <int D, bool BF16>
 int launch_d(const PrefillLaunch &a, const DeviceInfo &dev, cudaStream_t stream) {
     using L = Layout<D>;
     static_assert(L::kSmemBytes <= 227 * 1024, "shared memory budget");
+    const bool packed = a.cu_q != nullptr;
     CUtensorMap mq, mk, mv;
-    const int BH = a.B * a.H;
     int rc;
-    if ((rc = make_map(&mq, a.q, D, a.N, BH, a.in_bf16)) != FA_OK) return rc;
-    if ((rc = make_map(&mk, a.k, D, a.N, BH, a.in_bf16)) != FA_OK) return rc;
-    if ((rc = make_map(&mv, a.v, D, a.N, BH, a.in_bf16)) != FA_OK) return rc;
+    if (packed) {
+        if ((rc = make_map(&mq, a.q, D, true, a.total_q, a.Hq, a.in_bf16)) != FA_OK) return rc;
+        if ((rc = make_map(&mk, a.k, D, true, a.total_k, a.Hkv, a.in_bf16)) != FA_OK) return rc;
+        if ((rc = make_map(&mv, a.v, D, true, a.total_k, a.Hkv, a.in_bf16)) != FA_OK) return rc;
+    } else {
+        if ((rc = make_map(&mq, a.q, D, false, a.Nq, (long long)a.B * a.Hq, a.in_bf16)) != FA_OK) return rc;
+        if ((rc = make_map(&mk, a.k, D, false, a.Nk, (long long)a.B * a.Hkv, a.in_bf16)) != FA_OK) return rc;
+        if ((rc = make_map(&mv, a.v, D, false, a.Nk, (long long)a.B * a.Hkv, a.in_bf16)) != FA_OK) return rc;
+    }
     cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D, BF16>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
     if (e != cudaSuccess) return cuda_fail(e);
@@ -762,12 +902,21 @@ int launch_d(const PrefillLaunch &a, const DeviceInfo &dev, cudaStream_t stream)
     if (e != cudaSuccess) return cuda_fail(e);
     if (fattr.numRegs < kMinLaunchRegs) return cuda_fail(cudaErrorInvalidConfiguration);
 
-    Params p;
+    static thread_local Params p;  // ~4 KB: keep it off the stack
     p.out = a.out;
-    p.N = a.N;
-    p.BH = BH;
-    p.n_qb = (a.N + kRowsPerUnit - 1) / kRowsPerUnit;
-    p.n_units = BH * p.n_qb;
+    p.cu_q = a.cu_q;
+    p.cu_k = a.cu_k;
+    p.B = a.B;
+    p.Hq = a.Hq;
+    p.Hkv = a.Hkv;
+    p.group = a.Hq / a.Hkv;
+    p.Nq = a.Nq;
+    p.Nk = a.Nk;
+    p.total_q = a.total_q;
+    p.total_k = a.total_k;
+    p.BH = a.B * a.Hq;
+    p.n_qb = (a.Nq + kRowsPerUnit - 1) / kRowsPerUnit;
+    p.n_units = p.BH * p.n_qb;
     p.causal = a.causal ? 1 : 0;
     p.no_skip = a.no_skip ? 1 : 0;
     p.in_bf16 = a.in_bf16;
@@ -778,54 +927,98 @@ int launch_d(const PrefillLaunch &a, const DeviceInfo &dev, cudaStream_t stream)
     p.scale_neg = scale < 0.f ? 1 : 0;
     p.scale_log2 = scale * 1.4426950408889634f;
     p.scale_log2_abs = fabsf(p.scale_log2);
-    p.T = (a.N + kBlockN - 1) / kBlockN;
-    p.W = static_cast<long long>(p.n_units) * p.T;
+    p.stream_k = 0;
+    p.HT = 0;
+    p.W = 0;
     p.ws_o = nullptr;
     p.ws_ml = nullptr;
-    // Non-causal units all cost T key-tile steps.  Unit by unit, the busiest
-    // CTA does ceil(U / G) * T steps; cut into equal ranges (stream-K) it does
-    // ceil(W / G) plus the cost of merging the cut units (a fixup pass over
-    // their partials and shorter pieces), measured at about 24 steps.  Take
-    // the cheaper of the two.
+
+    // ---- schedule.  Unit by unit (static round robin, heaviest causal blocks
+    // first) the busiest CTA does `busiest` key-tile steps; cut into equal
+    // step ranges (stream-K) it does W / G (8% dearer when causal) plus the
+    // merge cost.  Take the cheaper, unless a flag forces one.  Stream-K needs every unit's cost on the
+    // host (dense batches) and every query row to see a key.
     const int sms = dev.num_sms < kMaxSplit ? dev.num_sms : kMaxSplit;
-    constexpr long long kMergeCostSteps = 24;
-    const long long unit_steps = static_cast<long long>((p.n_units + sms - 1) / sms) * p.T;
-    const long long sk_steps = (p.W + sms - 1) / sms + kMergeCostSteps;
-    p.stream_k = (!p.causal && p.n_units > sms && sk_steps < unit_steps) ? 1 : 0;
+    const bool sk_ok = !packed && p.n_qb <= kMaxPre && p.n_units >= 2 &&
+                       (!p.causal || p.no_skip || a.Nk >= a.Nq) && a.schedule != 1;
+    if (sk_ok) {
+        p.pre[0] = 0;
+        for (int qb = 0; qb < p.n_qb; ++qb) {
+            const int c0 = host_kv_tiles(p.causal, p.no_skip, a.Nq, a.Nk, qb * kRowsPerUnit);
+            const int c1 = host_kv_tiles(p.causal, p.no_skip, a.Nq, a.Nk, qb * kRowsPerUnit + kBlockM);
+            p.pre[qb + 1] = p.pre[qb] + std::max(c0, c1);
+        }
+        p.HT = p.pre[p.n_qb];
+        p.W = static_cast<long long>(p.BH) * p.HT;
+        bool take = a.schedule == 2;
+        if (!take && p.n_units <= 65536) {
+            const int gu = std::min(std::min(p.n_units, dev.num_sms), 1024);
+            long long busiest = 0;
+            if (p.causal) {
+                static thread_local long long load[1024];
+                for (int c = 0; c < gu; ++c) load[c] = 0;
+                for (int u = 0; u < p.n_units; ++u) {
+                    const int qb = p.n_qb - 1 - u / p.BH;
+                    load[u % gu] += p.pre[qb + 1] - p.pre[qb];
+                }
+                for (int c = 0; c < gu; ++c) busiest = std::max(busiest, load[c]);
+            } else {
+                busiest = static_cast<long long>((p.n_units + gu - 1) / gu) * p.pre[1];
+            }
+            const long long pct = p.causal ? kCausalStepPct : 100;
+            take = (p.W * pct + 100LL * sms - 1) / (100LL * sms) + kMergeCostSteps < busiest;
+        }
+        p.stream_k = take ? 1 : 0;
+    }
     int grid = p.n_units < dev.num_sms ? p.n_units : dev.num_sms;
-    FixupParams f;
+    static thread_local FixupParams f;
     f.n_split = 0;
     void *ws = nullptr;
     if (p.stream_k) {
         grid = sms;
         f.out = a.out;
-        f.N = a.N;
+        f.Hq = a.Hq;
+        f.Nq = a.Nq;
+        f.Nk = a.Nk;
         f.n_qb = p.n_qb;
-        f.T = p.T;
+        f.causal = p.causal;
+        f.no_skip = p.no_skip;
         f.G = grid;
         f.W = p.W;
         f.out_dtype = a.out_dtype;
         auto first_step = [&](long long c) { return c * p.W / grid; };
         auto cta_of = [&](long long step) {  // c with first_step(c) <= step < first_step(c + 1)
             long long c = (step + 1) * grid / p.W;
+            if (c >= grid) c = grid - 1;
             while (c > 0 && first_step(c) > step) --c;
             while (c + 1 < grid && first_step(c + 1) <= step) ++c;
             return static_cast<int>(c);
         };
+        auto unit_of = [&](long long step, long long &ustart, int &cost) {
+            const long long bh = step / p.HT;
+            const int rem = static_cast<int>(step - bh * p.HT);
+            const int qb = static_cast<int>(std::upper_bound(p.pre, p.pre + p.n_qb + 1, rem) - p.pre) - 1;
+            ustart = bh * p.HT + p.pre[qb];
+            cost = p.pre[qb + 1] - p.pre[qb];
+            return static_cast<int>(bh * p.n_qb + qb);
+        };
         int last_u = -1;
         for (int c = 1; c < grid; ++c) {
             const long long b = first_step(c);
-            if (b % p.T == 0) continue;  // boundary between units: nothing to merge
-            const int u = static_cast<int>(b / p.T);
-            if (u == last_u) continue;
+            if (b >= p.W) break;
+            long long us;
+            int cost;
+            const int u = unit_of(b, us, cost);
+            if (b == us || u == last_u) continue;  // a boundary between units, or done
             last_u = u;
-            f.item[f.n_split++] = make_int4(u, cta_of(static_cast<long long>(u) * p.T),
-                                            cta_of(static_cast<long long>(u + 1) * p.T - 1), 0);
+            f.item[f.n_split] = make_int4(u, cta_of(us), cta_of(us + cost - 1), cost);
+            f.ustart[f.n_split] = us;
+            ++f.n_split;
         }
         if (f.n_split > 0) {
             const size_t o_bytes = static_cast<size_t>(grid) * 2 * kRowsPerUnit * D * sizeof(float);
             const size_t ml_bytes = static_cast<size_t>(grid) * 2 * kRowsPerUnit * 2 * sizeof(float);
-            e = cudaMallocAsync(&ws, o_bytes + ml_bytes, stream);
+            e = scratch_alloc(&ws, o_bytes + ml_bytes, stream);
             if (e != cudaSuccess) {
                 cuda_fail(e);
                 return FA_ERR_WORKSPACE;
@@ -852,7 +1045,7 @@ int launch_d(const PrefillLaunch &a, const DeviceInfo &dev, cudaStream_t stream)
         if (e == cudaSuccess) e = cudaGetLastError();
     }
     if (ws) {
-        const cudaError_t e2 = cudaFreeAsync(ws, stream);
+        const cudaError_t e2 = scratch_free(ws, stream);
         if (e == cudaSuccess) e = e2;
     }
     if (e != cudaSuccess) return cuda_fail(e);

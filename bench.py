@@ -287,6 +287,12 @@ def run_ours(args):
     dec_s_max, _ = aggregate(dec_time_s, 0.0, world, device)
     step_ms_max, _ = aggregate(step_ms, 0.0, world, device)
 
+    peaks, peak_src = load_peaks()
+    configs = None
+    if rank == 0 and not args.no_configs and not args.case:
+        configs = measure_configs(torch, binding, device, stream, flush, peaks)
+        assert binding.fa_device_status(False) == 0
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
         cpu = cpu_baseline(args.cpu_seconds)
@@ -296,7 +302,6 @@ def run_ours(args):
             dist.destroy_process_group()
         return None
 
-    peaks, peak_src = load_peaks()
     value = tot_flops / tot_s / 1e12 if do_pre else None
     n_launch = len(do_pre) * args.steps + (2 * args.steps if do_dec else 0)
     detail = {}
@@ -347,6 +352,7 @@ def run_ours(args):
         },
         "decode": None,
         "detail": detail,
+        "configs": configs,
         "e2e": e2e,
         "gpu_launches": n_launch,
         "clocks": clocks,
@@ -367,9 +373,95 @@ def run_ours(args):
     return line
 
 
+# ------------------------------------------------------------------ every config
+def time_kernel(torch, stream, flush, fn, reps):
+    """Median and min device time (ms) of fn() over reps runs, L2 flushed before each."""
+    ms = []
+    for _ in range(reps):
+        flush.zero_()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+        e1.synchronize()
+        ms.append(e0.elapsed_time(e1))
+    return statistics.median(ms), min(ms)
+
+
+def measure_configs(torch, binding, device, stream, flush, peaks, reps=7):
+    """The other workloads of the target (tiny, GPT-2 shape, stress, every decode
+    batch), timed one kernel at a time outside the main timed region."""
+    from attention_forward_prefill_gb300 import inputs as fin
+    g = torch.Generator(device=device)
+    g.manual_seed(0xFA00F00D)
+    res = {}
+
+    def rnd(shape, dtype):
+        return torch.randn(shape, generator=g, device=device, dtype=torch.float32).to(dtype)
+
+    pre_cases = [("tiny", 1, 2, 128, 64, torch.float16, torch.float32, 0.125),
+                 ("gpt2_b1", 1, 12, 2048, 64, torch.float16, torch.float16, 0.125),
+                 ("gpt2_b4", 4, 12, 2048, 64, torch.float16, torch.float16, 0.125),
+                 ("stress", 8, 32, 8192, 128, torch.bfloat16, torch.bfloat16,
+                  float(1.0 / math.sqrt(128)))]
+    for name, B, H, N, d, dt, odt, scale in pre_cases:
+        q, k, v = (rnd((B, H, N, d), dt) for _ in range(3))
+        if name == "stress":  # 1% of the key rows x20 (same rows in every head)
+            idx = torch.randperm(N, generator=g, device=device)[: round(0.01 * N)]
+            k[:, :, idx] *= 20
+        out = torch.empty((B, H, N, d), dtype=odt, device=device)
+        for causal in ((True,) if name == "stress" else (False, True)):
+            def fn():
+                binding.prefill(q, k, v, causal=causal, scale=scale, out=out, out_dtype=odt)
+            fn()
+            med, mn = time_kernel(torch, stream, flush, fn, reps)
+            tf = prefill_flops(B, H, N, d, causal) / (med / 1e3) / 1e12
+            res[f"{name}_{'causal' if causal else 'full'}"] = {
+                "shape": [B, H, N, d], "median_us": round(med * 1e3, 2),
+                "min_us": round(mn * 1e3, 2), "tflops": round(tf, 1),
+                "frac_of_peak": round(tf / peaks["bf16_tflops"], 4)}
+        del q, k, v, out
+    for B in (1, 8, 32):
+        for H in (14, 12):
+            shp = (B, H, DECODE_L, DECODE_D)
+            dq = rnd((B, H, 1, DECODE_D), torch.float16)
+            dk, dv = rnd(shp, torch.float16), rnd(shp, torch.float16)
+            lens_np = fin.seq_lens(fin.seed_for(3, fin.TENSOR_SEQLEN) + B, B, DECODE_L)
+            lens = torch.from_numpy(lens_np).to(device)
+            out = torch.empty_like(dq)
+            splits = binding.fa_decode_choose_splits(B, H, DECODE_L, 0)
+            ws = torch.empty(binding.fa_decode_workspace_bytes(B, H, DECODE_L, DECODE_D, splits),
+                             dtype=torch.uint8, device=device)
+
+            def fn():
+                binding.decode(dq, dk, dv, lens, scale=0.125, num_splits=splits, workspace=ws,
+                               out=out)
+            fn()
+            med, mn = time_kernel(torch, stream, flush, fn, reps)
+            gbs = decode_bytes(lens_np, H, DECODE_D) / (med / 1e3) / 1e9
+            res[f"decode_b{B}_h{H}"] = {
+                "shape": list(shp), "splits": splits, "median_us": round(med * 1e3, 2),
+                "min_us": round(mn * 1e3, 2), "gbs": round(gbs, 1),
+                "frac_of_peak": round(gbs / peaks["hbm_gbs"], 4)}
+    # read-only streaming probe (a library reduction over 4 GiB), beside decode
+    x = torch.ones(1 << 31, dtype=torch.float16, device=device)
+    med, _ = time_kernel(torch, stream, flush, lambda: torch.sum(x, dtype=torch.float32), reps)
+    res["read_probe"] = {"what": "torch.sum over 4 GiB fp16 (library kernel)",
+                         "gbs": round(x.numel() * 2 / (med / 1e3) / 1e9, 1)}
+    del x
+    return res
+
+
 # ------------------------------------------------------------------ oracle legs
-def oracle_sample(seconds: float, N: int = 16384):
-    """Time the fp64 oracle on whole rows of the N-length prefill (one head)."""
+def oracle_sample(seconds: float, N: int = 16384, threads: int = 1):
+    """Time the fp64 oracle on whole rows of the N-length prefill (one head).
+
+    threads > 1 spreads blocks of rows over host threads (the C routine runs
+    outside the GIL), the row-parallel form of the same oracle.
+    """
+    from concurrent.futures import ThreadPoolExecutor
+
     import numpy as np
 
     from attention_forward_prefill_gb300 import inputs as fin
@@ -384,10 +476,13 @@ def oracle_sample(seconds: float, N: int = 16384):
     oracle.attention(q, k, v, False, scale, rows=[0])  # load / build
     done = 0
     t0 = time.perf_counter()
-    while time.perf_counter() - t0 < seconds:
-        rows = np.arange(done, done + rows_per_call) % N
-        oracle.attention(q, k, v, False, scale, rows=rows, threads=1)
-        done += rows_per_call
+    with ThreadPoolExecutor(max_workers=threads) as ex:
+        while time.perf_counter() - t0 < seconds:
+            blocks = [np.arange(done + i * rows_per_call, done + (i + 1) * rows_per_call) % N
+                      for i in range(threads)]
+            list(ex.map(lambda r: oracle.attention(q, k, v, False, scale, rows=r, threads=1),
+                        blocks))
+            done += rows_per_call * threads
     dt = time.perf_counter() - t0
     flops = 4.0 * N * d * done
     return flops / dt / 1e12, done, dt
@@ -395,10 +490,15 @@ def oracle_sample(seconds: float, N: int = 16384):
 
 def cpu_baseline(seconds: float):
     value, rows, dt = oracle_sample(seconds)
+    cores = os.cpu_count() or 1
+    par, prow, pdt = oracle_sample(max(2.0, seconds / 4), threads=cores)
     return {"value": value, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
             "sample": (f"{rows} query rows of one head of the N=16384 d=128 dense prefill "
                        f"({dt:.1f} s single-threaded fp64 C oracle); FLOPs counted as 4*N*d "
-                       "per row")}
+                       "per row"),
+            "all_cores": {"value": par, "unit": "TFLOP/s", "cores": cores,
+                          "sample": f"{prow} rows, row blocks over {cores} host threads, "
+                                    f"{pdt:.1f} s"}}
 
 
 def run_reference(args):
@@ -452,6 +552,8 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the per-config table (tiny, GPT-2 shape, stress, decode batches)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "ours" and not args.case:

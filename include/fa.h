@@ -65,6 +65,17 @@ typedef enum {
  * bit-identical to the default ("Kernel design" table, causal tile skipping,
  * "verified bit-identical"); the flag exists so that tests can check that. */
 #define FA_FLAG_NO_CAUSAL_SKIP 1u
+/* Work schedule of the prefill kernel (performance tuning and tests; the
+ * result stays within the tolerance either way and is bit-identical run to run
+ * for a given choice).  By default the library picks, from the shapes and the
+ * SM count only: one CTA per SM walks whole 256-row query blocks, or, for a
+ * dense batch, the key-tile steps of all blocks are cut into equal ranges per
+ * CTA ("stream-K") and the blocks cut between CTAs are merged by a second
+ * kernel.  UNITS forces the first; STREAM_K asks for the second where it
+ * applies (dense batches in which every query row sees at least one key).
+ * If both are set, UNITS wins.  Other bits are reserved and ignored. */
+#define FA_FLAG_SCHEDULE_UNITS 2u
+#define FA_FLAG_SCHEDULE_STREAM_K 4u
 
 /*
  * Prefill (flash-attention-cuda README, "What did I implement?" prompt phase,
@@ -87,11 +98,58 @@ int fa_prefill(const void *q, const void *k, const void *v, void *out,
  *   in_dtype  : FA_F16 or FA_BF16 (q, k and v share it)
  *   out_dtype : FA_F16, FA_BF16 or FA_F32 (rounded to nearest even)
  *   flags     : FA_FLAG_* bits
+ * Large problems may take a stream-ordered scratch buffer (at most
+ * SMs x 2 x 256 x d x 4 bytes plus 8 bytes per row of it) from the library's
+ * device memory pool; FA_ERR_WORKSPACE if that allocation fails.
  */
 int fa_prefill_ex(const void *q, const void *k, const void *v, void *out,
                   int B, int H, int N, int d, int causal, float scale,
                   fa_dtype in_dtype, fa_dtype out_dtype, unsigned flags,
                   void *stream);
+
+/*
+ * Prefill with grouped key/value heads and separate query / key lengths
+ * (flash-attention-cuda README, "Future work": kernel-side GQA instead of a
+ * host-side repeat of the key/value heads; a prompt processed in chunks
+ * attends from its newest Nq positions over all Nk keys, as the generation
+ * phase of "What did I implement?" does with Nq = 1).
+ *   q, out : [B][Hq][Nq][d]      k, v : [B][Hkv][Nk][d]
+ *   Hq     : a multiple of Hkv; query head h reads key/value head h / (Hq / Hkv)
+ *   causal : the queries are the last Nq positions: query i sees keys
+ *            j <= i + (Nk - Nq).  When Nq > Nk the first Nq - Nk rows see no
+ *            key and are written as zeros.
+ * Other arguments as fa_prefill_ex.  Errors: FA_ERR_SHAPE when a size is < 1,
+ * Hq % Hkv != 0 or an element count exceeds INT_MAX; the others as above.
+ */
+int fa_prefill_gqa(const void *q, const void *k, const void *v, void *out,
+                   int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal,
+                   float scale, fa_dtype in_dtype, fa_dtype out_dtype,
+                   unsigned flags, void *stream);
+
+/*
+ * Prefill of a packed batch of variable-length sequences.  Sequence b owns
+ * query tokens [cu_seqlens_q[b], cu_seqlens_q[b+1]) and key/value tokens
+ * [cu_seqlens_k[b], cu_seqlens_k[b+1]); sequences never see each other.
+ *   q, out      : [total_q][Hq][d]     k, v : [total_k][Hkv][d]
+ *   cu_seqlens_q, cu_seqlens_k : int32 device arrays of B + 1 non-decreasing
+ *                 offsets from 0 to total_q / total_k (4-byte aligned).  The
+ *                 kernel clamps them to [0, total], so a bad array cannot make
+ *                 it write outside `out`.
+ *   max_seqlen_q, max_seqlen_k : host upper bounds of the per-sequence
+ *                 lengths; rows past max_seqlen_q of a longer sequence are
+ *                 left unwritten and keys past max_seqlen_k are ignored.
+ *   causal      : per sequence, as fa_prefill_gqa (queries are the last
+ *                 positions of their sequence).
+ * A sequence with no keys gives zero rows; total_q == 0 returns FA_OK at once.
+ * Always scheduled unit by unit (no scratch memory).  The lengths stay on the
+ * device: nothing is copied back to the host.
+ */
+int fa_prefill_varlen(const void *q, const void *k, const void *v, void *out,
+                      const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
+                      int B, int Hq, int Hkv, int total_q, int total_k,
+                      int max_seqlen_q, int max_seqlen_k, int d, int causal,
+                      float scale, fa_dtype in_dtype, fa_dtype out_dtype,
+                      unsigned flags, void *stream);
 
 /*
  * Split-K decode (flash-attention-cuda README, "What did I implement?"
@@ -110,7 +168,8 @@ int fa_prefill_ex(const void *q, const void *k, const void *v, void *out,
  * The split count is chosen from (B, H, max_len, SM count) only, never from
  * the device-resident lengths, so it needs no device-to-host copy and gives
  * bit-identical results run to run.  The partials workspace is allocated
- * stream-ordered (cudaMallocAsync / cudaFreeAsync on `stream`).
+ * stream-ordered on `stream` from a memory pool the library creates once per
+ * device; the pool keeps up to 256 MiB of freed scratch mapped for reuse.
  */
 int fa_decode(const void *q, const void *k_cache, const void *v_cache,
               const int32_t *seq_lens, void *out,

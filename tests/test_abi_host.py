@@ -64,6 +64,40 @@ def test_prefill_argument_errors(lib, args, status):
     assert binding.fa_prefill_ex(q, k, v, out, B, H, N, d, causal, scale, it, ot, fl, None) == status
 
 
+@pytest.mark.parametrize("args,status", [
+    ((None, A, A, B_, 1, 4, 2, 8, 8, 64, 0, 1.0, 0, 0, 0), 1),
+    ((A, A, A, B_, 1, 6, 4, 8, 8, 64, 0, 1.0, 0, 0, 0), 2),      # Hq not a multiple of Hkv
+    ((A, A, A, B_, 1, 4, 0, 8, 8, 64, 0, 1.0, 0, 0, 0), 2),
+    ((A, A, A, B_, 1, 4, 2, 8, 0, 64, 0, 1.0, 0, 0, 0), 2),      # no keys
+    ((A, A, A, B_, 1, 4, 2, 0, 8, 64, 0, 1.0, 0, 0, 0), 2),
+    ((A, A, A, B_, 1, 4, 2, 8, 8, 80, 0, 1.0, 0, 0, 0), 3),
+    ((A, A, A, B_, 1, 4, 2, 8, 8, 64, 0, 1.0, 0, 3, 0), 4),
+    ((A, A, A + 4, B_, 1, 4, 2, 8, 8, 64, 0, 1.0, 0, 0, 0), 5),
+    ((A, A, A, B_, 1, 4, 2, 8, 8, 64, 0, float("-inf"), 0, 0, 0), 6),
+    ((A, B_ - 64, A, B_, 1, 4, 2, 8, 1024, 64, 0, 1.0, 0, 0, 0), 11),  # k runs into out
+])
+def test_gqa_prefill_argument_errors(lib, args, status):
+    assert binding.fa_prefill_gqa(*args, None) == status
+
+
+CU = 1 << 16
+
+
+@pytest.mark.parametrize("args,status", [
+    ((A, A, A, B_, None, CU, 2, 4, 2, 64, 64, 32, 32, 64, 1, 1.0, 0, 0, 0), 1),
+    ((A, A, A, B_, CU + 2, CU, 2, 4, 2, 64, 64, 32, 32, 64, 1, 1.0, 0, 0, 0), 5),
+    ((A, A, A, B_, CU, CU, 2, 4, 3, 64, 64, 32, 32, 64, 1, 1.0, 0, 0, 0), 2),
+    ((A, A, A, B_, CU, CU, 0, 4, 2, 64, 64, 32, 32, 64, 1, 1.0, 0, 0, 0), 2),
+    ((A, A, A, B_, CU, CU, 2, 4, 2, 64, -1, 32, 32, 64, 1, 1.0, 0, 0, 0), 2),
+    ((A, A, A, B_, CU, CU, 2, 4, 2, 64, 64, 32, 32, 100, 1, 1.0, 0, 0, 0), 3),
+    ((A, A, A, A, CU, CU, 2, 4, 2, 64, 64, 32, 32, 64, 1, 1.0, 0, 0, 0), 11),
+    # no query rows: nothing to do, and no device is touched
+    ((A, A, A, B_, CU, CU, 2, 4, 2, 0, 64, 0, 32, 64, 1, 1.0, 0, 0, 0), 0),
+])
+def test_varlen_prefill_argument_errors(lib, args, status):
+    assert binding.fa_prefill_varlen(*args, None) == status
+
+
 def test_plain_prefill_checks_too(lib):
     assert binding.fa_prefill(None, A, A, B_, 1, 1, 1, 64, 0, 1.0, None) == 1
     assert binding.fa_prefill(A, A, A, B_, 1, 1, 1, 80, 0, 1.0, None) == 3
