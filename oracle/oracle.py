@@ -213,21 +213,27 @@ def decode(q: np.ndarray, k_cache: np.ndarray, v_cache: np.ndarray,
            seq_lens, scale: float, threads: int = 1) -> np.ndarray:
     """Decode: each (b, h) query row attends over cache rows [0, seq_lens[b]).
 
-    q: [B, H, 1, d] (or [B, H, d]); caches: [B, H, max_len, d]; returns [B, H, 1, d].
+    q: [B, Hq, 1, d] (or [B, Hq, d]); caches: [B, Hkv, max_len, d] with Hkv | Hq
+    (query head h reads cache head h // (Hq // Hkv)); returns [B, Hq, 1, d].
     """
-    q = np.ascontiguousarray(q, dtype=np.float64).reshape(k_cache.shape[0], k_cache.shape[1], -1)
     k_cache = np.ascontiguousarray(k_cache, dtype=np.float64)
     v_cache = np.ascontiguousarray(v_cache, dtype=np.float64)
-    B, H, max_len, d = k_cache.shape
+    B, h_kv, max_len, d = k_cache.shape
+    q = np.ascontiguousarray(q, dtype=np.float64).reshape(B, -1, d)
+    H = q.shape[1]
+    if H % h_kv != 0 or v_cache.shape != k_cache.shape:
+        raise ValueError("bad shapes: q [B,Hq,1,d], caches [B,Hkv,L,d] with Hkv | Hq")
+    group = H // h_kv
     lens = np.asarray(seq_lens, dtype=np.int64).reshape(-1)
     out = np.zeros((B, H, 1, d), dtype=np.float64)
     lib = _load()
 
     def one(bh):
         b, h = divmod(bh, H)
+        hk = h // group
         o = np.zeros(d, dtype=np.float64)
-        rc = lib.oracle_decode_head(_dptr(q[b, h]), _dptr(k_cache[b, h]),
-                                    _dptr(v_cache[b, h]), int(lens[b]), max_len,
+        rc = lib.oracle_decode_head(_dptr(q[b, h]), _dptr(k_cache[b, hk]),
+                                    _dptr(v_cache[b, hk]), int(lens[b]), max_len,
                                     d, float(scale), _dptr(o))
         if rc != 0:
             raise RuntimeError("oracle_decode_head failed")

@@ -357,3 +357,17 @@ def test_packed_batch_equals_each_sequence_alone(oracle_mod, causal):
     assert np.array_equal(got2[cu_q[0]:cu_q[1]], got[cu_q[0]:cu_q[1]])
     assert np.array_equal(got2[cu_q[2]:], got[cu_q[2]:])
     assert np.max(np.abs(got2[cu_q[1]:cu_q[2]] - got[cu_q[1]:cu_q[2]])) > 1e-3
+
+
+def test_grouped_decode_equals_repeated_caches_and_a_one_row_chunk(oracle_mod):
+    r = rng(26)
+    B, Hq, Hkv, L, d = 3, 14, 2, 50, 8
+    q = r.normal(size=(B, Hq, 1, d))
+    kc, vc = r.normal(size=(2, B, Hkv, L, d))
+    lens = [1, 33, 50]
+    got = oracle_mod.decode(q, kc, vc, lens, 0.3)
+    rep = oracle_mod.decode(q, np.repeat(kc, 7, axis=1), np.repeat(vc, 7, axis=1), lens, 0.3)
+    assert np.array_equal(got, rep)
+    for b, n in enumerate(lens):   # the same row as a one-query causal chunk over n keys
+        one = oracle_mod.attention(q[b:b + 1], kc[b:b + 1, :, :n], vc[b:b + 1, :, :n], True, 0.3)
+        assert np.max(np.abs(one[0, :, 0] - got[b, :, 0])) < 1e-15
