@@ -39,6 +39,9 @@ _SIGNATURES = {
                                _f, _i, _i, _u, _vp]),
     "fa_decode": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _vp]),
     "fa_decode_ex": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _i, _i, _vp, _sz, _vp]),
+    "fa_decode_gqa": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _i, _i, _vp, _sz,
+                           _vp]),
+    "fa_decode_gqa_choose_splits": (_i, [_i, _i, _i, _i, _i]),
     "fa_decode_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _i, _i, _vp]),
     "fa_decode_noalloc_max_bytes": (_sz, []),
     "fa_decode_choose_splits": (_i, [_i, _i, _i, _i]),
@@ -118,6 +121,17 @@ def fa_decode_ex(q, k_cache, v_cache, seq_lens, out, B, H, max_len, d, scale, in
     return load().fa_decode_ex(q, k_cache, v_cache, seq_lens, out, B, H, max_len, d,
                                float(scale), in_dtype, out_dtype, num_splits, workspace,
                                workspace_bytes, stream)
+
+
+def fa_decode_gqa(q, k_cache, v_cache, seq_lens, out, B, Hq, Hkv, max_len, d, scale, in_dtype,
+                  out_dtype, num_splits=0, workspace=None, workspace_bytes=0, stream=0) -> int:
+    return load().fa_decode_gqa(q, k_cache, v_cache, seq_lens, out, B, Hq, Hkv, max_len, d,
+                                float(scale), in_dtype, out_dtype, num_splits, workspace,
+                                workspace_bytes, stream)
+
+
+def fa_decode_gqa_choose_splits(B, Hq, Hkv, max_len, num_sms=0) -> int:
+    return load().fa_decode_gqa_choose_splits(B, Hq, Hkv, max_len, num_sms)
 
 
 def fa_decode_noalloc(q, k_cache, v_cache, seq_lens, out, B, H, max_len, d, scale, in_dtype,
@@ -270,30 +284,34 @@ def decode(q, k_cache, v_cache, seq_lens, scale: float | None = None, out_dtype=
            num_splits: int = 0, workspace=None, out=None):
     """One query row per (b, h) over the first seq_lens[b] rows of the cache.
 
-    q: [B, H, 1, d]; caches: [B, H, max_len, d]; seq_lens: int32 [B] on the
-    same device.  Returns [B, H, 1, d].
+    q: [B, Hq, 1, d]; caches: [B, Hkv, max_len, d] with Hkv dividing Hq (query
+    head h reads cache head h // (Hq // Hkv)); seq_lens: int32 [B] on the same
+    device.  Returns [B, Hq, 1, d].
     """
     torch = _torch()
-    B, H, max_len, d = k_cache.shape
+    B, Hkv, max_len, d = k_cache.shape
     _check_cuda("k_cache", k_cache)
     _check_cuda("v_cache", v_cache, k_cache.shape, k_cache.dtype)
-    _check_cuda("q", q, (B, H, 1, d), k_cache.dtype)
+    _check_cuda("q", q, None, k_cache.dtype)
+    if q.dim() != 4 or q.shape[0] != B or q.shape[2] != 1 or q.shape[3] != d:
+        raise ValueError(f"q has shape {tuple(q.shape)}, expected [{B}, Hq, 1, {d}]")
+    Hq = q.shape[1]
     _check_cuda("seq_lens", seq_lens, (B,), torch.int32)
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     out_dtype = q.dtype if out_dtype is None else out_dtype
     if out is None:
-        out = torch.empty((B, H, 1, d), dtype=out_dtype, device=q.device)
+        out = torch.empty((B, Hq, 1, d), dtype=out_dtype, device=q.device)
     else:
-        _check_cuda("out", out, (B, H, 1, d), out_dtype)
+        _check_cuda("out", out, (B, Hq, 1, d), out_dtype)
     ws_ptr, ws_bytes = None, 0
     if workspace is not None:
         _check_cuda("workspace", workspace)
         ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
-    rc = fa_decode_ex(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), seq_lens.data_ptr(),
-                      out.data_ptr(), B, H, max_len, d, scale, dtype_code(q.dtype),
-                      dtype_code(out_dtype), num_splits, ws_ptr, ws_bytes,
-                      _stream_handle(q.device))
+    rc = fa_decode_gqa(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), seq_lens.data_ptr(),
+                       out.data_ptr(), B, Hq, Hkv, max_len, d, scale, dtype_code(q.dtype),
+                       dtype_code(out_dtype), num_splits, ws_ptr, ws_bytes,
+                       _stream_handle(q.device))
     if rc != FA_OK:
-        raise FaError(rc, "fa_decode_ex")
+        raise FaError(rc, "fa_decode_gqa")
     return out

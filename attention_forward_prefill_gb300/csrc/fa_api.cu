@@ -300,6 +300,14 @@ int fa_decode_choose_splits(int B, int H, int max_len, int num_sms) {
     return decode_effective_splits(max_len, static_cast<int>(splits), nullptr);
 }
 
+int fa_decode_gqa_choose_splits(int B, int Hq, int Hkv, int max_len, int num_sms) {
+    if (B < 1 || Hq < 1 || Hkv < 1 || max_len < 1 || Hq % Hkv != 0) return -FA_ERR_SHAPE;
+    // the same rule over the CTA rows of the grouped kernel: one per slice of
+    // each cache head's group of query heads
+    const long long rows = static_cast<long long>(Hkv) * decode_group_slices(Hq / Hkv);
+    return fa_decode_choose_splits(B, static_cast<int>(rows), max_len, num_sms);
+}
+
 size_t fa_decode_workspace_bytes(int B, int H, int max_len, int d, int num_splits) {
     if (B < 1 || H < 1 || max_len < 1 || num_splits < 1) return 0;
     if (d != 64 && d != 128) return 0;
@@ -308,13 +316,14 @@ size_t fa_decode_workspace_bytes(int B, int H, int max_len, int d, int num_split
     return ws_ml_bytes(bh, splits) + static_cast<size_t>(bh) * splits * d * 4;
 }
 
-int fa_decode_ex(const void *q, const void *k_cache, const void *v_cache, const int32_t *seq_lens,
-                 void *out, int B, int H, int max_len, int d, float scale, fa_dtype in_dtype,
-                 fa_dtype out_dtype, int num_splits, void *workspace, size_t workspace_bytes,
-                 void *stream) {
+int fa_decode_gqa(const void *q, const void *k_cache, const void *v_cache, const int32_t *seq_lens,
+                  void *out, int B, int Hq, int Hkv, int max_len, int d, float scale,
+                  fa_dtype in_dtype, fa_dtype out_dtype, int num_splits, void *workspace,
+                  size_t workspace_bytes, void *stream) {
     if (!q || !k_cache || !v_cache || !seq_lens || !out) return FA_ERR_NULL;
-    if (B < 1 || H < 1 || max_len < 1) return FA_ERR_SHAPE;
-    if (static_cast<long long>(B) * H * max_len > INT_MAX) return FA_ERR_SHAPE;
+    if (B < 1 || Hq < 1 || Hkv < 1 || max_len < 1 || Hq % Hkv != 0) return FA_ERR_SHAPE;
+    if (static_cast<long long>(B) * Hkv * max_len > INT_MAX || static_cast<long long>(B) * Hq > INT_MAX)
+        return FA_ERR_SHAPE;
     if (d != 64 && d != 128) return FA_ERR_HEAD_DIM;
     if (in_dtype != FA_F16 && in_dtype != FA_BF16) return FA_ERR_DTYPE;
     if (out_dtype != FA_F16 && out_dtype != FA_BF16 && out_dtype != FA_F32) return FA_ERR_DTYPE;
@@ -324,23 +333,29 @@ int fa_decode_ex(const void *q, const void *k_cache, const void *v_cache, const 
     if (!std::isfinite(scale)) return FA_ERR_SCALE;
     const long long max_splits = ceil_div(max_len, kDecodeRowAlign);
     if (num_splits < 0 || num_splits > max_splits) return FA_ERR_SPLITS;
-    const size_t bh = static_cast<size_t>(B) * H;
-    const size_t out_bytes = bh * d * dtype_size(out_dtype);
-    const size_t cache_bytes = bh * static_cast<size_t>(max_len) * d * 2;
-    if (overlaps(out, out_bytes, q, bh * d * 2) || overlaps(out, out_bytes, k_cache, cache_bytes) ||
+    const size_t bhq = static_cast<size_t>(B) * Hq;
+    const size_t out_bytes = bhq * d * dtype_size(out_dtype);
+    const size_t cache_bytes = static_cast<size_t>(B) * Hkv * static_cast<size_t>(max_len) * d * 2;
+    if (overlaps(out, out_bytes, q, bhq * d * 2) || overlaps(out, out_bytes, k_cache, cache_bytes) ||
         overlaps(out, out_bytes, v_cache, cache_bytes) ||
         overlaps(out, out_bytes, seq_lens, static_cast<size_t>(B) * 4))
         return FA_ERR_ALIAS;
 
     int splits = num_splits;
     if (splits == 0) {
-        splits = fa_decode_choose_splits(B, H, max_len, 0);
+        splits = fa_decode_gqa_choose_splits(B, Hq, Hkv, max_len, 0);
         if (splits < 0) return -splits;
     }
     int chunk = 0;
     splits = decode_effective_splits(max_len, splits, &chunk);
-    if (chunk > kDecodeMaxChunk) return FA_ERR_SPLITS;
-    const size_t need = fa_decode_workspace_bytes(B, H, max_len, d, splits);
+    // A CTA keeps the scores of its chunk for up to 8 query heads (2, 4 or 8
+    // rows of shared memory) within 192 KB.
+    const int group = Hq / Hkv;
+    const int slices = decode_group_slices(group);
+    const int gper = (group + slices - 1) / slices;
+    const int rows = group == 1 ? 1 : (gper <= 2 ? 2 : (gper <= 4 ? 4 : 8));
+    if (static_cast<long long>(chunk) * rows > kDecodeMaxChunk) return FA_ERR_SPLITS;
+    const size_t need = fa_decode_workspace_bytes(B, Hq, max_len, d, splits);
     if (workspace && workspace_bytes < need) return FA_ERR_WORKSPACE;
 
     DeviceInfo dev;
@@ -362,7 +377,8 @@ int fa_decode_ex(const void *q, const void *k_cache, const void *v_cache, const 
     a.seq_lens = seq_lens;
     a.out = out;
     a.B = B;
-    a.H = H;
+    a.H = Hq;
+    a.Hkv = Hkv;
     a.max_len = max_len;
     a.d = d;
     a.scale = scale;
@@ -372,13 +388,21 @@ int fa_decode_ex(const void *q, const void *k_cache, const void *v_cache, const 
     a.chunk = chunk;
     a.partial_ml = static_cast<float *>(ws);
     a.partial_acc = reinterpret_cast<float *>(static_cast<char *>(ws) +
-                                              ws_ml_bytes(static_cast<long long>(bh), splits));
+                                              ws_ml_bytes(static_cast<long long>(bhq), splits));
     rc = launch_decode(a, dev, st);
     if (!workspace) {
         cudaError_t e = scratch_free(ws, st);
         if (rc == FA_OK && e != cudaSuccess) rc = cuda_fail(e);
     }
     return rc;
+}
+
+int fa_decode_ex(const void *q, const void *k_cache, const void *v_cache, const int32_t *seq_lens,
+                 void *out, int B, int H, int max_len, int d, float scale, fa_dtype in_dtype,
+                 fa_dtype out_dtype, int num_splits, void *workspace, size_t workspace_bytes,
+                 void *stream) {
+    return fa_decode_gqa(q, k_cache, v_cache, seq_lens, out, B, H, H, max_len, d, scale, in_dtype,
+                         out_dtype, num_splits, workspace, workspace_bytes, stream);
 }
 
 int fa_decode(const void *q, const void *k_cache, const void *v_cache, const int32_t *seq_lens,

@@ -42,8 +42,12 @@ struct DParams {
     void *out;
     float *ml;
     float *acc;
-    int H;
-    int BH;
+    int H;         // query heads
+    int BH;        // B * H
+    int Hkv;       // cache heads (H for plain multi-head decode)
+    int group;     // H / Hkv: query head h reads cache head h / group
+    int gper;      // grouped decode: query heads per CTA (a slice of one group)
+    int ngb;       // slices per group
     int max_len;
     int chunk;
     int splits;
@@ -203,6 +207,175 @@ __global__ void __launch_bounds__(kSplitThreads)
     }
 }
 
+// Grouped decode: the query heads of one cache head (flash-attention-cuda
+// README, "Future work": kernel-side GQA instead of a host-side repeat) share
+// each K and V row the CTA streams.  CTA (s, hk * ngb + slice, b) covers up to
+// GP query heads h0 .. h0 + gcnt - 1 of cache head hk over the same chunk as
+// the plain kernel, and writes one partial per query head in the same layout,
+// so the merge kernel is shared.
+template <int D, int GP>
+__global__ void __launch_bounds__(kSplitThreads)
+    decode_split_gqa_kernel(const DParams p) {
+    constexpr int LPK = D * 2 / 16;          // lanes per cache row (16 bytes each)
+    constexpr int KPW = 32 / LPK;            // rows per warp per step
+    constexpr int KPC = KPW * kSplitWarps;   // rows per CTA per step
+    extern __shared__ float sh[];            // [GP][chunk] scores, then weights
+    __shared__ float red[kSplitWarps][GP][D];
+    __shared__ float red1[kSplitWarps][GP];
+
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const int s = blockIdx.x, b = blockIdx.z;
+    const int hk = blockIdx.y / p.ngb, slice = blockIdx.y % p.ngb;
+    const int h0 = hk * p.group + slice * p.gper;
+    const int gcnt = min(p.gper, p.group - slice * p.gper);
+    const int len = clamp_len(p.seq_lens[b], p.max_len);
+    const int start = s * p.chunk;
+    if (start >= len || gcnt <= 0) return;
+    const int n = min(start + p.chunk, len) - start;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int sub = lane % LPK, kw = lane / LPK;
+    const int ch = p.chunk;
+
+    float qf[GP][8];
+#pragma unroll
+    for (int g = 0; g < GP; ++g) {
+        if (g < gcnt) {
+            const size_t bhq = static_cast<size_t>(b) * p.H + h0 + g;
+            unpack8(*reinterpret_cast<const uint4 *>(p.q + bhq * D + sub * 8), p.in_bf16, qf[g]);
+        } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) qf[g][e] = 0.f;
+        }
+    }
+    const size_t bhk = static_cast<size_t>(b) * p.Hkv + hk;
+    const uint16_t *kbase = p.k + (bhk * p.max_len + start) * D + sub * 8;
+    const uint16_t *vbase = p.v + (bhk * p.max_len + start) * D + sub * 8;
+
+    // ---- scores x_gj = c * q_g.k_j, each K row read once for all GP heads
+    for (int base0 = warp * KPW; base0 < n; base0 += KPC * kUnroll) {
+        const int base = base0 + kw;
+        uint4 kr[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int key = base + u * KPC;
+            kr[u] = key < n ? ldg_stream(kbase + static_cast<size_t>(key) * D) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            float kf[8];
+            unpack8(kr[u], p.in_bf16, kf);
+            const int key = base + u * KPC;
+#pragma unroll
+            for (int g = 0; g < GP; ++g) {
+                float dot = 0.f;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) dot = fmaf(qf[g][e], kf[e], dot);
+#pragma unroll
+                for (int off = 1; off < LPK; off <<= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
+                if (sub == 0 && key < n) sh[g * ch + key] = dot * p.scale_log2;
+            }
+        }
+    }
+    __syncthreads();
+
+    // ---- per head: chunk maximum, then weights 2^(x - m) and their sum
+    float m[GP], l[GP];
+#pragma unroll
+    for (int g = 0; g < GP; ++g) {
+        float mx = -INFINITY;
+        for (int i = threadIdx.x; i < n; i += kSplitThreads) mx = fmaxf(mx, sh[g * ch + i]);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+        if (lane == 0) red1[warp][g] = mx;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int g = 0; g < GP; ++g) {
+        m[g] = red1[0][g];
+#pragma unroll
+        for (int w = 1; w < kSplitWarps; ++w) m[g] = fmaxf(m[g], red1[w][g]);
+    }
+    __syncthreads();
+#pragma unroll
+    for (int g = 0; g < GP; ++g) {
+        float sum = 0.f;
+        for (int i = threadIdx.x; i < n; i += kSplitThreads) {
+            const float e = ex2_approx(sh[g * ch + i] - m[g]);
+            sh[g * ch + i] = e;
+            sum += e;
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+        if (lane == 0) red1[warp][g] = sum;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int g = 0; g < GP; ++g) {
+        l[g] = red1[0][g];
+#pragma unroll
+        for (int w = 1; w < kSplitWarps; ++w) l[g] += red1[w][g];
+    }
+
+    // ---- acc_g = sum_j w_gj v_j, each V row read once for all GP heads
+    float acc[GP][8];
+#pragma unroll
+    for (int g = 0; g < GP; ++g)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[g][e] = 0.f;
+    for (int base0 = warp * KPW; base0 < n; base0 += KPC * kUnroll) {
+        const int base = base0 + kw;
+        uint4 vr[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int key = base + u * KPC;
+            vr[u] = key < n ? ldg_stream(vbase + static_cast<size_t>(key) * D) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int key = base + u * KPC;
+            float vf[8];
+            unpack8(vr[u], p.in_bf16, vf);
+#pragma unroll
+            for (int g = 0; g < GP; ++g) {
+                const float w = key < n ? sh[g * ch + key] : 0.f;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc[g][e] = fmaf(w, vf[e], acc[g][e]);
+            }
+        }
+    }
+#pragma unroll
+    for (int g = 0; g < GP; ++g)
+#pragma unroll
+        for (int off = LPK; off < 32; off <<= 1)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[g][e] += __shfl_xor_sync(0xffffffffu, acc[g][e], off);
+    if (kw == 0)
+#pragma unroll
+        for (int g = 0; g < GP; ++g)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) red[warp][g][sub * 8 + e] = acc[g][e];
+    __syncthreads();
+
+    for (int i = threadIdx.x; i < gcnt * D; i += kSplitThreads) {
+        const int g = i / D, c = i % D;
+        float a = red[0][g][c];
+#pragma unroll
+        for (int w = 1; w < kSplitWarps; ++w) a += red[w][g][c];
+        const size_t part = (static_cast<size_t>(b) * p.H + h0 + g) * p.splits + s;
+        p.acc[part * D + c] = a;
+    }
+    if (threadIdx.x < gcnt) {
+        const int g = threadIdx.x;
+        float mg = m[0], lg = l[0];
+#pragma unroll
+        for (int k = 1; k < GP; ++k)
+            if (k == g) { mg = m[k]; lg = l[k]; }
+        const size_t part = (static_cast<size_t>(b) * p.H + h0 + g) * p.splits + s;
+        p.ml[part * 2 + 0] = mg;
+        p.ml[part * 2 + 1] = lg;
+    }
+}
+
 template <int D>
 __global__ void __launch_bounds__(kMergeWarps * 32)
     decode_merge_kernel(const DParams p) {
@@ -250,6 +423,17 @@ __global__ void __launch_bounds__(kMergeWarps * 32)
     }
 }
 
+template <int D, int GP>
+cudaError_t launch_gqa_split(const DParams &p, const DecodeLaunch &a, cudaStream_t stream) {
+    const size_t smem = static_cast<size_t>(GP) * a.chunk * sizeof(float);
+    cudaError_t e = cudaFuncSetAttribute(decode_split_gqa_kernel<D, GP>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    dim3 grid(a.num_splits, a.Hkv * p.ngb, a.B);
+    decode_split_gqa_kernel<D, GP><<<grid, kSplitThreads, smem, stream>>>(p);
+    return cudaGetLastError();
+}
+
 template <int D>
 int launch_decode_d(const DecodeLaunch &a, cudaStream_t stream) {
     DParams p;
@@ -262,19 +446,32 @@ int launch_decode_d(const DecodeLaunch &a, cudaStream_t stream) {
     p.acc = a.partial_acc;
     p.H = a.H;
     p.BH = a.B * a.H;
+    p.Hkv = a.Hkv;
+    p.group = a.H / a.Hkv;
+    p.ngb = decode_group_slices(p.group);
+    p.gper = (p.group + p.ngb - 1) / p.ngb;
     p.max_len = a.max_len;
     p.chunk = a.chunk;
     p.splits = a.num_splits;
     p.in_bf16 = a.in_bf16;
     p.out_dtype = a.out_dtype;
     p.scale_log2 = a.scale * 1.4426950408889634f;
-    const size_t smem = static_cast<size_t>(a.chunk) * sizeof(float);
-    cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<D>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return cuda_fail(e);
-    dim3 grid(a.num_splits, a.H, a.B);
-    decode_split_kernel<D><<<grid, kSplitThreads, smem, stream>>>(p);
-    e = cudaGetLastError();
+    cudaError_t e;
+    if (p.group == 1) {
+        const size_t smem = static_cast<size_t>(a.chunk) * sizeof(float);
+        e = cudaFuncSetAttribute(decode_split_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem);
+        if (e != cudaSuccess) return cuda_fail(e);
+        dim3 grid(a.num_splits, a.H, a.B);
+        decode_split_kernel<D><<<grid, kSplitThreads, smem, stream>>>(p);
+        e = cudaGetLastError();
+    } else if (p.gper <= 2) {
+        e = launch_gqa_split<D, 2>(p, a, stream);
+    } else if (p.gper <= 4) {
+        e = launch_gqa_split<D, 4>(p, a, stream);
+    } else {
+        e = launch_gqa_split<D, 8>(p, a, stream);
+    }
     if (e != cudaSuccess) return cuda_fail(e);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((p.BH + kMergeWarps - 1) / kMergeWarps);

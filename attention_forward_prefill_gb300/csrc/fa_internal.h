@@ -50,11 +50,16 @@ struct PrefillLaunch {
 // Validated arguments -> encode tensor maps, launch the persistent kernel.
 int launch_prefill(const PrefillLaunch &a, const DeviceInfo &dev, cudaStream_t stream);
 
+// Grouped decode: a group of G query heads is cut into ceil(G / 8) slices,
+// one CTA row each, so that a CTA holds at most 8 query heads.
+inline int decode_group_slices(int group) { return (group + 7) / 8; }
+
 struct DecodeLaunch {
     const void *q, *k_cache, *v_cache;
     const int32_t *seq_lens;
     void *out;
     int B, H, max_len, d;
+    int Hkv;              // cache heads; H / Hkv query heads share each
     float scale;
     int in_bf16;
     int out_dtype;

@@ -392,6 +392,8 @@ def time_kernel(torch, stream, flush, fn, reps):
 def measure_configs(torch, binding, device, stream, flush, peaks, reps=7):
     """The other workloads of the target (tiny, GPT-2 shape, stress, every decode
     batch), timed one kernel at a time outside the main timed region."""
+    import numpy as np
+
     from attention_forward_prefill_gb300 import inputs as fin
     g = torch.Generator(device=device)
     g.manual_seed(0xFA00F00D)
@@ -422,6 +424,42 @@ def measure_configs(torch, binding, device, stream, flush, peaks, reps=7):
                 "min_us": round(mn * 1e3, 2), "tflops": round(tf, 1),
                 "frac_of_peak": round(tf / peaks["bf16_tflops"], 4)}
         del q, k, v, out
+    # the general prefill forms: grouped heads, a prompt chunk over a longer
+    # cache, and a packed batch of ragged sequences (FLOPs = 4 d per visible
+    # (query, key) pair, counted exactly)
+    def gen_case(name, q, k, v, fn, pairs, d, H):
+        fn()
+        med, mn = time_kernel(torch, stream, flush, fn, reps)
+        tf = 4.0 * d * H * pairs / (med / 1e3) / 1e12
+        res[name] = {"shape": [list(q.shape), list(k.shape)], "median_us": round(med * 1e3, 2),
+                     "min_us": round(mn * 1e3, 2), "tflops": round(tf, 1),
+                     "frac_of_peak": round(tf / peaks["bf16_tflops"], 4)}
+    B, Hq, Hkv, N, d = 4, 14, 2, 4096, 64
+    q = rnd((B, Hq, N, d), torch.float16)
+    k, v = rnd((B, Hkv, N, d), torch.float16), rnd((B, Hkv, N, d), torch.float16)
+    o = torch.empty_like(q)
+    gen_case("gqa_prefill_b4_h14_kv2_causal", q, k, v,
+             lambda: binding.prefill(q, k, v, causal=True, scale=0.125, out=o),
+             B * N * (N + 1) / 2, d, Hq)
+    Nq, Nk, H, d = 1024, 8192, 16, 128
+    q = rnd((1, H, Nq, d), torch.bfloat16)
+    k, v = rnd((1, H, Nk, d), torch.bfloat16), rnd((1, H, Nk, d), torch.bfloat16)
+    o = torch.empty_like(q)
+    gen_case("chunk_prefill_1024_over_8192_causal", q, k, v,
+             lambda: binding.prefill(q, k, v, causal=True, scale=1 / math.sqrt(d), out=o),
+             Nq * (Nk - Nq) + Nq * (Nq + 1) / 2, d, H)
+    lens = fin.seq_lens(0xFA00F00D, 16, 4096)
+    cu = torch.from_numpy(np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)).to(device)
+    T, H, d = int(lens.sum()), 16, 128
+    q = rnd((T, H, d), torch.bfloat16)
+    k, v = rnd((T, H, d), torch.bfloat16), rnd((T, H, d), torch.bfloat16)
+    o = torch.empty_like(q)
+    mx = int(lens.max())
+    gen_case("varlen_prefill_16seqs_causal", q, k, v,
+             lambda: binding.prefill_varlen(q, k, v, cu, cu, mx, mx, causal=True,
+                                            scale=1 / math.sqrt(d), out=o),
+             float(sum(int(n) * (int(n) + 1) / 2 for n in lens)), d, H)
+    del q, k, v, o
     for B in (1, 8, 32):
         for H in (14, 12):
             shp = (B, H, DECODE_L, DECODE_D)
@@ -444,6 +482,29 @@ def measure_configs(torch, binding, device, stream, flush, peaks, reps=7):
                 "shape": list(shp), "splits": splits, "median_us": round(med * 1e3, 2),
                 "min_us": round(mn * 1e3, 2), "gbs": round(gbs, 1),
                 "frac_of_peak": round(gbs / peaks["hbm_gbs"], 4)}
+    # grouped decode, Qwen2.5-0.5B-like heads (14 query heads over 2 cache
+    # heads): bytes are the K and V rows actually read (per cache head)
+    for B in (8, 32):
+        Hq, Hkv = 14, 2
+        dq = rnd((B, Hq, 1, DECODE_D), torch.float16)
+        dk = rnd((B, Hkv, DECODE_L, DECODE_D), torch.float16)
+        dv = rnd((B, Hkv, DECODE_L, DECODE_D), torch.float16)
+        lens_np = fin.seq_lens(fin.seed_for(3, fin.TENSOR_SEQLEN) + B, B, DECODE_L)
+        lens = torch.from_numpy(lens_np).to(device)
+        out = torch.empty_like(dq)
+        splits = binding.fa_decode_gqa_choose_splits(B, Hq, Hkv, DECODE_L, 0)
+        ws = torch.empty(binding.fa_decode_workspace_bytes(B, Hq, DECODE_L, DECODE_D, splits),
+                         dtype=torch.uint8, device=device)
+
+        def fn():
+            binding.decode(dq, dk, dv, lens, scale=0.125, num_splits=splits, workspace=ws, out=out)
+        fn()
+        med, mn = time_kernel(torch, stream, flush, fn, reps)
+        gbs = decode_bytes(lens_np, Hkv, DECODE_D) / (med / 1e3) / 1e9
+        res[f"decode_gqa_b{B}_h{Hq}_kv{Hkv}"] = {
+            "shape": [B, Hq, Hkv, DECODE_L, DECODE_D], "splits": splits,
+            "median_us": round(med * 1e3, 2), "min_us": round(mn * 1e3, 2), "gbs": round(gbs, 1),
+            "frac_of_peak": round(gbs / peaks["hbm_gbs"], 4)}
     # read-only streaming probe (a library reduction over 4 GiB), beside decode
     x = torch.ones(1 << 31, dtype=torch.float16, device=device)
     med, _ = time_kernel(torch, stream, flush, lambda: torch.sum(x, dtype=torch.float32), reps)

@@ -209,6 +209,32 @@ size_t fa_decode_workspace_bytes(int B, int H, int max_len, int d,
                                  int num_splits);
 
 /*
+ * Grouped decode (flash-attention-cuda README, "Future work": kernel-side GQA,
+ * instead of repeating the cache heads on the host).  Hq query heads share Hkv
+ * cache heads; query head h reads cache head h / (Hq / Hkv).  Each K and V row
+ * is read from HBM once for all query heads of its group.
+ *   q, out  : [B][Hq][1][d]          k_cache, v_cache : [B][Hkv][max_len][d]
+ *   Hq      : a multiple of Hkv (Hq == Hkv is plain multi-head decode and runs
+ *             the same kernels as fa_decode_ex)
+ *   workspace : NULL or at least fa_decode_workspace_bytes(B, Hq, max_len, d,
+ *             splits) bytes, splits being num_splits or, for 0, the value of
+ *             fa_decode_gqa_choose_splits(B, Hq, Hkv, max_len, 0)
+ * Other arguments, results and errors as fa_decode_ex; in addition
+ * FA_ERR_SHAPE when Hq % Hkv != 0, and FA_ERR_SPLITS when a chunk would need
+ * more than 192 KB of shared memory for the scores of its query heads
+ * (chunk x 8 > 48K rows for groups of more than 4 heads per CTA).
+ */
+int fa_decode_gqa(const void *q, const void *k_cache, const void *v_cache,
+                  const int32_t *seq_lens, void *out,
+                  int B, int Hq, int Hkv, int max_len, int d, float scale,
+                  fa_dtype in_dtype, fa_dtype out_dtype, int num_splits,
+                  void *workspace, size_t workspace_bytes, void *stream);
+
+/* Split count fa_decode_gqa uses for num_splits == 0 (negative fa_status on
+ * bad arguments; num_sms <= 0 queries the current device). */
+int fa_decode_gqa_choose_splits(int B, int Hq, int Hkv, int max_len, int num_sms);
+
+/*
  * Decode that allocates nothing.  The pages have no counterpart: this entry
  * point exists for callers that cannot allocate device memory while they run
  * -- for example a host that reserves the whole device up front for its own

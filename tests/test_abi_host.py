@@ -98,6 +98,37 @@ def test_varlen_prefill_argument_errors(lib, args, status):
     assert binding.fa_prefill_varlen(*args, None) == status
 
 
+def test_grouped_decode_argument_errors(lib):
+    L = 1 << 24
+    base = dict(q=A, k=A, v=A, lens=L, out=B_, B=2, Hq=14, Hkv=2, max_len=4096, d=64, scale=0.125,
+                it=0, ot=0, splits=0, ws=None, wsb=0)
+
+    def call(**kw):
+        a = {**base, **kw}
+        return binding.fa_decode_gqa(a["q"], a["k"], a["v"], a["lens"], a["out"], a["B"], a["Hq"],
+                                     a["Hkv"], a["max_len"], a["d"], a["scale"], a["it"], a["ot"],
+                                     a["splits"], a["ws"], a["wsb"], None)
+    assert call(Hkv=4) == 2           # 14 query heads cannot share 4 cache heads
+    assert call(Hkv=0) == 2
+    assert call(q=None) == 1
+    assert call(d=32) == 3
+    assert call(lens=L + 2) == 5
+    assert call(splits=4096 // 64 + 1) == 12
+    # 32 query heads per cache head: 8 per CTA, so a chunk may hold 6K rows
+    assert call(Hq=32, Hkv=1, max_len=60000, splits=1) == 12
+    assert call(ws=1 << 12, wsb=16, splits=4) == 8
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,L", [(1, 14, 2, 4096), (32, 14, 2, 4096), (8, 32, 1, 1000),
+                                        (4, 8, 8, 4096)])
+def test_grouped_split_choice(lib, B, Hq, Hkv, L):
+    s = binding.fa_decode_gqa_choose_splits(B, Hq, Hkv, L, 152)
+    rows = Hkv * ((Hq // Hkv + 7) // 8)
+    assert s == binding.fa_decode_choose_splits(B, rows, L, 152)
+    assert 1 <= s <= (L + 63) // 64
+    assert binding.fa_decode_gqa_choose_splits(B, Hq, 3, L, 152) < 0 or Hq % 3 == 0
+
+
 def test_plain_prefill_checks_too(lib):
     assert binding.fa_prefill(None, A, A, B_, 1, 1, 1, 64, 0, 1.0, None) == 1
     assert binding.fa_prefill(A, A, A, B_, 1, 1, 1, 80, 0, 1.0, None) == 3

@@ -135,3 +135,61 @@ def test_other_head_dims_and_dtypes(fa, oracle_mod, d, dtype):
     got = G.device_to_f64(run_decode(fa, q, kc, vc, lens, dtype, 1.0 / np.sqrt(d), "f32"))
     want = oracle_decode(oracle_mod, q, kc, vc, lens, dtype, 1.0 / np.sqrt(d))
     G.assert_close(got, want, dtype, "f32", f"decode d={d} {dtype}")
+
+
+# ------------------------------------------------------------ grouped cache heads
+def make_gqa(B, Hq, Hkv, L, d, dtype, seed, lens=None):
+    q = inputs.normal_bits((B, Hq, 1, d), seed, dtype)
+    kc = inputs.normal_bits((B, Hkv, L, d), seed + 1, dtype)
+    vc = inputs.normal_bits((B, Hkv, L, d), seed + 2, dtype)
+    if lens is None:
+        lens = inputs.seq_lens(seed + 3, B, L)
+    return q, kc, vc, np.asarray(lens, dtype=np.int32)
+
+
+@pytest.mark.parametrize("B", [1, 8, 32])
+def test_grouped_decode_qwen_shape(fa, oracle_mod, B):
+    # Qwen2.5-0.5B-like attention: 14 query heads over 2 cache heads, d = 64
+    q, kc, vc, lens = make_gqa(B, 14, 2, 4096, 64, "f16", 1500 + B)
+    got = G.device_to_f64(run_decode(fa, q, kc, vc, lens, "f16", 0.125))
+    want = oracle_decode(oracle_mod, q, kc, vc, lens, "f16", 0.125)
+    G.assert_close(got, want, "f16", "f16", f"grouped decode B={B}")
+
+
+@pytest.mark.parametrize("Hq,Hkv,d,dtype", [(8, 1, 64, "f16"), (4, 2, 128, "bf16"), (32, 2, 64, "f16"),
+                                            (12, 1, 128, "bf16"), (6, 2, 64, "bf16")])
+def test_grouped_decode_group_sizes(fa, oracle_mod, Hq, Hkv, d, dtype):
+    q, kc, vc, lens = make_gqa(3, Hq, Hkv, 2000, d, dtype, 1600 + Hq, [2000, 1, 777])
+    got = G.device_to_f64(run_decode(fa, q, kc, vc, lens, dtype, 1.0 / np.sqrt(d), "f32"))
+    want = oracle_decode(oracle_mod, q, kc, vc, lens, dtype, 1.0 / np.sqrt(d))
+    G.assert_close(got, want, dtype, "f32", f"grouped decode Hq={Hq} Hkv={Hkv} d={d}")
+
+
+def test_grouped_decode_equals_repeated_caches_bitwise(fa):
+    # the grouped kernel does each head's arithmetic in the plain kernel's order
+    import torch
+    B, Hq, Hkv, L = 4, 14, 2, 3000
+    q, kc, vc, lens = make_gqa(B, Hq, Hkv, L, 64, "f16", 1700)
+    qd, kd, vd = (G.bits_to_device(x, "f16") for x in (q, kc, vc))
+    ld = torch.from_numpy(lens).cuda()
+    a = fa.decode(qd, kd, vd, ld, scale=0.125, num_splits=6)
+    b = fa.decode(qd, kd.repeat_interleave(7, dim=1).contiguous(),
+                  vd.repeat_interleave(7, dim=1).contiguous(), ld, scale=0.125, num_splits=6)
+    torch.cuda.synchronize()
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def test_grouped_decode_equals_one_row_chunk_prefill(fa):
+    import torch
+    B, Hq, Hkv, N, d = 2, 14, 2, 1500, 64
+    q = G.bits_to_device(inputs.normal_bits((B, Hq, N, d), 1800, "f16"), "f16")
+    k = G.bits_to_device(inputs.normal_bits((B, Hkv, N, d), 1801, "f16"), "f16")
+    v = G.bits_to_device(inputs.normal_bits((B, Hkv, N, d), 1802, "f16"), "f16")
+    for t in [0, 127, 128, 999, N - 1]:
+        lens = torch.full((B,), t + 1, dtype=torch.int32, device="cuda")
+        qt = q[:, :, t:t + 1].contiguous()
+        dec = fa.decode(qt, k, v, lens, scale=0.125, out_dtype=torch.float32)
+        pre = fa.prefill(qt, k[:, :, : t + 1].contiguous(), v[:, :, : t + 1].contiguous(), causal=True,
+                         scale=0.125, out_dtype=torch.float32)
+        torch.cuda.synchronize()
+        assert (dec - pre).abs().max().item() <= 2e-3, t
