@@ -37,6 +37,7 @@ _SIGNATURES = {
     "fa_prefill_gqa": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _f, _i, _i, _u, _vp]),
     "fa_prefill_varlen": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _i,
                                _f, _i, _i, _u, _vp]),
+    "fa_prefill_plan": (_i, [_i, _i, _i, _i, _i, _u, _i, _vp, _vp, _i]),
     "fa_decode": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _vp]),
     "fa_decode_ex": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _i, _i, _vp, _sz, _vp]),
     "fa_decode_gqa": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _i, _i, _vp, _sz,
@@ -109,6 +110,16 @@ def fa_prefill_varlen(q, k, v, out, cu_seqlens_q, cu_seqlens_k, B, Hq, Hkv, tota
     return load().fa_prefill_varlen(q, k, v, out, cu_seqlens_q, cu_seqlens_k, B, Hq, Hkv, total_q,
                                     total_k, max_seqlen_q, max_seqlen_k, d, int(causal),
                                     float(scale), in_dtype, out_dtype, flags, stream)
+
+
+def fa_prefill_plan(B, Hq, Nq, Nk, causal, flags=0, num_sms=0, max_items=192):
+    """The prefill schedule as (status, info[6], items[n][5]) -- host arithmetic only."""
+    info = (ctypes.c_longlong * 6)()
+    items = (ctypes.c_longlong * (5 * max_items))()
+    rc = load().fa_prefill_plan(B, Hq, Nq, Nk, int(causal), flags, num_sms, info, items, max_items)
+    n = int(info[5]) if rc == FA_OK else 0
+    rows = [tuple(int(items[5 * i + c]) for c in range(5)) for i in range(min(n, max_items))]
+    return rc, [int(x) for x in info], rows
 
 
 def fa_decode(q, k_cache, v_cache, seq_lens, out, B, H, max_len, d, scale, stream=0) -> int:

@@ -259,6 +259,22 @@ int fa_prefill_varlen(const void *q, const void *k, const void *v, void *out,
     return launch_prefill(a, dev, static_cast<cudaStream_t>(stream));
 }
 
+int fa_prefill_plan(int B, int Hq, int Nq, int Nk, int causal, unsigned flags, int num_sms,
+                    long long *info, long long *items, int max_items) {
+    if (!info) return FA_ERR_NULL;
+    if (B < 1 || Hq < 1 || Nq < 1 || Nk < 1 || max_items < 0) return FA_ERR_SHAPE;
+    if (static_cast<long long>(B) * Hq * ((static_cast<long long>(Nq) + 255) / 256) > INT_MAX)
+        return FA_ERR_SHAPE;
+    if (num_sms <= 0) {
+        DeviceInfo dev;
+        const int rc = current_device_info(&dev);
+        if (rc != FA_OK) return rc;
+        num_sms = dev.num_sms;
+    }
+    return plan_prefill(B, Hq, Nq, Nk, causal, (flags & FA_FLAG_NO_CAUSAL_SKIP) ? 1 : 0,
+                        schedule_of(flags), num_sms, info, items, max_items);
+}
+
 int fa_prefill_ex(const void *q, const void *k, const void *v, void *out, int B, int H, int N,
                   int d, int causal, float scale, fa_dtype in_dtype, fa_dtype out_dtype,
                   unsigned flags, void *stream) {
@@ -279,19 +295,18 @@ int fa_decode_chunk_len(int max_len, int num_splits) {
     return chunk;
 }
 
-int fa_decode_choose_splits(int B, int H, int max_len, int num_sms) {
-    if (B < 1 || H < 1 || max_len < 1) return -FA_ERR_SHAPE;
+namespace {
+// About `per_sm` CTAs per SM over the whole (b, row, chunk) grid, and no CTA
+// longer than 512 rows, so that ragged lengths do not leave a few long CTAs
+// running alone at the end.
+int choose_splits(int B, long long rows, int max_len, int num_sms, int per_sm) {
     if (num_sms <= 0) {
         DeviceInfo dev;
         int rc = current_device_info(&dev);
         if (rc != FA_OK) return -rc;
         num_sms = dev.num_sms;
     }
-    const long long bh = static_cast<long long>(B) * H;
-    // About two CTAs per SM over the whole (b, h, chunk) grid, and no CTA
-    // longer than 512 rows, so that ragged lengths do not leave a few long
-    // CTAs running alone at the end.
-    long long splits = ceil_div(2LL * num_sms, bh);
+    long long splits = ceil_div(static_cast<long long>(per_sm) * num_sms, B * rows);
     const long long max_splits = ceil_div(max_len, kDecodeRowAlign);
     const long long min_splits = ceil_div(max_len, kDecodeAutoMaxChunk);
     if (splits > max_splits) splits = max_splits;
@@ -299,13 +314,21 @@ int fa_decode_choose_splits(int B, int H, int max_len, int num_sms) {
     if (splits < 1) splits = 1;
     return decode_effective_splits(max_len, static_cast<int>(splits), nullptr);
 }
+}  // namespace
+
+int fa_decode_choose_splits(int B, int H, int max_len, int num_sms) {
+    if (B < 1 || H < 1 || max_len < 1) return -FA_ERR_SHAPE;
+    return choose_splits(B, H, max_len, num_sms, 2);
+}
 
 int fa_decode_gqa_choose_splits(int B, int Hq, int Hkv, int max_len, int num_sms) {
     if (B < 1 || Hq < 1 || Hkv < 1 || max_len < 1 || Hq % Hkv != 0) return -FA_ERR_SHAPE;
-    // the same rule over the CTA rows of the grouped kernel: one per slice of
-    // each cache head's group of query heads
+    if (Hq == Hkv) return choose_splits(B, Hq, max_len, num_sms, 2);
+    // A grouped CTA does up to 8 heads' arithmetic per row it loads, so it is
+    // latency- rather than bandwidth-bound: aim for about 5 CTAs per SM
+    // (measured best at B = 8 and 32 with 14 query over 2 cache heads).
     const long long rows = static_cast<long long>(Hkv) * decode_group_slices(Hq / Hkv);
-    return fa_decode_choose_splits(B, static_cast<int>(rows), max_len, num_sms);
+    return choose_splits(B, rows, max_len, num_sms, 5);
 }
 
 size_t fa_decode_workspace_bytes(int B, int H, int max_len, int d, int num_splits) {

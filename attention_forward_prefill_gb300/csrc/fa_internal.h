@@ -47,6 +47,10 @@ struct PrefillLaunch {
     int schedule;   // 0: choose, 1: unit by unit, 2: stream-K where possible
 };
 
+// Host-only: the schedule the launch would use (see fa_prefill_plan).
+int plan_prefill(int B, int Hq, int Nq, int Nk, int causal, int no_skip, int schedule, int num_sms,
+                 long long *info, long long *items, int max_items);
+
 // Validated arguments -> encode tensor maps, launch the persistent kernel.
 int launch_prefill(const PrefillLaunch &a, const DeviceInfo &dev, cudaStream_t stream);
 

@@ -101,7 +101,13 @@ struct Params {
     long long W;           // BH * HT
     float *ws_o;           // [gridDim.x][2 slots][256 rows][D]  unnormalised O
     float *ws_ml;          // [gridDim.x][2 slots][256 rows][2]  (m_ref, l)
-    int pre[kMaxPre + 1];  // steps of a head before query block qb
+};
+
+// Stream-K: key-tile steps of a head before query block qb.  A kernel argument
+// of its own, so that only this table is indexed at run time and every field
+// of Params stays a plain constant operand.
+struct StepTable {
+    int pre[kMaxPre + 1];
 };
 
 // One piece of work: unit u = (sequence b, query head h, query block) and its
@@ -157,7 +163,8 @@ __device__ __forceinline__ void load_seq(const Params &p, Work &w) {
     w.off = w.nk - w.nq;
 }
 
-__device__ __forceinline__ bool seg_next(const Params &p, SegCursor &c, Work &w) {
+__device__ __forceinline__ bool seg_next(const Params &p, const StepTable &tab, SegCursor &c,
+                                         Work &w) {
     int bh, qb;
     if (p.stream_k) {
         if (c.s >= c.s_end) return false;
@@ -166,11 +173,11 @@ __device__ __forceinline__ bool seg_next(const Params &p, SegCursor &c, Work &w)
         int lo = 0, hi = p.n_qb - 1;  // last qb with pre[qb] <= rem
         while (lo < hi) {
             const int mid = (lo + hi + 1) >> 1;
-            if (p.pre[mid] <= rem) lo = mid; else hi = mid - 1;
+            if (tab.pre[mid] <= rem) lo = mid; else hi = mid - 1;
         }
         qb = lo;
-        w.j0 = rem - p.pre[qb];
-        const int cost = p.pre[qb + 1] - p.pre[qb];
+        w.j0 = rem - tab.pre[qb];
+        const int cost = tab.pre[qb + 1] - tab.pre[qb];
         const long long left = c.s_end - c.s;
         w.j1 = static_cast<int>(left < cost - w.j0 ? w.j0 + left : cost);
         c.s += w.j1 - w.j0;
@@ -320,7 +327,8 @@ template <int D, bool BF16>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap map_q,
                    const __grid_constant__ CUtensorMap map_k,
-                   const __grid_constant__ CUtensorMap map_v, const __grid_constant__ Params p) {
+                   const __grid_constant__ CUtensorMap map_v, const Params p,
+                   const __grid_constant__ StepTable tab) {
     using L = Layout<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -384,7 +392,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             seg_begin(p, cur);
             Work w;
             const bool packed = p.cu_q != nullptr;
-            while (ok && seg_next(p, cur, w)) {
+            while (ok && seg_next(p, tab, cur, w)) {
                 if (w.j1 <= w.j0) continue;  // no key tiles: the softmax warps write zeros
                 // query tile t is loaded when it has key tiles in [j0, j1)
                 const bool need0 = min(w.n0, w.j1) > w.j0, need1 = min(w.n1, w.j1) > w.j0;
@@ -458,7 +466,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             SegCursor cur;
             seg_begin(p, cur);
             Work w;
-            while (ok && seg_next(p, cur, w)) {
+            while (ok && seg_next(p, tab, cur, w)) {
                 const int j0 = w.j0, j1 = w.j1;
                 if (j1 <= j0) continue;  // no key tiles: nothing to multiply
                 // key tiles [j0, e_t) for query tile t (empty when e_t <= j0)
@@ -556,7 +564,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         SegCursor cur;
         seg_begin(p, cur);
         Work w;
-        for (int seg = 0; ok && seg_next(p, cur, w); ++seg) {
+        for (int seg = 0; ok && seg_next(p, tab, cur, w); ++seg) {
             const int j0 = w.j0, j1 = w.j1;
             const int tile_row0 = w.q0 + t * kBlockM;
             const int row = tile_row0 + r;  // query index within the sequence
@@ -582,6 +590,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             // last visible key of this row (< 0: none)
             const int lim = p.causal ? min(row + w.off, w.nk - 1) : w.nk - 1;
             float m_ref = -INFINITY;
+            // -m_ref once a key has been seen; 0 before, so that the masked
+            // scores of a row with nothing visible yet still map to exactly 0
+            float neg_m = 0.f;
             float l = 0.f;
             for (int j = j0; j < ntile; ++j) {
                 if (!warp_wait(s_full + t, sc & 1, abort_flag)) { ok = false; break; }
@@ -608,16 +619,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();  // the masked branch above may diverge per lane
                 const bool need = m_tile > m_ref + kTau;
                 float alpha = 1.f;
-                if (need) {
+                if (need) {  // (m_tile is finite here)
                     alpha = ex2_approx(m_ref - m_tile);  // 0 on the first tile
                     l *= alpha;
                     m_ref = m_tile;
+                    neg_m = -m_tile;
                 }
-                // A row with nothing visible yet keeps m_ref = -inf: its masked
-                // scores still map to exactly 0 with a zero offset.
-                const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
                 const uint64_t c2 = f2_pack(cexp, cexp);
-                const uint64_t nm2 = f2_pack(-m_use, -m_use);
+                const uint64_t nm2 = f2_pack(neg_m, neg_m);
                 uint64_t sum2[4] = {0, 0, 0, 0};
                 // P in 32-key quarters: 16 packed registers per TMEM store.
 #pragma unroll
@@ -876,6 +885,103 @@ int host_kv_tiles(int causal, int no_skip, int nq, int nk, int row0) {
 constexpr long long kMergeCostSteps = 20;
 constexpr long long kCausalStepPct = 108;
 
+struct Plan {
+    int stream_k;
+    int grid;
+    int n_qb;
+    int HT;
+    long long W;
+    int n_split;
+    int4 item[kMaxSplit];         // (unit, first CTA, last CTA, unit's steps)
+    long long ustart[kMaxSplit];  // first step of the unit
+    StepTable tab;
+};
+
+// The schedule of a problem, from the shapes and the SM count only.  Unit by
+// unit (static round robin, heaviest causal blocks first) the busiest CTA does
+// `busiest` key-tile steps; cut into equal step ranges (stream-K) it does W / G
+// (8% dearer when causal) plus the merge cost.  Take the cheaper, unless
+// `schedule` forces one (1 units, 2 stream-K).  Stream-K needs every unit's
+// cost on the host (dense batches) and every query row to see a key.
+void make_plan(bool packed, int B, int Hq, int Nq, int Nk, int causal, int no_skip, int schedule,
+               int num_sms, Plan &pl) {
+    const int BH = B * Hq;
+    const int n_qb = (Nq + kRowsPerUnit - 1) / kRowsPerUnit;
+    const int n_units = BH * n_qb;
+    const int sms = num_sms < kMaxSplit ? num_sms : kMaxSplit;
+    pl.stream_k = 0;
+    pl.n_qb = n_qb;
+    pl.HT = 0;
+    pl.W = 0;
+    pl.n_split = 0;
+    pl.grid = n_units < num_sms ? n_units : num_sms;
+    pl.tab.pre[0] = 0;
+    const bool sk_ok = !packed && n_qb <= kMaxPre && n_units >= 2 && (!causal || no_skip || Nk >= Nq) &&
+                       schedule != 1;
+    if (!sk_ok) return;
+    int *pre = pl.tab.pre;
+    for (int qb = 0; qb < n_qb; ++qb) {
+        const int c0 = host_kv_tiles(causal, no_skip, Nq, Nk, qb * kRowsPerUnit);
+        const int c1 = host_kv_tiles(causal, no_skip, Nq, Nk, qb * kRowsPerUnit + kBlockM);
+        pre[qb + 1] = pre[qb] + std::max(c0, c1);
+    }
+    const int HT = pre[n_qb];
+    const long long W = static_cast<long long>(BH) * HT;
+    bool take = schedule == 2;
+    if (!take && n_units <= 65536) {
+        const int gu = std::min(std::min(n_units, num_sms), 1024);
+        long long busiest = 0;
+        if (causal) {
+            static thread_local long long load[1024];
+            for (int c = 0; c < gu; ++c) load[c] = 0;
+            for (int u = 0; u < n_units; ++u) {
+                const int qb = n_qb - 1 - u / BH;
+                load[u % gu] += pre[qb + 1] - pre[qb];
+            }
+            for (int c = 0; c < gu; ++c) busiest = std::max(busiest, load[c]);
+        } else {
+            busiest = static_cast<long long>((n_units + gu - 1) / gu) * pre[1];
+        }
+        const long long pct = causal ? kCausalStepPct : 100;
+        take = (W * pct + 100LL * sms - 1) / (100LL * sms) + kMergeCostSteps < busiest;
+    }
+    if (!take) return;
+    pl.stream_k = 1;
+    pl.HT = HT;
+    pl.W = W;
+    const int grid = sms;
+    pl.grid = grid;
+    auto first_step = [&](long long c) { return c * W / grid; };
+    auto cta_of = [&](long long step) {  // c with first_step(c) <= step < first_step(c + 1)
+        long long c = (step + 1) * grid / W;
+        if (c >= grid) c = grid - 1;
+        while (c > 0 && first_step(c) > step) --c;
+        while (c + 1 < grid && first_step(c + 1) <= step) ++c;
+        return static_cast<int>(c);
+    };
+    auto unit_of = [&](long long step, long long &ustart, int &cost) {
+        const long long bh = step / HT;
+        const int rem = static_cast<int>(step - bh * HT);
+        const int qb = static_cast<int>(std::upper_bound(pre, pre + n_qb + 1, rem) - pre) - 1;
+        ustart = bh * HT + pre[qb];
+        cost = pre[qb + 1] - pre[qb];
+        return static_cast<int>(bh * n_qb + qb);
+    };
+    int last_u = -1;
+    for (int c = 1; c < grid; ++c) {
+        const long long b = first_step(c);
+        if (b >= W) break;
+        long long us;
+        int cost;
+        const int u = unit_of(b, us, cost);
+        if (b == us || u == last_u) continue;  // a boundary between units, or done
+        last_u = u;
+        pl.item[pl.n_split] = make_int4(u, cta_of(us), cta_of(us + cost - 1), cost);
+        pl.ustart[pl.n_split] = us;
+        ++pl.n_split;
+    }
+}
+
 template <int D, bool BF16>
 int launch_d(const PrefillLaunch &a, const DeviceInfo &dev, cudaStream_t stream) {
     using L = Layout<D>;
@@ -902,7 +1008,7 @@ int launch_d(const PrefillLaunch &a, const DeviceInfo &dev, cudaStream_t stream)
     if (e != cudaSuccess) return cuda_fail(e);
     if (fattr.numRegs < kMinLaunchRegs) return cuda_fail(cudaErrorInvalidConfiguration);
 
-    static thread_local Params p;  // ~4 KB: keep it off the stack
+    Params p;
     p.out = a.out;
     p.cu_q = a.cu_q;
     p.cu_k = a.cu_k;
@@ -933,49 +1039,16 @@ int launch_d(const PrefillLaunch &a, const DeviceInfo &dev, cudaStream_t stream)
     p.ws_o = nullptr;
     p.ws_ml = nullptr;
 
-    // ---- schedule.  Unit by unit (static round robin, heaviest causal blocks
-    // first) the busiest CTA does `busiest` key-tile steps; cut into equal
-    // step ranges (stream-K) it does W / G (8% dearer when causal) plus the
-    // merge cost.  Take the cheaper, unless a flag forces one.  Stream-K needs every unit's cost on the
-    // host (dense batches) and every query row to see a key.
-    const int sms = dev.num_sms < kMaxSplit ? dev.num_sms : kMaxSplit;
-    const bool sk_ok = !packed && p.n_qb <= kMaxPre && p.n_units >= 2 &&
-                       (!p.causal || p.no_skip || a.Nk >= a.Nq) && a.schedule != 1;
-    if (sk_ok) {
-        p.pre[0] = 0;
-        for (int qb = 0; qb < p.n_qb; ++qb) {
-            const int c0 = host_kv_tiles(p.causal, p.no_skip, a.Nq, a.Nk, qb * kRowsPerUnit);
-            const int c1 = host_kv_tiles(p.causal, p.no_skip, a.Nq, a.Nk, qb * kRowsPerUnit + kBlockM);
-            p.pre[qb + 1] = p.pre[qb] + std::max(c0, c1);
-        }
-        p.HT = p.pre[p.n_qb];
-        p.W = static_cast<long long>(p.BH) * p.HT;
-        bool take = a.schedule == 2;
-        if (!take && p.n_units <= 65536) {
-            const int gu = std::min(std::min(p.n_units, dev.num_sms), 1024);
-            long long busiest = 0;
-            if (p.causal) {
-                static thread_local long long load[1024];
-                for (int c = 0; c < gu; ++c) load[c] = 0;
-                for (int u = 0; u < p.n_units; ++u) {
-                    const int qb = p.n_qb - 1 - u / p.BH;
-                    load[u % gu] += p.pre[qb + 1] - p.pre[qb];
-                }
-                for (int c = 0; c < gu; ++c) busiest = std::max(busiest, load[c]);
-            } else {
-                busiest = static_cast<long long>((p.n_units + gu - 1) / gu) * p.pre[1];
-            }
-            const long long pct = p.causal ? kCausalStepPct : 100;
-            take = (p.W * pct + 100LL * sms - 1) / (100LL * sms) + kMergeCostSteps < busiest;
-        }
-        p.stream_k = take ? 1 : 0;
-    }
-    int grid = p.n_units < dev.num_sms ? p.n_units : dev.num_sms;
+    static thread_local Plan pl;  // ~8 KB: keep it off the stack
+    make_plan(packed, a.B, a.Hq, a.Nq, a.Nk, p.causal, p.no_skip, a.schedule, dev.num_sms, pl);
+    p.stream_k = pl.stream_k;
+    p.HT = pl.HT;
+    p.W = pl.W;
+    const int grid = pl.grid;
     static thread_local FixupParams f;
     f.n_split = 0;
     void *ws = nullptr;
     if (p.stream_k) {
-        grid = sms;
         f.out = a.out;
         f.Hq = a.Hq;
         f.Nq = a.Nq;
@@ -986,34 +1059,10 @@ int launch_d(const PrefillLaunch &a, const DeviceInfo &dev, cudaStream_t stream)
         f.G = grid;
         f.W = p.W;
         f.out_dtype = a.out_dtype;
-        auto first_step = [&](long long c) { return c * p.W / grid; };
-        auto cta_of = [&](long long step) {  // c with first_step(c) <= step < first_step(c + 1)
-            long long c = (step + 1) * grid / p.W;
-            if (c >= grid) c = grid - 1;
-            while (c > 0 && first_step(c) > step) --c;
-            while (c + 1 < grid && first_step(c + 1) <= step) ++c;
-            return static_cast<int>(c);
-        };
-        auto unit_of = [&](long long step, long long &ustart, int &cost) {
-            const long long bh = step / p.HT;
-            const int rem = static_cast<int>(step - bh * p.HT);
-            const int qb = static_cast<int>(std::upper_bound(p.pre, p.pre + p.n_qb + 1, rem) - p.pre) - 1;
-            ustart = bh * p.HT + p.pre[qb];
-            cost = p.pre[qb + 1] - p.pre[qb];
-            return static_cast<int>(bh * p.n_qb + qb);
-        };
-        int last_u = -1;
-        for (int c = 1; c < grid; ++c) {
-            const long long b = first_step(c);
-            if (b >= p.W) break;
-            long long us;
-            int cost;
-            const int u = unit_of(b, us, cost);
-            if (b == us || u == last_u) continue;  // a boundary between units, or done
-            last_u = u;
-            f.item[f.n_split] = make_int4(u, cta_of(us), cta_of(us + cost - 1), cost);
-            f.ustart[f.n_split] = us;
-            ++f.n_split;
+        f.n_split = pl.n_split;
+        for (int i = 0; i < pl.n_split; ++i) {
+            f.item[i] = pl.item[i];
+            f.ustart[i] = pl.ustart[i];
         }
         if (f.n_split > 0) {
             const size_t o_bytes = static_cast<size_t>(grid) * 2 * kRowsPerUnit * D * sizeof(float);
@@ -1029,7 +1078,8 @@ int launch_d(const PrefillLaunch &a, const DeviceInfo &dev, cudaStream_t stream)
             f.ws_ml = p.ws_ml;
         }
     }
-    prefill_kernel<D, BF16><<<grid, kThreads, L::kSmemBytes, stream>>>(mq, mk, mv, p);
+    const StepTable &tab = pl.tab;
+    prefill_kernel<D, BF16><<<grid, kThreads, L::kSmemBytes, stream>>>(mq, mk, mv, p, tab);
     e = cudaGetLastError();
     if (e == cudaSuccess && f.n_split > 0) {
         cudaLaunchConfig_t cfg = {};
@@ -1053,6 +1103,27 @@ int launch_d(const PrefillLaunch &a, const DeviceInfo &dev, cudaStream_t stream)
 }
 
 }  // namespace
+
+int plan_prefill(int B, int Hq, int Nq, int Nk, int causal, int no_skip, int schedule, int num_sms,
+                 long long *info, long long *items, int max_items) {
+    static thread_local Plan pl;
+    make_plan(false, B, Hq, Nq, Nk, causal ? 1 : 0, no_skip, schedule, num_sms, pl);
+    info[0] = pl.stream_k;
+    info[1] = pl.grid;
+    info[2] = pl.W;
+    info[3] = pl.HT;
+    info[4] = pl.n_qb;
+    info[5] = pl.n_split;
+    if (items)
+        for (int i = 0; i < pl.n_split && i < max_items; ++i) {
+            items[i * 5 + 0] = pl.item[i].x;
+            items[i * 5 + 1] = pl.item[i].y;
+            items[i * 5 + 2] = pl.item[i].z;
+            items[i * 5 + 3] = pl.item[i].w;
+            items[i * 5 + 4] = pl.ustart[i];
+        }
+    return FA_OK;
+}
 
 int launch_prefill(const PrefillLaunch &a, const DeviceInfo &dev, cudaStream_t stream) {
     if (a.d == 64) return a.in_bf16 ? launch_d<64, true>(a, dev, stream) : launch_d<64, false>(a, dev, stream);

@@ -127,6 +127,24 @@ int fa_prefill_gqa(const void *q, const void *k, const void *v, void *out,
                    unsigned flags, void *stream);
 
 /*
+ * The schedule fa_prefill_gqa would use for a dense problem on num_sms SMs
+ * (num_sms <= 0: the current device's count).  Host arithmetic only, for
+ * tuning and tests; nothing runs on a device.
+ *   flags : FA_FLAG_NO_CAUSAL_SKIP and the FA_FLAG_SCHEDULE_* bits, as for
+ *           the prefill call
+ *   info  : 6 values: stream-K (1) or unit by unit (0), CTAs launched, key-tile
+ *           steps W of all units, steps per (sequence, head), 256-row query
+ *           blocks per head, units cut between CTAs
+ *   items : NULL or room for max_items rows of 5 values, one per cut unit:
+ *           unit, first CTA, last CTA, the unit's steps, the unit's first step.
+ *           Units number (b * Hq + h) * blocks + block; CTA c owns steps
+ *           [c * W / CTAs, (c + 1) * W / CTAs).
+ * Returns FA_OK, FA_ERR_NULL (info), FA_ERR_SHAPE (a size < 1).
+ */
+int fa_prefill_plan(int B, int Hq, int Nq, int Nk, int causal, unsigned flags,
+                    int num_sms, long long *info, long long *items, int max_items);
+
+/*
  * Prefill of a packed batch of variable-length sequences.  Sequence b owns
  * query tokens [cu_seqlens_q[b], cu_seqlens_q[b+1]) and key/value tokens
  * [cu_seqlens_k[b], cu_seqlens_k[b+1]); sequences never see each other.

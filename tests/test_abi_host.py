@@ -124,7 +124,13 @@ def test_grouped_decode_argument_errors(lib):
 def test_grouped_split_choice(lib, B, Hq, Hkv, L):
     s = binding.fa_decode_gqa_choose_splits(B, Hq, Hkv, L, 152)
     rows = Hkv * ((Hq // Hkv + 7) // 8)
-    assert s == binding.fa_decode_choose_splits(B, rows, L, 152)
+    if Hq == Hkv:
+        assert s == binding.fa_decode_choose_splits(B, Hq, L, 152)
+    else:   # about 5 CTAs per SM, chunks of 64..512 rows, rounded to 64-row chunks
+        cdiv = lambda a, b: -(-a // b)
+        want = min(max(cdiv(5 * 152, B * rows), cdiv(L, 512)), cdiv(L, 64))
+        chunk = cdiv(cdiv(L, want), 64) * 64
+        assert s == cdiv(L, chunk)
     assert 1 <= s <= (L + 63) // 64
     assert binding.fa_decode_gqa_choose_splits(B, Hq, 3, L, 152) < 0 or Hq % 3 == 0
 
