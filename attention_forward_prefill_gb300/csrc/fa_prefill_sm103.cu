@@ -64,12 +64,20 @@ struct Layout {
     static constexpr int kQOff = 0;
     static constexpr int kRingOff = 2 * kTileBytes;
     static constexpr int kBarOff = kRingOff + kStages * kTileBytes;
-    // q_full, q_empty, s_full[2], p_full[2], o_done[2], drain, kv_full[S], kv_empty[S]
-    static constexpr int kNumBars = 9 + 2 * kStages;
+    // q_full, q_empty, s_full[2], p_full[2], o_done[2], drain, s_free[2], pv_done[2],
+    // kv_full[S], kv_empty[S]
+    static constexpr int kNumBars = 13 + 2 * kStages;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
     static constexpr int kSmemBytes = kMiscOff + 16 + 1024;  // + alignment slack
     static constexpr uint32_t kSCol0 = 0, kSCol1 = 128;
     static constexpr uint32_t kOCol0 = 256, kOCol1 = 256 + D;
+    // d = 64 leaves room for P beside S (columns 384..511): the softmax then
+    // frees S as soon as it has loaded it, and the next Q K^T overlaps the
+    // exponentials.  At d = 128, P overwrites the first 64 columns of S.
+    static constexpr bool kSepP = (D == 64);
+    static constexpr uint32_t kPCol0 = kSepP ? 256 + 2 * D : kSCol0;
+    static constexpr uint32_t kPCol1 = kSepP ? 256 + 2 * D + 64 : kSCol1;
+    static_assert(!kSepP || kPCol1 + 64 <= 512, "TMEM columns");
 };
 
 constexpr int kMaxPre = 1024;  // stream-K: query blocks per head with a step table
@@ -340,8 +348,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *p_full = bars + 4;   // [2]
     uint64_t *o_done = bars + 6;   // [2]
     uint64_t *drain = bars + 8;
-    uint64_t *kv_full = bars + 9;
-    uint64_t *kv_empty = bars + 9 + L::kStages;
+    uint64_t *s_free = bars + 9;    // [2] (separate-P mode)
+    uint64_t *pv_done = bars + 11;  // [2] (separate-P mode)
+    uint64_t *kv_full = bars + 13;
+    uint64_t *kv_empty = bars + 13 + L::kStages;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kMiscOff);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kMiscOff + 4);
 
@@ -355,6 +365,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(s_full + t, 1);
             mbar_init(p_full + t, 4);  // one arrival per softmax warp
             mbar_init(o_done + t, 1);
+            mbar_init(s_free + t, 4);  // one arrival per softmax warp
+            mbar_init(pv_done + t, 1);
         }
         mbar_init(drain, 1);
         for (int s = 0; s < L::kStages; ++s) {
@@ -461,7 +473,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t ring_addr = smem_u32(smem + L::kRingOff);
             const uint32_t s_tmem0 = tmem + L::kSCol0, s_tmem1 = tmem + L::kSCol1;
             const uint32_t o_tmem0 = tmem + L::kOCol0, o_tmem1 = tmem + L::kOCol1;
+            const uint32_t p_tmem0 = tmem + L::kPCol0, p_tmem1 = tmem + L::kPCol1;
             uint32_t qc = 0, rc = 0, pc0 = 0, pc1 = 0;
+            uint32_t qk0 = 0, qk1 = 0;  // Q K^T products issued per tile (separate-P mode)
             bool ok = true;
             SegCursor cur;
             seg_begin(p, cur);
@@ -482,13 +496,37 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     tc_fence_after();
                     const uint64_t k_desc = sdesc_sw128(ring_addr + slot * L::kTileBytes, 16, 1024);
-                    if (n0 > j0) {
-                        issue_qk<D>(s_tmem0, q_desc0, k_desc, idesc_qk);
-                        umma_commit(s_full + 0);
-                    }
-                    if (n1 > j0) {
-                        issue_qk<D>(s_tmem1, q_desc1, k_desc, idesc_qk);
-                        umma_commit(s_full + 1);
+                    if constexpr (L::kSepP) {
+                        // S_t is free once the softmax has loaded the previous one
+                        if (n0 > j0) {
+                            if (qk0 > 0 && !mbar_wait(s_free + 0, (qk0 - 1) & 1, abort_flag, kWatchdogNs)) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
+                            issue_qk<D>(s_tmem0, q_desc0, k_desc, idesc_qk);
+                            umma_commit(s_full + 0);
+                            ++qk0;
+                        }
+                        if (n1 > j0) {
+                            if (qk1 > 0 && !mbar_wait(s_free + 1, (qk1 - 1) & 1, abort_flag, kWatchdogNs)) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
+                            issue_qk<D>(s_tmem1, q_desc1, k_desc, idesc_qk);
+                            umma_commit(s_full + 1);
+                            ++qk1;
+                        }
+                    } else {
+                        if (n0 > j0) {
+                            issue_qk<D>(s_tmem0, q_desc0, k_desc, idesc_qk);
+                            umma_commit(s_full + 0);
+                        }
+                        if (n1 > j0) {
+                            issue_qk<D>(s_tmem1, q_desc1, k_desc, idesc_qk);
+                            umma_commit(s_full + 1);
+                        }
                     }
                     umma_commit(kv_empty + slot);
                     ++rc;
@@ -530,9 +568,42 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                         return true;
                     };
-                    ok = tile_step(n0, p_full + 0, pc0, s_tmem0, o_tmem0, q_desc0, s_full + 0, o_done + 0) &&
-                         tile_step(n1, p_full + 1, pc1, s_tmem1, o_tmem1, q_desc1, s_full + 1,
-                                   o_done + 1);
+                    // Separate-P step: S_t = Q_t K_{j+1}^T as soon as the softmax has
+                    // loaded S_t(j), then O_t (+)= P_t V_j once P_t(j) is written.
+                    auto tile_step_sep = [&](int nt, uint64_t *pf, uint32_t &pc, uint64_t *sfree,
+                                             uint32_t &qk, uint32_t s_t, uint32_t p_t, uint32_t o_t,
+                                             uint64_t q_desc, uint64_t *sf, uint64_t *pvd) {
+                        if (j >= nt) return true;
+                        if (j + 1 < nt) {
+                            if (!mbar_wait(sfree, (qk - 1) & 1, abort_flag, kWatchdogNs)) return false;
+                            if (!k_ready) {
+                                if (!mbar_wait(kv_full + slot_k, k_parity, abort_flag, kWatchdogNs))
+                                    return false;
+                                k_ready = true;
+                            }
+                            tc_fence_after();
+                            issue_qk<D>(s_t, q_desc, k_desc, idesc_qk);
+                            umma_commit(sf);
+                            ++qk;
+                        }
+                        if (!mbar_wait(pf, pc & 1, abort_flag, kWatchdogNs)) return false;
+                        ++pc;
+                        tc_fence_after();
+                        issue_pv<D>(o_t, p_t, v_desc, idesc_pv, j > j0);
+                        umma_commit(pvd);
+                        return true;
+                    };
+                    if constexpr (L::kSepP) {
+                        ok = tile_step_sep(n0, p_full + 0, pc0, s_free + 0, qk0, s_tmem0, p_tmem0, o_tmem0,
+                                           q_desc0, s_full + 0, pv_done + 0) &&
+                             tile_step_sep(n1, p_full + 1, pc1, s_free + 1, qk1, s_tmem1, p_tmem1, o_tmem1,
+                                           q_desc1, s_full + 1, pv_done + 1);
+                    } else {
+                        ok = tile_step(n0, p_full + 0, pc0, s_tmem0, o_tmem0, q_desc0, s_full + 0,
+                                       o_done + 0) &&
+                             tile_step(n1, p_full + 1, pc1, s_tmem1, o_tmem1, q_desc1, s_full + 1,
+                                       o_done + 1);
+                    }
                     if (!ok) break;
                     umma_commit(kv_empty + slot_v);
                     if (j + 1 < j1) {
@@ -557,9 +628,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
         const uint32_t s_addr = tmem + lane_off + (t ? L::kSCol1 : L::kSCol0);
         const uint32_t o_addr = tmem + lane_off + (t ? L::kOCol1 : L::kOCol0);
+        const uint32_t p_addr = tmem + lane_off + (t ? L::kPCol1 : L::kPCol0);
         const float cexp = p.scale_log2;
         const int osize = p.out_dtype == FA_F32 ? 4 : 2;
-        uint32_t sc = 0, oc = 0;
+        uint32_t sc = 0, oc = 0, pvc = 0;
         bool ok = true;
         SegCursor cur;
         seg_begin(p, cur);
@@ -604,6 +676,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_ld_wait();
 #pragma unroll
                 for (int q = 0; q < 4; ++q) reg_fence32(sr[q]);
+                if constexpr (L::kSepP) {
+                    // S_t is in registers: the next Q K^T may overwrite it now.
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(s_free + t);
+                }
 
                 const int cmax = lim - j * kBlockN;  // columns > cmax are masked
                 if (cmax < kBlockN - 1) {
@@ -625,6 +703,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     m_ref = m_tile;
                     neg_m = -m_tile;
                 }
+                if constexpr (L::kSepP) {
+                    // P_t(j-1) and O_t must be done with before P_t(j) and a rescale
+                    if (j > j0) {
+                        if (!warp_wait(pv_done + t, pvc & 1, abort_flag)) { ok = false; break; }
+                        ++pvc;
+                        tc_fence_after();
+                    }
+                }
                 const uint64_t c2 = f2_pack(cexp, cexp);
                 const uint64_t nm2 = f2_pack(neg_m, neg_m);
                 uint64_t sum2[4] = {0, 0, 0, 0};
@@ -642,7 +728,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         // so a row dominated by one key returns that value row.
                         sum2[c2i & 3] = fadd2(sum2[c2i & 3], unpack2<BF16>(pk[c2i]));
                     }
-                    tmem_st16(s_addr + q * 16, pk);
+                    tmem_st16(p_addr + q * 16, pk);
                 }
                 const uint64_t s01 = fadd2(sum2[0], sum2[1]), s23 = fadd2(sum2[2], sum2[3]);
                 const uint64_t st = fadd2(s01, s23);
@@ -672,8 +758,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (!ok) break;
             // ---- epilogue: O / l -> out
-            if (!warp_wait(o_done + t, oc & 1, abort_flag)) { ok = false; break; }
-            ++oc;
+            if constexpr (L::kSepP) {
+                if (!warp_wait(pv_done + t, pvc & 1, abort_flag)) { ok = false; break; }
+                ++pvc;
+            } else {
+                if (!warp_wait(o_done + t, oc & 1, abort_flag)) { ok = false; break; }
+                ++oc;
+            }
             tc_fence_after();
             if (partial) {
                 // Part of a unit: keep O unnormalised with its (m_ref, l) for the
