@@ -143,3 +143,91 @@ int oracle_decode_head(const double *q, const double *k_cache,
     free(s);
     return 0;
 }
+
+/*
+ * Log-sum-exp of every visible score row (the quantity a backward pass needs
+ * to recompute the weights): lse_i = log sum_{j visible} exp(s_ij), with
+ * s_ij = scale * q_i . k_j and the causal visibility of oracle_attention_head.
+ * A row with no visible key gets -INFINITY.
+ */
+int oracle_lse_head(const double *q, const double *k, long n_q, long n_k, int d, int causal,
+                    double scale, double *lse) {
+    if (d <= 0 || n_q < 0 || n_k < 0) return -1;
+    double *s = (double *)malloc(sizeof(double) * (size_t)(n_k > 0 ? n_k : 1));
+    if (!s) return -1;
+    for (long i = 0; i < n_q; ++i) {
+        long n_vis = n_k;
+        if (causal) {
+            n_vis = i + 1 + (n_k - n_q);
+            if (n_vis > n_k) n_vis = n_k;
+            if (n_vis < 0) n_vis = 0;
+        }
+        if (n_vis == 0) {
+            lse[i] = -INFINITY;
+            continue;
+        }
+        score_row(q + i * (long)d, k, n_vis, d, scale, s);
+        double m = s[0];
+        for (long j = 1; j < n_vis; ++j)
+            if (s[j] > m) m = s[j];
+        double z = 0.0;
+        for (long j = 0; j < n_vis; ++j) z += exp(s[j] - m);
+        lse[i] = m + log(z);
+    }
+    free(s);
+    return 0;
+}
+
+/*
+ * Gradients of one head of O = softmax(scale * Q K^T [mask]) V with respect to
+ * Q, K and V, given dO (the backward pass that the flash-attention-cuda README
+ * lists under "Future work").  The chain rule through the definition:
+ *   P_ij   = softmax weights (as in oracle_attention_head; 0 where masked)
+ *   dV_j   = sum_i P_ij dO_i
+ *   dP_ij  = dO_i . V_j
+ *   dS_ij  = P_ij (dP_ij - sum_k P_ik dP_ik)        (softmax Jacobian)
+ *   dQ_i   = scale * sum_j dS_ij K_j
+ *   dK_j   = scale * sum_i dS_ij Q_i
+ * Explicit n_q x n_k tables, fp64, index order.  Rows with no visible key
+ * contribute nothing.
+ */
+int oracle_backward_head(const double *q, const double *k, const double *v, const double *dout,
+                         long n_q, long n_k, int d, int causal, double scale, double *dq, double *dk,
+                         double *dv) {
+    if (d <= 0 || n_q < 0 || n_k < 0) return -1;
+    double *p = (double *)malloc(sizeof(double) * (size_t)(n_k > 0 ? n_k : 1));
+    double *dp = (double *)malloc(sizeof(double) * (size_t)(n_k > 0 ? n_k : 1));
+    if (!p || !dp) { free(p); free(dp); return -1; }
+    for (long x = 0; x < n_q * (long)d; ++x) dq[x] = 0.0;
+    for (long x = 0; x < n_k * (long)d; ++x) { dk[x] = 0.0; dv[x] = 0.0; }
+    for (long i = 0; i < n_q; ++i) {
+        long n_vis = n_k;
+        if (causal) {
+            n_vis = i + 1 + (n_k - n_q);
+            if (n_vis > n_k) n_vis = n_k;
+            if (n_vis < 0) n_vis = 0;
+        }
+        if (n_vis == 0) continue;
+        const double *qi = q + i * (long)d, *doi = dout + i * (long)d;
+        score_row(qi, k, n_vis, d, scale, p);
+        softmax_inplace(p, n_vis);
+        double rowdot = 0.0;
+        for (long j = 0; j < n_vis; ++j) {
+            double t = 0.0;
+            for (int c = 0; c < d; ++c) t += doi[c] * v[j * (long)d + c];
+            dp[j] = t;
+            rowdot += p[j] * t;
+        }
+        for (long j = 0; j < n_vis; ++j) {
+            const double ds = p[j] * (dp[j] - rowdot);
+            for (int c = 0; c < d; ++c) {
+                dv[j * (long)d + c] += p[j] * doi[c];
+                dq[i * (long)d + c] += scale * ds * k[j * (long)d + c];
+                dk[j * (long)d + c] += scale * ds * qi[c];
+            }
+        }
+    }
+    free(p);
+    free(dp);
+    return 0;
+}

@@ -62,6 +62,13 @@ def _load():
                 dp, dp, dp, ctypes.c_long, ctypes.c_long, ctypes.c_int,
                 ctypes.c_double, dp]
             lib.oracle_decode_head.restype = ctypes.c_int
+            lib.oracle_lse_head.argtypes = [dp, dp, ctypes.c_long, ctypes.c_long, ctypes.c_int,
+                                            ctypes.c_int, ctypes.c_double, dp]
+            lib.oracle_lse_head.restype = ctypes.c_int
+            lib.oracle_backward_head.argtypes = [dp, dp, dp, dp, ctypes.c_long, ctypes.c_long,
+                                                 ctypes.c_int, ctypes.c_int, ctypes.c_double,
+                                                 dp, dp, dp]
+            lib.oracle_backward_head.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -246,3 +253,63 @@ def decode(q: np.ndarray, k_cache: np.ndarray, v_cache: np.ndarray,
         for bh in range(B * H):
             one(bh)
     return out
+
+
+# --------------------------------------------------------------------------
+# Training: the log-sum-exp of the forward, and the backward pass.
+# --------------------------------------------------------------------------
+def attention_lse(q: np.ndarray, k: np.ndarray, causal: bool, scale: float) -> np.ndarray:
+    """lse[b, h, i] = log sum_{j visible} exp(scale * q_i . k_j); -inf for an empty row.
+
+    q: [B, H, Nq, d]; k: [B, H, Nk, d].
+    """
+    q = np.ascontiguousarray(q, dtype=np.float64)
+    k = np.ascontiguousarray(k, dtype=np.float64)
+    B, H, n_q, d = q.shape
+    n_k = k.shape[2]
+    out = np.zeros((B, H, n_q), dtype=np.float64)
+    lib = _load()
+    for b in range(B):
+        for h in range(H):
+            o = np.zeros(n_q, dtype=np.float64)
+            if lib.oracle_lse_head(_dptr(q[b, h]), _dptr(k[b, h]), n_q, n_k, d,
+                                   int(bool(causal)), float(scale), _dptr(o)) != 0:
+                raise RuntimeError("oracle_lse_head failed")
+            out[b, h] = o
+    return out
+
+
+def attention_backward(q: np.ndarray, k: np.ndarray, v: np.ndarray, dout: np.ndarray,
+                       causal: bool, scale: float, threads: int = 1):
+    """(dQ, dK, dV) of O = softmax(scale Q K^T [mask]) V for the upstream gradient dO.
+
+    q, dout: [B, H, Nq, d]; k, v: [B, H, Nk, d] (float64).  Causal alignment as
+    in ``attention``.  Heads are independent and may be spread over threads.
+    """
+    q = np.ascontiguousarray(q, dtype=np.float64)
+    k = np.ascontiguousarray(k, dtype=np.float64)
+    v = np.ascontiguousarray(v, dtype=np.float64)
+    dout = np.ascontiguousarray(dout, dtype=np.float64)
+    B, H, n_q, d = q.shape
+    n_k = k.shape[2]
+    dq = np.zeros_like(q)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    lib = _load()
+
+    def one(bh):
+        b, h = divmod(bh, H)
+        a, bb, c = np.zeros((n_q, d)), np.zeros((n_k, d)), np.zeros((n_k, d))
+        if lib.oracle_backward_head(_dptr(q[b, h]), _dptr(k[b, h]), _dptr(v[b, h]),
+                                    _dptr(dout[b, h]), n_q, n_k, d, int(bool(causal)),
+                                    float(scale), _dptr(a), _dptr(bb), _dptr(c)) != 0:
+            raise RuntimeError("oracle_backward_head failed")
+        dq[b, h], dk[b, h], dv[b, h] = a, bb, c
+
+    if threads > 1 and B * H > 1:
+        with ThreadPoolExecutor(max_workers=threads) as ex:
+            list(ex.map(one, range(B * H)))
+    else:
+        for bh in range(B * H):
+            one(bh)
+    return dq, dk, dv
