@@ -37,6 +37,10 @@ _SIGNATURES = {
     "fa_prefill_gqa": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _f, _i, _i, _u, _vp]),
     "fa_prefill_varlen": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _i,
                                _f, _i, _i, _u, _vp]),
+    "fa_prefill_lse": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _f, _i, _i, _u,
+                            _vp]),
+    "fa_prefill_backward": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i,
+                                 _f, _i, _i, _vp]),
     "fa_prefill_plan": (_i, [_i, _i, _i, _i, _i, _u, _i, _vp, _vp, _i]),
     "fa_decode": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _vp]),
     "fa_decode_ex": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _i, _i, _vp, _sz, _vp]),
@@ -110,6 +114,18 @@ def fa_prefill_varlen(q, k, v, out, cu_seqlens_q, cu_seqlens_k, B, Hq, Hkv, tota
     return load().fa_prefill_varlen(q, k, v, out, cu_seqlens_q, cu_seqlens_k, B, Hq, Hkv, total_q,
                                     total_k, max_seqlen_q, max_seqlen_k, d, int(causal),
                                     float(scale), in_dtype, out_dtype, flags, stream)
+
+
+def fa_prefill_lse(q, k, v, out, lse, B, Hq, Hkv, Nq, Nk, d, causal, scale, in_dtype, out_dtype,
+                   flags=0, stream=0) -> int:
+    return load().fa_prefill_lse(q, k, v, out, lse, B, Hq, Hkv, Nq, Nk, d, int(causal),
+                                 float(scale), in_dtype, out_dtype, flags, stream)
+
+
+def fa_prefill_backward(q, k, v, out, dout, lse, dq, dk, dv, B, H, N, d, causal, scale, in_dtype,
+                        grad_dtype, stream=0) -> int:
+    return load().fa_prefill_backward(q, k, v, out, dout, lse, dq, dk, dv, B, H, N, d, int(causal),
+                                      float(scale), in_dtype, grad_dtype, stream)
 
 
 def fa_prefill_plan(B, Hq, Nq, Nk, causal, flags=0, num_sms=0, max_items=192):
@@ -256,6 +272,48 @@ def prefill(q, k, v, causal: bool = False, scale: float | None = None, out_dtype
     if rc != FA_OK:
         raise FaError(rc, "fa_prefill_gqa")
     return out
+
+
+def prefill_with_lse(q, k, v, causal: bool = False, scale: float | None = None, flags: int = 0):
+    """Forward for training: returns (out, lse) with out in q's dtype and lse
+    fp32 [B, Hq, Nq] (natural-log row log-sum-exp of the visible scores)."""
+    torch = _torch()
+    B, Hq, Nq, d = q.shape
+    _check_cuda("q", q)
+    _check_cuda("k", k, None, q.dtype)
+    Hkv, Nk = k.shape[1], k.shape[2]
+    _check_cuda("v", v, k.shape, q.dtype)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    out = torch.empty(q.shape, dtype=q.dtype, device=q.device)
+    lse = torch.empty((B, Hq, Nq), dtype=torch.float32, device=q.device)
+    rc = fa_prefill_lse(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(), B,
+                        Hq, Hkv, Nq, Nk, d, causal, scale, dtype_code(q.dtype), dtype_code(q.dtype),
+                        flags, _stream_handle(q.device))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_prefill_lse")
+    return out, lse
+
+
+def prefill_backward(q, k, v, out, dout, lse, causal: bool = False, scale: float | None = None,
+                     grad_dtype=None):
+    """(dq, dk, dv) for square multi-head prefill, from the forward's out and lse."""
+    torch = _torch()
+    B, H, N, d = q.shape
+    for name, t in (("q", q), ("k", k), ("v", v), ("out", out), ("dout", dout)):
+        _check_cuda(name, t, q.shape, q.dtype)
+    _check_cuda("lse", lse, (B, H, N), torch.float32)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    grad_dtype = q.dtype if grad_dtype is None else grad_dtype
+    dq, dk, dv = (torch.empty(q.shape, dtype=grad_dtype, device=q.device) for _ in range(3))
+    rc = fa_prefill_backward(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                             dout.data_ptr(), lse.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                             dv.data_ptr(), B, H, N, d, causal, scale, dtype_code(q.dtype),
+                             dtype_code(grad_dtype), _stream_handle(q.device))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_prefill_backward")
+    return dq, dk, dv
 
 
 def prefill_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, max_seqlen_k: int,

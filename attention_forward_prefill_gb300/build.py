@@ -17,7 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_NAME = "libfa_gb300.so"
 LIB_PATH = os.path.join(HERE, LIB_NAME)
-SOURCES = ["fa_api.cu", "fa_prefill_sm103.cu", "fa_decode_sm103.cu"]
+SOURCES = ["fa_api.cu", "fa_prefill_sm103.cu", "fa_decode_sm103.cu", "fa_backward_sm103.cu"]
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
           "-Xcompiler", "-Wall"]

@@ -143,9 +143,10 @@ int fa_last_cuda_error(void) { return t_last_cuda_error; }
 
 int fa_device_status(int reset) {
     if (cudaDeviceSynchronize() != cudaSuccess) return -1;
-    const int a = read_prefill_status(reset), b = read_decode_status(reset);
-    if (a < 0 || b < 0) return -1;
-    return a ? a : b;
+    const int a = read_prefill_status(reset), b = read_decode_status(reset),
+              c = read_backward_status(reset);
+    if (a < 0 || b < 0 || c < 0) return -1;
+    return a ? a : (b ? b : c);
 }
 
 namespace {
@@ -167,10 +168,11 @@ int schedule_of(unsigned flags) {
 }
 }  // namespace
 
-int fa_prefill_gqa(const void *q, const void *k, const void *v, void *out, int B, int Hq, int Hkv,
-                   int Nq, int Nk, int d, int causal, float scale, fa_dtype in_dtype,
-                   fa_dtype out_dtype, unsigned flags, void *stream) {
+int fa_prefill_lse(const void *q, const void *k, const void *v, void *out, float *lse, int B,
+                   int Hq, int Hkv, int Nq, int Nk, int d, int causal, float scale,
+                   fa_dtype in_dtype, fa_dtype out_dtype, unsigned flags, void *stream) {
     int rc = prefill_common_checks(q, k, v, out, d, in_dtype, out_dtype, scale);
+    if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return FA_ERR_ALIGN;
     if (rc != FA_OK) return rc;
     if (B < 1 || Hq < 1 || Hkv < 1 || Nq < 1 || Nk < 1) return FA_ERR_SHAPE;
     if (Hq % Hkv != 0) return FA_ERR_SHAPE;
@@ -182,6 +184,12 @@ int fa_prefill_gqa(const void *q, const void *k, const void *v, void *out, int B
     if (overlaps(out, out_bytes, q, q_bytes) || overlaps(out, out_bytes, k, kv_bytes) ||
         overlaps(out, out_bytes, v, kv_bytes))
         return FA_ERR_ALIAS;
+    if (lse) {
+        const size_t lse_bytes = static_cast<size_t>(B) * Hq * Nq * 4;
+        if (overlaps(lse, lse_bytes, out, out_bytes) || overlaps(lse, lse_bytes, q, q_bytes) ||
+            overlaps(lse, lse_bytes, k, kv_bytes) || overlaps(lse, lse_bytes, v, kv_bytes))
+            return FA_ERR_ALIAS;
+    }
     DeviceInfo dev;
     rc = current_device_info(&dev);
     if (rc != FA_OK) return rc;
@@ -190,6 +198,7 @@ int fa_prefill_gqa(const void *q, const void *k, const void *v, void *out, int B
     a.k = k;
     a.v = v;
     a.out = out;
+    a.lse = lse;
     a.cu_q = nullptr;
     a.cu_k = nullptr;
     a.B = B;
@@ -207,6 +216,13 @@ int fa_prefill_gqa(const void *q, const void *k, const void *v, void *out, int B
     a.out_dtype = out_dtype;
     a.schedule = schedule_of(flags);
     return launch_prefill(a, dev, static_cast<cudaStream_t>(stream));
+}
+
+int fa_prefill_gqa(const void *q, const void *k, const void *v, void *out, int B, int Hq, int Hkv,
+                   int Nq, int Nk, int d, int causal, float scale, fa_dtype in_dtype,
+                   fa_dtype out_dtype, unsigned flags, void *stream) {
+    return fa_prefill_lse(q, k, v, out, nullptr, B, Hq, Hkv, Nq, Nk, d, causal, scale, in_dtype,
+                          out_dtype, flags, stream);
 }
 
 int fa_prefill_varlen(const void *q, const void *k, const void *v, void *out,
@@ -240,6 +256,7 @@ int fa_prefill_varlen(const void *q, const void *k, const void *v, void *out,
     a.k = k;
     a.v = v;
     a.out = out;
+    a.lse = nullptr;
     a.cu_q = cu_seqlens_q;
     a.cu_k = cu_seqlens_k;
     a.B = B;
@@ -273,6 +290,55 @@ int fa_prefill_plan(int B, int Hq, int Nq, int Nk, int causal, unsigned flags, i
     }
     return plan_prefill(B, Hq, Nq, Nk, causal, (flags & FA_FLAG_NO_CAUSAL_SKIP) ? 1 : 0,
                         schedule_of(flags), num_sms, info, items, max_items);
+}
+
+int fa_prefill_backward(const void *q, const void *k, const void *v, const void *out,
+                        const void *dout, const float *lse, void *dq, void *dk, void *dv, int B,
+                        int H, int N, int d, int causal, float scale, fa_dtype in_dtype,
+                        fa_dtype grad_dtype, void *stream) {
+    if (!q || !k || !v || !out || !dout || !lse || !dq || !dk || !dv) return FA_ERR_NULL;
+    if (B < 1 || H < 1 || N < 1 || static_cast<long long>(B) * H * N > INT_MAX) return FA_ERR_SHAPE;
+    if (d != 64 && d != 128) return FA_ERR_HEAD_DIM;
+    if (in_dtype != FA_F16 && in_dtype != FA_BF16) return FA_ERR_DTYPE;
+    if (grad_dtype != FA_F16 && grad_dtype != FA_BF16 && grad_dtype != FA_F32) return FA_ERR_DTYPE;
+    if (misaligned(q) || misaligned(k) || misaligned(v) || misaligned(out) || misaligned(dout) ||
+        misaligned(dq) || misaligned(dk) || misaligned(dv) || (reinterpret_cast<uintptr_t>(lse) & 3u))
+        return FA_ERR_ALIGN;
+    if (!std::isfinite(scale)) return FA_ERR_SCALE;
+    const size_t in_bytes = static_cast<size_t>(B) * H * N * d * 2;
+    const size_t g_bytes = static_cast<size_t>(B) * H * N * d * dtype_size(grad_dtype);
+    const size_t lse_bytes = static_cast<size_t>(B) * H * N * 4;
+    const void *ins[6] = {q, k, v, out, dout, lse};
+    const size_t in_sz[6] = {in_bytes, in_bytes, in_bytes, in_bytes, in_bytes, lse_bytes};
+    void *gs[3] = {dq, dk, dv};
+    for (int g = 0; g < 3; ++g) {
+        for (int i = 0; i < 6; ++i)
+            if (overlaps(gs[g], g_bytes, ins[i], in_sz[i])) return FA_ERR_ALIAS;
+        for (int h = g + 1; h < 3; ++h)
+            if (overlaps(gs[g], g_bytes, gs[h], g_bytes)) return FA_ERR_ALIAS;
+    }
+    DeviceInfo dev;
+    int rc = current_device_info(&dev);
+    if (rc != FA_OK) return rc;
+    BackwardLaunch a;
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.out = out;
+    a.dout = dout;
+    a.lse = lse;
+    a.dq = dq;
+    a.dk = dk;
+    a.dv = dv;
+    a.B = B;
+    a.H = H;
+    a.N = N;
+    a.d = d;
+    a.causal = causal ? 1 : 0;
+    a.scale = scale;
+    a.in_bf16 = in_dtype == FA_BF16 ? 1 : 0;
+    a.grad_dtype = grad_dtype;
+    return launch_backward(a, static_cast<cudaStream_t>(stream));
 }
 
 int fa_prefill_ex(const void *q, const void *k, const void *v, void *out, int B, int H, int N,

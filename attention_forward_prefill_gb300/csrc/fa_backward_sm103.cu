@@ -1,0 +1,592 @@
+// fa_backward_sm103.cu -- backward pass of the fused attention (the training
+// step that the flash-attention-cuda README lists under "Future work"), for
+// sm_103a.  Given Q, K, V, the forward output O, its gradient dO and the row
+// log-sum-exp L saved by the forward, it recomputes the weights tile by tile
+// and never stores the N x N tables:
+//   P_ij  = exp(s_ij - L_i),  s_ij = scale q_i.k_j     (2^(c s - L2) with c = scale log2 e)
+//   D_i   = dO_i . O_i
+//   dV_j  = sum_i P_ij dO_i
+//   dS_ij = P_ij (dO_i . v_j - D_i)
+//   dK_j  = scale sum_i dS_ij q_i,    dQ_i = scale sum_j dS_ij k_j
+// (the chain rule through softmax: sum_j P_ij dP_ij = dO_i . O_i).
+//
+// Three kernels, no atomics, so every gradient is bit-identical run to run:
+//   bwd_prep   D_i and L2_i = L_i log2 e for every row (fp32);
+//   bwd_dkdv   one CTA per 128-key tile: S^T = K Q_i^T and dP^T = V dO_i^T in
+//              TMEM, P^T and dS^T written back over them as 16-bit, then
+//              dV += P^T dO_i and dK += dS^T Q_i accumulate in TMEM over the
+//              query tiles that see the keys;
+//   bwd_dq     one CTA per 128-query tile: S = Q K_j^T, dP = dO V_j^T, dS over
+//              dP, dQ += dS K_j over the key tiles the queries see.
+// Warp roles per CTA (192 threads): warps 0-3 elementwise work, thread = TMEM
+// lane = tile row; warp 4 TMA producer; warp 5 tcgen05 issuer and TMEM owner.
+#include <cfloat>
+
+#include "fa_internal.h"
+#include "fa_tiles.cuh"
+#include "sm103_ptx.cuh"
+
+namespace fa {
+
+namespace {
+
+constexpr int kBwdThreads = 192;
+constexpr int kBwdTmaWarp = 4;
+constexpr int kBwdMmaWarp = 5;
+constexpr int kRows = 128;
+
+__device__ int g_backward_status = 0;
+
+template <int D>
+struct BwdLayout {
+    static constexpr int kChunks = D / 64;
+    static constexpr int kTileBytes = kChunks * kSlabBytes;  // 128 rows x D 16-bit
+    static constexpr int kStages = (D == 128) ? 2 : 3;
+    static constexpr int kFixOff = 0;                       // two tiles loaded once per CTA
+    static constexpr int kRingOff = 2 * kTileBytes;         // stages of two tiles each
+    static constexpr int kStageBytes = 2 * kTileBytes;
+    static constexpr int kVecOff = kRingOff + kStages * kStageBytes;  // [4 warps][2 buf][2][128] floats
+    static constexpr int kBarOff = kVecOff + 4 * 2 * 2 * kRows * 4;
+    // fix_full, s_full, p_ready, acc_done, drain, ring_full[S], ring_empty[S]
+    static constexpr int kNumBars = 5 + 2 * kStages;
+    static constexpr int kMiscOff = kBarOff + kNumBars * 8;
+    static constexpr int kSmemBytes = kMiscOff + 16 + 1024;
+    // TMEM: X (S or S^T) | Y (dP or dP^T) | accumulator A | accumulator B
+    static constexpr uint32_t kXCol = 0, kYCol = 128, kACol = 256, kBCol = 256 + D;
+};
+
+struct BwdParams {
+    const float *lse2;  // [BH][N] row log-sum-exp in log2 units
+    const float *dsum;  // [BH][N] D_i = dO_i . O_i
+    void *g0;           // dkdv: dK; dq: dQ        [BH][N][d]
+    void *g1;           // dkdv: dV
+    int N;
+    int n_t;            // 128-row tiles per head
+    int causal;
+    int grad_dtype;
+    float scale;
+    float c;            // scale * log2(e)
+};
+
+// ---------------------------------------------------------------- D and L2
+__global__ void __launch_bounds__(256) bwd_prep_kernel(const uint16_t *o, const uint16_t *dout,
+                                                       const float *lse, float *lse2, float *dsum,
+                                                       long long rows, int d, int bf16) {
+    const long long row = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (row >= rows) return;
+    float acc = 0.f;
+    for (int c = lane * 2; c < d; c += 64) {
+        const uint32_t a = *reinterpret_cast<const uint32_t *>(o + row * d + c);
+        const uint32_t b = *reinterpret_cast<const uint32_t *>(dout + row * d + c);
+        float a0, a1, b0, b1;
+        if (bf16) {
+            a0 = __uint_as_float(a << 16); a1 = __uint_as_float(a & 0xffff0000u);
+            b0 = __uint_as_float(b << 16); b1 = __uint_as_float(b & 0xffff0000u);
+        } else {
+            const float2 fa = __half22float2(*reinterpret_cast<const __half2 *>(&a));
+            const float2 fb = __half22float2(*reinterpret_cast<const __half2 *>(&b));
+            a0 = fa.x; a1 = fa.y; b0 = fb.x; b1 = fb.y;
+        }
+        acc = fmaf(a0, b0, acc);
+        acc = fmaf(a1, b1, acc);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (lane == 0) {
+        dsum[row] = acc;
+        lse2[row] = lse[row] * 1.4426950408889634f;
+    }
+}
+
+// Elementwise work on one 32-column quarter of a score tile held in TMEM:
+// returns, for the thread's row, the packed 16-bit weights and dS values.
+template <bool BF16, bool WANT_P>
+__device__ __forceinline__ void weights_quarter(const uint32_t (&sr)[32], const uint32_t (&dr)[32],
+                                                uint32_t (&pk)[16], uint32_t (&dk)[16], float c,
+                                                const float *lse2_col, const float *dsum_col,
+                                                float lse2_row, float dsum_row, uint32_t vis_mask) {
+#pragma unroll
+    for (int e2 = 0; e2 < 16; ++e2) {
+        float pp[2], dd[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int col = 2 * e2 + h;
+            const float l2 = lse2_col ? lse2_col[col] : lse2_row;
+            const float dsv = dsum_col ? dsum_col[col] : dsum_row;
+            const bool vis = (vis_mask >> col) & 1u;
+            const float p = vis ? ex2_approx(__uint_as_float(sr[col]) * c - l2) : 0.f;
+            pp[h] = p;
+            dd[h] = p * (__uint_as_float(dr[col]) - dsv);
+        }
+        if (WANT_P) pk[e2] = pack2t<BF16>(pp[0], pp[1]);
+        dk[e2] = pack2t<BF16>(dd[0], dd[1]);
+    }
+}
+
+// ---------------------------------------------------------------- dK, dV
+template <int D, bool BF16>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
+                    const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_do,
+                    const BwdParams p) {
+    using L = BwdLayout<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kBarOff);
+    uint64_t *fix_full = bars + 0, *s_full = bars + 1, *p_ready = bars + 2, *acc_done = bars + 3;
+    uint64_t *drain = bars + 4, *ring_full = bars + 5, *ring_empty = bars + 5 + L::kStages;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kMiscOff);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kMiscOff + 4);
+    float *vec = reinterpret_cast<float *>(smem + L::kVecOff);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int bh = blockIdx.x / p.n_t;
+    const int jt = blockIdx.x % p.n_t;         // key tile (small first: most query tiles)
+    const int i_first = p.causal ? jt : 0;     // query tiles that see key tile jt
+    const int n_iter = p.n_t - i_first;
+
+    if (threadIdx.x == 0) {
+        mbar_init(fix_full, 1);
+        mbar_init(s_full, 1);
+        mbar_init(p_ready, 4);
+        mbar_init(acc_done, 1);
+        mbar_init(drain, 1);
+        for (int s = 0; s < L::kStages; ++s) {
+            mbar_init(ring_full + s, 1);
+            mbar_init(ring_empty + s, 1);
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == kBwdMmaWarp) {
+        tmem_alloc(tmem_slot, 512);
+        tmem_relinquish();
+    }
+    if (warp == kBwdTmaWarp && lane == 0) {
+        prefetch_tensormap(&map_q);
+        prefetch_tensormap(&map_k);
+        prefetch_tensormap(&map_v);
+        prefetch_tensormap(&map_do);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == kBwdTmaWarp) {
+        if (lane == 0) {
+            uint8_t *fix = smem + L::kFixOff, *ring = smem + L::kRingOff;
+            const uint64_t pol = l2_policy_evict_last();
+            bool ok = true;
+            mbar_arrive_expect_tx(fix_full, 2 * L::kTileBytes);
+            for (int c = 0; c < L::kChunks; ++c) {
+                tma_load_3d(fix + c * kSlabBytes, &map_k, fix_full, c * 64, jt * kRows, bh, pol);
+                tma_load_3d(fix + L::kTileBytes + c * kSlabBytes, &map_v, fix_full, c * 64, jt * kRows, bh,
+                            pol);
+            }
+            int n = 0;
+            for (; n < n_iter && ok; ++n) {
+                const int slot = n % L::kStages;
+                if (n >= L::kStages &&
+                    !mbar_wait(ring_empty + slot, ((n / L::kStages) - 1) & 1, abort_flag, kWatchdogNs)) {
+                    ok = false;
+                    break;
+                }
+                const int row = (i_first + n) * kRows;
+                uint8_t *st = ring + slot * L::kStageBytes;
+                mbar_arrive_expect_tx(ring_full + slot, 2 * L::kTileBytes);
+                for (int c = 0; c < L::kChunks; ++c) {
+                    tma_load_3d(st + c * kSlabBytes, &map_q, ring_full + slot, c * 64, row, bh, pol);
+                    tma_load_3d(st + L::kTileBytes + c * kSlabBytes, &map_do, ring_full + slot, c * 64, row,
+                                bh, pol);
+                }
+            }
+            if (!ok) {  // let every copy already issued land
+                constexpr uint64_t kDrainNs = 200ull * 1000ull * 1000ull;
+                int dummy = 0;
+                mbar_wait(fix_full, 0, &dummy, kDrainNs);
+                for (int m = (n > L::kStages ? n - L::kStages : 0); m < n; ++m)
+                    mbar_wait(ring_full + (m % L::kStages), (m / L::kStages) & 1, &dummy, kDrainNs);
+            }
+        }
+        __syncwarp();
+    } else if (warp == kBwdMmaWarp) {
+        if (lane == 0) {
+            const uint32_t idesc_s = idesc_f16(BF16, kRows, kRows, false, false);
+            const uint32_t idesc_acc = idesc_f16(BF16, kRows, D, false, true);
+            const uint32_t fix = smem_u32(smem + L::kFixOff), ring = smem_u32(smem + L::kRingOff);
+            const uint64_t k_desc = sdesc_sw128(fix, 16, 1024);
+            const uint64_t v_desc = sdesc_sw128(fix + L::kTileBytes, 16, 1024);
+            bool ok = mbar_wait(fix_full, 0, abort_flag, kWatchdogNs);
+            for (int n = 0; n < n_iter && ok; ++n) {
+                const int slot = n % L::kStages;
+                if (!mbar_wait(ring_full + slot, (n / L::kStages) & 1, abort_flag, kWatchdogNs)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t st = ring + slot * L::kStageBytes;
+                // S^T = K Q_i^T and dP^T = V dO_i^T (keys on TMEM lanes)
+                issue_qk<D>(tmem + L::kXCol, k_desc, sdesc_sw128(st, 16, 1024), idesc_s);
+                issue_qk<D>(tmem + L::kYCol, v_desc, sdesc_sw128(st + L::kTileBytes, 16, 1024), idesc_s);
+                umma_commit(s_full);
+                if (!mbar_wait(p_ready, n & 1, abort_flag, kWatchdogNs)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                // dV += P^T dO_i and dK += dS^T Q_i (P^T, dS^T from TMEM; dO_i, Q_i MN-major)
+                issue_pv<D>(tmem + L::kACol, tmem + L::kXCol,
+                            sdesc_sw128(st + L::kTileBytes, kSlabBytes, 1024), idesc_acc, n > 0);
+                issue_pv<D>(tmem + L::kBCol, tmem + L::kYCol, sdesc_sw128(st, kSlabBytes, 1024), idesc_acc,
+                            n > 0);
+                umma_commit(ring_empty + slot);
+            }
+            umma_commit(acc_done);
+            umma_commit(drain);
+            int dummy = 0;
+            mbar_wait(drain, 0, &dummy, kWatchdogNs);
+        }
+        __syncwarp();
+    } else {
+        // ---------------------------------------------------------------- elementwise
+        const int r = warp * 32 + lane;
+        const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+        const int key = jt * kRows + r;
+        const float *lse2_h = p.lse2 + static_cast<size_t>(bh) * p.N;
+        const float *dsum_h = p.dsum + static_cast<size_t>(bh) * p.N;
+        bool ok = true;
+        for (int n = 0; n < n_iter && ok; ++n) {
+            const int q0 = (i_first + n) * kRows;
+            // this query tile's L2 and D, needed by every row: each warp stages its
+            // own copy (double-buffered), so no barrier spans warps
+            float *vb = vec + (warp * 2 + (n & 1)) * 2 * kRows;
+#pragma unroll
+            for (int x = lane; x < kRows; x += 32) {
+                vb[x] = q0 + x < p.N ? lse2_h[q0 + x] : 0.f;
+                vb[kRows + x] = q0 + x < p.N ? dsum_h[q0 + x] : 0.f;
+            }
+            __syncwarp();
+            if (!warp_wait(s_full, n & 1, abort_flag)) { ok = false; break; }
+            tc_fence_after();
+#pragma unroll 1
+            for (int q = 0; q < 4; ++q) {
+                uint32_t sr[32], dr[32];
+                tmem_ld32(tmem + lane_off + L::kXCol + q * 32, sr);
+                tmem_ld32(tmem + lane_off + L::kYCol + q * 32, dr);
+                tmem_ld_wait();
+                reg_fence32(sr);
+                reg_fence32(dr);
+                // column col is query q0 + 32 q + col; it sees the key when it exists
+                // and, causally, when key <= query
+                const int qb = q0 + q * 32;
+                uint32_t vis = 0xffffffffu;
+                if (qb + 32 > p.N) vis = p.N > qb ? (0xffffffffu >> (32 - (p.N - qb))) : 0u;
+                if (p.causal) {
+                    const int lo = key - qb;  // first visible column
+                    vis &= lo <= 0 ? 0xffffffffu : (lo >= 32 ? 0u : (0xffffffffu << lo));
+                }
+                uint32_t pk[16], dk[16];
+                weights_quarter<BF16, true>(sr, dr, pk, dk, p.c, vb + q * 32, vb + kRows + q * 32, 0.f, 0.f, vis);
+                tmem_st16(tmem + lane_off + L::kXCol + q * 16, pk);   // P^T over S^T (already read)
+                tmem_st16(tmem + lane_off + L::kYCol + q * 16, dk);   // dS^T over dP^T
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(p_ready);
+        }
+        if (ok && warp_wait(acc_done, 0, abort_flag)) {
+            tc_fence_after();
+            const int osize = p.grad_dtype == FA_F32 ? 4 : 2;
+            const size_t row_off = (static_cast<size_t>(bh) * p.N + key) * D * osize;
+#pragma unroll
+            for (int q = 0; q < D / 32; ++q) {
+                uint32_t o[32];
+                tmem_ld32(tmem + lane_off + L::kACol + q * 32, o);
+                tmem_ld_wait();
+                reg_fence32(o);
+                if (key < p.N)
+                    store_out32(static_cast<uint8_t *>(p.g1) + row_off + q * 32 * osize, o, 1.f, p.grad_dtype);
+                tmem_ld32(tmem + lane_off + L::kBCol + q * 32, o);
+                tmem_ld_wait();
+                reg_fence32(o);
+                if (key < p.N)
+                    store_out32(static_cast<uint8_t *>(p.g0) + row_off + q * 32 * osize, o, p.scale,
+                                p.grad_dtype);
+            }
+            tc_fence_before();
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kBwdMmaWarp) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+    if (threadIdx.x == 0 && *abort_flag) atomicCAS(&g_backward_status, 0, (int)FA_ERR_WATCHDOG);
+}
+
+// ---------------------------------------------------------------- dQ
+template <int D, bool BF16>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
+                  const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_do,
+                  const BwdParams p) {
+    using L = BwdLayout<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kBarOff);
+    uint64_t *fix_full = bars + 0, *s_full = bars + 1, *p_ready = bars + 2, *acc_done = bars + 3;
+    uint64_t *drain = bars + 4, *ring_full = bars + 5, *ring_empty = bars + 5 + L::kStages;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kMiscOff);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kMiscOff + 4);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int bh = blockIdx.x / p.n_t;
+    const int it = p.causal ? p.n_t - 1 - blockIdx.x % p.n_t   // most key tiles first
+                            : blockIdx.x % p.n_t;
+    const int n_iter = p.causal ? it + 1 : p.n_t;              // key tiles the queries see
+
+    if (threadIdx.x == 0) {
+        mbar_init(fix_full, 1);
+        mbar_init(s_full, 1);
+        mbar_init(p_ready, 4);
+        mbar_init(acc_done, 1);
+        mbar_init(drain, 1);
+        for (int s = 0; s < L::kStages; ++s) {
+            mbar_init(ring_full + s, 1);
+            mbar_init(ring_empty + s, 1);
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == kBwdMmaWarp) {
+        tmem_alloc(tmem_slot, 512);
+        tmem_relinquish();
+    }
+    if (warp == kBwdTmaWarp && lane == 0) {
+        prefetch_tensormap(&map_q);
+        prefetch_tensormap(&map_k);
+        prefetch_tensormap(&map_v);
+        prefetch_tensormap(&map_do);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == kBwdTmaWarp) {
+        if (lane == 0) {
+            uint8_t *fix = smem + L::kFixOff, *ring = smem + L::kRingOff;
+            const uint64_t pol = l2_policy_evict_last();
+            bool ok = true;
+            mbar_arrive_expect_tx(fix_full, 2 * L::kTileBytes);
+            for (int c = 0; c < L::kChunks; ++c) {
+                tma_load_3d(fix + c * kSlabBytes, &map_q, fix_full, c * 64, it * kRows, bh, pol);
+                tma_load_3d(fix + L::kTileBytes + c * kSlabBytes, &map_do, fix_full, c * 64, it * kRows, bh,
+                            pol);
+            }
+            int n = 0;
+            for (; n < n_iter && ok; ++n) {
+                const int slot = n % L::kStages;
+                if (n >= L::kStages &&
+                    !mbar_wait(ring_empty + slot, ((n / L::kStages) - 1) & 1, abort_flag, kWatchdogNs)) {
+                    ok = false;
+                    break;
+                }
+                uint8_t *st = ring + slot * L::kStageBytes;
+                mbar_arrive_expect_tx(ring_full + slot, 2 * L::kTileBytes);
+                for (int c = 0; c < L::kChunks; ++c) {
+                    tma_load_3d(st + c * kSlabBytes, &map_k, ring_full + slot, c * 64, n * kRows, bh, pol);
+                    tma_load_3d(st + L::kTileBytes + c * kSlabBytes, &map_v, ring_full + slot, c * 64, n * kRows,
+                                bh, pol);
+                }
+            }
+            if (!ok) {
+                constexpr uint64_t kDrainNs = 200ull * 1000ull * 1000ull;
+                int dummy = 0;
+                mbar_wait(fix_full, 0, &dummy, kDrainNs);
+                for (int m = (n > L::kStages ? n - L::kStages : 0); m < n; ++m)
+                    mbar_wait(ring_full + (m % L::kStages), (m / L::kStages) & 1, &dummy, kDrainNs);
+            }
+        }
+        __syncwarp();
+    } else if (warp == kBwdMmaWarp) {
+        if (lane == 0) {
+            const uint32_t idesc_s = idesc_f16(BF16, kRows, kRows, false, false);
+            const uint32_t idesc_acc = idesc_f16(BF16, kRows, D, false, true);
+            const uint32_t fix = smem_u32(smem + L::kFixOff), ring = smem_u32(smem + L::kRingOff);
+            const uint64_t q_desc = sdesc_sw128(fix, 16, 1024);
+            const uint64_t do_desc = sdesc_sw128(fix + L::kTileBytes, 16, 1024);
+            bool ok = mbar_wait(fix_full, 0, abort_flag, kWatchdogNs);
+            for (int n = 0; n < n_iter && ok; ++n) {
+                const int slot = n % L::kStages;
+                if (!mbar_wait(ring_full + slot, (n / L::kStages) & 1, abort_flag, kWatchdogNs)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t st = ring + slot * L::kStageBytes;
+                // S = Q K_j^T and dP = dO V_j^T (queries on TMEM lanes)
+                issue_qk<D>(tmem + L::kXCol, q_desc, sdesc_sw128(st, 16, 1024), idesc_s);
+                issue_qk<D>(tmem + L::kYCol, do_desc, sdesc_sw128(st + L::kTileBytes, 16, 1024), idesc_s);
+                umma_commit(s_full);
+                if (!mbar_wait(p_ready, n & 1, abort_flag, kWatchdogNs)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                // dQ += dS K_j (dS from TMEM over dP; K_j MN-major)
+                issue_pv<D>(tmem + L::kACol, tmem + L::kYCol, sdesc_sw128(st, kSlabBytes, 1024), idesc_acc,
+                            n > 0);
+                umma_commit(ring_empty + slot);
+            }
+            umma_commit(acc_done);
+            umma_commit(drain);
+            int dummy = 0;
+            mbar_wait(drain, 0, &dummy, kWatchdogNs);
+        }
+        __syncwarp();
+    } else {
+        const int r = warp * 32 + lane;
+        const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+        const int qrow = it * kRows + r;
+        const size_t li = static_cast<size_t>(bh) * p.N + qrow;
+        const float lse2_r = qrow < p.N ? p.lse2[li] : 0.f;
+        const float dsum_r = qrow < p.N ? p.dsum[li] : 0.f;
+        bool ok = true;
+        for (int n = 0; n < n_iter && ok; ++n) {
+            if (!warp_wait(s_full, n & 1, abort_flag)) { ok = false; break; }
+            tc_fence_after();
+#pragma unroll 1
+            for (int q = 0; q < 4; ++q) {
+                uint32_t sr[32], dr[32];
+                tmem_ld32(tmem + lane_off + L::kXCol + q * 32, sr);
+                tmem_ld32(tmem + lane_off + L::kYCol + q * 32, dr);
+                tmem_ld_wait();
+                reg_fence32(sr);
+                reg_fence32(dr);
+                // column col is key n * 128 + 32 q + col: visible when it exists, the
+                // row exists and, causally, key <= query
+                const int kb = n * kRows + q * 32;
+                uint32_t vis = 0xffffffffu;
+                if (kb + 32 > p.N) vis = p.N > kb ? (0xffffffffu >> (32 - (p.N - kb))) : 0u;
+                if (qrow >= p.N) vis = 0u;
+                if (p.causal) {
+                    const int hi = qrow - kb;  // last visible column
+                    vis &= hi < 0 ? 0u : (hi >= 31 ? 0xffffffffu : (0xffffffffu >> (31 - hi)));
+                }
+                uint32_t pk[16], dk[16];
+                weights_quarter<BF16, false>(sr, dr, pk, dk, p.c, nullptr, nullptr, lse2_r, dsum_r, vis);
+                tmem_st16(tmem + lane_off + L::kYCol + q * 16, dk);  // dS over dP (already read)
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(p_ready);
+        }
+        if (ok && warp_wait(acc_done, 0, abort_flag)) {
+            tc_fence_after();
+            const int osize = p.grad_dtype == FA_F32 ? 4 : 2;
+            const size_t row_off = li * D * osize;
+#pragma unroll
+            for (int q = 0; q < D / 32; ++q) {
+                uint32_t o[32];
+                tmem_ld32(tmem + lane_off + L::kACol + q * 32, o);
+                tmem_ld_wait();
+                reg_fence32(o);
+                if (qrow < p.N)
+                    store_out32(static_cast<uint8_t *>(p.g0) + row_off + q * 32 * osize, o, p.scale,
+                                p.grad_dtype);
+            }
+            tc_fence_before();
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kBwdMmaWarp) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+    if (threadIdx.x == 0 && *abort_flag) atomicCAS(&g_backward_status, 0, (int)FA_ERR_WATCHDOG);
+}
+
+template <int D, bool BF16>
+int launch_bwd_d(const BackwardLaunch &a, cudaStream_t stream) {
+    using L = BwdLayout<D>;
+    static_assert(L::kSmemBytes <= 227 * 1024, "shared memory budget");
+    const long long BH = static_cast<long long>(a.B) * a.H;
+    const long long rows = BH * a.N;
+    CUtensorMap mq, mk, mv, mdo;
+    int rc;
+    if ((rc = make_map(&mq, a.q, D, false, a.N, BH, a.in_bf16)) != FA_OK) return rc;
+    if ((rc = make_map(&mk, a.k, D, false, a.N, BH, a.in_bf16)) != FA_OK) return rc;
+    if ((rc = make_map(&mv, a.v, D, false, a.N, BH, a.in_bf16)) != FA_OK) return rc;
+    if ((rc = make_map(&mdo, a.dout, D, false, a.N, BH, a.in_bf16)) != FA_OK) return rc;
+    cudaError_t e;
+    if ((e = cudaFuncSetAttribute(bwd_dkdv_kernel<D, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  L::kSmemBytes)) != cudaSuccess ||
+        (e = cudaFuncSetAttribute(bwd_dq_kernel<D, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  L::kSmemBytes)) != cudaSuccess)
+        return cuda_fail(e);
+    void *ws = nullptr;
+    if ((e = scratch_alloc(&ws, static_cast<size_t>(rows) * 2 * sizeof(float), stream)) != cudaSuccess) {
+        cuda_fail(e);
+        return FA_ERR_WORKSPACE;
+    }
+    float *lse2 = static_cast<float *>(ws), *dsum = lse2 + rows;
+    bwd_prep_kernel<<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(
+        static_cast<const uint16_t *>(a.out), static_cast<const uint16_t *>(a.dout), a.lse, lse2, dsum, rows,
+        D, a.in_bf16);
+    e = cudaGetLastError();
+    BwdParams p;
+    p.lse2 = lse2;
+    p.dsum = dsum;
+    p.N = a.N;
+    p.n_t = (a.N + kRows - 1) / kRows;
+    p.causal = a.causal ? 1 : 0;
+    p.grad_dtype = a.grad_dtype;
+    p.scale = a.scale;
+    p.c = a.scale * 1.4426950408889634f;
+    const unsigned grid = static_cast<unsigned>(BH * p.n_t);
+    if (e == cudaSuccess) {
+        p.g0 = a.dk;
+        p.g1 = a.dv;
+        bwd_dkdv_kernel<D, BF16><<<grid, kBwdThreads, L::kSmemBytes, stream>>>(mq, mk, mv, mdo, p);
+        e = cudaGetLastError();
+    }
+    if (e == cudaSuccess) {
+        p.g0 = a.dq;
+        p.g1 = nullptr;
+        bwd_dq_kernel<D, BF16><<<grid, kBwdThreads, L::kSmemBytes, stream>>>(mq, mk, mv, mdo, p);
+        e = cudaGetLastError();
+    }
+    const cudaError_t e2 = scratch_free(ws, stream);
+    if (e == cudaSuccess) e = e2;
+    if (e != cudaSuccess) return cuda_fail(e);
+    return FA_OK;
+}
+
+}  // namespace
+
+int launch_backward(const BackwardLaunch &a, cudaStream_t stream) {
+    if (a.d == 64) return a.in_bf16 ? launch_bwd_d<64, true>(a, stream) : launch_bwd_d<64, false>(a, stream);
+    if (a.d == 128) return a.in_bf16 ? launch_bwd_d<128, true>(a, stream) : launch_bwd_d<128, false>(a, stream);
+    return FA_ERR_HEAD_DIM;
+}
+
+int read_backward_status(int reset) {
+    int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_backward_status, sizeof(int)) != cudaSuccess) return -1;
+    if (reset && v) {
+        int z = 0;
+        if (cudaMemcpyToSymbol(g_backward_status, &z, sizeof(int)) != cudaSuccess) return -1;
+    }
+    return v;
+}
+
+}  // namespace fa

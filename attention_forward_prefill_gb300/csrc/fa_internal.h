@@ -34,6 +34,7 @@ cudaError_t scratch_free(void *ptr, cudaStream_t stream);
 struct PrefillLaunch {
     const void *q, *k, *v;
     void *out;
+    float *lse;                  // optional row log-sum-exp output (natural log)
     const int32_t *cu_q, *cu_k;  // packed batch: [B+1] token offsets (device); null when dense
     int B, Hq, Hkv;
     int Nq, Nk;                  // dense: lengths; packed: max_seqlen_q / max_seqlen_k
@@ -75,8 +76,22 @@ struct DecodeLaunch {
 
 int launch_decode(const DecodeLaunch &a, const DeviceInfo &dev, cudaStream_t stream);
 
+struct BackwardLaunch {
+    const void *q, *k, *v, *out, *dout;  // [B][H][N][d] 16-bit
+    const float *lse;                    // [B][H][N] natural-log row log-sum-exp of the forward
+    void *dq, *dk, *dv;                  // [B][H][N][d] in grad_dtype
+    int B, H, N, d;
+    int causal;
+    float scale;
+    int in_bf16;
+    int grad_dtype;
+};
+
+int launch_backward(const BackwardLaunch &a, cudaStream_t stream);
+
 // Device-side watchdog words (one per kernel translation unit).
 int read_prefill_status(int reset);
 int read_decode_status(int reset);
+int read_backward_status(int reset);
 
 }  // namespace fa

@@ -32,6 +32,7 @@
 #include <cuda_fp16.h>
 
 #include "fa_internal.h"
+#include "fa_tiles.cuh"
 #include "sm103_ptx.cuh"
 
 namespace fa {
@@ -50,7 +51,6 @@ constexpr int kBlockM = 128;   // query rows per tile
 constexpr int kBlockN = 128;   // keys per tile
 constexpr int kRowsPerUnit = 2 * kBlockM;
 constexpr float kTau = 8.0f;   // lazy-rescale threshold, log2 units
-constexpr uint64_t kWatchdogNs = 1500ull * 1000ull * 1000ull;
 constexpr uint32_t kTmemCols = 512;
 
 __device__ int g_prefill_status = 0;
@@ -84,6 +84,8 @@ constexpr int kMaxPre = 1024;  // stream-K: query blocks per head with a step ta
 
 struct Params {
     void *out;
+    float *lse;            // optional: natural-log log-sum-exp of every row (dense [B][Hq][Nq],
+                           // packed [tokens][Hq]); -inf for a row that sees no key
     // A packed batch (variable lengths) keeps tokens [cu_q[b], cu_q[b+1]) of
     // sequence b in a [tokens][H][d] tensor; a dense batch is [B][H][N][d].
     const int *cu_q;       // packed: [B+1] query-token offsets (device); null when dense
@@ -212,123 +214,6 @@ __device__ __forceinline__ bool seg_next(const Params &p, const StepTable &tab, 
     w.n1 = kv_tiles(p.causal, p.no_skip, w.nq, w.nk, w.off, w.q0 + kBlockM);
     if (w.j1 < 0) w.j1 = max(w.n0, w.n1);
     return true;
-}
-
-// Warp-uniform bounded wait: lane 0 polls, the verdict is broadcast.
-__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag) {
-    int ok = 1;
-    if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort_flag, kWatchdogNs) ? 1 : 0;
-    ok = __shfl_sync(0xffffffffu, ok, 0);
-    return ok != 0;
-}
-
-// S (+)= Q K^T over d: a_desc / b_desc describe the Q and K tiles at K-step 0;
-// step kk moves (kk / 4) 64-column slabs and (kk % 4) 32-byte atoms along d.
-// Descriptors are built once per tile; each step only adds a constant to the
-// start-address field (shared addresses stay below 256 KB, so it cannot carry).
-template <int D>
-__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                         uint32_t idesc) {
-#pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk) {
-        const uint64_t off = ((kk >> 2) * Layout<D>::kChunkBytes + (kk & 3) * 32) >> 4;
-        umma_ss(d_tmem, a_desc + off, b_desc + off, idesc, kk > 0 ? 1u : 0u);
-    }
-}
-
-// O (+)= P V: P from TMEM (16 keys = 8 columns per step), V tile [key][d] with d
-// contiguous is an MN-major B operand: 16 keys per step = two 8-key groups
-// (SBO apart), 64-column slabs of d LBO apart.
-template <int D>
-__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint64_t v_desc,
-                                         uint32_t idesc, bool accumulate) {
-#pragma unroll
-    for (int kk = 0; kk < kBlockN / 16; ++kk)
-        umma_ts(d_tmem, p_tmem + kk * 8, v_desc + ((kk * 16 * 128) >> 4), idesc,
-                (accumulate || kk > 0) ? 1u : 0u);
-}
-
-// The two 16-bit values of a packed pair, back in fp32 (exact), as an f32x2.
-template <bool BF16>
-__device__ __forceinline__ uint64_t unpack2(uint32_t w) {
-    if constexpr (BF16) {
-        return f2_pack(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
-    } else {
-        const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&w));
-        return f2_pack(f.x, f.y);
-    }
-}
-
-template <bool BF16>
-__device__ __forceinline__ uint32_t pack2t(float lo, float hi) {
-    if constexpr (BF16) {
-        __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
-        return *reinterpret_cast<uint32_t *>(&h);
-    } else {
-        __half2 h = __floats2half2_rn(lo, hi);
-        return *reinterpret_cast<uint32_t *>(&h);
-    }
-}
-
-// Row maximum of 128 scores: eight independent chains of 3-input maxima.
-template <bool NEG>
-__device__ __forceinline__ float row_max128(const uint32_t (&sr)[4][32]) {
-    float m[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const float a = __uint_as_float(sr[i >> 1][(i & 1) * 16 + 0]);
-        m[i] = NEG ? -a : a;
-    }
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        // chain i covers columns [16 i, 16 i + 16)
-#pragma unroll
-        for (int c = 1; c < 16; c += 2) {
-            const int col = 16 * i + c;
-            const float a = __uint_as_float(sr[col >> 5][col & 31]);
-            const float b = (c + 1 < 16) ? __uint_as_float(sr[(col + 1) >> 5][(col + 1) & 31]) : a;
-            m[i] = NEG ? fmax3(m[i], -a, -b) : fmax3(m[i], a, b);
-        }
-    }
-    return fmaxf(fmax3(m[0], m[1], m[2]), fmax3(fmax3(m[3], m[4], m[5]), m[6], m[7]));
-}
-
-__device__ __forceinline__ uint32_t pack2(float lo, float hi, int bf16) {
-    if (bf16) {
-        __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
-        return *reinterpret_cast<uint32_t *>(&h);
-    }
-    __half2 h = __floats2half2_rn(lo, hi);
-    return *reinterpret_cast<uint32_t *>(&h);
-}
-
-// One 32-column slice of a finished output row: O * inv_l -> out dtype.
-__device__ __forceinline__ void store_out32(void *dst, const uint32_t (&r)[32], float inv,
-                                            int out_dtype) {
-    if (out_dtype == FA_F32) {
-        uint4 *d4 = reinterpret_cast<uint4 *>(dst);
-#pragma unroll
-        for (int v = 0; v < 8; ++v) {
-            uint4 w;
-            w.x = __float_as_uint(__uint_as_float(r[4 * v + 0]) * inv);
-            w.y = __float_as_uint(__uint_as_float(r[4 * v + 1]) * inv);
-            w.z = __float_as_uint(__uint_as_float(r[4 * v + 2]) * inv);
-            w.w = __float_as_uint(__uint_as_float(r[4 * v + 3]) * inv);
-            d4[v] = w;
-        }
-    } else {
-        const int bf = out_dtype == FA_BF16;
-        uint4 *d4 = reinterpret_cast<uint4 *>(dst);
-#pragma unroll
-        for (int v = 0; v < 4; ++v) {
-            uint4 w;
-            w.x = pack2(__uint_as_float(r[8 * v + 0]) * inv, __uint_as_float(r[8 * v + 1]) * inv, bf);
-            w.y = pack2(__uint_as_float(r[8 * v + 2]) * inv, __uint_as_float(r[8 * v + 3]) * inv, bf);
-            w.z = pack2(__uint_as_float(r[8 * v + 4]) * inv, __uint_as_float(r[8 * v + 5]) * inv, bf);
-            w.w = pack2(__uint_as_float(r[8 * v + 6]) * inv, __uint_as_float(r[8 * v + 7]) * inv, bf);
-            d4[v] = w;
-        }
-    }
 }
 
 template <int D, bool BF16>
@@ -789,6 +674,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 continue;
             }
             const float inv = l > 0.f ? 1.0f / l : 0.f;  // l = 0: no visible key
+            if (p.lse != nullptr && row_ok) {
+                // the row's index in [B][Hq][Nq] (dense) or [tokens][Hq] (packed) is its
+                // output offset in elements divided by d
+                const long long li = ((orow - reinterpret_cast<uint8_t *>(p.out)) >> (osize == 4 ? 2 : 1)) / D;
+                p.lse[li] = l > 0.f ? (m_ref + __log2f(l)) * 0.6931471805599453f : -INFINITY;
+            }
 #pragma unroll
             for (int q = 0; q < D / 32; ++q) {
                 uint32_t o[32];
@@ -821,6 +712,7 @@ constexpr int kMaxSplit = 192;
 
 struct FixupParams {
     void *out;
+    float *lse;
     const float *ws_o;
     const float *ws_ml;
     int Hq, Nq, Nk;
@@ -895,6 +787,8 @@ __global__ void __launch_bounds__(256) prefill_fixup(const __grid_constant__ Fix
         }
     }
     const float inv = L > 0.f ? 1.0f / L : 0.f;
+    if (f.lse != nullptr && lane == 0)
+        f.lse[static_cast<size_t>(bh) * f.Nq + row] = L > 0.f ? (M + __log2f(L)) * 0.6931471805599453f : -INFINITY;
     const size_t off = (static_cast<size_t>(bh) * f.Nq + row) * D + lane * EPL;
     if (f.out_dtype == FA_F32) {
         float *dst = reinterpret_cast<float *>(f.out) + off;
@@ -912,54 +806,6 @@ __global__ void __launch_bounds__(256) prefill_fixup(const __grid_constant__ Fix
 }
 
 // ---------------------------------------------------------------- host side
-typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
-                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
-                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = [] {
-        void *ptr = nullptr;
-        cudaDriverEntryPointQueryResult qres;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
-                                             &qres) != cudaSuccess ||
-            qres != cudaDriverEntryPointSuccess)
-            ptr = nullptr;
-        return reinterpret_cast<EncodeTiledFn>(ptr);
-    }();
-    return fn;
-}
-
-// A dense [BH][N][d] tensor is viewed as (d, N, BH) with 64 x 128 x 1 boxes; a
-// packed [tokens][H][d] tensor as (d, H, tokens) with 64 x 1 x 128 boxes.  Both
-// land in shared memory as 128 rows of 128 bytes, 128-byte swizzled.  Rows past
-// the end of the tensor read as zero.
-int make_map(CUtensorMap *map, const void *base, int d, bool packed, long long rows, long long outer,
-             int bf16) {
-    EncodeTiledFn enc = encode_fn();
-    if (!enc) return cuda_fail(cudaErrorNotSupported);
-    cuuint64_t dims[3], strides[2];
-    cuuint32_t box[3];
-    if (packed) {  // rows = tokens, outer = heads
-        dims[0] = d; dims[1] = (cuuint64_t)outer; dims[2] = (cuuint64_t)(rows > 0 ? rows : 1);
-        strides[0] = (cuuint64_t)d * 2;
-        strides[1] = (cuuint64_t)d * 2 * (cuuint64_t)outer;
-        box[0] = 64; box[1] = 1; box[2] = 128;
-    } else {       // rows = sequence length, outer = batch x heads
-        dims[0] = d; dims[1] = (cuuint64_t)rows; dims[2] = (cuuint64_t)outer;
-        strides[0] = (cuuint64_t)d * 2;
-        strides[1] = (cuuint64_t)d * 2 * (cuuint64_t)rows;
-        box[0] = 64; box[1] = 128; box[2] = 1;
-    }
-    cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = enc(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
-                     const_cast<void *>(base), dims, strides, box, estr,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) return cuda_fail(cudaErrorInvalidValue);
-    return FA_OK;
-}
-
 int host_kv_tiles(int causal, int no_skip, int nq, int nk, int row0) {
     if (row0 >= nq) return 0;
     const int tk = (nk + kBlockN - 1) / kBlockN;
@@ -1101,6 +947,7 @@ int launch_d(const PrefillLaunch &a, const DeviceInfo &dev, cudaStream_t stream)
 
     Params p;
     p.out = a.out;
+    p.lse = a.lse;
     p.cu_q = a.cu_q;
     p.cu_k = a.cu_k;
     p.B = a.B;
@@ -1141,6 +988,7 @@ int launch_d(const PrefillLaunch &a, const DeviceInfo &dev, cudaStream_t stream)
     void *ws = nullptr;
     if (p.stream_k) {
         f.out = a.out;
+        f.lse = a.lse;
         f.Hq = a.Hq;
         f.Nq = a.Nq;
         f.Nk = a.Nk;

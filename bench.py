@@ -460,6 +460,24 @@ def measure_configs(torch, binding, device, stream, flush, peaks, reps=7):
                                             scale=1 / math.sqrt(d), out=o),
              float(sum(int(n) * (int(n) + 1) / 2 for n in lens)), d, H)
     del q, k, v, o
+    # backward pass (training): dQ, dK, dV from the forward's output and
+    # log-sum-exp; FLOPs counted as five N^2 d products (10 B H N^2 d, halved
+    # for causal), the algorithmic count of a backward that recomputes S
+    for name, B, H, N, d, dt, causal in [("backward_long_n8192_full", 1, 16, 8192, 128, torch.bfloat16, False),
+                                         ("backward_long_n8192_causal", 1, 16, 8192, 128, torch.bfloat16, True),
+                                         ("backward_gpt2_b4_causal", 4, 12, 2048, 64, torch.float16, True)]:
+        q, k, v, do = (rnd((B, H, N, d), dt) for _ in range(4))
+        out, lse = binding.prefill_with_lse(q, k, v, causal=causal, scale=1 / math.sqrt(d))
+
+        def fn():
+            binding.prefill_backward(q, k, v, out, do, lse, causal=causal, scale=1 / math.sqrt(d))
+        fn()
+        med, mn = time_kernel(torch, stream, flush, fn, reps)
+        fl = 10.0 * B * H * N * N * d / (2 if causal else 1)
+        tf = fl / (med / 1e3) / 1e12
+        res[name] = {"shape": [B, H, N, d], "median_us": round(med * 1e3, 2), "min_us": round(mn * 1e3, 2),
+                     "tflops": round(tf, 1), "frac_of_peak": round(tf / peaks["bf16_tflops"], 4)}
+        del q, k, v, do, out, lse
     for B in (1, 8, 32):
         for H in (14, 12):
             shp = (B, H, DECODE_L, DECODE_D)

@@ -127,6 +127,44 @@ int fa_prefill_gqa(const void *q, const void *k, const void *v, void *out,
                    unsigned flags, void *stream);
 
 /*
+ * Prefill that also returns, for every query row, the log-sum-exp of its
+ * visible scores, lse_i = log sum_j exp(scale q_i.k_j) (natural log; -inf for
+ * a row that sees no key).  It is what fa_prefill_backward needs to recompute
+ * the weights.  Arguments as fa_prefill_gqa plus
+ *   lse : fp32 device array [B][Hq][Nq] (4-byte aligned), or NULL (then this
+ *         is fa_prefill_gqa)
+ */
+int fa_prefill_lse(const void *q, const void *k, const void *v, void *out,
+                   float *lse, int B, int Hq, int Hkv, int Nq, int Nk, int d,
+                   int causal, float scale, fa_dtype in_dtype,
+                   fa_dtype out_dtype, unsigned flags, void *stream);
+
+/*
+ * Backward pass of prefill (flash-attention-cuda README, "Future work":
+ * training), for square multi-head problems: given the inputs, the forward
+ * output `out`, its gradient `dout` and the forward's `lse`, writes
+ *   dq = dL/dq, dk = dL/dk, dv = dL/dv
+ * of L = sum(dout * out), with the weights recomputed tile by tile (the N x N
+ * tables never reach memory).  No atomics: the result is bit-identical run to
+ * run.
+ *   q, k, v, out, dout : 16-bit [B][H][N][d] in in_dtype (out as written by
+ *                        fa_prefill_lse with out_dtype == in_dtype)
+ *   lse                : fp32 [B][H][N] from fa_prefill_lse
+ *   dq, dk, dv         : [B][H][N][d] in grad_dtype (FA_F16, FA_BF16, FA_F32),
+ *                        accumulated in fp32; none may overlap another argument
+ *   causal, scale      : as in the forward call
+ * Scratch of 8 bytes per row comes from the library's pool.  Errors as for
+ * prefill: FA_ERR_NULL, FA_ERR_SHAPE, FA_ERR_HEAD_DIM, FA_ERR_DTYPE,
+ * FA_ERR_ALIGN, FA_ERR_SCALE, FA_ERR_ALIAS, FA_ERR_WORKSPACE, FA_ERR_ARCH,
+ * FA_ERR_CUDA.
+ */
+int fa_prefill_backward(const void *q, const void *k, const void *v,
+                        const void *out, const void *dout, const float *lse,
+                        void *dq, void *dk, void *dv, int B, int H, int N, int d,
+                        int causal, float scale, fa_dtype in_dtype,
+                        fa_dtype grad_dtype, void *stream);
+
+/*
  * The schedule fa_prefill_gqa would use for a dense problem on num_sms SMs
  * (num_sms <= 0: the current device's count).  Host arithmetic only, for
  * tuning and tests; nothing runs on a device.

@@ -165,3 +165,30 @@ def split_decode(q, k_cache, v_cache, seq_len, scale, chunk, tau=8.0, p_dtype=No
     cuts = list(range(chunk, n, chunk))
     return tiled_attention(q, k_cache[:n], v_cache[:n], False, scale, block=chunk, tau=tau,
                            cuts=cuts, p_dtype=p_dtype, out_dtype=out_dtype)[0]
+
+
+# ------------------------------------------------------------- backward model
+def backward_with_rounding(q, k, v, dout, causal, scale, p_dtype):
+    """Gradients computed with the backward kernels' rounding points, in fp64.
+
+    The forward (``tiled_attention`` with 16-bit weights) gives the output O,
+    rounded to p_dtype as a training step stores it, and the row log-sum-exp
+    lse = log(l) + m over the rounded weights it normalised by.  The backward
+    recomputes P = exp(s - lse), forms dP = dO V^T and D = rowsum(dO * O16),
+    dS = P (dP - D), and feeds the tensor-core products with 16-bit P and dS:
+    dV = P16^T dO, dK = scale dS16^T Q, dQ = scale dS16 K.
+    Returns (dq, dk, dv).  Square problems, one head: q, k, v, dout [N, d].
+    """
+    q, k, v, dout = (np.asarray(x, dtype=np.float64) for x in (q, k, v, dout))
+    n = q.shape[0]
+    vis = _visible(n, n, causal, 0)
+    o, m_ref, l = partial_over_keys(q, k, v, scale, vis, 0, n, 128, 8.0, p_dtype)
+    o16 = round_to(o / l[:, None], p_dtype)
+    lse = (m_ref + np.log2(l)) * math.log(2.0)
+    s = np.where(vis, scale * (q @ k.T), -np.inf)
+    p = np.exp(s - lse[:, None])
+    dp = dout @ v.T
+    dsum = (dout * o16).sum(axis=1)
+    ds = p * (dp - dsum[:, None])
+    p16, ds16 = round_to(p, p_dtype), round_to(ds, p_dtype)
+    return scale * ds16 @ k, scale * ds16.T @ q, p16.T @ dout

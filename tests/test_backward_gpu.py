@@ -1,0 +1,108 @@
+"""GPU parity of the backward pass (and the forward's log-sum-exp) against
+the fp64 oracle, through the C ABI.
+
+The inputs are 16-bit N(0,1) Q, K, V and an N(0,1) upstream gradient dO; the
+forward output O comes from the library itself in the input type (as a
+training step would have it).  The oracle differentiates the exact forward,
+so the bound per gradient tensor is relative to its largest entry (see the
+tolerance note below), checked on every element.
+"""
+import numpy as np
+import pytest
+
+from attention_forward_prefill_gb300 import inputs
+from tests import gpu_util as G
+
+pytestmark = pytest.mark.gpu
+
+# Rounding points of the kernels: P and dS enter the tensor core as 16-bit
+# (relative 2^-9 for bf16, 2^-12 for fp16), O (for D = dO.O) is the 16-bit
+# forward output, accumulation is fp32.  The fp64 model of those rounding
+# points (oracle/method_model.py, backward_with_rounding) puts the worst
+# element error at about 0.2% (bf16) / 0.03% (fp16) of max|G|; the kernels
+# measured up to 0.41% / 0.051% on these shapes.  The bounds below are 1% /
+# 0.15% of max|G| per tensor.
+REL_TOL = {"bf16": 1e-2, "f16": 1.5e-3}
+# The log-sum-exp sums the 16-bit weights the forward normalised by, so it
+# carries their rounding: at most about 2^-8 (bf16) / 2^-11 (fp16) in log units.
+LSE_TOL = {"bf16": 4e-3, "f16": 5e-4}
+
+
+@pytest.fixture(scope="module")
+def fa():
+    import torch
+    from attention_forward_prefill_gb300 import binding, build
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    assert torch.cuda.get_device_capability() == (10, 3), "libfa_gb300 targets sm_103a"
+    build.build()
+    binding.load()
+    assert binding.fa_device_status(True) == 0
+    yield binding
+    assert binding.fa_device_status(False) == 0, "a kernel watchdog fired"
+
+
+def run(fa, shape, dtype, causal, seed, grad="f32"):
+    import torch
+    q, k, v, g = (inputs.normal_bits(shape, seed + i, dtype) for i in range(4))
+    qd, kd, vd, gd = (G.bits_to_device(x, dtype) for x in (q, k, v, g))
+    scale = 1.0 / np.sqrt(shape[-1])
+    out, lse = fa.prefill_with_lse(qd, kd, vd, causal=causal, scale=scale)
+    dq, dk, dv = fa.prefill_backward(qd, kd, vd, out, gd, lse, causal=causal, scale=scale,
+                                     grad_dtype=G.torch_dtype(grad))
+    torch.cuda.synchronize()
+    return (q, k, v, g), scale, lse, (dq, dk, dv)
+
+
+def rel_err(got, want):
+    return float(np.abs(got - want).max() / max(np.abs(want).max(), 1e-30))
+
+
+@pytest.mark.parametrize("shape,dtype", [((1, 2, 128, 64), "f16"), ((2, 3, 257, 64), "f16"),
+                                         ((1, 2, 300, 128), "bf16"), ((1, 4, 1024, 128), "bf16"),
+                                         ((1, 2, 1000, 64), "bf16")])
+@pytest.mark.parametrize("causal", [False, True])
+def test_gradients_match_oracle(fa, oracle_mod, shape, dtype, causal):
+    (q, k, v, g), scale, lse, grads = run(fa, shape, dtype, causal, 3000 + shape[2])
+    f = [oracle_mod.bits_to_f64(x, dtype) for x in (q, k, v, g)]
+    want = oracle_mod.attention_backward(*f, causal, scale, threads=G.THREADS)
+    for name, got_t, w in zip(("dq", "dk", "dv"), grads, want):
+        e = rel_err(G.device_to_f64(got_t), w)
+        assert e <= REL_TOL[dtype], f"{name} {shape} {dtype} causal={causal}: {e:.3e}"
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_forward_lse_matches_oracle(fa, oracle_mod, causal):
+    shape, dtype = (2, 3, 700, 128), "bf16"
+    (q, k, v, g), scale, lse, _ = run(fa, shape, dtype, causal, 3100)
+    want = oracle_mod.attention_lse(oracle_mod.bits_to_f64(q, dtype), oracle_mod.bits_to_f64(k, dtype),
+                                    causal, scale)
+    assert np.abs(G.device_to_f64(lse) - want).max() <= LSE_TOL[dtype]
+
+
+def test_lse_under_the_stream_k_schedule(fa, oracle_mod):
+    # the fixup kernel writes the log-sum-exp of rows whose keys were cut
+    import torch
+    shape = (1, 3, 1000, 64)
+    q, k, v = (inputs.normal_bits(shape, 3200 + i, "f16") for i in range(3))
+    qd, kd, vd = (G.bits_to_device(x, "f16") for x in (q, k, v))
+    _, lse = fa.prefill_with_lse(qd, kd, vd, causal=False, scale=0.125,
+                                 flags=fa.FA_FLAG_SCHEDULE_STREAM_K)
+    torch.cuda.synchronize()
+    want = oracle_mod.attention_lse(oracle_mod.bits_to_f64(q, "f16"), oracle_mod.bits_to_f64(k, "f16"),
+                                    False, 0.125)
+    assert np.abs(G.device_to_f64(lse) - want).max() <= LSE_TOL["f16"]
+
+
+def test_gradients_are_bit_identical_run_to_run(fa):
+    import torch
+    a = run(fa, (2, 4, 1000, 128), "bf16", True, 3300, grad="bf16")[3]
+    b = run(fa, (2, 4, 1000, 128), "bf16", True, 3300, grad="bf16")[3]
+    for x, y in zip(a, b):
+        assert torch.equal(x.view(torch.int16), y.view(torch.int16))
+
+
+def test_key_gradients_sum_to_zero(fa):
+    # rows of dS sum to zero, so dK summed over the keys vanishes (fp32 grads)
+    (q, k, v, g), scale, lse, (dq, dk, dv) = run(fa, (1, 2, 512, 64), "f16", False, 3400)
+    s = G.device_to_f64(dk).sum(axis=2)
+    assert np.abs(s).max() <= 1e-3 * np.abs(G.device_to_f64(dk)).max() * 512 ** 0.5

@@ -118,3 +118,30 @@ def test_l_over_rounded_weights_is_an_exact_convex_combination():
 def test_bf16_rounding_helper_ties_to_even():
     x = np.array([1.0 + 2.0 ** -8, 1.0 + 3 * 2.0 ** -8, 1.0 + 2.0 ** -9, -2.5, 0.0])
     assert list(mm.round_to(x, "bf16")) == [1.0, 1.0 + 2.0 ** -6, 1.0, -2.5, 0.0]
+
+
+@pytest.mark.parametrize("dtype,bound", [("bf16", 1e-2), ("f16", 1.5e-3)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_rounding_model_fits_the_gradient_tolerance(oracle_mod, dtype, bound, causal):
+    # the kernels' rounding points predict errors well inside the GPU bound
+    # (max |err| / max |grad| per tensor), with at least a 2x margin
+    n, d = 300, 128 if dtype == "bf16" else 64
+    q, k, v, g = (oracle_mod.bits_to_f64(inputs.normal_bits((n, d), 70 + i, dtype), dtype)
+                  for i in range(4))
+    scale = 1.0 / np.sqrt(d)
+    got = mm.backward_with_rounding(q, k, v, g, causal, scale, dtype)
+    want = oracle_mod.attention_backward(q[None, None], k[None, None], v[None, None], g[None, None],
+                                         causal, scale)
+    for a, b in zip(got, want):
+        rel = np.abs(a - b[0, 0]).max() / np.abs(b).max()
+        assert rel <= bound / 2, rel
+
+
+def test_backward_model_without_rounding_is_exact(oracle_mod):
+    n, d = 200, 32
+    q, k, v, g = normal((4, n, d), 80)
+    got = mm.backward_with_rounding(q, k, v, g, True, 0.3, None)
+    want = oracle_mod.attention_backward(q[None, None], k[None, None], v[None, None], g[None, None],
+                                         True, 0.3)
+    for a, b in zip(got, want):
+        assert np.abs(a - b[0, 0]).max() <= 1e-11
