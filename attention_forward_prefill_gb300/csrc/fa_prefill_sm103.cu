@@ -109,6 +109,11 @@ struct Params {
     int stream_k;
     int HT;                // key-tile steps per (sequence, head) = pre[n_qb]
     long long W;           // BH * HT
+    // Non-causal stream-K first deals dp_full whole units to every CTA (unit
+    // blockIdx.x + k * gridDim.x); only the steps [sk_s0, W) after them are cut
+    // into equal ranges, so fewer units are split.  Causal: dp_full = sk_s0 = 0.
+    int dp_full;
+    long long sk_s0;
     float *ws_o;           // [gridDim.x][2 slots][256 rows][D]  unnormalised O
     float *ws_ml;          // [gridDim.x][2 slots][256 rows][2]  (m_ref, l)
 };
@@ -133,13 +138,14 @@ struct Work {
 
 struct SegCursor {
     long long s, s_end;  // stream-K step range
-    int u;               // unit-granular schedule
+    int u;               // unit-granular schedule; stream-K: whole units dealt so far
 };
 
 __device__ __forceinline__ void seg_begin(const Params &p, SegCursor &c) {
-    c.s = static_cast<long long>(blockIdx.x) * p.W / gridDim.x;
-    c.s_end = static_cast<long long>(blockIdx.x + 1) * p.W / gridDim.x;
-    c.u = blockIdx.x;
+    const long long span = p.W - p.sk_s0;
+    c.s = p.sk_s0 + static_cast<long long>(blockIdx.x) * span / gridDim.x;
+    c.s_end = p.sk_s0 + static_cast<long long>(blockIdx.x + 1) * span / gridDim.x;
+    c.u = p.stream_k ? 0 : blockIdx.x;
 }
 
 // Key tiles a 128-row query tile starting at row0 must visit.
@@ -176,7 +182,14 @@ __device__ __forceinline__ void load_seq(const Params &p, Work &w) {
 __device__ __forceinline__ bool seg_next(const Params &p, const StepTable &tab, SegCursor &c,
                                          Work &w) {
     int bh, qb;
-    if (p.stream_k) {
+    if (p.stream_k && c.u < p.dp_full) {  // a whole unit dealt before the cut ranges
+        w.u = blockIdx.x + c.u * gridDim.x;
+        ++c.u;
+        bh = w.u / p.n_qb;
+        qb = w.u % p.n_qb;
+        w.j0 = 0;
+        w.j1 = -1;
+    } else if (p.stream_k) {
         if (c.s >= c.s_end) return false;
         bh = static_cast<int>(c.s / p.HT);
         const int rem = static_cast<int>(c.s - static_cast<long long>(bh) * p.HT);
@@ -216,7 +229,9 @@ __device__ __forceinline__ bool seg_next(const Params &p, const StepTable &tab, 
     return true;
 }
 
-template <int D, bool BF16>
+// LSE: also write the row log-sum-exp (a separate instantiation, so that the
+// plain forward keeps its registers).
+template <int D, bool BF16, bool LSE>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap map_q,
                    const __grid_constant__ CUtensorMap map_k,
@@ -654,7 +669,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (partial) {
                 // Part of a unit: keep O unnormalised with its (m_ref, l) for the
                 // fixup kernel.  Slot 0 = the CTA's first piece, 1 = its last.
-                const size_t rec = (static_cast<size_t>(blockIdx.x) * 2 + (seg == 0 ? 0 : 1)) * kRowsPerUnit +
+                const size_t rec = (static_cast<size_t>(blockIdx.x) * 2 + (seg == p.dp_full ? 0 : 1)) * kRowsPerUnit +
                                    t * kBlockM + r;
                 float *wo = p.ws_o + rec * D;
 #pragma unroll
@@ -674,12 +689,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 continue;
             }
             const float inv = l > 0.f ? 1.0f / l : 0.f;  // l = 0: no visible key
-            if (p.lse != nullptr && row_ok) {
-                // the row's index in [B][Hq][Nq] (dense) or [tokens][Hq] (packed) is its
-                // output offset in elements divided by d
-                const long long li = ((orow - reinterpret_cast<uint8_t *>(p.out)) >> (osize == 4 ? 2 : 1)) / D;
-                p.lse[li] = l > 0.f ? (m_ref + __log2f(l)) * 0.6931471805599453f : -INFINITY;
-            }
 #pragma unroll
             for (int q = 0; q < D / 32; ++q) {
                 uint32_t o[32];
@@ -689,6 +698,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (row_ok) store_out32(orow + q * 32 * osize, o, inv, p.out_dtype);
             }
             tc_fence_before();
+            if (LSE && row_ok) {
+                // the row's index in [B][Hq][Nq] (dense) or [tokens][Hq] (packed) is its
+                // output offset in elements divided by d
+                const long long li = ((orow - reinterpret_cast<uint8_t *>(p.out)) >> (osize == 4 ? 2 : 1)) / D;
+                p.lse[li] = l > 0.f ? (m_ref + __log2f(l)) * 0.6931471805599453f : -INFINITY;
+            }
         }
     } else {
         regs_shrink<kRegsOther>();  // idle warps 10-11
@@ -720,6 +735,7 @@ struct FixupParams {
     int causal, no_skip;
     int G;
     long long W;
+    long long sk_s0;                 // first step of the cut ranges
     int out_dtype;
     int n_split;
     int4 item[kMaxSplit];            // (unit, first CTA, last CTA, unit's key-tile steps)
@@ -742,7 +758,7 @@ __global__ void __launch_bounds__(256) prefill_fixup(const __grid_constant__ Fix
     const int tile_row0 = qb * kRowsPerUnit + (rrow / kBlockM) * kBlockM;
     const int n_t = kv_tiles(f.causal, f.no_skip, f.Nq, f.Nk, f.Nk - f.Nq, tile_row0);
     const long long ustart = f.ustart[blockIdx.x];
-    auto first_of = [&](int c) { return static_cast<long long>(c) * f.W / f.G; };
+    auto first_of = [&](int c) { return f.sk_s0 + static_cast<long long>(c) * (f.W - f.sk_s0) / f.G; };
     // piece of CTA c: (record, first key tile of the piece within the unit)
     auto piece = [&](int c, int &j_first) {
         const long long first = first_of(c);
@@ -828,6 +844,8 @@ struct Plan {
     int n_qb;
     int HT;
     long long W;
+    int dp_full;
+    long long sk_s0;
     int n_split;
     int4 item[kMaxSplit];         // (unit, first CTA, last CTA, unit's steps)
     long long ustart[kMaxSplit];  // first step of the unit
@@ -850,6 +868,8 @@ void make_plan(bool packed, int B, int Hq, int Nq, int Nk, int causal, int no_sk
     pl.n_qb = n_qb;
     pl.HT = 0;
     pl.W = 0;
+    pl.dp_full = 0;
+    pl.sk_s0 = 0;
     pl.n_split = 0;
     pl.grid = n_units < num_sms ? n_units : num_sms;
     pl.tab.pre[0] = 0;
@@ -888,9 +908,17 @@ void make_plan(bool packed, int B, int Hq, int Nq, int Nk, int causal, int no_sk
     pl.W = W;
     const int grid = sms;
     pl.grid = grid;
-    auto first_step = [&](long long c) { return c * W / grid; };
+    // Non-causal units all cost the same: deal whole units round robin first
+    // and cut only the remainder (every CTA still does about W / G steps).
+    if (!causal) {
+        pl.dp_full = n_units / grid;
+        pl.sk_s0 = static_cast<long long>(pl.dp_full) * grid * pre[1];
+    }
+    const long long s0 = pl.sk_s0, span = W - s0;
+    if (span == 0) return;  // whole units only: nothing is cut
+    auto first_step = [&](long long c) { return s0 + c * span / grid; };
     auto cta_of = [&](long long step) {  // c with first_step(c) <= step < first_step(c + 1)
-        long long c = (step + 1) * grid / W;
+        long long c = (step - s0 + 1) * grid / span;
         if (c >= grid) c = grid - 1;
         while (c > 0 && first_step(c) > step) --c;
         while (c + 1 < grid && first_step(c + 1) <= step) ++c;
@@ -919,8 +947,8 @@ void make_plan(bool packed, int B, int Hq, int Nq, int Nk, int causal, int no_sk
     }
 }
 
-template <int D, bool BF16>
-int launch_d(const PrefillLaunch &a, const DeviceInfo &dev, cudaStream_t stream) {
+template <int D, bool BF16, bool LSE>
+int launch_d_lse(const PrefillLaunch &a, const DeviceInfo &dev, cudaStream_t stream) {
     using L = Layout<D>;
     static_assert(L::kSmemBytes <= 227 * 1024, "shared memory budget");
     const bool packed = a.cu_q != nullptr;
@@ -935,13 +963,13 @@ int launch_d(const PrefillLaunch &a, const DeviceInfo &dev, cudaStream_t stream)
         if ((rc = make_map(&mk, a.k, D, false, a.Nk, (long long)a.B * a.Hkv, a.in_bf16)) != FA_OK) return rc;
         if ((rc = make_map(&mv, a.v, D, false, a.Nk, (long long)a.B * a.Hkv, a.in_bf16)) != FA_OK) return rc;
     }
-    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D, BF16>,
+    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D, BF16, LSE>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
     if (e != cudaSuccess) return cuda_fail(e);
     // The setmaxnreg split inside the kernel draws on the launch allocation:
     // refuse to launch a build whose register count would make it wait forever.
     cudaFuncAttributes fattr;
-    e = cudaFuncGetAttributes(&fattr, prefill_kernel<D, BF16>);
+    e = cudaFuncGetAttributes(&fattr, prefill_kernel<D, BF16, LSE>);
     if (e != cudaSuccess) return cuda_fail(e);
     if (fattr.numRegs < kMinLaunchRegs) return cuda_fail(cudaErrorInvalidConfiguration);
 
@@ -982,6 +1010,8 @@ int launch_d(const PrefillLaunch &a, const DeviceInfo &dev, cudaStream_t stream)
     p.stream_k = pl.stream_k;
     p.HT = pl.HT;
     p.W = pl.W;
+    p.dp_full = pl.dp_full;
+    p.sk_s0 = pl.sk_s0;
     const int grid = pl.grid;
     static thread_local FixupParams f;
     f.n_split = 0;
@@ -997,6 +1027,7 @@ int launch_d(const PrefillLaunch &a, const DeviceInfo &dev, cudaStream_t stream)
         f.no_skip = p.no_skip;
         f.G = grid;
         f.W = p.W;
+        f.sk_s0 = pl.sk_s0;
         f.out_dtype = a.out_dtype;
         f.n_split = pl.n_split;
         for (int i = 0; i < pl.n_split; ++i) {
@@ -1018,7 +1049,7 @@ int launch_d(const PrefillLaunch &a, const DeviceInfo &dev, cudaStream_t stream)
         }
     }
     const StepTable &tab = pl.tab;
-    prefill_kernel<D, BF16><<<grid, kThreads, L::kSmemBytes, stream>>>(mq, mk, mv, p, tab);
+    prefill_kernel<D, BF16, LSE><<<grid, kThreads, L::kSmemBytes, stream>>>(mq, mk, mv, p, tab);
     e = cudaGetLastError();
     if (e == cudaSuccess && f.n_split > 0) {
         cudaLaunchConfig_t cfg = {};
@@ -1053,6 +1084,8 @@ int plan_prefill(int B, int Hq, int Nq, int Nk, int causal, int no_skip, int sch
     info[3] = pl.HT;
     info[4] = pl.n_qb;
     info[5] = pl.n_split;
+    info[6] = pl.dp_full;
+    info[7] = pl.sk_s0;
     if (items)
         for (int i = 0; i < pl.n_split && i < max_items; ++i) {
             items[i * 5 + 0] = pl.item[i].x;
@@ -1062,6 +1095,11 @@ int plan_prefill(int B, int Hq, int Nq, int Nk, int causal, int no_skip, int sch
             items[i * 5 + 4] = pl.ustart[i];
         }
     return FA_OK;
+}
+
+template <int D, bool BF16>
+int launch_d(const PrefillLaunch &a, const DeviceInfo &dev, cudaStream_t stream) {
+    return a.lse ? launch_d_lse<D, BF16, true>(a, dev, stream) : launch_d_lse<D, BF16, false>(a, dev, stream);
 }
 
 int launch_prefill(const PrefillLaunch &a, const DeviceInfo &dev, cudaStream_t stream) {

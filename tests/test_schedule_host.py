@@ -36,7 +36,7 @@ def kv_tiles(causal, no_skip, nq, nk, row0):
 def check_plan(B, H, Nq, Nk, causal, no_skip, sms, flags):
     rc, info, items = binding.fa_prefill_plan(B, H, Nq, Nk, causal, flags, sms)
     assert rc == 0
-    stream_k, G, W, HT, n_qb, n_split = info
+    stream_k, G, W, HT, n_qb, n_split, dp_full, s0 = info
     assert n_qb == (Nq + R - 1) // R and len(items) == n_split
     n_units = B * H * n_qb
     if not stream_k:
@@ -50,10 +50,19 @@ def check_plan(B, H, Nq, Nk, causal, no_skip, sms, flags):
         assert c >= 1
         pre.append(pre[-1] + c)
     assert HT == pre[-1] and W == B * H * HT
-    fs = lambda c: c * W // G
+    if causal:
+        assert dp_full == 0 and s0 == 0
+    else:                                    # whole units first, then the cut ranges
+        assert dp_full == n_units // G and s0 == dp_full * G * cost[0]
+    fs = lambda c: s0 + c * (W - s0) // G
     writes, whole = {}, set()
     for c in range(G):                       # the kernel's per-CTA walk
-        s, e, seg = fs(c), fs(c + 1), 0
+        for kk in range(dp_full):
+            u = c + kk * G
+            for t in range(2):
+                if kv_tiles(causal, no_skip, Nq, Nk, (u % n_qb) * R + t * BM) > 0:
+                    whole.add((u, t))
+        s, e, seg = fs(c), fs(c + 1), dp_full
         while s < e:
             bh, rem = divmod(s, HT)
             qb = bisect.bisect_right(pre, rem) - 1
@@ -67,7 +76,7 @@ def check_plan(B, H, Nq, Nk, causal, no_skip, sms, flags):
                 if nt <= j0:
                     continue
                 if partial:
-                    key = (c, 0 if seg == 0 else 1, t)
+                    key = (c, 0 if seg == dp_full else 1, t)
                     assert key not in writes
                     writes[key] = (u, j0, nt)
                 else:
@@ -136,6 +145,14 @@ def test_rule_choices_on_the_benchmark_shapes(lib):
     for (B, H, N, causal), sk in want.items():
         _, info, _ = binding.fa_prefill_plan(B, H, N, N, causal, 0, 152)
         assert info[0] == sk, (B, H, N, causal)
+
+
+def test_whole_units_first_cut_fewer(lib):
+    # N = 8192, 16 heads: 512 units on 152 CTAs -> 3 whole units each, and only
+    # the last 56 units are cut between CTAs
+    _, info, items = binding.fa_prefill_plan(1, 16, 8192, 8192, 0, 0, 152)
+    assert info[0] == 1 and info[6] == 3 and info[7] == 3 * 152 * 64
+    assert len(items) <= 56 and all(it[0] >= 3 * 152 for it in items)
 
 
 def test_units_flag_and_packed_rows_never_cut(lib):
