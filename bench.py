@@ -42,9 +42,11 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 NCU_TRAFFIC = {
     # Measured at N=8192 (ncu --set full, profiles/prefill_kernel_d128_n8192.md);
     # the other lengths are scaled by the bytes the launch must move (linear in N).
-    "prefill": {"src_sha": "bd4267fe943e3762",
-                "bytes_per_launch": {"4096": 124.65e6 / 2, "8192": 124.65e6, "16384": 124.65e6 * 2},
+    "prefill": {"src": "fa_prefill_sm103.cu", "src_sha": "0f278391e7aae731",
+                "bytes_per_launch": {"4096": 115.71e6 / 2, "8192": 115.71e6, "16384": 115.71e6 * 2},
                 "measured_at": "8192", "scaled": ["4096", "16384"]},
+    # B=32, H=14 (profiles/decode_split_b32_h14.md): DRAM bytes of one split-kernel launch
+    "decode": {"src": "fa_decode_sm103.cu", "src_sha": "4ff185fa2bee8b5b", "bytes_per_launch": 263.6e6},
 }
 
 
@@ -204,6 +206,12 @@ def run_ours(args):
     cases = args.case.split(",") if args.case else None
     do_pre = [N for N in PREFILL_NS if cases is None or f"prefill:{N}" in cases]
     do_dec = cases is None or "decode" in cases
+    # backward (training) case, only when asked for: B=1, H=16, N=4096, d=128, bf16
+    do_bwd = cases is not None and "backward" in cases
+    if do_bwd:
+        bq, bk, bv, bdo = (torch.randn((1, 16, 4096, PREFILL_D), device=device).to(torch.bfloat16)
+                           for _ in range(4))
+        bout, blse = binding.prefill_with_lse(bq, bk, bv, causal=False, scale=scale_p)
 
     def step(record):
         ev = []
@@ -225,6 +233,14 @@ def run_ours(args):
                            out=dout)
             e1.record(stream)
             ev.append(("decode", 0, e0, e1))
+        if do_bwd:
+            flush.zero_()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            binding.prefill_backward(bq, bk, bv, bout, bdo, blse, causal=False, scale=scale_p)
+            e1.record(stream)
+            ev.append(("backward", 4096, e0, e1))
         if record is not None:
             record.append(ev)
 
@@ -255,9 +271,11 @@ def run_ours(args):
 
     pre_ms = {N: [] for N in do_pre}
     dec_ms = []
+    bwd_ms = []
     for ev in records:
         for kind, N, e0, e1 in ev:
-            (pre_ms[N] if kind == "prefill" else dec_ms).append(e0.elapsed_time(e1))
+            {"prefill": pre_ms.get(N), "decode": dec_ms, "backward": bwd_ms}[kind].append(
+                e0.elapsed_time(e1))
     pre_time_s = sum(sum(v) for v in pre_ms.values()) / 1e3
     pre_flops = sum(prefill_flops(PREFILL_B, PREFILL_H, N, PREFILL_D) for N in do_pre) * args.steps
     dec_time_s = sum(dec_ms) / 1e3
@@ -303,7 +321,8 @@ def run_ours(args):
         return None
 
     value = tot_flops / tot_s / 1e12 if do_pre else None
-    n_launch = len(do_pre) * args.steps + (2 * args.steps if do_dec else 0)
+    n_launch = (len(do_pre) * args.steps + (2 * args.steps if do_dec else 0)
+                + (3 * args.steps if do_bwd else 0))
     detail = {}
     for N in do_pre:
         ms = statistics.median(pre_ms[N])
@@ -312,7 +331,7 @@ def run_ours(args):
                                    "tflops": round(tf, 1)}
     traffic = None
     rec = NCU_TRAFFIC.get("prefill")
-    if rec and rec.get("src_sha") == src_sha("fa_prefill_sm103.cu") and do_pre:
+    if rec and rec.get("src_sha") == src_sha(rec["src"]) and do_pre:
         per = [rec["bytes_per_launch"].get(str(N)) for N in do_pre]
         if all(x is not None for x in per):
             traffic = sum(per) / len(per)
@@ -359,6 +378,9 @@ def run_ours(args):
         "cpu_baseline": cpu,
     }
     if do_dec:
+        drec = NCU_TRAFFIC.get("decode")
+        dec_traffic = (drec["bytes_per_launch"] if drec and drec["src_sha"] == src_sha(drec["src"])
+                       else None)
         gbs = tot_dec_bytes / dec_s_max / 1e9
         line["decode"] = {
             "value": round(gbs, 1), "unit": "GB/s", "dtype": "f16",
@@ -366,8 +388,12 @@ def run_ours(args):
             "kv_bytes_per_step": decode_bytes(lens_np, DECODE_H, DECODE_D),
             "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
                          "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4),
-                         "traffic": None, "peak_source": f"{peak_src} copy bandwidth"},
+                         "traffic": dec_traffic, "peak_source": f"{peak_src} copy bandwidth"},
         }
+    if do_bwd and bwd_ms:
+        ms = statistics.median(bwd_ms)
+        line["backward"] = {"shape": [1, 16, 4096, PREFILL_D], "median_ms": round(ms, 4),
+                            "tflops": round(10.0 * 16 * 4096 ** 2 * PREFILL_D / (ms / 1e3) / 1e12, 1)}
     if world > 1:
         dist.destroy_process_group()
     return line
