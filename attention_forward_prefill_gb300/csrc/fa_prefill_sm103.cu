@@ -833,9 +833,9 @@ int host_kv_tiles(int causal, int no_skip, int nq, int nk, int row0) {
 
 // Stream-K costs, in key-tile steps, fitted to measured launch times on GB300
 // (d = 64 and 128, dense and causal): cutting units between CTAs costs about
-// 20 steps (partial writes, extra pipeline fills, the fixup pass), and a causal
+// 15 steps (partial writes, extra pipeline fills, the fixup pass), and a causal
 // stream-K step runs about 8% slower than a step of the unit schedule.
-constexpr long long kMergeCostSteps = 20;
+constexpr long long kMergeCostSteps = 15;
 constexpr long long kCausalStepPct = 108;
 
 struct Plan {
