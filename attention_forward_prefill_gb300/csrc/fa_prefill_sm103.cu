@@ -138,14 +138,14 @@ struct Work {
 
 struct SegCursor {
     long long s, s_end;  // stream-K step range
-    int u;               // unit-granular schedule; stream-K: whole units dealt so far
+    int u;               // units taken so far (unit schedule: rounds of gridDim.x units)
 };
 
 __device__ __forceinline__ void seg_begin(const Params &p, SegCursor &c) {
     const long long span = p.W - p.sk_s0;
     c.s = p.sk_s0 + static_cast<long long>(blockIdx.x) * span / gridDim.x;
     c.s_end = p.sk_s0 + static_cast<long long>(blockIdx.x + 1) * span / gridDim.x;
-    c.u = p.stream_k ? 0 : blockIdx.x;
+    c.u = 0;
 }
 
 // Key tiles a 128-row query tile starting at row0 must visit.
@@ -206,9 +206,13 @@ __device__ __forceinline__ bool seg_next(const Params &p, const StepTable &tab, 
         c.s += w.j1 - w.j0;
         w.u = bh * p.n_qb + qb;
     } else {
-        if (c.u >= p.n_units) return false;
-        w.u = c.u;
-        c.u += gridDim.x;
+        // Round k deals units [k G, (k + 1) G); odd rounds in reverse CTA order
+        // ("snake"), so a CTA that drew a heavy causal block draws a light one next.
+        const int k = c.u++;
+        const int r = (k & 1) ? static_cast<int>(gridDim.x) - 1 - static_cast<int>(blockIdx.x)
+                              : static_cast<int>(blockIdx.x);
+        w.u = k * static_cast<int>(gridDim.x) + r;
+        if (w.u >= p.n_units) return false;
         if (p.causal) {  // heaviest query blocks first
             qb = p.n_qb - 1 - w.u / p.BH;
             bh = w.u % p.BH;
@@ -833,9 +837,11 @@ int host_kv_tiles(int causal, int no_skip, int nq, int nk, int row0) {
 
 // Stream-K costs, in key-tile steps, fitted to measured launch times on GB300
 // (d = 64 and 128, dense and causal): cutting units between CTAs costs about
-// 15 steps (partial writes, extra pipeline fills, the fixup pass), and a causal
-// stream-K step runs about 8% slower than a step of the unit schedule.
+// 15 steps (partial writes, extra pipeline fills, the fixup pass) when the
+// units are non-causal and 20 when they are causal, and a causal stream-K step
+// runs about 8% slower than a step of the unit schedule.
 constexpr long long kMergeCostSteps = 15;
+constexpr long long kCausalMergeCostSteps = 20;
 constexpr long long kCausalStepPct = 108;
 
 struct Plan {
@@ -853,7 +859,7 @@ struct Plan {
 };
 
 // The schedule of a problem, from the shapes and the SM count only.  Unit by
-// unit (static round robin, heaviest causal blocks first) the busiest CTA does
+// unit (rounds of G units dealt in snake order, heaviest causal blocks first) the busiest CTA does
 // `busiest` key-tile steps; cut into equal step ranges (stream-K) it does W / G
 // (8% dearer when causal) plus the merge cost.  Take the cheaper, unless
 // `schedule` forces one (1 units, 2 stream-K).  Stream-K needs every unit's
@@ -891,16 +897,18 @@ void make_plan(bool packed, int B, int Hq, int Nq, int Nk, int causal, int no_sk
         if (causal) {
             static thread_local long long load[1024];
             for (int c = 0; c < gu; ++c) load[c] = 0;
-            for (int u = 0; u < n_units; ++u) {
+            for (int u = 0; u < n_units; ++u) {  // the kernel's snake order
                 const int qb = n_qb - 1 - u / BH;
-                load[u % gu] += pre[qb + 1] - pre[qb];
+                const int k = u / gu, r = u % gu;
+                load[(k & 1) ? gu - 1 - r : r] += pre[qb + 1] - pre[qb];
             }
             for (int c = 0; c < gu; ++c) busiest = std::max(busiest, load[c]);
         } else {
             busiest = static_cast<long long>((n_units + gu - 1) / gu) * pre[1];
         }
         const long long pct = causal ? kCausalStepPct : 100;
-        take = (W * pct + 100LL * sms - 1) / (100LL * sms) + kMergeCostSteps < busiest;
+        take = (W * pct + 100LL * sms - 1) / (100LL * sms) +
+                   (causal ? kCausalMergeCostSteps : kMergeCostSteps) < busiest;
     }
     if (!take) return;
     pl.stream_k = 1;

@@ -140,8 +140,9 @@ def test_random_shapes_forced_stream_k(lib):
 
 def test_rule_choices_on_the_benchmark_shapes(lib):
     # the fitted rule: stream-K where it measured faster on 152 SMs
+    # (causal shapes now balance well enough unit by unit in snake order)
     want = {(1, 16, 4096, 0): 0, (1, 16, 8192, 0): 1, (1, 16, 16384, 0): 1, (8, 32, 8192, 1): 0,
-            (1, 16, 8192, 1): 1, (1, 12, 2048, 1): 0, (4, 12, 2048, 0): 0}
+            (1, 16, 8192, 1): 0, (1, 12, 2048, 1): 0, (4, 12, 2048, 0): 0, (2, 16, 4096, 0): 1}
     for (B, H, N, causal), sk in want.items():
         _, info, _ = binding.fa_prefill_plan(B, H, N, N, causal, 0, 152)
         assert info[0] == sk, (B, H, N, causal)
