@@ -283,28 +283,35 @@ def attention_backward(q: np.ndarray, k: np.ndarray, v: np.ndarray, dout: np.nda
                        causal: bool, scale: float, threads: int = 1):
     """(dQ, dK, dV) of O = softmax(scale Q K^T [mask]) V for the upstream gradient dO.
 
-    q, dout: [B, H, Nq, d]; k, v: [B, H, Nk, d] (float64).  Causal alignment as
-    in ``attention``.  Heads are independent and may be spread over threads.
+    q, dout: [B, Hq, Nq, d]; k, v: [B, Hkv, Nk, d] (float64), Hkv | Hq with
+    query head h reading key/value head h // (Hq // Hkv) as in ``attention``;
+    the gradient of a shared key/value head is the sum over the query heads
+    that read it (the chain rule through the repeat).  Causal alignment as in
+    ``attention``.  Heads are independent and may be spread over threads.
     """
     q = np.ascontiguousarray(q, dtype=np.float64)
     k = np.ascontiguousarray(k, dtype=np.float64)
     v = np.ascontiguousarray(v, dtype=np.float64)
     dout = np.ascontiguousarray(dout, dtype=np.float64)
     B, H, n_q, d = q.shape
-    n_k = k.shape[2]
+    h_kv, n_k = k.shape[1], k.shape[2]
+    if H % h_kv != 0:
+        raise ValueError("Hkv must divide Hq")
+    group = H // h_kv
     dq = np.zeros_like(q)
-    dk = np.zeros_like(k)
-    dv = np.zeros_like(v)
+    dk_h = np.zeros((B, H, n_k, d))   # per query head, summed into the shared heads below
+    dv_h = np.zeros((B, H, n_k, d))
     lib = _load()
 
     def one(bh):
         b, h = divmod(bh, H)
+        hk = h // group
         a, bb, c = np.zeros((n_q, d)), np.zeros((n_k, d)), np.zeros((n_k, d))
-        if lib.oracle_backward_head(_dptr(q[b, h]), _dptr(k[b, h]), _dptr(v[b, h]),
+        if lib.oracle_backward_head(_dptr(q[b, h]), _dptr(k[b, hk]), _dptr(v[b, hk]),
                                     _dptr(dout[b, h]), n_q, n_k, d, int(bool(causal)),
                                     float(scale), _dptr(a), _dptr(bb), _dptr(c)) != 0:
             raise RuntimeError("oracle_backward_head failed")
-        dq[b, h], dk[b, h], dv[b, h] = a, bb, c
+        dq[b, h], dk_h[b, h], dv_h[b, h] = a, bb, c
 
     if threads > 1 and B * H > 1:
         with ThreadPoolExecutor(max_workers=threads) as ex:
@@ -312,4 +319,9 @@ def attention_backward(q: np.ndarray, k: np.ndarray, v: np.ndarray, dout: np.nda
     else:
         for bh in range(B * H):
             one(bh)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    for h in range(H):          # in query-head order
+        dk[:, h // group] += dk_h[:, h]
+        dv[:, h // group] += dv_h[:, h]
     return dq, dk, dv

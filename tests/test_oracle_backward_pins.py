@@ -82,3 +82,21 @@ def test_lse_closed_forms_and_library(oracle_mod):
     # the weights the backward recomputes: exp(s - lse) equals the forward's P
     p = oracle_mod.attention_weights(q[0, 0], k[0, 0], False, 0.5)
     assert np.max(np.abs(np.exp(s - want[:, None]) - p)) < 1e-14
+
+
+def test_grouped_head_gradients_match_library_autograd(oracle_mod):
+    # a shared key/value head collects the gradients of every query head that
+    # reads it: torch's own grouped SDPA in float64 differentiates the same thing
+    torch = pytest.importorskip("torch")
+    r = rng(34)
+    B, Hq, Hkv, N, d = 1, 6, 2, 21, 8
+    q, g = r.normal(size=(2, B, Hq, N, d))
+    k, v = r.normal(size=(2, B, Hkv, N, d))
+    tq, tk, tv = (torch.tensor(x, requires_grad=True) for x in (q, k, v))
+    out = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, is_causal=True, scale=0.3,
+                                                           enable_gqa=True)
+    out.backward(torch.from_numpy(g))
+    dq, dk, dv = oracle_mod.attention_backward(q, k, v, g, True, 0.3)
+    for ours, theirs in ((dq, tq.grad), (dk, tk.grad), (dv, tv.grad)):
+        assert ours.shape == tuple(theirs.shape)
+        assert np.max(np.abs(ours - theirs.numpy())) < 1e-12
