@@ -40,7 +40,7 @@ _SIGNATURES = {
     "fa_prefill_lse": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _f, _i, _i, _u,
                             _vp]),
     "fa_prefill_backward": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i,
-                                 _f, _i, _i, _vp]),
+                                 _i, _f, _i, _i, _vp]),
     "fa_prefill_plan": (_i, [_i, _i, _i, _i, _i, _u, _i, _vp, _vp, _i]),
     "fa_decode": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _vp]),
     "fa_decode_ex": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _i, _i, _vp, _sz, _vp]),
@@ -122,10 +122,10 @@ def fa_prefill_lse(q, k, v, out, lse, B, Hq, Hkv, Nq, Nk, d, causal, scale, in_d
                                  float(scale), in_dtype, out_dtype, flags, stream)
 
 
-def fa_prefill_backward(q, k, v, out, dout, lse, dq, dk, dv, B, H, N, d, causal, scale, in_dtype,
-                        grad_dtype, stream=0) -> int:
-    return load().fa_prefill_backward(q, k, v, out, dout, lse, dq, dk, dv, B, H, N, d, int(causal),
-                                      float(scale), in_dtype, grad_dtype, stream)
+def fa_prefill_backward(q, k, v, out, dout, lse, dq, dk, dv, B, H, Hkv, N, d, causal, scale,
+                        in_dtype, grad_dtype, stream=0) -> int:
+    return load().fa_prefill_backward(q, k, v, out, dout, lse, dq, dk, dv, B, H, Hkv, N, d,
+                                      int(causal), float(scale), in_dtype, grad_dtype, stream)
 
 
 def fa_prefill_plan(B, Hq, Nq, Nk, causal, flags=0, num_sms=0, max_items=192):
@@ -297,19 +297,26 @@ def prefill_with_lse(q, k, v, causal: bool = False, scale: float | None = None, 
 
 def prefill_backward(q, k, v, out, dout, lse, causal: bool = False, scale: float | None = None,
                      grad_dtype=None):
-    """(dq, dk, dv) for square multi-head prefill, from the forward's out and lse."""
+    """(dq, dk, dv) for square prefill with q, out, dout [B, H, N, d] and k, v
+    [B, Hkv, N, d], from the forward's out and lse; dk, dv have k's shape."""
     torch = _torch()
     B, H, N, d = q.shape
-    for name, t in (("q", q), ("k", k), ("v", v), ("out", out), ("dout", dout)):
+    for name, t in (("q", q), ("out", out), ("dout", dout)):
         _check_cuda(name, t, q.shape, q.dtype)
+    _check_cuda("k", k, None, q.dtype)
+    if k.dim() != 4 or k.shape[0] != B or k.shape[2] != N or k.shape[3] != d:
+        raise ValueError(f"k has shape {tuple(k.shape)}, expected [{B}, Hkv, {N}, {d}]")
+    _check_cuda("v", v, k.shape, q.dtype)
+    Hkv = k.shape[1]
     _check_cuda("lse", lse, (B, H, N), torch.float32)
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     grad_dtype = q.dtype if grad_dtype is None else grad_dtype
-    dq, dk, dv = (torch.empty(q.shape, dtype=grad_dtype, device=q.device) for _ in range(3))
+    dq = torch.empty(q.shape, dtype=grad_dtype, device=q.device)
+    dk, dv = (torch.empty(k.shape, dtype=grad_dtype, device=q.device) for _ in range(2))
     rc = fa_prefill_backward(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
                              dout.data_ptr(), lse.data_ptr(), dq.data_ptr(), dk.data_ptr(),
-                             dv.data_ptr(), B, H, N, d, causal, scale, dtype_code(q.dtype),
+                             dv.data_ptr(), B, H, Hkv, N, d, causal, scale, dtype_code(q.dtype),
                              dtype_code(grad_dtype), _stream_handle(q.device))
     if rc != FA_OK:
         raise FaError(rc, "fa_prefill_backward")

@@ -294,10 +294,12 @@ int fa_prefill_plan(int B, int Hq, int Nq, int Nk, int causal, unsigned flags, i
 
 int fa_prefill_backward(const void *q, const void *k, const void *v, const void *out,
                         const void *dout, const float *lse, void *dq, void *dk, void *dv, int B,
-                        int H, int N, int d, int causal, float scale, fa_dtype in_dtype,
+                        int H, int Hkv, int N, int d, int causal, float scale, fa_dtype in_dtype,
                         fa_dtype grad_dtype, void *stream) {
     if (!q || !k || !v || !out || !dout || !lse || !dq || !dk || !dv) return FA_ERR_NULL;
-    if (B < 1 || H < 1 || N < 1 || static_cast<long long>(B) * H * N > INT_MAX) return FA_ERR_SHAPE;
+    if (B < 1 || H < 1 || Hkv < 1 || N < 1 || H % Hkv != 0 ||
+        static_cast<long long>(B) * H * N > INT_MAX)
+        return FA_ERR_SHAPE;
     if (d != 64 && d != 128) return FA_ERR_HEAD_DIM;
     if (in_dtype != FA_F16 && in_dtype != FA_BF16) return FA_ERR_DTYPE;
     if (grad_dtype != FA_F16 && grad_dtype != FA_BF16 && grad_dtype != FA_F32) return FA_ERR_DTYPE;
@@ -306,16 +308,19 @@ int fa_prefill_backward(const void *q, const void *k, const void *v, const void 
         return FA_ERR_ALIGN;
     if (!std::isfinite(scale)) return FA_ERR_SCALE;
     const size_t in_bytes = static_cast<size_t>(B) * H * N * d * 2;
-    const size_t g_bytes = static_cast<size_t>(B) * H * N * d * dtype_size(grad_dtype);
+    const size_t kv_bytes = static_cast<size_t>(B) * Hkv * N * d * 2;
+    const size_t gq_bytes = static_cast<size_t>(B) * H * N * d * dtype_size(grad_dtype);
+    const size_t gkv_bytes = static_cast<size_t>(B) * Hkv * N * d * dtype_size(grad_dtype);
     const size_t lse_bytes = static_cast<size_t>(B) * H * N * 4;
     const void *ins[6] = {q, k, v, out, dout, lse};
-    const size_t in_sz[6] = {in_bytes, in_bytes, in_bytes, in_bytes, in_bytes, lse_bytes};
+    const size_t in_sz[6] = {in_bytes, kv_bytes, kv_bytes, in_bytes, in_bytes, lse_bytes};
     void *gs[3] = {dq, dk, dv};
+    const size_t g_sz[3] = {gq_bytes, gkv_bytes, gkv_bytes};
     for (int g = 0; g < 3; ++g) {
         for (int i = 0; i < 6; ++i)
-            if (overlaps(gs[g], g_bytes, ins[i], in_sz[i])) return FA_ERR_ALIAS;
+            if (overlaps(gs[g], g_sz[g], ins[i], in_sz[i])) return FA_ERR_ALIAS;
         for (int h = g + 1; h < 3; ++h)
-            if (overlaps(gs[g], g_bytes, gs[h], g_bytes)) return FA_ERR_ALIAS;
+            if (overlaps(gs[g], g_sz[g], gs[h], g_sz[h])) return FA_ERR_ALIAS;
     }
     DeviceInfo dev;
     int rc = current_device_info(&dev);
@@ -332,6 +337,7 @@ int fa_prefill_backward(const void *q, const void *k, const void *v, const void 
     a.dv = dv;
     a.B = B;
     a.H = H;
+    a.Hkv = Hkv;
     a.N = N;
     a.d = d;
     a.causal = causal ? 1 : 0;

@@ -12,10 +12,11 @@
 //
 // Three kernels, no atomics, so every gradient is bit-identical run to run:
 //   bwd_prep   D_i and L2_i = L_i log2 e for every row (fp32);
-//   bwd_dkdv   one CTA per 128-key tile: S^T = K Q_i^T and dP^T = V dO_i^T in
-//              TMEM, P^T and dS^T written back over them as 16-bit, then
-//              dV += P^T dO_i and dK += dS^T Q_i accumulate in TMEM over the
-//              query tiles that see the keys;
+//   bwd_dkdv   one CTA per 128-key tile of a key/value head: S^T = K Q_i^T and
+//              dP^T = V dO_i^T in TMEM, P^T and dS^T written back over them as
+//              16-bit, then dV += P^T dO_i and dK += dS^T Q_i accumulate in TMEM
+//              over the query tiles that see the keys, of every query head
+//              that reads this key/value head;
 //   bwd_dq     one CTA per 128-query tile: S = Q K_j^T, dP = dO V_j^T, dS over
 //              dP, dQ += dS K_j over the key tiles the queries see.
 // Warp roles per CTA (192 threads): warps 0-3 elementwise work, thread = TMEM
@@ -56,10 +57,11 @@ struct BwdLayout {
 };
 
 struct BwdParams {
-    const float *lse2;  // [BH][N] row log-sum-exp in log2 units
-    const float *dsum;  // [BH][N] D_i = dO_i . O_i
-    void *g0;           // dkdv: dK; dq: dQ        [BH][N][d]
-    void *g1;           // dkdv: dV
+    const float *lse2;  // [B Hq][N] row log-sum-exp in log2 units
+    const float *dsum;  // [B Hq][N] D_i = dO_i . O_i
+    void *g0;           // dkdv: dK [B Hkv][N][d]; dq: dQ [B Hq][N][d]
+    void *g1;           // dkdv: dV [B Hkv][N][d]
+    int Hq, Hkv, group; // query head h reads key/value head h / group
     int N;
     int n_t;            // 128-row tiles per head
     int causal;
@@ -142,10 +144,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     float *vec = reinterpret_cast<float *>(smem + L::kVecOff);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int bh = blockIdx.x / p.n_t;
+    const int bhk = blockIdx.x / p.n_t;        // (batch, key/value head)
     const int jt = blockIdx.x % p.n_t;         // key tile (small first: most query tiles)
     const int i_first = p.causal ? jt : 0;     // query tiles that see key tile jt
-    const int n_iter = p.n_t - i_first;
+    const int n_qt = p.n_t - i_first;
+    const int n_iter = p.group * n_qt;         // every query head of the group, every tile
+    const int bhq0 = (bhk / p.Hkv) * p.Hq + (bhk % p.Hkv) * p.group;  // first query head
 
     if (threadIdx.x == 0) {
         mbar_init(fix_full, 1);
@@ -182,8 +186,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             bool ok = true;
             mbar_arrive_expect_tx(fix_full, 2 * L::kTileBytes);
             for (int c = 0; c < L::kChunks; ++c) {
-                tma_load_3d(fix + c * kSlabBytes, &map_k, fix_full, c * 64, jt * kRows, bh, pol);
-                tma_load_3d(fix + L::kTileBytes + c * kSlabBytes, &map_v, fix_full, c * 64, jt * kRows, bh,
+                tma_load_3d(fix + c * kSlabBytes, &map_k, fix_full, c * 64, jt * kRows, bhk, pol);
+                tma_load_3d(fix + L::kTileBytes + c * kSlabBytes, &map_v, fix_full, c * 64, jt * kRows, bhk,
                             pol);
             }
             int n = 0;
@@ -194,13 +198,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     ok = false;
                     break;
                 }
-                const int row = (i_first + n) * kRows;
+                const int row = (i_first + n % n_qt) * kRows;
+                const int bhq = bhq0 + n / n_qt;
                 uint8_t *st = ring + slot * L::kStageBytes;
                 mbar_arrive_expect_tx(ring_full + slot, 2 * L::kTileBytes);
                 for (int c = 0; c < L::kChunks; ++c) {
-                    tma_load_3d(st + c * kSlabBytes, &map_q, ring_full + slot, c * 64, row, bh, pol);
+                    tma_load_3d(st + c * kSlabBytes, &map_q, ring_full + slot, c * 64, row, bhq, pol);
                     tma_load_3d(st + L::kTileBytes + c * kSlabBytes, &map_do, ring_full + slot, c * 64, row,
-                                bh, pol);
+                                bhq, pol);
                 }
             }
             if (!ok) {  // let every copy already issued land
@@ -255,11 +260,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int r = warp * 32 + lane;
         const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
         const int key = jt * kRows + r;
-        const float *lse2_h = p.lse2 + static_cast<size_t>(bh) * p.N;
-        const float *dsum_h = p.dsum + static_cast<size_t>(bh) * p.N;
         bool ok = true;
         for (int n = 0; n < n_iter && ok; ++n) {
-            const int q0 = (i_first + n) * kRows;
+            const int q0 = (i_first + n % n_qt) * kRows;
+            const size_t hrow = static_cast<size_t>(bhq0 + n / n_qt) * p.N;
+            const float *lse2_h = p.lse2 + hrow;
+            const float *dsum_h = p.dsum + hrow;
             // this query tile's L2 and D, needed by every row: each warp stages its
             // own copy (double-buffered), so no barrier spans warps
             float *vb = vec + (warp * 2 + (n & 1)) * 2 * kRows;
@@ -301,7 +307,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (ok && warp_wait(acc_done, 0, abort_flag)) {
             tc_fence_after();
             const int osize = p.grad_dtype == FA_F32 ? 4 : 2;
-            const size_t row_off = (static_cast<size_t>(bh) * p.N + key) * D * osize;
+            const size_t row_off = (static_cast<size_t>(bhk) * p.N + key) * D * osize;
 #pragma unroll
             for (int q = 0; q < D / 32; ++q) {
                 uint32_t o[32];
@@ -346,7 +352,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kMiscOff + 4);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int bh = blockIdx.x / p.n_t;
+    const int bh = blockIdx.x / p.n_t;                          // (batch, query head)
+    const int bhk = (bh / p.Hq) * p.Hkv + (bh % p.Hq) / p.group;  // its key/value head
     const int it = p.causal ? p.n_t - 1 - blockIdx.x % p.n_t   // most key tiles first
                             : blockIdx.x % p.n_t;
     const int n_iter = p.causal ? it + 1 : p.n_t;              // key tiles the queries see
@@ -401,9 +408,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 uint8_t *st = ring + slot * L::kStageBytes;
                 mbar_arrive_expect_tx(ring_full + slot, 2 * L::kTileBytes);
                 for (int c = 0; c < L::kChunks; ++c) {
-                    tma_load_3d(st + c * kSlabBytes, &map_k, ring_full + slot, c * 64, n * kRows, bh, pol);
+                    tma_load_3d(st + c * kSlabBytes, &map_k, ring_full + slot, c * 64, n * kRows, bhk, pol);
                     tma_load_3d(st + L::kTileBytes + c * kSlabBytes, &map_v, ring_full + slot, c * 64, n * kRows,
-                                bh, pol);
+                                bhk, pol);
                 }
             }
             if (!ok) {
@@ -519,13 +526,14 @@ template <int D, bool BF16>
 int launch_bwd_d(const BackwardLaunch &a, cudaStream_t stream) {
     using L = BwdLayout<D>;
     static_assert(L::kSmemBytes <= 227 * 1024, "shared memory budget");
-    const long long BH = static_cast<long long>(a.B) * a.H;
+    const long long BH = static_cast<long long>(a.B) * a.H;      // query heads
+    const long long BHk = static_cast<long long>(a.B) * a.Hkv;   // key/value heads
     const long long rows = BH * a.N;
     CUtensorMap mq, mk, mv, mdo;
     int rc;
     if ((rc = make_map(&mq, a.q, D, false, a.N, BH, a.in_bf16)) != FA_OK) return rc;
-    if ((rc = make_map(&mk, a.k, D, false, a.N, BH, a.in_bf16)) != FA_OK) return rc;
-    if ((rc = make_map(&mv, a.v, D, false, a.N, BH, a.in_bf16)) != FA_OK) return rc;
+    if ((rc = make_map(&mk, a.k, D, false, a.N, BHk, a.in_bf16)) != FA_OK) return rc;
+    if ((rc = make_map(&mv, a.v, D, false, a.N, BHk, a.in_bf16)) != FA_OK) return rc;
     if ((rc = make_map(&mdo, a.dout, D, false, a.N, BH, a.in_bf16)) != FA_OK) return rc;
     cudaError_t e;
     if ((e = cudaFuncSetAttribute(bwd_dkdv_kernel<D, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -546,23 +554,27 @@ int launch_bwd_d(const BackwardLaunch &a, cudaStream_t stream) {
     BwdParams p;
     p.lse2 = lse2;
     p.dsum = dsum;
+    p.Hq = a.H;
+    p.Hkv = a.Hkv;
+    p.group = a.H / a.Hkv;
     p.N = a.N;
     p.n_t = (a.N + kRows - 1) / kRows;
     p.causal = a.causal ? 1 : 0;
     p.grad_dtype = a.grad_dtype;
     p.scale = a.scale;
     p.c = a.scale * 1.4426950408889634f;
-    const unsigned grid = static_cast<unsigned>(BH * p.n_t);
     if (e == cudaSuccess) {
         p.g0 = a.dk;
         p.g1 = a.dv;
-        bwd_dkdv_kernel<D, BF16><<<grid, kBwdThreads, L::kSmemBytes, stream>>>(mq, mk, mv, mdo, p);
+        bwd_dkdv_kernel<D, BF16><<<static_cast<unsigned>(BHk * p.n_t), kBwdThreads, L::kSmemBytes, stream>>>(
+            mq, mk, mv, mdo, p);
         e = cudaGetLastError();
     }
     if (e == cudaSuccess) {
         p.g0 = a.dq;
         p.g1 = nullptr;
-        bwd_dq_kernel<D, BF16><<<grid, kBwdThreads, L::kSmemBytes, stream>>>(mq, mk, mv, mdo, p);
+        bwd_dq_kernel<D, BF16><<<static_cast<unsigned>(BH * p.n_t), kBwdThreads, L::kSmemBytes, stream>>>(
+            mq, mk, mv, mdo, p);
         e = cudaGetLastError();
     }
     const cudaError_t e2 = scratch_free(ws, stream);

@@ -77,10 +77,10 @@ struct DecodeLaunch {
 int launch_decode(const DecodeLaunch &a, const DeviceInfo &dev, cudaStream_t stream);
 
 struct BackwardLaunch {
-    const void *q, *k, *v, *out, *dout;  // [B][H][N][d] 16-bit
+    const void *q, *k, *v, *out, *dout;  // q, out, dout [B][H][N][d]; k, v [B][Hkv][N][d] 16-bit
     const float *lse;                    // [B][H][N] natural-log row log-sum-exp of the forward
-    void *dq, *dk, *dv;                  // [B][H][N][d] in grad_dtype
-    int B, H, N, d;
+    void *dq, *dk, *dv;                  // dq [B][H][N][d], dk, dv [B][Hkv][N][d] in grad_dtype
+    int B, H, Hkv, N, d;
     int causal;
     float scale;
     int in_bf16;

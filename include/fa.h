@@ -141,17 +141,21 @@ int fa_prefill_lse(const void *q, const void *k, const void *v, void *out,
 
 /*
  * Backward pass of prefill (flash-attention-cuda README, "Future work":
- * training), for square multi-head problems: given the inputs, the forward
- * output `out`, its gradient `dout` and the forward's `lse`, writes
+ * training), for square problems (Nq = Nk = N) with H query heads over Hkv
+ * key/value heads: given the inputs, the forward output `out`, its gradient
+ * `dout` and the forward's `lse`, writes
  *   dq = dL/dq, dk = dL/dk, dv = dL/dv
  * of L = sum(dout * out), with the weights recomputed tile by tile (the N x N
- * tables never reach memory).  No atomics: the result is bit-identical run to
- * run.
- *   q, k, v, out, dout : 16-bit [B][H][N][d] in in_dtype (out as written by
+ * tables never reach memory).  The gradient of a shared key/value head is the
+ * sum over the query heads that read it.  No atomics: the result is
+ * bit-identical run to run.
+ *   q, out, dout       : 16-bit [B][H][N][d] in in_dtype (out as written by
  *                        fa_prefill_lse with out_dtype == in_dtype)
+ *   k, v               : 16-bit [B][Hkv][N][d]; H a multiple of Hkv
  *   lse                : fp32 [B][H][N] from fa_prefill_lse
- *   dq, dk, dv         : [B][H][N][d] in grad_dtype (FA_F16, FA_BF16, FA_F32),
- *                        accumulated in fp32; none may overlap another argument
+ *   dq                 : [B][H][N][d], dk, dv : [B][Hkv][N][d], in grad_dtype
+ *                        (FA_F16, FA_BF16, FA_F32), accumulated in fp32; none
+ *                        may overlap another argument
  *   causal, scale      : as in the forward call
  * Scratch of 8 bytes per row comes from the library's pool.  Errors as for
  * prefill: FA_ERR_NULL, FA_ERR_SHAPE, FA_ERR_HEAD_DIM, FA_ERR_DTYPE,
@@ -160,8 +164,8 @@ int fa_prefill_lse(const void *q, const void *k, const void *v, void *out,
  */
 int fa_prefill_backward(const void *q, const void *k, const void *v,
                         const void *out, const void *dout, const float *lse,
-                        void *dq, void *dk, void *dv, int B, int H, int N, int d,
-                        int causal, float scale, fa_dtype in_dtype,
+                        void *dq, void *dk, void *dv, int B, int H, int Hkv, int N,
+                        int d, int causal, float scale, fa_dtype in_dtype,
                         fa_dtype grad_dtype, void *stream);
 
 /*

@@ -135,6 +135,28 @@ def test_grouped_split_choice(lib, B, Hq, Hkv, L):
     assert binding.fa_decode_gqa_choose_splits(B, Hq, 3, L, 152) < 0 or Hq % 3 == 0
 
 
+def test_backward_argument_errors(lib):
+    args = dict(q=A, k=A + 4096, v=A + 8192, out=A + 12288, dout=A + 16384, lse=A + 20480,
+                dq=B_, dk=B_ + (1 << 20), dv=B_ + (2 << 20), B=1, H=6, Hkv=2, N=8, d=64, causal=1,
+                scale=0.125, it=0, gt=2)
+
+    def call(**kw):
+        a = {**args, **kw}
+        return binding.fa_prefill_backward(a["q"], a["k"], a["v"], a["out"], a["dout"], a["lse"],
+                                           a["dq"], a["dk"], a["dv"], a["B"], a["H"], a["Hkv"],
+                                           a["N"], a["d"], a["causal"], a["scale"], a["it"], a["gt"],
+                                           None)
+    assert call(lse=None) == 1
+    assert call(Hkv=4) == 2          # 6 query heads cannot share 4 key/value heads
+    assert call(N=0) == 2
+    assert call(d=96) == 3
+    assert call(gt=7) == 4
+    assert call(lse=A + 20482) == 5
+    assert call(scale=float("nan")) == 6
+    assert call(dk=A) == 11          # dk over q
+    assert call(dv=B_ + 16) == 11    # dv over dq
+
+
 def test_plain_prefill_checks_too(lib):
     assert binding.fa_prefill(None, A, A, B_, 1, 1, 1, 64, 0, 1.0, None) == 1
     assert binding.fa_prefill(A, A, A, B_, 1, 1, 1, 80, 0, 1.0, None) == 3

@@ -41,9 +41,11 @@ def fa():
     assert binding.fa_device_status(False) == 0, "a kernel watchdog fired"
 
 
-def run(fa, shape, dtype, causal, seed, grad="f32"):
+def run(fa, shape, dtype, causal, seed, grad="f32", hkv=None):
     import torch
-    q, k, v, g = (inputs.normal_bits(shape, seed + i, dtype) for i in range(4))
+    kv_shape = shape if hkv is None else (shape[0], hkv, shape[2], shape[3])
+    q, g = (inputs.normal_bits(shape, seed + i, dtype) for i in (0, 3))
+    k, v = (inputs.normal_bits(kv_shape, seed + i, dtype) for i in (1, 2))
     qd, kd, vd, gd = (G.bits_to_device(x, dtype) for x in (q, k, v, g))
     scale = 1.0 / np.sqrt(shape[-1])
     out, lse = fa.prefill_with_lse(qd, kd, vd, causal=causal, scale=scale)
@@ -91,6 +93,21 @@ def test_lse_under_the_stream_k_schedule(fa, oracle_mod):
     want = oracle_mod.attention_lse(oracle_mod.bits_to_f64(q, "f16"), oracle_mod.bits_to_f64(k, "f16"),
                                     False, 0.125)
     assert np.abs(G.device_to_f64(lse) - want).max() <= LSE_TOL["f16"]
+
+
+@pytest.mark.parametrize("shape,hkv,dtype", [((1, 6, 300, 64), 2, "f16"), ((2, 8, 512, 128), 1, "bf16"),
+                                             ((1, 14, 257, 64), 2, "bf16")])
+@pytest.mark.parametrize("causal", [False, True])
+def test_grouped_head_gradients_match_oracle(fa, oracle_mod, shape, hkv, dtype, causal):
+    # a shared key/value head collects the gradients of all its query heads
+    (q, k, v, g), scale, lse, grads = run(fa, shape, dtype, causal, 3500 + shape[1], hkv=hkv)
+    f = [oracle_mod.bits_to_f64(x, dtype) for x in (q, k, v, g)]
+    want = oracle_mod.attention_backward(*f, causal, scale, threads=G.THREADS)
+    for name, got_t, w in zip(("dq", "dk", "dv"), grads, want):
+        got = G.device_to_f64(got_t)
+        assert got.shape == w.shape
+        e = rel_err(got, w)
+        assert e <= REL_TOL[dtype], f"{name} {shape}/{hkv} {dtype} causal={causal}: {e:.3e}"
 
 
 def test_gradients_are_bit_identical_run_to_run(fa):
