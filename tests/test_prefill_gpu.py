@@ -213,3 +213,15 @@ def test_host_tensors_end_to_end(fa, oracle_mod):
     assert not out.is_cuda
     want = oracle_rows(oracle_mod, q, k, v, "f16", True, 0.125)
     assert np.abs(out.numpy().astype(np.float64) - want).max() <= 2e-3
+
+
+# ------------------------------------------------------------ very long sequences
+@pytest.mark.parametrize("shape,causal", [((1, 1, 300_000, 64), True), ((1, 2, 65_536, 128), False)])
+def test_very_long_sequences_sampled(fa, oracle_mod, shape, causal):
+    # 300K rows: more query blocks than the stream-K step table holds (1024),
+    # so the unit schedule runs; 64K rows dense: stream-K with a 256-entry table.
+    # Row indices and TMA coordinates run far past 2^16.
+    B, H, N, d = shape
+    dtype = "bf16" if d == 128 else "f16"
+    rows = G.sample_rows(N, 19, extra=(65_535, 65_536, 131_071, 262_143, 299_999))
+    check(fa, oracle_mod, shape, dtype, "f32", causal, 1.0 / np.sqrt(d), 230, rows=rows)
