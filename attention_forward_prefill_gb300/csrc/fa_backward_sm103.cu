@@ -19,8 +19,9 @@
 //              that reads this key/value head;
 //   bwd_dq     one CTA per 128-query tile: S = Q K_j^T, dP = dO V_j^T, dS over
 //              dP, dQ += dS K_j over the key tiles the queries see.
-// Warp roles per CTA (192 threads): warps 0-3 elementwise work, thread = TMEM
-// lane = tile row; warp 4 TMA producer; warp 5 tcgen05 issuer and TMEM owner.
+// Warp roles per CTA (320 threads): warps 0-7 elementwise work, thread = TMEM
+// lane = tile row, two warps per row quadrant taking half of the tile's columns
+// each; warp 8 TMA producer; warp 9 tcgen05 issuer and TMEM owner.
 #include <cfloat>
 
 #include "fa_internal.h"
@@ -31,9 +32,12 @@ namespace fa {
 
 namespace {
 
-constexpr int kBwdThreads = 192;
-constexpr int kBwdTmaWarp = 4;
-constexpr int kBwdMmaWarp = 5;
+// warps 0-7: elementwise, two per sub-partition: warp w serves TMEM lanes
+// 32 (w % 4) .. +31 and half w / 4 of a tile's 128 columns; 8: TMA; 9: MMA
+constexpr int kBwdThreads = 320;
+constexpr int kBwdEltWarps = 8;
+constexpr int kBwdTmaWarp = 8;
+constexpr int kBwdMmaWarp = 9;
 constexpr int kRows = 128;
 
 __device__ int g_backward_status = 0;
@@ -46,10 +50,10 @@ struct BwdLayout {
     static constexpr int kFixOff = 0;                       // two tiles loaded once per CTA
     static constexpr int kRingOff = 2 * kTileBytes;         // stages of two tiles each
     static constexpr int kStageBytes = 2 * kTileBytes;
-    static constexpr int kVecOff = kRingOff + kStages * kStageBytes;  // [4 warps][2 buf][2][128] floats
-    static constexpr int kBarOff = kVecOff + 4 * 2 * 2 * kRows * 4;
-    // fix_full, s_full, p_ready, acc_done, drain, ring_full[S], ring_empty[S]
-    static constexpr int kNumBars = 5 + 2 * kStages;
+    static constexpr int kVecOff = kRingOff + kStages * kStageBytes;  // [8 warps][2 buf][2][64] floats
+    static constexpr int kBarOff = kVecOff + kBwdEltWarps * 2 * 2 * 64 * 4;
+    // fix_full, s_full, p_ready, acc_done, drain, s_loaded, ring_full[S], ring_empty[S]
+    static constexpr int kNumBars = 6 + 2 * kStages;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
     static constexpr int kSmemBytes = kMiscOff + 16 + 1024;
     // TMEM: X (S or S^T) | Y (dP or dP^T) | accumulator A | accumulator B
@@ -103,11 +107,11 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const uint16_t *o, const 
 
 // Elementwise work on one 32-column quarter of a score tile held in TMEM:
 // returns, for the thread's row, the packed 16-bit weights and dS values.
-template <bool BF16, bool WANT_P>
-__device__ __forceinline__ void weights_quarter(const uint32_t (&sr)[32], const uint32_t (&dr)[32],
-                                                uint32_t (&pk)[16], uint32_t (&dk)[16], float c,
-                                                const float *lse2_col, const float *dsum_col,
-                                                float lse2_row, float dsum_row, uint32_t vis_mask) {
+template <bool BF16, bool WANT_P, bool MASKED>
+__device__ __forceinline__ void weights_quarter_impl(const uint32_t (&sr)[32], const uint32_t (&dr)[32],
+                                                     uint32_t (&pk)[16], uint32_t (&dk)[16], float c,
+                                                     const float *lse2_col, const float *dsum_col,
+                                                     float lse2_row, float dsum_row, uint32_t vis_mask) {
 #pragma unroll
     for (int e2 = 0; e2 < 16; ++e2) {
         float pp[2], dd[2];
@@ -116,14 +120,29 @@ __device__ __forceinline__ void weights_quarter(const uint32_t (&sr)[32], const 
             const int col = 2 * e2 + h;
             const float l2 = lse2_col ? lse2_col[col] : lse2_row;
             const float dsv = dsum_col ? dsum_col[col] : dsum_row;
-            const bool vis = (vis_mask >> col) & 1u;
-            const float p = vis ? ex2_approx(__uint_as_float(sr[col]) * c - l2) : 0.f;
+            float p = ex2_approx(__uint_as_float(sr[col]) * c - l2);
+            if (MASKED) p = ((vis_mask >> col) & 1u) ? p : 0.f;
             pp[h] = p;
             dd[h] = p * (__uint_as_float(dr[col]) - dsv);
         }
         if (WANT_P) pk[e2] = pack2t<BF16>(pp[0], pp[1]);
         dk[e2] = pack2t<BF16>(dd[0], dd[1]);
     }
+}
+
+// The weights of a 32-column quarter; the select is only paid where some
+// column of the thread's row is masked.
+template <bool BF16, bool WANT_P>
+__device__ __forceinline__ void weights_quarter(const uint32_t (&sr)[32], const uint32_t (&dr)[32],
+                                                uint32_t (&pk)[16], uint32_t (&dk)[16], float c,
+                                                const float *lse2_col, const float *dsum_col,
+                                                float lse2_row, float dsum_row, uint32_t vis_mask) {
+    if (vis_mask == 0xffffffffu)
+        weights_quarter_impl<BF16, WANT_P, false>(sr, dr, pk, dk, c, lse2_col, dsum_col, lse2_row, dsum_row,
+                                                  vis_mask);
+    else
+        weights_quarter_impl<BF16, WANT_P, true>(sr, dr, pk, dk, c, lse2_col, dsum_col, lse2_row, dsum_row,
+                                                 vis_mask);
 }
 
 // ---------------------------------------------------------------- dK, dV
@@ -138,7 +157,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kBarOff);
     uint64_t *fix_full = bars + 0, *s_full = bars + 1, *p_ready = bars + 2, *acc_done = bars + 3;
-    uint64_t *drain = bars + 4, *ring_full = bars + 5, *ring_empty = bars + 5 + L::kStages;
+    uint64_t *drain = bars + 4, *s_loaded = bars + 5;
+    uint64_t *ring_full = bars + 6, *ring_empty = bars + 6 + L::kStages;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kMiscOff);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kMiscOff + 4);
     float *vec = reinterpret_cast<float *>(smem + L::kVecOff);
@@ -154,9 +174,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (threadIdx.x == 0) {
         mbar_init(fix_full, 1);
         mbar_init(s_full, 1);
-        mbar_init(p_ready, 4);
+        mbar_init(p_ready, kBwdEltWarps);
         mbar_init(acc_done, 1);
         mbar_init(drain, 1);
+        mbar_init(s_loaded, kBwdEltWarps);
         for (int s = 0; s < L::kStages; ++s) {
             mbar_init(ring_full + s, 1);
             mbar_init(ring_empty + s, 1);
@@ -257,8 +278,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         __syncwarp();
     } else {
         // ---------------------------------------------------------------- elementwise
-        const int r = warp * 32 + lane;
-        const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+        const int wq = warp & 3, hf = warp >> 2;  // TMEM lane quadrant; column half
+        const int r = wq * 32 + lane;
+        const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
         const int key = jt * kRows + r;
         bool ok = true;
         for (int n = 0; n < n_iter && ok; ++n) {
@@ -266,25 +288,39 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             const size_t hrow = static_cast<size_t>(bhq0 + n / n_qt) * p.N;
             const float *lse2_h = p.lse2 + hrow;
             const float *dsum_h = p.dsum + hrow;
-            // this query tile's L2 and D, needed by every row: each warp stages its
-            // own copy (double-buffered), so no barrier spans warps
-            float *vb = vec + (warp * 2 + (n & 1)) * 2 * kRows;
+            // this half's 64 query columns: L2 and D, staged per warp (double-buffered)
+            float *vb = vec + (warp * 2 + (n & 1)) * 2 * 64;
+            const int c0 = q0 + hf * 64;
 #pragma unroll
-            for (int x = lane; x < kRows; x += 32) {
-                vb[x] = q0 + x < p.N ? lse2_h[q0 + x] : 0.f;
-                vb[kRows + x] = q0 + x < p.N ? dsum_h[q0 + x] : 0.f;
+            for (int x = lane; x < 64; x += 32) {
+                vb[x] = c0 + x < p.N ? lse2_h[c0 + x] : 0.f;
+                vb[64 + x] = c0 + x < p.N ? dsum_h[c0 + x] : 0.f;
             }
             __syncwarp();
             if (!warp_wait(s_full, n & 1, abort_flag)) { ok = false; break; }
             tc_fence_after();
-#pragma unroll 1
-            for (int q = 0; q < 4; ++q) {
-                uint32_t sr[32], dr[32];
-                tmem_ld32(tmem + lane_off + L::kXCol + q * 32, sr);
-                tmem_ld32(tmem + lane_off + L::kYCol + q * 32, dr);
-                tmem_ld_wait();
-                reg_fence32(sr);
-                reg_fence32(dr);
+            uint32_t sr[2][32], dr[2][32];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                tmem_ld32(tmem + lane_off + L::kXCol + (2 * hf + h) * 32, sr[h]);
+                tmem_ld32(tmem + lane_off + L::kYCol + (2 * hf + h) * 32, dr[h]);
+            }
+            tmem_ld_wait();
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                reg_fence32(sr[h]);
+                reg_fence32(dr[h]);
+            }
+            // P^T and dS^T of the upper half land on columns the lower half reads:
+            // every warp's loads complete before any warp stores
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(s_loaded);
+            if (!warp_wait(s_loaded, n & 1, abort_flag)) { ok = false; break; }
+            tc_fence_after();
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int q = 2 * hf + h;
                 // column col is query q0 + 32 q + col; it sees the key when it exists
                 // and, causally, when key <= query
                 const int qb = q0 + q * 32;
@@ -295,8 +331,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     vis &= lo <= 0 ? 0xffffffffu : (lo >= 32 ? 0u : (0xffffffffu << lo));
                 }
                 uint32_t pk[16], dk[16];
-                weights_quarter<BF16, true>(sr, dr, pk, dk, p.c, vb + q * 32, vb + kRows + q * 32, 0.f, 0.f, vis);
-                tmem_st16(tmem + lane_off + L::kXCol + q * 16, pk);   // P^T over S^T (already read)
+                weights_quarter<BF16, true>(sr[h], dr[h], pk, dk, p.c, vb + h * 32, vb + 64 + h * 32, 0.f, 0.f,
+                                            vis);
+                tmem_st16(tmem + lane_off + L::kXCol + q * 16, pk);   // P^T over S^T
                 tmem_st16(tmem + lane_off + L::kYCol + q * 16, dk);   // dS^T over dP^T
             }
             tmem_st_wait();
@@ -305,23 +342,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             if (lane == 0) mbar_arrive(p_ready);
         }
         if (ok && warp_wait(acc_done, 0, abort_flag)) {
+            // the lower half stores dV, the upper half dK
             tc_fence_after();
             const int osize = p.grad_dtype == FA_F32 ? 4 : 2;
             const size_t row_off = (static_cast<size_t>(bhk) * p.N + key) * D * osize;
+            uint8_t *dst = static_cast<uint8_t *>(hf ? p.g0 : p.g1) + row_off;
+            const uint32_t acc_col = hf ? L::kBCol : L::kACol;
+            const float mul = hf ? p.scale : 1.f;
 #pragma unroll
             for (int q = 0; q < D / 32; ++q) {
                 uint32_t o[32];
-                tmem_ld32(tmem + lane_off + L::kACol + q * 32, o);
+                tmem_ld32(tmem + lane_off + acc_col + q * 32, o);
                 tmem_ld_wait();
                 reg_fence32(o);
-                if (key < p.N)
-                    store_out32(static_cast<uint8_t *>(p.g1) + row_off + q * 32 * osize, o, 1.f, p.grad_dtype);
-                tmem_ld32(tmem + lane_off + L::kBCol + q * 32, o);
-                tmem_ld_wait();
-                reg_fence32(o);
-                if (key < p.N)
-                    store_out32(static_cast<uint8_t *>(p.g0) + row_off + q * 32 * osize, o, p.scale,
-                                p.grad_dtype);
+                if (key < p.N) store_out32(dst + q * 32 * osize, o, mul, p.grad_dtype);
             }
             tc_fence_before();
         }
@@ -347,7 +381,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kBarOff);
     uint64_t *fix_full = bars + 0, *s_full = bars + 1, *p_ready = bars + 2, *acc_done = bars + 3;
-    uint64_t *drain = bars + 4, *ring_full = bars + 5, *ring_empty = bars + 5 + L::kStages;
+    uint64_t *drain = bars + 4, *s_loaded = bars + 5;
+    uint64_t *ring_full = bars + 6, *ring_empty = bars + 6 + L::kStages;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kMiscOff);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kMiscOff + 4);
 
@@ -361,9 +396,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (threadIdx.x == 0) {
         mbar_init(fix_full, 1);
         mbar_init(s_full, 1);
-        mbar_init(p_ready, 4);
+        mbar_init(p_ready, kBwdEltWarps);
         mbar_init(acc_done, 1);
         mbar_init(drain, 1);
+        mbar_init(s_loaded, kBwdEltWarps);
         for (int s = 0; s < L::kStages; ++s) {
             mbar_init(ring_full + s, 1);
             mbar_init(ring_empty + s, 1);
@@ -459,8 +495,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
         __syncwarp();
     } else {
-        const int r = warp * 32 + lane;
-        const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+        const int wq = warp & 3, hf = warp >> 2;  // TMEM lane quadrant; column half
+        const int r = wq * 32 + lane;
+        const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
         const int qrow = it * kRows + r;
         const size_t li = static_cast<size_t>(bh) * p.N + qrow;
         const float lse2_r = qrow < p.N ? p.lse2[li] : 0.f;
@@ -469,14 +506,27 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         for (int n = 0; n < n_iter && ok; ++n) {
             if (!warp_wait(s_full, n & 1, abort_flag)) { ok = false; break; }
             tc_fence_after();
-#pragma unroll 1
-            for (int q = 0; q < 4; ++q) {
-                uint32_t sr[32], dr[32];
-                tmem_ld32(tmem + lane_off + L::kXCol + q * 32, sr);
-                tmem_ld32(tmem + lane_off + L::kYCol + q * 32, dr);
-                tmem_ld_wait();
-                reg_fence32(sr);
-                reg_fence32(dr);
+            uint32_t sr[2][32], dr[2][32];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                tmem_ld32(tmem + lane_off + L::kXCol + (2 * hf + h) * 32, sr[h]);
+                tmem_ld32(tmem + lane_off + L::kYCol + (2 * hf + h) * 32, dr[h]);
+            }
+            tmem_ld_wait();
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                reg_fence32(sr[h]);
+                reg_fence32(dr[h]);
+            }
+            // dS of the upper half lands on columns of dP the lower half reads
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(s_loaded);
+            if (!warp_wait(s_loaded, n & 1, abort_flag)) { ok = false; break; }
+            tc_fence_after();
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int q = 2 * hf + h;
                 // column col is key n * 128 + 32 q + col: visible when it exists, the
                 // row exists and, causally, key <= query
                 const int kb = n * kRows + q * 32;
@@ -488,8 +538,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     vis &= hi < 0 ? 0u : (hi >= 31 ? 0xffffffffu : (0xffffffffu >> (31 - hi)));
                 }
                 uint32_t pk[16], dk[16];
-                weights_quarter<BF16, false>(sr, dr, pk, dk, p.c, nullptr, nullptr, lse2_r, dsum_r, vis);
-                tmem_st16(tmem + lane_off + L::kYCol + q * 16, dk);  // dS over dP (already read)
+                weights_quarter<BF16, false>(sr[h], dr[h], pk, dk, p.c, nullptr, nullptr, lse2_r, dsum_r, vis);
+                tmem_st16(tmem + lane_off + L::kYCol + q * 16, dk);  // dS over dP
             }
             tmem_st_wait();
             tc_fence_before();
@@ -497,17 +547,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             if (lane == 0) mbar_arrive(p_ready);
         }
         if (ok && warp_wait(acc_done, 0, abort_flag)) {
+            // each half stores half of the dQ columns
             tc_fence_after();
             const int osize = p.grad_dtype == FA_F32 ? 4 : 2;
             const size_t row_off = li * D * osize;
 #pragma unroll
-            for (int q = 0; q < D / 32; ++q) {
+            for (int q = 0; q < D / 64; ++q) {
+                const int cq = hf * (D / 64) + q;
                 uint32_t o[32];
-                tmem_ld32(tmem + lane_off + L::kACol + q * 32, o);
+                tmem_ld32(tmem + lane_off + L::kACol + cq * 32, o);
                 tmem_ld_wait();
                 reg_fence32(o);
                 if (qrow < p.N)
-                    store_out32(static_cast<uint8_t *>(p.g0) + row_off + q * 32 * osize, o, p.scale,
+                    store_out32(static_cast<uint8_t *>(p.g0) + row_off + cq * 32 * osize, o, p.scale,
                                 p.grad_dtype);
             }
             tc_fence_before();
