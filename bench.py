@@ -321,8 +321,15 @@ def run_ours(args):
         return None
 
     value = tot_flops / tot_s / 1e12 if do_pre else None
-    n_launch = (len(do_pre) * args.steps + (2 * args.steps if do_dec else 0)
-                + (3 * args.steps if do_bwd else 0))
+    # our kernels per step: each prefill launch, plus its fixup pass when the
+    # library's plan cuts units between CTAs; decode split + merge; backward
+    # prep + dK/dV + dQ
+    per_step = 0
+    for N in do_pre:
+        _, info, _ = binding.fa_prefill_plan(PREFILL_B, PREFILL_H, N, N, 0, 0, 0)
+        per_step += 1 + (1 if info[0] and info[5] > 0 else 0)
+    per_step += (2 if do_dec else 0) + (3 if do_bwd else 0)
+    n_launch = per_step * args.steps
     detail = {}
     for N in do_pre:
         ms = statistics.median(pre_ms[N])
