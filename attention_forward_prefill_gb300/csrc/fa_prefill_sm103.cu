@@ -748,80 +748,115 @@ struct FixupParams {
 
 template <int D>
 __global__ void __launch_bounds__(256) prefill_fixup(const __grid_constant__ FixupParams f) {
-    constexpr int EPL = D / 32;  // columns per lane
+    // CTA (item, g): rows [32 g, 32 g + 32) of the cut unit, in query tile g / 4;
+    // warp w merges four of them.  A warp reads one 512-byte record row per load
+    // (lane = 4 or 2 columns) and keeps every piece of its rows in flight.
+    constexpr int CPL = D / 32;
+    constexpr int kRows = 4;     // rows per warp
+    constexpr int kChunk = 4;    // pieces in flight per pass
+    using Vec = typename std::conditional<CPL == 4, float4, float2>::type;
+    __shared__ int s_rec[kMaxSplit];  // record index of row 0 of the unit, per piece
+    __shared__ int s_np;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int4 it = f.item[blockIdx.x];
+    const int u = it.x;
+    const int bh = u / f.n_qb, qb = u % f.n_qb;
+    const int t = blockIdx.y >> 2;
+    const int tile_row0 = qb * kRowsPerUnit + t * kBlockM;
+    const int n_t = kv_tiles(f.causal, f.no_skip, f.Nq, f.Nk, f.Nk - f.Nq, tile_row0);
+    const long long ustart = f.ustart[blockIdx.x];
+    // The pieces holding keys of this tile, in CTA order: CTA c's range starts at
+    // sk_s0 + floor(c (W - sk_s0) / G); slot 0 when the piece opened it, 1 when it
+    // closed it.  Worked out before the main kernel has finished.
+    if (warp == 0) {
+        const long long span = f.W - f.sk_s0;
+        int np = 0;
+        for (int c0 = it.y; c0 <= it.z; c0 += 32) {
+            const int c = c0 + lane;
+            bool has = false;
+            int rec = 0;
+            if (c <= it.z) {
+                const long long first = f.sk_s0 + static_cast<long long>(c) * span / f.G;
+                const long long next = f.sk_s0 + static_cast<long long>(c + 1) * span / f.G;
+                const long long jf = first > ustart ? first - ustart : 0;
+                has = next > first && jf < n_t;
+                rec = (c * 2 + (first >= ustart ? 0 : 1)) * kRowsPerUnit;
+            }
+            const unsigned m = __ballot_sync(0xffffffffu, has);
+            if (has) s_rec[np + __popc(m & ((1u << lane) - 1))] = rec;
+            np += __popc(m);
+        }
+        if (lane == 0) s_np = np;
+    }
+    __syncthreads();
     // Launched with programmatic dependent launch: wait until the main kernel
     // has completed and its partials are visible.
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    const int4 it = f.item[blockIdx.x];
-    const int u = it.x;
-    const int rrow = blockIdx.y * 8 + warp;  // row within the 256-row unit
-    const int bh = u / f.n_qb, qb = u % f.n_qb;
-    const int row = qb * kRowsPerUnit + rrow;
-    if (row >= f.Nq) return;
-    const int tile_row0 = qb * kRowsPerUnit + (rrow / kBlockM) * kBlockM;
-    const int n_t = kv_tiles(f.causal, f.no_skip, f.Nq, f.Nk, f.Nk - f.Nq, tile_row0);
-    const long long ustart = f.ustart[blockIdx.x];
-    auto first_of = [&](int c) { return f.sk_s0 + static_cast<long long>(c) * (f.W - f.sk_s0) / f.G; };
-    // piece of CTA c: (record, first key tile of the piece within the unit)
-    auto piece = [&](int c, int &j_first) {
-        const long long first = first_of(c);
-        j_first = first > ustart ? static_cast<int>(first - ustart) : 0;
-        return (static_cast<size_t>(c) * 2 + (first >= ustart ? 0 : 1)) * kRowsPerUnit + rrow;
-    };
-    float M = -INFINITY;
-    // CTAs with an empty step range (more CTAs than steps) hold no piece.
-    auto empty = [&](int c) { return first_of(c + 1) <= first_of(c); };
-    for (int c = it.y; c <= it.z; ++c) {
-        int jf;
-        const size_t rec = piece(c, jf);
-        if (!empty(c) && jf < n_t) M = fmaxf(M, f.ws_ml[rec * 2]);
-    }
-    float L = 0.f, o[EPL];
+    const int np = s_np;
+    const int rr0 = blockIdx.y * 32 + warp * kRows;  // first row of the warp within the unit
+    // the max and the weighted sum of l, per row (every lane computes all four)
+    float M[kRows], L[kRows];
 #pragma unroll
-    for (int e = 0; e < EPL; ++e) o[e] = 0.f;
-    for (int c = it.y; c <= it.z; ++c) {
-        int jf;
-        const size_t rec = piece(c, jf);
-        if (empty(c) || jf >= n_t) continue;  // no keys of this row in the piece
-        const float m = f.ws_ml[rec * 2];
-        if (m == -INFINITY) continue;
-        const float w = ex2_approx(m - M);
-        L = fmaf(w, f.ws_ml[rec * 2 + 1], L);
-        const float *src = f.ws_o + rec * D + lane * EPL;
+    for (int r = 0; r < kRows; ++r) M[r] = -INFINITY, L[r] = 0.f;
+    for (int k = 0; k < np; ++k)
 #pragma unroll
-        for (int e = 0; e < EPL; e += 2) {
-            if constexpr (EPL % 4 == 0) {
-                if (e % 4 == 0) {
-                    const float4 y = *reinterpret_cast<const float4 *>(src + e);
-                    o[e] = fmaf(w, y.x, o[e]);
-                    o[e + 1] = fmaf(w, y.y, o[e + 1]);
-                    o[e + 2] = fmaf(w, y.z, o[e + 2]);
-                    o[e + 3] = fmaf(w, y.w, o[e + 3]);
-                }
-                continue;
+        for (int r = 0; r < kRows; ++r) M[r] = fmaxf(M[r], __ldg(f.ws_ml + (static_cast<size_t>(s_rec[k]) + rr0 + r) * 2));
+    for (int k = 0; k < np; ++k)
+#pragma unroll
+        for (int r = 0; r < kRows; ++r) {
+            const float2 ml = __ldg(reinterpret_cast<const float2 *>(f.ws_ml) + s_rec[k] + rr0 + r);
+            if (ml.x != -INFINITY) L[r] = fmaf(ex2_approx(ml.x - M[r]), ml.y, L[r]);
+        }
+    float acc[kRows][CPL];
+#pragma unroll
+    for (int r = 0; r < kRows; ++r)
+#pragma unroll
+        for (int e = 0; e < CPL; ++e) acc[r][e] = 0.f;
+    for (int k0 = 0; k0 < np; k0 += kChunk) {
+        Vec x[kChunk][kRows];
+        float wgt[kChunk][kRows];
+#pragma unroll
+        for (int j = 0; j < kChunk; ++j) {
+            const int k = k0 + j < np ? k0 + j : k0;
+            const size_t rec = static_cast<size_t>(s_rec[k]) + rr0;
+#pragma unroll
+            for (int r = 0; r < kRows; ++r) {
+                x[j][r] = __ldg(reinterpret_cast<const Vec *>(f.ws_o + (rec + r) * D) + lane);
+                const float m = __ldg(f.ws_ml + (rec + r) * 2);
+                wgt[j][r] = (k0 + j < np && m != -INFINITY) ? ex2_approx(m - M[r]) : 0.f;
             }
-            const float2 x = *reinterpret_cast<const float2 *>(src + e);
-            o[e] = fmaf(w, x.x, o[e]);
-            o[e + 1] = fmaf(w, x.y, o[e + 1]);
+        }
+        // pieces in CTA order, one fma each: the same sum whatever the chunking
+#pragma unroll
+        for (int j = 0; j < kChunk; ++j) {
+            if (k0 + j >= np) break;
+#pragma unroll
+            for (int r = 0; r < kRows; ++r) {
+                const float *xv = reinterpret_cast<const float *>(&x[j][r]);
+#pragma unroll
+                for (int e = 0; e < CPL; ++e) acc[r][e] = fmaf(wgt[j][r], xv[e], acc[r][e]);
+            }
         }
     }
-    const float inv = L > 0.f ? 1.0f / L : 0.f;
-    if (f.lse != nullptr && lane == 0)
-        f.lse[static_cast<size_t>(bh) * f.Nq + row] = L > 0.f ? (M + __log2f(L)) * 0.6931471805599453f : -INFINITY;
-    const size_t off = (static_cast<size_t>(bh) * f.Nq + row) * D + lane * EPL;
-    if (f.out_dtype == FA_F32) {
-        float *dst = reinterpret_cast<float *>(f.out) + off;
 #pragma unroll
-        for (int e = 0; e < EPL; ++e) dst[e] = o[e] * inv;
-    } else if (f.out_dtype == FA_BF16) {
-        __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(f.out) + off;
+    for (int r = 0; r < kRows; ++r) {
+        const int row = qb * kRowsPerUnit + rr0 + r;
+        if (row >= f.Nq) break;
+        const float inv = L[r] > 0.f ? 1.0f / L[r] : 0.f;
+        if (f.lse != nullptr && lane == 0)
+            f.lse[static_cast<size_t>(bh) * f.Nq + row] =
+                L[r] > 0.f ? (M[r] + __log2f(L[r])) * 0.6931471805599453f : -INFINITY;
+        const size_t off = (static_cast<size_t>(bh) * f.Nq + row) * D + lane * CPL;
+        if (f.out_dtype == FA_F32) {
+            float *dst = reinterpret_cast<float *>(f.out) + off;
 #pragma unroll
-        for (int e = 0; e < EPL; ++e) dst[e] = __float2bfloat16_rn(o[e] * inv);
-    } else {
-        __half *dst = reinterpret_cast<__half *>(f.out) + off;
+            for (int e = 0; e < CPL; ++e) dst[e] = acc[r][e] * inv;
+        } else {
+            const int bf = f.out_dtype == FA_BF16;
+            uint32_t *dst = reinterpret_cast<uint32_t *>(reinterpret_cast<uint16_t *>(f.out) + off);
 #pragma unroll
-        for (int e = 0; e < EPL; ++e) dst[e] = __float2half_rn(o[e] * inv);
+            for (int e = 0; e < CPL; e += 2) dst[e / 2] = pack2(acc[r][e] * inv, acc[r][e + 1] * inv, bf);
+        }
     }
 }
 
@@ -837,10 +872,10 @@ int host_kv_tiles(int causal, int no_skip, int nq, int nk, int row0) {
 
 // Stream-K costs, in key-tile steps, fitted to measured launch times on GB300
 // (d = 64 and 128, dense and causal): cutting units between CTAs costs about
-// 15 steps (partial writes, extra pipeline fills, the fixup pass) when the
-// units are non-causal and 20 when they are causal, and a causal stream-K step
-// runs about 8% slower than a step of the unit schedule.
-constexpr long long kMergeCostSteps = 15;
+// 10 steps (partial writes, extra pipeline fills, the fixup pass of 7-10 us)
+// when the units are non-causal and 20 when they are causal, and a causal
+// stream-K step runs about 8% slower than a step of the unit schedule.
+constexpr long long kMergeCostSteps = 10;
 constexpr long long kCausalMergeCostSteps = 20;
 constexpr long long kCausalStepPct = 108;
 
@@ -1061,7 +1096,7 @@ int launch_d_lse(const PrefillLaunch &a, const DeviceInfo &dev, cudaStream_t str
     e = cudaGetLastError();
     if (e == cudaSuccess && f.n_split > 0) {
         cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(f.n_split, kRowsPerUnit / 8);
+        cfg.gridDim = dim3(f.n_split, kRowsPerUnit / 32);
         cfg.blockDim = dim3(256);
         cfg.stream = stream;
         cudaLaunchAttribute attr[1];
