@@ -35,6 +35,7 @@ _SIGNATURES = {
     "fa_prefill": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp]),
     "fa_prefill_ex": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _i, _u, _vp]),
     "fa_prefill_gqa": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _f, _i, _i, _u, _vp]),
+    "fa_prefill_host": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _f, _i, _i, _u, _vp]),
     "fa_prefill_varlen": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _i,
                                _f, _i, _i, _u, _vp]),
     "fa_prefill_lse": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _f, _i, _i, _u,
@@ -106,6 +107,12 @@ def fa_prefill_gqa(q, k, v, out, B, Hq, Hkv, Nq, Nk, d, causal, scale, in_dtype,
                    flags=0, stream=0) -> int:
     return load().fa_prefill_gqa(q, k, v, out, B, Hq, Hkv, Nq, Nk, d, int(causal), float(scale),
                                  in_dtype, out_dtype, flags, stream)
+
+
+def fa_prefill_host(q, k, v, out, B, Hq, Hkv, Nq, Nk, d, causal, scale, in_dtype, out_dtype,
+                    flags=0, stream=0) -> int:
+    return load().fa_prefill_host(q, k, v, out, B, Hq, Hkv, Nq, Nk, d, int(causal), float(scale),
+                                  in_dtype, out_dtype, flags, stream)
 
 
 def fa_prefill_varlen(q, k, v, out, cu_seqlens_q, cu_seqlens_k, B, Hq, Hkv, total_q, total_k,
@@ -240,18 +247,13 @@ def prefill(q, k, v, causal: bool = False, scale: float | None = None, out_dtype
     last Nq positions).
 
     CUDA inputs run on the current stream and return a CUDA tensor.  Host
-    inputs are copied to the current device first and the result is copied
-    back to host memory (the end-to-end form of the same call).
+    inputs go through fa_prefill_host (copies in, compute and copies out
+    pipelined over chunks of heads); the call waits for the current stream and
+    returns the host result (pinned when q is).
     """
     torch = _torch()
-    host = not q.is_cuda
-    if host:
-        dev = torch.device("cuda", torch.cuda.current_device())
-        res = prefill(q.to(dev, non_blocking=True), k.to(dev, non_blocking=True),
-                      v.to(dev, non_blocking=True), causal, scale, out_dtype, flags)
-        dst = torch.empty(res.shape, dtype=res.dtype, pin_memory=q.is_pinned())
-        dst.copy_(res, non_blocking=False)
-        return dst
+    if not q.is_cuda:
+        return _prefill_host(torch, q, k, v, causal, scale, out_dtype, flags, out)
     B, Hq, Nq, d = q.shape
     _check_cuda("q", q)
     _check_cuda("k", k, None, q.dtype)
@@ -271,6 +273,44 @@ def prefill(q, k, v, causal: bool = False, scale: float | None = None, out_dtype
                         _stream_handle(q.device))
     if rc != FA_OK:
         raise FaError(rc, "fa_prefill_gqa")
+    return out
+
+
+def _check_host(name, t, shape=None, dtype=None):
+    if t.is_cuda:
+        raise ValueError(f"{name} must be a host tensor when q is")
+    if t.dtype not in (_torch().float16, _torch().bfloat16) and name != "out":
+        raise ValueError(f"{name} must be float16 or bfloat16, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} has dtype {t.dtype}, expected {dtype}")
+
+
+def _prefill_host(torch, q, k, v, causal, scale, out_dtype, flags, out):
+    B, Hq, Nq, d = q.shape
+    _check_host("q", q)
+    _check_host("k", k, None, q.dtype)
+    if k.dim() != 4 or k.shape[0] != B or k.shape[3] != d:
+        raise ValueError(f"k has shape {tuple(k.shape)}, expected [{B}, Hkv, Nk, {d}]")
+    Hkv, Nk = k.shape[1], k.shape[2]
+    _check_host("v", v, k.shape, q.dtype)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    out_dtype = q.dtype if out_dtype is None else out_dtype
+    if out is None:
+        out = torch.empty(q.shape, dtype=out_dtype, pin_memory=q.is_pinned())
+    else:
+        _check_host("out", out, q.shape, out_dtype)
+    stream = torch.cuda.current_stream()
+    rc = fa_prefill_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, Hq, Hkv, Nq,
+                         Nk, d, causal, scale, dtype_code(q.dtype), dtype_code(out_dtype), flags,
+                         stream.cuda_stream)
+    if rc != FA_OK:
+        raise FaError(rc, "fa_prefill_host")
+    stream.synchronize()
     return out
 
 

@@ -5,6 +5,7 @@
 // usage: prefill(q, k, v, causal, scale) and decode(q, k_cache, v_cache,
 // seq_lens, scale)) with the validation its bindings layer performs
 // ("Project structure": bindings.cpp, "input validation").
+#include <algorithm>
 #include <climits>
 #include <cmath>
 #include <cstdint>
@@ -23,7 +24,7 @@ DeviceInfo g_dev_cache[kMaxDevices];
 bool g_dev_have[kMaxDevices] = {};
 
 cudaMemPool_t g_pool[kMaxDevices] = {};
-constexpr uint64_t kPoolKeepBytes = 256ull << 20;  // freed scratch kept mapped
+constexpr uint64_t kPoolKeepBytes = 1024ull << 20;  // freed scratch kept mapped
 
 constexpr int kDecodeRowAlign = 64;      // chunk lengths are multiples of this
 constexpr int kDecodeAutoMaxChunk = 512;  // automatic choice: at most 512 rows per CTA
@@ -223,6 +224,147 @@ int fa_prefill_gqa(const void *q, const void *k, const void *v, void *out, int B
                    fa_dtype out_dtype, unsigned flags, void *stream) {
     return fa_prefill_lse(q, k, v, out, nullptr, B, Hq, Hkv, Nq, Nk, d, causal, scale, in_dtype,
                           out_dtype, flags, stream);
+}
+
+}  // extern "C"
+
+namespace {
+// Copy streams and events of the host-buffer pipeline, one set per device,
+// created on first use and kept for the life of the process.
+constexpr int kHostChunks = 4;
+struct HostPipe {
+    bool ready = false;
+    cudaStream_t s_in = nullptr, s_out = nullptr;
+    cudaEvent_t start = nullptr, done = nullptr;
+    cudaEvent_t in[kHostChunks] = {}, comp[kHostChunks] = {};
+};
+std::mutex g_pipe_mu;
+HostPipe g_pipe[kMaxDevices];
+
+cudaError_t host_pipe(int dev, HostPipe **out) {
+    HostPipe &hp = g_pipe[dev];
+    if (!hp.ready) {
+        cudaError_t e;
+        if ((e = cudaStreamCreateWithFlags(&hp.s_in, cudaStreamNonBlocking)) ||
+            (e = cudaStreamCreateWithFlags(&hp.s_out, cudaStreamNonBlocking)) ||
+            (e = cudaEventCreateWithFlags(&hp.start, cudaEventDisableTiming)) ||
+            (e = cudaEventCreateWithFlags(&hp.done, cudaEventDisableTiming)))
+            return e;
+        for (int c = 0; c < kHostChunks; ++c)
+            if ((e = cudaEventCreateWithFlags(&hp.in[c], cudaEventDisableTiming)) ||
+                (e = cudaEventCreateWithFlags(&hp.comp[c], cudaEventDisableTiming)))
+                return e;
+        hp.ready = true;
+    }
+    *out = &hp;
+    return cudaSuccess;
+}
+
+size_t round_up256(size_t x) { return (x + 255) / 256 * 256; }
+}  // namespace
+
+extern "C" {
+
+int fa_prefill_host(const void *q_host, const void *k_host, const void *v_host, void *out_host,
+                    int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal, float scale,
+                    fa_dtype in_dtype, fa_dtype out_dtype, unsigned flags, void *stream) {
+    int rc = prefill_common_checks(q_host, k_host, v_host, out_host, d, in_dtype, out_dtype, scale);
+    if (rc != FA_OK) return rc;
+    if (B < 1 || Hq < 1 || Hkv < 1 || Nq < 1 || Nk < 1) return FA_ERR_SHAPE;
+    if (Hq % Hkv != 0) return FA_ERR_SHAPE;
+    if (static_cast<long long>(B) * Hq * Nq > INT_MAX || static_cast<long long>(B) * Hkv * Nk > INT_MAX)
+        return FA_ERR_SHAPE;
+    const int group = Hq / Hkv;
+    const size_t q_head = static_cast<size_t>(Nq) * d * 2, kv_head = static_cast<size_t>(Nk) * d * 2;
+    const size_t o_head = static_cast<size_t>(Nq) * d * dtype_size(out_dtype);
+    const long long n_kv = static_cast<long long>(B) * Hkv;  // flattened key/value heads
+    const size_t q_bytes = q_head * group * n_kv, kv_bytes = kv_head * n_kv, o_bytes = o_head * group * n_kv;
+    if (overlaps(out_host, o_bytes, q_host, q_bytes) || overlaps(out_host, o_bytes, k_host, kv_bytes) ||
+        overlaps(out_host, o_bytes, v_host, kv_bytes))
+        return FA_ERR_ALIAS;
+    DeviceInfo dev;
+    rc = current_device_info(&dev);
+    if (rc != FA_OK) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+    std::lock_guard<std::mutex> lk(g_pipe_mu);
+    HostPipe *hp = nullptr;
+    cudaError_t e = host_pipe(dev.device, &hp);
+    if (e != cudaSuccess) return cuda_fail(e);
+    void *buf = nullptr;
+    const size_t off_k = round_up256(q_bytes), off_v = off_k + round_up256(kv_bytes),
+                 off_o = off_v + round_up256(kv_bytes);
+    e = scratch_alloc(&buf, off_o + o_bytes, st);
+    if (e != cudaSuccess) {
+        cuda_fail(e);
+        return FA_ERR_WORKSPACE;
+    }
+    char *qd = static_cast<char *>(buf), *kd = qd + off_k, *vd = qd + off_v, *od = qd + off_o;
+    const char *qh = static_cast<const char *>(q_host), *kh = static_cast<const char *>(k_host),
+               *vh = static_cast<const char *>(v_host);
+    char *oh = static_cast<char *>(out_host);
+    // Small problems gain nothing from overlap: one chunk under 8 MB of traffic.
+    const size_t total = q_bytes + 2 * kv_bytes + o_bytes;
+    const int n_ch = static_cast<int>(std::min<long long>(total < (8u << 20) ? 1 : kHostChunks, n_kv));
+    // the copy streams start after the work already on `stream` (which also
+    // orders the pool allocation before them)
+    if ((e = cudaEventRecord(hp->start, st)) || (e = cudaStreamWaitEvent(hp->s_in, hp->start, 0)) ||
+        (e = cudaStreamWaitEvent(hp->s_out, hp->start, 0))) {
+        scratch_free(buf, st);
+        return cuda_fail(e);
+    }
+    rc = FA_OK;
+    for (int c = 0; c < n_ch && rc == FA_OK; ++c) {
+        const long long h0 = n_kv * c / n_ch, h1 = n_kv * (c + 1) / n_ch;  // key/value heads [h0, h1)
+        const size_t qo = q_head * group * h0, qn = q_head * group * (h1 - h0);
+        const size_t ko = kv_head * h0, kn = kv_head * (h1 - h0);
+        const size_t oo = o_head * group * h0, on = o_head * group * (h1 - h0);
+        if ((e = cudaMemcpyAsync(qd + qo, qh + qo, qn, cudaMemcpyHostToDevice, hp->s_in)) ||
+            (e = cudaMemcpyAsync(kd + ko, kh + ko, kn, cudaMemcpyHostToDevice, hp->s_in)) ||
+            (e = cudaMemcpyAsync(vd + ko, vh + ko, kn, cudaMemcpyHostToDevice, hp->s_in)) ||
+            (e = cudaEventRecord(hp->in[c], hp->s_in)) || (e = cudaStreamWaitEvent(st, hp->in[c], 0))) {
+            rc = cuda_fail(e);
+            break;
+        }
+        // the chunk as one sequence batch of (h1 - h0) * group query heads
+        PrefillLaunch a;
+        a.q = qd + qo;
+        a.k = kd + ko;
+        a.v = vd + ko;
+        a.out = od + oo;
+        a.lse = nullptr;
+        a.cu_q = nullptr;
+        a.cu_k = nullptr;
+        a.B = 1;
+        a.Hq = static_cast<int>(h1 - h0) * group;
+        a.Hkv = static_cast<int>(h1 - h0);
+        a.Nq = Nq;
+        a.Nk = Nk;
+        a.total_q = 0;
+        a.total_k = 0;
+        a.d = d;
+        a.causal = causal ? 1 : 0;
+        a.no_skip = (flags & FA_FLAG_NO_CAUSAL_SKIP) ? 1 : 0;
+        a.scale = scale;
+        a.in_bf16 = in_dtype == FA_BF16 ? 1 : 0;
+        a.out_dtype = out_dtype;
+        a.schedule = schedule_of(flags);
+        rc = launch_prefill(a, dev, st);
+        if (rc != FA_OK) break;
+        if ((e = cudaEventRecord(hp->comp[c], st)) || (e = cudaStreamWaitEvent(hp->s_out, hp->comp[c], 0)) ||
+            (e = cudaMemcpyAsync(oh + oo, od + oo, on, cudaMemcpyDeviceToHost, hp->s_out)))
+            rc = cuda_fail(e);
+    }
+    // `stream` continues after both copy streams (the last output copy, and on
+    // an error any input copy already issued); the buffers then go back to the
+    // pool, stream-ordered.
+    for (cudaStream_t s : {hp->s_in, hp->s_out}) {
+        if ((e = cudaEventRecord(hp->done, s)) == cudaSuccess) e = cudaStreamWaitEvent(st, hp->done, 0);
+        if (e != cudaSuccess && rc == FA_OK) rc = cuda_fail(e);
+    }
+    e = scratch_free(buf, st);
+    if (e != cudaSuccess && rc == FA_OK) rc = cuda_fail(e);
+    return rc;
 }
 
 int fa_prefill_varlen(const void *q, const void *k, const void *v, void *out,

@@ -127,6 +127,28 @@ int fa_prefill_gqa(const void *q, const void *k, const void *v, void *out,
                    unsigned flags, void *stream);
 
 /*
+ * Prefill on host buffers (the end-to-end form of fa_prefill_gqa): copies q,
+ * k and v to the device, computes, and copies the output back, all ordered on
+ * `stream`.  The call returns once the work is enqueued; out_host holds the
+ * result when the stream reaches that point, and the four host buffers must
+ * stay valid until then.  Page-locked (pinned) host memory lets the copies run
+ * asynchronously; other host memory works but its copies serialise.
+ * The flattened key/value heads (B * Hkv) are cut into up to four chunks:
+ * chunk c's input copies (on a library-owned copy stream), its kernel (on
+ * `stream`) and its output copy (on a second copy stream) overlap the
+ * neighbouring chunks'.  Device buffers for q, k, v and out come from the
+ * library's stream-ordered pool and go back to it after the last copy.
+ *   q_host, out_host : [B][Hq][Nq][d]    k_host, v_host : [B][Hkv][Nk][d]
+ * Other arguments as fa_prefill_gqa.  Errors as fa_prefill_gqa, plus
+ * FA_ERR_WORKSPACE when the device buffers cannot be allocated.  Calls from
+ * several host threads are serialised while they enqueue.
+ */
+int fa_prefill_host(const void *q_host, const void *k_host, const void *v_host,
+                    void *out_host, int B, int Hq, int Hkv, int Nq, int Nk, int d,
+                    int causal, float scale, fa_dtype in_dtype,
+                    fa_dtype out_dtype, unsigned flags, void *stream);
+
+/*
  * Prefill that also returns, for every query row, the log-sum-exp of its
  * visible scores, lse_i = log sum_j exp(scale q_i.k_j) (natural log; -inf for
  * a row that sees no key).  It is what fa_prefill_backward needs to recompute
@@ -231,7 +253,7 @@ int fa_prefill_varlen(const void *q, const void *k, const void *v, void *out,
  * the device-resident lengths, so it needs no device-to-host copy and gives
  * bit-identical results run to run.  The partials workspace is allocated
  * stream-ordered on `stream` from a memory pool the library creates once per
- * device; the pool keeps up to 256 MiB of freed scratch mapped for reuse.
+ * device; the pool keeps up to 1 GiB of freed scratch mapped for reuse.
  */
 int fa_decode(const void *q, const void *k_cache, const void *v_cache,
               const int32_t *seq_lens, void *out,

@@ -80,6 +80,22 @@ def test_gqa_prefill_argument_errors(lib, args, status):
     assert binding.fa_prefill_gqa(*args, None) == status
 
 
+@pytest.mark.parametrize("args,status", [
+    ((None, A, A, B_, 1, 4, 2, 8, 8, 64, 0, 1.0, 0, 0, 0), 1),
+    ((A, A, A, None, 1, 4, 2, 8, 8, 64, 0, 1.0, 0, 0, 0), 1),
+    ((A, A, A, B_, 1, 6, 4, 8, 8, 64, 0, 1.0, 0, 0, 0), 2),      # Hq not a multiple of Hkv
+    ((A, A, A, B_, 0, 4, 2, 8, 8, 64, 0, 1.0, 0, 0, 0), 2),
+    ((A, A, A, B_, 1, 4, 2, 8, 8, 96, 0, 1.0, 0, 0, 0), 3),
+    ((A, A, A, B_, 1, 4, 2, 8, 8, 64, 0, 1.0, 2, 0, 0), 4),
+    ((A, A, A + 8, B_, 1, 4, 2, 8, 8, 64, 0, 1.0, 0, 0, 0), 5),
+    ((A, A, A, B_, 1, 4, 2, 8, 8, 64, 0, float("nan"), 0, 0, 0), 6),
+    ((A, A, A, A + 256, 1, 4, 2, 8, 8, 64, 0, 1.0, 0, 0, 0), 11),  # out inside q
+])
+def test_host_buffer_prefill_argument_errors(lib, args, status):
+    # the host-buffer entry point validates like the device one, before any CUDA call
+    assert binding.fa_prefill_host(*args, None) == status
+
+
 CU = 1 << 16
 
 
