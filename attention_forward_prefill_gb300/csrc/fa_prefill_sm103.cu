@@ -242,6 +242,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const __grid_constant__ CUtensorMap map_v, const Params p,
                    const __grid_constant__ StepTable tab) {
     using L = Layout<D>;
+    constexpr uint32_t kGroups = L::kStages / 2;  // key/value groups of two ring slots
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -302,12 +303,35 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t pol_q = l2_policy_evict_first();
             uint8_t *q_smem = smem + L::kQOff;
             uint8_t *ring = smem + L::kRingOff;
-            uint32_t qc = 0, rc = 0;
+            uint32_t qc = 0, gc = 0;
             bool ok = true;
             SegCursor cur;
             seg_begin(p, cur);
             Work w;
             const bool packed = p.cu_q != nullptr;
+            // Key/value tiles travel in groups, one per MMA step: {K_j0}, then
+            // {V_j, K_j+1} for every step j, the last {V_j1-1}.  A group takes one
+            // two-slot stage of the ring and one full/empty barrier pair.
+            auto open_group = [&](uint32_t bytes) {
+                const uint32_t st = gc % kGroups;
+                if (gc >= kGroups &&
+                    !mbar_wait(kv_empty + st, ((gc / kGroups) - 1) & 1, abort_flag, kWatchdogNs))
+                    return -1;
+                mbar_arrive_expect_tx(kv_full + st, bytes);
+                return static_cast<int>(st);
+            };
+            auto load_tile = [&](int st, int half, bool is_v, int j) {
+                uint8_t *dst = ring + (2 * st + half) * L::kTileBytes;
+                const CUtensorMap *m = is_v ? &map_v : &map_k;
+                for (int c = 0; c < L::kChunks; ++c) {
+                    if (packed)
+                        tma_load_3d(dst + c * L::kChunkBytes, m, kv_full + st, c * 64, w.hk,
+                                    static_cast<int>(w.kt0 + j * kBlockN), pol_kv);
+                    else
+                        tma_load_3d(dst + c * L::kChunkBytes, m, kv_full + st, c * 64, j * kBlockN,
+                                    w.b * p.Hkv + w.hk, pol_kv);
+                }
+            };
             while (ok && seg_next(p, tab, cur, w)) {
                 if (w.j1 <= w.j0) continue;  // no key tiles: the softmax warps write zeros
                 // query tile t is loaded when it has key tiles in [j0, j1)
@@ -330,29 +354,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 ++qc;
-                for (int j = w.j0; j < w.j1 && ok; ++j) {
-                    for (int kv = 0; kv < 2; ++kv) {
-                        const uint32_t slot = rc % L::kStages;
-                        if (rc >= (uint32_t)L::kStages &&
-                            !mbar_wait(kv_empty + slot, ((rc / L::kStages) - 1) & 1, abort_flag,
-                                       kWatchdogNs)) {
-                            ok = false;
-                            break;
-                        }
-                        mbar_arrive_expect_tx(kv_full + slot, L::kTileBytes);
-                        const CUtensorMap *m = kv ? &map_v : &map_k;
-                        for (int c = 0; c < L::kChunks; ++c) {
-                            if (packed)
-                                tma_load_3d(ring + slot * L::kTileBytes + c * L::kChunkBytes, m,
-                                            kv_full + slot, c * 64, w.hk,
-                                            static_cast<int>(w.kt0 + j * kBlockN), pol_kv);
-                            else
-                                tma_load_3d(ring + slot * L::kTileBytes + c * L::kChunkBytes, m,
-                                            kv_full + slot, c * 64, j * kBlockN, w.b * p.Hkv + w.hk,
-                                            pol_kv);
-                        }
-                        ++rc;
-                    }
+                int st = open_group(L::kTileBytes);
+                if (st < 0) { ok = false; break; }
+                load_tile(st, 0, false, w.j0);
+                ++gc;
+                for (int j = w.j0; j < w.j1; ++j) {
+                    const bool next_k = j + 1 < w.j1;
+                    st = open_group((next_k ? 2 : 1) * L::kTileBytes);
+                    if (st < 0) { ok = false; break; }
+                    load_tile(st, 0, true, j);
+                    if (next_k) load_tile(st, 1, false, j + 1);
+                    ++gc;
                 }
             }
             if (!ok) {
@@ -360,8 +372,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 constexpr uint64_t kDrainNs = 200ull * 1000ull * 1000ull;
                 int dummy = 0;
                 if (qc > 0) mbar_wait(q_full, (qc - 1) & 1, &dummy, kDrainNs);
-                for (uint32_t i = (rc > (uint32_t)L::kStages ? rc - L::kStages : 0); i < rc; ++i)
-                    mbar_wait(kv_full + (i % L::kStages), (i / L::kStages) & 1, &dummy, kDrainNs);
+                for (uint32_t i = (gc > (uint32_t)kGroups ? gc - kGroups : 0); i < gc; ++i)
+                    mbar_wait(kv_full + (i % kGroups), (i / kGroups) & 1, &dummy, kDrainNs);
             }
         }
         __syncwarp();
@@ -378,12 +390,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t s_tmem0 = tmem + L::kSCol0, s_tmem1 = tmem + L::kSCol1;
             const uint32_t o_tmem0 = tmem + L::kOCol0, o_tmem1 = tmem + L::kOCol1;
             const uint32_t p_tmem0 = tmem + L::kPCol0, p_tmem1 = tmem + L::kPCol1;
-            uint32_t qc = 0, rc = 0, pc0 = 0, pc1 = 0;
+            uint32_t qc = 0, gc = 0, pc0 = 0, pc1 = 0;
             uint32_t qk0 = 0, qk1 = 0;  // Q K^T products issued per tile (separate-P mode)
             bool ok = true;
             SegCursor cur;
             seg_begin(p, cur);
             Work w;
+            // the next key/value group in shared memory: its ring stage.  Within a
+            // step the tcgen05 fence after the first P (or S-free) wait also covers it.
+            auto take_group = [&](bool fence) {
+                const uint32_t st = gc % kGroups;
+                if (!mbar_wait(kv_full + st, (gc / kGroups) & 1, abort_flag, kWatchdogNs)) return -1;
+                if (fence) tc_fence_after();
+                return static_cast<int>(st);
+            };
             while (ok && seg_next(p, tab, cur, w)) {
                 const int j0 = w.j0, j1 = w.j1;
                 if (j1 <= j0) continue;  // no key tiles: nothing to multiply
@@ -392,14 +412,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!mbar_wait(q_full, qc & 1, abort_flag, kWatchdogNs)) { ok = false; break; }
                 ++qc;
                 tc_fence_after();
-                {   // S_t = Q_t K_0^T
-                    const uint32_t slot = rc % L::kStages;
-                    if (!mbar_wait(kv_full + slot, (rc / L::kStages) & 1, abort_flag, kWatchdogNs)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint64_t k_desc = sdesc_sw128(ring_addr + slot * L::kTileBytes, 16, 1024);
+                {   // S_t = Q_t K_j0^T from the group {K_j0}
+                    const int st = take_group(true);
+                    if (st < 0) { ok = false; break; }
+                    const uint64_t k_desc = sdesc_sw128(ring_addr + 2 * st * L::kTileBytes, 16, 1024);
                     if constexpr (L::kSepP) {
                         // S_t is free once the softmax has loaded the previous one
                         if (n0 > j0) {
@@ -432,24 +448,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                             umma_commit(s_full + 1);
                         }
                     }
-                    umma_commit(kv_empty + slot);
-                    ++rc;
+                    umma_commit(kv_empty + st);
+                    ++gc;
                     if (j1 - j0 == 1) umma_commit(q_empty);
                 }
                 for (int j = j0; j < j1 && ok; ++j) {
-                    const uint32_t slot_v = rc % L::kStages;
-                    if (!mbar_wait(kv_full + slot_v, (rc / L::kStages) & 1, abort_flag, kWatchdogNs)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    ++rc;
-                    const uint64_t v_desc =
-                        sdesc_sw128(ring_addr + slot_v * L::kTileBytes, L::kChunkBytes, 1024);
-                    const uint32_t slot_k = rc % L::kStages;
-                    const uint64_t k_desc = sdesc_sw128(ring_addr + slot_k * L::kTileBytes, 16, 1024);
-                    const uint32_t k_parity = (rc / L::kStages) & 1;
-                    bool k_ready = false;
+                    // the group {V_j, K_j+1} (the last step's group holds V_j alone)
+                    const int st = take_group(false);
+                    if (st < 0) { ok = false; break; }
+                    const uint32_t stage_addr = ring_addr + 2 * st * L::kTileBytes;
+                    const uint64_t v_desc = sdesc_sw128(stage_addr, L::kChunkBytes, 1024);
+                    const uint64_t k_desc = sdesc_sw128(stage_addr + L::kTileBytes, 16, 1024);
                     // One query tile's step: wait for P_t, O_t (+)= P_t V_j, then
                     // S_t = Q_t K_{j+1}^T (issued after the PV product that reads P_t).
                     auto tile_step = [&](int nt, uint64_t *pf, uint32_t &pc, uint32_t s_t,
@@ -461,12 +470,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                         issue_pv<D>(o_t, s_t, v_desc, idesc_pv, j > j0);
                         if (j == nt - 1) umma_commit(od);
                         if (j + 1 < nt) {
-                            if (!k_ready) {
-                                if (!mbar_wait(kv_full + slot_k, k_parity, abort_flag, kWatchdogNs))
-                                    return false;
-                                tc_fence_after();
-                                k_ready = true;
-                            }
                             issue_qk<D>(s_t, q_desc, k_desc, idesc_qk);
                             umma_commit(sf);
                         }
@@ -480,11 +483,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (j >= nt) return true;
                         if (j + 1 < nt) {
                             if (!mbar_wait(sfree, (qk - 1) & 1, abort_flag, kWatchdogNs)) return false;
-                            if (!k_ready) {
-                                if (!mbar_wait(kv_full + slot_k, k_parity, abort_flag, kWatchdogNs))
-                                    return false;
-                                k_ready = true;
-                            }
                             tc_fence_after();
                             issue_qk<D>(s_t, q_desc, k_desc, idesc_qk);
                             umma_commit(sf);
@@ -509,12 +507,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                                        o_done + 1);
                     }
                     if (!ok) break;
-                    umma_commit(kv_empty + slot_v);
-                    if (j + 1 < j1) {
-                        umma_commit(kv_empty + slot_k);
-                        ++rc;
-                        if (j + 1 == j1 - 1) umma_commit(q_empty);
-                    }
+                    umma_commit(kv_empty + st);
+                    ++gc;
+                    if (j + 1 == j1 - 1) umma_commit(q_empty);
                 }
             }
             // Nothing may still be running on the tensor core at teardown.
