@@ -27,6 +27,7 @@
 // than TAU (log2 units), so p <= 2^TAU; O and l share m_ref, so the final O/l
 // is unchanged.
 #include <algorithm>
+#include <type_traits>
 #include <cfloat>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -60,7 +61,7 @@ struct Layout {
     static constexpr int kChunkBytes = kBlockM * 128;  // 128 rows x 64 16-bit columns
     static constexpr int kChunks = D / 64;
     static constexpr int kTileBytes = kChunks * kChunkBytes;
-    static constexpr int kStages = (D == 128) ? 4 : 8;
+    static constexpr int kStages = 4;  // two key/value groups of two tiles
     static constexpr int kQOff = 0;
     static constexpr int kRingOff = 2 * kTileBytes;
     static constexpr int kBarOff = kRingOff + kStages * kTileBytes;
@@ -387,6 +388,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t q_desc0 = sdesc_sw128(q_addr, 16, 1024);
             const uint64_t q_desc1 = sdesc_sw128(q_addr + L::kTileBytes, 16, 1024);
             const uint32_t ring_addr = smem_u32(smem + L::kRingOff);
+            // Descriptors of every ring stage, built once: a step picks its stage
+            // at compile time (below), so no descriptor is computed in the loop.
+            // stage st: slot 2 st holds V_j (or K_j0 of a unit's first group), slot
+            // 2 st + 1 holds K_j+1.
+            uint64_t vdesc[kGroups], kdesc[kGroups], k0desc[kGroups];
+#pragma unroll
+            for (int g = 0; g < (int)kGroups; ++g) {
+                const uint32_t a = ring_addr + 2 * g * L::kTileBytes;
+                vdesc[g] = sdesc_sw128(a, L::kChunkBytes, 1024);
+                kdesc[g] = sdesc_sw128(a + L::kTileBytes, 16, 1024);
+                k0desc[g] = sdesc_sw128(a, 16, 1024);
+            }
             const uint32_t s_tmem0 = tmem + L::kSCol0, s_tmem1 = tmem + L::kSCol1;
             const uint32_t o_tmem0 = tmem + L::kOCol0, o_tmem1 = tmem + L::kOCol1;
             const uint32_t p_tmem0 = tmem + L::kPCol0, p_tmem1 = tmem + L::kPCol1;
@@ -415,7 +428,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 {   // S_t = Q_t K_j0^T from the group {K_j0}
                     const int st = take_group(true);
                     if (st < 0) { ok = false; break; }
-                    const uint64_t k_desc = sdesc_sw128(ring_addr + 2 * st * L::kTileBytes, 16, 1024);
+                    uint64_t k_desc = k0desc[0];
+#pragma unroll
+                    for (int g = 1; g < (int)kGroups; ++g)
+                        if (st == g) k_desc = k0desc[g];
                     if constexpr (L::kSepP) {
                         // S_t is free once the softmax has loaded the previous one
                         if (n0 > j0) {
@@ -456,9 +472,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // the group {V_j, K_j+1} (the last step's group holds V_j alone)
                     const int st = take_group(false);
                     if (st < 0) { ok = false; break; }
-                    const uint32_t stage_addr = ring_addr + 2 * st * L::kTileBytes;
-                    const uint64_t v_desc = sdesc_sw128(stage_addr, L::kChunkBytes, 1024);
-                    const uint64_t k_desc = sdesc_sw128(stage_addr + L::kTileBytes, 16, 1024);
+                    // the step's body, instantiated per ring stage (a compile-time constant)
+                    auto step = [&](auto stage) {
+                    constexpr int ST = decltype(stage)::value;
+                    const uint64_t v_desc = vdesc[ST];
+                    const uint64_t k_desc = kdesc[ST];
                     // One query tile's step: wait for P_t, O_t (+)= P_t V_j, then
                     // S_t = Q_t K_{j+1}^T (issued after the PV product that reads P_t).
                     auto tile_step = [&](int nt, uint64_t *pf, uint32_t &pc, uint32_t s_t,
@@ -506,8 +524,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                              tile_step(n1, p_full + 1, pc1, s_tmem1, o_tmem1, q_desc1, s_full + 1,
                                        o_done + 1);
                     }
+                    if (ok) umma_commit(kv_empty + ST);
+                    };
+                    static_assert(kGroups == 2, "two ring stages");
+                    if (st == 0) step(std::integral_constant<int, 0>{});
+                    else if (st == 1) step(std::integral_constant<int, 1>{});
                     if (!ok) break;
-                    umma_commit(kv_empty + st);
                     ++gc;
                     if (j + 1 == j1 - 1) umma_commit(q_empty);
                 }
