@@ -482,7 +482,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     auto tile_step = [&](int nt, uint64_t *pf, uint32_t &pc, uint32_t s_t,
                                          uint32_t o_t, uint64_t q_desc, uint64_t *sf, uint64_t *od) {
                         if (j >= nt) return true;
-                        if (!mbar_wait(pf, pc & 1, abort_flag, kWatchdogNs)) return false;
+                        // polled, not suspended: the product should start the moment P is in
+                        if (!mbar_spin(pf, pc & 1, abort_flag, kWatchdogNs)) return false;
                         ++pc;
                         tc_fence_after();
                         issue_pv<D>(o_t, s_t, v_desc, idesc_pv, j > j0);
