@@ -241,19 +241,22 @@ def _stream_handle(device) -> int:
 
 
 def prefill(q, k, v, causal: bool = False, scale: float | None = None, out_dtype=None,
-            flags: int = 0, out=None):
+            flags: int = 0, out=None, sync: bool = True):
     """out = softmax(scale * q k^T [causal]) v for q [B, Hq, Nq, d] and k, v
     [B, Hkv, Nk, d] (fp16/bf16; Hq a multiple of Hkv; causal queries are the
     last Nq positions).
 
     CUDA inputs run on the current stream and return a CUDA tensor.  Host
     inputs go through fa_prefill_host (copies in, compute and copies out
-    pipelined over chunks of heads); the call waits for the current stream and
-    returns the host result (pinned when q is).
+    pipelined over chunks of heads) on the current stream and return the host
+    result (pinned when q is).  With sync (the default) the call waits for the
+    stream first; with sync=False it returns at once, like the C call, and the
+    result is ready, and the host tensors free to reuse, once the stream has
+    passed the call.
     """
     torch = _torch()
     if not q.is_cuda:
-        return _prefill_host(torch, q, k, v, causal, scale, out_dtype, flags, out)
+        return _prefill_host(torch, q, k, v, causal, scale, out_dtype, flags, out, sync)
     B, Hq, Nq, d = q.shape
     _check_cuda("q", q)
     _check_cuda("k", k, None, q.dtype)
@@ -289,7 +292,7 @@ def _check_host(name, t, shape=None, dtype=None):
         raise ValueError(f"{name} has dtype {t.dtype}, expected {dtype}")
 
 
-def _prefill_host(torch, q, k, v, causal, scale, out_dtype, flags, out):
+def _prefill_host(torch, q, k, v, causal, scale, out_dtype, flags, out, sync=True):
     B, Hq, Nq, d = q.shape
     _check_host("q", q)
     _check_host("k", k, None, q.dtype)
@@ -310,7 +313,8 @@ def _prefill_host(torch, q, k, v, causal, scale, out_dtype, flags, out):
                          stream.cuda_stream)
     if rc != FA_OK:
         raise FaError(rc, "fa_prefill_host")
-    stream.synchronize()
+    if sync:
+        stream.synchronize()
     return out
 
 

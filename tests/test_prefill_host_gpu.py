@@ -81,3 +81,22 @@ def test_host_buffers_repeat_on_a_side_stream(fa):
         outs = [fa.prefill(q, k, v, causal=True, scale=0.125) for _ in range(3)]
     for o in outs:
         assert torch.equal(o.view(torch.int16), ref.view(torch.int16))
+
+
+def test_host_buffers_asynchronous_on_several_streams(fa):
+    # sync=False: the calls return at once; after a device synchronisation every
+    # output equals the synchronous call's
+    import torch
+    shapes = [(1, 4, 1024, 64), (1, 8, 2048, 64), (2, 4, 512, 64)]
+    ins = [[host_tensor(inputs.normal_bits(sh, 1800 + 3 * n + i, "f16"), "f16", True) for i in range(3)]
+           for n, sh in enumerate(shapes)]
+    refs = [fa.prefill(*x, causal=True, scale=0.125) for x in ins]
+    outs = [torch.empty(sh, dtype=torch.float16, pin_memory=True) for sh in shapes]
+    streams = [torch.cuda.Stream() for _ in shapes]
+    for _ in range(2):
+        for x, o, s in zip(ins, outs, streams):
+            with torch.cuda.stream(s):
+                fa.prefill(*x, causal=True, scale=0.125, out=o, sync=False)
+        torch.cuda.synchronize()
+        for o, r in zip(outs, refs):
+            assert torch.equal(o.view(torch.int16), r.view(torch.int16))
