@@ -501,13 +501,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                                              uint64_t q_desc, uint64_t *sf, uint64_t *pvd) {
                         if (j >= nt) return true;
                         if (j + 1 < nt) {
-                            if (!mbar_wait(sfree, (qk - 1) & 1, abort_flag, kWatchdogNs)) return false;
+                            if (!mbar_spin(sfree, (qk - 1) & 1, abort_flag, kWatchdogNs)) return false;
                             tc_fence_after();
                             issue_qk<D>(s_t, q_desc, k_desc, idesc_qk);
                             umma_commit(sf);
                             ++qk;
                         }
-                        if (!mbar_wait(pf, pc & 1, abort_flag, kWatchdogNs)) return false;
+                        if (!mbar_spin(pf, pc & 1, abort_flag, kWatchdogNs)) return false;
                         ++pc;
                         tc_fence_after();
                         issue_pv<D>(o_t, p_t, v_desc, idesc_pv, j > j0);
