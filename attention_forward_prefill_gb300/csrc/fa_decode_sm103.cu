@@ -376,34 +376,76 @@ __global__ void __launch_bounds__(kSplitThreads)
     }
 }
 
+template <int N> struct VecF;
+template <> struct VecF<2> { using T = float2; };
+template <> struct VecF<4> { using T = float4; };
+
+__device__ __forceinline__ void vadd_scaled(float (&o)[2], float w, const float2 &a) {
+    o[0] = fmaf(w, a.x, o[0]);
+    o[1] = fmaf(w, a.y, o[1]);
+}
+__device__ __forceinline__ void vadd_scaled(float (&o)[4], float w, const float4 &a) {
+    o[0] = fmaf(w, a.x, o[0]);
+    o[1] = fmaf(w, a.y, o[1]);
+    o[2] = fmaf(w, a.z, o[2]);
+    o[3] = fmaf(w, a.w, o[3]);
+}
+
 template <int D>
 __global__ void __launch_bounds__(kMergeWarps * 32)
     decode_merge_kernel(const DParams p) {
     constexpr int EPL = D / 32;  // output elements per lane
+    constexpr int G = 8;         // partial vectors in flight per lane
+    using Vec = typename VecF<EPL>::T;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int gw = blockIdx.x * kMergeWarps + warp;
+    const bool live = gw < p.BH;
+    // The lengths are the caller's input, not the split kernel's output, so
+    // they are read before the wait.
+    int n_act = 0;
+    if (live) {
+        const int len = clamp_len(p.seq_lens[gw / p.H], p.max_len);
+        n_act = (len + p.chunk - 1) / p.chunk;
+    }
     // Wait until the split kernel has completed and its partials are visible.
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    if (gw >= p.BH) return;
-    const int b = gw / p.H;
-    const int len = clamp_len(p.seq_lens[b], p.max_len);
-    const int n_act = (len + p.chunk - 1) / p.chunk;
+    if (!live) return;
     float o[EPL];
 #pragma unroll
     for (int e = 0; e < EPL; ++e) o[e] = 0.f;
     if (n_act > 0) {
-        const float *ml = p.ml + static_cast<size_t>(gw) * p.splits * 2;
-        const float *acc = p.acc + static_cast<size_t>(gw) * p.splits * D + lane * EPL;
-        float M = ml[0];
-        for (int s = 1; s < n_act; ++s) M = fmaxf(M, ml[2 * s]);
-        float L = 0.f;
-        for (int s = 0; s < n_act; ++s) {
-            const float w = ex2_approx(ml[2 * s] - M);
-            L = fmaf(w, ml[2 * s + 1], L);
+        const float2 *ml = reinterpret_cast<const float2 *>(p.ml) + static_cast<size_t>(gw) * p.splits;
+        const Vec *acc = reinterpret_cast<const Vec *>(p.acc + static_cast<size_t>(gw) * p.splits * D) + lane;
+        constexpr int VPS = D / EPL;  // Vec per split
+        // Split s's (m_s, l_s) lives in lane s % 32; the first G partial
+        // vectors are requested together with them.
+        Vec a[G];
 #pragma unroll
-            for (int e = 0; e < EPL; ++e) o[e] = fmaf(w, acc[static_cast<size_t>(s) * D + e], o[e]);
+        for (int u = 0; u < G; ++u) a[u] = u < n_act ? acc[u * VPS] : Vec{};
+        float2 mv = lane < n_act ? ml[lane] : make_float2(-INFINITY, 0.f);
+        float M = mv.x;
+        for (int s = 32 + lane; s < n_act; s += 32) M = fmaxf(M, ml[s].x);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+        float lsum = 0.f, w = 0.f;
+        for (int g0 = 0; g0 < n_act; g0 += G) {
+            if ((g0 & 31) == 0) {  // the next 32 splits' weights w_s = 2^(m_s - M)
+                if (g0 > 0) mv = g0 + lane < n_act ? ml[g0 + lane] : make_float2(-INFINITY, 0.f);
+                w = g0 + lane < n_act ? ex2_approx(mv.x - M) : 0.f;
+                lsum = fmaf(w, mv.y, lsum);
+            }
+            if (g0 > 0) {
+#pragma unroll
+                for (int u = 0; u < G; ++u) a[u] = g0 + u < n_act ? acc[(g0 + u) * VPS] : Vec{};
+            }
+            // splits in index order; past n_act both w and a are 0
+#pragma unroll
+            for (int u = 0; u < G; ++u)
+                vadd_scaled(o, __shfl_sync(0xffffffffu, w, (g0 & 31) + u), a[u]);
         }
-        const float inv = 1.0f / L;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, off);
+        const float inv = 1.0f / lsum;
 #pragma unroll
         for (int e = 0; e < EPL; ++e) o[e] *= inv;
     }
