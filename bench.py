@@ -46,7 +46,7 @@ NCU_TRAFFIC = {
                 "bytes_per_launch": {"4096": 115.74e6 / 2, "8192": 115.74e6, "16384": 115.74e6 * 2},
                 "measured_at": "8192", "scaled": ["4096", "16384"]},
     # B=32, H=14 (profiles/decode_split_b32_h14.md): DRAM bytes of one split-kernel launch
-    "decode": {"src": "fa_decode_sm103.cu", "src_sha": "4ff185fa2bee8b5b", "bytes_per_launch": 263.6e6},
+    "decode": {"src": "fa_decode_sm103.cu", "src_sha": "b66f8ad7b76c86db", "bytes_per_launch": 263.9e6},
 }
 
 
