@@ -52,12 +52,15 @@ struct BwdLayout {
     static constexpr int kStageBytes = 2 * kTileBytes;
     static constexpr int kVecOff = kRingOff + kStages * kStageBytes;  // [8 warps][2 buf][2][64] floats
     static constexpr int kBarOff = kVecOff + kBwdEltWarps * 2 * 2 * 64 * 4;
-    // fix_full, s_full, p_ready, acc_done, drain, s_loaded, ring_full[S], ring_empty[S]
-    static constexpr int kNumBars = 6 + 2 * kStages;
+    // fix_full, s_full, p_ready, acc_done, drain, s_loaded, ring_full[S], ring_empty[S], dq_done
+    static constexpr int kNumBars = 7 + 2 * kStages;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
     static constexpr int kSmemBytes = kMiscOff + 16 + 1024;
-    // TMEM: X (S or S^T) | Y (dP or dP^T) | accumulator A | accumulator B
+    // TMEM: X (S or S^T) | Y (dP or dP^T) | accumulator A | accumulator B; the dQ
+    // kernel keeps dS in 64 columns of its own at column 384 (B is unused there,
+    // and at d = 64 those columns are free).
     static constexpr uint32_t kXCol = 0, kYCol = 128, kACol = 256, kBCol = 256 + D;
+    static constexpr uint32_t kDsCol = 384;
 };
 
 struct BwdParams {
@@ -383,6 +386,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     uint64_t *fix_full = bars + 0, *s_full = bars + 1, *p_ready = bars + 2, *acc_done = bars + 3;
     uint64_t *drain = bars + 4, *s_loaded = bars + 5;
     uint64_t *ring_full = bars + 6, *ring_empty = bars + 6 + L::kStages;
+    uint64_t *dq_done = bars + 6 + 2 * L::kStages;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kMiscOff);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kMiscOff + 4);
 
@@ -400,6 +404,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_init(acc_done, 1);
         mbar_init(drain, 1);
         mbar_init(s_loaded, kBwdEltWarps);
+        mbar_init(dq_done, 1);
         for (int s = 0; s < L::kStages; ++s) {
             mbar_init(ring_full + s, 1);
             mbar_init(ring_empty + s, 1);
@@ -466,27 +471,44 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             const uint64_t q_desc = sdesc_sw128(fix, 16, 1024);
             const uint64_t do_desc = sdesc_sw128(fix + L::kTileBytes, 16, 1024);
             bool ok = mbar_wait(fix_full, 0, abort_flag, kWatchdogNs);
-            for (int n = 0; n < n_iter && ok; ++n) {
-                const int slot = n % L::kStages;
-                if (!mbar_wait(ring_full + slot, (n / L::kStages) & 1, abort_flag, kWatchdogNs)) {
-                    ok = false;
-                    break;
-                }
+            // S = Q K_j^T and dP = dO V_j^T (queries on TMEM lanes) for key tile j
+            auto issue_scores = [&](int j) {
+                const int slot = j % L::kStages;
+                if (!mbar_wait(ring_full + slot, (j / L::kStages) & 1, abort_flag, kWatchdogNs)) return false;
                 tc_fence_after();
                 const uint32_t st = ring + slot * L::kStageBytes;
-                // S = Q K_j^T and dP = dO V_j^T (queries on TMEM lanes)
                 issue_qk<D>(tmem + L::kXCol, q_desc, sdesc_sw128(st, 16, 1024), idesc_s);
                 issue_qk<D>(tmem + L::kYCol, do_desc, sdesc_sw128(st + L::kTileBytes, 16, 1024), idesc_s);
                 umma_commit(s_full);
+                return true;
+            };
+            if (ok) ok = issue_scores(0);
+            for (int n = 0; n < n_iter && ok; ++n) {
+                // Once every elementwise warp holds S and dP of tile n in registers,
+                // the next tile's products run under their elementwise work.
+                if (n + 1 < n_iter) {
+                    if (!mbar_wait(s_loaded, n & 1, abort_flag, kWatchdogNs)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    if (!issue_scores(n + 1)) {
+                        ok = false;
+                        break;
+                    }
+                }
                 if (!mbar_wait(p_ready, n & 1, abort_flag, kWatchdogNs)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                // dQ += dS K_j (dS from TMEM over dP; K_j MN-major)
-                issue_pv<D>(tmem + L::kACol, tmem + L::kYCol, sdesc_sw128(st, kSlabBytes, 1024), idesc_acc,
+                // dQ += dS K_n (dS from its TMEM buffer; K_n MN-major)
+                const int slot = n % L::kStages;
+                const uint32_t st = ring + slot * L::kStageBytes;
+                issue_pv<D>(tmem + L::kACol, tmem + L::kDsCol, sdesc_sw128(st, kSlabBytes, 1024), idesc_acc,
                             n > 0);
                 umma_commit(ring_empty + slot);
+                umma_commit(dq_done);
             }
             umma_commit(acc_done);
             umma_commit(drain);
@@ -518,12 +540,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 reg_fence32(sr[h]);
                 reg_fence32(dr[h]);
             }
-            // dS of the upper half lands on columns of dP the lower half reads
+            // S and dP are in registers: the MMA thread may overwrite them
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(s_loaded);
-            if (!warp_wait(s_loaded, n & 1, abort_flag)) { ok = false; break; }
-            tc_fence_after();
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 const int q = 2 * hf + h;
@@ -539,8 +559,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 }
                 uint32_t pk[16], dk[16];
                 weights_quarter<BF16, false>(sr[h], dr[h], pk, dk, p.c, nullptr, nullptr, lse2_r, dsum_r, vis);
-                tmem_st16(tmem + lane_off + L::kYCol + q * 16, dk);  // dS over dP
+                if (h == 0 && n > 0) {
+                    // dS of tile n - 1 must have been read by its product.  This also
+                    // keeps p_ready from completing twice before the MMA thread,
+                    // which committed dq_done after seeing p_ready of tile n - 1, looks.
+                    if (!warp_wait(dq_done, (n - 1) & 1, abort_flag)) { ok = false; break; }
+                    tc_fence_after();
+                }
+                tmem_st16(tmem + lane_off + L::kDsCol + q * 16, dk);
             }
+            if (!ok) break;
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
