@@ -52,15 +52,34 @@ struct BwdLayout {
     static constexpr int kStageBytes = 2 * kTileBytes;
     static constexpr int kVecOff = kRingOff + kStages * kStageBytes;  // [8 warps][2 buf][2][64] floats
     static constexpr int kBarOff = kVecOff + kBwdEltWarps * 2 * 2 * 64 * 4;
-    // fix_full, s_full, p_ready, acc_done, drain, s_loaded, ring_full[S], ring_empty[S], dq_done
-    static constexpr int kNumBars = 7 + 2 * kStages;
+    // fix_full, s_full, p_ready, acc_done, drain, s_loaded, ring_full[S], ring_empty[S]
+    static constexpr int kNumBars = 6 + 2 * kStages;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
     static constexpr int kSmemBytes = kMiscOff + 16 + 1024;
-    // TMEM: X (S or S^T) | Y (dP or dP^T) | accumulator A | accumulator B; the dQ
-    // kernel keeps dS in 64 columns of its own at column 384 (B is unused there,
-    // and at d = 64 those columns are free).
+    // TMEM: X (S^T) | Y (dP^T) | accumulator A (dV) | accumulator B (dK)
     static constexpr uint32_t kXCol = 0, kYCol = 128, kACol = 256, kBCol = 256 + D;
-    static constexpr uint32_t kDsCol = 384;
+};
+
+// The dQ kernel's shared memory: Q_i and dO_i loaded once, then K_j and V_j
+// through rings of their own.  V_j is free once dP is computed, K_j only after
+// dQ += dS K_j, so K gets one stage more; with it the tiles the next score
+// products read are in place while the current elementwise work runs.
+template <int D>
+struct DqLayout {
+    static constexpr int kChunks = D / 64;
+    static constexpr int kTileBytes = kChunks * kSlabBytes;  // 128 rows x D 16-bit
+    static constexpr int kKStages = D == 128 ? 3 : 4, kVStages = D == 128 ? 2 : 3;
+    static constexpr int kFixOff = 0;                        // Q_i, dO_i
+    static constexpr int kKOff = 2 * kTileBytes;
+    static constexpr int kVOff = kKOff + kKStages * kTileBytes;
+    static constexpr int kBarOff = kVOff + kVStages * kTileBytes;
+    // fix_full, s_full, p_ready, acc_done, drain, s_loaded, dq_done,
+    // k_full[KS], k_empty[KS], v_full[VS], v_empty[VS]
+    static constexpr int kNumBars = 7 + 2 * kKStages + 2 * kVStages;
+    static constexpr int kMiscOff = kBarOff + kNumBars * 8;
+    static constexpr int kSmemBytes = kMiscOff + 16 + 1024;
+    // TMEM: S | dP | dQ accumulator | dS (16-bit, 64 columns)
+    static constexpr uint32_t kXCol = 0, kYCol = 128, kACol = 256, kDsCol = 384;
 };
 
 struct BwdParams {
@@ -378,15 +397,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                   const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_do,
                   const BwdParams p) {
-    using L = BwdLayout<D>;
+    using L = DqLayout<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kBarOff);
     uint64_t *fix_full = bars + 0, *s_full = bars + 1, *p_ready = bars + 2, *acc_done = bars + 3;
     uint64_t *drain = bars + 4, *s_loaded = bars + 5;
-    uint64_t *ring_full = bars + 6, *ring_empty = bars + 6 + L::kStages;
-    uint64_t *dq_done = bars + 6 + 2 * L::kStages;
+    uint64_t *dq_done = bars + 6;
+    uint64_t *k_full = bars + 7, *k_empty = k_full + L::kKStages;
+    uint64_t *v_full = k_empty + L::kKStages, *v_empty = v_full + L::kVStages;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kMiscOff);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kMiscOff + 4);
 
@@ -405,9 +425,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_init(drain, 1);
         mbar_init(s_loaded, kBwdEltWarps);
         mbar_init(dq_done, 1);
-        for (int s = 0; s < L::kStages; ++s) {
-            mbar_init(ring_full + s, 1);
-            mbar_init(ring_empty + s, 1);
+        for (int s = 0; s < L::kKStages; ++s) {
+            mbar_init(k_full + s, 1);
+            mbar_init(k_empty + s, 1);
+        }
+        for (int s = 0; s < L::kVStages; ++s) {
+            mbar_init(v_full + s, 1);
+            mbar_init(v_empty + s, 1);
         }
         *abort_flag = 0;
         fence_mbar_init();
@@ -429,7 +453,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
     if (warp == kBwdTmaWarp) {
         if (lane == 0) {
-            uint8_t *fix = smem + L::kFixOff, *ring = smem + L::kRingOff;
+            uint8_t *fix = smem + L::kFixOff, *kring = smem + L::kKOff, *vring = smem + L::kVOff;
             const uint64_t pol = l2_policy_evict_last();
             bool ok = true;
             mbar_arrive_expect_tx(fix_full, 2 * L::kTileBytes);
@@ -438,28 +462,39 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 tma_load_3d(fix + L::kTileBytes + c * kSlabBytes, &map_do, fix_full, c * 64, it * kRows, bh,
                             pol);
             }
-            int n = 0;
-            for (; n < n_iter && ok; ++n) {
-                const int slot = n % L::kStages;
-                if (n >= L::kStages &&
-                    !mbar_wait(ring_empty + slot, ((n / L::kStages) - 1) & 1, abort_flag, kWatchdogNs)) {
+            int nk = 0, nv = 0;  // K and V tiles issued
+            for (int n = 0; n < n_iter && ok; ++n) {
+                const int ks = n % L::kKStages;
+                if (n >= L::kKStages &&
+                    !mbar_wait(k_empty + ks, ((n / L::kKStages) - 1) & 1, abort_flag, kWatchdogNs)) {
                     ok = false;
                     break;
                 }
-                uint8_t *st = ring + slot * L::kStageBytes;
-                mbar_arrive_expect_tx(ring_full + slot, 2 * L::kTileBytes);
-                for (int c = 0; c < L::kChunks; ++c) {
-                    tma_load_3d(st + c * kSlabBytes, &map_k, ring_full + slot, c * 64, n * kRows, bhk, pol);
-                    tma_load_3d(st + L::kTileBytes + c * kSlabBytes, &map_v, ring_full + slot, c * 64, n * kRows,
+                mbar_arrive_expect_tx(k_full + ks, L::kTileBytes);
+                for (int c = 0; c < L::kChunks; ++c)
+                    tma_load_3d(kring + ks * L::kTileBytes + c * kSlabBytes, &map_k, k_full + ks, c * 64, n * kRows,
                                 bhk, pol);
+                ++nk;
+                const int vs = n % L::kVStages;
+                if (n >= L::kVStages &&
+                    !mbar_wait(v_empty + vs, ((n / L::kVStages) - 1) & 1, abort_flag, kWatchdogNs)) {
+                    ok = false;
+                    break;
                 }
+                mbar_arrive_expect_tx(v_full + vs, L::kTileBytes);
+                for (int c = 0; c < L::kChunks; ++c)
+                    tma_load_3d(vring + vs * L::kTileBytes + c * kSlabBytes, &map_v, v_full + vs, c * 64, n * kRows,
+                                bhk, pol);
+                ++nv;
             }
             if (!ok) {
                 constexpr uint64_t kDrainNs = 200ull * 1000ull * 1000ull;
                 int dummy = 0;
                 mbar_wait(fix_full, 0, &dummy, kDrainNs);
-                for (int m = (n > L::kStages ? n - L::kStages : 0); m < n; ++m)
-                    mbar_wait(ring_full + (m % L::kStages), (m / L::kStages) & 1, &dummy, kDrainNs);
+                for (int m = (nk > L::kKStages ? nk - L::kKStages : 0); m < nk; ++m)
+                    mbar_wait(k_full + (m % L::kKStages), (m / L::kKStages) & 1, &dummy, kDrainNs);
+                for (int m = (nv > L::kVStages ? nv - L::kVStages : 0); m < nv; ++m)
+                    mbar_wait(v_full + (m % L::kVStages), (m / L::kVStages) & 1, &dummy, kDrainNs);
             }
         }
         __syncwarp();
@@ -467,19 +502,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (lane == 0) {
             const uint32_t idesc_s = idesc_f16(BF16, kRows, kRows, false, false);
             const uint32_t idesc_acc = idesc_f16(BF16, kRows, D, false, true);
-            const uint32_t fix = smem_u32(smem + L::kFixOff), ring = smem_u32(smem + L::kRingOff);
+            const uint32_t fix = smem_u32(smem + L::kFixOff);
+            const uint32_t kring = smem_u32(smem + L::kKOff), vring = smem_u32(smem + L::kVOff);
             const uint64_t q_desc = sdesc_sw128(fix, 16, 1024);
             const uint64_t do_desc = sdesc_sw128(fix + L::kTileBytes, 16, 1024);
             bool ok = mbar_wait(fix_full, 0, abort_flag, kWatchdogNs);
             // S = Q K_j^T and dP = dO V_j^T (queries on TMEM lanes) for key tile j
             auto issue_scores = [&](int j) {
-                const int slot = j % L::kStages;
-                if (!mbar_wait(ring_full + slot, (j / L::kStages) & 1, abort_flag, kWatchdogNs)) return false;
+                const int ks = j % L::kKStages, vs = j % L::kVStages;
+                if (!mbar_wait(k_full + ks, (j / L::kKStages) & 1, abort_flag, kWatchdogNs)) return false;
+                if (!mbar_wait(v_full + vs, (j / L::kVStages) & 1, abort_flag, kWatchdogNs)) return false;
                 tc_fence_after();
-                const uint32_t st = ring + slot * L::kStageBytes;
-                issue_qk<D>(tmem + L::kXCol, q_desc, sdesc_sw128(st, 16, 1024), idesc_s);
-                issue_qk<D>(tmem + L::kYCol, do_desc, sdesc_sw128(st + L::kTileBytes, 16, 1024), idesc_s);
+                issue_qk<D>(tmem + L::kXCol, q_desc, sdesc_sw128(kring + ks * L::kTileBytes, 16, 1024), idesc_s);
+                issue_qk<D>(tmem + L::kYCol, do_desc, sdesc_sw128(vring + vs * L::kTileBytes, 16, 1024), idesc_s);
                 umma_commit(s_full);
+                umma_commit(v_empty + vs);  // V_j is read by dP alone
                 return true;
             };
             if (ok) ok = issue_scores(0);
@@ -502,12 +539,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     break;
                 }
                 tc_fence_after();
-                // dQ += dS K_n (dS from its TMEM buffer; K_n MN-major)
-                const int slot = n % L::kStages;
-                const uint32_t st = ring + slot * L::kStageBytes;
-                issue_pv<D>(tmem + L::kACol, tmem + L::kDsCol, sdesc_sw128(st, kSlabBytes, 1024), idesc_acc,
-                            n > 0);
-                umma_commit(ring_empty + slot);
+                // dQ += dS K_n (dS from its TMEM columns; K_n MN-major)
+                const int ks = n % L::kKStages;
+                issue_pv<D>(tmem + L::kACol, tmem + L::kDsCol, sdesc_sw128(kring + ks * L::kTileBytes, kSlabBytes, 1024),
+                            idesc_acc, n > 0);
+                umma_commit(k_empty + ks);
                 umma_commit(dq_done);
             }
             umma_commit(acc_done);
@@ -605,7 +641,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 template <int D, bool BF16>
 int launch_bwd_d(const BackwardLaunch &a, cudaStream_t stream) {
     using L = BwdLayout<D>;
-    static_assert(L::kSmemBytes <= 227 * 1024, "shared memory budget");
+    static_assert(L::kSmemBytes <= 227 * 1024 && DqLayout<D>::kSmemBytes <= 227 * 1024,
+                  "shared memory budget");
     const long long BH = static_cast<long long>(a.B) * a.H;      // query heads
     const long long BHk = static_cast<long long>(a.B) * a.Hkv;   // key/value heads
     const long long rows = BH * a.N;
@@ -619,7 +656,7 @@ int launch_bwd_d(const BackwardLaunch &a, cudaStream_t stream) {
     if ((e = cudaFuncSetAttribute(bwd_dkdv_kernel<D, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   L::kSmemBytes)) != cudaSuccess ||
         (e = cudaFuncSetAttribute(bwd_dq_kernel<D, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  L::kSmemBytes)) != cudaSuccess)
+                                  DqLayout<D>::kSmemBytes)) != cudaSuccess)
         return cuda_fail(e);
     void *ws = nullptr;
     if ((e = scratch_alloc(&ws, static_cast<size_t>(rows) * 2 * sizeof(float), stream)) != cudaSuccess) {
@@ -653,7 +690,8 @@ int launch_bwd_d(const BackwardLaunch &a, cudaStream_t stream) {
     if (e == cudaSuccess) {
         p.g0 = a.dq;
         p.g1 = nullptr;
-        bwd_dq_kernel<D, BF16><<<static_cast<unsigned>(BH * p.n_t), kBwdThreads, L::kSmemBytes, stream>>>(
+        bwd_dq_kernel<D, BF16><<<static_cast<unsigned>(BH * p.n_t), kBwdThreads, DqLayout<D>::kSmemBytes,
+                                 stream>>>(
             mq, mk, mv, mdo, p);
         e = cudaGetLastError();
     }
