@@ -52,12 +52,16 @@ struct BwdLayout {
     static constexpr int kStageBytes = 2 * kTileBytes;
     static constexpr int kVecOff = kRingOff + kStages * kStageBytes;  // [8 warps][2 buf][2][64] floats
     static constexpr int kBarOff = kVecOff + kBwdEltWarps * 2 * 2 * 64 * 4;
-    // fix_full, s_full, p_ready, acc_done, drain, s_loaded, ring_full[S], ring_empty[S]
-    static constexpr int kNumBars = 6 + 2 * kStages;
+    // fix_full, s_full, p_ready, acc_done, drain, s_loaded, ring_full[S], ring_empty[S], pd_done
+    static constexpr int kNumBars = 7 + 2 * kStages;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
     static constexpr int kSmemBytes = kMiscOff + 16 + 1024;
-    // TMEM: X (S^T) | Y (dP^T) | accumulator A (dV) | accumulator B (dK)
+    // TMEM: X (S^T) | Y (dP^T) | accumulator A (dV) | accumulator B (dK).  At
+    // d = 64 that leaves columns 384-511, where P^T and dS^T get 64 columns each;
+    // at d = 128 they are written over S^T and dP^T.
     static constexpr uint32_t kXCol = 0, kYCol = 128, kACol = 256, kBCol = 256 + D;
+    static constexpr bool kOwnPds = D == 64;
+    static constexpr uint32_t kPCol = kOwnPds ? 384 : kXCol, kDsCol = kOwnPds ? 448 : kYCol;
 };
 
 // The dQ kernel's shared memory: Q_i and dO_i loaded once, then K_j and V_j
@@ -181,6 +185,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     uint64_t *fix_full = bars + 0, *s_full = bars + 1, *p_ready = bars + 2, *acc_done = bars + 3;
     uint64_t *drain = bars + 4, *s_loaded = bars + 5;
     uint64_t *ring_full = bars + 6, *ring_empty = bars + 6 + L::kStages;
+    uint64_t *pd_done = bars + 6 + 2 * L::kStages;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kMiscOff);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kMiscOff + 4);
     float *vec = reinterpret_cast<float *>(smem + L::kVecOff);
@@ -200,6 +205,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_init(acc_done, 1);
         mbar_init(drain, 1);
         mbar_init(s_loaded, kBwdEltWarps);
+        mbar_init(pd_done, 1);
         for (int s = 0; s < L::kStages; ++s) {
             mbar_init(ring_full + s, 1);
             mbar_init(ring_empty + s, 1);
@@ -268,29 +274,53 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             const uint64_t k_desc = sdesc_sw128(fix, 16, 1024);
             const uint64_t v_desc = sdesc_sw128(fix + L::kTileBytes, 16, 1024);
             bool ok = mbar_wait(fix_full, 0, abort_flag, kWatchdogNs);
-            for (int n = 0; n < n_iter && ok; ++n) {
-                const int slot = n % L::kStages;
-                if (!mbar_wait(ring_full + slot, (n / L::kStages) & 1, abort_flag, kWatchdogNs)) {
-                    ok = false;
-                    break;
-                }
+            // S^T = K Q_i^T and dP^T = V dO_i^T (keys on TMEM lanes) for ring item j
+            auto issue_scores = [&](int j) {
+                const int slot = j % L::kStages;
+                if (!mbar_wait(ring_full + slot, (j / L::kStages) & 1, abort_flag, kWatchdogNs)) return false;
                 tc_fence_after();
                 const uint32_t st = ring + slot * L::kStageBytes;
-                // S^T = K Q_i^T and dP^T = V dO_i^T (keys on TMEM lanes)
                 issue_qk<D>(tmem + L::kXCol, k_desc, sdesc_sw128(st, 16, 1024), idesc_s);
                 issue_qk<D>(tmem + L::kYCol, v_desc, sdesc_sw128(st + L::kTileBytes, 16, 1024), idesc_s);
                 umma_commit(s_full);
+                return true;
+            };
+            if (ok && L::kOwnPds) ok = issue_scores(0);
+            for (int n = 0; n < n_iter && ok; ++n) {
+                if constexpr (L::kOwnPds) {
+                    // P^T and dS^T have columns of their own: once every elementwise warp
+                    // holds this item's scores, the next item's products may start.
+                    if (n + 1 < n_iter) {
+                        if (!mbar_wait(s_loaded, n & 1, abort_flag, kWatchdogNs)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        if (!issue_scores(n + 1)) {
+                            ok = false;
+                            break;
+                        }
+                    }
+                } else {
+                    if (!issue_scores(n)) {
+                        ok = false;
+                        break;
+                    }
+                }
                 if (!mbar_wait(p_ready, n & 1, abort_flag, kWatchdogNs)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 // dV += P^T dO_i and dK += dS^T Q_i (P^T, dS^T from TMEM; dO_i, Q_i MN-major)
-                issue_pv<D>(tmem + L::kACol, tmem + L::kXCol,
+                const int slot = n % L::kStages;
+                const uint32_t st = ring + slot * L::kStageBytes;
+                issue_pv<D>(tmem + L::kACol, tmem + L::kPCol,
                             sdesc_sw128(st + L::kTileBytes, kSlabBytes, 1024), idesc_acc, n > 0);
-                issue_pv<D>(tmem + L::kBCol, tmem + L::kYCol, sdesc_sw128(st, kSlabBytes, 1024), idesc_acc,
+                issue_pv<D>(tmem + L::kBCol, tmem + L::kDsCol, sdesc_sw128(st, kSlabBytes, 1024), idesc_acc,
                             n > 0);
                 umma_commit(ring_empty + slot);
+                if constexpr (L::kOwnPds) umma_commit(pd_done);
             }
             umma_commit(acc_done);
             umma_commit(drain);
@@ -333,13 +363,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 reg_fence32(sr[h]);
                 reg_fence32(dr[h]);
             }
-            // P^T and dS^T of the upper half land on columns the lower half reads:
-            // every warp's loads complete before any warp stores
+            // At d = 128 P^T and dS^T of the upper half land on columns the lower
+            // half reads: every warp's loads complete before any warp stores.  At
+            // d = 64 the arrival tells the MMA thread the score columns are free.
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(s_loaded);
-            if (!warp_wait(s_loaded, n & 1, abort_flag)) { ok = false; break; }
-            tc_fence_after();
+            if constexpr (!L::kOwnPds) {
+                if (!warp_wait(s_loaded, n & 1, abort_flag)) { ok = false; break; }
+                tc_fence_after();
+            }
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 const int q = 2 * hf + h;
@@ -355,9 +388,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 uint32_t pk[16], dk[16];
                 weights_quarter<BF16, true>(sr[h], dr[h], pk, dk, p.c, vb + h * 32, vb + 64 + h * 32, 0.f, 0.f,
                                             vis);
-                tmem_st16(tmem + lane_off + L::kXCol + q * 16, pk);   // P^T over S^T
-                tmem_st16(tmem + lane_off + L::kYCol + q * 16, dk);   // dS^T over dP^T
+                if constexpr (L::kOwnPds) {
+                    if (h == 0 && n > 0) {
+                        // the previous item's P^T and dS^T must have been read.  This
+                        // also keeps p_ready from completing twice before the MMA
+                        // thread, which committed pd_done after seeing it, looks.
+                        if (!warp_wait(pd_done, (n - 1) & 1, abort_flag)) { ok = false; break; }
+                        tc_fence_after();
+                    }
+                }
+                tmem_st16(tmem + lane_off + L::kPCol + q * 16, pk);
+                tmem_st16(tmem + lane_off + L::kDsCol + q * 16, dk);
             }
+            if (!ok) break;
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();

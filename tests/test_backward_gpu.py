@@ -110,10 +110,12 @@ def test_grouped_head_gradients_match_oracle(fa, oracle_mod, shape, hkv, dtype, 
         assert e <= REL_TOL[dtype], f"{name} {shape}/{hkv} {dtype} causal={causal}: {e:.3e}"
 
 
-def test_gradients_are_bit_identical_run_to_run(fa):
+@pytest.mark.parametrize("shape,dtype,hkv", [((2, 4, 1000, 128), "bf16", None), ((2, 6, 1000, 64), "f16", 2)])
+def test_gradients_are_bit_identical_run_to_run(fa, shape, dtype, hkv):
+    # d = 64 runs the dK/dV pipeline whose score products overlap the elementwise work
     import torch
-    a = run(fa, (2, 4, 1000, 128), "bf16", True, 3300, grad="bf16")[3]
-    b = run(fa, (2, 4, 1000, 128), "bf16", True, 3300, grad="bf16")[3]
+    a = run(fa, shape, dtype, True, 3300, grad=dtype, hkv=hkv)[3]
+    b = run(fa, shape, dtype, True, 3300, grad=dtype, hkv=hkv)[3]
     for x, y in zip(a, b):
         assert torch.equal(x.view(torch.int16), y.view(torch.int16))
 
