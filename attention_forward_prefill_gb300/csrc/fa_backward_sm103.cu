@@ -48,12 +48,14 @@ struct BwdLayout {
     static constexpr int kTileBytes = kChunks * kSlabBytes;  // 128 rows x D 16-bit
     static constexpr int kStages = (D == 128) ? 2 : 3;
     static constexpr int kFixOff = 0;                       // two tiles loaded once per CTA
-    static constexpr int kRingOff = 2 * kTileBytes;         // stages of two tiles each
-    static constexpr int kStageBytes = 2 * kTileBytes;
-    static constexpr int kVecOff = kRingOff + kStages * kStageBytes;  // [8 warps][2 buf][2][64] floats
-    static constexpr int kBarOff = kVecOff + kBwdEltWarps * 2 * 2 * 64 * 4;
-    // fix_full, s_full, p_ready, acc_done, drain, s_loaded, ring_full[S], ring_empty[S], pd_done
-    static constexpr int kNumBars = 7 + 2 * kStages;
+    static constexpr int kRingOff = 2 * kTileBytes;         // stages of Q_i, dO_i and the vectors
+    // L2 and D of the stage's 128 queries (two 512-byte bulk copies) after its tiles
+    static constexpr int kVecInStage = 2 * kTileBytes;
+    static constexpr int kStageBytes = 2 * kTileBytes + 2 * kRows * 4;
+    static constexpr int kBarOff = kRingOff + kStages * kStageBytes;
+    // fix_full, s_full, p_ready, acc_done, drain, s_loaded, ring_full[S], ring_empty[S], pd_done,
+    // dp_full, dp_loaded, ds_ready
+    static constexpr int kNumBars = 10 + 2 * kStages;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
     static constexpr int kSmemBytes = kMiscOff + 16 + 1024;
     // TMEM: X (S^T) | Y (dP^T) | accumulator A (dV) | accumulator B (dK).  At
@@ -87,13 +89,14 @@ struct DqLayout {
 };
 
 struct BwdParams {
-    const float *lse2;  // [B Hq][N] row log-sum-exp in log2 units
-    const float *dsum;  // [B Hq][N] D_i = dO_i . O_i
+    const float *lse2;  // [B Hq][npad] row log-sum-exp in log2 units
+    const float *dsum;  // [B Hq][npad] D_i = dO_i . O_i
     void *g0;           // dkdv: dK [B Hkv][N][d]; dq: dQ [B Hq][N][d]
     void *g1;           // dkdv: dV [B Hkv][N][d]
     int Hq, Hkv, group; // query head h reads key/value head h / group
     int N;
     int n_t;            // 128-row tiles per head
+    int npad;           // n_t * 128: row stride of lse2 and dsum per head (zero past N)
     int causal;
     int grad_dtype;
     float scale;
@@ -101,12 +104,23 @@ struct BwdParams {
 };
 
 // ---------------------------------------------------------------- D and L2
+// One warp per row of the padded [B Hq][npad] layout; rows past N get zeros, so
+// that every 128-row tile of it can be copied whole.
 __global__ void __launch_bounds__(256) bwd_prep_kernel(const uint16_t *o, const uint16_t *dout,
                                                        const float *lse, float *lse2, float *dsum,
-                                                       long long rows, int d, int bf16) {
-    const long long row = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+                                                       long long rows_pad, int N, int npad, int d, int bf16) {
+    const long long prow = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
-    if (row >= rows) return;
+    if (prow >= rows_pad) return;
+    const long long i = prow % npad;
+    if (i >= N) {
+        if (lane == 0) {
+            dsum[prow] = 0.f;
+            lse2[prow] = 0.f;
+        }
+        return;
+    }
+    const long long row = (prow / npad) * N + i;
     float acc = 0.f;
     for (int c = lane * 2; c < d; c += 64) {
         const uint32_t a = *reinterpret_cast<const uint32_t *>(o + row * d + c);
@@ -126,8 +140,8 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const uint16_t *o, const 
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
     if (lane == 0) {
-        dsum[row] = acc;
-        lse2[row] = lse[row] * 1.4426950408889634f;
+        dsum[prow] = acc;
+        lse2[prow] = lse[row] * 1.4426950408889634f;
     }
 }
 
@@ -171,6 +185,53 @@ __device__ __forceinline__ void weights_quarter(const uint32_t (&sr)[32], const 
                                                  vis_mask);
 }
 
+// The same work in two steps, for a pipeline that multiplies P^T before dS^T is
+// known.  First the weights of a quarter: sr holds the scores on entry and the
+// fp32 weights on return, pk the packed 16-bit weights.
+template <bool BF16, bool MASKED>
+__device__ __forceinline__ void p_quarter_impl(uint32_t (&sr)[32], uint32_t (&pk)[16], float c,
+                                               const float *lse2_col, uint32_t vis_mask) {
+#pragma unroll
+    for (int e2 = 0; e2 < 16; ++e2) {
+        float pp[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int col = 2 * e2 + h;
+            float p = ex2_approx(__uint_as_float(sr[col]) * c - lse2_col[col]);
+            if (MASKED) p = ((vis_mask >> col) & 1u) ? p : 0.f;
+            pp[h] = p;
+            sr[col] = __float_as_uint(p);
+        }
+        pk[e2] = pack2t<BF16>(pp[0], pp[1]);
+    }
+}
+
+template <bool BF16>
+__device__ __forceinline__ void p_quarter(uint32_t (&sr)[32], uint32_t (&pk)[16], float c, const float *lse2_col,
+                                          uint32_t vis_mask) {
+    if (vis_mask == 0xffffffffu)
+        p_quarter_impl<BF16, false>(sr, pk, c, lse2_col, vis_mask);
+    else
+        p_quarter_impl<BF16, true>(sr, pk, c, lse2_col, vis_mask);
+}
+
+// Then dS = P (dP - D) of the quarter from the kept weights (exactly the
+// arithmetic of weights_quarter, so the two pipelines give the same bits).
+template <bool BF16>
+__device__ __forceinline__ void ds_quarter(const uint32_t (&pr)[32], const uint32_t (&dr)[32], uint32_t (&dk)[16],
+                                           const float *dsum_col) {
+#pragma unroll
+    for (int e2 = 0; e2 < 16; ++e2) {
+        float dd[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int col = 2 * e2 + h;
+            dd[h] = __uint_as_float(pr[col]) * (__uint_as_float(dr[col]) - dsum_col[col]);
+        }
+        dk[e2] = pack2t<BF16>(dd[0], dd[1]);
+    }
+}
+
 // ---------------------------------------------------------------- dK, dV
 template <int D, bool BF16>
 __global__ void __launch_bounds__(kBwdThreads, 1)
@@ -186,9 +247,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     uint64_t *drain = bars + 4, *s_loaded = bars + 5;
     uint64_t *ring_full = bars + 6, *ring_empty = bars + 6 + L::kStages;
     uint64_t *pd_done = bars + 6 + 2 * L::kStages;
+    // d = 128: dP^T ready, every warp's dP^T loaded, dS^T ready
+    uint64_t *dp_full = pd_done + 1, *dp_loaded = pd_done + 2, *ds_ready = pd_done + 3;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kMiscOff);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kMiscOff + 4);
-    float *vec = reinterpret_cast<float *>(smem + L::kVecOff);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int bhk = blockIdx.x / p.n_t;        // (batch, key/value head)
@@ -206,6 +268,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_init(drain, 1);
         mbar_init(s_loaded, kBwdEltWarps);
         mbar_init(pd_done, 1);
+        mbar_init(dp_full, 1);
+        mbar_init(dp_loaded, kBwdEltWarps);
+        mbar_init(ds_ready, kBwdEltWarps);
         for (int s = 0; s < L::kStages; ++s) {
             mbar_init(ring_full + s, 1);
             mbar_init(ring_empty + s, 1);
@@ -250,12 +315,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 const int row = (i_first + n % n_qt) * kRows;
                 const int bhq = bhq0 + n / n_qt;
                 uint8_t *st = ring + slot * L::kStageBytes;
-                mbar_arrive_expect_tx(ring_full + slot, 2 * L::kTileBytes);
+                mbar_arrive_expect_tx(ring_full + slot, 2 * L::kTileBytes + 2 * kRows * 4);
                 for (int c = 0; c < L::kChunks; ++c) {
                     tma_load_3d(st + c * kSlabBytes, &map_q, ring_full + slot, c * 64, row, bhq, pol);
                     tma_load_3d(st + L::kTileBytes + c * kSlabBytes, &map_do, ring_full + slot, c * 64, row,
                                 bhq, pol);
                 }
+                // the 128 queries' L2 and D (the padded layout keeps both copies whole)
+                const size_t vrow = static_cast<size_t>(bhq) * p.npad + row;
+                bulk_load(st + L::kVecInStage, p.lse2 + vrow, kRows * 4, ring_full + slot);
+                bulk_load(st + L::kVecInStage + kRows * 4, p.dsum + vrow, kRows * 4, ring_full + slot);
             }
             if (!ok) {  // let every copy already issued land
                 constexpr uint64_t kDrainNs = 200ull * 1000ull * 1000ull;
@@ -285,24 +354,54 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 umma_commit(s_full);
                 return true;
             };
-            if (ok && L::kOwnPds) ok = issue_scores(0);
-            for (int n = 0; n < n_iter && ok; ++n) {
-                if constexpr (L::kOwnPds) {
-                    // P^T and dS^T have columns of their own: once every elementwise warp
-                    // holds this item's scores, the next item's products may start.
-                    if (n + 1 < n_iter) {
-                        if (!mbar_wait(s_loaded, n & 1, abort_flag, kWatchdogNs)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                        if (!issue_scores(n + 1)) {
-                            ok = false;
-                            break;
-                        }
+            if constexpr (!L::kOwnPds) {
+                // d = 128: P^T and dS^T are written over S^T and dP^T, in two steps.
+                // dP^T runs while the weights are computed, dV += P^T dO_i while dS^T is.
+                auto issue_item = [&](int j) {
+                    const int slot = j % L::kStages;
+                    if (!mbar_wait(ring_full + slot, (j / L::kStages) & 1, abort_flag, kWatchdogNs)) return false;
+                    tc_fence_after();
+                    const uint32_t st = ring + slot * L::kStageBytes;
+                    issue_qk<D>(tmem + L::kXCol, k_desc, sdesc_sw128(st, 16, 1024), idesc_s);
+                    umma_commit(s_full);
+                    issue_qk<D>(tmem + L::kYCol, v_desc, sdesc_sw128(st + L::kTileBytes, 16, 1024), idesc_s);
+                    umma_commit(dp_full);
+                    return true;
+                };
+                if (ok) ok = issue_item(0);
+                for (int n = 0; n < n_iter && ok; ++n) {
+                    const int slot = n % L::kStages;
+                    const uint32_t st = ring + slot * L::kStageBytes;
+                    if (!mbar_wait(p_ready, n & 1, abort_flag, kWatchdogNs)) {
+                        ok = false;
+                        break;
                     }
-                } else {
-                    if (!issue_scores(n)) {
+                    tc_fence_after();
+                    issue_pv<D>(tmem + L::kACol, tmem + L::kPCol,
+                                sdesc_sw128(st + L::kTileBytes, kSlabBytes, 1024), idesc_acc, n > 0);
+                    if (!mbar_wait(ds_ready, n & 1, abort_flag, kWatchdogNs)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    issue_pv<D>(tmem + L::kBCol, tmem + L::kDsCol, sdesc_sw128(st, kSlabBytes, 1024), idesc_acc,
+                                n > 0);
+                    umma_commit(ring_empty + slot);
+                    // the next item's products follow the ones that read its columns
+                    if (n + 1 < n_iter && !issue_item(n + 1)) ok = false;
+                }
+            }
+            if (ok && L::kOwnPds) ok = issue_scores(0);
+            for (int n = 0; n < n_iter && ok && L::kOwnPds; ++n) {
+                // P^T and dS^T have columns of their own: once every elementwise warp
+                // holds this item's scores, the next item's products may start.
+                if (n + 1 < n_iter) {
+                    if (!mbar_wait(s_loaded, n & 1, abort_flag, kWatchdogNs)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    if (!issue_scores(n + 1)) {
                         ok = false;
                         break;
                     }
@@ -320,7 +419,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 issue_pv<D>(tmem + L::kBCol, tmem + L::kDsCol, sdesc_sw128(st, kSlabBytes, 1024), idesc_acc,
                             n > 0);
                 umma_commit(ring_empty + slot);
-                if constexpr (L::kOwnPds) umma_commit(pd_done);
+                umma_commit(pd_done);
             }
             umma_commit(acc_done);
             umma_commit(drain);
@@ -337,58 +436,48 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         bool ok = true;
         for (int n = 0; n < n_iter && ok; ++n) {
             const int q0 = (i_first + n % n_qt) * kRows;
-            const size_t hrow = static_cast<size_t>(bhq0 + n / n_qt) * p.N;
-            const float *lse2_h = p.lse2 + hrow;
-            const float *dsum_h = p.dsum + hrow;
-            // this half's 64 query columns: L2 and D, staged per warp (double-buffered)
-            float *vb = vec + (warp * 2 + (n & 1)) * 2 * 64;
-            const int c0 = q0 + hf * 64;
-#pragma unroll
-            for (int x = lane; x < 64; x += 32) {
-                vb[x] = c0 + x < p.N ? lse2_h[c0 + x] : 0.f;
-                vb[64 + x] = c0 + x < p.N ? dsum_h[c0 + x] : 0.f;
-            }
-            __syncwarp();
+            // this half's 64 query columns: L2 and D, brought into the ring stage with
+            // Q_i and dO_i (the MMA thread waited for the same barrier; so do we)
+            const int slot = n % L::kStages;
+            if (!warp_wait(ring_full + slot, (n / L::kStages) & 1, abort_flag)) { ok = false; break; }
+            const float *vstage = reinterpret_cast<const float *>(smem + L::kRingOff + slot * L::kStageBytes +
+                                                                  L::kVecInStage);
+            const float *lse2_v = vstage + hf * 64, *dsum_v = vstage + kRows + hf * 64;
             if (!warp_wait(s_full, n & 1, abort_flag)) { ok = false; break; }
             tc_fence_after();
-            uint32_t sr[2][32], dr[2][32];
+            if constexpr (L::kOwnPds) {
+                // d = 64: P^T and dS^T have columns of their own
+                uint32_t sr[2][32], dr[2][32];
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                tmem_ld32(tmem + lane_off + L::kXCol + (2 * hf + h) * 32, sr[h]);
-                tmem_ld32(tmem + lane_off + L::kYCol + (2 * hf + h) * 32, dr[h]);
-            }
-            tmem_ld_wait();
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                reg_fence32(sr[h]);
-                reg_fence32(dr[h]);
-            }
-            // At d = 128 P^T and dS^T of the upper half land on columns the lower
-            // half reads: every warp's loads complete before any warp stores.  At
-            // d = 64 the arrival tells the MMA thread the score columns are free.
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(s_loaded);
-            if constexpr (!L::kOwnPds) {
-                if (!warp_wait(s_loaded, n & 1, abort_flag)) { ok = false; break; }
-                tc_fence_after();
-            }
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int q = 2 * hf + h;
-                // column col is query q0 + 32 q + col; it sees the key when it exists
-                // and, causally, when key <= query
-                const int qb = q0 + q * 32;
-                uint32_t vis = 0xffffffffu;
-                if (qb + 32 > p.N) vis = p.N > qb ? (0xffffffffu >> (32 - (p.N - qb))) : 0u;
-                if (p.causal) {
-                    const int lo = key - qb;  // first visible column
-                    vis &= lo <= 0 ? 0xffffffffu : (lo >= 32 ? 0u : (0xffffffffu << lo));
+                for (int h = 0; h < 2; ++h) {
+                    tmem_ld32(tmem + lane_off + L::kXCol + (2 * hf + h) * 32, sr[h]);
+                    tmem_ld32(tmem + lane_off + L::kYCol + (2 * hf + h) * 32, dr[h]);
                 }
-                uint32_t pk[16], dk[16];
-                weights_quarter<BF16, true>(sr[h], dr[h], pk, dk, p.c, vb + h * 32, vb + 64 + h * 32, 0.f, 0.f,
-                                            vis);
-                if constexpr (L::kOwnPds) {
+                tmem_ld_wait();
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    reg_fence32(sr[h]);
+                    reg_fence32(dr[h]);
+                }
+                // The arrival tells the MMA thread the score columns are free.
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(s_loaded);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int q = 2 * hf + h;
+                    // column col is query q0 + 32 q + col; it sees the key when it exists
+                    // and, causally, when key <= query
+                    const int qb = q0 + q * 32;
+                    uint32_t vis = 0xffffffffu;
+                    if (qb + 32 > p.N) vis = p.N > qb ? (0xffffffffu >> (32 - (p.N - qb))) : 0u;
+                    if (p.causal) {
+                        const int lo = key - qb;  // first visible column
+                        vis &= lo <= 0 ? 0xffffffffu : (lo >= 32 ? 0u : (0xffffffffu << lo));
+                    }
+                    uint32_t pk[16], dk[16];
+                    weights_quarter<BF16, true>(sr[h], dr[h], pk, dk, p.c, lse2_v + h * 32, dsum_v + h * 32, 0.f, 0.f,
+                                                vis);
                     if (h == 0 && n > 0) {
                         // the previous item's P^T and dS^T must have been read.  This
                         // also keeps p_ready from completing twice before the MMA
@@ -396,15 +485,73 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         if (!warp_wait(pd_done, (n - 1) & 1, abort_flag)) { ok = false; break; }
                         tc_fence_after();
                     }
+                    tmem_st16(tmem + lane_off + L::kPCol + q * 16, pk);
+                    tmem_st16(tmem + lane_off + L::kDsCol + q * 16, dk);
                 }
-                tmem_st16(tmem + lane_off + L::kPCol + q * 16, pk);
-                tmem_st16(tmem + lane_off + L::kDsCol + q * 16, dk);
+                if (!ok) break;
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(p_ready);
+            } else {
+                // d = 128 in two steps.  First P^T from S^T, over S^T: the upper
+                // half's P^T lands on columns the lower half reads, so every warp's
+                // loads complete before any warp stores.
+                uint32_t sr[2][32], dr[2][32];
+#pragma unroll
+                for (int h = 0; h < 2; ++h) tmem_ld32(tmem + lane_off + L::kXCol + (2 * hf + h) * 32, sr[h]);
+                tmem_ld_wait();
+#pragma unroll
+                for (int h = 0; h < 2; ++h) reg_fence32(sr[h]);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(s_loaded);
+                if (!warp_wait(s_loaded, n & 1, abort_flag)) { ok = false; break; }
+                tc_fence_after();
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int q = 2 * hf + h;
+                    // column col is query q0 + 32 q + col; it sees the key when it
+                    // exists and, causally, when key <= query
+                    const int qb = q0 + q * 32;
+                    uint32_t vis = 0xffffffffu;
+                    if (qb + 32 > p.N) vis = p.N > qb ? (0xffffffffu >> (32 - (p.N - qb))) : 0u;
+                    if (p.causal) {
+                        const int lo = key - qb;  // first visible column
+                        vis &= lo <= 0 ? 0xffffffffu : (lo >= 32 ? 0u : (0xffffffffu << lo));
+                    }
+                    uint32_t pk[16];
+                    p_quarter<BF16>(sr[h], pk, p.c, lse2_v + h * 32, vis);
+                    tmem_st16(tmem + lane_off + L::kPCol + q * 16, pk);
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(p_ready);
+                // Then dS^T = P^T (dP^T - D) over dP^T, the same way.
+                if (!warp_wait(dp_full, n & 1, abort_flag)) { ok = false; break; }
+                tc_fence_after();
+#pragma unroll
+                for (int h = 0; h < 2; ++h) tmem_ld32(tmem + lane_off + L::kYCol + (2 * hf + h) * 32, dr[h]);
+                tmem_ld_wait();
+#pragma unroll
+                for (int h = 0; h < 2; ++h) reg_fence32(dr[h]);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(dp_loaded);
+                if (!warp_wait(dp_loaded, n & 1, abort_flag)) { ok = false; break; }
+                tc_fence_after();
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    uint32_t dk[16];
+                    ds_quarter<BF16>(sr[h], dr[h], dk, dsum_v + h * 32);
+                    tmem_st16(tmem + lane_off + L::kDsCol + (2 * hf + h) * 16, dk);
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(ds_ready);
             }
-            if (!ok) break;
-            tmem_st_wait();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(p_ready);
         }
         if (ok && warp_wait(acc_done, 0, abort_flag)) {
             // the lower half stores dV, the upper half dK
@@ -600,9 +747,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int r = wq * 32 + lane;
         const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
         const int qrow = it * kRows + r;
+        // the vectors are padded to whole tiles per head; dQ rows are not
+        const size_t vi = static_cast<size_t>(bh) * p.npad + qrow;
         const size_t li = static_cast<size_t>(bh) * p.N + qrow;
-        const float lse2_r = qrow < p.N ? p.lse2[li] : 0.f;
-        const float dsum_r = qrow < p.N ? p.dsum[li] : 0.f;
+        const float lse2_r = qrow < p.N ? p.lse2[vi] : 0.f;
+        const float dsum_r = qrow < p.N ? p.dsum[vi] : 0.f;
         bool ok = true;
         for (int n = 0; n < n_iter && ok; ++n) {
             if (!warp_wait(s_full, n & 1, abort_flag)) { ok = false; break; }
@@ -688,7 +837,8 @@ int launch_bwd_d(const BackwardLaunch &a, cudaStream_t stream) {
                   "shared memory budget");
     const long long BH = static_cast<long long>(a.B) * a.H;      // query heads
     const long long BHk = static_cast<long long>(a.B) * a.Hkv;   // key/value heads
-    const long long rows = BH * a.N;
+    const int n_t = (a.N + kRows - 1) / kRows;
+    const long long rows_pad = BH * n_t * kRows;  // lse2 and dsum, padded to whole tiles
     CUtensorMap mq, mk, mv, mdo;
     int rc;
     if ((rc = make_map(&mq, a.q, D, false, a.N, BH, a.in_bf16)) != FA_OK) return rc;
@@ -702,14 +852,14 @@ int launch_bwd_d(const BackwardLaunch &a, cudaStream_t stream) {
                                   DqLayout<D>::kSmemBytes)) != cudaSuccess)
         return cuda_fail(e);
     void *ws = nullptr;
-    if ((e = scratch_alloc(&ws, static_cast<size_t>(rows) * 2 * sizeof(float), stream)) != cudaSuccess) {
+    if ((e = scratch_alloc(&ws, static_cast<size_t>(rows_pad) * 2 * sizeof(float), stream)) != cudaSuccess) {
         cuda_fail(e);
         return FA_ERR_WORKSPACE;
     }
-    float *lse2 = static_cast<float *>(ws), *dsum = lse2 + rows;
-    bwd_prep_kernel<<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(
-        static_cast<const uint16_t *>(a.out), static_cast<const uint16_t *>(a.dout), a.lse, lse2, dsum, rows,
-        D, a.in_bf16);
+    float *lse2 = static_cast<float *>(ws), *dsum = lse2 + rows_pad;
+    bwd_prep_kernel<<<static_cast<unsigned>((rows_pad + 7) / 8), 256, 0, stream>>>(
+        static_cast<const uint16_t *>(a.out), static_cast<const uint16_t *>(a.dout), a.lse, lse2, dsum, rows_pad,
+        a.N, n_t * kRows, D, a.in_bf16);
     e = cudaGetLastError();
     BwdParams p;
     p.lse2 = lse2;
@@ -718,7 +868,8 @@ int launch_bwd_d(const BackwardLaunch &a, cudaStream_t stream) {
     p.Hkv = a.Hkv;
     p.group = a.H / a.Hkv;
     p.N = a.N;
-    p.n_t = (a.N + kRows - 1) / kRows;
+    p.n_t = n_t;
+    p.npad = n_t * kRows;
     p.causal = a.causal ? 1 : 0;
     p.grad_dtype = a.grad_dtype;
     p.scale = a.scale;
