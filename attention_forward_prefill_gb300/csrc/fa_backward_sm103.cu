@@ -357,18 +357,27 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             if constexpr (!L::kOwnPds) {
                 // d = 128: P^T and dS^T are written over S^T and dP^T, in two steps.
                 // dP^T runs while the weights are computed, dV += P^T dO_i while dS^T is.
-                auto issue_item = [&](int j) {
-                    const int slot = j % L::kStages;
-                    if (!mbar_wait(ring_full + slot, (j / L::kStages) & 1, abort_flag, kWatchdogNs)) return false;
-                    tc_fence_after();
-                    const uint32_t st = ring + slot * L::kStageBytes;
+                // S^T of item j (Q_j from its stage) and dP^T (dO_j)
+                auto issue_s = [&](int j) {
+                    const uint32_t st = ring + (j % L::kStages) * L::kStageBytes;
                     issue_qk<D>(tmem + L::kXCol, k_desc, sdesc_sw128(st, 16, 1024), idesc_s);
                     umma_commit(s_full);
+                };
+                auto issue_dp = [&](int j) {
+                    const uint32_t st = ring + (j % L::kStages) * L::kStageBytes;
                     issue_qk<D>(tmem + L::kYCol, v_desc, sdesc_sw128(st + L::kTileBytes, 16, 1024), idesc_s);
                     umma_commit(dp_full);
+                };
+                auto stage_ready = [&](int j) {
+                    if (!mbar_wait(ring_full + j % L::kStages, (j / L::kStages) & 1, abort_flag, kWatchdogNs))
+                        return false;
+                    tc_fence_after();
                     return true;
                 };
-                if (ok) ok = issue_item(0);
+                if (ok && (ok = stage_ready(0))) {
+                    issue_s(0);
+                    issue_dp(0);
+                }
                 for (int n = 0; n < n_iter && ok; ++n) {
                     const int slot = n % L::kStages;
                     const uint32_t st = ring + slot * L::kStageBytes;
@@ -379,6 +388,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     tc_fence_after();
                     issue_pv<D>(tmem + L::kACol, tmem + L::kPCol,
                                 sdesc_sw128(st + L::kTileBytes, kSlabBytes, 1024), idesc_acc, n > 0);
+                    // S^T of the next item may overwrite P^T once dV has been issued (the
+                    // products run in order); take it now if its Q tile has landed, so it
+                    // runs under the dS^T step, else after dK.
+                    const int nx = n + 1;
+                    bool s_issued = false;
+                    if (nx < n_iter && mbar_test_wait(ring_full + nx % L::kStages, (nx / L::kStages) & 1)) {
+                        tc_fence_after();
+                        issue_s(nx);
+                        s_issued = true;
+                    }
                     if (!mbar_wait(ds_ready, n & 1, abort_flag, kWatchdogNs)) {
                         ok = false;
                         break;
@@ -387,8 +406,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     issue_pv<D>(tmem + L::kBCol, tmem + L::kDsCol, sdesc_sw128(st, kSlabBytes, 1024), idesc_acc,
                                 n > 0);
                     umma_commit(ring_empty + slot);
-                    // the next item's products follow the ones that read its columns
-                    if (n + 1 < n_iter && !issue_item(n + 1)) ok = false;
+                    if (nx < n_iter) {
+                        if (!s_issued) {
+                            if (!stage_ready(nx)) {
+                                ok = false;
+                                break;
+                            }
+                            issue_s(nx);
+                        }
+                        issue_dp(nx);  // over dS^T, after the dK product that reads it
+                    }
                 }
             }
             if (ok && L::kOwnPds) ok = issue_scores(0);
