@@ -495,18 +495,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                         return true;
                     };
                     // Separate-P step: S_t = Q_t K_{j+1}^T as soon as the softmax has
-                    // loaded S_t(j), then O_t (+)= P_t V_j once P_t(j) is written.
-                    auto tile_step_sep = [&](int nt, uint64_t *pf, uint32_t &pc, uint64_t *sfree,
-                                             uint32_t &qk, uint32_t s_t, uint32_t p_t, uint32_t o_t,
-                                             uint64_t q_desc, uint64_t *sf, uint64_t *pvd) {
+                    // loaded S_t(j), then O_t (+)= P_t V_j once P_t(j) is written.  Both
+                    // tiles' Q K^T products go first, so neither tile's next scores wait
+                    // behind the other tile's P.
+                    auto sep_qk = [&](int nt, uint64_t *sfree, uint32_t &qk, uint32_t s_t, uint64_t q_desc,
+                                      uint64_t *sf) {
+                        if (j + 1 >= nt) return true;
+                        if (!mbar_spin(sfree, (qk - 1) & 1, abort_flag, kWatchdogNs)) return false;
+                        tc_fence_after();
+                        issue_qk<D>(s_t, q_desc, k_desc, idesc_qk);
+                        umma_commit(sf);
+                        ++qk;
+                        return true;
+                    };
+                    auto sep_pv = [&](int nt, uint64_t *pf, uint32_t &pc, uint32_t p_t, uint32_t o_t,
+                                      uint64_t *pvd) {
                         if (j >= nt) return true;
-                        if (j + 1 < nt) {
-                            if (!mbar_spin(sfree, (qk - 1) & 1, abort_flag, kWatchdogNs)) return false;
-                            tc_fence_after();
-                            issue_qk<D>(s_t, q_desc, k_desc, idesc_qk);
-                            umma_commit(sf);
-                            ++qk;
-                        }
                         if (!mbar_spin(pf, pc & 1, abort_flag, kWatchdogNs)) return false;
                         ++pc;
                         tc_fence_after();
@@ -515,10 +519,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         return true;
                     };
                     if constexpr (L::kSepP) {
-                        ok = tile_step_sep(n0, p_full + 0, pc0, s_free + 0, qk0, s_tmem0, p_tmem0, o_tmem0,
-                                           q_desc0, s_full + 0, pv_done + 0) &&
-                             tile_step_sep(n1, p_full + 1, pc1, s_free + 1, qk1, s_tmem1, p_tmem1, o_tmem1,
-                                           q_desc1, s_full + 1, pv_done + 1);
+                        ok = sep_qk(n0, s_free + 0, qk0, s_tmem0, q_desc0, s_full + 0) &&
+                             sep_qk(n1, s_free + 1, qk1, s_tmem1, q_desc1, s_full + 1) &&
+                             sep_pv(n0, p_full + 0, pc0, p_tmem0, o_tmem0, pv_done + 0) &&
+                             sep_pv(n1, p_full + 1, pc1, p_tmem1, o_tmem1, pv_done + 1);
                     } else {
                         ok = tile_step(n0, p_full + 0, pc0, s_tmem0, o_tmem0, q_desc0, s_full + 0,
                                        o_done + 0) &&
