@@ -42,8 +42,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 NCU_TRAFFIC = {
     # Measured at N=8192 (ncu --set full, profiles/prefill_kernel_d128_n8192.md);
     # the other lengths are scaled by the bytes the launch must move (linear in N).
-    "prefill": {"src": "fa_prefill_sm103.cu", "src_sha": "180cd4359aa3d0aa",
-                "bytes_per_launch": {"4096": 116.14e6 / 2, "8192": 116.14e6, "16384": 116.14e6 * 2},
+    "prefill": {"src": "fa_prefill_sm103.cu", "src_sha": "5d414b32c8783a0a",
+                "bytes_per_launch": {"4096": 116.25e6 / 2, "8192": 116.25e6, "16384": 116.25e6 * 2},
                 "measured_at": "8192", "scaled": ["4096", "16384"]},
     # B=32, H=14 (profiles/decode_split_b32_h14.md): DRAM bytes of one split-kernel launch
     "decode": {"src": "fa_decode_sm103.cu", "src_sha": "b66f8ad7b76c86db", "bytes_per_launch": 263.9e6},
