@@ -89,8 +89,8 @@ struct DqLayout {
 };
 
 struct BwdParams {
-    const float *lse2;  // [B Hq][npad] row log-sum-exp in log2 units
-    const float *dsum;  // [B Hq][npad] D_i = dO_i . O_i
+    const float *lse2;  // [B Hq][npad] minus the row log-sum-exp in log2 units, -L_i log2 e
+    const float *dsum;  // [B Hq][npad] minus D_i = dO_i . O_i
     void *g0;           // dkdv: dK [B Hkv][N][d]; dq: dQ [B Hq][N][d]
     void *g1;           // dkdv: dV [B Hkv][N][d]
     int Hq, Hkv, group; // query head h reads key/value head h / group
@@ -105,7 +105,8 @@ struct BwdParams {
 
 // ---------------------------------------------------------------- D and L2
 // One warp per row of the padded [B Hq][npad] layout; rows past N get zeros, so
-// that every 128-row tile of it can be copied whole.
+// that every 128-row tile of it can be copied whole.  Both are stored negated,
+// the sign the elementwise work adds them with.
 __global__ void __launch_bounds__(256) bwd_prep_kernel(const uint16_t *o, const uint16_t *dout,
                                                        const float *lse, float *lse2, float *dsum,
                                                        long long rows_pad, int N, int npad, int d, int bf16) {
@@ -140,33 +141,37 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const uint16_t *o, const 
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
     if (lane == 0) {
-        dsum[prow] = acc;
-        lse2[prow] = lse[row] * 1.4426950408889634f;
+        dsum[prow] = -acc;
+        lse2[prow] = -(lse[row] * 1.4426950408889634f);
     }
 }
 
 // Elementwise work on one 32-column quarter of a score tile held in TMEM:
-// returns, for the thread's row, the packed 16-bit weights and dS values.
+// returns, for the thread's row, the packed 16-bit weights and dS values.  The
+// L2 and D values come negated (nl2 = -L2, nd = -D), per column from shared
+// memory or per row, and the arithmetic runs on fp32 pairs:
+//   p = 2^(c s + nl2),  dS = p (dP + nd).
 template <bool BF16, bool WANT_P, bool MASKED>
 __device__ __forceinline__ void weights_quarter_impl(const uint32_t (&sr)[32], const uint32_t (&dr)[32],
                                                      uint32_t (&pk)[16], uint32_t (&dk)[16], float c,
-                                                     const float *lse2_col, const float *dsum_col,
-                                                     float lse2_row, float dsum_row, uint32_t vis_mask) {
+                                                     const float *nl2_col, const float *nd_col,
+                                                     float nl2_row, float nd_row, uint32_t vis_mask) {
+    const uint64_t c2 = f2_pack(c, c);
 #pragma unroll
     for (int e2 = 0; e2 < 16; ++e2) {
-        float pp[2], dd[2];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int col = 2 * e2 + h;
-            const float l2 = lse2_col ? lse2_col[col] : lse2_row;
-            const float dsv = dsum_col ? dsum_col[col] : dsum_row;
-            float p = ex2_approx(__uint_as_float(sr[col]) * c - l2);
-            if (MASKED) p = ((vis_mask >> col) & 1u) ? p : 0.f;
-            pp[h] = p;
-            dd[h] = p * (__uint_as_float(dr[col]) - dsv);
+        const int col = 2 * e2;
+        const uint64_t nl2 = nl2_col ? *reinterpret_cast<const uint64_t *>(nl2_col + col) : f2_pack(nl2_row, nl2_row);
+        const uint64_t nd = nd_col ? *reinterpret_cast<const uint64_t *>(nd_col + col) : f2_pack(nd_row, nd_row);
+        const uint64_t x = ffma2(f2_pack(__uint_as_float(sr[col]), __uint_as_float(sr[col + 1])), c2, nl2);
+        float p0 = ex2_approx(f2_lo(x)), p1 = ex2_approx(f2_hi(x));
+        if (MASKED) {
+            p0 = ((vis_mask >> col) & 1u) ? p0 : 0.f;
+            p1 = ((vis_mask >> (col + 1)) & 1u) ? p1 : 0.f;
         }
-        if (WANT_P) pk[e2] = pack2t<BF16>(pp[0], pp[1]);
-        dk[e2] = pack2t<BF16>(dd[0], dd[1]);
+        const uint64_t dd =
+            fmul2(f2_pack(p0, p1), fadd2(f2_pack(__uint_as_float(dr[col]), __uint_as_float(dr[col + 1])), nd));
+        if (WANT_P) pk[e2] = pack2t<BF16>(p0, p1);
+        dk[e2] = pack2t<BF16>(f2_lo(dd), f2_hi(dd));
     }
 }
 
@@ -175,13 +180,13 @@ __device__ __forceinline__ void weights_quarter_impl(const uint32_t (&sr)[32], c
 template <bool BF16, bool WANT_P>
 __device__ __forceinline__ void weights_quarter(const uint32_t (&sr)[32], const uint32_t (&dr)[32],
                                                 uint32_t (&pk)[16], uint32_t (&dk)[16], float c,
-                                                const float *lse2_col, const float *dsum_col,
-                                                float lse2_row, float dsum_row, uint32_t vis_mask) {
+                                                const float *nl2_col, const float *nd_col,
+                                                float nl2_row, float nd_row, uint32_t vis_mask) {
     if (vis_mask == 0xffffffffu)
-        weights_quarter_impl<BF16, WANT_P, false>(sr, dr, pk, dk, c, lse2_col, dsum_col, lse2_row, dsum_row,
+        weights_quarter_impl<BF16, WANT_P, false>(sr, dr, pk, dk, c, nl2_col, nd_col, nl2_row, nd_row,
                                                   vis_mask);
     else
-        weights_quarter_impl<BF16, WANT_P, true>(sr, dr, pk, dk, c, lse2_col, dsum_col, lse2_row, dsum_row,
+        weights_quarter_impl<BF16, WANT_P, true>(sr, dr, pk, dk, c, nl2_col, nd_col, nl2_row, nd_row,
                                                  vis_mask);
 }
 
@@ -190,45 +195,45 @@ __device__ __forceinline__ void weights_quarter(const uint32_t (&sr)[32], const 
 // fp32 weights on return, pk the packed 16-bit weights.
 template <bool BF16, bool MASKED>
 __device__ __forceinline__ void p_quarter_impl(uint32_t (&sr)[32], uint32_t (&pk)[16], float c,
-                                               const float *lse2_col, uint32_t vis_mask) {
+                                               const float *nl2_col, uint32_t vis_mask) {
+    const uint64_t c2 = f2_pack(c, c);
 #pragma unroll
     for (int e2 = 0; e2 < 16; ++e2) {
-        float pp[2];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int col = 2 * e2 + h;
-            float p = ex2_approx(__uint_as_float(sr[col]) * c - lse2_col[col]);
-            if (MASKED) p = ((vis_mask >> col) & 1u) ? p : 0.f;
-            pp[h] = p;
-            sr[col] = __float_as_uint(p);
+        const int col = 2 * e2;
+        const uint64_t x = ffma2(f2_pack(__uint_as_float(sr[col]), __uint_as_float(sr[col + 1])), c2,
+                                 *reinterpret_cast<const uint64_t *>(nl2_col + col));
+        float p0 = ex2_approx(f2_lo(x)), p1 = ex2_approx(f2_hi(x));
+        if (MASKED) {
+            p0 = ((vis_mask >> col) & 1u) ? p0 : 0.f;
+            p1 = ((vis_mask >> (col + 1)) & 1u) ? p1 : 0.f;
         }
-        pk[e2] = pack2t<BF16>(pp[0], pp[1]);
+        sr[col] = __float_as_uint(p0);
+        sr[col + 1] = __float_as_uint(p1);
+        pk[e2] = pack2t<BF16>(p0, p1);
     }
 }
 
 template <bool BF16>
-__device__ __forceinline__ void p_quarter(uint32_t (&sr)[32], uint32_t (&pk)[16], float c, const float *lse2_col,
+__device__ __forceinline__ void p_quarter(uint32_t (&sr)[32], uint32_t (&pk)[16], float c, const float *nl2_col,
                                           uint32_t vis_mask) {
     if (vis_mask == 0xffffffffu)
-        p_quarter_impl<BF16, false>(sr, pk, c, lse2_col, vis_mask);
+        p_quarter_impl<BF16, false>(sr, pk, c, nl2_col, vis_mask);
     else
-        p_quarter_impl<BF16, true>(sr, pk, c, lse2_col, vis_mask);
+        p_quarter_impl<BF16, true>(sr, pk, c, nl2_col, vis_mask);
 }
 
-// Then dS = P (dP - D) of the quarter from the kept weights (exactly the
-// arithmetic of weights_quarter, so the two pipelines give the same bits).
+// Then dS = P (dP - D) of the quarter from the kept weights (the arithmetic of
+// weights_quarter, so the two pipelines give the same bits).
 template <bool BF16>
 __device__ __forceinline__ void ds_quarter(const uint32_t (&pr)[32], const uint32_t (&dr)[32], uint32_t (&dk)[16],
-                                           const float *dsum_col) {
+                                           const float *nd_col) {
 #pragma unroll
     for (int e2 = 0; e2 < 16; ++e2) {
-        float dd[2];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int col = 2 * e2 + h;
-            dd[h] = __uint_as_float(pr[col]) * (__uint_as_float(dr[col]) - dsum_col[col]);
-        }
-        dk[e2] = pack2t<BF16>(dd[0], dd[1]);
+        const int col = 2 * e2;
+        const uint64_t dd = fmul2(f2_pack(__uint_as_float(pr[col]), __uint_as_float(pr[col + 1])),
+                                  fadd2(f2_pack(__uint_as_float(dr[col]), __uint_as_float(dr[col + 1])),
+                                        *reinterpret_cast<const uint64_t *>(nd_col + col)));
+        dk[e2] = pack2t<BF16>(f2_lo(dd), f2_hi(dd));
     }
 }
 
@@ -469,7 +474,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             if (!warp_wait(ring_full + slot, (n / L::kStages) & 1, abort_flag)) { ok = false; break; }
             const float *vstage = reinterpret_cast<const float *>(smem + L::kRingOff + slot * L::kStageBytes +
                                                                   L::kVecInStage);
-            const float *lse2_v = vstage + hf * 64, *dsum_v = vstage + kRows + hf * 64;
+            const float *nl2_v = vstage + hf * 64, *nd_v = vstage + kRows + hf * 64;
             if (!warp_wait(s_full, n & 1, abort_flag)) { ok = false; break; }
             tc_fence_after();
             if constexpr (L::kOwnPds) {
@@ -503,7 +508,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         vis &= lo <= 0 ? 0xffffffffu : (lo >= 32 ? 0u : (0xffffffffu << lo));
                     }
                     uint32_t pk[16], dk[16];
-                    weights_quarter<BF16, true>(sr[h], dr[h], pk, dk, p.c, lse2_v + h * 32, dsum_v + h * 32, 0.f, 0.f,
+                    weights_quarter<BF16, true>(sr[h], dr[h], pk, dk, p.c, nl2_v + h * 32, nd_v + h * 32, 0.f, 0.f,
                                                 vis);
                     if (h == 0 && n > 0) {
                         // the previous item's P^T and dS^T must have been read.  This
@@ -548,7 +553,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         vis &= lo <= 0 ? 0xffffffffu : (lo >= 32 ? 0u : (0xffffffffu << lo));
                     }
                     uint32_t pk[16];
-                    p_quarter<BF16>(sr[h], pk, p.c, lse2_v + h * 32, vis);
+                    p_quarter<BF16>(sr[h], pk, p.c, nl2_v + h * 32, vis);
                     tmem_st16(tmem + lane_off + L::kPCol + q * 16, pk);
                 }
                 tmem_st_wait();
@@ -571,7 +576,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     uint32_t dk[16];
-                    ds_quarter<BF16>(sr[h], dr[h], dk, dsum_v + h * 32);
+                    ds_quarter<BF16>(sr[h], dr[h], dk, nd_v + h * 32);
                     tmem_st16(tmem + lane_off + L::kDsCol + (2 * hf + h) * 16, dk);
                 }
                 tmem_st_wait();
@@ -777,8 +782,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         // the vectors are padded to whole tiles per head; dQ rows are not
         const size_t vi = static_cast<size_t>(bh) * p.npad + qrow;
         const size_t li = static_cast<size_t>(bh) * p.N + qrow;
-        const float lse2_r = qrow < p.N ? p.lse2[vi] : 0.f;
-        const float dsum_r = qrow < p.N ? p.dsum[vi] : 0.f;
+        const float nl2_r = qrow < p.N ? p.lse2[vi] : 0.f;
+        const float nd_r = qrow < p.N ? p.dsum[vi] : 0.f;
         bool ok = true;
         for (int n = 0; n < n_iter && ok; ++n) {
             if (!warp_wait(s_full, n & 1, abort_flag)) { ok = false; break; }
@@ -813,7 +818,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     vis &= hi < 0 ? 0u : (hi >= 31 ? 0xffffffffu : (0xffffffffu >> (31 - hi)));
                 }
                 uint32_t pk[16], dk[16];
-                weights_quarter<BF16, false>(sr[h], dr[h], pk, dk, p.c, nullptr, nullptr, lse2_r, dsum_r, vis);
+                weights_quarter<BF16, false>(sr[h], dr[h], pk, dk, p.c, nullptr, nullptr, nl2_r, nd_r, vis);
                 if (h == 0 && n > 0) {
                     // dS of tile n - 1 must have been read by its product.  This also
                     // keeps p_ready from completing twice before the MMA thread,
