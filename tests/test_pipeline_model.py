@@ -1,0 +1,397 @@
+"""The barrier protocols of the backward kernels, on the host (no GPU).
+
+Each role of a CTA -- the TMA producer, the MMA-issuing thread and each of the
+eight elementwise warps -- is restated as the sequence of mbarrier waits and
+arrivals, tcgen05 commits, TMA loads, MMAs and tensor-memory accesses it makes,
+in the order of the kernels in fa_backward_sm103.cu.  A scheduler then runs the
+roles under many random interleavings, with the tensor core executing the MMAs
+in issue order (each one reads its operands and writes its result when it
+runs) and TMA loads completing in any order.  Every run must finish (no
+deadlock), every parity wait must see the phase it waits for before the
+barrier can complete the next one (no skipped phase), and every read of tensor
+or shared memory must find the item it expects there (no overwrite too early,
+no read too late).  Planted mistakes, one or two per kernel, check that the
+model catches them.
+"""
+import random
+
+import pytest
+
+
+class Bar:
+    def __init__(self, count):
+        self.count, self.pending, self.done = count, 0, 0
+
+
+class ProtocolError(AssertionError):
+    pass
+
+
+class Sim:
+    def __init__(self, seed):
+        self.rng = random.Random(seed)
+        self.bars = {}
+        self.mem = {}
+        self.mma_q = []
+        self.tma = []
+        self.roles = []
+
+    def bar(self, name, count=1):
+        self.bars[name] = Bar(count)
+
+    def arrive(self, name):
+        b = self.bars[name]
+        b.pending += 1
+        if b.pending == b.count:
+            b.pending, b.done = 0, b.done + 1
+
+    def check_read(self, region, expect, who):
+        got = self.mem.get(region)
+        if got != expect:
+            raise ProtocolError(f"{who} read {region}: found {got}, expected {expect}")
+
+    def role(self, name, gen):
+        self.roles.append([name, gen, None, False])  # name, generator, pending action, finished
+
+    def _advance(self, r, send=None):
+        # the role's next action (send delivers the result of a non-blocking test)
+        try:
+            r[2] = r[1].send(send)
+        except StopIteration:
+            r[3] = True
+
+    def _ready(self, r):
+        act = r[2]
+        if act[0] == "wait":
+            return self.bars[act[1]].done >= act[2] + 1
+        return True
+
+    def _step(self, r):
+        act, name = r[2], r[0]
+        kind = act[0]
+        result = None
+        if kind == "wait":
+            b = self.bars[act[1]]
+            if b.done >= act[2] + 2:
+                raise ProtocolError(f"{name}: {act[1]} completed phase {act[2] + 1} before the wait "
+                                    f"for phase {act[2]} was seen")
+        elif kind == "test":
+            b = self.bars[act[1]]
+            if b.done >= act[2] + 2:
+                raise ProtocolError(f"{name}: {act[1]} skipped a phase under a test")
+            result = b.done >= act[2] + 1
+        elif kind == "arrive":
+            self.arrive(act[1])
+        elif kind == "read":
+            self.check_read(act[1], act[2], name)
+        elif kind == "write":
+            self.mem[act[1]] = act[2]
+        elif kind == "mma":
+            self.mma_q.append(("mma", act[1], act[2], name))
+        elif kind == "commit":
+            self.mma_q.append(("commit", act[1]))
+        elif kind == "load":
+            self.tma.append((act[1], act[2]))
+        else:
+            raise ValueError(kind)
+        self._advance(r, result)
+
+    def run(self, max_steps=200000):
+        for r in self.roles:
+            self._advance(r)  # to the first action
+        for _ in range(max_steps):
+            choices = [("role", r) for r in self.roles if not r[3] and self._ready(r)]
+            if self.mma_q:
+                choices.append(("mma", None))
+            if self.tma:
+                choices.append(("tma", None))
+            if not choices:
+                stuck = [(r[0], r[2]) for r in self.roles if not r[3]]
+                if stuck:
+                    raise ProtocolError(f"deadlock: {stuck[:4]}")
+                return
+            kind, r = self.rng.choice(choices)
+            if kind == "role":
+                self._step(r)
+            elif kind == "mma":
+                op = self.mma_q.pop(0)
+                if op[0] == "commit":
+                    self.arrive(op[1])
+                else:
+                    for region, expect in op[1]:
+                        self.check_read(region, expect, f"MMA issued by {op[3]}")
+                    for region, value in op[2]:
+                        self.mem[region] = value
+            else:
+                writes, bar = self.tma.pop(self.rng.randrange(len(self.tma)))
+                for region, value in writes:
+                    self.mem[region] = value
+                self.arrive(bar)
+        raise ProtocolError("no end within the step limit")
+
+
+WARPS = [(wq, hf) for hf in range(2) for wq in range(4)]  # warp w: quadrant w % 4, half w // 4
+
+
+def cols(prefix, n_sub=8):
+    # every 16-column piece of a 128-column TMEM area in every lane quadrant
+    return [f"{prefix}{wq}.{sb}" for wq in range(4) for sb in range(n_sub)]
+
+
+def dq_kernel(sim, n_iter, plant=None):
+    """bwd_dq_kernel: S and dP of tile j+1 issued once every warp holds tile j's,
+    dS in columns of its own, K and V in rings of their own (3 and 2 stages)."""
+    KS, VS = 3, 2
+    for name, count in [("s_full", 1), ("s_loaded", 8), ("p_ready", 8), ("dq_done", 1), ("acc_done", 1)]:
+        sim.bar(name, count)
+    for s in range(KS):
+        sim.bar(f"k_full{s}"), sim.bar(f"k_empty{s}")
+    for s in range(VS):
+        sim.bar(f"v_full{s}"), sim.bar(f"v_empty{s}")
+
+    def producer():
+        for n in range(n_iter):
+            ks, vs = n % KS, n % VS
+            if n >= KS:
+                yield ("wait", f"k_empty{ks}", n // KS - 1)
+            yield ("load", [(f"K{ks}", ("K", n))], f"k_full{ks}")
+            if n >= VS:
+                yield ("wait", f"v_empty{vs}", n // VS - 1)
+            yield ("load", [(f"V{vs}", ("V", n))], f"v_full{vs}")
+
+    def mma():
+        def scores(j):
+            ks, vs = j % KS, j % VS
+            yield ("wait", f"k_full{ks}", j // KS)
+            yield ("wait", f"v_full{vs}", j // VS)
+            yield ("mma", [(f"K{ks}", ("K", j))], [(x, ("S", j)) for x in cols("X")])
+            yield ("mma", [(f"V{vs}", ("V", j))], [(y, ("dP", j)) for y in cols("Y")])
+            yield ("commit", "s_full")
+            yield ("commit", f"v_empty{vs}")
+        yield from scores(0)
+        for n in range(n_iter):
+            if n + 1 < n_iter:
+                if plant != "scores_before_loaded":
+                    yield ("wait", "s_loaded", n)
+                yield from scores(n + 1)
+            yield ("wait", "p_ready", n)
+            ks = n % KS
+            reads = [(f"DS{wq}.{q}", ("dS", n)) for wq in range(4) for q in range(4)] + [(f"K{ks}", ("K", n))]
+            if n > 0:
+                reads.append(("ACC", ("dQ", n - 1)))
+            yield ("mma", reads, [("ACC", ("dQ", n))])
+            yield ("commit", f"k_empty{ks}")
+            yield ("commit", "dq_done")
+        yield ("commit", "acc_done")
+
+    def elementwise(wq, hf):
+        mine = [4 * hf + i for i in range(4)]
+        for n in range(n_iter):
+            yield ("wait", "s_full", n)
+            for sb in mine:
+                yield ("read", f"X{wq}.{sb}", ("S", n))
+                yield ("read", f"Y{wq}.{sb}", ("dP", n))
+            yield ("arrive", "s_loaded")
+            if n > 0 and plant != "no_dq_done":
+                yield ("wait", "dq_done", n - 1)
+            for h in range(2):
+                yield ("write", f"DS{wq}.{2 * hf + h}", ("dS", n))
+            yield ("arrive", "p_ready")
+        yield ("wait", "acc_done", 0)
+        yield ("read", "ACC", ("dQ", n_iter - 1))
+
+    sim.role("tma", producer())
+    sim.role("mma", mma())
+    for wq, hf in WARPS:
+        sim.role(f"warp{wq + 4 * hf}", elementwise(wq, hf))
+
+
+def dkdv_kernel_128(sim, n_iter, plant=None):
+    """bwd_dkdv_kernel at d = 128: P^T then dS^T written over S^T and dP^T in two
+    steps, the next item's S^T issued right after dV when its stage has landed."""
+    S = 2
+    for name, count in [("s_full", 1), ("s_loaded", 8), ("p_ready", 8), ("dp_full", 1), ("dp_loaded", 8),
+                        ("ds_ready", 8), ("acc_done", 1)]:
+        sim.bar(name, count)
+    for s in range(S):
+        sim.bar(f"ring_full{s}"), sim.bar(f"ring_empty{s}")
+
+    def producer():
+        for n in range(n_iter):
+            slot = n % S
+            if n >= S:
+                yield ("wait", f"ring_empty{slot}", n // S - 1)
+            yield ("load", [(f"Q{slot}", ("Q", n)), (f"dO{slot}", ("dO", n)), (f"vec{slot}", ("vec", n))],
+                   f"ring_full{slot}")
+
+    def mma():
+        def issue_s(j):
+            slot = j % S
+            yield ("mma", [(f"Q{slot}", ("Q", j))], [(x, ("S", j)) for x in cols("X")])
+            yield ("commit", "s_full")
+
+        def issue_dp(j):
+            slot = j % S
+            yield ("mma", [(f"dO{slot}", ("dO", j))], [(y, ("dP", j)) for y in cols("Y")])
+            yield ("commit", "dp_full")
+        yield ("wait", "ring_full0", 0)
+        yield from issue_s(0)
+        yield from issue_dp(0)
+        for n in range(n_iter):
+            slot = n % S
+            nx, s_issued = n + 1, False
+            yield ("wait", "p_ready", n)
+            if nx < n_iter and plant == "s_before_dv":
+                # the mistake: the next S^T goes ahead of the dV product that reads P^T
+                yield ("wait", f"ring_full{nx % S}", nx // S)
+                yield from issue_s(nx)
+                s_issued = True
+            reads = [(f"X{wq}.{sb}", ("P", n)) for wq in range(4) for sb in range(4)] + [(f"dO{slot}", ("dO", n))]
+            if n > 0:
+                reads.append(("dV", ("dV", n - 1)))
+            yield ("mma", reads, [("dV", ("dV", n))])
+            if nx < n_iter and not s_issued:
+                landed = yield ("test", f"ring_full{nx % S}", nx // S)
+                if landed:
+                    yield from issue_s(nx)
+                    s_issued = True
+            yield ("wait", "ds_ready", n)
+            reads = [(f"Y{wq}.{sb}", ("dS", n)) for wq in range(4) for sb in range(4)] + [(f"Q{slot}", ("Q", n))]
+            if n > 0:
+                reads.append(("dK", ("dK", n - 1)))
+            yield ("mma", reads, [("dK", ("dK", n))])
+            yield ("commit", f"ring_empty{slot}")
+            if nx < n_iter:
+                if not s_issued:
+                    yield ("wait", f"ring_full{nx % S}", nx // S)
+                    yield from issue_s(nx)
+                yield from issue_dp(nx)
+        yield ("commit", "acc_done")
+
+    def elementwise(wq, hf):
+        mine = [4 * hf + i for i in range(4)]
+        for n in range(n_iter):
+            slot = n % S
+            yield ("wait", f"ring_full{slot}", n // S)
+            yield ("wait", "s_full", n)
+            for sb in mine:
+                yield ("read", f"X{wq}.{sb}", ("S", n))
+            yield ("arrive", "s_loaded")
+            if plant != "no_intra_sync":
+                yield ("wait", "s_loaded", n)
+            yield ("read", f"vec{slot}", ("vec", n))
+            for h in range(2):
+                yield ("write", f"X{wq}.{2 * hf + h}", ("P", n))
+            yield ("arrive", "p_ready")
+            yield ("wait", "dp_full", n)
+            for sb in mine:
+                yield ("read", f"Y{wq}.{sb}", ("dP", n))
+            yield ("arrive", "dp_loaded")
+            yield ("wait", "dp_loaded", n)
+            yield ("read", f"vec{slot}", ("vec", n))
+            for h in range(2):
+                yield ("write", f"Y{wq}.{2 * hf + h}", ("dS", n))
+            yield ("arrive", "ds_ready")
+        yield ("wait", "acc_done", 0)
+        yield ("read", "dV", ("dV", n_iter - 1))
+        yield ("read", "dK", ("dK", n_iter - 1))
+
+    sim.role("tma", producer())
+    sim.role("mma", mma())
+    for wq, hf in WARPS:
+        sim.role(f"warp{wq + 4 * hf}", elementwise(wq, hf))
+
+
+def dkdv_kernel_64(sim, n_iter, plant=None):
+    """bwd_dkdv_kernel at d = 64: P^T and dS^T in columns of their own, the next
+    item's S^T and dP^T issued once every warp holds the current ones."""
+    S = 3
+    for name, count in [("s_full", 1), ("s_loaded", 8), ("p_ready", 8), ("pd_done", 1), ("acc_done", 1)]:
+        sim.bar(name, count)
+    for s in range(S):
+        sim.bar(f"ring_full{s}"), sim.bar(f"ring_empty{s}")
+
+    def producer():
+        for n in range(n_iter):
+            slot = n % S
+            if n >= S:
+                yield ("wait", f"ring_empty{slot}", n // S - 1)
+            yield ("load", [(f"Q{slot}", ("Q", n)), (f"dO{slot}", ("dO", n)), (f"vec{slot}", ("vec", n))],
+                   f"ring_full{slot}")
+
+    def mma():
+        def scores(j):
+            slot = j % S
+            yield ("wait", f"ring_full{slot}", j // S)
+            yield ("mma", [(f"Q{slot}", ("Q", j))], [(x, ("S", j)) for x in cols("X")])
+            yield ("mma", [(f"dO{slot}", ("dO", j))], [(y, ("dP", j)) for y in cols("Y")])
+            yield ("commit", "s_full")
+        yield from scores(0)
+        for n in range(n_iter):
+            slot = n % S
+            if n + 1 < n_iter:
+                yield ("wait", "s_loaded", n)
+                yield from scores(n + 1)
+            yield ("wait", "p_ready", n)
+            pr = [(f"PP{wq}.{q}", ("P", n)) for wq in range(4) for q in range(4)]
+            dr = [(f"DD{wq}.{q}", ("dS", n)) for wq in range(4) for q in range(4)]
+            yield ("mma", pr + [(f"dO{slot}", ("dO", n))] + ([("dV", ("dV", n - 1))] if n else []),
+                   [("dV", ("dV", n))])
+            yield ("mma", dr + [(f"Q{slot}", ("Q", n))] + ([("dK", ("dK", n - 1))] if n else []),
+                   [("dK", ("dK", n))])
+            yield ("commit", f"ring_empty{slot}")
+            yield ("commit", "pd_done")
+        yield ("commit", "acc_done")
+
+    def elementwise(wq, hf):
+        mine = [4 * hf + i for i in range(4)]
+        for n in range(n_iter):
+            slot = n % S
+            yield ("wait", f"ring_full{slot}", n // S)
+            yield ("wait", "s_full", n)
+            for sb in mine:
+                yield ("read", f"X{wq}.{sb}", ("S", n))
+                yield ("read", f"Y{wq}.{sb}", ("dP", n))
+            yield ("arrive", "s_loaded")
+            yield ("read", f"vec{slot}", ("vec", n))
+            if n > 0 and plant != "no_pd_done":
+                yield ("wait", "pd_done", n - 1)
+            for h in range(2):
+                yield ("write", f"PP{wq}.{2 * hf + h}", ("P", n))
+                yield ("write", f"DD{wq}.{2 * hf + h}", ("dS", n))
+            yield ("arrive", "p_ready")
+        yield ("wait", "acc_done", 0)
+        yield ("read", "dV", ("dV", n_iter - 1))
+        yield ("read", "dK", ("dK", n_iter - 1))
+
+    sim.role("tma", producer())
+    sim.role("mma", mma())
+    for wq, hf in WARPS:
+        sim.role(f"warp{wq + 4 * hf}", elementwise(wq, hf))
+
+
+KERNELS = {"dq": dq_kernel, "dkdv128": dkdv_kernel_128, "dkdv64": dkdv_kernel_64}
+
+
+@pytest.mark.parametrize("kernel", sorted(KERNELS))
+@pytest.mark.parametrize("n_iter", [1, 2, 3, 7])
+def test_protocol_holds_under_random_interleavings(kernel, n_iter):
+    for seed in range(150):
+        sim = Sim(1000 * n_iter + seed)
+        KERNELS[kernel](sim, n_iter)
+        sim.run()
+
+
+@pytest.mark.parametrize("kernel,plant", [("dq", "no_dq_done"), ("dq", "scores_before_loaded"),
+                                          ("dkdv128", "no_intra_sync"), ("dkdv128", "s_before_dv"),
+                                          ("dkdv64", "no_pd_done")])
+def test_the_model_catches_a_planted_mistake(kernel, plant):
+    caught = 0
+    for seed in range(150):
+        sim = Sim(seed)
+        KERNELS[kernel](sim, 5, plant)
+        try:
+            sim.run()
+        except ProtocolError:
+            caught += 1
+    assert caught > 0, f"{kernel} with {plant} passed every interleaving"
