@@ -1,4 +1,4 @@
-"""The barrier protocols of the backward kernels, on the host (no GPU).
+"""The barrier protocols of the attention kernels, on the host (no GPU).
 
 Each role of a CTA -- the TMA producer, the MMA-issuing thread and each of the
 eight elementwise warps -- is restated as the sequence of mbarrier waits and
@@ -10,8 +10,9 @@ runs) and TMA loads completing in any order.  Every run must finish (no
 deadlock), every parity wait must see the phase it waits for before the
 barrier can complete the next one (no skipped phase), and every read of tensor
 or shared memory must find the item it expects there (no overwrite too early,
-no read too late).  Planted mistakes, one or two per kernel, check that the
-model catches them.
+no read too late).  The forward kernel's roles are restated the same way, for
+both head sizes.  Planted mistakes, one or two per kernel, check that the model
+catches them.
 """
 import random
 
@@ -395,3 +396,176 @@ def test_the_model_catches_a_planted_mistake(kernel, plant):
         except ProtocolError:
             caught += 1
     assert caught > 0, f"{kernel} with {plant} passed every interleaving"
+
+
+def prefill_kernel(sim, units, sep_p, plant=None):
+    """prefill_kernel, one CTA running `units` = [(n0, n1), ...] back to back (key
+    tiles of its two query tiles, every unit from key tile 0).  d = 128 (sep_p
+    False): P over S, o_done after a tile's last PV.  d = 64 (sep_p True): P in
+    columns of its own, s_free / pv_done, both Q K^T products of a step before
+    both PV products.  Each softmax warp may rescale O at any step."""
+    for name in ["q_full", "q_empty", "kv_full0", "kv_full1", "kv_empty0", "kv_empty1"]:
+        sim.bar(name)
+    for t in range(2):
+        sim.bar(f"s_full{t}"), sim.bar(f"o_done{t}"), sim.bar(f"pv_done{t}")
+        sim.bar(f"p_full{t}", 4), sim.bar(f"s_free{t}", 4)
+
+    def producer():
+        gc = 0
+
+        def group(writes):
+            nonlocal gc
+            st = gc % 2
+            if gc >= 2:
+                yield ("wait", f"kv_empty{st}", gc // 2 - 1)
+            yield ("load", [(f"ring{2 * st + half}", v) for half, v in writes], f"kv_full{st}")
+            gc += 1
+        for u, (n0, n1) in enumerate(units):
+            if u > 0:
+                yield ("wait", "q_empty", u - 1)
+            yield ("load", [(f"Q{t}", ("Q", u, t)) for t in range(2)], "q_full")
+            j1 = max(n0, n1)
+            yield from group([(0, ("K", u, 0))])
+            for j in range(j1):
+                writes = [(0, ("V", u, j))] + ([(1, ("K", u, j + 1))] if j + 1 < j1 else [])
+                yield from group(writes)
+
+    def mma():
+        gc, pc, qk = 0, [0, 0], [0, 0]
+
+        def take_group():
+            nonlocal gc
+            st = gc % 2
+            yield ("wait", f"kv_full{st}", gc // 2)
+            return st
+
+        def qk_mma(u, t, j, kslot):
+            reads = [(f"Q{t}", ("Q", u, t)), (f"ring{kslot}", ("K", u, j))]
+            return ("mma", reads, [(f"S{t}.{w}", ("S", u, t, j)) for w in range(4)])
+
+        def pv_mma(u, t, j, vslot):
+            reads = [(f"P{t}.{w}", ("P", u, t, j)) for w in range(4)]
+            reads += [(f"ring{vslot}", ("V", u, j))]
+            if j > 0:
+                reads += [(f"O{t}.{w}", ("O", u, t, j - 1)) for w in range(4)]
+            return ("mma", reads, [(f"O{t}.{w}", ("O", u, t, j)) for w in range(4)])
+        for u, n in enumerate(units):
+            j1 = max(n)
+            yield ("wait", "q_full", u)
+            st = yield from take_group()
+            for t in range(2):
+                if n[t] > 0:
+                    if sep_p and qk[t] > 0:
+                        yield ("wait", f"s_free{t}", qk[t] - 1)
+                    yield qk_mma(u, t, 0, 2 * st)
+                    yield ("commit", f"s_full{t}")
+                    qk[t] += 1
+            yield ("commit", f"kv_empty{st}")
+            gc += 1
+            if j1 == 1:
+                yield ("commit", "q_empty")
+            for j in range(j1):
+                st = yield from take_group()
+                if not sep_p:
+                    for t in range(2):
+                        if j >= n[t]:
+                            continue
+                        yield ("wait", f"p_full{t}", pc[t])
+                        pc[t] += 1
+                        if plant == "qk_before_pv" and j + 1 < n[t]:
+                            yield qk_mma(u, t, j + 1, 2 * st + 1)
+                        yield pv_mma(u, t, j, 2 * st)
+                        if j == n[t] - 1:
+                            yield ("commit", f"o_done{t}")
+                        if j + 1 < n[t]:
+                            if plant != "qk_before_pv":
+                                yield qk_mma(u, t, j + 1, 2 * st + 1)
+                            yield ("commit", f"s_full{t}")
+                else:
+                    for t in range(2):
+                        if j + 1 < n[t]:
+                            if plant != "qk_without_s_free":
+                                yield ("wait", f"s_free{t}", qk[t] - 1)
+                            yield qk_mma(u, t, j + 1, 2 * st + 1)
+                            yield ("commit", f"s_full{t}")
+                            qk[t] += 1
+                    for t in range(2):
+                        if j >= n[t]:
+                            continue
+                        yield ("wait", f"p_full{t}", pc[t])
+                        pc[t] += 1
+                        yield pv_mma(u, t, j, 2 * st)
+                        yield ("commit", f"pv_done{t}")
+                yield ("commit", f"kv_empty{st}")
+                gc += 1
+                if j + 1 == j1 - 1:
+                    yield ("commit", "q_empty")
+
+    def softmax(t, w):
+        sc = oc = pvc = 0
+        for u, n in enumerate(units):
+            for j in range(n[t]):
+                yield ("wait", f"s_full{t}", sc)
+                sc += 1
+                yield ("read", f"S{t}.{w}", ("S", u, t, j))
+                if sep_p:
+                    yield ("arrive", f"s_free{t}")
+                    if j > 0:
+                        yield ("wait", f"pv_done{t}", pvc)
+                        pvc += 1
+                yield ("write", f"P{t}.{w}", ("P", u, t, j))
+                if j > 0 and sim.rng.random() < 0.3:  # the lazy rescale of O
+                    yield ("read", f"O{t}.{w}", ("O", u, t, j - 1))
+                    yield ("write", f"O{t}.{w}", ("O", u, t, j - 1))
+                yield ("arrive", f"p_full{t}")
+            if n[t] > 0:
+                if sep_p:
+                    yield ("wait", f"pv_done{t}", pvc)
+                    pvc += 1
+                else:
+                    yield ("wait", f"o_done{t}", oc)
+                    oc += 1
+                yield ("read", f"O{t}.{w}", ("O", u, t, n[t] - 1))
+
+    if not sep_p:
+        # P is written over S: the same tensor-memory area under two names
+        class Alias(dict):
+            def _k(self, k):
+                return k.replace("P", "S", 1) if k.startswith("P") else k
+
+            def get(self, k, d=None):
+                return dict.get(self, self._k(k), d)
+
+            def __setitem__(self, k, v):
+                dict.__setitem__(self, self._k(k), v)
+        sim.mem = Alias()
+    sim.role("tma", producer())
+    sim.role("mma", mma())
+    for t in range(2):
+        for w in range(4):
+            sim.role(f"softmax{t}.{w}", softmax(t, w))
+
+
+PREFILL_UNITS = [[(3, 3)], [(1, 1), (2, 2)], [(2, 3), (3, 2), (1, 1)], [(4, 4), (1, 2), (2, 1)]]
+
+
+@pytest.mark.parametrize("sep_p", [False, True], ids=["d128", "d64"])
+@pytest.mark.parametrize("units", PREFILL_UNITS, ids=lambda u: "-".join(f"{a}{b}" for a, b in u))
+def test_prefill_protocol_holds_under_random_interleavings(sep_p, units):
+    for seed in range(150):
+        sim = Sim(seed)
+        prefill_kernel(sim, units, sep_p)
+        sim.run()
+
+
+@pytest.mark.parametrize("sep_p,plant", [(False, "qk_before_pv"), (True, "qk_without_s_free")])
+def test_the_prefill_model_catches_a_planted_mistake(sep_p, plant):
+    caught = 0
+    for seed in range(150):
+        sim = Sim(seed)
+        prefill_kernel(sim, [(3, 3), (2, 3)], sep_p, plant)
+        try:
+            sim.run()
+        except ProtocolError:
+            caught += 1
+    assert caught > 0, f"prefill sep_p={sep_p} with {plant} passed every interleaving"
