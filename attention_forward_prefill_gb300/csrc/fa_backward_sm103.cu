@@ -352,17 +352,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             const uint64_t k_desc = sdesc_sw128(fix, 16, 1024);
             const uint64_t v_desc = sdesc_sw128(fix + L::kTileBytes, 16, 1024);
             bool ok = mbar_wait(fix_full, 0, abort_flag, kWatchdogNs);
-            // S^T = K Q_i^T and dP^T = V dO_i^T (keys on TMEM lanes) for ring item j
-            auto issue_scores = [&](int j) {
-                const int slot = j % L::kStages;
-                if (!mbar_wait(ring_full + slot, (j / L::kStages) & 1, abort_flag, kWatchdogNs)) return false;
-                tc_fence_after();
-                const uint32_t st = ring + slot * L::kStageBytes;
-                issue_qk<D>(tmem + L::kXCol, k_desc, sdesc_sw128(st, 16, 1024), idesc_s);
-                issue_qk<D>(tmem + L::kYCol, v_desc, sdesc_sw128(st + L::kTileBytes, 16, 1024), idesc_s);
-                umma_commit(s_full);
-                return true;
-            };
             if constexpr (!L::kOwnPds) {
                 // d = 128: P^T and dS^T are written over S^T and dP^T, in two steps.
                 // dP^T runs while the weights are computed, dV += P^T dO_i while dS^T is.
@@ -426,36 +415,48 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         issue_dp(nx);  // over dS^T, after the dK product that reads it
                     }
                 }
-            }
-            if (ok && L::kOwnPds) ok = issue_scores(0);
-            for (int n = 0; n < n_iter && ok && L::kOwnPds; ++n) {
-                // P^T and dS^T have columns of their own: once every elementwise warp
-                // holds this item's scores, the next item's products may start.
-                if (n + 1 < n_iter) {
-                    if (!mbar_wait(s_loaded, n & 1, abort_flag, kWatchdogNs)) {
+            } else {
+                // S^T = K Q_i^T and dP^T = V dO_i^T (keys on TMEM lanes) for ring item j
+                auto issue_scores = [&](int j) {
+                    const int slot = j % L::kStages;
+                    if (!mbar_wait(ring_full + slot, (j / L::kStages) & 1, abort_flag, kWatchdogNs)) return false;
+                    tc_fence_after();
+                    const uint32_t st = ring + slot * L::kStageBytes;
+                    issue_qk<D>(tmem + L::kXCol, k_desc, sdesc_sw128(st, 16, 1024), idesc_s);
+                    issue_qk<D>(tmem + L::kYCol, v_desc, sdesc_sw128(st + L::kTileBytes, 16, 1024), idesc_s);
+                    umma_commit(s_full);
+                    return true;
+                };
+                if (ok) ok = issue_scores(0);
+                for (int n = 0; n < n_iter && ok; ++n) {
+                    // P^T and dS^T have columns of their own: once every elementwise warp
+                    // holds this item's scores, the next item's products may start.
+                    if (n + 1 < n_iter) {
+                        if (!mbar_wait(s_loaded, n & 1, abort_flag, kWatchdogNs)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        if (!issue_scores(n + 1)) {
+                            ok = false;
+                            break;
+                        }
+                    }
+                    if (!mbar_wait(p_ready, n & 1, abort_flag, kWatchdogNs)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    if (!issue_scores(n + 1)) {
-                        ok = false;
-                        break;
-                    }
+                    // dV += P^T dO_i and dK += dS^T Q_i (P^T, dS^T from TMEM; dO_i, Q_i MN-major)
+                    const int slot = n % L::kStages;
+                    const uint32_t st = ring + slot * L::kStageBytes;
+                    issue_pv<D>(tmem + L::kACol, tmem + L::kPCol,
+                                sdesc_sw128(st + L::kTileBytes, kSlabBytes, 1024), idesc_acc, n > 0);
+                    issue_pv<D>(tmem + L::kBCol, tmem + L::kDsCol, sdesc_sw128(st, kSlabBytes, 1024), idesc_acc,
+                                n > 0);
+                    umma_commit(ring_empty + slot);
+                    umma_commit(pd_done);
                 }
-                if (!mbar_wait(p_ready, n & 1, abort_flag, kWatchdogNs)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                // dV += P^T dO_i and dK += dS^T Q_i (P^T, dS^T from TMEM; dO_i, Q_i MN-major)
-                const int slot = n % L::kStages;
-                const uint32_t st = ring + slot * L::kStageBytes;
-                issue_pv<D>(tmem + L::kACol, tmem + L::kPCol,
-                            sdesc_sw128(st + L::kTileBytes, kSlabBytes, 1024), idesc_acc, n > 0);
-                issue_pv<D>(tmem + L::kBCol, tmem + L::kDsCol, sdesc_sw128(st, kSlabBytes, 1024), idesc_acc,
-                            n > 0);
-                umma_commit(ring_empty + slot);
-                umma_commit(pd_done);
             }
             umma_commit(acc_done);
             umma_commit(drain);
