@@ -399,11 +399,13 @@ def test_the_model_catches_a_planted_mistake(kernel, plant):
 
 
 def prefill_kernel(sim, units, sep_p, plant=None):
-    """prefill_kernel, one CTA running `units` = [(n0, n1), ...] back to back (key
-    tiles of its two query tiles, every unit from key tile 0).  d = 128 (sep_p
-    False): P over S, o_done after a tile's last PV.  d = 64 (sep_p True): P in
-    columns of its own, s_free / pv_done, both Q K^T products of a step before
-    both PV products.  Each softmax warp may rescale O at any step."""
+    """prefill_kernel, one CTA running `units` = [(j0, n0, n1), ...] back to back:
+    whole units (j0 = 0) or stream-K pieces (j0 > 0), query tile t taking key
+    tiles [j0, n_t) of the piece's [j0, max(n0, n1)) (none when n_t <= j0).
+    d = 128 (sep_p False): P over S, o_done after a tile's last PV.  d = 64
+    (sep_p True): P in columns of its own, s_free / pv_done, both Q K^T products
+    of a step before both PV products.  Each softmax warp may rescale O at any
+    step after a piece's first."""
     for name in ["q_full", "q_empty", "kv_full0", "kv_full1", "kv_empty0", "kv_empty1"]:
         sim.bar(name)
     for t in range(2):
@@ -420,13 +422,13 @@ def prefill_kernel(sim, units, sep_p, plant=None):
                 yield ("wait", f"kv_empty{st}", gc // 2 - 1)
             yield ("load", [(f"ring{2 * st + half}", v) for half, v in writes], f"kv_full{st}")
             gc += 1
-        for u, (n0, n1) in enumerate(units):
+        for u, (j0, n0, n1) in enumerate(units):
             if u > 0:
                 yield ("wait", "q_empty", u - 1)
-            yield ("load", [(f"Q{t}", ("Q", u, t)) for t in range(2)], "q_full")
+            yield ("load", [(f"Q{t}", ("Q", u, t)) for t in range(2) if (n0, n1)[t] > j0], "q_full")
             j1 = max(n0, n1)
-            yield from group([(0, ("K", u, 0))])
-            for j in range(j1):
+            yield from group([(0, ("K", u, j0))])
+            for j in range(j0, j1):
                 writes = [(0, ("V", u, j))] + ([(1, ("K", u, j + 1))] if j + 1 < j1 else [])
                 yield from group(writes)
 
@@ -443,28 +445,28 @@ def prefill_kernel(sim, units, sep_p, plant=None):
             reads = [(f"Q{t}", ("Q", u, t)), (f"ring{kslot}", ("K", u, j))]
             return ("mma", reads, [(f"S{t}.{w}", ("S", u, t, j)) for w in range(4)])
 
-        def pv_mma(u, t, j, vslot):
+        def pv_mma(u, t, j, j0, vslot):
             reads = [(f"P{t}.{w}", ("P", u, t, j)) for w in range(4)]
             reads += [(f"ring{vslot}", ("V", u, j))]
-            if j > 0:
+            if j > j0:
                 reads += [(f"O{t}.{w}", ("O", u, t, j - 1)) for w in range(4)]
             return ("mma", reads, [(f"O{t}.{w}", ("O", u, t, j)) for w in range(4)])
-        for u, n in enumerate(units):
+        for u, (j0, *n) in enumerate(units):
             j1 = max(n)
             yield ("wait", "q_full", u)
             st = yield from take_group()
             for t in range(2):
-                if n[t] > 0:
+                if n[t] > j0:
                     if sep_p and qk[t] > 0:
                         yield ("wait", f"s_free{t}", qk[t] - 1)
-                    yield qk_mma(u, t, 0, 2 * st)
+                    yield qk_mma(u, t, j0, 2 * st)
                     yield ("commit", f"s_full{t}")
                     qk[t] += 1
             yield ("commit", f"kv_empty{st}")
             gc += 1
-            if j1 == 1:
+            if j1 - j0 == 1:
                 yield ("commit", "q_empty")
-            for j in range(j1):
+            for j in range(j0, j1):
                 st = yield from take_group()
                 if not sep_p:
                     for t in range(2):
@@ -474,7 +476,7 @@ def prefill_kernel(sim, units, sep_p, plant=None):
                         pc[t] += 1
                         if plant == "qk_before_pv" and j + 1 < n[t]:
                             yield qk_mma(u, t, j + 1, 2 * st + 1)
-                        yield pv_mma(u, t, j, 2 * st)
+                        yield pv_mma(u, t, j, j0, 2 * st)
                         if j == n[t] - 1:
                             yield ("commit", f"o_done{t}")
                         if j + 1 < n[t]:
@@ -494,7 +496,7 @@ def prefill_kernel(sim, units, sep_p, plant=None):
                             continue
                         yield ("wait", f"p_full{t}", pc[t])
                         pc[t] += 1
-                        yield pv_mma(u, t, j, 2 * st)
+                        yield pv_mma(u, t, j, j0, 2 * st)
                         yield ("commit", f"pv_done{t}")
                 yield ("commit", f"kv_empty{st}")
                 gc += 1
@@ -503,22 +505,22 @@ def prefill_kernel(sim, units, sep_p, plant=None):
 
     def softmax(t, w):
         sc = oc = pvc = 0
-        for u, n in enumerate(units):
-            for j in range(n[t]):
+        for u, (j0, *n) in enumerate(units):
+            for j in range(j0, n[t]):
                 yield ("wait", f"s_full{t}", sc)
                 sc += 1
                 yield ("read", f"S{t}.{w}", ("S", u, t, j))
                 if sep_p:
                     yield ("arrive", f"s_free{t}")
-                    if j > 0:
+                    if j > j0:
                         yield ("wait", f"pv_done{t}", pvc)
                         pvc += 1
                 yield ("write", f"P{t}.{w}", ("P", u, t, j))
-                if j > 0 and sim.rng.random() < 0.3:  # the lazy rescale of O
+                if j > j0 and sim.rng.random() < 0.3:  # the lazy rescale of O
                     yield ("read", f"O{t}.{w}", ("O", u, t, j - 1))
                     yield ("write", f"O{t}.{w}", ("O", u, t, j - 1))
                 yield ("arrive", f"p_full{t}")
-            if n[t] > 0:
+            if n[t] > j0:
                 if sep_p:
                     yield ("wait", f"pv_done{t}", pvc)
                     pvc += 1
@@ -546,11 +548,15 @@ def prefill_kernel(sim, units, sep_p, plant=None):
             sim.role(f"softmax{t}.{w}", softmax(t, w))
 
 
-PREFILL_UNITS = [[(3, 3)], [(1, 1), (2, 2)], [(2, 3), (3, 2), (1, 1)], [(4, 4), (1, 2), (2, 1)]]
+# whole units, causal units whose tiles end apart, and stream-K pieces: a cut
+# piece first, whole units after, tiles without keys in a piece
+PREFILL_UNITS = [[(0, 3, 3)], [(0, 1, 1), (0, 2, 2)], [(0, 2, 3), (0, 3, 2), (0, 1, 1)],
+                 [(0, 4, 4), (0, 1, 2), (0, 2, 1)], [(2, 5, 5), (0, 3, 3), (0, 2, 2)],
+                 [(1, 2, 4), (0, 3, 1), (3, 4, 4)], [(3, 2, 5), (0, 1, 3), (2, 4, 2)]]
 
 
 @pytest.mark.parametrize("sep_p", [False, True], ids=["d128", "d64"])
-@pytest.mark.parametrize("units", PREFILL_UNITS, ids=lambda u: "-".join(f"{a}{b}" for a, b in u))
+@pytest.mark.parametrize("units", PREFILL_UNITS, ids=lambda u: "-".join(f"{a}{b}{c}" for a, b, c in u))
 def test_prefill_protocol_holds_under_random_interleavings(sep_p, units):
     for seed in range(150):
         sim = Sim(seed)
@@ -563,7 +569,7 @@ def test_the_prefill_model_catches_a_planted_mistake(sep_p, plant):
     caught = 0
     for seed in range(150):
         sim = Sim(seed)
-        prefill_kernel(sim, [(3, 3), (2, 3)], sep_p, plant)
+        prefill_kernel(sim, [(0, 3, 3), (1, 2, 3)], sep_p, plant)
         try:
             sim.run()
         except ProtocolError:
