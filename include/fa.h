@@ -179,7 +179,8 @@ int fa_prefill_lse(const void *q, const void *k, const void *v, void *out,
  *                        (FA_F16, FA_BF16, FA_F32), accumulated in fp32; none
  *                        may overlap another argument
  *   causal, scale      : as in the forward call
- * Scratch of 8 bytes per row comes from the library's pool.  Errors as for
+ * Scratch of 8 bytes per query row, with each head's rows rounded up to a
+ * multiple of 128, comes from the library's pool.  Errors as for
  * prefill: FA_ERR_NULL, FA_ERR_SHAPE, FA_ERR_HEAD_DIM, FA_ERR_DTYPE,
  * FA_ERR_ALIGN, FA_ERR_SCALE, FA_ERR_ALIAS, FA_ERR_WORKSPACE, FA_ERR_ARCH,
  * FA_ERR_CUDA.
