@@ -86,6 +86,19 @@ def test_every_split_count_agrees(fa, oracle_mod):
         assert np.abs(got - first).max() <= 2e-3
 
 
+def test_more_than_32_splits(fa, oracle_mod):
+    # the merge kernel reads (m, l) 32 splits to a batch: past 32 splits it takes
+    # a second batch of lanes.  At 64 splits the chunks are 64 rows, so these
+    # lengths have 64, 40 and 33 splits with keys; 32 splits stay in one batch.
+    L, B, H = 4096, 3, 2
+    assert fa.fa_decode_chunk_len(L, 64) == 64
+    q, kc, vc, lens = make_decode(B, H, L, 64, "f16", 302, [4096, 2500, 2049])
+    want = oracle_decode(oracle_mod, q, kc, vc, lens, "f16", 0.125)
+    for s in (32, 64):
+        got = G.device_to_f64(run_decode(fa, q, kc, vc, lens, "f16", 0.125, "f32", num_splits=s))
+        G.assert_close(got, want, "f16", "f32", f"decode splits={s}")
+
+
 def test_fixed_split_is_bit_identical_and_workspace_paths_agree(fa):
     import torch
     B, H, L = 8, 14, 4096
