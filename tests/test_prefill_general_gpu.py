@@ -170,6 +170,17 @@ def test_causal_stream_k_schedule(fa, oracle_mod, shape):
     assert np.abs(sk - un).max() <= 4e-3
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_stream_k_unit_cut_into_many_pieces(fa, oracle_mod, causal):
+    # a 256-query chunk over 16384 keys with two heads: the schedule cuts each of
+    # the two units over 76 CTAs, so the fixup's piece list takes several warp
+    # ballots and merges 76 partials per row
+    _, info, items = fa.fa_prefill_plan(1, 2, 256, 16384, causal, 0, 0)  # this device's SMs
+    if info[0] and info[1] == 152:
+        assert [it[2] - it[1] + 1 for it in items] == [76, 76]
+    check_dense(fa, oracle_mod, 1, 2, 2, 256, 16384, 128, causal, 1500 + causal, rows=G.sample_rows(256, 19))
+
+
 def test_stream_k_is_bit_identical_run_to_run(fa):
     import torch
     B, H, N, d = 1, 12, 2048, 64
