@@ -24,8 +24,11 @@ STATUS_NAMES = {
     0: "FA_OK", 1: "FA_ERR_NULL", 2: "FA_ERR_SHAPE", 3: "FA_ERR_HEAD_DIM",
     4: "FA_ERR_DTYPE", 5: "FA_ERR_ALIGN", 6: "FA_ERR_SCALE", 7: "FA_ERR_ARCH",
     8: "FA_ERR_WORKSPACE", 9: "FA_ERR_CUDA", 10: "FA_ERR_WATCHDOG",
-    11: "FA_ERR_ALIAS", 12: "FA_ERR_SPLITS",
+    11: "FA_ERR_SEQ_LEN", 12: "FA_ERR_ALIAS", 13: "FA_ERR_SPLITS",
 }
+(FA_ERR_NULL, FA_ERR_SHAPE, FA_ERR_HEAD_DIM, FA_ERR_DTYPE, FA_ERR_ALIGN, FA_ERR_SCALE, FA_ERR_ARCH,
+ FA_ERR_WORKSPACE, FA_ERR_CUDA, FA_ERR_WATCHDOG, FA_ERR_SEQ_LEN, FA_ERR_ALIAS,
+ FA_ERR_SPLITS) = range(1, 14)
 
 _lock = threading.Lock()
 _lib = None
@@ -33,7 +36,7 @@ _lib = None
 _vp, _i, _f, _u, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_uint, ctypes.c_size_t
 _SIGNATURES = {
     "fa_prefill": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp]),
-    "fa_prefill_ex": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _i, _u, _vp]),
+    "fa_prefill_ex": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _i, _vp]),
     "fa_prefill_gqa": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _f, _i, _i, _u, _vp]),
     "fa_prefill_host": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _f, _i, _i, _u, _vp]),
     "fa_prefill_varlen": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _i,
@@ -48,6 +51,7 @@ _SIGNATURES = {
     "fa_decode_gqa": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _i, _i, _vp, _sz,
                            _vp]),
     "fa_decode_gqa_choose_splits": (_i, [_i, _i, _i, _i, _i]),
+    "fa_decode_splits_for_sms": (_i, [_i, _i, _i, _i, _i]),
     "fa_decode_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _i, _i, _vp]),
     "fa_decode_noalloc_max_bytes": (_sz, []),
     "fa_decode_choose_splits": (_i, [_i, _i, _i, _i]),
@@ -56,6 +60,9 @@ _SIGNATURES = {
     "fa_status_string": (ctypes.c_char_p, [_i]),
     "fa_last_cuda_error": (_i, []),
     "fa_device_status": (_i, [_i]),
+    "fa_watchdog_selftest": (_i, [ctypes.c_longlong, _vp, _vp]),
+    "fa_pool_stats": (_i, [_vp, _i]),
+    "fa_read_probe": (_i, [_vp, _sz, _vp, _vp]),
     "fa_version": (_i, []),
 }
 
@@ -97,10 +104,10 @@ def fa_prefill(q, k, v, out, B, H, N, d, causal, scale, stream=0) -> int:
     return load().fa_prefill(q, k, v, out, B, H, N, d, int(causal), float(scale), stream)
 
 
-def fa_prefill_ex(q, k, v, out, B, H, N, d, causal, scale, in_dtype, out_dtype, flags=0,
+def fa_prefill_ex(q, k, v, out, B, H, N, d, causal, scale, in_dtype, out_dtype,
                   stream=0) -> int:
     return load().fa_prefill_ex(q, k, v, out, B, H, N, d, int(causal), float(scale),
-                                in_dtype, out_dtype, flags, stream)
+                                in_dtype, out_dtype, stream)
 
 
 def fa_prefill_gqa(q, k, v, out, B, Hq, Hkv, Nq, Nk, d, causal, scale, in_dtype, out_dtype,
@@ -164,8 +171,12 @@ def fa_decode_gqa(q, k_cache, v_cache, seq_lens, out, B, Hq, Hkv, max_len, d, sc
                                 workspace_bytes, stream)
 
 
-def fa_decode_gqa_choose_splits(B, Hq, Hkv, max_len, num_sms=0) -> int:
-    return load().fa_decode_gqa_choose_splits(B, Hq, Hkv, max_len, num_sms)
+def fa_decode_gqa_choose_splits(B, Hq, Hkv, max_len, device=-1) -> int:
+    return load().fa_decode_gqa_choose_splits(B, Hq, Hkv, max_len, device)
+
+
+def fa_decode_splits_for_sms(B, Hq, Hkv, max_len, num_sms) -> int:
+    return load().fa_decode_splits_for_sms(B, Hq, Hkv, max_len, num_sms)
 
 
 def fa_decode_noalloc(q, k_cache, v_cache, seq_lens, out, B, H, max_len, d, scale, in_dtype,
@@ -179,8 +190,8 @@ def fa_decode_noalloc_max_bytes() -> int:
     return load().fa_decode_noalloc_max_bytes()
 
 
-def fa_decode_choose_splits(B, H, max_len, num_sms=0) -> int:
-    return load().fa_decode_choose_splits(B, H, max_len, num_sms)
+def fa_decode_choose_splits(B, H, max_len, device=-1) -> int:
+    return load().fa_decode_choose_splits(B, H, max_len, device)
 
 
 def fa_decode_chunk_len(max_len, num_splits) -> int:
@@ -205,6 +216,21 @@ def fa_device_status(reset: bool = False) -> int:
 
 def fa_version() -> int:
     return load().fa_version()
+
+
+def fa_watchdog_selftest(limit_ns, result, stream=0) -> int:
+    return load().fa_watchdog_selftest(int(limit_ns), result, stream)
+
+
+def fa_pool_stats(reset_high: bool = False):
+    """(status, [reserved, reserved_high, used, used_high]) of the library's scratch pool."""
+    out = (ctypes.c_longlong * 4)()
+    rc = load().fa_pool_stats(out, int(reset_high))
+    return rc, [int(x) for x in out]
+
+
+def fa_read_probe(src, nbytes, xor_out, stream=0) -> int:
+    return load().fa_read_probe(src, nbytes, xor_out, stream)
 
 
 # ---------------------------------------------------------------- torch calls

@@ -18,7 +18,6 @@ namespace fa {
 namespace {
 thread_local int t_last_cuda_error = 0;
 
-constexpr int kMaxDevices = 64;
 std::mutex g_dev_mu;
 DeviceInfo g_dev_cache[kMaxDevices];
 bool g_dev_have[kMaxDevices] = {};
@@ -119,7 +118,7 @@ using namespace fa;
 
 extern "C" {
 
-int fa_version(void) { return 1 * 10000 + 1 * 100 + 0; }
+int fa_version(void) { return 2 * 10000 + 0 * 100 + 0; }
 
 const char *fa_status_string(int status) {
     switch (status) {
@@ -134,6 +133,7 @@ const char *fa_status_string(int status) {
         case FA_ERR_WORKSPACE: return "workspace too small or allocation failed";
         case FA_ERR_CUDA: return "CUDA runtime error (see fa_last_cuda_error)";
         case FA_ERR_WATCHDOG: return "a device-side wait ran out of time";
+        case FA_ERR_SEQ_LEN: return "a device-resident sequence length was out of range (clamped)";
         case FA_ERR_ALIAS: return "output overlaps an input";
         case FA_ERR_SPLITS: return "num_splits out of range";
         default: return "unknown status";
@@ -147,7 +147,39 @@ int fa_device_status(int reset) {
     const int a = read_prefill_status(reset), b = read_decode_status(reset),
               c = read_backward_status(reset);
     if (a < 0 || b < 0 || c < 0) return -1;
+    // a watchdog report wins over a clamped length
+    for (int v : {a, b, c})
+        if (v == FA_ERR_WATCHDOG) return v;
     return a ? a : (b ? b : c);
+}
+
+int fa_pool_stats(long long *out, int reset_high) {
+    if (!out) return FA_ERR_NULL;
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (dev < 0 || dev >= kMaxDevices) return cuda_fail(cudaErrorInvalidDevice);
+    cudaMemPool_t pool;
+    {
+        std::lock_guard<std::mutex> lk(g_dev_mu);
+        pool = g_pool[dev];
+    }
+    for (int i = 0; i < 4; ++i) out[i] = 0;
+    if (!pool) return FA_OK;  // nothing was ever allocated on this device
+    const cudaMemPoolAttr attrs[4] = {cudaMemPoolAttrReservedMemCurrent, cudaMemPoolAttrReservedMemHigh,
+                                      cudaMemPoolAttrUsedMemCurrent, cudaMemPoolAttrUsedMemHigh};
+    for (int i = 0; i < 4; ++i) {
+        uint64_t v = 0;
+        if ((e = cudaMemPoolGetAttribute(pool, attrs[i], &v)) != cudaSuccess) return cuda_fail(e);
+        out[i] = static_cast<long long>(v);
+    }
+    if (reset_high) {
+        uint64_t zero = 0;
+        if ((e = cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReservedMemHigh, &zero)) != cudaSuccess ||
+            (e = cudaMemPoolSetAttribute(pool, cudaMemPoolAttrUsedMemHigh, &zero)) != cudaSuccess)
+            return cuda_fail(e);
+    }
+    return FA_OK;
 }
 
 namespace {
@@ -491,15 +523,14 @@ int fa_prefill_backward(const void *q, const void *k, const void *v, const void 
 
 int fa_prefill_ex(const void *q, const void *k, const void *v, void *out, int B, int H, int N,
                   int d, int causal, float scale, fa_dtype in_dtype, fa_dtype out_dtype,
-                  unsigned flags, void *stream) {
-    return fa_prefill_gqa(q, k, v, out, B, H, H, N, N, d, causal, scale, in_dtype, out_dtype, flags,
-                          stream);
+                  void *stream) {
+    return fa_prefill_gqa(q, k, v, out, B, H, H, N, N, d, causal, scale, in_dtype, out_dtype,
+                          FA_FLAG_NONE, stream);
 }
 
 int fa_prefill(const void *q, const void *k, const void *v, void *out, int B, int H, int N, int d,
                int causal, float scale, void *stream) {
-    return fa_prefill_ex(q, k, v, out, B, H, N, d, causal, scale, FA_F16, FA_F16, FA_FLAG_NONE,
-                         stream);
+    return fa_prefill_ex(q, k, v, out, B, H, N, d, causal, scale, FA_F16, FA_F16, stream);
 }
 
 int fa_decode_chunk_len(int max_len, int num_splits) {
@@ -514,12 +545,6 @@ namespace {
 // longer than 512 rows, so that ragged lengths do not leave a few long CTAs
 // running alone at the end.
 int choose_splits(int B, long long rows, int max_len, int num_sms, int per_sm) {
-    if (num_sms <= 0) {
-        DeviceInfo dev;
-        int rc = current_device_info(&dev);
-        if (rc != FA_OK) return -rc;
-        num_sms = dev.num_sms;
-    }
     long long splits = ceil_div(static_cast<long long>(per_sm) * num_sms, B * rows);
     const long long max_splits = ceil_div(max_len, kDecodeRowAlign);
     const long long min_splits = ceil_div(max_len, kDecodeAutoMaxChunk);
@@ -530,19 +555,38 @@ int choose_splits(int B, long long rows, int max_len, int num_sms, int per_sm) {
 }
 }  // namespace
 
-int fa_decode_choose_splits(int B, int H, int max_len, int num_sms) {
-    if (B < 1 || H < 1 || max_len < 1) return -FA_ERR_SHAPE;
-    return choose_splits(B, H, max_len, num_sms, 2);
-}
-
-int fa_decode_gqa_choose_splits(int B, int Hq, int Hkv, int max_len, int num_sms) {
-    if (B < 1 || Hq < 1 || Hkv < 1 || max_len < 1 || Hq % Hkv != 0) return -FA_ERR_SHAPE;
+int fa_decode_splits_for_sms(int B, int Hq, int Hkv, int max_len, int num_sms) {
+    if (B < 1 || Hq < 1 || Hkv < 1 || max_len < 1 || Hq % Hkv != 0 || num_sms < 1)
+        return -FA_ERR_SHAPE;
     if (Hq == Hkv) return choose_splits(B, Hq, max_len, num_sms, 2);
     // A grouped CTA does up to 8 heads' arithmetic per row it loads, so it is
     // latency- rather than bandwidth-bound: aim for about 5 CTAs per SM
     // (measured best at B = 8 and 32 with 14 query over 2 cache heads).
     const long long rows = static_cast<long long>(Hkv) * decode_group_slices(Hq / Hkv);
     return choose_splits(B, rows, max_len, num_sms, 5);
+}
+
+namespace {
+// SM count of a device ordinal (< 0: the current device), or a negative status.
+int device_sms(int device) {
+    cudaError_t e;
+    if (device < 0 && (e = cudaGetDevice(&device)) != cudaSuccess) return -cuda_fail(e);
+    int sms = 0;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device)) != cudaSuccess)
+        return -cuda_fail(e);
+    return sms;
+}
+}  // namespace
+
+int fa_decode_gqa_choose_splits(int B, int Hq, int Hkv, int max_len, int device) {
+    if (B < 1 || Hq < 1 || Hkv < 1 || max_len < 1 || Hq % Hkv != 0) return -FA_ERR_SHAPE;
+    const int sms = device_sms(device);
+    if (sms < 0) return sms;
+    return fa_decode_splits_for_sms(B, Hq, Hkv, max_len, sms);
+}
+
+int fa_decode_choose_splits(int B, int H, int max_len, int device) {
+    return fa_decode_gqa_choose_splits(B, H, H, max_len, device);
 }
 
 size_t fa_decode_workspace_bytes(int B, int H, int max_len, int d, int num_splits) {
@@ -580,7 +624,7 @@ int fa_decode_gqa(const void *q, const void *k_cache, const void *v_cache, const
 
     int splits = num_splits;
     if (splits == 0) {
-        splits = fa_decode_gqa_choose_splits(B, Hq, Hkv, max_len, 0);
+        splits = fa_decode_gqa_choose_splits(B, Hq, Hkv, max_len, -1);
         if (splits < 0) return -splits;
     }
     int chunk = 0;

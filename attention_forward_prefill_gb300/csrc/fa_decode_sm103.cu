@@ -32,7 +32,9 @@ constexpr int kSplitWarps = kSplitThreads / 32;
 constexpr int kUnroll = 8;
 constexpr int kMergeWarps = 4;
 
-__device__ int g_decode_status = 0;  // reserved for device-side waits; the decode kernels have none
+// Device status word of the decode kernels: FA_ERR_SEQ_LEN once a length
+// outside [0, max_len] has been clamped (the decode kernels have no waits).
+__device__ int g_decode_status = 0;
 
 struct DParams {
     const uint16_t *q;
@@ -404,7 +406,11 @@ __global__ void __launch_bounds__(kMergeWarps * 32)
     // they are read before the wait.
     int n_act = 0;
     if (live) {
-        const int len = clamp_len(p.seq_lens[gw / p.H], p.max_len);
+        const int raw = p.seq_lens[gw / p.H];
+        // one report per sequence (its first head); the length is clamped either way
+        if (lane == 0 && gw % p.H == 0 && (raw < 0 || raw > p.max_len))
+            atomicCAS(&g_decode_status, 0, static_cast<int>(FA_ERR_SEQ_LEN));
+        const int len = clamp_len(raw, p.max_len);
         n_act = (len + p.chunk - 1) / p.chunk;
     }
     // Wait until the split kernel has completed and its partials are visible.
@@ -462,6 +468,42 @@ __global__ void __launch_bounds__(kMergeWarps * 32)
         __half *out = reinterpret_cast<__half *>(p.out) + off;
 #pragma unroll
         for (int e = 0; e < EPL; ++e) out[e] = __float2half_rn(o[e]);
+    }
+}
+
+// Read-bandwidth probe: every thread streams 16-byte words with the split
+// kernel's non-caching load, four in flight, over a grid-stride loop; the XOR
+// of all words is the result, so no load can be dropped.
+constexpr int kProbeThreads = 512;
+constexpr int kProbeUnroll = 4;
+
+__global__ void __launch_bounds__(kProbeThreads) read_probe_kernel(const uint4 *src, size_t n16,
+                                                                   uint32_t *xor_out) {
+    __shared__ uint32_t red[kProbeThreads / 32];
+    const size_t stride = static_cast<size_t>(gridDim.x) * kProbeThreads;
+    size_t i = static_cast<size_t>(blockIdx.x) * kProbeThreads + threadIdx.x;
+    uint32_t x = 0;
+    for (; i + (kProbeUnroll - 1) * stride < n16; i += kProbeUnroll * stride) {
+        uint4 r[kProbeUnroll];
+#pragma unroll
+        for (int u = 0; u < kProbeUnroll; ++u)
+            r[u] = ldg_stream(reinterpret_cast<const uint16_t *>(src + i + u * stride));
+#pragma unroll
+        for (int u = 0; u < kProbeUnroll; ++u) x ^= r[u].x ^ r[u].y ^ r[u].z ^ r[u].w;
+    }
+    for (; i < n16; i += stride) {
+        const uint4 r = ldg_stream(reinterpret_cast<const uint16_t *>(src + i));
+        x ^= r.x ^ r.y ^ r.z ^ r.w;
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) x ^= __shfl_xor_sync(0xffffffffu, x, off);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = x;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        uint32_t t = 0;
+#pragma unroll
+        for (int w = 0; w < kProbeThreads / 32; ++w) t ^= red[w];
+        atomicXor(xor_out, t);
     }
 }
 
@@ -550,6 +592,18 @@ int launch_decode(const DecodeLaunch &a, const DeviceInfo &dev, cudaStream_t str
     return FA_ERR_HEAD_DIM;
 }
 
+int launch_read_probe(const void *src, size_t bytes, uint32_t *xor_out, const DeviceInfo &dev,
+                      cudaStream_t stream) {
+    cudaError_t e = cudaMemsetAsync(xor_out, 0, sizeof(uint32_t), stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+    // four CTAs of 512 threads per SM: 2048 resident threads, 128 KB of loads in flight
+    read_probe_kernel<<<dev.num_sms * 4, kProbeThreads, 0, stream>>>(static_cast<const uint4 *>(src),
+                                                                      bytes / 16, xor_out);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e);
+    return FA_OK;
+}
+
 }  // namespace fa
 
 // ---------------------------------------------------------------------------
@@ -568,21 +622,22 @@ namespace {
 constexpr size_t kNoAllocScratchBytes = size_t(4) << 20;  // 4 MiB
 static __device__ __align__(256) unsigned char g_decode_scratch[kNoAllocScratchBytes];
 
-constexpr int kMaxScratchDevices = 64;
 std::mutex g_scratch_mu;
-void *g_scratch_addr[kMaxScratchDevices] = {};
+void *g_scratch_addr[kMaxDevices] = {};
 
 // Device address of the static scratch on the current device (set up on the
-// first call per device, with that device current).
+// first call per device, with that device current).  The device and its
+// architecture are checked first, so that a wrong device reports FA_ERR_ARCH
+// as the allocating entry point does, not a failed symbol lookup.
 int noalloc_scratch(void **out) {
-    int dev = -1;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return cuda_fail(e);
-    if (dev < 0 || dev >= kMaxScratchDevices) return cuda_fail(cudaErrorInvalidDevice);
+    DeviceInfo info;
+    const int rc = current_device_info(&info);
+    if (rc != FA_OK) return rc;
+    const int dev = info.device;
     std::lock_guard<std::mutex> lk(g_scratch_mu);
     if (!g_scratch_addr[dev]) {
         void *p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_decode_scratch);
+        const cudaError_t e = cudaGetSymbolAddress(&p, g_decode_scratch);
         if (e != cudaSuccess) return cuda_fail(e);
         g_scratch_addr[dev] = p;
     }
@@ -605,7 +660,7 @@ extern "C" int fa_decode_noalloc(const void *q, const void *k_cache, const void 
     if (B >= 1 && H >= 1 && max_len >= 1 && (d == 64 || d == 128) && num_splits >= 0) {
         int splits = num_splits;
         if (splits == 0) {
-            splits = fa_decode_choose_splits(B, H, max_len, 0);
+            splits = fa_decode_choose_splits(B, H, max_len, -1);
             if (splits < 0) return -splits;
         }
         if (fa_decode_workspace_bytes(B, H, max_len, d, splits) > fa::kNoAllocScratchBytes)
@@ -617,4 +672,15 @@ extern "C" int fa_decode_noalloc(const void *q, const void *k_cache, const void 
     // With a workspace supplied, fa_decode_ex allocates nothing.
     return fa_decode_ex(q, k_cache, v_cache, seq_lens, out, B, H, max_len, d, scale, in_dtype,
                         out_dtype, num_splits, scratch, fa::kNoAllocScratchBytes, stream);
+}
+
+extern "C" int fa_read_probe(const void *src, size_t bytes, uint32_t *xor_out, void *stream) {
+    if (!src || !xor_out) return FA_ERR_NULL;
+    if ((reinterpret_cast<uintptr_t>(src) & 15u) || (reinterpret_cast<uintptr_t>(xor_out) & 3u))
+        return FA_ERR_ALIGN;
+    if (bytes == 0 || bytes % 16 != 0) return FA_ERR_SHAPE;
+    fa::DeviceInfo dev;
+    const int rc = fa::current_device_info(&dev);
+    if (rc != FA_OK) return rc;
+    return fa::launch_read_probe(src, bytes, xor_out, dev, static_cast<cudaStream_t>(stream));
 }

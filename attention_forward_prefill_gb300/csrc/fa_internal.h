@@ -10,6 +10,10 @@
 
 namespace fa {
 
+// Per-device state (attribute cache, scratch pool, copy streams, the static
+// decode scratch address) is kept for device ordinals below this bound.
+constexpr int kMaxDevices = 64;
+
 struct DeviceInfo {
     int device = -1;
     int num_sms = 0;
@@ -75,6 +79,10 @@ struct DecodeLaunch {
 };
 
 int launch_decode(const DecodeLaunch &a, const DeviceInfo &dev, cudaStream_t stream);
+
+// Streaming-read probe over `bytes` (a multiple of 16) with the decode loads.
+int launch_read_probe(const void *src, size_t bytes, uint32_t *xor_out, const DeviceInfo &dev,
+                      cudaStream_t stream);
 
 struct BackwardLaunch {
     const void *q, *k, *v, *out, *dout;  // q, out, dout [B][H][N][d]; k, v [B][Hkv][N][d] 16-bit

@@ -159,7 +159,8 @@ __device__ __forceinline__ int kv_tiles(int causal, int no_skip, int nq, int nk,
     return min(tk, last / kBlockN + 1);
 }
 
-// Fill sequence fields of w from (b, h).
+// Fill sequence fields of w from (b, h).  Packed offsets are clamped into the
+// tensors (check_seq reports values that needed it).
 __device__ __forceinline__ void load_seq(const Params &p, Work &w) {
     w.hk = w.h / p.group;
     if (p.cu_q) {
@@ -178,6 +179,17 @@ __device__ __forceinline__ void load_seq(const Params &p, Work &w) {
         w.nk = p.Nk;
     }
     w.off = w.nk - w.nq;
+}
+
+// Packed batch: record FA_ERR_SEQ_LEN when sequence w.b's offsets had to be
+// clamped (outside [0, total] or decreasing) or a length exceeds the stated
+// maximum.  Run by the producer thread only, for every unit it visits.
+__device__ __forceinline__ void check_seq(const Params &p, const Work &w) {
+    const int q0 = __ldg(p.cu_q + w.b), q1 = __ldg(p.cu_q + w.b + 1);
+    const int k0 = __ldg(p.cu_k + w.b), k1 = __ldg(p.cu_k + w.b + 1);
+    const bool bad = q0 < 0 || q1 < q0 || q1 > p.total_q || q1 - q0 > p.Nq || k0 < 0 || k1 < k0 ||
+                     k1 > p.total_k || k1 - k0 > p.Nk;
+    if (bad) atomicCAS(&g_prefill_status, 0, static_cast<int>(FA_ERR_SEQ_LEN));
 }
 
 __device__ __forceinline__ bool seg_next(const Params &p, const StepTable &tab, SegCursor &c,
@@ -334,6 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             };
             while (ok && seg_next(p, tab, cur, w)) {
+                if (packed) check_seq(p, w);
                 if (w.j1 <= w.j0) continue;  // no key tiles: the softmax warps write zeros
                 // query tile t is loaded when it has key tiles in [j0, j1)
                 const bool need0 = min(w.n0, w.j1) > w.j0, need1 = min(w.n1, w.j1) > w.j0;
@@ -639,7 +652,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 const uint64_t c2 = f2_pack(cexp, cexp);
                 const uint64_t nm2 = f2_pack(neg_m, neg_m);
-                uint64_t sum2[4] = {0, 0, 0, 0};
+                // eight fp32 partial sums: (lo, hi) halves of four pair slots
+                float sum_lo[4] = {0.f, 0.f, 0.f, 0.f}, sum_hi[4] = {0.f, 0.f, 0.f, 0.f};
                 // P in 32-key quarters: 16 packed registers per TMEM store.
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
@@ -652,11 +666,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                         pk[c2i] = pack2t<BF16>(ex2_approx(f2_lo(x)), ex2_approx(f2_hi(x)));
                         // l sums the same rounded weights the PV product uses,
                         // so a row dominated by one key returns that value row.
-                        sum2[c2i & 3] = fadd2(sum2[c2i & 3], unpack2<BF16>(pk[c2i]));
+                        // Each 16-bit weight is added straight into fp32.
+                        add_pair16<BF16>(sum_lo[c2i & 3], sum_hi[c2i & 3], pk[c2i]);
                     }
                     tmem_st16(p_addr + q * 16, pk);
                 }
-                const uint64_t s01 = fadd2(sum2[0], sum2[1]), s23 = fadd2(sum2[2], sum2[3]);
+                const uint64_t s01 = fadd2(f2_pack(sum_lo[0], sum_hi[0]), f2_pack(sum_lo[1], sum_hi[1]));
+                const uint64_t s23 = fadd2(f2_pack(sum_lo[2], sum_hi[2]), f2_pack(sum_lo[3], sum_hi[3]));
                 const uint64_t st = fadd2(s01, s23);
                 l += f2_lo(st) + f2_hi(st);
                 if (j > j0 && __any_sync(0xffffffffu, need)) {
@@ -880,6 +896,37 @@ __global__ void __launch_bounds__(256) prefill_fixup(const __grid_constant__ Fix
             for (int e = 0; e < CPL; e += 2) dst[e / 2] = pack2(acc[r][e] * inv, acc[r][e + 1] * inv, bf);
         }
     }
+}
+
+// ---------------------------------------------------------------- watchdog self-test
+// Two warps wait on barriers that nothing completes: warp 0 with a short
+// limit (suspending between polls, as mbar_wait does everywhere), warp 1
+// polling (as mbar_spin does for the MMA issuer) with the kernels' own limit,
+// which it must abandon once warp 0 raises the abort flag.  The exit path is
+// the attention kernel's: a raised flag becomes FA_ERR_WATCHDOG.
+__global__ void __launch_bounds__(64, 1) watchdog_selftest_kernel(long long limit_ns, long long *result) {
+    __shared__ __align__(8) uint64_t bars[2];
+    __shared__ int abort_word;
+    volatile int *abort_flag = &abort_word;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        mbar_init(bars + 0, 1);
+        mbar_init(bars + 1, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (lane == 0) {
+        const uint64_t t0 = globaltimer_ns();
+        // phase 0 of a fresh barrier completes only after an arrival: never here
+        const bool done = warp == 0 ? mbar_wait(bars + 0, 0, abort_flag, static_cast<uint64_t>(limit_ns))
+                                    : mbar_spin(bars + 1, 0, abort_flag, kWatchdogNs);
+        const uint64_t t1 = globaltimer_ns();
+        result[warp] = done ? 0 : 1;
+        result[2 + warp] = static_cast<long long>(t1 - t0);
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 && *abort_flag) atomicCAS(&g_prefill_status, 0, (int)FA_ERR_WATCHDOG);
 }
 
 // ---------------------------------------------------------------- host side
@@ -1185,3 +1232,16 @@ int read_prefill_status(int reset) {
 }
 
 }  // namespace fa
+
+extern "C" int fa_watchdog_selftest(long long limit_ns, long long *result, void *stream) {
+    if (!result) return FA_ERR_NULL;
+    if (reinterpret_cast<uintptr_t>(result) & 7u) return FA_ERR_ALIGN;
+    if (limit_ns < 1000 || limit_ns > 1000000000LL) return FA_ERR_SHAPE;
+    fa::DeviceInfo dev;
+    const int rc = fa::current_device_info(&dev);
+    if (rc != FA_OK) return rc;
+    fa::watchdog_selftest_kernel<<<1, 64, 0, static_cast<cudaStream_t>(stream)>>>(limit_ns, result);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fa::cuda_fail(e);
+    return FA_OK;
+}

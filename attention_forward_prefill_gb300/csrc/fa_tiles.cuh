@@ -64,6 +64,27 @@ __device__ __forceinline__ uint64_t unpack2(uint32_t w) {
     }
 }
 
+// lo += w.lo, hi += w.hi for the two 16-bit values of a packed pair, each
+// widened exactly inside a mixed-precision add (sm_100+), round to nearest.
+template <bool BF16>
+__device__ __forceinline__ void add_pair16(float &lo, float &hi, uint32_t w) {
+    if constexpr (BF16) {
+        asm("{\n\t.reg .b16 a, b;\n\t"
+            "mov.b32 {a, b}, %2;\n\t"
+            "add.rn.f32.bf16 %0, a, %0;\n\t"
+            "add.rn.f32.bf16 %1, b, %1;\n\t}"
+            : "+f"(lo), "+f"(hi)
+            : "r"(w));
+    } else {
+        asm("{\n\t.reg .b16 a, b;\n\t"
+            "mov.b32 {a, b}, %2;\n\t"
+            "add.rn.f32.f16 %0, a, %0;\n\t"
+            "add.rn.f32.f16 %1, b, %1;\n\t}"
+            : "+f"(lo), "+f"(hi)
+            : "r"(w));
+    }
+}
+
 template <bool BF16>
 __device__ __forceinline__ uint32_t pack2t(float lo, float hi) {
     if constexpr (BF16) {

@@ -200,7 +200,7 @@ def run_ours(args):
     l2 = torch.cuda.get_device_properties(device).L2_cache_size
     flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=device)
     stream = torch.cuda.current_stream(device)
-    splits = binding.fa_decode_choose_splits(DECODE_B, DECODE_H, DECODE_L, 0)
+    splits = binding.fa_decode_choose_splits(DECODE_B, DECODE_H, DECODE_L, -1)
     ws = torch.empty(binding.fa_decode_workspace_bytes(DECODE_B, DECODE_H, DECODE_L, DECODE_D,
                                                        splits), dtype=torch.uint8, device=device)
     cases = args.case.split(",") if args.case else None
@@ -528,7 +528,7 @@ def measure_configs(torch, binding, device, stream, flush, peaks, reps=7):
             lens_np = fin.seq_lens(fin.seed_for(3, fin.TENSOR_SEQLEN) + B, B, DECODE_L)
             lens = torch.from_numpy(lens_np).to(device)
             out = torch.empty_like(dq)
-            splits = binding.fa_decode_choose_splits(B, H, DECODE_L, 0)
+            splits = binding.fa_decode_choose_splits(B, H, DECODE_L, -1)
             ws = torch.empty(binding.fa_decode_workspace_bytes(B, H, DECODE_L, DECODE_D, splits),
                              dtype=torch.uint8, device=device)
 
@@ -552,7 +552,7 @@ def measure_configs(torch, binding, device, stream, flush, peaks, reps=7):
         lens_np = fin.seq_lens(fin.seed_for(3, fin.TENSOR_SEQLEN) + B, B, DECODE_L)
         lens = torch.from_numpy(lens_np).to(device)
         out = torch.empty_like(dq)
-        splits = binding.fa_decode_gqa_choose_splits(B, Hq, Hkv, DECODE_L, 0)
+        splits = binding.fa_decode_gqa_choose_splits(B, Hq, Hkv, DECODE_L, -1)
         ws = torch.empty(binding.fa_decode_workspace_bytes(B, Hq, DECODE_L, DECODE_D, splits),
                          dtype=torch.uint8, device=device)
 

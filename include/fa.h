@@ -54,11 +54,13 @@ typedef enum {
     FA_ERR_WORKSPACE = 8,  /* caller workspace too small, or allocation failed    */
     FA_ERR_CUDA = 9,       /* a CUDA runtime call failed: see fa_last_cuda_error  */
     FA_ERR_WATCHDOG = 10,  /* a device-side wait ran out (see fa_device_status)   */
-    FA_ERR_ALIAS = 11,     /* out overlaps an input                               */
-    FA_ERR_SPLITS = 12     /* num_splits outside [0, ceil(max_len / 64)]          */
+    FA_ERR_SEQ_LEN = 11,   /* a device-resident length was out of range and was
+                              clamped (reported by fa_device_status only)         */
+    FA_ERR_ALIAS = 12,     /* out overlaps an input                               */
+    FA_ERR_SPLITS = 13     /* num_splits outside [0, ceil(max_len / 64)]          */
 } fa_status;
 
-/* Flags for fa_prefill_ex. */
+/* Flags for fa_prefill_gqa and the other prefill forms that take `flags`. */
 #define FA_FLAG_NONE 0u
 /* Causal only: run the key-tile loop over every tile instead of stopping at
  * the diagonal (tiles above it are then fully masked).  The result must be
@@ -94,18 +96,19 @@ int fa_prefill(const void *q, const void *k, const void *v, void *out,
                void *stream);
 
 /*
- * Prefill with explicit dtypes and flags.
+ * Prefill with explicit dtypes (the configurations need bf16 in / bf16 out
+ * and fp16 in / fp32 out besides the plain fp16 form).
  *   in_dtype  : FA_F16 or FA_BF16 (q, k and v share it)
  *   out_dtype : FA_F16, FA_BF16 or FA_F32 (rounded to nearest even)
- *   flags     : FA_FLAG_* bits
- * Large problems may take a stream-ordered scratch buffer (at most
- * SMs x 2 x 256 x d x 4 bytes plus 8 bytes per row of it) from the library's
- * device memory pool; FA_ERR_WORKSPACE if that allocation fails.
+ * Other arguments as fa_prefill.  The library picks the work schedule; the
+ * schedule flags are taken by fa_prefill_gqa.  Large problems may take a
+ * stream-ordered scratch buffer (at most SMs x 2 x 256 x d x 4 bytes plus 8
+ * bytes per row of it) from the library's device memory pool;
+ * FA_ERR_WORKSPACE if that allocation fails.
  */
 int fa_prefill_ex(const void *q, const void *k, const void *v, void *out,
                   int B, int H, int N, int d, int causal, float scale,
-                  fa_dtype in_dtype, fa_dtype out_dtype, unsigned flags,
-                  void *stream);
+                  fa_dtype in_dtype, fa_dtype out_dtype, void *stream);
 
 /*
  * Prefill with grouped key/value heads and separate query / key lengths
@@ -118,6 +121,7 @@ int fa_prefill_ex(const void *q, const void *k, const void *v, void *out,
  *   causal : the queries are the last Nq positions: query i sees keys
  *            j <= i + (Nk - Nq).  When Nq > Nk the first Nq - Nk rows see no
  *            key and are written as zeros.
+ *   flags  : FA_FLAG_* bits (schedule choice and the causal-skip check)
  * Other arguments as fa_prefill_ex.  Errors: FA_ERR_SHAPE when a size is < 1,
  * Hq % Hkv != 0 or an element count exceeds INT_MAX; the others as above.
  */
@@ -219,7 +223,9 @@ int fa_prefill_plan(int B, int Hq, int Nq, int Nk, int causal, unsigned flags,
  *   cu_seqlens_q, cu_seqlens_k : int32 device arrays of B + 1 non-decreasing
  *                 offsets from 0 to total_q / total_k (4-byte aligned).  The
  *                 kernel clamps them to [0, total], so a bad array cannot make
- *                 it write outside `out`.
+ *                 it write outside `out`; an offset outside [0, total], a
+ *                 decreasing pair or a length above max_seqlen_* is recorded as
+ *                 FA_ERR_SEQ_LEN in the device status word (fa_device_status).
  *   max_seqlen_q, max_seqlen_k : host upper bounds of the per-sequence
  *                 lengths; rows past max_seqlen_q of a longer sequence are
  *                 left unwritten and keys past max_seqlen_k are ignored.
@@ -247,7 +253,11 @@ int fa_prefill_varlen(const void *q, const void *k, const void *v, void *out,
  *   k_cache, v_cache : fp16 [B][H][max_len][d]
  *   seq_lens : int32 device array [B]; precondition 1 <= seq_lens[b] <= max_len.
  *              Values are clamped to [0, max_len]; a length of 0 yields a zero
- *              output row.
+ *              output row.  A value outside [0, max_len] is recorded as
+ *              FA_ERR_SEQ_LEN in the device status word, read (and cleared) by
+ *              fa_device_status; the call itself has already returned FA_OK,
+ *              since the lengths stay on the device.  The check runs in every
+ *              build: it is one compare per (b, h) in the merge kernel.
  *   out      : fp16 [B][H][1][d]
  *   d        : 64 or 128
  * The split count is chosen from (B, H, max_len, SM count) only, never from
@@ -280,11 +290,21 @@ int fa_decode_ex(const void *q, const void *k_cache, const void *v_cache,
  * The automatic split count ("Kernel design" table: choose_decode_split
  * targets about two resident blocks per SM): enough (b, h, chunk) CTAs for
  * two per SM, and chunks of at most 512 rows so that ragged lengths do not
- * leave a few long CTAs running alone.  Pure host arithmetic on its
- * arguments; num_sms <= 0 means "the current device's SM count".
- * Returns the split count (>= 1), or a negative fa_status on bad arguments.
+ * leave a few long CTAs running alone.  Host arithmetic on the arguments and
+ * the SM count of `device` (a CUDA device ordinal; < 0 = the current device).
+ * Returns the split count (>= 1), or a negative fa_status: -FA_ERR_SHAPE on
+ * bad sizes, -FA_ERR_CUDA if the device cannot be queried.
  */
-int fa_decode_choose_splits(int B, int H, int max_len, int num_sms);
+int fa_decode_choose_splits(int B, int H, int max_len, int device);
+
+/*
+ * The split count that fa_decode_gqa would choose on a GPU with num_sms SMs
+ * (Hq == Hkv: plain multi-head decode, the rule of fa_decode_choose_splits).
+ * Pure host arithmetic, for tuning and tests; nothing touches a device.
+ * Returns the split count, or -FA_ERR_SHAPE on bad arguments (num_sms < 1
+ * included).
+ */
+int fa_decode_splits_for_sms(int B, int Hq, int Hkv, int max_len, int num_sms);
 
 /* Keys per chunk for a given split count: round_up(ceil(max_len/splits), 64). */
 int fa_decode_chunk_len(int max_len, int num_splits);
@@ -303,7 +323,7 @@ size_t fa_decode_workspace_bytes(int B, int H, int max_len, int d,
  *             the same kernels as fa_decode_ex)
  *   workspace : NULL or at least fa_decode_workspace_bytes(B, Hq, max_len, d,
  *             splits) bytes, splits being num_splits or, for 0, the value of
- *             fa_decode_gqa_choose_splits(B, Hq, Hkv, max_len, 0)
+ *             fa_decode_gqa_choose_splits(B, Hq, Hkv, max_len, -1)
  * Other arguments, results and errors as fa_decode_ex; in addition
  * FA_ERR_SHAPE when Hq % Hkv != 0, and FA_ERR_SPLITS when a chunk would need
  * more than 192 KB of shared memory for the scores of its query heads
@@ -315,9 +335,9 @@ int fa_decode_gqa(const void *q, const void *k_cache, const void *v_cache,
                   fa_dtype in_dtype, fa_dtype out_dtype, int num_splits,
                   void *workspace, size_t workspace_bytes, void *stream);
 
-/* Split count fa_decode_gqa uses for num_splits == 0 (negative fa_status on
- * bad arguments; num_sms <= 0 queries the current device). */
-int fa_decode_gqa_choose_splits(int B, int Hq, int Hkv, int max_len, int num_sms);
+/* Split count fa_decode_gqa uses for num_splits == 0 on `device` (< 0 = the
+ * current device); a negative fa_status as for fa_decode_choose_splits. */
+int fa_decode_gqa_choose_splits(int B, int Hq, int Hkv, int max_len, int device);
 
 /*
  * Decode that allocates nothing.  The pages have no counterpart: this entry
@@ -356,10 +376,55 @@ const char *fa_status_string(int status);
 /* The cudaError_t behind the calling thread's last FA_ERR_CUDA (0 if none). */
 int fa_last_cuda_error(void);
 
-/* Device-side status word of the current device: 0 or FA_ERR_WATCHDOG after a
- * kernel's bounded wait ran out.  Synchronises the device.  If reset is
- * nonzero the word is cleared.  Returns a negative value if it cannot be read. */
+/* Device-side status word of the current device: 0, FA_ERR_WATCHDOG after a
+ * kernel's bounded wait ran out (this wins when both were recorded), or
+ * FA_ERR_SEQ_LEN after a kernel clamped a device-resident length.
+ * Synchronises the device.  If reset is nonzero the word is cleared.  Returns
+ * a negative value if it cannot be read. */
 int fa_device_status(int reset);
+
+/* ---------------------------------------------------------------- diagnostics
+ * The calls below have no counterpart in the pages: they exist to test the
+ * library's failure detection and its memory use, and to measure the GPU. */
+
+/*
+ * Self-test of the bounded waits behind FA_ERR_WATCHDOG.  Launches one CTA of
+ * two warps on `stream`.  Warp 0 waits, suspending between polls, on a
+ * shared-memory barrier that nothing ever completes, for at most `limit_ns`;
+ * warp 1 polls another such barrier with the kernels' own limit (1.5 s) and
+ * must give up as soon as warp 0's timeout raises the CTA's abort flag.  The
+ * CTA then records FA_ERR_WATCHDOG in the device status word exactly as the
+ * attention kernels do at exit.  Nothing else is in flight, so the context
+ * stays usable.
+ *   limit_ns : 1e3 .. 1e9
+ *   result   : device array of 4 int64 (8-byte aligned), written as
+ *              [0] 1 if warp 0's wait reported a timeout, [1] 1 if warp 1's
+ *              wait returned early on the abort flag, [2] and [3] the
+ *              nanoseconds warps 0 and 1 waited (%globaltimer).
+ * Errors: FA_ERR_NULL, FA_ERR_ALIGN, FA_ERR_SHAPE (limit out of range),
+ * FA_ERR_ARCH, FA_ERR_CUDA.
+ */
+int fa_watchdog_selftest(long long limit_ns, long long *result, void *stream);
+
+/*
+ * Bytes of the library's stream-ordered scratch pool on the current device:
+ * out[0] reserved now, out[1] reserved high-water mark, out[2] in use now,
+ * out[3] in-use high-water mark; all 0 when the pool has never been used on
+ * this device (nothing is created by this call).  With reset_high nonzero
+ * both high-water marks are reset after they are read.  Does not
+ * synchronise: sizes of stream-ordered work not yet run are not counted.
+ */
+int fa_pool_stats(long long *out, int reset_high);
+
+/*
+ * Read-bandwidth probe: streams `bytes` (a positive multiple of 16) from the
+ * device buffer `src` (16-byte aligned) with the decode kernels' 16-byte
+ * non-caching loads, over a grid sized to the SM count, and stores the XOR of
+ * all its 32-bit words in *xor_out (device, 4-byte aligned; it is first set
+ * to 0 on `stream`).  The XOR lets a caller check that every byte was read.
+ * Errors: FA_ERR_NULL, FA_ERR_ALIGN, FA_ERR_SHAPE, FA_ERR_ARCH, FA_ERR_CUDA.
+ */
+int fa_read_probe(const void *src, size_t bytes, uint32_t *xor_out, void *stream);
 
 /* ABI version: major * 10000 + minor * 100 + patch. */
 int fa_version(void);

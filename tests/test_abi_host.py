@@ -33,11 +33,76 @@ def test_every_declared_symbol_is_exported(lib):
     assert set(binding._SIGNATURES) >= set(names)
 
 
+def declarations():
+    """{name: (return type, [parameter declarations])} from include/fa.h."""
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    out = {}
+    for m in re.finditer(r"([A-Za-z_][\w \*]*?)\b(fa_\w+)\s*\(([^)]*)\)\s*;", text):
+        ret = re.sub(r"\s+", " ", m.group(1)).replace(" *", "*").strip()
+        params = [re.sub(r"\s+", " ", x).replace(" *", "* ").replace("* ", "*").strip()
+                  for x in m.group(3).split(",")]
+        out[m.group(2)] = (ret, params)
+    return out
+
+
+# The boundary as the survey's hot-path table lists it, call for call.
+BOUNDARY = {
+    "fa_prefill": ("int", ["const void*q", "const void*k", "const void*v", "void*out", "int B",
+                           "int H", "int N", "int d", "int causal", "float scale", "void*stream"]),
+    "fa_prefill_ex": ("int", ["const void*q", "const void*k", "const void*v", "void*out", "int B",
+                              "int H", "int N", "int d", "int causal", "float scale",
+                              "fa_dtype in_dtype", "fa_dtype out_dtype", "void*stream"]),
+    "fa_decode": ("int", ["const void*q", "const void*k_cache", "const void*v_cache",
+                          "const int32_t*seq_lens", "void*out", "int B", "int H", "int max_len",
+                          "int d", "float scale", "void*stream"]),
+    "fa_decode_ex": ("int", ["const void*q", "const void*k_cache", "const void*v_cache",
+                             "const int32_t*seq_lens", "void*out", "int B", "int H", "int max_len",
+                             "int d", "float scale", "fa_dtype in_dtype", "fa_dtype out_dtype",
+                             "int num_splits", "void*workspace", "size_t workspace_bytes",
+                             "void*stream"]),
+    "fa_decode_choose_splits": ("int", ["int B", "int H", "int max_len", "int device"]),
+    "fa_decode_workspace_bytes": ("size_t", ["int B", "int H", "int max_len", "int d",
+                                             "int num_splits"]),
+    "fa_status_string": ("const char*", ["int status"]),
+    "fa_last_cuda_error": ("int", ["void"]),
+}
+
+
+def test_header_matches_the_boundary_call_for_call():
+    decl = declarations()
+    for name, (ret, params) in BOUNDARY.items():
+        assert name in decl, name
+        assert decl[name] == (ret, params), (name, decl[name])
+    text = open(HEADER).read()
+    want = ["FA_OK = 0", "FA_ERR_NULL = 1", "FA_ERR_SHAPE = 2", "FA_ERR_HEAD_DIM = 3",
+            "FA_ERR_DTYPE = 4", "FA_ERR_ALIGN = 5", "FA_ERR_SCALE = 6", "FA_ERR_ARCH = 7",
+            "FA_ERR_WORKSPACE = 8", "FA_ERR_CUDA = 9", "FA_ERR_WATCHDOG = 10",
+            "FA_ERR_SEQ_LEN = 11"]
+    for w in want:
+        assert w in text, w
+    assert "FA_F16 = 0, FA_BF16 = 1, FA_F32 = 2" in text
+    for code, name in binding.STATUS_NAMES.items():
+        assert f"{name} = {code}" in text
+
+
+def test_diagnostic_calls_check_arguments_first(lib):
+    assert binding.fa_watchdog_selftest(1_000_000, None, None) == binding.FA_ERR_NULL
+    assert binding.fa_watchdog_selftest(1_000_000, A + 4, None) == binding.FA_ERR_ALIGN
+    assert binding.fa_watchdog_selftest(10, A, None) == binding.FA_ERR_SHAPE
+    assert binding.fa_watchdog_selftest(2_000_000_000, A, None) == binding.FA_ERR_SHAPE
+    assert binding.fa_read_probe(None, 16, A, None) == binding.FA_ERR_NULL
+    assert binding.fa_read_probe(A + 8, 16, A, None) == binding.FA_ERR_ALIGN
+    assert binding.fa_read_probe(A, 16, A + 2, None) == binding.FA_ERR_ALIGN
+    assert binding.fa_read_probe(A, 0, A, None) == binding.FA_ERR_SHAPE
+    assert binding.fa_read_probe(A, 24, A, None) == binding.FA_ERR_SHAPE
+    assert binding.load().fa_pool_stats(None, 0) == binding.FA_ERR_NULL
+
+
 def test_status_strings_and_version(lib):
-    for code in range(13):
+    for code in range(14):
         assert binding.status_string(code) != "unknown status"
     assert binding.status_string(999) == "unknown status"
-    assert binding.fa_version() >= 10000
+    assert binding.fa_version() >= 20000
 
 
 A = 1 << 20   # an aligned fake address: validation must reject before using it
@@ -45,23 +110,23 @@ B_ = 1 << 28
 
 
 @pytest.mark.parametrize("args,status", [
-    ((None, A, A, B_, 1, 1, 1, 64, 0, 1.0, 0, 0, 0), 1),
-    ((A, A, A, B_, 0, 1, 1, 64, 0, 1.0, 0, 0, 0), 2),
-    ((A, A, A, B_, 1, 1, -3, 64, 0, 1.0, 0, 0, 0), 2),
-    ((A, A, A, B_, 65536, 65536, 2, 64, 0, 1.0, 0, 0, 0), 2),
-    ((A, A, A, B_, 1, 1, 1, 96, 0, 1.0, 0, 0, 0), 3),
-    ((A, A, A, B_, 1, 1, 1, 64, 0, 1.0, 2, 0, 0), 4),
-    ((A, A, A, B_, 1, 1, 1, 64, 0, 1.0, 0, 7, 0), 4),
-    ((A + 8, A, A, B_, 1, 1, 1, 64, 0, 1.0, 0, 0, 0), 5),
-    ((A, A, A, B_ + 2, 1, 1, 1, 64, 0, 1.0, 0, 0, 0), 5),
-    ((A, A, A, B_, 1, 1, 1, 64, 0, float("nan"), 0, 0, 0), 6),
-    ((A, A, A, B_, 1, 1, 1, 64, 0, float("inf"), 0, 0, 0), 6),
-    ((A, A, A, A, 1, 1, 1, 64, 0, 1.0, 0, 0, 0), 11),
-    ((A, A, A, A + 64, 1, 2, 8, 64, 0, 1.0, 0, 0, 0), 11),
+    ((None, A, A, B_, 1, 1, 1, 64, 0, 1.0, 0, 0), 1),
+    ((A, A, A, B_, 0, 1, 1, 64, 0, 1.0, 0, 0), 2),
+    ((A, A, A, B_, 1, 1, -3, 64, 0, 1.0, 0, 0), 2),
+    ((A, A, A, B_, 65536, 65536, 2, 64, 0, 1.0, 0, 0), 2),
+    ((A, A, A, B_, 1, 1, 1, 96, 0, 1.0, 0, 0), 3),
+    ((A, A, A, B_, 1, 1, 1, 64, 0, 1.0, 2, 0), 4),
+    ((A, A, A, B_, 1, 1, 1, 64, 0, 1.0, 0, 7), 4),
+    ((A + 8, A, A, B_, 1, 1, 1, 64, 0, 1.0, 0, 0), 5),
+    ((A, A, A, B_ + 2, 1, 1, 1, 64, 0, 1.0, 0, 0), 5),
+    ((A, A, A, B_, 1, 1, 1, 64, 0, float("nan"), 0, 0), 6),
+    ((A, A, A, B_, 1, 1, 1, 64, 0, float("inf"), 0, 0), 6),
+    ((A, A, A, A, 1, 1, 1, 64, 0, 1.0, 0, 0), binding.FA_ERR_ALIAS),
+    ((A, A, A, A + 64, 1, 2, 8, 64, 0, 1.0, 0, 0), binding.FA_ERR_ALIAS),
 ])
 def test_prefill_argument_errors(lib, args, status):
-    q, k, v, out, B, H, N, d, causal, scale, it, ot, fl = args
-    assert binding.fa_prefill_ex(q, k, v, out, B, H, N, d, causal, scale, it, ot, fl, None) == status
+    q, k, v, out, B, H, N, d, causal, scale, it, ot = args
+    assert binding.fa_prefill_ex(q, k, v, out, B, H, N, d, causal, scale, it, ot, None) == status
 
 
 @pytest.mark.parametrize("args,status", [
@@ -74,7 +139,7 @@ def test_prefill_argument_errors(lib, args, status):
     ((A, A, A, B_, 1, 4, 2, 8, 8, 64, 0, 1.0, 0, 3, 0), 4),
     ((A, A, A + 4, B_, 1, 4, 2, 8, 8, 64, 0, 1.0, 0, 0, 0), 5),
     ((A, A, A, B_, 1, 4, 2, 8, 8, 64, 0, float("-inf"), 0, 0, 0), 6),
-    ((A, B_ - 64, A, B_, 1, 4, 2, 8, 1024, 64, 0, 1.0, 0, 0, 0), 11),  # k runs into out
+    ((A, B_ - 64, A, B_, 1, 4, 2, 8, 1024, 64, 0, 1.0, 0, 0, 0), binding.FA_ERR_ALIAS),  # k runs into out
 ])
 def test_gqa_prefill_argument_errors(lib, args, status):
     assert binding.fa_prefill_gqa(*args, None) == status
@@ -89,7 +154,7 @@ def test_gqa_prefill_argument_errors(lib, args, status):
     ((A, A, A, B_, 1, 4, 2, 8, 8, 64, 0, 1.0, 2, 0, 0), 4),
     ((A, A, A + 8, B_, 1, 4, 2, 8, 8, 64, 0, 1.0, 0, 0, 0), 5),
     ((A, A, A, B_, 1, 4, 2, 8, 8, 64, 0, float("nan"), 0, 0, 0), 6),
-    ((A, A, A, A + 256, 1, 4, 2, 8, 8, 64, 0, 1.0, 0, 0, 0), 11),  # out inside q
+    ((A, A, A, A + 256, 1, 4, 2, 8, 8, 64, 0, 1.0, 0, 0, 0), binding.FA_ERR_ALIAS),  # out inside q
 ])
 def test_host_buffer_prefill_argument_errors(lib, args, status):
     # the host-buffer entry point validates like the device one, before any CUDA call
@@ -106,7 +171,7 @@ CU = 1 << 16
     ((A, A, A, B_, CU, CU, 0, 4, 2, 64, 64, 32, 32, 64, 1, 1.0, 0, 0, 0), 2),
     ((A, A, A, B_, CU, CU, 2, 4, 2, 64, -1, 32, 32, 64, 1, 1.0, 0, 0, 0), 2),
     ((A, A, A, B_, CU, CU, 2, 4, 2, 64, 64, 32, 32, 100, 1, 1.0, 0, 0, 0), 3),
-    ((A, A, A, A, CU, CU, 2, 4, 2, 64, 64, 32, 32, 64, 1, 1.0, 0, 0, 0), 11),
+    ((A, A, A, A, CU, CU, 2, 4, 2, 64, 64, 32, 32, 64, 1, 1.0, 0, 0, 0), binding.FA_ERR_ALIAS),
     # no query rows: nothing to do, and no device is touched
     ((A, A, A, B_, CU, CU, 2, 4, 2, 0, 64, 0, 32, 64, 1, 1.0, 0, 0, 0), 0),
 ])
@@ -129,26 +194,26 @@ def test_grouped_decode_argument_errors(lib):
     assert call(q=None) == 1
     assert call(d=32) == 3
     assert call(lens=L + 2) == 5
-    assert call(splits=4096 // 64 + 1) == 12
+    assert call(splits=4096 // 64 + 1) == binding.FA_ERR_SPLITS
     # 32 query heads per cache head: 8 per CTA, so a chunk may hold 6K rows
-    assert call(Hq=32, Hkv=1, max_len=60000, splits=1) == 12
+    assert call(Hq=32, Hkv=1, max_len=60000, splits=1) == binding.FA_ERR_SPLITS
     assert call(ws=1 << 12, wsb=16, splits=4) == 8
 
 
 @pytest.mark.parametrize("B,Hq,Hkv,L", [(1, 14, 2, 4096), (32, 14, 2, 4096), (8, 32, 1, 1000),
                                         (4, 8, 8, 4096)])
 def test_grouped_split_choice(lib, B, Hq, Hkv, L):
-    s = binding.fa_decode_gqa_choose_splits(B, Hq, Hkv, L, 152)
+    s = binding.fa_decode_splits_for_sms(B, Hq, Hkv, L, 152)
     rows = Hkv * ((Hq // Hkv + 7) // 8)
     if Hq == Hkv:
-        assert s == binding.fa_decode_choose_splits(B, Hq, L, 152)
+        assert s == binding.fa_decode_splits_for_sms(B, Hq, Hq, L, 152)
     else:   # about 5 CTAs per SM, chunks of 64..512 rows, rounded to 64-row chunks
         cdiv = lambda a, b: -(-a // b)
         want = min(max(cdiv(5 * 152, B * rows), cdiv(L, 512)), cdiv(L, 64))
         chunk = cdiv(cdiv(L, want), 64) * 64
         assert s == cdiv(L, chunk)
     assert 1 <= s <= (L + 63) // 64
-    assert binding.fa_decode_gqa_choose_splits(B, Hq, 3, L, 152) < 0 or Hq % 3 == 0
+    assert binding.fa_decode_splits_for_sms(B, Hq, 3, L, 152) < 0 or Hq % 3 == 0
 
 
 def test_backward_argument_errors(lib):
@@ -169,8 +234,8 @@ def test_backward_argument_errors(lib):
     assert call(gt=7) == 4
     assert call(lse=A + 20482) == 5
     assert call(scale=float("nan")) == 6
-    assert call(dk=A) == 11          # dk over q
-    assert call(dv=B_ + 16) == 11    # dv over dq
+    assert call(dk=A) == binding.FA_ERR_ALIAS          # dk over q
+    assert call(dv=B_ + 16) == binding.FA_ERR_ALIAS    # dv over dq
 
 
 def test_plain_prefill_checks_too(lib):
@@ -190,10 +255,10 @@ S = 1 << 24  # seq_lens
     (dict(seq_lens=S + 2), 5),
     (dict(workspace=A + 8, workspace_bytes=1 << 20), 5),
     (dict(scale=float("nan")), 6),
-    (dict(num_splits=-1), 12),
-    (dict(num_splits=65), 12),
+    (dict(num_splits=-1), binding.FA_ERR_SPLITS),
+    (dict(num_splits=65), binding.FA_ERR_SPLITS),
     (dict(num_splits=4, workspace=1 << 30, workspace_bytes=16), 8),
-    (dict(out=S), 11),
+    (dict(out=S), binding.FA_ERR_ALIAS),
 ])
 def test_decode_argument_errors(lib, kw, status):
     a = dict(q=A, k=1 << 26, v=1 << 27, seq_lens=S, out=B_, B=2, H=3, max_len=4096, d=64,
@@ -210,7 +275,7 @@ def test_decode_argument_errors(lib, kw, status):
                                        (1, 12, 4096, 148), (3, 2, 1000, 152), (1, 1, 1, 152),
                                        (2, 2, 100000, 152), (64, 64, 4096, 152)])
 def test_split_choice_host_logic(lib, B, H, L, sms):
-    s = binding.fa_decode_choose_splits(B, H, L, sms)
+    s = binding.fa_decode_splits_for_sms(B, H, H, L, sms)
     assert s >= 1
     chunk = binding.fa_decode_chunk_len(L, s)
     assert chunk % 64 == 0
@@ -226,7 +291,9 @@ def test_split_choice_host_logic(lib, B, H, L, sms):
 
 
 def test_split_choice_bad_args(lib):
-    assert binding.fa_decode_choose_splits(0, 1, 10, 152) < 0
+    assert binding.fa_decode_choose_splits(0, 1, 10, 0) == -binding.FA_ERR_SHAPE
+    assert binding.fa_decode_splits_for_sms(0, 1, 1, 10, 152) == -binding.FA_ERR_SHAPE
+    assert binding.fa_decode_splits_for_sms(1, 1, 1, 10, 0) == -binding.FA_ERR_SHAPE
     assert binding.fa_decode_chunk_len(0, 1) < 0
     assert binding.fa_decode_workspace_bytes(1, 1, 10, 48, 1) == 0
 

@@ -72,6 +72,21 @@ def test_gradients_match_oracle(fa, oracle_mod, shape, dtype, causal):
         assert e <= REL_TOL[dtype], f"{name} {shape} {dtype} causal={causal}: {e:.3e}"
 
 
+@pytest.mark.parametrize("N", [4096, 8192])
+@pytest.mark.parametrize("causal", [False, True])
+def test_gradients_at_bench_size_on_sampled_heads(fa, oracle_mod, N, causal):
+    # the timed backward shape (1, 16, N, 128) bf16, run whole on the GPU; heads
+    # are independent, so two of them (every row and column) are checked in full
+    shape, dtype = (1, 16, N, 128), "bf16"
+    (q, k, v, g), scale, lse, grads = run(fa, shape, dtype, causal, 3600 + N)
+    heads = [0, 15]
+    f = [oracle_mod.bits_to_f64(np.ascontiguousarray(x[:, heads]), dtype) for x in (q, k, v, g)]
+    want = oracle_mod.attention_backward(*f, causal, scale, threads=len(heads))
+    for name, got_t, w in zip(("dq", "dk", "dv"), grads, want):
+        e = rel_err(G.device_to_f64(got_t)[:, heads], w)
+        assert e <= REL_TOL[dtype], f"{name} N={N} causal={causal}: {e:.3e}"
+
+
 @pytest.mark.parametrize("causal", [False, True])
 def test_forward_lse_matches_oracle(fa, oracle_mod, causal):
     shape, dtype = (2, 3, 700, 128), "bf16"

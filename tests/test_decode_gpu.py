@@ -62,7 +62,7 @@ def test_ragged_decode_config(fa, oracle_mod, B, H):
 
 def test_lengths_at_chunk_edges(fa, oracle_mod):
     L, B, H = 4096, 11, 3
-    splits = fa.fa_decode_choose_splits(B, H, L, 0)
+    splits = fa.fa_decode_choose_splits(B, H, L, -1)
     chunk = fa.fa_decode_chunk_len(L, splits)
     lens = [1, 2, chunk - 1, chunk, chunk + 1, 2 * chunk, 2 * chunk + 1, L - 1, L, 63, 65]
     lens = [min(max(x, 1), L) for x in lens]
@@ -105,7 +105,7 @@ def test_fixed_split_is_bit_identical_and_workspace_paths_agree(fa):
     q, kc, vc, lens = make_decode(B, H, L, 64, "f16", CFG_DECODE)
     a = run_decode(fa, q, kc, vc, lens, "f16", 0.125)
     b = run_decode(fa, q, kc, vc, lens, "f16", 0.125)
-    splits = fa.fa_decode_choose_splits(B, H, L, 0)
+    splits = fa.fa_decode_choose_splits(B, H, L, -1)
     nbytes = fa.fa_decode_workspace_bytes(B, H, L, 64, splits)
     ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
     c = run_decode(fa, q, kc, vc, lens, "f16", 0.125, workspace=ws)
@@ -133,12 +133,20 @@ def test_decode_of_token_t_equals_causal_prefill_row_t(fa):
 def test_length_clamping_and_zero_length(fa, oracle_mod):
     B, H, L = 4, 2, 300
     q, kc, vc, _ = make_decode(B, H, L, 64, "f16", 302, [1, 1, 1, 1])
+    assert fa.fa_device_status(True) == 0
+    # a zero length is legal (a zero row) and is not reported
+    lens = np.array([0, 300, 17, 0], dtype=np.int32)
+    got = G.device_to_f64(run_decode(fa, q, kc, vc, lens, "f16", 0.125, "f32"))
+    assert fa.fa_device_status(False) == 0
+    # lengths outside [0, max_len] are clamped, and the clamp is reported once
     lens = np.array([0, 300, 5000, -7], dtype=np.int32)
     got = G.device_to_f64(run_decode(fa, q, kc, vc, lens, "f16", 0.125, "f32"))
     want = oracle_decode(oracle_mod, q, kc, vc, np.clip(lens, 0, L), "f16", 0.125)
     assert np.array_equal(got[0], np.zeros_like(got[0]))
     assert np.array_equal(got[3], np.zeros_like(got[3]))
     G.assert_close(got, want, "f16", "f32", "decode clamped lengths")
+    assert fa.fa_device_status(True) == fa.FA_ERR_SEQ_LEN
+    assert fa.fa_device_status(False) == 0
 
 
 @pytest.mark.parametrize("d,dtype", [(128, "bf16"), (64, "bf16"), (128, "f16")])

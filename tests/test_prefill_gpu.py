@@ -93,23 +93,39 @@ def test_gpt2_config_b4_sampled(fa, oracle_mod, causal):
           rows=G.sample_rows(2048, 11))
 
 
+def check_bf16_and_strict_fp32(fa, oracle_mod, shape, causal, cfg, rows, outliers=False,
+                               extra_rows_fn=None):
+    """One bf16 problem run twice: bf16 output against 8e-3 + half an output
+    ulp, and fp32 output against the plain 8e-3 (the output rounding then
+    cannot hide a kernel error), both on the same oracle rows."""
+    scale = float(np.float32(1.0 / np.sqrt(shape[-1])))
+    q, k, v, orows = make_qkv(shape, "bf16", cfg, outliers)
+    if extra_rows_fn is not None:
+        rows = np.unique(np.concatenate([rows, extra_rows_fn(orows)]))
+    want = oracle_rows(oracle_mod, q, k, v, "bf16", causal, scale, rows=rows)
+    got = G.device_to_f64(run_prefill(fa, q, k, v, "bf16", causal, scale, "bf16"))[:, :, rows]
+    G.assert_close(got, want, "bf16", "bf16", f"prefill {shape} bf16 causal={causal}")
+    got32 = G.device_to_f64(run_prefill(fa, q, k, v, "bf16", causal, scale, "f32"))[:, :, rows]
+    err = float(np.abs(got32 - want).max())
+    assert err <= 8e-3, f"prefill {shape} fp32 output: max abs err {err:.3e} > 8e-3"
+
+
 @pytest.mark.parametrize("N", [4096, 8192, 16384])
 def test_long_dense_config_sampled(fa, oracle_mod, N):
-    scale = float(np.float32(1.0 / np.sqrt(128.0)))
-    check(fa, oracle_mod, (1, 16, N, 128), "bf16", "bf16", False, scale, CFG_LONG,
-          rows=G.sample_rows(N, N))
+    check_bf16_and_strict_fp32(fa, oracle_mod, (1, 16, N, 128), False, CFG_LONG,
+                               G.sample_rows(N, N))
 
 
 def test_stress_config_sampled(fa, oracle_mod):
-    scale = float(np.float32(1.0 / np.sqrt(128.0)))
     N = 8192
 
     def outlier_neighbourhood(orows):
         r = np.unique(orows[:, :4].reshape(-1))[:8]
         return np.clip(np.concatenate([r, r + 1]), 0, N - 1)
 
-    check(fa, oracle_mod, (8, 32, N, 128), "bf16", "bf16", True, scale, CFG_STRESS,
-          rows=G.sample_rows(N, 5), outliers=True, extra_rows_fn=outlier_neighbourhood)
+    check_bf16_and_strict_fp32(fa, oracle_mod, (8, 32, N, 128), True, CFG_STRESS,
+                               G.sample_rows(N, 5), outliers=True,
+                               extra_rows_fn=outlier_neighbourhood)
 
 
 # ------------------------------------------------------------ edge shapes
@@ -125,15 +141,6 @@ def test_edge_lengths_full_check(fa, oracle_mod, N, d, causal):
                                                 ("bf16", "f32"), ("f16", "f16")])
 def test_dtype_combinations(fa, oracle_mod, in_dtype, out_dtype):
     check(fa, oracle_mod, (1, 4, 384, 64), in_dtype, out_dtype, True, 0.125, 200)
-
-
-def test_long_dense_fp32_output_strict(fa, oracle_mod):
-    scale = float(np.float32(1.0 / np.sqrt(128.0)))
-    q, k, v, _ = make_qkv((1, 16, 4096, 128), "bf16", CFG_LONG)
-    got = G.device_to_f64(run_prefill(fa, q, k, v, "bf16", False, scale, "f32"))
-    rows = G.sample_rows(4096, 3)
-    want = oracle_rows(oracle_mod, q, k, v, "bf16", False, scale, rows=rows)
-    assert np.abs(got[:, :, rows] - want).max() <= 8e-3
 
 
 # ------------------------------------------------------------ special cases
