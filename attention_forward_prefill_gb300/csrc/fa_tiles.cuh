@@ -27,31 +27,81 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volati
     return ok != 0;
 }
 
-// S (+)= Q K^T over d: a_desc / b_desc describe the Q and K tiles at K-step 0;
-// step kk moves (kk / 4) 64-column slabs and (kk % 4) 32-byte atoms along d.
-// Descriptors are built once per tile; each step only adds a constant to the
-// start-address field (shared addresses stay below 256 KB, so it cannot carry).
+// The MMA chains below are issued from one asm block each: the descriptors'
+// start-address fields are advanced by 32-bit adds on their low words
+// (shared addresses stay below 256 KB, so a field can never carry into the
+// next), and only the first product of a chain reads its accumulate flag.
+#define FA_MMA_SS(OFFA, OFFB)                                                 \
+    "add.u32 xa, %1, " #OFFA ";\n\t"                                        \
+    "add.u32 xb, %3, " #OFFB ";\n\t"                                        \
+    "mov.b64 a, {xa, %2};\n\t"                                              \
+    "mov.b64 b, {xb, %4};\n\t"                                              \
+    "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %5, pt;\n\t"
+
+// S = Q K^T over d: a_desc / b_desc describe the Q and K tiles at K-step 0;
+// step kk moves (kk / 4) 64-column slabs and (kk % 4) 32-byte atoms along d,
+// i.e. ((kk / 4) * 16384 + (kk % 4) * 32) / 16 in the descriptors' address field.
 template <int D>
 __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                          uint32_t idesc) {
-#pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk) {
-        const uint64_t off = ((kk >> 2) * kSlabBytes + (kk & 3) * 32) >> 4;
-        umma_ss(d_tmem, a_desc + off, b_desc + off, idesc, kk > 0 ? 1u : 0u);
+    const uint32_t alo = static_cast<uint32_t>(a_desc), ahi = static_cast<uint32_t>(a_desc >> 32);
+    const uint32_t blo = static_cast<uint32_t>(b_desc), bhi = static_cast<uint32_t>(b_desc >> 32);
+    if constexpr (D == 128) {
+        asm volatile(
+            "{\n\t.reg .pred pf, pt;\n\t.reg .b64 a, b;\n\t.reg .b32 xa, xb;\n\t"
+            "setp.ne.b32 pf, %6, %6;\n\t"
+            "setp.eq.b32 pt, %6, %6;\n\t"
+            "mov.b64 a, {%1, %2};\n\t"
+            "mov.b64 b, {%3, %4};\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %5, pf;\n\t"
+            FA_MMA_SS(2, 2) FA_MMA_SS(4, 4) FA_MMA_SS(6, 6)
+            FA_MMA_SS(1024, 1024) FA_MMA_SS(1026, 1026) FA_MMA_SS(1028, 1028) FA_MMA_SS(1030, 1030)
+            "}" ::"r"(d_tmem), "r"(alo), "r"(ahi), "r"(blo), "r"(bhi), "r"(idesc), "r"(0)
+            : "memory");
+    } else {
+        static_assert(D == 64, "head sizes 64 and 128");
+        asm volatile(
+            "{\n\t.reg .pred pf, pt;\n\t.reg .b64 a, b;\n\t.reg .b32 xa, xb;\n\t"
+            "setp.ne.b32 pf, %6, %6;\n\t"
+            "setp.eq.b32 pt, %6, %6;\n\t"
+            "mov.b64 a, {%1, %2};\n\t"
+            "mov.b64 b, {%3, %4};\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %5, pf;\n\t"
+            FA_MMA_SS(2, 2) FA_MMA_SS(4, 4) FA_MMA_SS(6, 6)
+            "}" ::"r"(d_tmem), "r"(alo), "r"(ahi), "r"(blo), "r"(bhi), "r"(idesc), "r"(0)
+            : "memory");
     }
 }
+#undef FA_MMA_SS
 
 // O (+)= P V: P from TMEM (16 keys = 8 columns per step), V tile [key][d] with d
 // contiguous is an MN-major B operand: 16 keys per step = two 8-key groups
-// (SBO apart), 64-column slabs of d LBO apart.
+// (SBO apart), i.e. 16 * 128 / 16 = 128 in the descriptor's address field;
+// 64-column slabs of d are LBO apart.  The first product accumulates only if
+// `accumulate` is set.
+#define FA_MMA_TS(OFFA, OFFB)                                                 \
+    "add.u32 ta, %1, " #OFFA ";\n\t"                                        \
+    "add.u32 xb, %2, " #OFFB ";\n\t"                                        \
+    "mov.b64 b, {xb, %3};\n\t"                                              \
+    "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], b, %4, pt;\n\t"
+
 template <int D>
 __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint64_t v_desc,
                                          uint32_t idesc, bool accumulate) {
-#pragma unroll
-    for (int kk = 0; kk < kTileKeys / 16; ++kk)
-        umma_ts(d_tmem, p_tmem + kk * 8, v_desc + ((kk * 16 * 128) >> 4), idesc,
-                (accumulate || kk > 0) ? 1u : 0u);
+    static_assert(kTileKeys == 128, "eight 16-key products per tile");
+    const uint32_t blo = static_cast<uint32_t>(v_desc), bhi = static_cast<uint32_t>(v_desc >> 32);
+    asm volatile(
+        "{\n\t.reg .pred pf, pt;\n\t.reg .b64 b;\n\t.reg .b32 ta, xb;\n\t"
+        "setp.ne.b32 pf, %5, 0;\n\t"
+        "setp.eq.b32 pt, %5, %5;\n\t"
+        "mov.b64 b, {%2, %3};\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], b, %4, pf;\n\t"
+        FA_MMA_TS(8, 128) FA_MMA_TS(16, 256) FA_MMA_TS(24, 384) FA_MMA_TS(32, 512)
+        FA_MMA_TS(40, 640) FA_MMA_TS(48, 768) FA_MMA_TS(56, 896)
+        "}" ::"r"(d_tmem), "r"(p_tmem), "r"(blo), "r"(bhi), "r"(idesc), "r"(accumulate ? 1u : 0u)
+        : "memory");
 }
+#undef FA_MMA_TS
 
 // The two 16-bit values of a packed pair, back in fp32 (exact), as an f32x2.
 template <bool BF16>

@@ -46,14 +46,17 @@ def splitmix64(seed: int, start: int, count: int) -> np.ndarray:
     return z
 
 
-def normal_f64(seed: int, count: int) -> np.ndarray:
-    """count i.i.d. N(0, 1) draws (float64) from the seeded stream."""
+def normal_f64_range(seed: int, start: int, count: int) -> np.ndarray:
+    """Draws start .. start+count-1 (start even) of the seeded N(0, 1) stream."""
+    if start % 2:
+        raise ValueError("a range of the normal stream starts at an even index")
     out = np.empty(count, dtype=np.float64)
     n_pairs = (count + 1) // 2
+    p0 = start // 2
     done = 0
     while done < n_pairs:
         m = min(_CHUNK, n_pairs - done)
-        z = splitmix64(seed, 2 * done, 2 * m)
+        z = splitmix64(seed, 2 * (p0 + done), 2 * m)
         top = (z >> np.uint64(11)).astype(np.float64)
         u1 = (top[0::2] + 1.0) * (2.0 ** -53)  # (0, 1]
         u2 = top[1::2] * (2.0 ** -53)          # [0, 1)
@@ -67,6 +70,17 @@ def normal_f64(seed: int, count: int) -> np.ndarray:
         out[lo:hi] = pair[: hi - lo]
         done += m
     return out
+
+
+def normal_f64(seed: int, count: int) -> np.ndarray:
+    """count i.i.d. N(0, 1) draws (float64) from the seeded stream."""
+    return normal_f64_range(seed, 0, count)
+
+
+def _blocks(n: int, threads: int, block: int):
+    """Even-aligned [lo, hi) blocks covering [0, n)."""
+    block = max(2, (block // 2) * 2)
+    return [(lo, min(n, lo + block)) for lo in range(0, n, block)] if threads > 1 else [(0, n)]
 
 
 def f64_to_f16_bits(x: np.ndarray) -> np.ndarray:
@@ -88,10 +102,27 @@ def to_bits(x: np.ndarray, dtype: str) -> np.ndarray:
     raise ValueError(f"unknown 16-bit dtype {dtype!r}")
 
 
-def normal_bits(shape, seed: int, dtype: str) -> np.ndarray:
-    """i.i.d. N(0,1) values rounded to fp16/bf16, as uint16 bit patterns."""
+def normal_bits(shape, seed: int, dtype: str, threads: int = 1) -> np.ndarray:
+    """i.i.d. N(0,1) values rounded to fp16/bf16, as uint16 bit patterns.
+
+    threads > 1 fills blocks of the same stream on host threads (numpy
+    releases the GIL): the bits do not depend on the thread count.
+    """
     n = int(np.prod(shape))
-    return to_bits(normal_f64(seed, n), dtype).reshape(shape)
+    out = np.empty(n, dtype=np.uint16)
+
+    def fill(b):
+        lo, hi = b
+        out[lo:hi] = to_bits(normal_f64_range(seed, lo, hi - lo), dtype)
+
+    blocks = _blocks(n, threads, 1 << 22)
+    if len(blocks) > 1:
+        from concurrent.futures import ThreadPoolExecutor
+        with ThreadPoolExecutor(max_workers=threads) as ex:
+            list(ex.map(fill, blocks))
+    else:
+        fill(blocks[0])
+    return out.reshape(shape)
 
 
 def outlier_rows(seed: int, n_rows: int, count: int) -> np.ndarray:
@@ -105,20 +136,35 @@ def outlier_rows(seed: int, n_rows: int, count: int) -> np.ndarray:
 
 
 def keys_with_outliers(shape, seed_k: int, seed_rows: int, dtype: str,
-                       fraction: float = 0.01, factor: float = 20.0):
+                       fraction: float = 0.01, factor: float = 20.0, threads: int = 1):
     """N(0,1) keys where round(fraction*N) rows per (b, h) are scaled by factor.
 
+    The draw is scaled before it is rounded to 16 bits.  Heads are generated
+    one by one (on host threads when threads > 1; the bits are the same).
     Returns (bits [B,H,N,d], rows [B*H, count]).
     """
     B, H, N, d = shape
-    x = normal_f64(seed_k, B * H * N * d).reshape(B * H, N, d)
+    out = np.empty((B * H, N, d), dtype=np.uint16)
     count = int(round(fraction * N))
     rows = np.zeros((B * H, count), dtype=np.int64)
-    for bh in range(B * H):
-        r = outlier_rows(seed_rows + (bh << 32), N, count) if count else rows[bh]
-        rows[bh] = r
-        x[bh, r, :] *= factor
-    return to_bits(x, dtype).reshape(shape), rows
+    head = N * d
+
+    def one(bh):
+        x = normal_f64_range(seed_k, bh * head, head).reshape(N, d)
+        if count:
+            r = outlier_rows(seed_rows + (bh << 32), N, count)
+            rows[bh] = r
+            x[r, :] *= factor
+        out[bh] = to_bits(x, dtype)
+
+    if threads > 1 and B * H > 1:
+        from concurrent.futures import ThreadPoolExecutor
+        with ThreadPoolExecutor(max_workers=threads) as ex:
+            list(ex.map(one, range(B * H)))
+    else:
+        for bh in range(B * H):
+            one(bh)
+    return out.reshape(shape), rows
 
 
 def seq_lens(seed: int, batch: int, max_len: int) -> np.ndarray:

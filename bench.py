@@ -156,21 +156,37 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ our path
-def make_inputs(torch, device, rank):
-    """Synthetic N(0,1) inputs generated on the device (seeded per rank)."""
+# configuration ids of the seeded generator (seed = 0xFA000000 + 16 * config + tensor)
+CFG_TINY, CFG_GPT2, CFG_LONG, CFG_DECODE, CFG_STRESS = 0, 1, 2, 3, 4
+GEN_THREADS = max(1, min(32, os.cpu_count() or 1))
+
+
+def gen_tensor(torch, device, shape, cfg, tensor, dtype, rank=0, extra=0):
+    """The repository's seeded N(0,1) generator (SplitMix64, Box-Muller, RNE to
+    16 bits), drawn on the host threads and copied to the device.  Ranks and
+    extra problems of a config get their own streams."""
     from attention_forward_prefill_gb300 import inputs as fin
-    g = torch.Generator(device=device)
-    g.manual_seed(0xFA000000 + 97 * rank)
+    seed = fin.seed_for(cfg, tensor) + (rank << 40) + (extra << 48)
+    bits = fin.normal_bits(shape, seed, "bf16" if dtype == torch.bfloat16 else "f16",
+                           threads=GEN_THREADS)
+    import numpy as np
+    return torch.from_numpy(bits.view(np.int16)).view(dtype).to(device)
+
+
+def make_inputs(torch, device, rank):
+    """Seeded synthetic inputs of the timed step (per rank), on the device."""
+    from attention_forward_prefill_gb300 import inputs as fin
     pre = {}
     for N in PREFILL_NS:
         shape = (PREFILL_B, PREFILL_H, N, PREFILL_D)
-        pre[N] = [torch.randn(shape, generator=g, device=device, dtype=torch.float32)
-                  .to(torch.bfloat16) for _ in range(3)]
+        pre[N] = [gen_tensor(torch, device, shape, CFG_LONG, t, torch.bfloat16, rank, N)
+                  for t in (fin.TENSOR_Q, fin.TENSOR_K, fin.TENSOR_V)]
     shp = (DECODE_B, DECODE_H, DECODE_L, DECODE_D)
-    dq = torch.randn((DECODE_B, DECODE_H, 1, DECODE_D), generator=g, device=device).half()
-    dk = torch.randn(shp, generator=g, device=device).half()
-    dv = torch.randn(shp, generator=g, device=device).half()
-    lens_np = fin.seq_lens(fin.seed_for(3, fin.TENSOR_SEQLEN) + rank, DECODE_B, DECODE_L)
+    dq = gen_tensor(torch, device, (DECODE_B, DECODE_H, 1, DECODE_D), CFG_DECODE, fin.TENSOR_Q,
+                    torch.float16, rank)
+    dk = gen_tensor(torch, device, shp, CFG_DECODE, fin.TENSOR_K, torch.float16, rank)
+    dv = gen_tensor(torch, device, shp, CFG_DECODE, fin.TENSOR_V, torch.float16, rank)
+    lens_np = fin.seq_lens(fin.seed_for(CFG_DECODE, fin.TENSOR_SEQLEN) + rank, DECODE_B, DECODE_L)
     lens = torch.from_numpy(lens_np).to(device)
     return pre, (dq, dk, dv, lens, lens_np)
 
@@ -437,23 +453,31 @@ def measure_configs(torch, binding, device, stream, flush, peaks, reps=7):
     import numpy as np
 
     from attention_forward_prefill_gb300 import inputs as fin
-    g = torch.Generator(device=device)
-    g.manual_seed(0xFA00F00D)
     res = {}
+    n_extra = [100]
 
-    def rnd(shape, dtype):
-        return torch.randn(shape, generator=g, device=device, dtype=torch.float32).to(dtype)
+    def rnd(shape, dtype, cfg=7):
+        # the seeded generator; every call draws its own stream
+        n_extra[0] += 1
+        return gen_tensor(torch, device, shape, cfg, 0, dtype, 0, n_extra[0])
 
-    pre_cases = [("tiny", 1, 2, 128, 64, torch.float16, torch.float32, 0.125),
-                 ("gpt2_b1", 1, 12, 2048, 64, torch.float16, torch.float16, 0.125),
-                 ("gpt2_b4", 4, 12, 2048, 64, torch.float16, torch.float16, 0.125),
-                 ("stress", 8, 32, 8192, 128, torch.bfloat16, torch.bfloat16,
+    pre_cases = [("tiny", CFG_TINY, 1, 2, 128, 64, torch.float16, torch.float32, 0.125),
+                 ("gpt2_b1", CFG_GPT2, 1, 12, 2048, 64, torch.float16, torch.float16, 0.125),
+                 ("gpt2_b4", CFG_GPT2, 4, 12, 2048, 64, torch.float16, torch.float16, 0.125),
+                 ("stress", CFG_STRESS, 8, 32, 8192, 128, torch.bfloat16, torch.bfloat16,
                   float(1.0 / math.sqrt(128)))]
-    for name, B, H, N, d, dt, odt, scale in pre_cases:
-        q, k, v = (rnd((B, H, N, d), dt) for _ in range(3))
-        if name == "stress":  # 1% of the key rows x20 (same rows in every head)
-            idx = torch.randperm(N, generator=g, device=device)[: round(0.01 * N)]
-            k[:, :, idx] *= 20
+    for name, cfg, B, H, N, d, dt, odt, scale in pre_cases:
+        q, v = (gen_tensor(torch, device, (B, H, N, d), cfg, t, dt) for t in (fin.TENSOR_Q, fin.TENSOR_V))
+        if name == "stress":
+            # 1% of the key rows of every (b, h), chosen per head, x20 before rounding
+            import numpy as np
+            kb, _ = fin.keys_with_outliers((B, H, N, d), fin.seed_for(cfg, fin.TENSOR_K),
+                                           fin.seed_for(cfg, fin.TENSOR_OUTLIER), "bf16",
+                                           threads=GEN_THREADS)
+            k = torch.from_numpy(kb.view(np.int16)).view(dt).to(device)
+            del kb
+        else:
+            k = gen_tensor(torch, device, (B, H, N, d), cfg, fin.TENSOR_K, dt)
         out = torch.empty((B, H, N, d), dtype=odt, device=device)
         for causal in ((True,) if name == "stress" else (False, True)):
             def fn():
@@ -565,11 +589,19 @@ def measure_configs(torch, binding, device, stream, flush, peaks, reps=7):
             "shape": [B, Hq, Hkv, DECODE_L, DECODE_D], "splits": splits,
             "median_us": round(med * 1e3, 2), "min_us": round(mn * 1e3, 2), "gbs": round(gbs, 1),
             "frac_of_peak": round(gbs / peaks["hbm_gbs"], 4)}
-    # read-only streaming probe (a library reduction over 4 GiB), beside decode
+    # read-only streaming probe beside decode: the library's own kernel, with
+    # the decode loads (16-byte, non-caching), over 4 GiB
     x = torch.ones(1 << 31, dtype=torch.float16, device=device)
-    med, _ = time_kernel(torch, stream, flush, lambda: torch.sum(x, dtype=torch.float32), reps)
-    res["read_probe"] = {"what": "torch.sum over 4 GiB fp16 (library kernel)",
-                         "gbs": round(x.numel() * 2 / (med / 1e3) / 1e9, 1)}
+    xo = torch.zeros(1, dtype=torch.int32, device=device)
+    nbytes = x.numel() * 2
+
+    def probe():
+        rc = binding.fa_read_probe(x.data_ptr(), nbytes, xo.data_ptr(), stream.cuda_stream)
+        assert rc == 0
+    med, _ = time_kernel(torch, stream, flush, probe, reps)
+    res["read_probe"] = {"what": "fa_read_probe over 4 GiB (16-byte non-caching loads, "
+                                 "XOR checksum)", "gbs": round(nbytes / (med / 1e3) / 1e9, 1),
+                         "frac_of_peak": round(nbytes / (med / 1e3) / 1e9 / peaks["hbm_gbs"], 4)}
     del x
     return res
 

@@ -55,3 +55,23 @@ def test_seq_lens_range_and_spread():
     assert lens.dtype == np.int32
     assert lens.min() >= 1 and lens.max() <= 4096
     assert abs(lens.mean() - 2048.5) < 60
+
+
+def test_threaded_generation_gives_the_same_bits():
+    # blocks of the counter-based stream on host threads: no dependence on the
+    # thread count or the block boundaries (an odd total length included)
+    n = (1 << 22) * 2 + 6
+    one = inputs.normal_bits((n,), 31, "bf16")
+    many = inputs.normal_bits((n,), 31, "bf16", threads=6)
+    assert np.array_equal(one, many)
+    assert np.array_equal(inputs.normal_bits((3, 333), 5, "f16", threads=4),
+                          inputs.normal_bits((3, 333), 5, "f16"))
+    a, ra = inputs.keys_with_outliers((2, 3, 200, 64), 11, 12, "bf16")
+    b, rb = inputs.keys_with_outliers((2, 3, 200, 64), 11, 12, "bf16", threads=5)
+    assert np.array_equal(a, b) and np.array_equal(ra, rb)
+
+
+def test_ranges_of_the_normal_stream_agree_with_the_whole():
+    whole = inputs.normal_f64(77, 1000)
+    assert np.array_equal(inputs.normal_f64_range(77, 400, 600), whole[400:])
+    assert np.array_equal(inputs.normal_f64_range(77, 0, 999), whole[:999])

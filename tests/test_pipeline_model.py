@@ -520,6 +520,8 @@ def prefill_kernel(sim, units, sep_p, plant=None):
                     yield ("read", f"O{t}.{w}", ("O", u, t, j - 1))
                     yield ("write", f"O{t}.{w}", ("O", u, t, j - 1))
                 yield ("arrive", f"p_full{t}")
+                if plant == "double_arrive":  # two lanes of a warp arriving, not one
+                    yield ("arrive", f"p_full{t}")
             if n[t] > j0:
                 if sep_p:
                     yield ("wait", f"pv_done{t}", pvc)
@@ -564,7 +566,8 @@ def test_prefill_protocol_holds_under_random_interleavings(sep_p, units):
         sim.run()
 
 
-@pytest.mark.parametrize("sep_p,plant", [(False, "qk_before_pv"), (True, "qk_without_s_free")])
+@pytest.mark.parametrize("sep_p,plant", [(False, "qk_before_pv"), (True, "qk_without_s_free"),
+                                         (False, "double_arrive"), (True, "double_arrive")])
 def test_the_prefill_model_catches_a_planted_mistake(sep_p, plant):
     caught = 0
     for seed in range(150):
