@@ -37,16 +37,20 @@ PREFILL_NS = (4096, 8192, 16384)
 DECODE_B, DECODE_H, DECODE_L, DECODE_D = 32, 14, 4096, 64
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
-# DRAM traffic per launch from an ncu capture, valid only for the kernel source
-# it was taken on (sha256 of the .cu file, first 16 hex digits).
+# DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one
+# ncu capture, valid only for the kernel source it was taken on: the first 16 hex
+# digits of the sha256 of the listed source files, in order.
 NCU_TRAFFIC = {
-    # Measured at N=8192 (ncu --set full, profiles/prefill_kernel_d128_n8192.md);
-    # the other lengths are scaled by the bytes the launch must move (linear in N).
-    "prefill": {"src": "fa_prefill_sm103.cu", "src_sha": "5d414b32c8783a0a",
-                "bytes_per_launch": {"4096": 116.25e6 / 2, "8192": 116.25e6, "16384": 116.25e6 * 2},
+    # ncu --set full of one prefill_kernel<128> launch of the N=8192 step problem
+    # (B=1, H=16, d=128, bf16); the other lengths are scaled by the bytes the
+    # launch must move (linear in N).
+    "prefill": {"src": ["fa_prefill_sm103.cu", "fa_tiles.cuh", "sm103_ptx.cuh"],
+                "src_sha": "8e4404321761bd75",
+                "bytes_per_launch": {"4096": 114.76e6 / 2, "8192": 114.76e6, "16384": 114.76e6 * 2},
                 "measured_at": "8192", "scaled": ["4096", "16384"]},
-    # B=32, H=14 (profiles/decode_split_b32_h14.md): DRAM bytes of one split-kernel launch
-    "decode": {"src": "fa_decode_sm103.cu", "src_sha": "b66f8ad7b76c86db", "bytes_per_launch": 263.9e6},
+    # one decode_split_kernel<64> launch of the step's decode problem (B=32, H=14)
+    "decode": {"src": ["fa_decode_sm103.cu", "sm103_ptx.cuh"], "src_sha": "b66f8ad7b76c86db",
+               "bytes_per_launch": 263.9e6},
 }
 
 
@@ -69,10 +73,12 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def src_sha(name):
-    path = os.path.join(ROOT, "attention_forward_prefill_gb300", "csrc", name)
-    with open(path, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+def src_sha(names):
+    h = hashlib.sha256()
+    for name in names:
+        with open(os.path.join(ROOT, "attention_forward_prefill_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 # ------------------------------------------------------------------ ranks
@@ -222,12 +228,35 @@ def run_ours(args):
     cases = args.case.split(",") if args.case else None
     do_pre = [N for N in PREFILL_NS if cases is None or f"prefill:{N}" in cases]
     do_dec = cases is None or "decode" in cases
-    # backward (training) case, only when asked for: B=1, H=16, N=4096, d=128, bf16
-    do_bwd = cases is not None and "backward" in cases
-    if do_bwd:
-        bq, bk, bv, bdo = (torch.randn((1, 16, 4096, PREFILL_D), device=device).to(torch.bfloat16)
-                           for _ in range(4))
-        bout, blse = binding.prefill_with_lse(bq, bk, bv, causal=False, scale=scale_p)
+    # Extra problems, only when asked for (profiling and diagnostics; not part of
+    # the headline): "shape:BxHxNxD[:causal]" is a forward prefill, "backward" the
+    # backward of (1, 16, 4096, 128) and "backward:BxHxNxD[:causal]" any other;
+    # fp16 at d = 64, bf16 at d = 128.
+    extras = []
+    for c in cases or []:
+        kind, _, spec = c.partition(":")
+        if kind == "backward" and not spec:
+            spec = "1x16x4096x128"
+        if kind not in ("shape", "backward") or not spec:
+            continue
+        dims, _, flag = spec.partition(":")
+        B, H, N, d = (int(x) for x in dims.split("x"))
+        dt = torch.float16 if d == 64 else torch.bfloat16
+        t = [gen_tensor(torch, device, (B, H, N, d), CFG_LONG, i, dt, rank, 1000 + len(extras))
+             for i in range(4 if kind == "backward" else 3)]
+        causal = flag == "causal"
+        sc = 1.0 / math.sqrt(d)
+        if kind == "backward":
+            o, lse = binding.prefill_with_lse(t[0], t[1], t[2], causal=causal, scale=sc)
+            fn = (lambda t=t, o=o, lse=lse, causal=causal, sc=sc:
+                  binding.prefill_backward(t[0], t[1], t[2], o, t[3], lse, causal=causal, scale=sc))
+            flops = 10.0 * B * H * N * N * d / (2 if causal else 1)
+        else:
+            o = torch.empty_like(t[0])
+            fn = (lambda t=t, o=o, causal=causal, sc=sc:
+                  binding.prefill(t[0], t[1], t[2], causal=causal, scale=sc, out=o))
+            flops = prefill_flops(B, H, N, d, causal)
+        extras.append((c, fn, flops))
 
     def step(record):
         ev = []
@@ -249,14 +278,14 @@ def run_ours(args):
                            out=dout)
             e1.record(stream)
             ev.append(("decode", 0, e0, e1))
-        if do_bwd:
+        for name, fn, _ in extras:
             flush.zero_()
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
             e0.record(stream)
-            binding.prefill_backward(bq, bk, bv, bout, bdo, blse, causal=False, scale=scale_p)
+            fn()
             e1.record(stream)
-            ev.append(("backward", 4096, e0, e1))
+            ev.append(("extra", name, e0, e1))
         if record is not None:
             record.append(ev)
 
@@ -287,10 +316,10 @@ def run_ours(args):
 
     pre_ms = {N: [] for N in do_pre}
     dec_ms = []
-    bwd_ms = []
+    extra_ms = {name: [] for name, _, _ in extras}
     for ev in records:
         for kind, N, e0, e1 in ev:
-            {"prefill": pre_ms.get(N), "decode": dec_ms, "backward": bwd_ms}[kind].append(
+            {"prefill": pre_ms.get(N), "decode": dec_ms, "extra": extra_ms.get(N)}[kind].append(
                 e0.elapsed_time(e1))
     pre_time_s = sum(sum(v) for v in pre_ms.values()) / 1e3
     pre_flops = sum(prefill_flops(PREFILL_B, PREFILL_H, N, PREFILL_D) for N in do_pre) * args.steps
@@ -353,7 +382,14 @@ def run_ours(args):
     for N in do_pre:
         _, info, _ = binding.fa_prefill_plan(PREFILL_B, PREFILL_H, N, N, 0, 0, 0)
         per_step += 1 + (1 if info[0] and info[5] > 0 else 0)
-    per_step += (2 if do_dec else 0) + (3 if do_bwd else 0)
+    per_step += 2 if do_dec else 0
+    for name, _, _ in extras:  # backward: prep + dK/dV + dQ; forward as above
+        if name.startswith("backward"):
+            per_step += 3
+        else:
+            B, H, N, d = (int(x) for x in name.split(":")[1].split("x"))
+            _, info, _ = binding.fa_prefill_plan(B, H, N, N, int(name.endswith(":causal")), 0, 0)
+            per_step += 1 + (1 if info[0] and info[5] > 0 else 0)
     n_launch = per_step * args.steps
     detail = {}
     for N in do_pre:
@@ -422,10 +458,10 @@ def run_ours(args):
                          "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4),
                          "traffic": dec_traffic, "peak_source": f"{peak_src} copy bandwidth"},
         }
-    if do_bwd and bwd_ms:
-        ms = statistics.median(bwd_ms)
-        line["backward"] = {"shape": [1, 16, 4096, PREFILL_D], "median_ms": round(ms, 4),
-                            "tflops": round(10.0 * 16 * 4096 ** 2 * PREFILL_D / (ms / 1e3) / 1e12, 1)}
+    if extras:
+        line["extras"] = {name: {"median_ms": round(statistics.median(extra_ms[name]), 4),
+                                 "tflops": round(fl / (statistics.median(extra_ms[name]) / 1e3) / 1e12, 1)}
+                          for name, _, fl in extras}
     if world > 1:
         dist.destroy_process_group()
     return line
