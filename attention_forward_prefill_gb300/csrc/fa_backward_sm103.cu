@@ -262,8 +262,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kMiscOff + 4);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int bhk = blockIdx.x / p.n_t;        // (batch, key/value head)
-    const int jt = blockIdx.x % p.n_t;         // key tile (small first: most query tiles)
+    // Causal: CTAs are dealt key-tile-major, so every head's heaviest tiles (the
+    // first key tiles see the most query tiles) start before any light one.
+    const int n_heads = static_cast<int>(gridDim.x) / p.n_t;
+    const int bhk = p.causal ? blockIdx.x % n_heads : blockIdx.x / p.n_t;  // (batch, key/value head)
+    const int jt = p.causal ? blockIdx.x / n_heads : blockIdx.x % p.n_t;   // key tile
     const int i_first = p.causal ? jt : 0;     // query tiles that see key tile jt
     const int n_qt = p.n_t - i_first;
     const int n_iter = p.group * n_qt;         // every query head of the group, every tile
@@ -638,10 +641,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kMiscOff + 4);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int bh = blockIdx.x / p.n_t;                          // (batch, query head)
-    const int bhk = (bh / p.Hq) * p.Hkv + (bh % p.Hq) / p.group;  // its key/value head
-    const int it = p.causal ? p.n_t - 1 - blockIdx.x % p.n_t   // most key tiles first
-                            : blockIdx.x % p.n_t;
+    // Causal: CTAs are dealt query-tile-major, heaviest (last) query tiles of
+    // every head first.
+    const int n_heads = static_cast<int>(gridDim.x) / p.n_t;
+    const int bh = p.causal ? blockIdx.x % n_heads : blockIdx.x / p.n_t;  // (batch, query head)
+    const int bhk = (bh / p.Hq) * p.Hkv + (bh % p.Hq) / p.group;          // its key/value head
+    const int it = p.causal ? p.n_t - 1 - blockIdx.x / n_heads : blockIdx.x % p.n_t;
     const int n_iter = p.causal ? it + 1 : p.n_t;              // key tiles the queries see
 
     if (threadIdx.x == 0) {
