@@ -214,3 +214,16 @@ def test_grouped_decode_equals_one_row_chunk_prefill(fa):
                          scale=0.125, out_dtype=torch.float32)
         torch.cuda.synchronize()
         assert (dec - pre).abs().max().item() <= 2e-3, t
+
+
+def test_very_long_cache_many_splits(fa, oracle_mod):
+    # 262,144 cache rows: the automatic choice keeps chunks at most 512 rows, so
+    # 512 splits and the merge walks 16 batches of 32 (m, l) lanes
+    B, H, L = 2, 2, 262_144
+    q, kc, vc, _ = make_decode(B, H, L, 64, "f16", 310, [1, 1])
+    lens = np.array([L, 100_003], dtype=np.int32)
+    splits = fa.fa_decode_choose_splits(B, H, L, -1)
+    assert splits >= 512
+    got = G.device_to_f64(run_decode(fa, q, kc, vc, lens, "f16", 0.125, "f32"))
+    want = oracle_decode(oracle_mod, q, kc, vc, lens, "f16", 0.125)
+    G.assert_close(got, want, "f16", "f32", "decode over 262144 rows")

@@ -197,3 +197,19 @@ def test_stream_k_non_causal_with_idle_ctas(fa, oracle_mod):
                 flags=fa.FA_FLAG_SCHEDULE_STREAM_K)
     check_dense(fa, oracle_mod, 1, 3, 1, 200, 900, 128, False, 1401,
                 flags=fa.FA_FLAG_SCHEDULE_STREAM_K)
+
+
+def test_many_small_units(fa, oracle_mod):
+    # 64 x 32 heads of 64 causal rows: 2048 one-tile units, about 13 rounds of
+    # the unit schedule per CTA, each unit's second query tile empty
+    check_dense(fa, oracle_mod, 64, 32, 32, 64, 64, 64, True, 4100, rows=None)
+
+
+def test_grouped_heads_under_stream_k_with_a_ragged_tail(fa, oracle_mod):
+    # 4 x 40 query heads over 8 key/value heads, N = 1000 (a ragged last tile):
+    # dense and non-causal, so the library may cut units between CTAs
+    _, info, _ = fa.fa_prefill_plan(4, 40, 1000, 1000, 0, 0, 0)
+    check_dense(fa, oracle_mod, 4, 40, 8, 1000, 1000, 128, False, 4200,
+                rows=G.sample_rows(1000, 3))
+    check_dense(fa, oracle_mod, 4, 40, 8, 1000, 1000, 128, False, 4200,
+                flags=fa.FA_FLAG_SCHEDULE_STREAM_K, rows=G.sample_rows(1000, 3))
