@@ -143,8 +143,8 @@ def fa_prefill_backward(q, k, v, out, dout, lse, dq, dk, dv, B, H, Hkv, N, d, ca
 
 
 def fa_prefill_plan(B, Hq, Nq, Nk, causal, flags=0, num_sms=0, max_items=192):
-    """The prefill schedule as (status, info[8], items[n][5]) -- host arithmetic only."""
-    info = (ctypes.c_longlong * 8)()
+    """The prefill schedule as (status, info[9], items[n][5]) -- host arithmetic only."""
+    info = (ctypes.c_longlong * 9)()
     items = (ctypes.c_longlong * (5 * max_items))()
     rc = load().fa_prefill_plan(B, Hq, Nq, Nk, int(causal), flags, num_sms, info, items, max_items)
     n = int(info[5]) if rc == FA_OK else 0

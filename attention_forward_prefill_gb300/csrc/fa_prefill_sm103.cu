@@ -108,6 +108,11 @@ struct Params {
     // into gridDim.x equal contiguous ranges; a unit cut between two CTAs is
     // finished by the fixup kernel from the partials in ws_o / ws_ml.
     int stream_k;
+    // Causal unit schedule in one round: unit i of a head pairs query tile i with
+    // tile T - 1 - i (T = 128-row tiles per sequence), so that no unit holds more
+    // than T - i key tiles and its two tiles overlap for the first i + 1.
+    int zigzag;
+    int n_tt;              // T
     int HT;                // key-tile steps per (sequence, head) = pre[n_qb]
     long long W;           // BH * HT
     // Non-causal stream-K first deals dp_full whole units to every CTA (unit
@@ -131,7 +136,7 @@ struct StepTable {
 // (0 = none: no rows, or rows that see no key).
 struct Work {
     int u, b, h, hk;
-    int q0;                // first query row of the unit, within the sequence
+    int r0, r1;            // first query rows of the unit's two tiles, within the sequence
     int nq, nk, off;       // the sequence's lengths; off = nk - nq (causal alignment)
     long long qt0, kt0;    // packed: first query / key token of the sequence
     int j0, j1, n0, n1;
@@ -226,7 +231,10 @@ __device__ __forceinline__ bool seg_next(const Params &p, const StepTable &tab, 
                               : static_cast<int>(blockIdx.x);
         w.u = k * static_cast<int>(gridDim.x) + r;
         if (w.u >= p.n_units) return false;
-        if (p.causal) {  // heaviest query blocks first
+        if (p.zigzag) {  // pair i (tiles i and T - 1 - i); pair 0 holds the most keys
+            qb = w.u / p.BH;
+            bh = w.u % p.BH;
+        } else if (p.causal) {  // heaviest query blocks first
             qb = p.n_qb - 1 - w.u / p.BH;
             bh = w.u % p.BH;
         } else {         // neighbouring CTAs share a head's K/V in L2
@@ -239,9 +247,16 @@ __device__ __forceinline__ bool seg_next(const Params &p, const StepTable &tab, 
     w.b = bh / p.Hq;
     w.h = bh % p.Hq;
     load_seq(p, w);
-    w.q0 = qb * kRowsPerUnit;
-    w.n0 = kv_tiles(p.causal, p.no_skip, w.nq, w.nk, w.off, w.q0);
-    w.n1 = kv_tiles(p.causal, p.no_skip, w.nq, w.nk, w.off, w.q0 + kBlockM);
+    if (p.zigzag) {  // (dense: every sequence has T tiles)
+        const int partner = p.n_tt - 1 - qb;
+        w.r0 = qb * kBlockM;
+        w.r1 = partner > qb ? partner * kBlockM : w.nq;  // an odd T leaves a middle tile alone
+    } else {
+        w.r0 = qb * kRowsPerUnit;
+        w.r1 = w.r0 + kBlockM;
+    }
+    w.n0 = kv_tiles(p.causal, p.no_skip, w.nq, w.nk, w.off, w.r0);
+    w.n1 = kv_tiles(p.causal, p.no_skip, w.nq, w.nk, w.off, w.r1);
     if (w.j1 < 0) w.j1 = max(w.n0, w.n1);
     return true;
 }
@@ -357,7 +372,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_arrive_expect_tx(q_full, ((need0 ? 1 : 0) + (need1 ? 1 : 0)) * L::kTileBytes);
                 for (int t = 0; t < 2; ++t) {
                     if (!(t ? need1 : need0)) continue;
-                    const int row = w.q0 + t * kBlockM;
+                    const int row = t ? w.r1 : w.r0;
                     for (int c = 0; c < L::kChunks; ++c) {
                         if (packed)
                             tma_load_3d(q_smem + t * L::kTileBytes + c * L::kChunkBytes, &map_q, q_full,
@@ -577,7 +592,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         Work w;
         for (int seg = 0; ok && seg_next(p, tab, cur, w); ++seg) {
             const int j0 = w.j0, j1 = w.j1;
-            const int tile_row0 = w.q0 + t * kBlockM;
+            const int tile_row0 = t ? w.r1 : w.r0;
             const int row = tile_row0 + r;  // query index within the sequence
             // Output row: dense [B][Hq][Nq][d], packed [tokens][Hq][d].
             uint8_t *const orow = reinterpret_cast<uint8_t *>(p.out) +
@@ -950,6 +965,7 @@ constexpr long long kCausalStepPct = 108;
 
 struct Plan {
     int stream_k;
+    int zigzag;
     int grid;
     int n_qb;
     int HT;
@@ -975,6 +991,7 @@ void make_plan(bool packed, int B, int Hq, int Nq, int Nk, int causal, int no_sk
     const int n_units = BH * n_qb;
     const int sms = num_sms < kMaxSplit ? num_sms : kMaxSplit;
     pl.stream_k = 0;
+    pl.zigzag = 0;
     pl.n_qb = n_qb;
     pl.HT = 0;
     pl.W = 0;
@@ -983,6 +1000,10 @@ void make_plan(bool packed, int B, int Hq, int Nq, int Nk, int causal, int no_sk
     pl.n_split = 0;
     pl.grid = n_units < num_sms ? n_units : num_sms;
     pl.tab.pre[0] = 0;
+    // A causal dense problem whose units fit in one round runs unit by unit with
+    // paired query tiles (i, T - 1 - i) unless stream-K is taken below.
+    const bool zz = !packed && causal && !no_skip && n_units <= num_sms && schedule != 2;
+    pl.zigzag = zz ? 1 : 0;
     const bool sk_ok = !packed && n_qb <= kMaxPre && n_units >= 2 && (!causal || no_skip || Nk >= Nq) &&
                        schedule != 1;
     if (!sk_ok) return;
@@ -1016,6 +1037,7 @@ void make_plan(bool packed, int B, int Hq, int Nq, int Nk, int causal, int no_sk
     }
     if (!take) return;
     pl.stream_k = 1;
+    pl.zigzag = 0;
     pl.HT = HT;
     pl.W = W;
     const int grid = sms;
@@ -1112,6 +1134,8 @@ int launch_d_lse(const PrefillLaunch &a, const DeviceInfo &dev, cudaStream_t str
     p.scale_log2 = scale * 1.4426950408889634f;
     p.scale_log2_abs = fabsf(p.scale_log2);
     p.stream_k = 0;
+    p.zigzag = 0;
+    p.n_tt = 0;
     p.HT = 0;
     p.W = 0;
     p.ws_o = nullptr;
@@ -1120,6 +1144,8 @@ int launch_d_lse(const PrefillLaunch &a, const DeviceInfo &dev, cudaStream_t str
     static thread_local Plan pl;  // ~8 KB: keep it off the stack
     make_plan(packed, a.B, a.Hq, a.Nq, a.Nk, p.causal, p.no_skip, a.schedule, dev.num_sms, pl);
     p.stream_k = pl.stream_k;
+    p.zigzag = pl.zigzag;
+    p.n_tt = (a.Nq + kBlockM - 1) / kBlockM;
     p.HT = pl.HT;
     p.W = pl.W;
     p.dp_full = pl.dp_full;
@@ -1198,6 +1224,7 @@ int plan_prefill(int B, int Hq, int Nq, int Nk, int causal, int no_skip, int sch
     info[5] = pl.n_split;
     info[6] = pl.dp_full;
     info[7] = pl.sk_s0;
+    info[8] = pl.zigzag;
     if (items)
         for (int i = 0; i < pl.n_split && i < max_items; ++i) {
             items[i * 5 + 0] = pl.item[i].x;

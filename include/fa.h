@@ -201,11 +201,13 @@ int fa_prefill_backward(const void *q, const void *k, const void *v,
  * tuning and tests; nothing runs on a device.
  *   flags : FA_FLAG_NO_CAUSAL_SKIP and the FA_FLAG_SCHEDULE_* bits, as for
  *           the prefill call
- *   info  : 8 values: stream-K (1) or unit by unit (0), CTAs launched, key-tile
+ *   info  : 9 values: stream-K (1) or unit by unit (0), CTAs launched, key-tile
  *           steps W of all units, steps per (sequence, head), 256-row query
  *           blocks per head, units cut between CTAs, whole units dealt to
  *           every CTA before the cut ranges (CTA c takes units c + k * CTAs),
- *           and the first step S0 of the cut ranges
+ *           the first step S0 of the cut ranges, and 1 when a causal unit
+ *           schedule pairs 128-row query tiles i and T - 1 - i (T tiles per
+ *           sequence) instead of taking adjacent ones
  *   items : NULL or room for max_items rows of 5 values, one per cut unit:
  *           unit, first CTA, last CTA, the unit's steps, the unit's first step.
  *           Units number (b * Hq + h) * blocks + block; CTA c owns the steps

@@ -33,15 +33,32 @@ def kv_tiles(causal, no_skip, nq, nk, row0):
     return 0 if last < 0 else min(tk, last // 128 + 1)
 
 
+def check_pairs(Nq):
+    # The kernel's pairing: unit i of a head holds 128-row tiles i and T - 1 - i
+    # (the latter absent when it is i itself), i < ceil(T / 2) = the units per head.
+    T = (Nq + BM - 1) // BM
+    seen = []
+    for i in range((Nq + R - 1) // R):
+        seen.append(i)
+        if T - 1 - i > i:
+            seen.append(T - 1 - i)
+    assert sorted(seen) == list(range(T)), (Nq, seen)
+
+
 def check_plan(B, H, Nq, Nk, causal, no_skip, sms, flags):
     rc, info, items = binding.fa_prefill_plan(B, H, Nq, Nk, causal, flags, sms)
     assert rc == 0
-    stream_k, G, W, HT, n_qb, n_split, dp_full, s0 = info
+    stream_k, G, W, HT, n_qb, n_split, dp_full, s0, paired = info
     assert n_qb == (Nq + R - 1) // R and len(items) == n_split
     n_units = B * H * n_qb
     if not stream_k:
         assert G == min(n_units, sms) and n_split == 0
+        forced_sk = bool(flags & binding.FA_FLAG_SCHEDULE_STREAM_K) and not (flags & binding.FA_FLAG_SCHEDULE_UNITS)
+        assert paired == int(bool(causal) and not no_skip and n_units <= sms and not forced_sk)
+        if paired:
+            check_pairs(Nq)
         return False
+    assert paired == 0
     assert G == min(sms, 192)
     cost = [max(kv_tiles(causal, no_skip, Nq, Nk, qb * R), kv_tiles(causal, no_skip, Nq, Nk, qb * R + BM))
             for qb in range(n_qb)]
