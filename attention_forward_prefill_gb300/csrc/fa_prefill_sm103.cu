@@ -108,10 +108,10 @@ struct Params {
     // into gridDim.x equal contiguous ranges; a unit cut between two CTAs is
     // finished by the fixup kernel from the partials in ws_o / ws_ml.
     int stream_k;
-    // Causal unit schedule in one round: unit i of a head pairs query tile i with
-    // tile T - 1 - i (T = 128-row tiles per sequence), so that no unit holds more
-    // than T - i key tiles and its two tiles overlap for the first i + 1.
-    int zigzag;
+    // Causal unit schedule in one round (the kernel's ZZ instantiation): unit i
+    // of a head pairs query tile i with tile T - 1 - i (T = 128-row tiles per
+    // sequence), so that no unit holds more than T - i key tiles and its two
+    // tiles overlap for the first i + 1.
     int n_tt;              // T
     int HT;                // key-tile steps per (sequence, head) = pre[n_qb]
     long long W;           // BH * HT
@@ -197,6 +197,7 @@ __device__ __forceinline__ void check_seq(const Params &p, const Work &w) {
     if (bad) atomicCAS(&g_prefill_status, 0, static_cast<int>(FA_ERR_SEQ_LEN));
 }
 
+template <bool ZZ>
 __device__ __forceinline__ bool seg_next(const Params &p, const StepTable &tab, SegCursor &c,
                                          Work &w) {
     int bh, qb;
@@ -231,7 +232,7 @@ __device__ __forceinline__ bool seg_next(const Params &p, const StepTable &tab, 
                               : static_cast<int>(blockIdx.x);
         w.u = k * static_cast<int>(gridDim.x) + r;
         if (w.u >= p.n_units) return false;
-        if (p.zigzag) {  // pair i (tiles i and T - 1 - i); pair 0 holds the most keys
+        if constexpr (ZZ) {  // pair i (tiles i and T - 1 - i); pair 0 holds the most keys
             qb = w.u / p.BH;
             bh = w.u % p.BH;
         } else if (p.causal) {  // heaviest query blocks first
@@ -247,7 +248,7 @@ __device__ __forceinline__ bool seg_next(const Params &p, const StepTable &tab, 
     w.b = bh / p.Hq;
     w.h = bh % p.Hq;
     load_seq(p, w);
-    if (p.zigzag) {  // (dense: every sequence has T tiles)
+    if constexpr (ZZ) {  // (dense: every sequence has T tiles)
         const int partner = p.n_tt - 1 - qb;
         w.r0 = qb * kBlockM;
         w.r1 = partner > qb ? partner * kBlockM : w.nq;  // an odd T leaves a middle tile alone
@@ -262,8 +263,9 @@ __device__ __forceinline__ bool seg_next(const Params &p, const StepTable &tab, 
 }
 
 // LSE: also write the row log-sum-exp (a separate instantiation, so that the
-// plain forward keeps its registers).
-template <int D, bool BF16, bool LSE>
+// plain forward keeps its registers).  ZZ: the paired-tile causal schedule (its
+// own instantiation, so that the other schedules' code is untouched by it).
+template <int D, bool BF16, bool LSE, bool ZZ>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap map_q,
                    const __grid_constant__ CUtensorMap map_k,
@@ -360,7 +362,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     w.b * p.Hkv + w.hk, pol_kv);
                 }
             };
-            while (ok && seg_next(p, tab, cur, w)) {
+            while (ok && seg_next<ZZ>(p, tab, cur, w)) {
                 if (packed) check_seq(p, w);
                 if (w.j1 <= w.j0) continue;  // no key tiles: the softmax warps write zeros
                 // query tile t is loaded when it has key tiles in [j0, j1)
@@ -445,7 +447,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (fence) tc_fence_after();
                 return static_cast<int>(st);
             };
-            while (ok && seg_next(p, tab, cur, w)) {
+            while (ok && seg_next<ZZ>(p, tab, cur, w)) {
                 const int j0 = w.j0, j1 = w.j1;
                 if (j1 <= j0) continue;  // no key tiles: nothing to multiply
                 // key tiles [j0, e_t) for query tile t (empty when e_t <= j0)
@@ -590,7 +592,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         SegCursor cur;
         seg_begin(p, cur);
         Work w;
-        for (int seg = 0; ok && seg_next(p, tab, cur, w); ++seg) {
+        for (int seg = 0; ok && seg_next<ZZ>(p, tab, cur, w); ++seg) {
             const int j0 = w.j0, j1 = w.j1;
             const int tile_row0 = t ? w.r1 : w.r0;
             const int row = tile_row0 + r;  // query index within the sequence
@@ -657,6 +659,31 @@ __global__ void __launch_bounds__(kThreads, 1)
                     m_ref = m_tile;
                     neg_m = -m_tile;
                 }
+                const uint64_t c2 = f2_pack(cexp, cexp);
+                const uint64_t nm2 = f2_pack(neg_m, neg_m);
+                // eight fp32 partial sums: (lo, hi) halves of four pair slots
+                float sum_lo[4] = {0.f, 0.f, 0.f, 0.f}, sum_hi[4] = {0.f, 0.f, 0.f, 0.f};
+                // P in 32-key quarters: 16 packed registers per TMEM store.  With P
+                // over S (d = 128) each quarter is stored as soon as it is made.  With
+                // a separate P buffer (d = 64) the whole row is made first and the
+                // store alone waits for the previous P V product (the last reader of
+                // the buffer), so the exponentials overlap that product.
+                uint32_t pk[4][16];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+#pragma unroll
+                    for (int c2i = 0; c2i < 16; ++c2i) {
+                        const uint64_t x = ffma2(f2_pack(__uint_as_float(sr[q][2 * c2i]),
+                                                         __uint_as_float(sr[q][2 * c2i + 1])),
+                                                 c2, nm2);
+                        pk[q][c2i] = pack2t<BF16>(ex2_approx(f2_lo(x)), ex2_approx(f2_hi(x)));
+                        // l sums the same rounded weights the PV product uses,
+                        // so a row dominated by one key returns that value row.
+                        // Each 16-bit weight is added straight into fp32.
+                        add_pair16<BF16>(sum_lo[c2i & 3], sum_hi[c2i & 3], pk[q][c2i]);
+                    }
+                    if constexpr (!L::kSepP) tmem_st16(p_addr + q * 16, pk[q]);
+                }
                 if constexpr (L::kSepP) {
                     // P_t(j-1) and O_t must be done with before P_t(j) and a rescale
                     if (j > j0) {
@@ -664,27 +691,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ++pvc;
                         tc_fence_after();
                     }
-                }
-                const uint64_t c2 = f2_pack(cexp, cexp);
-                const uint64_t nm2 = f2_pack(neg_m, neg_m);
-                // eight fp32 partial sums: (lo, hi) halves of four pair slots
-                float sum_lo[4] = {0.f, 0.f, 0.f, 0.f}, sum_hi[4] = {0.f, 0.f, 0.f, 0.f};
-                // P in 32-key quarters: 16 packed registers per TMEM store.
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    uint32_t pk[16];
-#pragma unroll
-                    for (int c2i = 0; c2i < 16; ++c2i) {
-                        const uint64_t x = ffma2(f2_pack(__uint_as_float(sr[q][2 * c2i]),
-                                                         __uint_as_float(sr[q][2 * c2i + 1])),
-                                                 c2, nm2);
-                        pk[c2i] = pack2t<BF16>(ex2_approx(f2_lo(x)), ex2_approx(f2_hi(x)));
-                        // l sums the same rounded weights the PV product uses,
-                        // so a row dominated by one key returns that value row.
-                        // Each 16-bit weight is added straight into fp32.
-                        add_pair16<BF16>(sum_lo[c2i & 3], sum_hi[c2i & 3], pk[c2i]);
-                    }
-                    tmem_st16(p_addr + q * 16, pk);
+                    for (int q = 0; q < 4; ++q) tmem_st16(p_addr + q * 16, pk[q]);
                 }
                 const uint64_t s01 = fadd2(f2_pack(sum_lo[0], sum_hi[0]), f2_pack(sum_lo[1], sum_hi[1]));
                 const uint64_t s23 = fadd2(f2_pack(sum_lo[2], sum_hi[2]), f2_pack(sum_lo[3], sum_hi[3]));
@@ -1097,16 +1105,6 @@ int launch_d_lse(const PrefillLaunch &a, const DeviceInfo &dev, cudaStream_t str
         if ((rc = make_map(&mk, a.k, D, false, a.Nk, (long long)a.B * a.Hkv, a.in_bf16)) != FA_OK) return rc;
         if ((rc = make_map(&mv, a.v, D, false, a.Nk, (long long)a.B * a.Hkv, a.in_bf16)) != FA_OK) return rc;
     }
-    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D, BF16, LSE>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
-    if (e != cudaSuccess) return cuda_fail(e);
-    // The setmaxnreg split inside the kernel draws on the launch allocation:
-    // refuse to launch a build whose register count would make it wait forever.
-    cudaFuncAttributes fattr;
-    e = cudaFuncGetAttributes(&fattr, prefill_kernel<D, BF16, LSE>);
-    if (e != cudaSuccess) return cuda_fail(e);
-    if (fattr.numRegs < kMinLaunchRegs) return cuda_fail(cudaErrorInvalidConfiguration);
-
     Params p;
     p.out = a.out;
     p.lse = a.lse;
@@ -1134,7 +1132,6 @@ int launch_d_lse(const PrefillLaunch &a, const DeviceInfo &dev, cudaStream_t str
     p.scale_log2 = scale * 1.4426950408889634f;
     p.scale_log2_abs = fabsf(p.scale_log2);
     p.stream_k = 0;
-    p.zigzag = 0;
     p.n_tt = 0;
     p.HT = 0;
     p.W = 0;
@@ -1144,8 +1141,16 @@ int launch_d_lse(const PrefillLaunch &a, const DeviceInfo &dev, cudaStream_t str
     static thread_local Plan pl;  // ~8 KB: keep it off the stack
     make_plan(packed, a.B, a.Hq, a.Nq, a.Nk, p.causal, p.no_skip, a.schedule, dev.num_sms, pl);
     p.stream_k = pl.stream_k;
-    p.zigzag = pl.zigzag;
     p.n_tt = (a.Nq + kBlockM - 1) / kBlockM;
+    const auto kernel = pl.zigzag ? prefill_kernel<D, BF16, LSE, true> : prefill_kernel<D, BF16, LSE, false>;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
+    if (e != cudaSuccess) return cuda_fail(e);
+    // The setmaxnreg split inside the kernel draws on the launch allocation:
+    // refuse to launch a build whose register count would make it wait forever.
+    cudaFuncAttributes fattr;
+    e = cudaFuncGetAttributes(&fattr, kernel);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (fattr.numRegs < kMinLaunchRegs) return cuda_fail(cudaErrorInvalidConfiguration);
     p.HT = pl.HT;
     p.W = pl.W;
     p.dp_full = pl.dp_full;
@@ -1187,7 +1192,7 @@ int launch_d_lse(const PrefillLaunch &a, const DeviceInfo &dev, cudaStream_t str
         }
     }
     const StepTable &tab = pl.tab;
-    prefill_kernel<D, BF16, LSE><<<grid, kThreads, L::kSmemBytes, stream>>>(mq, mk, mv, p, tab);
+    kernel<<<grid, kThreads, L::kSmemBytes, stream>>>(mq, mk, mv, p, tab);
     e = cudaGetLastError();
     if (e == cudaSuccess && f.n_split > 0) {
         cudaLaunchConfig_t cfg = {};
