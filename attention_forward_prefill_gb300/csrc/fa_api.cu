@@ -263,7 +263,7 @@ int fa_prefill_gqa(const void *q, const void *k, const void *v, void *out, int B
 namespace {
 // Copy streams and events of the host-buffer pipeline, one set per device,
 // created on first use and kept for the life of the process.
-constexpr int kHostChunks = 4;
+constexpr int kHostChunks = 8;
 struct HostPipe {
     bool ready = false;
     cudaStream_t s_in = nullptr, s_out = nullptr;
@@ -293,6 +293,38 @@ cudaError_t host_pipe(int dev, HostPipe **out) {
 }
 
 size_t round_up256(size_t x) { return (x + 255) / 256 * 256; }
+
+// Chunks of the host-buffer pipeline, as key/value-head boundaries
+// bound[0] = 0 < bound[1] < ... < bound[n] = n_kv; returns n.  Only the first
+// chunk's copy in and the last chunk's copy out run under no kernel, so the
+// chunk sizes ramp up from a small first chunk and back down to a small last
+// one (weights min(i + 1, n - i)).  Every chunk still holds at least
+// kHostMinSteps key-tile steps per SM, so that its kernel keeps the GPU busy:
+// long sequences can go a head at a time, short ones take fewer, larger chunks.
+constexpr long long kHostMinSteps = 24;
+int host_chunk_plan(long long n_kv, int group, int Nq, int Nk, bool causal, int num_sms,
+                    long long bound[kHostChunks + 1]) {
+    const long long q_tiles = (Nq + 127) / 128, k_tiles = (Nk + 127) / 128;
+    long long steps = group * q_tiles * k_tiles;  // 128 x 128 tile products per key/value head
+    if (causal) steps = (steps + 1) / 2;
+    const long long min_heads = std::max(1LL, (kHostMinSteps * num_sms + steps - 1) / steps);
+    int n = static_cast<int>(std::min<long long>(kHostChunks, n_kv));
+    for (; n > 1; --n) {
+        long long w = 0;
+        for (int i = 0; i < n; ++i) w += std::min(i + 1, n - i);
+        if (n_kv >= min_heads * w) break;  // the first and last chunks hold min_heads or more
+    }
+    long long w_total = 0;
+    for (int i = 0; i < n; ++i) w_total += std::min(i + 1, n - i);
+    bound[0] = 0;
+    long long w_cum = 0;
+    for (int i = 0; i < n; ++i) {
+        w_cum += std::min(i + 1, n - i);
+        const long long b = (n_kv * w_cum + w_total / 2) / w_total;
+        bound[i + 1] = std::min(n_kv - (n - 1 - i), std::max(bound[i] + 1, b));
+    }
+    return n;
+}
 }  // namespace
 
 extern "C" {
@@ -337,7 +369,11 @@ int fa_prefill_host(const void *q_host, const void *k_host, const void *v_host, 
     char *oh = static_cast<char *>(out_host);
     // Small problems gain nothing from overlap: one chunk under 8 MB of traffic.
     const size_t total = q_bytes + 2 * kv_bytes + o_bytes;
-    const int n_ch = static_cast<int>(std::min<long long>(total < (8u << 20) ? 1 : kHostChunks, n_kv));
+    long long bound[kHostChunks + 1];
+    int n_ch = 1;
+    bound[0] = 0;
+    bound[1] = n_kv;
+    if (total >= (8u << 20)) n_ch = host_chunk_plan(n_kv, group, Nq, Nk, causal != 0, dev.num_sms, bound);
     // the copy streams start after the work already on `stream` (which also
     // orders the pool allocation before them)
     if ((e = cudaEventRecord(hp->start, st)) || (e = cudaStreamWaitEvent(hp->s_in, hp->start, 0)) ||
@@ -347,7 +383,7 @@ int fa_prefill_host(const void *q_host, const void *k_host, const void *v_host, 
     }
     rc = FA_OK;
     for (int c = 0; c < n_ch && rc == FA_OK; ++c) {
-        const long long h0 = n_kv * c / n_ch, h1 = n_kv * (c + 1) / n_ch;  // key/value heads [h0, h1)
+        const long long h0 = bound[c], h1 = bound[c + 1];  // key/value heads [h0, h1)
         const size_t qo = q_head * group * h0, qn = q_head * group * (h1 - h0);
         const size_t ko = kv_head * h0, kn = kv_head * (h1 - h0);
         const size_t oo = o_head * group * h0, on = o_head * group * (h1 - h0);

@@ -137,10 +137,14 @@ int fa_prefill_gqa(const void *q, const void *k, const void *v, void *out,
  * result when the stream reaches that point, and the four host buffers must
  * stay valid until then.  Page-locked (pinned) host memory lets the copies run
  * asynchronously; other host memory works but its copies serialise.
- * The flattened key/value heads (B * Hkv) are cut into up to four chunks:
+ * The flattened key/value heads (B * Hkv) are cut into up to eight chunks:
  * chunk c's input copies (on a library-owned copy stream), its kernel (on
  * `stream`) and its output copy (on a second copy stream) overlap the
- * neighbouring chunks'.  Device buffers for q, k, v and out come from the
+ * neighbouring chunks'.  Only the first chunk's input copies and the last
+ * chunk's output copy overlap no kernel, so the chunk sizes ramp up from a
+ * small first chunk and back down to a small last one, each chunk holding at
+ * least 24 128 x 128 tile products per SM (fewer, larger chunks for short
+ * sequences).  Device buffers for q, k, v and out come from the
  * library's stream-ordered pool and go back to it after the last copy.
  *   q_host, out_host : [B][Hq][Nq][d]    k_host, v_host : [B][Hkv][Nk][d]
  * Other arguments as fa_prefill_gqa.  Errors as fa_prefill_gqa, plus

@@ -33,7 +33,8 @@ def host_tensor(bits, dtype, pinned):
 
 @pytest.mark.parametrize("shape,causal,pinned,out_dtype", [
     ((2, 4, 2, 300, 700, 64), True, True, "f32"),       # one chunk (under 8 MB), chunk prompt
-    ((1, 8, 8, 2048, 2048, 128), False, True, "f32"),   # four chunks of two heads
+    ((1, 6, 6, 8192, 8192, 128), False, True, "f32"),   # chunks of 1, 2, 2 and 1 heads
+    ((1, 16, 4, 4096, 4096, 64), True, True, "bf16"),   # grouped heads, two chunks of 2 KV heads
     ((2, 6, 2, 1500, 1500, 64), True, False, "f16"),    # pageable memory, grouped heads
 ])
 def test_host_buffers_match_the_oracle(fa, oracle_mod, shape, causal, pinned, out_dtype):
@@ -56,8 +57,9 @@ def test_host_buffers_match_the_oracle(fa, oracle_mod, shape, causal, pinned, ou
 
 
 def test_host_buffers_equal_the_device_call_bit_for_bit(fa):
+    # four key/value heads of 8192 keys: chunks of 1, 2 and 1 heads
     import torch
-    B, Hq, Hkv, N, d = 2, 8, 2, 2048, 128
+    B, Hq, Hkv, N, d = 2, 8, 2, 8192, 128
     q, k, v = (inputs.normal_bits((B, h, N, d), 1600 + i, "bf16") for i, h in enumerate((Hq, Hkv, Hkv)))
     hq, hk, hv = (host_tensor(x, "bf16", True) for x in (q, k, v))
     for causal in (False, True):
