@@ -4,9 +4,10 @@ Each case draws its shape and options from a fixed seed: batch, query and
 key/value heads (grouped or not), query and key lengths (square, chunked, or
 more queries than keys), head size, causal mask, input and output types and
 the schedule flags for prefill; a packed batch of random lengths; decode with
-random lengths (zero included) and a random split count, plain and grouped.
-The sizes stay small enough for the oracle to finish in seconds, and span
-several tiles and ragged tails.
+random lengths (zero included) and a random split count, plain and grouped;
+the backward with grouped heads, both masks, every gradient type and tiny
+lengths.  The sizes stay small enough for the oracle to finish in seconds,
+and span several tiles and ragged tails.
 """
 import numpy as np
 import pytest
@@ -126,3 +127,63 @@ def test_random_decode(fa, oracle_mod, case):
     want = oracle_mod.decode(*(oracle_mod.bits_to_f64(x, dt) for x in (q, kc, vc)), lens, 1.0 / np.sqrt(d))
     G.assert_close(G.device_to_f64(out), want, dt, "f32",
                    f"decode case {case}: B={B} Hq={Hq} Hkv={Hkv} L={L} d={d} splits={splits}")
+
+
+# The backward: the bound against the exact gradient is the per-tensor one of
+# the fixed-shape backward tests (1% / 0.15% of max|G| for bf16 / fp16 inputs),
+# or 1.25 times the error that the method's own rounding points (16-bit P and dS
+# into the products, D = dO.O over the 16-bit forward output) give on the same
+# inputs in fp64, whichever is larger, plus the rounding of the gradient's output
+# type.  The second term matters for tiny problems: with two keys per row, dQ is
+# small next to the rounding of O inside D.
+BWD_TOL = {"bf16": 1e-2, "f16": 1.5e-3}
+GRAD_ROUND = {"f32": 0.0, "f16": 2.0 ** -11, "bf16": 2.0 ** -8}
+
+
+def rounding_model_backward(f, causal, scale, dt, group):
+    from oracle import method_model as mm
+    q, k, v, g = f
+    dq, dk, dv = np.zeros(q.shape), np.zeros(k.shape), np.zeros(v.shape)
+    for b in range(q.shape[0]):
+        for h in range(q.shape[1]):
+            a, bb, c = mm.backward_with_rounding(q[b, h], k[b, h // group], v[b, h // group], g[b, h],
+                                                 causal, scale, dt)
+            dq[b, h] = a
+            dk[b, h // group] += bb
+            dv[b, h // group] += c
+    return dq, dk, dv
+
+
+@pytest.mark.parametrize("case", range(12))
+def test_random_backward(fa, oracle_mod, case):
+    import torch
+    rng = np.random.default_rng(8000 + case)
+    B = int(rng.integers(1, 3))
+    Hkv = int(rng.integers(1, 4))
+    H = Hkv * int(rng.choice([1, 2, 3]))
+    N = int(rng.integers(1, 600))
+    if case % 4 == 3:
+        N = int(rng.choice([1, 2, 127, 129]))  # a single row, a single tile, one past a tile
+    d = int(rng.choice([64, 128]))
+    dt = str(rng.choice(["f16", "bf16"]))
+    causal = case % 2 == 1
+    grad = str(rng.choice(["f32", "f16", "bf16"]))
+    scale = float(rng.choice([1.0 / np.sqrt(d), 0.3, -0.2]))
+    q, g = (inputs.normal_bits((B, H, N, d), 8100 + 10 * case + i, dt) for i in (0, 3))
+    k, v = (inputs.normal_bits((B, Hkv, N, d), 8100 + 10 * case + i, dt) for i in (1, 2))
+    qd, kd, vd, gd = (G.bits_to_device(x, dt) for x in (q, k, v, g))
+    out, lse = fa.prefill_with_lse(qd, kd, vd, causal=causal, scale=scale)
+    grads = fa.prefill_backward(qd, kd, vd, out, gd, lse, causal=causal, scale=scale,
+                                grad_dtype=G.torch_dtype(grad))
+    torch.cuda.synchronize()
+    f = [oracle_mod.bits_to_f64(x, dt) for x in (q, k, v, g)]
+    want = oracle_mod.attention_backward(*f, causal, scale, threads=G.THREADS)
+    model = rounding_model_backward(f, causal, scale, dt, H // Hkv)
+    for name, got_t, w, m in zip(("dq", "dk", "dv"), grads, want, model):
+        got = G.device_to_f64(got_t)
+        assert got.shape == w.shape
+        top = max(np.abs(w).max(), 1e-30)
+        tol = max(BWD_TOL[dt], 1.25 * float(np.abs(m - w).max() / top)) + GRAD_ROUND[grad]
+        e = float(np.abs(got - w).max() / top)
+        assert e <= tol, (f"{name} case {case}: B={B} H={H} Hkv={Hkv} N={N} d={d} {dt}->{grad} "
+                          f"causal={causal} scale={scale:.3f}: {e:.3e} > {tol:.3e}")
