@@ -41,13 +41,12 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # ncu capture, valid only for the kernel source it was taken on: the first 16 hex
 # digits of the sha256 of the listed source files, in order.
 NCU_TRAFFIC = {
-    # ncu --set full of one prefill_kernel<128> launch of the N=8192 step problem
-    # (B=1, H=16, d=128, bf16); the other lengths are scaled by the bytes the
-    # launch must move (linear in N).
+    # one prefill_kernel<128> launch of each of the step's problems (B=1, H=16,
+    # d=128, bf16): --set full at N=8192, the two DRAM counters alone at 4096 and
+    # 16384 (one pass each, on the full-size problem).
     "prefill": {"src": ["fa_prefill_sm103.cu", "fa_tiles.cuh", "sm103_ptx.cuh"],
-                "src_sha": "8e4404321761bd75",
-                "bytes_per_launch": {"4096": 114.76e6 / 2, "8192": 114.76e6, "16384": 114.76e6 * 2},
-                "measured_at": "8192", "scaled": ["4096", "16384"]},
+                "src_sha": "aa0b899ef579541d",
+                "bytes_per_launch": {"4096": 50.45e6, "8192": 114.47e6, "16384": 253.67e6}},
     # one decode_split_kernel<64> launch of the step's decode problem (B=32, H=14)
     "decode": {"src": ["fa_decode_sm103.cu", "sm103_ptx.cuh"], "src_sha": "c3e7decaeb0c1c3f",
                "bytes_per_launch": 263.59e6},
