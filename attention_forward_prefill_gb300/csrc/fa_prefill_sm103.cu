@@ -108,7 +108,7 @@ struct Params {
     // into gridDim.x equal contiguous ranges; a unit cut between two CTAs is
     // finished by the fixup kernel from the partials in ws_o / ws_ml.
     int stream_k;
-    // Causal unit schedule in one round (the kernel's ZZ instantiation): unit i
+    // Causal unit schedule in one round (the kernel's PAIRED instantiation): unit i
     // of a head pairs query tile i with tile T - 1 - i (T = 128-row tiles per
     // sequence), so that no unit holds more than T - i key tiles and its two
     // tiles overlap for the first i + 1.
@@ -197,7 +197,7 @@ __device__ __forceinline__ void check_seq(const Params &p, const Work &w) {
     if (bad) atomicCAS(&g_prefill_status, 0, static_cast<int>(FA_ERR_SEQ_LEN));
 }
 
-template <bool ZZ>
+template <bool PAIRED>
 __device__ __forceinline__ bool seg_next(const Params &p, const StepTable &tab, SegCursor &c,
                                          Work &w) {
     int bh, qb;
@@ -232,7 +232,7 @@ __device__ __forceinline__ bool seg_next(const Params &p, const StepTable &tab, 
                               : static_cast<int>(blockIdx.x);
         w.u = k * static_cast<int>(gridDim.x) + r;
         if (w.u >= p.n_units) return false;
-        if constexpr (ZZ) {  // pair i (tiles i and T - 1 - i); pair 0 holds the most keys
+        if constexpr (PAIRED) {  // pair i (tiles i and T - 1 - i); pair 0 holds the most keys
             qb = w.u / p.BH;
             bh = w.u % p.BH;
         } else if (p.causal) {  // heaviest query blocks first
@@ -248,7 +248,7 @@ __device__ __forceinline__ bool seg_next(const Params &p, const StepTable &tab, 
     w.b = bh / p.Hq;
     w.h = bh % p.Hq;
     load_seq(p, w);
-    if constexpr (ZZ) {  // (dense: every sequence has T tiles)
+    if constexpr (PAIRED) {  // (dense: every sequence has T tiles)
         const int partner = p.n_tt - 1 - qb;
         w.r0 = qb * kBlockM;
         w.r1 = partner > qb ? partner * kBlockM : w.nq;  // an odd T leaves a middle tile alone
@@ -263,9 +263,9 @@ __device__ __forceinline__ bool seg_next(const Params &p, const StepTable &tab, 
 }
 
 // LSE: also write the row log-sum-exp (a separate instantiation, so that the
-// plain forward keeps its registers).  ZZ: the paired-tile causal schedule (its
+// plain forward keeps its registers).  PAIRED: the paired-tile causal schedule (its
 // own instantiation, so that the other schedules' code is untouched by it).
-template <int D, bool BF16, bool LSE, bool ZZ>
+template <int D, bool BF16, bool LSE, bool PAIRED>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap map_q,
                    const __grid_constant__ CUtensorMap map_k,
@@ -362,7 +362,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     w.b * p.Hkv + w.hk, pol_kv);
                 }
             };
-            while (ok && seg_next<ZZ>(p, tab, cur, w)) {
+            while (ok && seg_next<PAIRED>(p, tab, cur, w)) {
                 if (packed) check_seq(p, w);
                 if (w.j1 <= w.j0) continue;  // no key tiles: the softmax warps write zeros
                 // query tile t is loaded when it has key tiles in [j0, j1)
@@ -447,7 +447,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (fence) tc_fence_after();
                 return static_cast<int>(st);
             };
-            while (ok && seg_next<ZZ>(p, tab, cur, w)) {
+            while (ok && seg_next<PAIRED>(p, tab, cur, w)) {
                 const int j0 = w.j0, j1 = w.j1;
                 if (j1 <= j0) continue;  // no key tiles: nothing to multiply
                 // key tiles [j0, e_t) for query tile t (empty when e_t <= j0)
@@ -592,7 +592,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         SegCursor cur;
         seg_begin(p, cur);
         Work w;
-        for (int seg = 0; ok && seg_next<ZZ>(p, tab, cur, w); ++seg) {
+        for (int seg = 0; ok && seg_next<PAIRED>(p, tab, cur, w); ++seg) {
             const int j0 = w.j0, j1 = w.j1;
             const int tile_row0 = t ? w.r1 : w.r0;
             const int row = tile_row0 + r;  // query index within the sequence
@@ -973,7 +973,7 @@ constexpr long long kCausalStepPct = 108;
 
 struct Plan {
     int stream_k;
-    int zigzag;
+    int paired;
     int grid;
     int n_qb;
     int HT;
@@ -999,7 +999,7 @@ void make_plan(bool packed, int B, int Hq, int Nq, int Nk, int causal, int no_sk
     const int n_units = BH * n_qb;
     const int sms = num_sms < kMaxSplit ? num_sms : kMaxSplit;
     pl.stream_k = 0;
-    pl.zigzag = 0;
+    pl.paired = 0;
     pl.n_qb = n_qb;
     pl.HT = 0;
     pl.W = 0;
@@ -1010,8 +1010,8 @@ void make_plan(bool packed, int B, int Hq, int Nq, int Nk, int causal, int no_sk
     pl.tab.pre[0] = 0;
     // A causal dense problem whose units fit in one round runs unit by unit with
     // paired query tiles (i, T - 1 - i) unless stream-K is taken below.
-    const bool zz = !packed && causal && !no_skip && n_units <= num_sms && schedule != 2;
-    pl.zigzag = zz ? 1 : 0;
+    const bool pair_tiles = !packed && causal && !no_skip && n_units <= num_sms && schedule != 2;
+    pl.paired = pair_tiles ? 1 : 0;
     const bool sk_ok = !packed && n_qb <= kMaxPre && n_units >= 2 && (!causal || no_skip || Nk >= Nq) &&
                        schedule != 1;
     if (!sk_ok) return;
@@ -1045,7 +1045,7 @@ void make_plan(bool packed, int B, int Hq, int Nq, int Nk, int causal, int no_sk
     }
     if (!take) return;
     pl.stream_k = 1;
-    pl.zigzag = 0;
+    pl.paired = 0;
     pl.HT = HT;
     pl.W = W;
     const int grid = sms;
@@ -1142,7 +1142,7 @@ int launch_d_lse(const PrefillLaunch &a, const DeviceInfo &dev, cudaStream_t str
     make_plan(packed, a.B, a.Hq, a.Nq, a.Nk, p.causal, p.no_skip, a.schedule, dev.num_sms, pl);
     p.stream_k = pl.stream_k;
     p.n_tt = (a.Nq + kBlockM - 1) / kBlockM;
-    const auto kernel = pl.zigzag ? prefill_kernel<D, BF16, LSE, true> : prefill_kernel<D, BF16, LSE, false>;
+    const auto kernel = pl.paired ? prefill_kernel<D, BF16, LSE, true> : prefill_kernel<D, BF16, LSE, false>;
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
     if (e != cudaSuccess) return cuda_fail(e);
     // The setmaxnreg split inside the kernel draws on the launch allocation:
@@ -1229,7 +1229,7 @@ int plan_prefill(int B, int Hq, int Nq, int Nk, int causal, int no_skip, int sch
     info[5] = pl.n_split;
     info[6] = pl.dp_full;
     info[7] = pl.sk_s0;
-    info[8] = pl.zigzag;
+    info[8] = pl.paired;
     if (items)
         for (int i = 0; i < pl.n_split && i < max_items; ++i) {
             items[i * 5 + 0] = pl.item[i].x;
