@@ -262,11 +262,17 @@ int fa_prefill_gqa(const void *q, const void *k, const void *v, void *out, int B
 
 namespace {
 // Copy streams and events of the host-buffer pipeline, one set per device,
-// created on first use and kept for the life of the process.
+// created on first use and kept for the life of the process.  The input copies
+// of every call share one stream (the host link carries one direction's copies
+// at full rate, so the calls' inputs go in call order); the output copies take
+// one of kOutStreams streams in turn, so that one call's outputs never queue
+// behind another call's kernels.
 constexpr int kHostChunks = 8;
+constexpr int kOutStreams = 4;
 struct HostPipe {
     bool ready = false;
-    cudaStream_t s_in = nullptr, s_out = nullptr;
+    cudaStream_t s_in = nullptr, s_out[kOutStreams] = {};
+    int next_out = 0;
     cudaEvent_t start = nullptr, done = nullptr;
     cudaEvent_t in[kHostChunks] = {}, comp[kHostChunks] = {};
 };
@@ -278,10 +284,11 @@ cudaError_t host_pipe(int dev, HostPipe **out) {
     if (!hp.ready) {
         cudaError_t e;
         if ((e = cudaStreamCreateWithFlags(&hp.s_in, cudaStreamNonBlocking)) ||
-            (e = cudaStreamCreateWithFlags(&hp.s_out, cudaStreamNonBlocking)) ||
             (e = cudaEventCreateWithFlags(&hp.start, cudaEventDisableTiming)) ||
             (e = cudaEventCreateWithFlags(&hp.done, cudaEventDisableTiming)))
             return e;
+        for (int i = 0; i < kOutStreams; ++i)
+            if ((e = cudaStreamCreateWithFlags(&hp.s_out[i], cudaStreamNonBlocking))) return e;
         for (int c = 0; c < kHostChunks; ++c)
             if ((e = cudaEventCreateWithFlags(&hp.in[c], cudaEventDisableTiming)) ||
                 (e = cudaEventCreateWithFlags(&hp.comp[c], cudaEventDisableTiming)))
@@ -374,10 +381,13 @@ int fa_prefill_host(const void *q_host, const void *k_host, const void *v_host, 
     bound[0] = 0;
     bound[1] = n_kv;
     if (total >= (8u << 20)) n_ch = host_chunk_plan(n_kv, group, Nq, Nk, causal != 0, dev.num_sms, bound);
+    // this call's output stream (the next of the pool)
+    cudaStream_t s_out = hp->s_out[hp->next_out];
+    hp->next_out = (hp->next_out + 1) % kOutStreams;
     // the copy streams start after the work already on `stream` (which also
     // orders the pool allocation before them)
     if ((e = cudaEventRecord(hp->start, st)) || (e = cudaStreamWaitEvent(hp->s_in, hp->start, 0)) ||
-        (e = cudaStreamWaitEvent(hp->s_out, hp->start, 0))) {
+        (e = cudaStreamWaitEvent(s_out, hp->start, 0))) {
         scratch_free(buf, st);
         return cuda_fail(e);
     }
@@ -419,14 +429,14 @@ int fa_prefill_host(const void *q_host, const void *k_host, const void *v_host, 
         a.schedule = schedule_of(flags);
         rc = launch_prefill(a, dev, st);
         if (rc != FA_OK) break;
-        if ((e = cudaEventRecord(hp->comp[c], st)) || (e = cudaStreamWaitEvent(hp->s_out, hp->comp[c], 0)) ||
-            (e = cudaMemcpyAsync(oh + oo, od + oo, on, cudaMemcpyDeviceToHost, hp->s_out)))
+        if ((e = cudaEventRecord(hp->comp[c], st)) || (e = cudaStreamWaitEvent(s_out, hp->comp[c], 0)) ||
+            (e = cudaMemcpyAsync(oh + oo, od + oo, on, cudaMemcpyDeviceToHost, s_out)))
             rc = cuda_fail(e);
     }
     // `stream` continues after both copy streams (the last output copy, and on
     // an error any input copy already issued); the buffers then go back to the
     // pool, stream-ordered.
-    for (cudaStream_t s : {hp->s_in, hp->s_out}) {
+    for (cudaStream_t s : {hp->s_in, s_out}) {
         if ((e = cudaEventRecord(hp->done, s)) == cudaSuccess) e = cudaStreamWaitEvent(st, hp->done, 0);
         if (e != cudaSuccess && rc == FA_OK) rc = cuda_fail(e);
     }

@@ -138,9 +138,10 @@ int fa_prefill_gqa(const void *q, const void *k, const void *v, void *out,
  * stay valid until then.  Page-locked (pinned) host memory lets the copies run
  * asynchronously; other host memory works but its copies serialise.
  * The flattened key/value heads (B * Hkv) are cut into up to eight chunks:
- * chunk c's input copies (on a library-owned copy stream), its kernel (on
- * `stream`) and its output copy (on a second copy stream) overlap the
- * neighbouring chunks'.  Only the first chunk's input copies and the last
+ * chunk c's input copies (on a library-owned copy stream shared by all
+ * calls), its kernel (on `stream`) and its output copy (on one of four
+ * library-owned output streams, taken in turn by successive calls) overlap
+ * the neighbouring chunks'.  Only the first chunk's input copies and the last
  * chunk's output copy overlap no kernel, so the chunk sizes ramp up from a
  * small first chunk and back down to a small last one, each chunk holding at
  * least 24 128 x 128 tile products per SM (fewer, larger chunks for short
