@@ -564,6 +564,7 @@ int fa_prefill_backward(const void *q, const void *k, const void *v, const void 
     a.scale = scale;
     a.in_bf16 = in_dtype == FA_BF16 ? 1 : 0;
     a.grad_dtype = grad_dtype;
+    a.num_sms = dev.num_sms;
     return launch_backward(a, static_cast<cudaStream_t>(stream));
 }
 

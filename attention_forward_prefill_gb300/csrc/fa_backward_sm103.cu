@@ -83,9 +83,9 @@ struct DqLayout {
     static constexpr int kKOff = 2 * kTileBytes;
     static constexpr int kVOff = kKOff + kKStages * kTileBytes;
     static constexpr int kBarOff = kVOff + kVStages * kTileBytes;
-    // fix_full, s_full, p_ready, acc_done, drain, s_loaded, dq_done,
+    // fix_full, s_full, p_ready, acc_done, drain, s_loaded, dq_done, fix_empty,
     // k_full[KS], k_empty[KS], v_full[VS], v_empty[VS]
-    static constexpr int kNumBars = 7 + 2 * kKStages + 2 * kVStages;
+    static constexpr int kNumBars = 8 + 2 * kKStages + 2 * kVStages;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
     static constexpr int kSmemBytes = kMiscOff + 16 + 1024;
     // TMEM: S | dP | dQ accumulator | dS (16-bit, 64 columns)
@@ -105,6 +105,7 @@ struct BwdParams {
     int grad_dtype;
     float scale;
     float c;            // scale * log2(e)
+    int n_units;        // dq: (query head, query tile) units, dealt to persistent CTAs
 };
 
 // ---------------------------------------------------------------- D and L2
@@ -622,6 +623,32 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 }
 
 // ---------------------------------------------------------------- dQ
+// One unit of the dQ pass: query tile `it` of (batch, query head) `bh`, and the
+// key tiles it sees.  A persistent CTA takes units k = 0, 1, ... of its own:
+// unit k * G + c, or k * G + G - 1 - c in odd rounds (snake order over rounds of
+// G = gridDim.x).  Causal units come heaviest first (the last query tiles of
+// every head), so the light ones fill the last round.
+struct DqUnit {
+    int bh, bhk, it, n_iter;
+};
+
+__device__ __forceinline__ bool dq_unit(const BwdParams &p, int k, DqUnit &u) {
+    const long long G = gridDim.x, c = blockIdx.x;
+    const long long idx = static_cast<long long>(k) * G + ((k & 1) ? G - 1 - c : c);
+    if (idx >= p.n_units) return false;
+    const int n_heads = p.n_units / p.n_t;
+    if (p.causal) {
+        u.bh = static_cast<int>(idx % n_heads);
+        u.it = p.n_t - 1 - static_cast<int>(idx / n_heads);
+    } else {
+        u.bh = static_cast<int>(idx / p.n_t);
+        u.it = static_cast<int>(idx % p.n_t);
+    }
+    u.bhk = (u.bh / p.Hq) * p.Hkv + (u.bh % p.Hq) / p.group;  // its key/value head
+    u.n_iter = p.causal ? u.it + 1 : p.n_t;                    // key tiles the queries see
+    return true;
+}
+
 template <int D, bool BF16>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
@@ -634,20 +661,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kBarOff);
     uint64_t *fix_full = bars + 0, *s_full = bars + 1, *p_ready = bars + 2, *acc_done = bars + 3;
     uint64_t *drain = bars + 4, *s_loaded = bars + 5;
-    uint64_t *dq_done = bars + 6;
-    uint64_t *k_full = bars + 7, *k_empty = k_full + L::kKStages;
+    uint64_t *dq_done = bars + 6, *fix_empty = bars + 7;
+    uint64_t *k_full = bars + 8, *k_empty = k_full + L::kKStages;
     uint64_t *v_full = k_empty + L::kKStages, *v_empty = v_full + L::kVStages;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kMiscOff);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kMiscOff + 4);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // Causal: CTAs are dealt query-tile-major, heaviest (last) query tiles of
-    // every head first.
-    const int n_heads = static_cast<int>(gridDim.x) / p.n_t;
-    const int bh = p.causal ? blockIdx.x % n_heads : blockIdx.x / p.n_t;  // (batch, query head)
-    const int bhk = (bh / p.Hq) * p.Hkv + (bh % p.Hq) / p.group;          // its key/value head
-    const int it = p.causal ? p.n_t - 1 - blockIdx.x / n_heads : blockIdx.x % p.n_t;
-    const int n_iter = p.causal ? it + 1 : p.n_t;              // key tiles the queries see
+    // Barriers that complete once per unit (fix_full, fix_empty, acc_done) wait on
+    // the parity of the unit counter k; those that complete once per key tile on
+    // the parity of the CTA's key-tile counter g, which runs on across units, and
+    // so do the K and V rings.
 
     if (threadIdx.x == 0) {
         mbar_init(fix_full, 1);
@@ -657,6 +681,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_init(drain, 1);
         mbar_init(s_loaded, kBwdEltWarps);
         mbar_init(dq_done, 1);
+        mbar_init(fix_empty, 1);
         for (int s = 0; s < L::kKStages; ++s) {
             mbar_init(k_full + s, 1);
             mbar_init(k_empty + s, 1);
@@ -688,41 +713,50 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             uint8_t *fix = smem + L::kFixOff, *kring = smem + L::kKOff, *vring = smem + L::kVOff;
             const uint64_t pol = l2_policy_evict_last();
             bool ok = true;
-            mbar_arrive_expect_tx(fix_full, 2 * L::kTileBytes);
-            for (int c = 0; c < L::kChunks; ++c) {
-                tma_load_3d(fix + c * kSlabBytes, &map_q, fix_full, c * 64, it * kRows, bh, pol);
-                tma_load_3d(fix + L::kTileBytes + c * kSlabBytes, &map_do, fix_full, c * 64, it * kRows, bh,
-                            pol);
-            }
-            int nk = 0, nv = 0;  // K and V tiles issued
-            for (int n = 0; n < n_iter && ok; ++n) {
-                const int ks = n % L::kKStages;
-                if (n >= L::kKStages &&
-                    !mbar_wait(k_empty + ks, ((n / L::kKStages) - 1) & 1, abort_flag, kWatchdogNs)) {
+            int nfix = 0, nk = 0, nv = 0;  // Q/dO, K and V tiles issued
+            DqUnit u;
+            for (int k = 0; ok && dq_unit(p, k, u); ++k) {
+                // Q and dO of the unit before must have been read by its last products
+                if (k > 0 && !mbar_wait(fix_empty, (k - 1) & 1, abort_flag, kWatchdogNs)) {
                     ok = false;
                     break;
                 }
-                mbar_arrive_expect_tx(k_full + ks, L::kTileBytes);
-                for (int c = 0; c < L::kChunks; ++c)
-                    tma_load_3d(kring + ks * L::kTileBytes + c * kSlabBytes, &map_k, k_full + ks, c * 64, n * kRows,
-                                bhk, pol);
-                ++nk;
-                const int vs = n % L::kVStages;
-                if (n >= L::kVStages &&
-                    !mbar_wait(v_empty + vs, ((n / L::kVStages) - 1) & 1, abort_flag, kWatchdogNs)) {
-                    ok = false;
-                    break;
+                mbar_arrive_expect_tx(fix_full, 2 * L::kTileBytes);
+                for (int c = 0; c < L::kChunks; ++c) {
+                    tma_load_3d(fix + c * kSlabBytes, &map_q, fix_full, c * 64, u.it * kRows, u.bh, pol);
+                    tma_load_3d(fix + L::kTileBytes + c * kSlabBytes, &map_do, fix_full, c * 64, u.it * kRows,
+                                u.bh, pol);
                 }
-                mbar_arrive_expect_tx(v_full + vs, L::kTileBytes);
-                for (int c = 0; c < L::kChunks; ++c)
-                    tma_load_3d(vring + vs * L::kTileBytes + c * kSlabBytes, &map_v, v_full + vs, c * 64, n * kRows,
-                                bhk, pol);
-                ++nv;
+                ++nfix;
+                for (int n = 0; n < u.n_iter; ++n) {
+                    const int ks = nk % L::kKStages;
+                    if (nk >= L::kKStages &&
+                        !mbar_wait(k_empty + ks, ((nk / L::kKStages) - 1) & 1, abort_flag, kWatchdogNs)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(k_full + ks, L::kTileBytes);
+                    for (int c = 0; c < L::kChunks; ++c)
+                        tma_load_3d(kring + ks * L::kTileBytes + c * kSlabBytes, &map_k, k_full + ks, c * 64,
+                                    n * kRows, u.bhk, pol);
+                    ++nk;
+                    const int vs = nv % L::kVStages;
+                    if (nv >= L::kVStages &&
+                        !mbar_wait(v_empty + vs, ((nv / L::kVStages) - 1) & 1, abort_flag, kWatchdogNs)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(v_full + vs, L::kTileBytes);
+                    for (int c = 0; c < L::kChunks; ++c)
+                        tma_load_3d(vring + vs * L::kTileBytes + c * kSlabBytes, &map_v, v_full + vs, c * 64,
+                                    n * kRows, u.bhk, pol);
+                    ++nv;
+                }
             }
-            if (!ok) {
+            if (!ok) {  // let every copy already issued land (only the last Q/dO can be in flight)
                 constexpr uint64_t kDrainNs = 200ull * 1000ull * 1000ull;
                 int dummy = 0;
-                mbar_wait(fix_full, 0, &dummy, kDrainNs);
+                if (nfix > 0) mbar_wait(fix_full, (nfix - 1) & 1, &dummy, kDrainNs);
                 for (int m = (nk > L::kKStages ? nk - L::kKStages : 0); m < nk; ++m)
                     mbar_wait(k_full + (m % L::kKStages), (m / L::kKStages) & 1, &dummy, kDrainNs);
                 for (int m = (nv > L::kVStages ? nv - L::kVStages : 0); m < nv; ++m)
@@ -738,8 +772,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             const uint32_t kring = smem_u32(smem + L::kKOff), vring = smem_u32(smem + L::kVOff);
             const uint64_t q_desc = sdesc_sw128(fix, 16, 1024);
             const uint64_t do_desc = sdesc_sw128(fix + L::kTileBytes, 16, 1024);
-            bool ok = mbar_wait(fix_full, 0, abort_flag, kWatchdogNs);
-            // S = Q K_j^T and dP = dO V_j^T (queries on TMEM lanes) for key tile j
+            // S = Q K_j^T and dP = dO V_j^T (queries on TMEM lanes) for the CTA's key tile j
             auto issue_scores = [&](int j) {
                 const int ks = j % L::kKStages, vs = j % L::kVStages;
                 if (!mbar_wait(k_full + ks, (j / L::kKStages) & 1, abort_flag, kWatchdogNs)) return false;
@@ -751,34 +784,53 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 umma_commit(v_empty + vs);  // V_j is read by dP alone
                 return true;
             };
-            if (ok) ok = issue_scores(0);
-            for (int n = 0; n < n_iter && ok; ++n) {
-                // Once every elementwise warp holds S and dP of tile n in registers,
-                // the next tile's products run under their elementwise work.
-                if (n + 1 < n_iter) {
-                    if (!mbar_wait(s_loaded, n & 1, abort_flag, kWatchdogNs)) {
+            bool ok = true;
+            int g = 0;
+            DqUnit u;
+            for (int k = 0; ok && dq_unit(p, k, u); ++k) {
+                if (!mbar_wait(fix_full, k & 1, abort_flag, kWatchdogNs)) { ok = false; break; }
+                tc_fence_after();
+                // The unit's first scores overwrite the last unit's S and dP: every
+                // warp holds those (implied by its P-ready arrival, awaited below).
+                if (g > 0) {
+                    if (!mbar_wait(s_loaded, (g - 1) & 1, abort_flag, kWatchdogNs)) { ok = false; break; }
+                    tc_fence_after();
+                }
+                if (!issue_scores(g)) { ok = false; break; }
+                if (u.n_iter == 1) umma_commit(fix_empty);
+                for (int n = 0; n < u.n_iter && ok; ++n) {
+                    const int gi = g + n;
+                    // Once every elementwise warp holds S and dP of tile gi in
+                    // registers, the next tile's products run under their work.
+                    if (n + 1 < u.n_iter) {
+                        if (!mbar_wait(s_loaded, gi & 1, abort_flag, kWatchdogNs)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        if (!issue_scores(gi + 1)) {
+                            ok = false;
+                            break;
+                        }
+                        // the unit's last reads of Q and dO are issued: free them once done
+                        if (n + 2 == u.n_iter) umma_commit(fix_empty);
+                    }
+                    if (!mbar_wait(p_ready, gi & 1, abort_flag, kWatchdogNs)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    if (!issue_scores(n + 1)) {
-                        ok = false;
-                        break;
-                    }
+                    // dQ += dS K_n (dS from its TMEM columns; K_n MN-major)
+                    const int ks = gi % L::kKStages;
+                    issue_pv<D>(tmem + L::kACol, tmem + L::kDsCol, sdesc_sw128(kring + ks * L::kTileBytes, kSlabBytes, 1024),
+                                idesc_acc, n > 0);
+                    umma_commit(k_empty + ks);
+                    umma_commit(dq_done);
                 }
-                if (!mbar_wait(p_ready, n & 1, abort_flag, kWatchdogNs)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                // dQ += dS K_n (dS from its TMEM columns; K_n MN-major)
-                const int ks = n % L::kKStages;
-                issue_pv<D>(tmem + L::kACol, tmem + L::kDsCol, sdesc_sw128(kring + ks * L::kTileBytes, kSlabBytes, 1024),
-                            idesc_acc, n > 0);
-                umma_commit(k_empty + ks);
-                umma_commit(dq_done);
+                if (!ok) break;
+                umma_commit(acc_done);
+                g += u.n_iter;
             }
-            umma_commit(acc_done);
             umma_commit(drain);
             int dummy = 0;
             mbar_wait(drain, 0, &dummy, kWatchdogNs);
@@ -788,64 +840,74 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int wq = warp & 3, hf = warp >> 2;  // TMEM lane quadrant; column half
         const int r = wq * 32 + lane;
         const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
-        const int qrow = it * kRows + r;
-        // the vectors are padded to whole tiles per head; dQ rows are not
-        const size_t vi = static_cast<size_t>(bh) * p.npad + qrow;
-        const size_t li = static_cast<size_t>(bh) * p.N + qrow;
-        const float nl2_r = qrow < p.N ? p.lse2[vi] : 0.f;
-        const float nd_r = qrow < p.N ? p.dsum[vi] : 0.f;
         bool ok = true;
-        for (int n = 0; n < n_iter && ok; ++n) {
-            if (!warp_wait(s_full, n & 1, abort_flag)) { ok = false; break; }
-            tc_fence_after();
-            uint32_t sr[2][32], dr[2][32];
+        int g = 0;
+        DqUnit u;
+        for (int k = 0; ok && dq_unit(p, k, u); ++k) {
+            const int qrow = u.it * kRows + r;
+            // the vectors are padded to whole tiles per head; dQ rows are not
+            const size_t vi = static_cast<size_t>(u.bh) * p.npad + qrow;
+            const size_t li = static_cast<size_t>(u.bh) * p.N + qrow;
+            const float nl2_r = qrow < p.N ? p.lse2[vi] : 0.f;
+            const float nd_r = qrow < p.N ? p.dsum[vi] : 0.f;
+            for (int n = 0; n < u.n_iter && ok; ++n) {
+                const int gi = g + n;
+                if (!warp_wait(s_full, gi & 1, abort_flag)) { ok = false; break; }
+                tc_fence_after();
+                uint32_t sr[2][32], dr[2][32];
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                tmem_ld32(tmem + lane_off + L::kXCol + (2 * hf + h) * 32, sr[h]);
-                tmem_ld32(tmem + lane_off + L::kYCol + (2 * hf + h) * 32, dr[h]);
-            }
-            tmem_ld_wait();
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                reg_fence32(sr[h]);
-                reg_fence32(dr[h]);
-            }
-            // S and dP are in registers: the MMA thread may overwrite them
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(s_loaded);
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int q = 2 * hf + h;
-                // column col is key n * 128 + 32 q + col: visible when it exists, the
-                // row exists and, causally, key <= query
-                const int kb = n * kRows + q * 32;
-                uint32_t vis = 0xffffffffu;
-                if (kb + 32 > p.N) vis = p.N > kb ? (0xffffffffu >> (32 - (p.N - kb))) : 0u;
-                if (qrow >= p.N) vis = 0u;
-                if (p.causal) {
-                    const int hi = qrow - kb;  // last visible column
-                    vis &= hi < 0 ? 0u : (hi >= 31 ? 0xffffffffu : (0xffffffffu >> (31 - hi)));
+                for (int h = 0; h < 2; ++h) {
+                    tmem_ld32(tmem + lane_off + L::kXCol + (2 * hf + h) * 32, sr[h]);
+                    tmem_ld32(tmem + lane_off + L::kYCol + (2 * hf + h) * 32, dr[h]);
                 }
-                uint32_t pk[16], dk[16];
-                weights_quarter<BF16, false>(sr[h], dr[h], pk, dk, p.c, nullptr, nullptr, nl2_r, nd_r, vis);
-                if (h == 0 && n > 0) {
-                    // dS of tile n - 1 must have been read by its product.  This also
-                    // keeps p_ready from completing twice before the MMA thread,
-                    // which committed dq_done after seeing p_ready of tile n - 1, looks.
-                    if (!warp_wait(dq_done, (n - 1) & 1, abort_flag)) { ok = false; break; }
-                    tc_fence_after();
+                tmem_ld_wait();
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    reg_fence32(sr[h]);
+                    reg_fence32(dr[h]);
                 }
-                tmem_st16(tmem + lane_off + L::kDsCol + q * 16, dk);
+                // S and dP are in registers: the MMA thread may overwrite them
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(s_loaded);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int q = 2 * hf + h;
+                    // column col is key n * 128 + 32 q + col: visible when it exists, the
+                    // row exists and, causally, key <= query
+                    const int kb = n * kRows + q * 32;
+                    uint32_t vis = 0xffffffffu;
+                    if (kb + 32 > p.N) vis = p.N > kb ? (0xffffffffu >> (32 - (p.N - kb))) : 0u;
+                    if (qrow >= p.N) vis = 0u;
+                    if (p.causal) {
+                        const int hi = qrow - kb;  // last visible column
+                        vis &= hi < 0 ? 0u : (hi >= 31 ? 0xffffffffu : (0xffffffffu >> (31 - hi)));
+                    }
+                    uint32_t pk[16], dk[16];
+                    weights_quarter<BF16, false>(sr[h], dr[h], pk, dk, p.c, nullptr, nullptr, nl2_r, nd_r, vis);
+                    if (h == 0 && gi > 0) {
+                        // dS of the CTA's previous key tile must have been read by its
+                        // product.  This also keeps p_ready from completing twice before
+                        // the MMA thread, which committed dq_done after seeing the
+                        // previous p_ready, looks.
+                        if (!warp_wait(dq_done, (gi - 1) & 1, abort_flag)) { ok = false; break; }
+                        tc_fence_after();
+                    }
+                    tmem_st16(tmem + lane_off + L::kDsCol + q * 16, dk);
+                }
+                if (!ok) break;
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(p_ready);
             }
-            if (!ok) break;
-            tmem_st_wait();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(p_ready);
-        }
-        if (ok && warp_wait(acc_done, 0, abort_flag)) {
-            // each half stores half of the dQ columns
+            if (!ok || !warp_wait(acc_done, k & 1, abort_flag)) {
+                ok = false;
+                break;
+            }
+            // each half stores half of the dQ columns; the next unit's first
+            // product (which overwrites the accumulator) waits for this warp's next
+            // P-ready arrival, after these loads
             tc_fence_after();
             const int osize = p.grad_dtype == FA_F32 ? 4 : 2;
             const size_t row_off = li * D * osize;
@@ -861,6 +923,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                 p.grad_dtype);
             }
             tc_fence_before();
+            g += u.n_iter;
         }
     }
     tc_fence_before();
@@ -924,10 +987,12 @@ int launch_bwd_d(const BackwardLaunch &a, cudaStream_t stream) {
         e = cudaGetLastError();
     }
     if (e == cudaSuccess) {
+        // one persistent CTA per SM (or per unit, when there are fewer units)
         p.g0 = a.dq;
         p.g1 = nullptr;
-        bwd_dq_kernel<D, BF16><<<static_cast<unsigned>(BH * p.n_t), kBwdThreads, DqLayout<D>::kSmemBytes,
-                                 stream>>>(
+        p.n_units = static_cast<int>(BH * p.n_t);
+        const int grid = p.n_units < a.num_sms ? p.n_units : a.num_sms;
+        bwd_dq_kernel<D, BF16><<<static_cast<unsigned>(grid), kBwdThreads, DqLayout<D>::kSmemBytes, stream>>>(
             mq, mk, mv, mdo, p);
         e = cudaGetLastError();
     }

@@ -93,6 +93,7 @@ struct BackwardLaunch {
     float scale;
     int in_bf16;
     int grad_dtype;
+    int num_sms;                         // persistent grids: at most one CTA per SM
 };
 
 int launch_backward(const BackwardLaunch &a, cudaStream_t stream);

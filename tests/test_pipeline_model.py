@@ -139,11 +139,19 @@ def cols(prefix, n_sub=8):
     return [f"{prefix}{wq}.{sb}" for wq in range(4) for sb in range(n_sub)]
 
 
-def dq_kernel(sim, n_iter, plant=None):
-    """bwd_dq_kernel: S and dP of tile j+1 issued once every warp holds tile j's,
-    dS in columns of its own, K and V in rings of their own (3 and 2 stages)."""
+def dq_kernel(sim, units, plant=None):
+    """bwd_dq_kernel: one persistent CTA runs its query tiles (units) in turn, each
+    with n_iter key tiles.  S and dP of key tile j+1 are issued once every warp
+    holds tile j's (across a unit boundary too), dS has columns of its own, K and
+    V stream through rings of their own (3 and 2 stages) that run on across
+    units, and Q, dO of the next unit are loaded once the last score products of
+    the unit before have read them.  The accumulator is read by the epilogue
+    before the next unit's first product overwrites it."""
+    if isinstance(units, int):
+        units = [units]
     KS, VS = 3, 2
-    for name, count in [("s_full", 1), ("s_loaded", 8), ("p_ready", 8), ("dq_done", 1), ("acc_done", 1)]:
+    for name, count in [("s_full", 1), ("s_loaded", 8), ("p_ready", 8), ("dq_done", 1), ("acc_done", 1),
+                        ("fix_full", 1), ("fix_empty", 1)]:
         sim.bar(name, count)
     for s in range(KS):
         sim.bar(f"k_full{s}"), sim.bar(f"k_empty{s}")
@@ -151,55 +159,83 @@ def dq_kernel(sim, n_iter, plant=None):
         sim.bar(f"v_full{s}"), sim.bar(f"v_empty{s}")
 
     def producer():
-        for n in range(n_iter):
-            ks, vs = n % KS, n % VS
-            if n >= KS:
-                yield ("wait", f"k_empty{ks}", n // KS - 1)
-            yield ("load", [(f"K{ks}", ("K", n))], f"k_full{ks}")
-            if n >= VS:
-                yield ("wait", f"v_empty{vs}", n // VS - 1)
-            yield ("load", [(f"V{vs}", ("V", n))], f"v_full{vs}")
+        g = 0
+        for k, n_iter in enumerate(units):
+            if k > 0 and plant != "no_fix_empty":
+                yield ("wait", "fix_empty", k - 1)
+            yield ("load", [("QDO", ("Q", k))], "fix_full")
+            for n in range(n_iter):
+                ks, vs = g % KS, g % VS
+                if g >= KS:
+                    yield ("wait", f"k_empty{ks}", g // KS - 1)
+                yield ("load", [(f"K{ks}", ("K", g))], f"k_full{ks}")
+                if g >= VS:
+                    yield ("wait", f"v_empty{vs}", g // VS - 1)
+                yield ("load", [(f"V{vs}", ("V", g))], f"v_full{vs}")
+                g += 1
 
     def mma():
-        def scores(j):
+        def scores(j, k):
             ks, vs = j % KS, j % VS
             yield ("wait", f"k_full{ks}", j // KS)
             yield ("wait", f"v_full{vs}", j // VS)
-            yield ("mma", [(f"K{ks}", ("K", j))], [(x, ("S", j)) for x in cols("X")])
-            yield ("mma", [(f"V{vs}", ("V", j))], [(y, ("dP", j)) for y in cols("Y")])
+            yield ("mma", [(f"K{ks}", ("K", j)), ("QDO", ("Q", k))], [(x, ("S", j)) for x in cols("X")])
+            yield ("mma", [(f"V{vs}", ("V", j)), ("QDO", ("Q", k))], [(y, ("dP", j)) for y in cols("Y")])
             yield ("commit", "s_full")
             yield ("commit", f"v_empty{vs}")
-        yield from scores(0)
-        for n in range(n_iter):
-            if n + 1 < n_iter:
-                if plant != "scores_before_loaded":
-                    yield ("wait", "s_loaded", n)
-                yield from scores(n + 1)
-            yield ("wait", "p_ready", n)
-            ks = n % KS
-            reads = [(f"DS{wq}.{q}", ("dS", n)) for wq in range(4) for q in range(4)] + [(f"K{ks}", ("K", n))]
-            if n > 0:
-                reads.append(("ACC", ("dQ", n - 1)))
-            yield ("mma", reads, [("ACC", ("dQ", n))])
-            yield ("commit", f"k_empty{ks}")
-            yield ("commit", "dq_done")
-        yield ("commit", "acc_done")
+        g = 0
+        for k, n_iter in enumerate(units):
+            yield ("wait", "fix_full", k)
+            if g > 0:  # implied by p_ready of the unit before, waited for all the same
+                yield ("wait", "s_loaded", g - 1)
+            yield from scores(g, k)
+            if n_iter == 1:
+                yield ("commit", "fix_empty")
+            for n in range(n_iter):
+                gi = g + n
+                if n + 1 < n_iter:
+                    if plant != "scores_before_loaded":
+                        yield ("wait", "s_loaded", gi)
+                    yield from scores(gi + 1, k)
+                    if n + 2 == n_iter:
+                        yield ("commit", "fix_empty")  # the unit's last reads of Q and dO
+                yield ("wait", "p_ready", gi)
+                ks = gi % KS
+                reads = [(f"DS{wq}.{q}", ("dS", gi)) for wq in range(4) for q in range(4)] + [(f"K{ks}", ("K", gi))]
+                if n > 0:
+                    reads.append(("ACC", ("dQ", k, n - 1)))
+                yield ("mma", reads, [("ACC", ("dQ", k, n))])
+                yield ("commit", f"k_empty{ks}")
+                yield ("commit", "dq_done")
+            yield ("commit", "acc_done")
+            g += n_iter
 
     def elementwise(wq, hf):
         mine = [4 * hf + i for i in range(4)]
-        for n in range(n_iter):
-            yield ("wait", "s_full", n)
-            for sb in mine:
-                yield ("read", f"X{wq}.{sb}", ("S", n))
-                yield ("read", f"Y{wq}.{sb}", ("dP", n))
-            yield ("arrive", "s_loaded")
-            if n > 0 and plant != "no_dq_done":
-                yield ("wait", "dq_done", n - 1)
-            for h in range(2):
-                yield ("write", f"DS{wq}.{2 * hf + h}", ("dS", n))
-            yield ("arrive", "p_ready")
-        yield ("wait", "acc_done", 0)
-        yield ("read", "ACC", ("dQ", n_iter - 1))
+        g = 0
+        late = None  # planted: an epilogue left until after the next unit's first item
+        for k, n_iter in enumerate(units):
+            for n in range(n_iter):
+                gi = g + n
+                yield ("wait", "s_full", gi)
+                for sb in mine:
+                    yield ("read", f"X{wq}.{sb}", ("S", gi))
+                    yield ("read", f"Y{wq}.{sb}", ("dP", gi))
+                yield ("arrive", "s_loaded")
+                if gi > 0 and plant != "no_dq_done":
+                    yield ("wait", "dq_done", gi - 1)
+                for h in range(2):
+                    yield ("write", f"DS{wq}.{2 * hf + h}", ("dS", gi))
+                yield ("arrive", "p_ready")
+                if late is not None:
+                    yield ("read", "ACC", late)
+                    late = None
+            yield ("wait", "acc_done", k)
+            if plant == "late_epilogue" and k + 1 < len(units):
+                late = ("dQ", k, n_iter - 1)
+            else:
+                yield ("read", "ACC", ("dQ", k, n_iter - 1))
+            g += n_iter
 
     sim.role("tma", producer())
     sim.role("mma", mma())
@@ -381,6 +417,28 @@ def test_protocol_holds_under_random_interleavings(kernel, n_iter):
         sim = Sim(1000 * n_iter + seed)
         KERNELS[kernel](sim, n_iter)
         sim.run()
+
+
+@pytest.mark.parametrize("units", [[1, 1], [2, 3], [3, 1, 2], [7, 2]])
+def test_persistent_dq_protocol_holds_under_random_interleavings(units):
+    # one CTA running several query tiles in turn
+    for seed in range(150):
+        sim = Sim(7000 + seed)
+        dq_kernel(sim, units)
+        sim.run()
+
+
+@pytest.mark.parametrize("plant", ["no_fix_empty", "late_epilogue"])
+def test_the_model_catches_a_planted_unit_boundary_mistake(plant):
+    caught = 0
+    for seed in range(150):
+        sim = Sim(seed)
+        dq_kernel(sim, [2, 1, 3], plant)
+        try:
+            sim.run()
+        except ProtocolError:
+            caught += 1
+    assert caught > 0, f"dq with {plant} passed every interleaving"
 
 
 @pytest.mark.parametrize("kernel,plant", [("dq", "no_dq_done"), ("dq", "scores_before_loaded"),
