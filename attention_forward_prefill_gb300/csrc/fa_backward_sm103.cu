@@ -109,45 +109,66 @@ struct BwdParams {
 };
 
 // ---------------------------------------------------------------- D and L2
-// One warp per row of the padded [B Hq][npad] layout; rows past N get zeros, so
-// that every 128-row tile of it can be copied whole.  Both are stored negated,
-// the sign the elementwise work adds them with.
-__global__ void __launch_bounds__(256) bwd_prep_kernel(const uint16_t *o, const uint16_t *dout,
-                                                       const float *lse, float *lse2, float *dsum,
-                                                       long long rows_pad, int N, int npad, int d, int bf16) {
-    const long long prow = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
-    if (prow >= rows_pad) return;
-    const long long i = prow % npad;
-    if (i >= N) {
-        if (lane == 0) {
-            dsum[prow] = 0.f;
-            lse2[prow] = 0.f;
-        }
-        return;
-    }
-    const long long row = (prow / npad) * N + i;
+// Rows of the padded [B Hq][npad] layout; rows past N get zeros, so that every
+// 128-row tile of it can be copied whole.  Both are stored negated, the sign the
+// elementwise work adds them with.  A row is read as 16-byte words, one per lane
+// (d / 8 lanes a row), and every thread keeps kPrepRows such words of O and of
+// dO in flight; each lane sums its eight products in order, then the row's lanes
+// combine by a fixed butterfly, so D is the same on every run.
+constexpr int kPrepThreads = 256;
+constexpr int kPrepRows = 4;
+
+template <int D, bool BF16>
+__device__ __forceinline__ float dot8(const uint4 &a, const uint4 &b) {
+    const uint32_t ua[4] = {a.x, a.y, a.z, a.w}, ub[4] = {b.x, b.y, b.z, b.w};
     float acc = 0.f;
-    for (int c = lane * 2; c < d; c += 64) {
-        const uint32_t a = *reinterpret_cast<const uint32_t *>(o + row * d + c);
-        const uint32_t b = *reinterpret_cast<const uint32_t *>(dout + row * d + c);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
         float a0, a1, b0, b1;
-        if (bf16) {
-            a0 = __uint_as_float(a << 16); a1 = __uint_as_float(a & 0xffff0000u);
-            b0 = __uint_as_float(b << 16); b1 = __uint_as_float(b & 0xffff0000u);
+        if constexpr (BF16) {
+            a0 = __uint_as_float(ua[i] << 16); a1 = __uint_as_float(ua[i] & 0xffff0000u);
+            b0 = __uint_as_float(ub[i] << 16); b1 = __uint_as_float(ub[i] & 0xffff0000u);
         } else {
-            const float2 fa = __half22float2(*reinterpret_cast<const __half2 *>(&a));
-            const float2 fb = __half22float2(*reinterpret_cast<const __half2 *>(&b));
+            const float2 fa = __half22float2(*reinterpret_cast<const __half2 *>(&ua[i]));
+            const float2 fb = __half22float2(*reinterpret_cast<const __half2 *>(&ub[i]));
             a0 = fa.x; a1 = fa.y; b0 = fb.x; b1 = fb.y;
         }
         acc = fmaf(a0, b0, acc);
         acc = fmaf(a1, b1, acc);
     }
+    return acc;
+}
+
+template <int D, bool BF16>
+__global__ void __launch_bounds__(kPrepThreads) bwd_prep_kernel(const uint16_t *o, const uint16_t *dout,
+                                                                const float *lse, float *lse2, float *dsum,
+                                                                long long rows_pad, int N, int npad) {
+    constexpr int LPR = D / 8;       // lanes per row
+    constexpr int RPW = 32 / LPR;    // rows per warp and word
+    const int lane = threadIdx.x & 31, sub = lane % LPR;
+    const long long warp_g = (static_cast<long long>(blockIdx.x) * kPrepThreads + threadIdx.x) >> 5;
+    const long long first = warp_g * RPW * kPrepRows + lane / LPR;
+    uint4 a[kPrepRows], b[kPrepRows];
+    long long row[kPrepRows];
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (lane == 0) {
-        dsum[prow] = -acc;
-        lse2[prow] = -(lse[row] * 1.4426950408889634f);
+    for (int u = 0; u < kPrepRows; ++u) {
+        const long long prow = first + u * RPW;
+        const long long i = prow % npad;
+        const bool live = prow < rows_pad && i < N;
+        row[u] = live ? (prow / npad) * N + i : -1;
+        a[u] = live ? __ldg(reinterpret_cast<const uint4 *>(o + row[u] * D) + sub) : make_uint4(0, 0, 0, 0);
+        b[u] = live ? __ldg(reinterpret_cast<const uint4 *>(dout + row[u] * D) + sub) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int u = 0; u < kPrepRows; ++u) {
+        float acc = dot8<D, BF16>(a[u], b[u]);
+#pragma unroll
+        for (int off = 1; off < LPR; off <<= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        const long long prow = first + u * RPW;
+        if (sub == 0 && prow < rows_pad) {
+            dsum[prow] = row[u] >= 0 ? -acc : 0.f;
+            lse2[prow] = row[u] >= 0 ? -(lse[row[u]] * 1.4426950408889634f) : 0.f;
+        }
     }
 }
 
@@ -962,9 +983,11 @@ int launch_bwd_d(const BackwardLaunch &a, cudaStream_t stream) {
         return FA_ERR_WORKSPACE;
     }
     float *lse2 = static_cast<float *>(ws), *dsum = lse2 + rows_pad;
-    bwd_prep_kernel<<<static_cast<unsigned>((rows_pad + 7) / 8), 256, 0, stream>>>(
+    constexpr long long kPrepRowsPerBlock = (kPrepThreads / 32) * (32 / (D / 8)) * kPrepRows;
+    bwd_prep_kernel<D, BF16><<<static_cast<unsigned>((rows_pad + kPrepRowsPerBlock - 1) / kPrepRowsPerBlock),
+                               kPrepThreads, 0, stream>>>(
         static_cast<const uint16_t *>(a.out), static_cast<const uint16_t *>(a.dout), a.lse, lse2, dsum, rows_pad,
-        a.N, n_t * kRows, D, a.in_bf16);
+        a.N, n_t * kRows);
     e = cudaGetLastError();
     BwdParams p;
     p.lse2 = lse2;
