@@ -51,15 +51,15 @@ struct BwdLayout {
     static constexpr int kChunks = D / 64;
     static constexpr int kTileBytes = kChunks * kSlabBytes;  // 128 rows x D 16-bit
     static constexpr int kStages = (D == 128) ? 2 : 3;
-    static constexpr int kFixOff = 0;                       // two tiles loaded once per CTA
+    static constexpr int kFixOff = 0;                       // K_j, V_j: loaded once per unit
     static constexpr int kRingOff = 2 * kTileBytes;         // stages of Q_i, dO_i and the vectors
     // L2 and D of the stage's 128 queries (two 512-byte bulk copies) after its tiles
     static constexpr int kVecInStage = 2 * kTileBytes;
     static constexpr int kStageBytes = 2 * kTileBytes + 2 * kRows * 4;
     static constexpr int kBarOff = kRingOff + kStages * kStageBytes;
     // fix_full, s_full, p_ready, acc_done, drain, s_loaded, ring_full[S], ring_empty[S], pd_done,
-    // dp_full, dp_loaded, ds_ready
-    static constexpr int kNumBars = 10 + 2 * kStages;
+    // dp_full, dp_loaded, ds_ready, fix_empty
+    static constexpr int kNumBars = 11 + 2 * kStages;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
     static constexpr int kSmemBytes = kMiscOff + 16 + 1024;
     // TMEM: X (S^T) | Y (dP^T) | accumulator A (dV) | accumulator B (dK).  At
@@ -105,7 +105,8 @@ struct BwdParams {
     int grad_dtype;
     float scale;
     float c;            // scale * log2(e)
-    int n_units;        // dq: (query head, query tile) units, dealt to persistent CTAs
+    int n_units;        // units dealt to the persistent CTAs: dkdv (key/value head, key
+                        // tile), dq (query head, query tile)
 };
 
 // ---------------------------------------------------------------- D and L2
@@ -264,6 +265,34 @@ __device__ __forceinline__ void ds_quarter(const uint32_t (&pr)[32], const uint3
 }
 
 // ---------------------------------------------------------------- dK, dV
+// One unit of the dK/dV pass: key tile `jt` of (batch, key/value head) `bhk`,
+// against every query tile that sees it of every query head of its group.  A
+// persistent CTA takes units k = 0, 1, ... in snake order over rounds of
+// G = gridDim.x, as in the dQ pass; causal units come heaviest first (the first
+// key tiles of every head see the most query tiles).
+struct DkdvUnit {
+    int bhk, jt, i_first, n_qt, n_iter, bhq0;
+};
+
+__device__ __forceinline__ bool dkdv_unit(const BwdParams &p, int k, DkdvUnit &u) {
+    const long long G = gridDim.x, c = blockIdx.x;
+    const long long idx = static_cast<long long>(k) * G + ((k & 1) ? G - 1 - c : c);
+    if (idx >= p.n_units) return false;
+    const int n_heads = p.n_units / p.n_t;
+    if (p.causal) {
+        u.bhk = static_cast<int>(idx % n_heads);
+        u.jt = static_cast<int>(idx / n_heads);
+    } else {
+        u.bhk = static_cast<int>(idx / p.n_t);
+        u.jt = static_cast<int>(idx % p.n_t);
+    }
+    u.i_first = p.causal ? u.jt : 0;  // query tiles that see key tile jt
+    u.n_qt = p.n_t - u.i_first;
+    u.n_iter = p.group * u.n_qt;      // every query head of the group, every tile
+    u.bhq0 = (u.bhk / p.Hkv) * p.Hq + (u.bhk % p.Hkv) * p.group;  // first query head
+    return true;
+}
+
 template <int D, bool BF16>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
@@ -280,19 +309,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     uint64_t *pd_done = bars + 6 + 2 * L::kStages;
     // d = 128: dP^T ready, every warp's dP^T loaded, dS^T ready
     uint64_t *dp_full = pd_done + 1, *dp_loaded = pd_done + 2, *ds_ready = pd_done + 3;
+    uint64_t *fix_empty = pd_done + 4;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kMiscOff);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kMiscOff + 4);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // Causal: CTAs are dealt key-tile-major, so every head's heaviest tiles (the
-    // first key tiles see the most query tiles) start before any light one.
-    const int n_heads = static_cast<int>(gridDim.x) / p.n_t;
-    const int bhk = p.causal ? blockIdx.x % n_heads : blockIdx.x / p.n_t;  // (batch, key/value head)
-    const int jt = p.causal ? blockIdx.x / n_heads : blockIdx.x % p.n_t;   // key tile
-    const int i_first = p.causal ? jt : 0;     // query tiles that see key tile jt
-    const int n_qt = p.n_t - i_first;
-    const int n_iter = p.group * n_qt;         // every query head of the group, every tile
-    const int bhq0 = (bhk / p.Hkv) * p.Hq + (bhk % p.Hkv) * p.group;  // first query head
+    // Barriers that complete once per unit (fix_full, fix_empty, acc_done) wait on
+    // the parity of the unit counter k; those that complete once per item on the
+    // parity of the CTA's item counter g, which runs on across units, and so does
+    // the ring of (Q, dO) stages.
 
     if (threadIdx.x == 0) {
         mbar_init(fix_full, 1);
@@ -305,6 +330,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_init(dp_full, 1);
         mbar_init(dp_loaded, kBwdEltWarps);
         mbar_init(ds_ready, kBwdEltWarps);
+        mbar_init(fix_empty, 1);
         for (int s = 0; s < L::kStages; ++s) {
             mbar_init(ring_full + s, 1);
             mbar_init(ring_empty + s, 1);
@@ -332,39 +358,49 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             uint8_t *fix = smem + L::kFixOff, *ring = smem + L::kRingOff;
             const uint64_t pol = l2_policy_evict_last();
             bool ok = true;
-            mbar_arrive_expect_tx(fix_full, 2 * L::kTileBytes);
-            for (int c = 0; c < L::kChunks; ++c) {
-                tma_load_3d(fix + c * kSlabBytes, &map_k, fix_full, c * 64, jt * kRows, bhk, pol);
-                tma_load_3d(fix + L::kTileBytes + c * kSlabBytes, &map_v, fix_full, c * 64, jt * kRows, bhk,
-                            pol);
-            }
-            int n = 0;
-            for (; n < n_iter && ok; ++n) {
-                const int slot = n % L::kStages;
-                if (n >= L::kStages &&
-                    !mbar_wait(ring_empty + slot, ((n / L::kStages) - 1) & 1, abort_flag, kWatchdogNs)) {
+            int nfix = 0, ni = 0;  // K/V pairs and ring items issued
+            DkdvUnit u;
+            for (int k = 0; ok && dkdv_unit(p, k, u); ++k) {
+                // K and V of the unit before must have been read by its last products
+                if (k > 0 && !mbar_wait(fix_empty, (k - 1) & 1, abort_flag, kWatchdogNs)) {
                     ok = false;
                     break;
                 }
-                const int row = (i_first + n % n_qt) * kRows;
-                const int bhq = bhq0 + n / n_qt;
-                uint8_t *st = ring + slot * L::kStageBytes;
-                mbar_arrive_expect_tx(ring_full + slot, 2 * L::kTileBytes + 2 * kRows * 4);
+                mbar_arrive_expect_tx(fix_full, 2 * L::kTileBytes);
                 for (int c = 0; c < L::kChunks; ++c) {
-                    tma_load_3d(st + c * kSlabBytes, &map_q, ring_full + slot, c * 64, row, bhq, pol);
-                    tma_load_3d(st + L::kTileBytes + c * kSlabBytes, &map_do, ring_full + slot, c * 64, row,
-                                bhq, pol);
+                    tma_load_3d(fix + c * kSlabBytes, &map_k, fix_full, c * 64, u.jt * kRows, u.bhk, pol);
+                    tma_load_3d(fix + L::kTileBytes + c * kSlabBytes, &map_v, fix_full, c * 64, u.jt * kRows,
+                                u.bhk, pol);
                 }
-                // the 128 queries' L2 and D (the padded layout keeps both copies whole)
-                const size_t vrow = static_cast<size_t>(bhq) * p.npad + row;
-                bulk_load(st + L::kVecInStage, p.lse2 + vrow, kRows * 4, ring_full + slot);
-                bulk_load(st + L::kVecInStage + kRows * 4, p.dsum + vrow, kRows * 4, ring_full + slot);
+                ++nfix;
+                for (int n = 0; n < u.n_iter; ++n) {
+                    const int slot = ni % L::kStages;
+                    if (ni >= L::kStages &&
+                        !mbar_wait(ring_empty + slot, ((ni / L::kStages) - 1) & 1, abort_flag, kWatchdogNs)) {
+                        ok = false;
+                        break;
+                    }
+                    const int row = (u.i_first + n % u.n_qt) * kRows;
+                    const int bhq = u.bhq0 + n / u.n_qt;
+                    uint8_t *st = ring + slot * L::kStageBytes;
+                    mbar_arrive_expect_tx(ring_full + slot, 2 * L::kTileBytes + 2 * kRows * 4);
+                    for (int c = 0; c < L::kChunks; ++c) {
+                        tma_load_3d(st + c * kSlabBytes, &map_q, ring_full + slot, c * 64, row, bhq, pol);
+                        tma_load_3d(st + L::kTileBytes + c * kSlabBytes, &map_do, ring_full + slot, c * 64, row,
+                                    bhq, pol);
+                    }
+                    // the 128 queries' L2 and D (the padded layout keeps both copies whole)
+                    const size_t vrow = static_cast<size_t>(bhq) * p.npad + row;
+                    bulk_load(st + L::kVecInStage, p.lse2 + vrow, kRows * 4, ring_full + slot);
+                    bulk_load(st + L::kVecInStage + kRows * 4, p.dsum + vrow, kRows * 4, ring_full + slot);
+                    ++ni;
+                }
             }
-            if (!ok) {  // let every copy already issued land
+            if (!ok) {  // let every copy already issued land (only the last K/V can be in flight)
                 constexpr uint64_t kDrainNs = 200ull * 1000ull * 1000ull;
                 int dummy = 0;
-                mbar_wait(fix_full, 0, &dummy, kDrainNs);
-                for (int m = (n > L::kStages ? n - L::kStages : 0); m < n; ++m)
+                if (nfix > 0) mbar_wait(fix_full, (nfix - 1) & 1, &dummy, kDrainNs);
+                for (int m = (ni > L::kStages ? ni - L::kStages : 0); m < ni; ++m)
                     mbar_wait(ring_full + (m % L::kStages), (m / L::kStages) & 1, &dummy, kDrainNs);
             }
         }
@@ -376,114 +412,134 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             const uint32_t fix = smem_u32(smem + L::kFixOff), ring = smem_u32(smem + L::kRingOff);
             const uint64_t k_desc = sdesc_sw128(fix, 16, 1024);
             const uint64_t v_desc = sdesc_sw128(fix + L::kTileBytes, 16, 1024);
-            bool ok = mbar_wait(fix_full, 0, abort_flag, kWatchdogNs);
-            if constexpr (!L::kOwnPds) {
-                // d = 128: P^T and dS^T are written over S^T and dP^T, in two steps.
-                // dP^T runs while the weights are computed, dV += P^T dO_i while dS^T is.
-                // S^T of item j (Q_j from its stage) and dP^T (dO_j)
-                auto issue_s = [&](int j) {
-                    const uint32_t st = ring + (j % L::kStages) * L::kStageBytes;
-                    issue_qk<D>(tmem + L::kXCol, k_desc, sdesc_sw128(st, 16, 1024), idesc_s);
-                    umma_commit(s_full);
-                };
-                auto issue_dp = [&](int j) {
-                    const uint32_t st = ring + (j % L::kStages) * L::kStageBytes;
-                    issue_qk<D>(tmem + L::kYCol, v_desc, sdesc_sw128(st + L::kTileBytes, 16, 1024), idesc_s);
-                    umma_commit(dp_full);
-                };
-                auto stage_ready = [&](int j) {
-                    if (!mbar_wait(ring_full + j % L::kStages, (j / L::kStages) & 1, abort_flag, kWatchdogNs))
-                        return false;
-                    tc_fence_after();
-                    return true;
-                };
-                if (ok && (ok = stage_ready(0))) {
-                    issue_s(0);
-                    issue_dp(0);
-                }
-                for (int n = 0; n < n_iter && ok; ++n) {
-                    const int slot = n % L::kStages;
-                    const uint32_t st = ring + slot * L::kStageBytes;
-                    if (!mbar_wait(p_ready, n & 1, abort_flag, kWatchdogNs)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    issue_pv<D>(tmem + L::kACol, tmem + L::kPCol,
-                                sdesc_sw128(st + L::kTileBytes, kSlabBytes, 1024), idesc_acc, n > 0);
-                    // S^T of the next item may overwrite P^T once dV has been issued (the
-                    // products run in order); take it now if its Q tile has landed, so it
-                    // runs under the dS^T step, else after dK.
-                    const int nx = n + 1;
-                    bool s_issued = false;
-                    if (nx < n_iter && mbar_test_wait(ring_full + nx % L::kStages, (nx / L::kStages) & 1)) {
+            bool ok = true;
+            int g = 0;
+            DkdvUnit u;
+            auto stage_ready = [&](int j) {
+                if (!mbar_wait(ring_full + j % L::kStages, (j / L::kStages) & 1, abort_flag, kWatchdogNs))
+                    return false;
+                tc_fence_after();
+                return true;
+            };
+            for (int k = 0; ok && dkdv_unit(p, k, u); ++k) {
+                if (!mbar_wait(fix_full, k & 1, abort_flag, kWatchdogNs)) { ok = false; break; }
+                tc_fence_after();
+                if constexpr (!L::kOwnPds) {
+                    // d = 128: P^T and dS^T are written over S^T and dP^T, in two steps.
+                    // dP^T runs while the weights are computed, dV += P^T dO_i while dS^T is.
+                    // S^T of item j (Q_j from its stage) and dP^T (dO_j).  At a unit's
+                    // start they overwrite the last unit's P^T and dS^T, which the dV and
+                    // dK products issued before them (and run in order) read.
+                    auto issue_s = [&](int j) {
+                        const uint32_t st = ring + (j % L::kStages) * L::kStageBytes;
+                        issue_qk<D>(tmem + L::kXCol, k_desc, sdesc_sw128(st, 16, 1024), idesc_s);
+                        umma_commit(s_full);
+                    };
+                    auto issue_dp = [&](int j) {
+                        const uint32_t st = ring + (j % L::kStages) * L::kStageBytes;
+                        issue_qk<D>(tmem + L::kYCol, v_desc, sdesc_sw128(st + L::kTileBytes, 16, 1024), idesc_s);
+                        umma_commit(dp_full);
+                    };
+                    if (!stage_ready(g)) { ok = false; break; }
+                    issue_s(g);
+                    issue_dp(g);
+                    if (u.n_iter == 1) umma_commit(fix_empty);
+                    for (int n = 0; n < u.n_iter && ok; ++n) {
+                        const int gi = g + n;
+                        const int slot = gi % L::kStages;
+                        const uint32_t st = ring + slot * L::kStageBytes;
+                        if (!mbar_wait(p_ready, gi & 1, abort_flag, kWatchdogNs)) {
+                            ok = false;
+                            break;
+                        }
                         tc_fence_after();
-                        issue_s(nx);
-                        s_issued = true;
+                        issue_pv<D>(tmem + L::kACol, tmem + L::kPCol,
+                                    sdesc_sw128(st + L::kTileBytes, kSlabBytes, 1024), idesc_acc, n > 0);
+                        // S^T of the next item may overwrite P^T once dV has been issued (the
+                        // products run in order); take it now if its Q tile has landed, so it
+                        // runs under the dS^T step, else after dK.
+                        const bool more = n + 1 < u.n_iter;
+                        bool s_issued = false;
+                        if (more && mbar_test_wait(ring_full + (gi + 1) % L::kStages, ((gi + 1) / L::kStages) & 1)) {
+                            tc_fence_after();
+                            issue_s(gi + 1);
+                            s_issued = true;
+                        }
+                        if (!mbar_wait(ds_ready, gi & 1, abort_flag, kWatchdogNs)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        issue_pv<D>(tmem + L::kBCol, tmem + L::kDsCol, sdesc_sw128(st, kSlabBytes, 1024), idesc_acc,
+                                    n > 0);
+                        umma_commit(ring_empty + slot);
+                        if (more) {
+                            if (!s_issued) {
+                                if (!stage_ready(gi + 1)) {
+                                    ok = false;
+                                    break;
+                                }
+                                issue_s(gi + 1);
+                            }
+                            issue_dp(gi + 1);  // over dS^T, after the dK product that reads it
+                            // the unit's last reads of K and V are issued: free them once done
+                            if (n + 2 == u.n_iter) umma_commit(fix_empty);
+                        }
                     }
-                    if (!mbar_wait(ds_ready, n & 1, abort_flag, kWatchdogNs)) {
-                        ok = false;
-                        break;
+                } else {
+                    // S^T = K Q_i^T and dP^T = V dO_i^T (keys on TMEM lanes) for ring item j
+                    auto issue_scores = [&](int j) {
+                        if (!stage_ready(j)) return false;
+                        const uint32_t st = ring + (j % L::kStages) * L::kStageBytes;
+                        issue_qk<D>(tmem + L::kXCol, k_desc, sdesc_sw128(st, 16, 1024), idesc_s);
+                        issue_qk<D>(tmem + L::kYCol, v_desc, sdesc_sw128(st + L::kTileBytes, 16, 1024), idesc_s);
+                        umma_commit(s_full);
+                        return true;
+                    };
+                    // The unit's first scores overwrite the last unit's S^T and dP^T:
+                    // every warp holds those (implied by its P-ready arrival, awaited).
+                    if (g > 0) {
+                        if (!mbar_wait(s_loaded, (g - 1) & 1, abort_flag, kWatchdogNs)) { ok = false; break; }
+                        tc_fence_after();
                     }
-                    tc_fence_after();
-                    issue_pv<D>(tmem + L::kBCol, tmem + L::kDsCol, sdesc_sw128(st, kSlabBytes, 1024), idesc_acc,
-                                n > 0);
-                    umma_commit(ring_empty + slot);
-                    if (nx < n_iter) {
-                        if (!s_issued) {
-                            if (!stage_ready(nx)) {
+                    if (!issue_scores(g)) { ok = false; break; }
+                    if (u.n_iter == 1) umma_commit(fix_empty);
+                    for (int n = 0; n < u.n_iter && ok; ++n) {
+                        const int gi = g + n;
+                        // P^T and dS^T have columns of their own: once every elementwise warp
+                        // holds this item's scores, the next item's products may start.
+                        if (n + 1 < u.n_iter) {
+                            if (!mbar_wait(s_loaded, gi & 1, abort_flag, kWatchdogNs)) {
                                 ok = false;
                                 break;
                             }
-                            issue_s(nx);
+                            tc_fence_after();
+                            if (!issue_scores(gi + 1)) {
+                                ok = false;
+                                break;
+                            }
+                            if (n + 2 == u.n_iter) umma_commit(fix_empty);
                         }
-                        issue_dp(nx);  // over dS^T, after the dK product that reads it
-                    }
-                }
-            } else {
-                // S^T = K Q_i^T and dP^T = V dO_i^T (keys on TMEM lanes) for ring item j
-                auto issue_scores = [&](int j) {
-                    const int slot = j % L::kStages;
-                    if (!mbar_wait(ring_full + slot, (j / L::kStages) & 1, abort_flag, kWatchdogNs)) return false;
-                    tc_fence_after();
-                    const uint32_t st = ring + slot * L::kStageBytes;
-                    issue_qk<D>(tmem + L::kXCol, k_desc, sdesc_sw128(st, 16, 1024), idesc_s);
-                    issue_qk<D>(tmem + L::kYCol, v_desc, sdesc_sw128(st + L::kTileBytes, 16, 1024), idesc_s);
-                    umma_commit(s_full);
-                    return true;
-                };
-                if (ok) ok = issue_scores(0);
-                for (int n = 0; n < n_iter && ok; ++n) {
-                    // P^T and dS^T have columns of their own: once every elementwise warp
-                    // holds this item's scores, the next item's products may start.
-                    if (n + 1 < n_iter) {
-                        if (!mbar_wait(s_loaded, n & 1, abort_flag, kWatchdogNs)) {
+                        if (!mbar_wait(p_ready, gi & 1, abort_flag, kWatchdogNs)) {
                             ok = false;
                             break;
                         }
                         tc_fence_after();
-                        if (!issue_scores(n + 1)) {
-                            ok = false;
-                            break;
-                        }
+                        // dV += P^T dO_i and dK += dS^T Q_i (P^T, dS^T from TMEM; dO_i, Q_i MN-major)
+                        const int slot = gi % L::kStages;
+                        const uint32_t st = ring + slot * L::kStageBytes;
+                        issue_pv<D>(tmem + L::kACol, tmem + L::kPCol,
+                                    sdesc_sw128(st + L::kTileBytes, kSlabBytes, 1024), idesc_acc, n > 0);
+                        issue_pv<D>(tmem + L::kBCol, tmem + L::kDsCol, sdesc_sw128(st, kSlabBytes, 1024), idesc_acc,
+                                    n > 0);
+                        umma_commit(ring_empty + slot);
+                        umma_commit(pd_done);
                     }
-                    if (!mbar_wait(p_ready, n & 1, abort_flag, kWatchdogNs)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    // dV += P^T dO_i and dK += dS^T Q_i (P^T, dS^T from TMEM; dO_i, Q_i MN-major)
-                    const int slot = n % L::kStages;
-                    const uint32_t st = ring + slot * L::kStageBytes;
-                    issue_pv<D>(tmem + L::kACol, tmem + L::kPCol,
-                                sdesc_sw128(st + L::kTileBytes, kSlabBytes, 1024), idesc_acc, n > 0);
-                    issue_pv<D>(tmem + L::kBCol, tmem + L::kDsCol, sdesc_sw128(st, kSlabBytes, 1024), idesc_acc,
-                                n > 0);
-                    umma_commit(ring_empty + slot);
-                    umma_commit(pd_done);
                 }
+                if (!ok) break;
+                umma_commit(acc_done);
+                g += u.n_iter;
             }
-            umma_commit(acc_done);
             umma_commit(drain);
             int dummy = 0;
             mbar_wait(drain, 0, &dummy, kWatchdogNs);
@@ -494,132 +550,142 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int wq = warp & 3, hf = warp >> 2;  // TMEM lane quadrant; column half
         const int r = wq * 32 + lane;
         const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
-        const int key = jt * kRows + r;
         bool ok = true;
-        for (int n = 0; n < n_iter && ok; ++n) {
-            const int q0 = (i_first + n % n_qt) * kRows;
-            // this half's 64 query columns: L2 and D, brought into the ring stage with
-            // Q_i and dO_i (the MMA thread waited for the same barrier; so do we)
-            const int slot = n % L::kStages;
-            if (!warp_wait(ring_full + slot, (n / L::kStages) & 1, abort_flag)) { ok = false; break; }
-            const float *vstage = reinterpret_cast<const float *>(smem + L::kRingOff + slot * L::kStageBytes +
-                                                                  L::kVecInStage);
-            const float *nl2_v = vstage + hf * 64, *nd_v = vstage + kRows + hf * 64;
-            if (!warp_wait(s_full, n & 1, abort_flag)) { ok = false; break; }
-            tc_fence_after();
-            if constexpr (L::kOwnPds) {
-                // d = 64: P^T and dS^T have columns of their own
-                uint32_t sr[2][32], dr[2][32];
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    tmem_ld32(tmem + lane_off + L::kXCol + (2 * hf + h) * 32, sr[h]);
-                    tmem_ld32(tmem + lane_off + L::kYCol + (2 * hf + h) * 32, dr[h]);
-                }
-                tmem_ld_wait();
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    reg_fence32(sr[h]);
-                    reg_fence32(dr[h]);
-                }
-                // The arrival tells the MMA thread the score columns are free.
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(s_loaded);
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int q = 2 * hf + h;
-                    // column col is query q0 + 32 q + col; it sees the key when it exists
-                    // and, causally, when key <= query
-                    const int qb = q0 + q * 32;
-                    uint32_t vis = 0xffffffffu;
-                    if (qb + 32 > p.N) vis = p.N > qb ? (0xffffffffu >> (32 - (p.N - qb))) : 0u;
-                    if (p.causal) {
-                        const int lo = key - qb;  // first visible column
-                        vis &= lo <= 0 ? 0xffffffffu : (lo >= 32 ? 0u : (0xffffffffu << lo));
-                    }
-                    uint32_t pk[16], dk[16];
-                    weights_quarter<BF16, true>(sr[h], dr[h], pk, dk, p.c, nl2_v + h * 32, nd_v + h * 32, 0.f, 0.f,
-                                                vis);
-                    if (h == 0 && n > 0) {
-                        // the previous item's P^T and dS^T must have been read.  This
-                        // also keeps p_ready from completing twice before the MMA
-                        // thread, which committed pd_done after seeing it, looks.
-                        if (!warp_wait(pd_done, (n - 1) & 1, abort_flag)) { ok = false; break; }
-                        tc_fence_after();
-                    }
-                    tmem_st16(tmem + lane_off + L::kPCol + q * 16, pk);
-                    tmem_st16(tmem + lane_off + L::kDsCol + q * 16, dk);
-                }
-                if (!ok) break;
-                tmem_st_wait();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(p_ready);
-            } else {
-                // d = 128 in two steps.  First P^T from S^T, over S^T: the upper
-                // half's P^T lands on columns the lower half reads, so every warp's
-                // loads complete before any warp stores.
-                uint32_t sr[2][32], dr[2][32];
-#pragma unroll
-                for (int h = 0; h < 2; ++h) tmem_ld32(tmem + lane_off + L::kXCol + (2 * hf + h) * 32, sr[h]);
-                tmem_ld_wait();
-#pragma unroll
-                for (int h = 0; h < 2; ++h) reg_fence32(sr[h]);
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(s_loaded);
-                if (!warp_wait(s_loaded, n & 1, abort_flag)) { ok = false; break; }
+        int g = 0;
+        DkdvUnit u;
+        for (int k = 0; ok && dkdv_unit(p, k, u); ++k) {
+            const int key = u.jt * kRows + r;
+            const int g_end = g + u.n_iter;
+            int qt = u.i_first;  // the item's query tile: i_first .. n_t - 1, once per query head
+            for (int gi = g; gi < g_end && ok; ++gi, qt = qt + 1 == p.n_t ? u.i_first : qt + 1) {
+                const int q0 = qt * kRows;
+                // this half's 64 query columns: L2 and D, brought into the ring stage with
+                // Q_i and dO_i (the MMA thread waited for the same barrier; so do we)
+                const int slot = gi % L::kStages;
+                if (!warp_wait(ring_full + slot, (gi / L::kStages) & 1, abort_flag)) { ok = false; break; }
+                const float *vstage = reinterpret_cast<const float *>(smem + L::kRingOff + slot * L::kStageBytes +
+                                                                      L::kVecInStage);
+                const float *nl2_v = vstage + hf * 64, *nd_v = vstage + kRows + hf * 64;
+                if (!warp_wait(s_full, gi & 1, abort_flag)) { ok = false; break; }
                 tc_fence_after();
+                if constexpr (L::kOwnPds) {
+                    // d = 64: P^T and dS^T have columns of their own
+                    uint32_t sr[2][32], dr[2][32];
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int q = 2 * hf + h;
-                    // column col is query q0 + 32 q + col; it sees the key when it
-                    // exists and, causally, when key <= query
-                    const int qb = q0 + q * 32;
-                    uint32_t vis = 0xffffffffu;
-                    if (qb + 32 > p.N) vis = p.N > qb ? (0xffffffffu >> (32 - (p.N - qb))) : 0u;
-                    if (p.causal) {
-                        const int lo = key - qb;  // first visible column
-                        vis &= lo <= 0 ? 0xffffffffu : (lo >= 32 ? 0u : (0xffffffffu << lo));
+                    for (int h = 0; h < 2; ++h) {
+                        tmem_ld32(tmem + lane_off + L::kXCol + (2 * hf + h) * 32, sr[h]);
+                        tmem_ld32(tmem + lane_off + L::kYCol + (2 * hf + h) * 32, dr[h]);
                     }
-                    uint32_t pk[16];
-                    p_quarter<BF16>(sr[h], pk, p.c, nl2_v + h * 32, vis);
-                    tmem_st16(tmem + lane_off + L::kPCol + q * 16, pk);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        reg_fence32(sr[h]);
+                        reg_fence32(dr[h]);
+                    }
+                    // The arrival tells the MMA thread the score columns are free.
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(s_loaded);
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int q = 2 * hf + h;
+                        // column col is query q0 + 32 q + col; it sees the key when it exists
+                        // and, causally, when key <= query
+                        const int qb = q0 + q * 32;
+                        uint32_t vis = 0xffffffffu;
+                        if (qb + 32 > p.N) vis = p.N > qb ? (0xffffffffu >> (32 - (p.N - qb))) : 0u;
+                        if (p.causal) {
+                            const int lo = key - qb;  // first visible column
+                            vis &= lo <= 0 ? 0xffffffffu : (lo >= 32 ? 0u : (0xffffffffu << lo));
+                        }
+                        uint32_t pk[16], dk[16];
+                        weights_quarter<BF16, true>(sr[h], dr[h], pk, dk, p.c, nl2_v + h * 32, nd_v + h * 32, 0.f, 0.f,
+                                                    vis);
+                        if (h == 0 && gi > 0) {
+                            // the previous item's P^T and dS^T must have been read.  This
+                            // also keeps p_ready from completing twice before the MMA
+                            // thread, which committed pd_done after seeing it, looks.
+                            if (!warp_wait(pd_done, (gi - 1) & 1, abort_flag)) { ok = false; break; }
+                            tc_fence_after();
+                        }
+                        tmem_st16(tmem + lane_off + L::kPCol + q * 16, pk);
+                        tmem_st16(tmem + lane_off + L::kDsCol + q * 16, dk);
+                    }
+                    if (!ok) break;
+                    tmem_st_wait();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(p_ready);
+                } else {
+                    // d = 128 in two steps.  First P^T from S^T, over S^T: the upper
+                    // half's P^T lands on columns the lower half reads, so every warp's
+                    // loads complete before any warp stores.
+                    uint32_t sr[2][32], dr[2][32];
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) tmem_ld32(tmem + lane_off + L::kXCol + (2 * hf + h) * 32, sr[h]);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) reg_fence32(sr[h]);
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(s_loaded);
+                    if (!warp_wait(s_loaded, gi & 1, abort_flag)) { ok = false; break; }
+                    tc_fence_after();
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int q = 2 * hf + h;
+                        // column col is query q0 + 32 q + col; it sees the key when it
+                        // exists and, causally, when key <= query
+                        const int qb = q0 + q * 32;
+                        uint32_t vis = 0xffffffffu;
+                        if (qb + 32 > p.N) vis = p.N > qb ? (0xffffffffu >> (32 - (p.N - qb))) : 0u;
+                        if (p.causal) {
+                            const int lo = key - qb;  // first visible column
+                            vis &= lo <= 0 ? 0xffffffffu : (lo >= 32 ? 0u : (0xffffffffu << lo));
+                        }
+                        uint32_t pk[16];
+                        p_quarter<BF16>(sr[h], pk, p.c, nl2_v + h * 32, vis);
+                        tmem_st16(tmem + lane_off + L::kPCol + q * 16, pk);
+                    }
+                    tmem_st_wait();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(p_ready);
+                    // Then dS^T = P^T (dP^T - D) over dP^T, the same way.
+                    if (!warp_wait(dp_full, gi & 1, abort_flag)) { ok = false; break; }
+                    tc_fence_after();
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) tmem_ld32(tmem + lane_off + L::kYCol + (2 * hf + h) * 32, dr[h]);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) reg_fence32(dr[h]);
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(dp_loaded);
+                    if (!warp_wait(dp_loaded, gi & 1, abort_flag)) { ok = false; break; }
+                    tc_fence_after();
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        uint32_t dk[16];
+                        ds_quarter<BF16>(sr[h], dr[h], dk, nd_v + h * 32);
+                        tmem_st16(tmem + lane_off + L::kDsCol + (2 * hf + h) * 16, dk);
+                    }
+                    tmem_st_wait();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(ds_ready);
                 }
-                tmem_st_wait();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(p_ready);
-                // Then dS^T = P^T (dP^T - D) over dP^T, the same way.
-                if (!warp_wait(dp_full, n & 1, abort_flag)) { ok = false; break; }
-                tc_fence_after();
-#pragma unroll
-                for (int h = 0; h < 2; ++h) tmem_ld32(tmem + lane_off + L::kYCol + (2 * hf + h) * 32, dr[h]);
-                tmem_ld_wait();
-#pragma unroll
-                for (int h = 0; h < 2; ++h) reg_fence32(dr[h]);
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(dp_loaded);
-                if (!warp_wait(dp_loaded, n & 1, abort_flag)) { ok = false; break; }
-                tc_fence_after();
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    uint32_t dk[16];
-                    ds_quarter<BF16>(sr[h], dr[h], dk, nd_v + h * 32);
-                    tmem_st16(tmem + lane_off + L::kDsCol + (2 * hf + h) * 16, dk);
-                }
-                tmem_st_wait();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(ds_ready);
             }
-        }
-        if (ok && warp_wait(acc_done, 0, abort_flag)) {
-            // the lower half stores dV, the upper half dK
+            if (!ok || !warp_wait(acc_done, k & 1, abort_flag)) {
+                ok = false;
+                break;
+            }
+            // the lower half stores dV, the upper half dK; the next unit's first dV and
+            // dK products (which overwrite the accumulators) wait for this warp's next
+            // P-ready (and, at d = 128, dS-ready) arrival, after these loads
             tc_fence_after();
             const int osize = p.grad_dtype == FA_F32 ? 4 : 2;
-            const size_t row_off = (static_cast<size_t>(bhk) * p.N + key) * D * osize;
+            const size_t row_off = (static_cast<size_t>(u.bhk) * p.N + key) * D * osize;
             uint8_t *dst = static_cast<uint8_t *>(hf ? p.g0 : p.g1) + row_off;
             const uint32_t acc_col = hf ? L::kBCol : L::kACol;
             const float mul = hf ? p.scale : 1.f;
@@ -632,6 +698,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 if (key < p.N) store_out32(dst + q * 32 * osize, o, mul, p.grad_dtype);
             }
             tc_fence_before();
+            g = g_end;
         }
     }
     tc_fence_before();
@@ -1003,9 +1070,12 @@ int launch_bwd_d(const BackwardLaunch &a, cudaStream_t stream) {
     p.scale = a.scale;
     p.c = a.scale * 1.4426950408889634f;
     if (e == cudaSuccess) {
+        // one persistent CTA per SM (or per unit, when there are fewer units)
         p.g0 = a.dk;
         p.g1 = a.dv;
-        bwd_dkdv_kernel<D, BF16><<<static_cast<unsigned>(BHk * p.n_t), kBwdThreads, L::kSmemBytes, stream>>>(
+        p.n_units = static_cast<int>(BHk * p.n_t);
+        const int grid = p.n_units < a.num_sms ? p.n_units : a.num_sms;
+        bwd_dkdv_kernel<D, BF16><<<static_cast<unsigned>(grid), kBwdThreads, L::kSmemBytes, stream>>>(
             mq, mk, mv, mdo, p);
         e = cudaGetLastError();
     }

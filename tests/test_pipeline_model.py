@@ -243,95 +243,122 @@ def dq_kernel(sim, units, plant=None):
         sim.role(f"warp{wq + 4 * hf}", elementwise(wq, hf))
 
 
-def dkdv_kernel_128(sim, n_iter, plant=None):
-    """bwd_dkdv_kernel at d = 128: P^T then dS^T written over S^T and dP^T in two
-    steps, the next item's S^T issued right after dV when its stage has landed."""
+def dkdv_kernel_128(sim, units, plant=None):
+    """bwd_dkdv_kernel at d = 128: one persistent CTA runs its key tiles (units) in
+    turn, each with n_iter (query head, query tile) items.  P^T then dS^T are
+    written over S^T and dP^T in two steps, the next item's S^T is issued right
+    after dV when its stage has landed (within a unit), K and V of the next unit
+    are loaded once the last score products of the unit before have read them,
+    and the ring and the per-item barriers run on across units."""
+    if isinstance(units, int):
+        units = [units]
     S = 2
     for name, count in [("s_full", 1), ("s_loaded", 8), ("p_ready", 8), ("dp_full", 1), ("dp_loaded", 8),
-                        ("ds_ready", 8), ("acc_done", 1)]:
+                        ("ds_ready", 8), ("acc_done", 1), ("fix_full", 1), ("fix_empty", 1)]:
         sim.bar(name, count)
     for s in range(S):
         sim.bar(f"ring_full{s}"), sim.bar(f"ring_empty{s}")
 
     def producer():
-        for n in range(n_iter):
-            slot = n % S
-            if n >= S:
-                yield ("wait", f"ring_empty{slot}", n // S - 1)
-            yield ("load", [(f"Q{slot}", ("Q", n)), (f"dO{slot}", ("dO", n)), (f"vec{slot}", ("vec", n))],
-                   f"ring_full{slot}")
+        g = 0
+        for k, n_iter in enumerate(units):
+            if k > 0 and plant != "no_fix_empty":
+                yield ("wait", "fix_empty", k - 1)
+            yield ("load", [("KV", ("KV", k))], "fix_full")
+            for n in range(n_iter):
+                slot = g % S
+                if g >= S:
+                    yield ("wait", f"ring_empty{slot}", g // S - 1)
+                yield ("load", [(f"Q{slot}", ("Q", g)), (f"dO{slot}", ("dO", g)), (f"vec{slot}", ("vec", g))],
+                       f"ring_full{slot}")
+                g += 1
 
     def mma():
-        def issue_s(j):
+        def issue_s(j, k):
             slot = j % S
-            yield ("mma", [(f"Q{slot}", ("Q", j))], [(x, ("S", j)) for x in cols("X")])
+            yield ("mma", [(f"Q{slot}", ("Q", j)), ("KV", ("KV", k))], [(x, ("S", j)) for x in cols("X")])
             yield ("commit", "s_full")
 
-        def issue_dp(j):
+        def issue_dp(j, k):
             slot = j % S
-            yield ("mma", [(f"dO{slot}", ("dO", j))], [(y, ("dP", j)) for y in cols("Y")])
+            yield ("mma", [(f"dO{slot}", ("dO", j)), ("KV", ("KV", k))], [(y, ("dP", j)) for y in cols("Y")])
             yield ("commit", "dp_full")
-        yield ("wait", "ring_full0", 0)
-        yield from issue_s(0)
-        yield from issue_dp(0)
-        for n in range(n_iter):
-            slot = n % S
-            nx, s_issued = n + 1, False
-            yield ("wait", "p_ready", n)
-            if nx < n_iter and plant == "s_before_dv":
-                # the mistake: the next S^T goes ahead of the dV product that reads P^T
-                yield ("wait", f"ring_full{nx % S}", nx // S)
-                yield from issue_s(nx)
-                s_issued = True
-            reads = [(f"X{wq}.{sb}", ("P", n)) for wq in range(4) for sb in range(4)] + [(f"dO{slot}", ("dO", n))]
-            if n > 0:
-                reads.append(("dV", ("dV", n - 1)))
-            yield ("mma", reads, [("dV", ("dV", n))])
-            if nx < n_iter and not s_issued:
-                landed = yield ("test", f"ring_full{nx % S}", nx // S)
-                if landed:
-                    yield from issue_s(nx)
+        g = 0
+        for k, n_iter in enumerate(units):
+            yield ("wait", "fix_full", k)
+            yield ("wait", f"ring_full{g % S}", g // S)
+            yield from issue_s(g, k)
+            yield from issue_dp(g, k)
+            if n_iter == 1:
+                yield ("commit", "fix_empty")
+            for n in range(n_iter):
+                gi = g + n
+                slot = gi % S
+                nx, s_issued = n + 1, False
+                yield ("wait", "p_ready", gi)
+                if nx < n_iter and plant == "s_before_dv":
+                    # the mistake: the next S^T goes ahead of the dV product that reads P^T
+                    yield ("wait", f"ring_full{(gi + 1) % S}", (gi + 1) // S)
+                    yield from issue_s(gi + 1, k)
                     s_issued = True
-            yield ("wait", "ds_ready", n)
-            reads = [(f"Y{wq}.{sb}", ("dS", n)) for wq in range(4) for sb in range(4)] + [(f"Q{slot}", ("Q", n))]
-            if n > 0:
-                reads.append(("dK", ("dK", n - 1)))
-            yield ("mma", reads, [("dK", ("dK", n))])
-            yield ("commit", f"ring_empty{slot}")
-            if nx < n_iter:
-                if not s_issued:
-                    yield ("wait", f"ring_full{nx % S}", nx // S)
-                    yield from issue_s(nx)
-                yield from issue_dp(nx)
-        yield ("commit", "acc_done")
+                reads = [(f"X{wq}.{sb}", ("P", gi)) for wq in range(4) for sb in range(4)] + \
+                        [(f"dO{slot}", ("dO", gi))]
+                if n > 0:
+                    reads.append(("dV", ("dV", k, n - 1)))
+                yield ("mma", reads, [("dV", ("dV", k, n))])
+                if nx < n_iter and not s_issued:
+                    landed = yield ("test", f"ring_full{(gi + 1) % S}", (gi + 1) // S)
+                    if landed:
+                        yield from issue_s(gi + 1, k)
+                        s_issued = True
+                yield ("wait", "ds_ready", gi)
+                reads = [(f"Y{wq}.{sb}", ("dS", gi)) for wq in range(4) for sb in range(4)] + \
+                        [(f"Q{slot}", ("Q", gi))]
+                if n > 0:
+                    reads.append(("dK", ("dK", k, n - 1)))
+                yield ("mma", reads, [("dK", ("dK", k, n))])
+                yield ("commit", f"ring_empty{slot}")
+                if nx < n_iter:
+                    if not s_issued:
+                        yield ("wait", f"ring_full{(gi + 1) % S}", (gi + 1) // S)
+                        yield from issue_s(gi + 1, k)
+                    yield from issue_dp(gi + 1, k)
+                    if nx + 1 == n_iter:
+                        yield ("commit", "fix_empty")  # the unit's last reads of K and V
+            yield ("commit", "acc_done")
+            g += n_iter
 
     def elementwise(wq, hf):
         mine = [4 * hf + i for i in range(4)]
-        for n in range(n_iter):
-            slot = n % S
-            yield ("wait", f"ring_full{slot}", n // S)
-            yield ("wait", "s_full", n)
-            for sb in mine:
-                yield ("read", f"X{wq}.{sb}", ("S", n))
-            yield ("arrive", "s_loaded")
-            if plant != "no_intra_sync":
-                yield ("wait", "s_loaded", n)
-            yield ("read", f"vec{slot}", ("vec", n))
-            for h in range(2):
-                yield ("write", f"X{wq}.{2 * hf + h}", ("P", n))
-            yield ("arrive", "p_ready")
-            yield ("wait", "dp_full", n)
-            for sb in mine:
-                yield ("read", f"Y{wq}.{sb}", ("dP", n))
-            yield ("arrive", "dp_loaded")
-            yield ("wait", "dp_loaded", n)
-            yield ("read", f"vec{slot}", ("vec", n))
-            for h in range(2):
-                yield ("write", f"Y{wq}.{2 * hf + h}", ("dS", n))
-            yield ("arrive", "ds_ready")
-        yield ("wait", "acc_done", 0)
-        yield ("read", "dV", ("dV", n_iter - 1))
-        yield ("read", "dK", ("dK", n_iter - 1))
+        g = 0
+        for k, n_iter in enumerate(units):
+            for n in range(n_iter):
+                gi = g + n
+                slot = gi % S
+                yield ("wait", f"ring_full{slot}", gi // S)
+                yield ("wait", "s_full", gi)
+                for sb in mine:
+                    yield ("read", f"X{wq}.{sb}", ("S", gi))
+                yield ("arrive", "s_loaded")
+                if plant != "no_intra_sync":
+                    yield ("wait", "s_loaded", gi)
+                yield ("read", f"vec{slot}", ("vec", gi))
+                for h in range(2):
+                    yield ("write", f"X{wq}.{2 * hf + h}", ("P", gi))
+                yield ("arrive", "p_ready")
+                yield ("wait", "dp_full", gi)
+                for sb in mine:
+                    yield ("read", f"Y{wq}.{sb}", ("dP", gi))
+                yield ("arrive", "dp_loaded")
+                yield ("wait", "dp_loaded", gi)
+                yield ("read", f"vec{slot}", ("vec", gi))
+                for h in range(2):
+                    yield ("write", f"Y{wq}.{2 * hf + h}", ("dS", gi))
+                yield ("arrive", "ds_ready")
+            yield ("wait", "acc_done", k)
+            yield ("read", "dV", ("dV", k, n_iter - 1))
+            yield ("read", "dK", ("dK", k, n_iter - 1))
+            g += n_iter
 
     sim.role("tma", producer())
     sim.role("mma", mma())
@@ -339,67 +366,99 @@ def dkdv_kernel_128(sim, n_iter, plant=None):
         sim.role(f"warp{wq + 4 * hf}", elementwise(wq, hf))
 
 
-def dkdv_kernel_64(sim, n_iter, plant=None):
+def dkdv_kernel_64(sim, units, plant=None):
     """bwd_dkdv_kernel at d = 64: P^T and dS^T in columns of their own, the next
-    item's S^T and dP^T issued once every warp holds the current ones."""
+    item's S^T and dP^T issued once every warp holds the current ones (across a
+    unit boundary once K and V of the next unit have landed)."""
+    if isinstance(units, int):
+        units = [units]
     S = 3
-    for name, count in [("s_full", 1), ("s_loaded", 8), ("p_ready", 8), ("pd_done", 1), ("acc_done", 1)]:
+    for name, count in [("s_full", 1), ("s_loaded", 8), ("p_ready", 8), ("pd_done", 1), ("acc_done", 1),
+                        ("fix_full", 1), ("fix_empty", 1)]:
         sim.bar(name, count)
     for s in range(S):
         sim.bar(f"ring_full{s}"), sim.bar(f"ring_empty{s}")
 
     def producer():
-        for n in range(n_iter):
-            slot = n % S
-            if n >= S:
-                yield ("wait", f"ring_empty{slot}", n // S - 1)
-            yield ("load", [(f"Q{slot}", ("Q", n)), (f"dO{slot}", ("dO", n)), (f"vec{slot}", ("vec", n))],
-                   f"ring_full{slot}")
+        g = 0
+        for k, n_iter in enumerate(units):
+            if k > 0 and plant != "no_fix_empty":
+                yield ("wait", "fix_empty", k - 1)
+            yield ("load", [("KV", ("KV", k))], "fix_full")
+            for n in range(n_iter):
+                slot = g % S
+                if g >= S:
+                    yield ("wait", f"ring_empty{slot}", g // S - 1)
+                yield ("load", [(f"Q{slot}", ("Q", g)), (f"dO{slot}", ("dO", g)), (f"vec{slot}", ("vec", g))],
+                       f"ring_full{slot}")
+                g += 1
 
     def mma():
-        def scores(j):
+        def scores(j, k):
             slot = j % S
             yield ("wait", f"ring_full{slot}", j // S)
-            yield ("mma", [(f"Q{slot}", ("Q", j))], [(x, ("S", j)) for x in cols("X")])
-            yield ("mma", [(f"dO{slot}", ("dO", j))], [(y, ("dP", j)) for y in cols("Y")])
+            yield ("mma", [(f"Q{slot}", ("Q", j)), ("KV", ("KV", k))], [(x, ("S", j)) for x in cols("X")])
+            yield ("mma", [(f"dO{slot}", ("dO", j)), ("KV", ("KV", k))], [(y, ("dP", j)) for y in cols("Y")])
             yield ("commit", "s_full")
-        yield from scores(0)
-        for n in range(n_iter):
-            slot = n % S
-            if n + 1 < n_iter:
-                yield ("wait", "s_loaded", n)
-                yield from scores(n + 1)
-            yield ("wait", "p_ready", n)
-            pr = [(f"PP{wq}.{q}", ("P", n)) for wq in range(4) for q in range(4)]
-            dr = [(f"DD{wq}.{q}", ("dS", n)) for wq in range(4) for q in range(4)]
-            yield ("mma", pr + [(f"dO{slot}", ("dO", n))] + ([("dV", ("dV", n - 1))] if n else []),
-                   [("dV", ("dV", n))])
-            yield ("mma", dr + [(f"Q{slot}", ("Q", n))] + ([("dK", ("dK", n - 1))] if n else []),
-                   [("dK", ("dK", n))])
-            yield ("commit", f"ring_empty{slot}")
-            yield ("commit", "pd_done")
-        yield ("commit", "acc_done")
+        g = 0
+        for k, n_iter in enumerate(units):
+            yield ("wait", "fix_full", k)
+            if g > 0:  # implied by p_ready of the unit before, waited for all the same
+                yield ("wait", "s_loaded", g - 1)
+            yield from scores(g, k)
+            if n_iter == 1:
+                yield ("commit", "fix_empty")
+            for n in range(n_iter):
+                gi = g + n
+                slot = gi % S
+                if n + 1 < n_iter:
+                    yield ("wait", "s_loaded", gi)
+                    yield from scores(gi + 1, k)
+                    if n + 2 == n_iter:
+                        yield ("commit", "fix_empty")
+                yield ("wait", "p_ready", gi)
+                pr = [(f"PP{wq}.{q}", ("P", gi)) for wq in range(4) for q in range(4)]
+                dr = [(f"DD{wq}.{q}", ("dS", gi)) for wq in range(4) for q in range(4)]
+                yield ("mma", pr + [(f"dO{slot}", ("dO", gi))] + ([("dV", ("dV", k, n - 1))] if n else []),
+                       [("dV", ("dV", k, n))])
+                yield ("mma", dr + [(f"Q{slot}", ("Q", gi))] + ([("dK", ("dK", k, n - 1))] if n else []),
+                       [("dK", ("dK", k, n))])
+                yield ("commit", f"ring_empty{slot}")
+                yield ("commit", "pd_done")
+            yield ("commit", "acc_done")
+            g += n_iter
 
     def elementwise(wq, hf):
         mine = [4 * hf + i for i in range(4)]
-        for n in range(n_iter):
-            slot = n % S
-            yield ("wait", f"ring_full{slot}", n // S)
-            yield ("wait", "s_full", n)
-            for sb in mine:
-                yield ("read", f"X{wq}.{sb}", ("S", n))
-                yield ("read", f"Y{wq}.{sb}", ("dP", n))
-            yield ("arrive", "s_loaded")
-            yield ("read", f"vec{slot}", ("vec", n))
-            if n > 0 and plant != "no_pd_done":
-                yield ("wait", "pd_done", n - 1)
-            for h in range(2):
-                yield ("write", f"PP{wq}.{2 * hf + h}", ("P", n))
-                yield ("write", f"DD{wq}.{2 * hf + h}", ("dS", n))
-            yield ("arrive", "p_ready")
-        yield ("wait", "acc_done", 0)
-        yield ("read", "dV", ("dV", n_iter - 1))
-        yield ("read", "dK", ("dK", n_iter - 1))
+        g = 0
+        late = None  # planted: an epilogue left until after the next unit's first item
+        for k, n_iter in enumerate(units):
+            for n in range(n_iter):
+                gi = g + n
+                slot = gi % S
+                yield ("wait", f"ring_full{slot}", gi // S)
+                yield ("wait", "s_full", gi)
+                for sb in mine:
+                    yield ("read", f"X{wq}.{sb}", ("S", gi))
+                    yield ("read", f"Y{wq}.{sb}", ("dP", gi))
+                yield ("arrive", "s_loaded")
+                yield ("read", f"vec{slot}", ("vec", gi))
+                if gi > 0 and plant != "no_pd_done":
+                    yield ("wait", "pd_done", gi - 1)
+                for h in range(2):
+                    yield ("write", f"PP{wq}.{2 * hf + h}", ("P", gi))
+                    yield ("write", f"DD{wq}.{2 * hf + h}", ("dS", gi))
+                yield ("arrive", "p_ready")
+                if late is not None:
+                    yield ("read", "dV", late)
+                    late = None
+            yield ("wait", "acc_done", k)
+            if plant == "late_epilogue" and k + 1 < len(units):
+                late = ("dV", k, n_iter - 1)
+            else:
+                yield ("read", "dV", ("dV", k, n_iter - 1))
+            yield ("read", "dK", ("dK", k, n_iter - 1))
+            g += n_iter
 
     sim.role("tma", producer())
     sim.role("mma", mma())
@@ -419,26 +478,29 @@ def test_protocol_holds_under_random_interleavings(kernel, n_iter):
         sim.run()
 
 
+@pytest.mark.parametrize("kernel", sorted(KERNELS))
 @pytest.mark.parametrize("units", [[1, 1], [2, 3], [3, 1, 2], [7, 2]])
-def test_persistent_dq_protocol_holds_under_random_interleavings(units):
-    # one CTA running several query tiles in turn
+def test_persistent_protocol_holds_under_random_interleavings(kernel, units):
+    # one CTA running several units (query tiles for dQ, key tiles for dK/dV) in turn
     for seed in range(150):
         sim = Sim(7000 + seed)
-        dq_kernel(sim, units)
+        KERNELS[kernel](sim, units)
         sim.run()
 
 
-@pytest.mark.parametrize("plant", ["no_fix_empty", "late_epilogue"])
-def test_the_model_catches_a_planted_unit_boundary_mistake(plant):
+@pytest.mark.parametrize("kernel,plant", [("dq", "no_fix_empty"), ("dq", "late_epilogue"),
+                                          ("dkdv128", "no_fix_empty"), ("dkdv64", "no_fix_empty"),
+                                          ("dkdv64", "late_epilogue")])
+def test_the_model_catches_a_planted_unit_boundary_mistake(kernel, plant):
     caught = 0
     for seed in range(150):
         sim = Sim(seed)
-        dq_kernel(sim, [2, 1, 3], plant)
+        KERNELS[kernel](sim, [2, 1, 3], plant)
         try:
             sim.run()
         except ProtocolError:
             caught += 1
-    assert caught > 0, f"dq with {plant} passed every interleaving"
+    assert caught > 0, f"{kernel} with {plant} passed every interleaving"
 
 
 @pytest.mark.parametrize("kernel,plant", [("dq", "no_dq_done"), ("dq", "scores_before_loaded"),
