@@ -45,8 +45,8 @@ NCU_TRAFFIC = {
     # d=128, bf16): --set full at N=8192, the two DRAM counters alone at 4096 and
     # 16384 (one pass each, on the full-size problem).
     "prefill": {"src": ["fa_prefill_sm103.cu", "fa_tiles.cuh", "sm103_ptx.cuh"],
-                "src_sha": "aa0b899ef579541d",
-                "bytes_per_launch": {"4096": 50.45e6, "8192": 114.47e6, "16384": 253.67e6}},
+                "src_sha": "530f2202b99ec8b5",
+                "bytes_per_launch": {"4096": 50.44e6, "8192": 114.70e6, "16384": 254.23e6}},
     # one decode_split_kernel<64> launch of the step's decode problem (B=32, H=14)
     "decode": {"src": ["fa_decode_sm103.cu", "sm103_ptx.cuh"], "src_sha": "c3e7decaeb0c1c3f",
                "bytes_per_launch": 263.59e6},
@@ -201,6 +201,7 @@ def run_ours(args):
 
     from attention_forward_prefill_gb300 import binding
     from attention_forward_prefill_gb300 import build as fa_build
+    from attention_forward_prefill_gb300 import inputs as fin
 
     world, rank, local = dist_env()
     device = torch.device("cuda", local)
@@ -230,12 +231,27 @@ def run_ours(args):
     # Extra problems, only when asked for (profiling and diagnostics; not part of
     # the headline): "shape:BxHxNxD[:causal]" is a forward prefill, "backward" the
     # backward of (1, 16, 4096, 128) and "backward:BxHxNxD[:causal]" any other;
-    # fp16 at d = 64, bf16 at d = 128.
+    # fp16 at d = 64, bf16 at d = 128.  "decode:BxHqxHkv" is a decode over caches
+    # of 4096 rows, d = 64, fp16, with the decode configs' ragged lengths for B
+    # (grouped when Hkv < Hq), reported in GB/s of K/V rows read.
     extras = []
     for c in cases or []:
         kind, _, spec = c.partition(":")
         if kind == "backward" and not spec:
             spec = "1x16x4096x128"
+        if kind == "decode" and spec:
+            B, Hq, Hkv = (int(x) for x in spec.split("x"))
+            xq = gen_tensor(torch, device, (B, Hq, 1, DECODE_D), CFG_DECODE, fin.TENSOR_Q, torch.float16,
+                            rank, 1000 + len(extras))
+            xk, xv = (gen_tensor(torch, device, (B, Hkv, DECODE_L, DECODE_D), CFG_DECODE, t, torch.float16,
+                                 rank, 1000 + len(extras)) for t in (fin.TENSOR_K, fin.TENSOR_V))
+            x_lens_np = fin.seq_lens(fin.seed_for(CFG_DECODE, fin.TENSOR_SEQLEN) + B, B, DECODE_L)
+            x_lens = torch.from_numpy(x_lens_np).to(device)
+            xo = torch.empty_like(xq)
+            fn = (lambda xq=xq, xk=xk, xv=xv, x_lens=x_lens, xo=xo:
+                  binding.decode(xq, xk, xv, x_lens, scale=0.125, out=xo))
+            extras.append((c, fn, decode_bytes(x_lens_np, Hkv, DECODE_D), "GB/s"))
+            continue
         if kind not in ("shape", "backward") or not spec:
             continue
         dims, _, flag = spec.partition(":")
@@ -255,7 +271,7 @@ def run_ours(args):
             fn = (lambda t=t, o=o, causal=causal, sc=sc:
                   binding.prefill(t[0], t[1], t[2], causal=causal, scale=sc, out=o))
             flops = prefill_flops(B, H, N, d, causal)
-        extras.append((c, fn, flops))
+        extras.append((c, fn, flops, "TFLOP/s"))
 
     def step(record):
         ev = []
@@ -277,7 +293,7 @@ def run_ours(args):
                            out=dout)
             e1.record(stream)
             ev.append(("decode", 0, e0, e1))
-        for name, fn, _ in extras:
+        for name, fn, _, _ in extras:
             flush.zero_()
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
@@ -315,7 +331,7 @@ def run_ours(args):
 
     pre_ms = {N: [] for N in do_pre}
     dec_ms = []
-    extra_ms = {name: [] for name, _, _ in extras}
+    extra_ms = {name: [] for name, _, _, _ in extras}
     for ev in records:
         for kind, N, e0, e1 in ev:
             {"prefill": pre_ms.get(N), "decode": dec_ms, "extra": extra_ms.get(N)}[kind].append(
@@ -384,9 +400,11 @@ def run_ours(args):
         _, info, _ = binding.fa_prefill_plan(PREFILL_B, PREFILL_H, N, N, 0, 0, 0)
         per_step += 1 + (1 if info[0] and info[5] > 0 else 0)
     per_step += 2 if do_dec else 0
-    for name, _, _ in extras:  # backward: prep + dK/dV + dQ; forward as above
+    for name, _, _, _ in extras:  # backward: prep + dK/dV + dQ; decode: split + merge
         if name.startswith("backward"):
             per_step += 3
+        elif name.startswith("decode"):
+            per_step += 2
         else:
             B, H, N, d = (int(x) for x in name.split(":")[1].split("x"))
             _, info, _ = binding.fa_prefill_plan(B, H, N, N, int(name.endswith(":causal")), 0, 0)
@@ -460,9 +478,11 @@ def run_ours(args):
                          "traffic": dec_traffic, "peak_source": f"{peak_src} copy bandwidth"},
         }
     if extras:
-        line["extras"] = {name: {"median_ms": round(statistics.median(extra_ms[name]), 4),
-                                 "tflops": round(fl / (statistics.median(extra_ms[name]) / 1e3) / 1e12, 1)}
-                          for name, _, fl in extras}
+        line["extras"] = {}
+        for name, _, amount, unit in extras:
+            ms = statistics.median(extra_ms[name])
+            key, scale = ("gbs", 1e9) if unit == "GB/s" else ("tflops", 1e12)
+            line["extras"][name] = {"median_ms": round(ms, 4), key: round(amount / (ms / 1e3) / scale, 1)}
     if world > 1:
         dist.destroy_process_group()
     return line
