@@ -676,12 +676,12 @@ int fa_decode_gqa(const void *q, const void *k_cache, const void *v_cache, const
     }
     int chunk = 0;
     splits = decode_effective_splits(max_len, splits, &chunk);
-    // A CTA keeps the scores of its chunk for up to 8 query heads (2, 4 or 8
+    // A CTA keeps the scores of its chunk for up to 4 query heads (2 or 4
     // rows of shared memory) within 192 KB.
     const int group = Hq / Hkv;
     const int slices = decode_group_slices(group);
     const int gper = (group + slices - 1) / slices;
-    const int rows = group == 1 ? 1 : (gper <= 2 ? 2 : (gper <= 4 ? 4 : 8));
+    const int rows = group == 1 ? 1 : (gper <= 2 ? 2 : 4);
     if (static_cast<long long>(chunk) * rows > kDecodeMaxChunk) return FA_ERR_SPLITS;
     const size_t need = fa_decode_workspace_bytes(B, Hq, max_len, d, splits);
     if (workspace && workspace_bytes < need) return FA_ERR_WORKSPACE;

@@ -551,10 +551,8 @@ int launch_decode_d(const DecodeLaunch &a, cudaStream_t stream) {
         e = cudaGetLastError();
     } else if (p.gper <= 2) {
         e = launch_gqa_split<D, 2>(p, a, stream);
-    } else if (p.gper <= 4) {
+    } else {  // decode_group_slices keeps gper <= 4
         e = launch_gqa_split<D, 4>(p, a, stream);
-    } else {
-        e = launch_gqa_split<D, 8>(p, a, stream);
     }
     if (e != cudaSuccess) return cuda_fail(e);
     cudaLaunchConfig_t cfg = {};

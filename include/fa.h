@@ -334,7 +334,8 @@ size_t fa_decode_workspace_bytes(int B, int H, int max_len, int d,
  * Other arguments, results and errors as fa_decode_ex; in addition
  * FA_ERR_SHAPE when Hq % Hkv != 0, and FA_ERR_SPLITS when a chunk would need
  * more than 192 KB of shared memory for the scores of its query heads
- * (chunk x 8 > 48K rows for groups of more than 4 heads per CTA).
+ * (chunk x 4 > 48K rows when a CTA serves 3 or 4 query heads: a group of G
+ * query heads is served by ceil(G / 4) CTAs per chunk).
  */
 int fa_decode_gqa(const void *q, const void *k_cache, const void *v_cache,
                   const int32_t *seq_lens, void *out,

@@ -195,7 +195,7 @@ def test_grouped_decode_argument_errors(lib):
     assert call(d=32) == 3
     assert call(lens=L + 2) == 5
     assert call(splits=4096 // 64 + 1) == binding.FA_ERR_SPLITS
-    # 32 query heads per cache head: 8 per CTA, so a chunk may hold 6K rows
+    # 32 query heads per cache head: 4 per CTA, so a chunk may hold 12K rows
     assert call(Hq=32, Hkv=1, max_len=60000, splits=1) == binding.FA_ERR_SPLITS
     assert call(ws=1 << 12, wsb=16, splits=4) == 8
 
@@ -204,7 +204,7 @@ def test_grouped_decode_argument_errors(lib):
                                         (4, 8, 8, 4096)])
 def test_grouped_split_choice(lib, B, Hq, Hkv, L):
     s = binding.fa_decode_splits_for_sms(B, Hq, Hkv, L, 152)
-    rows = Hkv * ((Hq // Hkv + 7) // 8)
+    rows = Hkv * ((Hq // Hkv + 3) // 4)
     if Hq == Hkv:
         assert s == binding.fa_decode_splits_for_sms(B, Hq, Hq, L, 152)
     else:   # about 5 CTAs per SM, chunks of 64..512 rows, rounded to 64-row chunks
