@@ -60,10 +60,10 @@ int plan_prefill(int B, int Hq, int Nq, int Nk, int causal, int no_skip, int sch
 int launch_prefill(const PrefillLaunch &a, const DeviceInfo &dev, cudaStream_t stream);
 
 // Grouped decode: a group of G query heads is cut into ceil(G / 4) slices,
-// one CTA row each, so that a CTA holds at most 4 query heads.  (With 8, a
-// thread's queries and accumulators took 168 registers and 3 CTAs fit an SM;
-// with 4, 96 registers and 5 CTAs: 14 query heads over 2 cache heads decode
-// 7-9% faster although each K/V row is read by two CTAs.)
+// one CTA row each, so that a CTA holds at most 4 query heads.  (With 8 at
+// d = 64, a thread's queries and accumulators took 168 registers and 3 CTAs fit
+// an SM; with 4, 112 registers and 4 CTAs: 14 query heads over 2 cache heads
+// decode 7-13% faster although each K/V row is read by two CTAs.)
 inline int decode_group_slices(int group) { return (group + 3) / 4; }
 
 struct DecodeLaunch {
