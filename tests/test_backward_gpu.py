@@ -125,6 +125,25 @@ def test_grouped_head_gradients_match_oracle(fa, oracle_mod, shape, hkv, dtype, 
         assert e <= REL_TOL[dtype], f"{name} {shape}/{hkv} {dtype} causal={causal}: {e:.3e}"
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_grouped_gradients_with_several_units_per_cta(fa, oracle_mod, causal):
+    # 64 query heads over 16 key/value heads at N = 2048: 256 dK/dV units and 1024 dQ
+    # units on the persistent grids, so every CTA runs several units in turn, each
+    # dK/dV unit summing over its 4 query heads.  Two whole groups are checked.
+    shape, hkv, dtype = (1, 64, 2048, 64), 16, "f16"
+    (q, k, v, g), scale, lse, grads = run(fa, shape, dtype, causal, 3700, hkv=hkv)
+    got = [G.device_to_f64(t) for t in grads]
+    for kvh in (0, hkv - 1):
+        qs = slice(4 * kvh, 4 * kvh + 4)
+        f = [oracle_mod.bits_to_f64(np.ascontiguousarray(x[:, sl]), dtype)
+             for x, sl in ((q, qs), (k, slice(kvh, kvh + 1)), (v, slice(kvh, kvh + 1)), (g, qs))]
+        want = oracle_mod.attention_backward(*f, causal, scale, threads=4)
+        for name, got_t, sl, w in zip(("dq", "dk", "dv"), got, (qs, slice(kvh, kvh + 1), slice(kvh, kvh + 1)),
+                                      want):
+            e = rel_err(got_t[:, sl], w)
+            assert e <= REL_TOL[dtype], f"{name} kv head {kvh} causal={causal}: {e:.3e}"
+
+
 @pytest.mark.parametrize("shape,dtype,hkv", [((2, 4, 1000, 128), "bf16", None), ((2, 6, 1000, 64), "f16", 2)])
 def test_gradients_are_bit_identical_run_to_run(fa, shape, dtype, hkv):
     # d = 64 runs the dK/dV pipeline whose score products overlap the elementwise work
