@@ -45,7 +45,7 @@ def declarations():
     return out
 
 
-# The boundary as the survey's hot-path table lists it, call for call.
+# The boundary's entry points, call for call, with their parameter lists.
 BOUNDARY = {
     "fa_prefill": ("int", ["const void*q", "const void*k", "const void*v", "void*out", "int B",
                            "int H", "int N", "int d", "int causal", "float scale", "void*stream"]),
