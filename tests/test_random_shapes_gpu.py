@@ -182,7 +182,11 @@ def test_random_backward(fa, oracle_mod, case):
     for name, got_t, w, m in zip(("dq", "dk", "dv"), grads, want, model):
         got = G.device_to_f64(got_t)
         assert got.shape == w.shape
-        top = max(np.abs(w).max(), 1e-30)
+        # A row that sees a single key has P = 1 and O = V, so dS = P (dP - D) and the
+        # exact dQ and dK are zero; only the fp32 rounding of dP - D remains.  Errors
+        # are therefore measured against at least 0.01, a hundredth of the gradient
+        # scale of these unit-variance inputs.
+        top = max(np.abs(w).max(), 1e-2)
         tol = max(BWD_TOL[dt], 1.25 * float(np.abs(m - w).max() / top)) + GRAD_ROUND[grad]
         e = float(np.abs(got - w).max() / top)
         assert e <= tol, (f"{name} case {case}: B={B} H={H} Hkv={Hkv} N={N} d={d} {dt}->{grad} "
