@@ -7,7 +7,9 @@ the schedule flags for prefill; a packed batch of random lengths; decode with
 random lengths (zero included) and a random split count, plain and grouped;
 the backward with grouped heads, both masks, every gradient type and tiny
 lengths.  The sizes stay small enough for the oracle to finish in seconds,
-and span several tiles and ragged tails.
+and span several tiles and ragged tails; a larger set (up to 6000 keys and 32
+heads) reaches the stream-K cuts and the persistent grids' several units per
+CTA, checked on sampled rows or whole key/value groups.
 """
 import numpy as np
 import pytest
@@ -191,3 +193,67 @@ def test_random_backward(fa, oracle_mod, case):
         e = float(np.abs(got - w).max() / top)
         assert e <= tol, (f"{name} case {case}: B={B} H={H} Hkv={Hkv} N={N} d={d} {dt}->{grad} "
                           f"causal={causal} scale={scale:.3f}: {e:.3e} > {tol:.3e}")
+
+
+# Larger shapes: 700 to 6000 keys and up to 32 heads, so that stream-K cuts units
+# between CTAs and the persistent grids run several units per CTA; the forward is
+# checked on sampled rows (tile edges, the middle, the end and seeded rows), the
+# backward on two whole key/value groups.
+@pytest.mark.parametrize("case", range(24))
+def test_random_large_prefill(fa, oracle_mod, case):
+    import torch
+    rng = np.random.default_rng(50000 + case)
+    B = int(rng.integers(1, 3))
+    Hkv = int(rng.integers(1, 9))
+    Hq = Hkv * int(rng.choice([1, 1, 2, 4]))
+    Nk = int(rng.integers(700, 6000))
+    Nq = Nk if rng.integers(0, 3) else int(rng.integers(100, Nk + 1))
+    d = int(rng.choice([64, 128]))
+    dt = str(rng.choice(["f16", "bf16"]))
+    causal = bool(rng.integers(0, 2))
+    flags = int(rng.choice([0, 2, 4]))
+    out_dt = str(rng.choice(["f32", dt]))
+    scale = 1 / np.sqrt(d)
+    q = inputs.normal_bits((B, Hq, Nq, d), 51000 + case, dt)
+    k = inputs.normal_bits((B, Hkv, Nk, d), 52000 + case, dt)
+    v = inputs.normal_bits((B, Hkv, Nk, d), 53000 + case, dt)
+    out = fa.prefill(*(G.bits_to_device(x, dt) for x in (q, k, v)), causal=causal, scale=scale,
+                     out_dtype=G.torch_dtype(out_dt), flags=flags)
+    torch.cuda.synchronize()
+    rows = G.sample_rows(Nq, case)
+    want = oracle_mod.attention(*(oracle_mod.bits_to_f64(x, dt) for x in (q, k, v)), causal, scale,
+                                rows=rows, threads=G.THREADS)
+    G.assert_close(G.device_to_f64(out)[:, :, rows], want, dt, out_dt,
+                   f"large case {case}: B={B} Hq={Hq} Hkv={Hkv} Nq={Nq} Nk={Nk} d={d} causal={causal} "
+                   f"flags={flags}")
+
+
+@pytest.mark.parametrize("case", range(8))
+def test_random_large_backward(fa, oracle_mod, case):
+    import torch
+    rng = np.random.default_rng(60000 + case)
+    B = int(rng.integers(1, 3))
+    Hkv = int(rng.integers(1, 9))
+    grp = int(rng.choice([1, 2, 4]))
+    H = Hkv * grp
+    N = int(rng.integers(500, 4000))
+    d = int(rng.choice([64, 128]))
+    dt = str(rng.choice(["f16", "bf16"]))
+    causal = bool(rng.integers(0, 2))
+    scale = 1 / np.sqrt(d)
+    q, g = (inputs.normal_bits((B, H, N, d), 61000 + 10 * case + i, dt) for i in (0, 3))
+    k, v = (inputs.normal_bits((B, Hkv, N, d), 61000 + 10 * case + i, dt) for i in (1, 2))
+    qd, kd, vd, gd = (G.bits_to_device(x, dt) for x in (q, k, v, g))
+    out, lse = fa.prefill_with_lse(qd, kd, vd, causal=causal, scale=scale)
+    grads = [G.device_to_f64(t) for t in fa.prefill_backward(qd, kd, vd, out, gd, lse, causal=causal,
+                                                             scale=scale, grad_dtype=torch.float32)]
+    torch.cuda.synchronize()
+    for b, kvh in ((0, 0), (B - 1, Hkv - 1)):
+        qs, ks = slice(grp * kvh, grp * kvh + grp), slice(kvh, kvh + 1)
+        f = [oracle_mod.bits_to_f64(np.ascontiguousarray(x[b:b + 1, sl]), dt)
+             for x, sl in ((q, qs), (k, ks), (v, ks), (g, qs))]
+        want = oracle_mod.attention_backward(*f, causal, scale, threads=G.THREADS)
+        for name, got, sl, w in zip(("dq", "dk", "dv"), grads, (qs, ks, ks), want):
+            e = float(np.abs(got[b:b + 1, sl] - w).max() / max(np.abs(w).max(), 1e-2))
+            assert e <= BWD_TOL[dt], (f"{name} large case {case}: B={B} H={H} Hkv={Hkv} N={N} d={d} {dt} "
+                                      f"causal={causal}, batch {b} kv head {kvh}: {e:.3e}")
