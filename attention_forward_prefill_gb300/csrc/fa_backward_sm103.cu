@@ -13,16 +13,17 @@
 // Three kernels, no atomics, so every gradient is bit-identical run to run:
 //   bwd_prep   -D_i and -L2_i = -L_i log2 e for every row (fp32), per head padded
 //              to whole 128-row tiles;
-//   bwd_dkdv   one CTA per 128-key tile of a key/value head: S^T = K Q_i^T and
+//   bwd_dkdv   per unit, a 128-key tile of a key/value head: S^T = K Q_i^T and
 //              dP^T = V dO_i^T in TMEM, then P^T and dS^T as 16-bit (over them
 //              at d = 128, in columns of their own at d = 64), then
 //              dV += P^T dO_i and dK += dS^T Q_i accumulate in TMEM over the
 //              query tiles that see the keys, of every query head that reads
 //              this key/value head;
-//   bwd_dq     one CTA per 128-query tile: S = Q K_j^T, dP = dO V_j^T, dS in
+//   bwd_dq     per unit, a 128-query tile: S = Q K_j^T, dP = dO V_j^T, dS in
 //              columns of its own, dQ += dS K_j over the key tiles the queries see.
-// Both main kernels issue the next tile's score products while the elementwise
-// warps still work on the current one, as far as TMEM and the rings allow.
+// Both main kernels are persistent (one CTA per SM, units dealt in snake order)
+// and issue the next tile's score products while the elementwise warps still
+// work on the current one, as far as TMEM and the rings allow.
 // Warp roles per CTA (320 threads): warps 0-7 elementwise work, thread = TMEM
 // lane = tile row, two warps per row quadrant taking half of the tile's columns
 // each; warp 8 TMA producer; warp 9 tcgen05 issuer and TMEM owner.
