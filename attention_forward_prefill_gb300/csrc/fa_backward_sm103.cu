@@ -147,6 +147,9 @@ __global__ void __launch_bounds__(kPrepThreads) bwd_prep_kernel(const uint16_t *
                                                                 long long rows_pad, int N, int npad) {
     constexpr int LPR = D / 8;       // lanes per row
     constexpr int RPW = 32 / LPR;    // rows per warp and word
+    // The dK/dV pass (launched with programmatic dependent launch) may start its
+    // set-up now; it waits for this grid before it reads D and L2.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int lane = threadIdx.x & 31, sub = lane % LPR;
     const long long warp_g = (static_cast<long long>(blockIdx.x) * kPrepThreads + threadIdx.x) >> 5;
     const long long first = warp_g * RPW * kPrepRows + lane / LPR;
@@ -319,6 +322,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // the parity of the unit counter k; those that complete once per item on the
     // parity of the CTA's item counter g, which runs on across units, and so does
     // the ring of (Q, dO) stages.
+    // The dQ pass (programmatic dependent launch) may start its set-up once this
+    // grid runs; it waits for this grid to finish before it reads D and L2.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     if (threadIdx.x == 0) {
         mbar_init(fix_full, 1);
@@ -360,6 +366,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             const uint64_t pol = l2_policy_evict_last();
             bool ok = true;
             int nfix = 0, ni = 0;  // K/V pairs and ring items issued
+            bool prep_done = false;  // D and L2 come from the grid before (prep)
             DkdvUnit u;
             for (int k = 0; ok && dkdv_unit(p, k, u); ++k) {
                 // K and V of the unit before must have been read by its last products
@@ -390,7 +397,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         tma_load_3d(st + L::kTileBytes + c * kSlabBytes, &map_do, ring_full + slot, c * 64, row,
                                     bhq, pol);
                     }
-                    // the 128 queries' L2 and D (the padded layout keeps both copies whole)
+                    // the 128 queries' L2 and D (the padded layout keeps both copies whole),
+                    // written by the prep grid this one may have started beside
+                    if (!prep_done) {
+                        asm volatile("griddepcontrol.wait;" ::: "memory");
+                        prep_done = true;
+                    }
                     const size_t vrow = static_cast<size_t>(bhq) * p.npad + row;
                     bulk_load(st + L::kVecInStage, p.lse2 + vrow, kRows * 4, ring_full + slot);
                     bulk_load(st + L::kVecInStage + kRows * 4, p.dsum + vrow, kRows * 4, ring_full + slot);
@@ -929,6 +941,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int wq = warp & 3, hf = warp >> 2;  // TMEM lane quadrant; column half
         const int r = wq * 32 + lane;
         const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+        // D and L2 are written by prep, two grids back: wait for the grids before
+        // this one (launched early beside the dK/dV pass) to finish.
+        asm volatile("griddepcontrol.wait;" ::: "memory");
         bool ok = true;
         int g = 0;
         DqUnit u;
@@ -1024,6 +1039,26 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (threadIdx.x == 0 && *abort_flag) atomicCAS(&g_backward_status, 0, (int)FA_ERR_WATCHDOG);
 }
 
+// A backward main kernel, launched so that it may start while the grid before it
+// still runs (programmatic dependent launch); it waits for that grid itself where
+// it reads what the grid wrote.
+template <typename K>
+cudaError_t launch_pdl(K kernel, int grid, size_t smem, cudaStream_t stream, const CUtensorMap &mq,
+                       const CUtensorMap &mk, const CUtensorMap &mv, const CUtensorMap &mdo, const BwdParams &p) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(kBwdThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, mq, mk, mv, mdo, p);
+    return e == cudaSuccess ? cudaGetLastError() : e;
+}
+
 template <int D, bool BF16>
 int launch_bwd_d(const BackwardLaunch &a, cudaStream_t stream) {
     using L = BwdLayout<D>;
@@ -1076,9 +1111,7 @@ int launch_bwd_d(const BackwardLaunch &a, cudaStream_t stream) {
         p.g1 = a.dv;
         p.n_units = static_cast<int>(BHk * p.n_t);
         const int grid = p.n_units < a.num_sms ? p.n_units : a.num_sms;
-        bwd_dkdv_kernel<D, BF16><<<static_cast<unsigned>(grid), kBwdThreads, L::kSmemBytes, stream>>>(
-            mq, mk, mv, mdo, p);
-        e = cudaGetLastError();
+        e = launch_pdl(bwd_dkdv_kernel<D, BF16>, grid, L::kSmemBytes, stream, mq, mk, mv, mdo, p);
     }
     if (e == cudaSuccess) {
         // one persistent CTA per SM (or per unit, when there are fewer units)
@@ -1086,9 +1119,7 @@ int launch_bwd_d(const BackwardLaunch &a, cudaStream_t stream) {
         p.g1 = nullptr;
         p.n_units = static_cast<int>(BH * p.n_t);
         const int grid = p.n_units < a.num_sms ? p.n_units : a.num_sms;
-        bwd_dq_kernel<D, BF16><<<static_cast<unsigned>(grid), kBwdThreads, DqLayout<D>::kSmemBytes, stream>>>(
-            mq, mk, mv, mdo, p);
-        e = cudaGetLastError();
+        e = launch_pdl(bwd_dq_kernel<D, BF16>, grid, DqLayout<D>::kSmemBytes, stream, mq, mk, mv, mdo, p);
     }
     const cudaError_t e2 = scratch_free(ws, stream);
     if (e == cudaSuccess) e = e2;
