@@ -19,6 +19,7 @@ from . import build as _build
 FA_F16, FA_BF16, FA_F32 = 0, 1, 2
 FA_FLAG_NONE, FA_FLAG_NO_CAUSAL_SKIP = 0, 1
 FA_FLAG_SCHEDULE_UNITS, FA_FLAG_SCHEDULE_STREAM_K = 2, 4
+FA_BWD_FLAG_NONE, FA_BWD_RECOMPUTE_DQ = 0, 1
 FA_OK = 0
 STATUS_NAMES = {
     0: "FA_OK", 1: "FA_ERR_NULL", 2: "FA_ERR_SHAPE", 3: "FA_ERR_HEAD_DIM",
@@ -45,6 +46,8 @@ _SIGNATURES = {
                             _vp]),
     "fa_prefill_backward": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i,
                                  _i, _f, _i, _i, _vp]),
+    "fa_prefill_backward_ex": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i,
+                                    _i, _f, _i, _i, _u, _vp]),
     "fa_prefill_plan": (_i, [_i, _i, _i, _i, _i, _u, _i, _vp, _vp, _i]),
     "fa_decode": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _vp]),
     "fa_decode_ex": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _i, _i, _vp, _sz, _vp]),
@@ -140,6 +143,13 @@ def fa_prefill_backward(q, k, v, out, dout, lse, dq, dk, dv, B, H, Hkv, N, d, ca
                         in_dtype, grad_dtype, stream=0) -> int:
     return load().fa_prefill_backward(q, k, v, out, dout, lse, dq, dk, dv, B, H, Hkv, N, d,
                                       int(causal), float(scale), in_dtype, grad_dtype, stream)
+
+
+def fa_prefill_backward_ex(q, k, v, out, dout, lse, dq, dk, dv, B, H, Hkv, N, d, causal, scale,
+                           in_dtype, grad_dtype, flags=0, stream=0) -> int:
+    return load().fa_prefill_backward_ex(q, k, v, out, dout, lse, dq, dk, dv, B, H, Hkv, N, d,
+                                         int(causal), float(scale), in_dtype, grad_dtype, flags,
+                                         stream)
 
 
 def fa_prefill_plan(B, Hq, Nq, Nk, causal, flags=0, num_sms=0, max_items=192):
@@ -366,9 +376,10 @@ def prefill_with_lse(q, k, v, causal: bool = False, scale: float | None = None, 
 
 
 def prefill_backward(q, k, v, out, dout, lse, causal: bool = False, scale: float | None = None,
-                     grad_dtype=None):
+                     grad_dtype=None, flags: int = 0):
     """(dq, dk, dv) for square prefill with q, out, dout [B, H, N, d] and k, v
-    [B, Hkv, N, d], from the forward's out and lse; dk, dv have k's shape."""
+    [B, Hkv, N, d], from the forward's out and lse; dk, dv have k's shape.
+    flags: FA_BWD_* bits (FA_BWD_RECOMPUTE_DQ)."""
     torch = _torch()
     B, H, N, d = q.shape
     for name, t in (("q", q), ("out", out), ("dout", dout)):
@@ -384,12 +395,12 @@ def prefill_backward(q, k, v, out, dout, lse, causal: bool = False, scale: float
     grad_dtype = q.dtype if grad_dtype is None else grad_dtype
     dq = torch.empty(q.shape, dtype=grad_dtype, device=q.device)
     dk, dv = (torch.empty(k.shape, dtype=grad_dtype, device=q.device) for _ in range(2))
-    rc = fa_prefill_backward(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
-                             dout.data_ptr(), lse.data_ptr(), dq.data_ptr(), dk.data_ptr(),
-                             dv.data_ptr(), B, H, Hkv, N, d, causal, scale, dtype_code(q.dtype),
-                             dtype_code(grad_dtype), _stream_handle(q.device))
+    rc = fa_prefill_backward_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                dout.data_ptr(), lse.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                                dv.data_ptr(), B, H, Hkv, N, d, causal, scale, dtype_code(q.dtype),
+                                dtype_code(grad_dtype), flags, _stream_handle(q.device))
     if rc != FA_OK:
-        raise FaError(rc, "fa_prefill_backward")
+        raise FaError(rc, "fa_prefill_backward_ex")
     return dq, dk, dv
 
 

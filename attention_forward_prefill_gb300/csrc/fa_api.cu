@@ -23,7 +23,7 @@ DeviceInfo g_dev_cache[kMaxDevices];
 bool g_dev_have[kMaxDevices] = {};
 
 cudaMemPool_t g_pool[kMaxDevices] = {};
-constexpr uint64_t kPoolKeepBytes = 1024ull << 20;  // freed scratch kept mapped
+constexpr uint64_t kPoolKeepBytes = 5ull << 30;  // freed scratch kept mapped (a backward dS table: up to 4 GiB)
 
 constexpr int kDecodeRowAlign = 64;      // chunk lengths are multiples of this
 constexpr int kDecodeAutoMaxChunk = 512;  // automatic choice: at most 512 rows per CTA
@@ -512,10 +512,10 @@ int fa_prefill_plan(int B, int Hq, int Nq, int Nk, int causal, unsigned flags, i
                         schedule_of(flags), num_sms, info, items, max_items);
 }
 
-int fa_prefill_backward(const void *q, const void *k, const void *v, const void *out,
-                        const void *dout, const float *lse, void *dq, void *dk, void *dv, int B,
-                        int H, int Hkv, int N, int d, int causal, float scale, fa_dtype in_dtype,
-                        fa_dtype grad_dtype, void *stream) {
+int fa_prefill_backward_ex(const void *q, const void *k, const void *v, const void *out,
+                           const void *dout, const float *lse, void *dq, void *dk, void *dv, int B,
+                           int H, int Hkv, int N, int d, int causal, float scale, fa_dtype in_dtype,
+                           fa_dtype grad_dtype, unsigned flags, void *stream) {
     if (!q || !k || !v || !out || !dout || !lse || !dq || !dk || !dv) return FA_ERR_NULL;
     if (B < 1 || H < 1 || Hkv < 1 || N < 1 || H % Hkv != 0 ||
         static_cast<long long>(B) * H * N > INT_MAX)
@@ -565,7 +565,16 @@ int fa_prefill_backward(const void *q, const void *k, const void *v, const void 
     a.in_bf16 = in_dtype == FA_BF16 ? 1 : 0;
     a.grad_dtype = grad_dtype;
     a.num_sms = dev.num_sms;
+    a.recompute_dq = (flags & FA_BWD_RECOMPUTE_DQ) ? 1 : 0;
     return launch_backward(a, static_cast<cudaStream_t>(stream));
+}
+
+int fa_prefill_backward(const void *q, const void *k, const void *v, const void *out,
+                        const void *dout, const float *lse, void *dq, void *dk, void *dv, int B,
+                        int H, int Hkv, int N, int d, int causal, float scale, fa_dtype in_dtype,
+                        fa_dtype grad_dtype, void *stream) {
+    return fa_prefill_backward_ex(q, k, v, out, dout, lse, dq, dk, dv, B, H, Hkv, N, d, causal, scale,
+                                  in_dtype, grad_dtype, FA_BWD_FLAG_NONE, stream);
 }
 
 int fa_prefill_ex(const void *q, const void *k, const void *v, void *out, int B, int H, int N,

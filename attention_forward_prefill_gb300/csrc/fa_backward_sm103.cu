@@ -108,7 +108,43 @@ struct BwdParams {
     float c;            // scale * log2(e)
     int n_units;        // units dealt to the persistent CTAs: dkdv (key/value head, key
                         // tile), dq (query head, query tile)
+    // dkdv: when set, dS of every (key tile j, query tile i) item of query head h is
+    // also written here, one 32 KB block per (h, j, i), for the dQ product pass that
+    // reads it instead of recomputing S and dP.
+    uint16_t *ds_t;
 };
+
+// The dS table.  A block holds the 128 x 128 16-bit dS values of (query head h,
+// key tile j, query tile i) in the tensor core's unswizzled layout for an MN-major
+// operand, so that the dQ pass copies it to shared memory as it is: 8 x 8 core
+// matrices of 128 bytes (8 keys, each with 8 consecutive queries), the 16 key
+// groups of a query group adjacent (128 bytes apart), query groups 2 KB apart.
+// Key row r of a warp's 32 writes its 8 queries of query group g at
+// g * 2048 + (r / 8) * 128 + (r % 8) * 16 bytes: the warp's 32 16-byte stores
+// fill 512 contiguous bytes.
+constexpr int kDsCoreBytes = 128;                    // 8 keys x 8 queries
+constexpr int kDsGroupBytes = 16 * kDsCoreBytes;     // a query group: 128 keys
+constexpr int kDsBlockBytes = kRows * kRows * 2;     // 32 KB
+
+__device__ __forceinline__ uint16_t *ds_block(const BwdParams &p, int h, int j, int i) {
+    return p.ds_t + ((static_cast<size_t>(h) * p.n_t + j) * p.n_t + i) * (kRows * kRows);
+}
+
+// Key row r's slot in query group 0 of its block.
+__device__ __forceinline__ uint16_t *ds_key_row(uint16_t *block, int r) {
+    return block + ((r >> 3) * kDsCoreBytes + (r & 7) * 16) / 2;
+}
+
+// Key row r's 32 dS values of queries 32 q .. 32 q + 31 (16 packed words), four
+// query groups, as streaming (evict-first) stores: the table passes through L2
+// once and should not push out the Q and dO tiles that the other key tiles read
+// there again.
+__device__ __forceinline__ void store_ds_quarter(uint16_t *row, int q, const uint32_t (&w)[16]) {
+#pragma unroll
+    for (int v = 0; v < 4; ++v)
+        __stcs(reinterpret_cast<uint4 *>(row + (4 * q + v) * (kDsGroupBytes / 2)),
+               make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]));
+}
 
 // ---------------------------------------------------------------- D and L2
 // Rows of the padded [B Hq][npad] layout; rows past N get zeros, so that every
@@ -570,8 +606,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             const int key = u.jt * kRows + r;
             const int g_end = g + u.n_iter;
             int qt = u.i_first;  // the item's query tile: i_first .. n_t - 1, once per query head
-            for (int gi = g; gi < g_end && ok; ++gi, qt = qt + 1 == p.n_t ? u.i_first : qt + 1) {
+            int hq = u.bhq0;     // the item's query head
+            for (int gi = g; gi < g_end && ok; ++gi) {
                 const int q0 = qt * kRows;
+                uint16_t *const ds_row = p.ds_t ? ds_key_row(ds_block(p, hq, u.jt, qt), r) : nullptr;
+                if (++qt == p.n_t) {
+                    qt = u.i_first;
+                    ++hq;
+                }
                 // this half's 64 query columns: L2 and D, brought into the ring stage with
                 // Q_i and dO_i (the MMA thread waited for the same barrier; so do we)
                 const int slot = gi % L::kStages;
@@ -607,6 +649,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         const int qb = q0 + q * 32;
                         uint32_t vis = 0xffffffffu;
                         if (qb + 32 > p.N) vis = p.N > qb ? (0xffffffffu >> (32 - (p.N - qb))) : 0u;
+                        if (key >= p.N) vis = 0u;  // a padding key row: P and dS stay 0
                         if (p.causal) {
                             const int lo = key - qb;  // first visible column
                             vis &= lo <= 0 ? 0xffffffffu : (lo >= 32 ? 0u : (0xffffffffu << lo));
@@ -623,6 +666,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         }
                         tmem_st16(tmem + lane_off + L::kPCol + q * 16, pk);
                         tmem_st16(tmem + lane_off + L::kDsCol + q * 16, dk);
+                        if (ds_row) store_ds_quarter(ds_row, q, dk);
                     }
                     if (!ok) break;
                     tmem_st_wait();
@@ -652,6 +696,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         const int qb = q0 + q * 32;
                         uint32_t vis = 0xffffffffu;
                         if (qb + 32 > p.N) vis = p.N > qb ? (0xffffffffu >> (32 - (p.N - qb))) : 0u;
+                        if (key >= p.N) vis = 0u;  // a padding key row: P and dS stay 0
                         if (p.causal) {
                             const int lo = key - qb;  // first visible column
                             vis &= lo <= 0 ? 0xffffffffu : (lo >= 32 ? 0u : (0xffffffffu << lo));
@@ -682,6 +727,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         uint32_t dk[16];
                         ds_quarter<BF16>(sr[h], dr[h], dk, nd_v + h * 32);
                         tmem_st16(tmem + lane_off + L::kDsCol + (2 * hf + h) * 16, dk);
+                        if (ds_row) store_ds_quarter(ds_row, 2 * hf + h, dk);
                     }
                     tmem_st_wait();
                     tc_fence_before();
@@ -1039,15 +1085,211 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (threadIdx.x == 0 && *abort_flag) atomicCAS(&g_backward_status, 0, (int)FA_ERR_WATCHDOG);
 }
 
+// ---------------------------------------------------------------- dQ from stored dS
+// dQ_i = scale sum_j dS_ij K_j, with the dS blocks the dK/dV pass wrote: a
+// pipelined product, no recomputation of S and dP.  Warps 0-3 epilogue (thread =
+// TMEM lane = query row), warp 4 copy producer, warp 5 MMA issuer.  Each ring
+// stage holds the dS block (j, i), copied whole by one bulk copy, and K_j
+// [128 keys][d] by TMA.  Both are MN-major operands: A = dS (queries along M) in
+// the unswizzled core-matrix layout, 256 bytes per 16 keys; B = K_j with d
+// contiguous, 128-byte swizzled, 2 KB per 16 keys.  Two TMEM accumulators let the
+// epilogue of one unit run under the next unit's products.  Units are the dQ
+// pass's (query head, query tile), dealt in the same snake order.
+template <int D>
+struct DqgLayout {
+    static constexpr int kChunks = D / 64;
+    static constexpr int kDsBytes = kDsBlockBytes;             // 128 keys x 128 queries
+    static constexpr int kKBytes = kChunks * kSlabBytes;       // 128 keys x D
+    static constexpr int kStageBytes = kDsBytes + kKBytes;
+    static constexpr int kStages = D == 128 ? 3 : 4;
+    static constexpr int kBarOff = kStages * kStageBytes;
+    // full[S], empty[S], acc_full[2], acc_free[2], drain
+    static constexpr int kNumBars = 2 * kStages + 5;
+    static constexpr int kMiscOff = kBarOff + kNumBars * 8;
+    static constexpr int kSmemBytes = kMiscOff + 16 + 1024;
+    static constexpr uint32_t kTmemCols = 256;                 // two accumulators of D columns
+};
+constexpr int kDqgThreads = 192;
+constexpr int kDqgTmaWarp = 4;
+constexpr int kDqgMmaWarp = 5;
+
+// O (+)= A B over 128 keys with both operands MN-major in shared memory: eight
+// products of 16 keys, each 256 bytes further on in A (16 in the descriptor's
+// address field) and 2 KB in B (128).
+#define FA_MMA_SS_MN(OA, OB)                                                  \
+    "add.u32 xa, %1, " #OA ";\n\t"                                          \
+    "add.u32 xb, %3, " #OB ";\n\t"                                          \
+    "mov.b64 a, {xa, %2};\n\t"                                              \
+    "mov.b64 b, {xb, %4};\n\t"                                              \
+    "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %5, pt;\n\t"
+
+__device__ __forceinline__ void issue_ss_mn(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                            bool accumulate) {
+    const uint32_t alo = static_cast<uint32_t>(a_desc), ahi = static_cast<uint32_t>(a_desc >> 32);
+    const uint32_t blo = static_cast<uint32_t>(b_desc), bhi = static_cast<uint32_t>(b_desc >> 32);
+    asm volatile(
+        "{\n\t.reg .pred pf, pt;\n\t.reg .b64 a, b;\n\t.reg .b32 xa, xb;\n\t"
+        "setp.ne.b32 pf, %6, 0;\n\t"
+        "setp.eq.b32 pt, %6, %6;\n\t"
+        "mov.b64 a, {%1, %2};\n\t"
+        "mov.b64 b, {%3, %4};\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %5, pf;\n\t"
+        FA_MMA_SS_MN(16, 128) FA_MMA_SS_MN(32, 256) FA_MMA_SS_MN(48, 384) FA_MMA_SS_MN(64, 512)
+        FA_MMA_SS_MN(80, 640) FA_MMA_SS_MN(96, 768) FA_MMA_SS_MN(112, 896)
+        "}" ::"r"(d_tmem), "r"(alo), "r"(ahi), "r"(blo), "r"(bhi), "r"(idesc), "r"(accumulate ? 1u : 0u)
+        : "memory");
+}
+#undef FA_MMA_SS_MN
+
+template <int D, bool BF16>
+__global__ void __launch_bounds__(kDqgThreads, 1)
+    bwd_dq_gemm_kernel(const __grid_constant__ CUtensorMap map_k, const BwdParams p) {
+    using L = DqgLayout<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kBarOff);
+    uint64_t *full = bars, *empty = bars + L::kStages;
+    uint64_t *acc_full = bars + 2 * L::kStages, *acc_free = acc_full + 2, *drain = acc_full + 4;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kMiscOff);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kMiscOff + 4);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < L::kStages; ++s) {
+            mbar_init(full + s, 1);
+            mbar_init(empty + s, 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(acc_full + b, 1);
+            mbar_init(acc_free + b, 4);  // one arrival per epilogue warp
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == kDqgMmaWarp) {
+        tmem_alloc(tmem_slot, L::kTmemCols);
+        tmem_relinquish();
+    }
+    if (warp == kDqgTmaWarp && lane == 0) prefetch_tensormap(&map_k);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == kDqgTmaWarp) {
+        if (lane == 0) {
+            // dS is read once; K_j by every query tile of the head
+            const uint64_t pol = l2_policy_evict_last(), pol_ds = l2_policy_evict_first();
+            bool ok = true;
+            int ni = 0;  // stages issued
+            // dS comes from the dK/dV grid this one may have started beside
+            asm volatile("griddepcontrol.wait;" ::: "memory");
+            DqUnit u;
+            for (int k = 0; ok && dq_unit(p, k, u); ++k) {
+                for (int j = 0; j < u.n_iter; ++j) {
+                    const int slot = ni % L::kStages;
+                    if (ni >= L::kStages &&
+                        !mbar_wait(empty + slot, ((ni / L::kStages) - 1) & 1, abort_flag, kWatchdogNs)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t *st = smem + slot * L::kStageBytes;
+                    mbar_arrive_expect_tx(full + slot, L::kStageBytes);
+                    bulk_load_hint(st, ds_block(p, u.bh, j, u.it), kDsBlockBytes, full + slot, pol_ds);
+                    for (int c = 0; c < L::kChunks; ++c)
+                        tma_load_3d(st + L::kDsBytes + c * kSlabBytes, &map_k, full + slot, c * 64, j * kRows,
+                                    u.bhk, pol);
+                    ++ni;
+                }
+            }
+            if (!ok) {  // let every copy already issued land
+                constexpr uint64_t kDrainNs = 200ull * 1000ull * 1000ull;
+                int dummy = 0;
+                for (int m = (ni > L::kStages ? ni - L::kStages : 0); m < ni; ++m)
+                    mbar_wait(full + (m % L::kStages), (m / L::kStages) & 1, &dummy, kDrainNs);
+            }
+        }
+        __syncwarp();
+    } else if (warp == kDqgMmaWarp) {
+        if (lane == 0) {
+            const uint32_t idesc = idesc_f16(BF16, kRows, D, true, true);
+            const uint32_t ring = smem_u32(smem);
+            bool ok = true;
+            int ni = 0;
+            DqUnit u;
+            for (int k = 0; ok && dq_unit(p, k, u); ++k) {
+                const int b = k & 1;
+                // this accumulator's last reader: the epilogue of unit k - 2
+                if (k >= 2 && !mbar_wait(acc_free + b, ((k - 2) >> 1) & 1, abort_flag, kWatchdogNs)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                for (int j = 0; j < u.n_iter; ++j) {
+                    const int slot = ni % L::kStages;
+                    if (!mbar_wait(full + slot, (ni / L::kStages) & 1, abort_flag, kWatchdogNs)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t st = ring + slot * L::kStageBytes;
+                    issue_ss_mn(tmem + b * D, sdesc_plain(st, kDsCoreBytes, kDsGroupBytes),
+                                sdesc_sw128(st + L::kDsBytes, kSlabBytes, 1024), idesc, j > 0);
+                    umma_commit(empty + slot);
+                    ++ni;
+                }
+                if (!ok) break;
+                umma_commit(acc_full + b);
+            }
+            umma_commit(drain);
+            int dummy = 0;
+            mbar_wait(drain, 0, &dummy, kWatchdogNs);
+        }
+        __syncwarp();
+    } else {
+        // ---------------------------------------------------------------- epilogue
+        const int r = warp * 32 + lane;  // warps 0-3: TMEM lane quadrant = warp
+        const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+        const int osize = p.grad_dtype == FA_F32 ? 4 : 2;
+        DqUnit u;
+        for (int k = 0; dq_unit(p, k, u); ++k) {
+            const int b = k & 1;
+            if (!warp_wait(acc_full + b, (k >> 1) & 1, abort_flag)) break;
+            tc_fence_after();
+            const int qrow = u.it * kRows + r;
+            uint8_t *dst = static_cast<uint8_t *>(p.g0) + (static_cast<size_t>(u.bh) * p.N + qrow) * D * osize;
+#pragma unroll
+            for (int q = 0; q < D / 32; ++q) {
+                uint32_t o[32];
+                tmem_ld32(tmem + lane_off + b * D + q * 32, o);
+                tmem_ld_wait();
+                reg_fence32(o);
+                if (qrow < p.N) store_out32(dst + q * 32 * osize, o, p.scale, p.grad_dtype);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acc_free + b);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kDqgMmaWarp) {
+        tc_fence_after();
+        tmem_dealloc(tmem, L::kTmemCols);
+    }
+    if (threadIdx.x == 0 && *abort_flag) atomicCAS(&g_backward_status, 0, (int)FA_ERR_WATCHDOG);
+}
+
 // A backward main kernel, launched so that it may start while the grid before it
 // still runs (programmatic dependent launch); it waits for that grid itself where
 // it reads what the grid wrote.
-template <typename K>
-cudaError_t launch_pdl(K kernel, int grid, size_t smem, cudaStream_t stream, const CUtensorMap &mq,
-                       const CUtensorMap &mk, const CUtensorMap &mv, const CUtensorMap &mdo, const BwdParams &p) {
+template <typename K, typename... Args>
+cudaError_t launch_pdl(K kernel, int grid, int threads, size_t smem, cudaStream_t stream, const Args &...args) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
-    cfg.blockDim = dim3(kBwdThreads);
+    cfg.blockDim = dim3(static_cast<unsigned>(threads));
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -1055,9 +1297,13 @@ cudaError_t launch_pdl(K kernel, int grid, size_t smem, cudaStream_t stream, con
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, mq, mk, mv, mdo, p);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, args...);
     return e == cudaSuccess ? cudaGetLastError() : e;
 }
+
+// The dQ pass reads dS from a workspace when it is at most this large; larger
+// problems (or a caller's flag) take the pass that recomputes S and dP.
+constexpr size_t kDsWorkspaceMax = 4ull << 30;
 
 template <int D, bool BF16>
 int launch_bwd_d(const BackwardLaunch &a, cudaStream_t stream) {
@@ -1078,7 +1324,9 @@ int launch_bwd_d(const BackwardLaunch &a, cudaStream_t stream) {
     if ((e = cudaFuncSetAttribute(bwd_dkdv_kernel<D, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   L::kSmemBytes)) != cudaSuccess ||
         (e = cudaFuncSetAttribute(bwd_dq_kernel<D, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  DqLayout<D>::kSmemBytes)) != cudaSuccess)
+                                  DqLayout<D>::kSmemBytes)) != cudaSuccess ||
+        (e = cudaFuncSetAttribute(bwd_dq_gemm_kernel<D, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  DqgLayout<D>::kSmemBytes)) != cudaSuccess)
         return cuda_fail(e);
     void *ws = nullptr;
     if ((e = scratch_alloc(&ws, static_cast<size_t>(rows_pad) * 2 * sizeof(float), stream)) != cudaSuccess) {
@@ -1086,6 +1334,13 @@ int launch_bwd_d(const BackwardLaunch &a, cudaStream_t stream) {
         return FA_ERR_WORKSPACE;
     }
     float *lse2 = static_cast<float *>(ws), *dsum = lse2 + rows_pad;
+    // dS^T blocks for the dQ product pass, when they fit the limit and the pool
+    void *ds = nullptr;
+    const size_t ds_bytes = static_cast<size_t>(BH) * n_t * n_t * kRows * kRows * 2;
+    if (!a.recompute_dq && ds_bytes <= kDsWorkspaceMax && scratch_alloc(&ds, ds_bytes, stream) != cudaSuccess) {
+        cudaGetLastError();  // an allocation failure only selects the recomputing pass
+        ds = nullptr;
+    }
     constexpr long long kPrepRowsPerBlock = (kPrepThreads / 32) * (32 / (D / 8)) * kPrepRows;
     bwd_prep_kernel<D, BF16><<<static_cast<unsigned>((rows_pad + kPrepRowsPerBlock - 1) / kPrepRowsPerBlock),
                                kPrepThreads, 0, stream>>>(
@@ -1105,13 +1360,14 @@ int launch_bwd_d(const BackwardLaunch &a, cudaStream_t stream) {
     p.grad_dtype = a.grad_dtype;
     p.scale = a.scale;
     p.c = a.scale * 1.4426950408889634f;
+    p.ds_t = static_cast<uint16_t *>(ds);
     if (e == cudaSuccess) {
         // one persistent CTA per SM (or per unit, when there are fewer units)
         p.g0 = a.dk;
         p.g1 = a.dv;
         p.n_units = static_cast<int>(BHk * p.n_t);
         const int grid = p.n_units < a.num_sms ? p.n_units : a.num_sms;
-        e = launch_pdl(bwd_dkdv_kernel<D, BF16>, grid, L::kSmemBytes, stream, mq, mk, mv, mdo, p);
+        e = launch_pdl(bwd_dkdv_kernel<D, BF16>, grid, kBwdThreads, L::kSmemBytes, stream, mq, mk, mv, mdo, p);
     }
     if (e == cudaSuccess) {
         // one persistent CTA per SM (or per unit, when there are fewer units)
@@ -1119,10 +1375,19 @@ int launch_bwd_d(const BackwardLaunch &a, cudaStream_t stream) {
         p.g1 = nullptr;
         p.n_units = static_cast<int>(BH * p.n_t);
         const int grid = p.n_units < a.num_sms ? p.n_units : a.num_sms;
-        e = launch_pdl(bwd_dq_kernel<D, BF16>, grid, DqLayout<D>::kSmemBytes, stream, mq, mk, mv, mdo, p);
+        if (ds) {
+            e = launch_pdl(bwd_dq_gemm_kernel<D, BF16>, grid, kDqgThreads, DqgLayout<D>::kSmemBytes, stream, mk, p);
+        } else {
+            e = launch_pdl(bwd_dq_kernel<D, BF16>, grid, kBwdThreads, DqLayout<D>::kSmemBytes, stream, mq, mk,
+                           mv, mdo, p);
+        }
     }
-    const cudaError_t e2 = scratch_free(ws, stream);
+    cudaError_t e2 = scratch_free(ws, stream);
     if (e == cudaSuccess) e = e2;
+    if (ds) {
+        e2 = scratch_free(ds, stream);
+        if (e == cudaSuccess) e = e2;
+    }
     if (e != cudaSuccess) return cuda_fail(e);
     return FA_OK;
 }

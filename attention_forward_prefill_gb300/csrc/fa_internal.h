@@ -97,6 +97,7 @@ struct BackwardLaunch {
     int in_bf16;
     int grad_dtype;
     int num_sms;                         // persistent grids: at most one CTA per SM
+    int recompute_dq;                    // 1: the dQ pass recomputes S and dP instead of reading dS
 };
 
 int launch_backward(const BackwardLaunch &a, cudaStream_t stream);

@@ -189,7 +189,11 @@ int fa_prefill_lse(const void *q, const void *k, const void *v, void *out,
  *                        may overlap another argument
  *   causal, scale      : as in the forward call
  * Scratch of 8 bytes per query row, with each head's rows rounded up to a
- * multiple of 128, comes from the library's pool.  Errors as for
+ * multiple of 128, comes from the library's pool.  So does, when it is at most
+ * 4 GiB (H x ceil(N / 128)^2 x 32 KB per sequence), a table of the score
+ * gradients dS that the dK/dV pass writes in 16-bit and the dQ pass multiplies
+ * by K; larger problems, or a failed allocation of that table, take a dQ pass
+ * that recomputes S and dP instead (as FA_BWD_RECOMPUTE_DQ).  Errors as for
  * prefill: FA_ERR_NULL, FA_ERR_SHAPE, FA_ERR_HEAD_DIM, FA_ERR_DTYPE,
  * FA_ERR_ALIGN, FA_ERR_SCALE, FA_ERR_ALIAS, FA_ERR_WORKSPACE, FA_ERR_ARCH,
  * FA_ERR_CUDA.
@@ -199,6 +203,23 @@ int fa_prefill_backward(const void *q, const void *k, const void *v,
                         void *dq, void *dk, void *dv, int B, int H, int Hkv, int N,
                         int d, int causal, float scale, fa_dtype in_dtype,
                         fa_dtype grad_dtype, void *stream);
+
+/* Flags for fa_prefill_backward_ex. */
+#define FA_BWD_FLAG_NONE 0u
+/* The dQ pass recomputes the scores and their gradient tile by tile instead of
+ * reading the dS table, and takes no table from the pool.  The result stays
+ * within the tolerance either way and is bit-identical run to run for a given
+ * choice.  Other bits are reserved and ignored. */
+#define FA_BWD_RECOMPUTE_DQ 1u
+
+/* fa_prefill_backward with `flags` (FA_BWD_* bits); same arguments, errors and
+ * results otherwise.  fa_prefill_backward is this call with FA_BWD_FLAG_NONE. */
+int fa_prefill_backward_ex(const void *q, const void *k, const void *v,
+                           const void *out, const void *dout, const float *lse,
+                           void *dq, void *dk, void *dv, int B, int H, int Hkv,
+                           int N, int d, int causal, float scale,
+                           fa_dtype in_dtype, fa_dtype grad_dtype,
+                           unsigned flags, void *stream);
 
 /*
  * The schedule fa_prefill_gqa would use for a dense problem on num_sms SMs
@@ -271,7 +292,8 @@ int fa_prefill_varlen(const void *q, const void *k, const void *v, void *out,
  * the device-resident lengths, so it needs no device-to-host copy and gives
  * bit-identical results run to run.  The partials workspace is allocated
  * stream-ordered on `stream` from a memory pool the library creates once per
- * device; the pool keeps up to 1 GiB of freed scratch mapped for reuse.
+ * device; the pool keeps up to 5 GiB of freed scratch mapped for reuse (the
+ * largest backward dS table is 4 GiB).
  */
 int fa_decode(const void *q, const void *k_cache, const void *v_cache,
               const int32_t *seq_lens, void *out,

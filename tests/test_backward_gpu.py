@@ -41,7 +41,7 @@ def fa():
     assert binding.fa_device_status(False) == 0, "a kernel watchdog fired"
 
 
-def run(fa, shape, dtype, causal, seed, grad="f32", hkv=None):
+def run(fa, shape, dtype, causal, seed, grad="f32", hkv=None, flags=0):
     import torch
     kv_shape = shape if hkv is None else (shape[0], hkv, shape[2], shape[3])
     q, g = (inputs.normal_bits(shape, seed + i, dtype) for i in (0, 3))
@@ -50,7 +50,7 @@ def run(fa, shape, dtype, causal, seed, grad="f32", hkv=None):
     scale = 1.0 / np.sqrt(shape[-1])
     out, lse = fa.prefill_with_lse(qd, kd, vd, causal=causal, scale=scale)
     dq, dk, dv = fa.prefill_backward(qd, kd, vd, out, gd, lse, causal=causal, scale=scale,
-                                     grad_dtype=G.torch_dtype(grad))
+                                     grad_dtype=G.torch_dtype(grad), flags=flags)
     torch.cuda.synchronize()
     return (q, k, v, g), scale, lse, (dq, dk, dv)
 
@@ -63,13 +63,29 @@ def rel_err(got, want):
                                          ((1, 2, 300, 128), "bf16"), ((1, 4, 1024, 128), "bf16"),
                                          ((1, 2, 1000, 64), "bf16")])
 @pytest.mark.parametrize("causal", [False, True])
-def test_gradients_match_oracle(fa, oracle_mod, shape, dtype, causal):
-    (q, k, v, g), scale, lse, grads = run(fa, shape, dtype, causal, 3000 + shape[2])
+@pytest.mark.parametrize("dq_path", ["ds_table", "recompute"])
+def test_gradients_match_oracle(fa, oracle_mod, shape, dtype, causal, dq_path):
+    flags = fa.FA_BWD_RECOMPUTE_DQ if dq_path == "recompute" else 0
+    (q, k, v, g), scale, lse, grads = run(fa, shape, dtype, causal, 3000 + shape[2], flags=flags)
     f = [oracle_mod.bits_to_f64(x, dtype) for x in (q, k, v, g)]
     want = oracle_mod.attention_backward(*f, causal, scale, threads=G.THREADS)
     for name, got_t, w in zip(("dq", "dk", "dv"), grads, want):
         e = rel_err(G.device_to_f64(got_t), w)
-        assert e <= REL_TOL[dtype], f"{name} {shape} {dtype} causal={causal}: {e:.3e}"
+        assert e <= REL_TOL[dtype], f"{name} {shape} {dtype} causal={causal} {dq_path}: {e:.3e}"
+
+
+@pytest.mark.parametrize("shape,dtype,hkv", [((2, 3, 1000, 128), "bf16", None), ((1, 6, 643, 64), "f16", 3)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_ds_table_and_recompute_paths_agree(fa, shape, dtype, hkv, causal):
+    # dK and dV come from the same pass either way: bit-identical.  dQ from the
+    # stored 16-bit dS and from the recomputed one differ only by the fp32 order
+    # of the score products, far inside the oracle bound.
+    a = run(fa, shape, dtype, causal, 3800, hkv=hkv)[3]
+    b = run(fa, shape, dtype, causal, 3800, hkv=hkv, flags=fa.FA_BWD_RECOMPUTE_DQ)[3]
+    for name, x, y in zip(("dk", "dv"), a[1:], b[1:]):
+        assert np.array_equal(G.device_to_f64(x), G.device_to_f64(y)), name
+    e = rel_err(G.device_to_f64(a[0]), G.device_to_f64(b[0]))
+    assert e <= REL_TOL[dtype] / 4, f"dq {shape} causal={causal}: {e:.3e}"
 
 
 @pytest.mark.parametrize("N", [4096, 8192])
@@ -113,9 +129,11 @@ def test_lse_under_the_stream_k_schedule(fa, oracle_mod):
 @pytest.mark.parametrize("shape,hkv,dtype", [((1, 6, 300, 64), 2, "f16"), ((2, 8, 512, 128), 1, "bf16"),
                                              ((1, 14, 257, 64), 2, "bf16")])
 @pytest.mark.parametrize("causal", [False, True])
-def test_grouped_head_gradients_match_oracle(fa, oracle_mod, shape, hkv, dtype, causal):
+@pytest.mark.parametrize("dq_path", ["ds_table", "recompute"])
+def test_grouped_head_gradients_match_oracle(fa, oracle_mod, shape, hkv, dtype, causal, dq_path):
     # a shared key/value head collects the gradients of all its query heads
-    (q, k, v, g), scale, lse, grads = run(fa, shape, dtype, causal, 3500 + shape[1], hkv=hkv)
+    flags = fa.FA_BWD_RECOMPUTE_DQ if dq_path == "recompute" else 0
+    (q, k, v, g), scale, lse, grads = run(fa, shape, dtype, causal, 3500 + shape[1], hkv=hkv, flags=flags)
     f = [oracle_mod.bits_to_f64(x, dtype) for x in (q, k, v, g)]
     want = oracle_mod.attention_backward(*f, causal, scale, threads=G.THREADS)
     for name, got_t, w in zip(("dq", "dk", "dv"), grads, want):
@@ -145,11 +163,13 @@ def test_grouped_gradients_with_several_units_per_cta(fa, oracle_mod, causal):
 
 
 @pytest.mark.parametrize("shape,dtype,hkv", [((2, 4, 1000, 128), "bf16", None), ((2, 6, 1000, 64), "f16", 2)])
-def test_gradients_are_bit_identical_run_to_run(fa, shape, dtype, hkv):
-    # d = 64 runs the dK/dV pipeline whose score products overlap the elementwise work
+@pytest.mark.parametrize("flags", [0, 1])
+def test_gradients_are_bit_identical_run_to_run(fa, shape, dtype, hkv, flags):
+    # d = 64 runs the dK/dV pipeline whose score products overlap the elementwise work;
+    # flags 1 is the dQ pass that recomputes S and dP
     import torch
-    a = run(fa, shape, dtype, True, 3300, grad=dtype, hkv=hkv)[3]
-    b = run(fa, shape, dtype, True, 3300, grad=dtype, hkv=hkv)[3]
+    a = run(fa, shape, dtype, True, 3300, grad=dtype, hkv=hkv, flags=flags)[3]
+    b = run(fa, shape, dtype, True, 3300, grad=dtype, hkv=hkv, flags=flags)[3]
     for x, y in zip(a, b):
         assert torch.equal(x.view(torch.int16), y.view(torch.int16))
 

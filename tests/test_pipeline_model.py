@@ -466,7 +466,65 @@ def dkdv_kernel_64(sim, units, plant=None):
         sim.role(f"warp{wq + 4 * hf}", elementwise(wq, hf))
 
 
-KERNELS = {"dq": dq_kernel, "dkdv128": dkdv_kernel_128, "dkdv64": dkdv_kernel_64}
+def dq_gemm_kernel(sim, units, plant=None):
+    """bwd_dq_gemm_kernel: dQ of one query tile (a unit) is the sum over its n_iter
+    key tiles of dS K.  One ring of 3 stages carries the dS block and K tile of
+    each product and runs on across units; the units alternate between two TMEM
+    accumulators, so the epilogue (4 warps) reads one while the next unit's
+    products fill the other.  The MMA thread takes an accumulator back only once
+    the epilogue of the unit two before has read it."""
+    if isinstance(units, int):
+        units = [units]
+    S = 3
+    for s in range(S):
+        sim.bar(f"full{s}"), sim.bar(f"empty{s}")
+    for b in range(2):
+        sim.bar(f"acc_full{b}"), sim.bar(f"acc_free{b}", 4)
+
+    def producer():
+        g = 0
+        for k, n_iter in enumerate(units):
+            for n in range(n_iter):
+                st = g % S
+                if g >= S and plant != "no_empty_wait":
+                    yield ("wait", f"empty{st}", g // S - 1)
+                yield ("load", [(f"DS{st}", ("dS", k, n)), (f"K{st}", ("K", k, n))], f"full{st}")
+                g += 1
+
+    def acc(k):
+        return 0 if plant == "one_accumulator" else k & 1
+
+    def mma():
+        g = 0
+        for k, n_iter in enumerate(units):
+            b = acc(k)
+            if k >= 2 and plant != "no_acc_free":
+                yield ("wait", f"acc_free{b}", (k - 2) >> 1)
+            for n in range(n_iter):
+                st = g % S
+                yield ("wait", f"full{st}", g // S)
+                reads = [(f"DS{st}", ("dS", k, n)), (f"K{st}", ("K", k, n))]
+                if n > 0:
+                    reads.append((f"ACC{b}", ("dQ", k, n - 1)))
+                yield ("mma", reads, [(f"ACC{b}", ("dQ", k, n))])
+                yield ("commit", f"empty{st}")
+                g += 1
+            yield ("commit", f"acc_full{b}")
+
+    def epilogue(w):
+        for k, n_iter in enumerate(units):
+            b = k & 1
+            yield ("wait", f"acc_full{b}", k >> 1)
+            yield ("read", f"ACC{acc(k)}", ("dQ", k, n_iter - 1))
+            yield ("arrive", f"acc_free{b}")
+
+    sim.role("tma", producer())
+    sim.role("mma", mma())
+    for w in range(4):
+        sim.role(f"warp{w}", epilogue(w))
+
+
+KERNELS = {"dq": dq_kernel, "dkdv128": dkdv_kernel_128, "dkdv64": dkdv_kernel_64, "dq_gemm": dq_gemm_kernel}
 
 
 @pytest.mark.parametrize("kernel", sorted(KERNELS))
@@ -490,7 +548,8 @@ def test_persistent_protocol_holds_under_random_interleavings(kernel, units):
 
 @pytest.mark.parametrize("kernel,plant", [("dq", "no_fix_empty"), ("dq", "late_epilogue"),
                                           ("dkdv128", "no_fix_empty"), ("dkdv64", "no_fix_empty"),
-                                          ("dkdv64", "late_epilogue")])
+                                          ("dkdv64", "late_epilogue"), ("dq_gemm", "no_acc_free"),
+                                          ("dq_gemm", "one_accumulator")])
 def test_the_model_catches_a_planted_unit_boundary_mistake(kernel, plant):
     caught = 0
     for seed in range(150):
@@ -505,7 +564,7 @@ def test_the_model_catches_a_planted_unit_boundary_mistake(kernel, plant):
 
 @pytest.mark.parametrize("kernel,plant", [("dq", "no_dq_done"), ("dq", "scores_before_loaded"),
                                           ("dkdv128", "no_intra_sync"), ("dkdv128", "s_before_dv"),
-                                          ("dkdv64", "no_pd_done")])
+                                          ("dkdv64", "no_pd_done"), ("dq_gemm", "no_empty_wait")])
 def test_the_model_catches_a_planted_mistake(kernel, plant):
     caught = 0
     for seed in range(150):
