@@ -98,7 +98,7 @@ struct BwdParams {
     const float *dsum;  // [B Hq][npad] minus D_i = dO_i . O_i
     void *g0;           // dkdv: dK [B Hkv][N][d]; dq: dQ [B Hq][N][d]
     void *g1;           // dkdv: dV [B Hkv][N][d]
-    int Hq, Hkv, group; // query head h reads key/value head h / group
+    int group;          // flat over (batch, head): query head x reads key/value head x / group
     int N;
     int n_t;            // 128-row tiles per head
     int npad;           // n_t * 128: row stride of lse2 and dsum per head (zero past N)
@@ -329,7 +329,7 @@ __device__ __forceinline__ bool dkdv_unit(const BwdParams &p, int k, DkdvUnit &u
     u.i_first = p.causal ? u.jt : 0;  // query tiles that see key tile jt
     u.n_qt = p.n_t - u.i_first;
     u.n_iter = p.group * u.n_qt;      // every query head of the group, every tile
-    u.bhq0 = (u.bhk / p.Hkv) * p.Hq + (u.bhk % p.Hkv) * p.group;  // first query head
+    u.bhq0 = u.bhk * p.group;         // first query head
     return true;
 }
 
@@ -791,7 +791,7 @@ __device__ __forceinline__ bool dq_unit(const BwdParams &p, int k, DqUnit &u) {
         u.bh = static_cast<int>(idx / p.n_t);
         u.it = static_cast<int>(idx % p.n_t);
     }
-    u.bhk = (u.bh / p.Hq) * p.Hkv + (u.bh % p.Hq) / p.group;  // its key/value head
+    u.bhk = u.bh / p.group;                                    // its key/value head
     u.n_iter = p.causal ? u.it + 1 : p.n_t;                    // key tiles the queries see
     return true;
 }
@@ -1301,8 +1301,8 @@ cudaError_t launch_pdl(K kernel, int grid, int threads, size_t smem, cudaStream_
     return e == cudaSuccess ? cudaGetLastError() : e;
 }
 
-// The dQ pass reads dS from a workspace when it is at most this large; larger
-// problems (or a caller's flag) take the pass that recomputes S and dP.
+// The dS table takes at most this much memory; larger problems run in chunks of
+// key/value heads that fit.
 constexpr size_t kDsWorkspaceMax = 4ull << 30;
 
 template <int D, bool BF16>
@@ -1314,12 +1314,7 @@ int launch_bwd_d(const BackwardLaunch &a, cudaStream_t stream) {
     const long long BHk = static_cast<long long>(a.B) * a.Hkv;   // key/value heads
     const int n_t = (a.N + kRows - 1) / kRows;
     const long long rows_pad = BH * n_t * kRows;  // lse2 and dsum, padded to whole tiles
-    CUtensorMap mq, mk, mv, mdo;
-    int rc;
-    if ((rc = make_map(&mq, a.q, D, false, a.N, BH, a.in_bf16)) != FA_OK) return rc;
-    if ((rc = make_map(&mk, a.k, D, false, a.N, BHk, a.in_bf16)) != FA_OK) return rc;
-    if ((rc = make_map(&mv, a.v, D, false, a.N, BHk, a.in_bf16)) != FA_OK) return rc;
-    if ((rc = make_map(&mdo, a.dout, D, false, a.N, BH, a.in_bf16)) != FA_OK) return rc;
+    const int group = a.H / a.Hkv;
     cudaError_t e;
     if ((e = cudaFuncSetAttribute(bwd_dkdv_kernel<D, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   L::kSmemBytes)) != cudaSuccess ||
@@ -1334,12 +1329,22 @@ int launch_bwd_d(const BackwardLaunch &a, cudaStream_t stream) {
         return FA_ERR_WORKSPACE;
     }
     float *lse2 = static_cast<float *>(ws), *dsum = lse2 + rows_pad;
-    // dS^T blocks for the dQ product pass, when they fit the limit and the pool
+    // The dS table for the dQ product pass.  It holds the blocks of `chunk` key/value
+    // heads (their chunk x group query heads); a problem whose table would pass the
+    // limit runs both passes chunk by chunk over the same table.  Without a table
+    // (a flag, no key/value head fits, or no memory) the dQ pass recomputes S and dP.
+    long long chunk = BHk;
     void *ds = nullptr;
-    const size_t ds_bytes = static_cast<size_t>(BH) * n_t * n_t * kRows * kRows * 2;
-    if (!a.recompute_dq && ds_bytes <= kDsWorkspaceMax && scratch_alloc(&ds, ds_bytes, stream) != cudaSuccess) {
-        cudaGetLastError();  // an allocation failure only selects the recomputing pass
-        ds = nullptr;
+    const size_t head_bytes = static_cast<size_t>(n_t) * n_t * kDsBlockBytes * group;  // per key/value head
+    if (!a.recompute_dq && head_bytes <= kDsWorkspaceMax) {
+        const long long fit = static_cast<long long>(kDsWorkspaceMax / head_bytes);
+        const long long n_chunks = (BHk + fit - 1) / fit;
+        chunk = (BHk + n_chunks - 1) / n_chunks;  // even chunks
+        if (scratch_alloc(&ds, static_cast<size_t>(chunk) * head_bytes, stream) != cudaSuccess) {
+            cudaGetLastError();  // an allocation failure only selects the recomputing pass
+            ds = nullptr;
+            chunk = BHk;
+        }
     }
     constexpr long long kPrepRowsPerBlock = (kPrepThreads / 32) * (32 / (D / 8)) * kPrepRows;
     bwd_prep_kernel<D, BF16><<<static_cast<unsigned>((rows_pad + kPrepRowsPerBlock - 1) / kPrepRowsPerBlock),
@@ -1347,12 +1352,10 @@ int launch_bwd_d(const BackwardLaunch &a, cudaStream_t stream) {
         static_cast<const uint16_t *>(a.out), static_cast<const uint16_t *>(a.dout), a.lse, lse2, dsum, rows_pad,
         a.N, n_t * kRows);
     e = cudaGetLastError();
+    // The kernels see the (batch, head) pairs as one flat list: query head x of a chunk
+    // reads key/value head x / group.
     BwdParams p;
-    p.lse2 = lse2;
-    p.dsum = dsum;
-    p.Hq = a.H;
-    p.Hkv = a.Hkv;
-    p.group = a.H / a.Hkv;
+    p.group = group;
     p.N = a.N;
     p.n_t = n_t;
     p.npad = n_t * kRows;
@@ -1361,20 +1364,38 @@ int launch_bwd_d(const BackwardLaunch &a, cudaStream_t stream) {
     p.scale = a.scale;
     p.c = a.scale * 1.4426950408889634f;
     p.ds_t = static_cast<uint16_t *>(ds);
-    if (e == cudaSuccess) {
+    const size_t in_head = static_cast<size_t>(a.N) * D * 2;                              // bytes of a 16-bit head
+    const size_t g_head = static_cast<size_t>(a.N) * D * (a.grad_dtype == FA_F32 ? 4 : 2);  // of a gradient head
+    for (long long c0 = 0; c0 < BHk && e == cudaSuccess; c0 += chunk) {
+        const long long ck = chunk < BHk - c0 ? chunk : BHk - c0;  // key/value heads of this chunk
+        const long long h0 = c0 * group;                             // its first query head
+        CUtensorMap mq, mk, mv, mdo;
+        int rc;
+        if ((rc = make_map(&mq, static_cast<const char *>(a.q) + h0 * in_head, D, false, a.N, ck * group,
+                           a.in_bf16)) != FA_OK ||
+            (rc = make_map(&mk, static_cast<const char *>(a.k) + c0 * in_head, D, false, a.N, ck, a.in_bf16)) !=
+                FA_OK ||
+            (rc = make_map(&mv, static_cast<const char *>(a.v) + c0 * in_head, D, false, a.N, ck, a.in_bf16)) !=
+                FA_OK ||
+            (rc = make_map(&mdo, static_cast<const char *>(a.dout) + h0 * in_head, D, false, a.N, ck * group,
+                           a.in_bf16)) != FA_OK) {
+            scratch_free(ws, stream);
+            if (ds) scratch_free(ds, stream);
+            return rc;
+        }
+        p.lse2 = lse2 + h0 * p.npad;
+        p.dsum = dsum + h0 * p.npad;
         // one persistent CTA per SM (or per unit, when there are fewer units)
-        p.g0 = a.dk;
-        p.g1 = a.dv;
-        p.n_units = static_cast<int>(BHk * p.n_t);
-        const int grid = p.n_units < a.num_sms ? p.n_units : a.num_sms;
+        p.g0 = static_cast<char *>(a.dk) + c0 * g_head;
+        p.g1 = static_cast<char *>(a.dv) + c0 * g_head;
+        p.n_units = static_cast<int>(ck * p.n_t);
+        int grid = p.n_units < a.num_sms ? p.n_units : a.num_sms;
         e = launch_pdl(bwd_dkdv_kernel<D, BF16>, grid, kBwdThreads, L::kSmemBytes, stream, mq, mk, mv, mdo, p);
-    }
-    if (e == cudaSuccess) {
-        // one persistent CTA per SM (or per unit, when there are fewer units)
-        p.g0 = a.dq;
+        if (e != cudaSuccess) break;
+        p.g0 = static_cast<char *>(a.dq) + h0 * g_head;
         p.g1 = nullptr;
-        p.n_units = static_cast<int>(BH * p.n_t);
-        const int grid = p.n_units < a.num_sms ? p.n_units : a.num_sms;
+        p.n_units = static_cast<int>(ck * group * p.n_t);
+        grid = p.n_units < a.num_sms ? p.n_units : a.num_sms;
         if (ds) {
             e = launch_pdl(bwd_dq_gemm_kernel<D, BF16>, grid, kDqgThreads, DqgLayout<D>::kSmemBytes, stream, mk, p);
         } else {

@@ -189,11 +189,13 @@ int fa_prefill_lse(const void *q, const void *k, const void *v, void *out,
  *                        may overlap another argument
  *   causal, scale      : as in the forward call
  * Scratch of 8 bytes per query row, with each head's rows rounded up to a
- * multiple of 128, comes from the library's pool.  So does, when it is at most
- * 4 GiB (H x ceil(N / 128)^2 x 32 KB per sequence), a table of the score
- * gradients dS that the dK/dV pass writes in 16-bit and the dQ pass multiplies
- * by K; larger problems, or a failed allocation of that table, take a dQ pass
- * that recomputes S and dP instead (as FA_BWD_RECOMPUTE_DQ).  Errors as for
+ * multiple of 128, comes from the library's pool.  So does a table of the
+ * score gradients dS that the dK/dV pass writes in 16-bit and the dQ pass
+ * multiplies by K: ceil(N / 128)^2 x 32 KB per query head, at most 4 GiB.  A
+ * larger problem runs both passes in chunks of key/value heads over a table of
+ * that size; when one key/value head's blocks alone pass 4 GiB, or the table
+ * cannot be allocated, the dQ pass recomputes S and dP instead (as
+ * FA_BWD_RECOMPUTE_DQ).  Errors as for
  * prefill: FA_ERR_NULL, FA_ERR_SHAPE, FA_ERR_HEAD_DIM, FA_ERR_DTYPE,
  * FA_ERR_ALIGN, FA_ERR_SCALE, FA_ERR_ALIAS, FA_ERR_WORKSPACE, FA_ERR_ARCH,
  * FA_ERR_CUDA.

@@ -88,6 +88,32 @@ def test_ds_table_and_recompute_paths_agree(fa, shape, dtype, hkv, causal):
     assert e <= REL_TOL[dtype] / 4, f"dq {shape} causal={causal}: {e:.3e}"
 
 
+@pytest.mark.parametrize("shape,dtype,hkv", [((1, 16, 16384, 128), "bf16", None), ((2, 20, 8192, 64), "f16", 5)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_a_table_over_the_limit_runs_in_chunks(fa, shape, dtype, hkv, causal):
+    # A dS table over 4 GiB (8 GiB, and 5 GiB over 10 key/value heads) is taken in
+    # two chunks of key/value heads on a table half that size; the second shape's
+    # chunk boundary falls between the two sequences.  dK and dV come from the same
+    # pass as with the recomputing dQ pass (bit-identical); dQ agrees within a
+    # fraction of the oracle bound (that pass is checked against the oracle above).
+    import torch
+    rc, _ = fa.fa_pool_stats(reset_high=True)
+    assert rc == fa.FA_OK
+    a = run(fa, shape, dtype, causal, 3900, hkv=hkv)[3]
+    rc, stats = fa.fa_pool_stats()
+    assert rc == fa.FA_OK
+    B, H, N, d = shape
+    n_t = (N + 127) // 128
+    table = B * H * n_t * n_t * 32768
+    assert table > 4 << 30
+    assert table // 2 <= stats[3] < table // 2 + (64 << 20), stats  # in-use high-water mark
+    b = run(fa, shape, dtype, causal, 3900, hkv=hkv, flags=fa.FA_BWD_RECOMPUTE_DQ)[3]
+    for name, x, y in zip(("dk", "dv"), a[1:], b[1:]):
+        assert torch.equal(x, y), name
+    e = rel_err(G.device_to_f64(a[0]), G.device_to_f64(b[0]))
+    assert e <= REL_TOL[dtype] / 4, f"dq {shape} causal={causal}: {e:.3e}"
+
+
 @pytest.mark.parametrize("N", [4096, 8192])
 @pytest.mark.parametrize("causal", [False, True])
 def test_gradients_at_bench_size_on_sampled_heads(fa, oracle_mod, N, causal):
