@@ -614,7 +614,9 @@ int choose_splits(int B, long long rows, int max_len, int num_sms, int per_sm) {
 int fa_decode_splits_for_sms(int B, int Hq, int Hkv, int max_len, int num_sms) {
     if (B < 1 || Hq < 1 || Hkv < 1 || max_len < 1 || Hq % Hkv != 0 || num_sms < 1)
         return -FA_ERR_SHAPE;
-    if (Hq == Hkv) return choose_splits(B, Hq, max_len, num_sms, 2);
+    // Plain decode: about three CTAs per SM (the pages' rule has two; three measured
+    // 11 us against 13 at B = 1 and the same at B = 8 and 32).
+    if (Hq == Hkv) return choose_splits(B, Hq, max_len, num_sms, 3);
     // A grouped CTA does up to 8 heads' arithmetic per row it loads, so it is
     // latency- rather than bandwidth-bound: aim for about 5 CTAs per SM
     // (measured best at B = 8 and 32 with 14 query over 2 cache heads).

@@ -319,8 +319,9 @@ int fa_decode_ex(const void *q, const void *k_cache, const void *v_cache,
 
 /*
  * The automatic split count ("Kernel design" table: choose_decode_split
- * targets about two resident blocks per SM): enough (b, h, chunk) CTAs for
- * two per SM, and chunks of at most 512 rows so that ragged lengths do not
+ * targets about two resident blocks per SM; here three, measured faster on
+ * GB300): enough (b, h, chunk) CTAs for three per SM, and chunks of at most
+ * 512 rows so that ragged lengths do not
  * leave a few long CTAs running alone.  Host arithmetic on the arguments and
  * the SM count of `device` (a CUDA device ordinal; < 0 = the current device).
  * Returns the split count (>= 1), or a negative fa_status: -FA_ERR_SHAPE on

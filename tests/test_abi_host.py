@@ -281,9 +281,9 @@ def test_split_choice_host_logic(lib, B, H, L, sms):
     assert chunk % 64 == 0
     assert chunk * s >= L and (s - 1) * chunk < L          # every row in exactly one chunk
     assert chunk <= 512                                     # no CTA longer than 512 rows
-    # target: about two CTAs per SM over the whole (b, h, chunk) grid, at
+    # target: about three CTAs per SM over the whole (b, h, chunk) grid, at
     # least one chunk per 512 rows, at most one per 64 rows
-    target = min(max(-(-2 * sms // (B * H)), -(-L // 512), 1), -(-L // 64))
+    target = min(max(-(-3 * sms // (B * H)), -(-L // 512), 1), -(-L // 64))
     assert s <= target
     assert chunk == 64 or -(-L // (chunk - 64)) > target    # chunk is the smallest that fits
     ws = binding.fa_decode_workspace_bytes(B, H, L, 64, s)
