@@ -118,7 +118,7 @@ using namespace fa;
 
 extern "C" {
 
-int fa_version(void) { return 2 * 10000 + 0 * 100 + 0; }
+int fa_version(void) { return 2 * 10000 + 1 * 100 + 0; }
 
 const char *fa_status_string(int status) {
     switch (status) {

@@ -176,8 +176,9 @@ int fa_prefill_lse(const void *q, const void *k, const void *v, void *out,
  * key/value heads: given the inputs, the forward output `out`, its gradient
  * `dout` and the forward's `lse`, writes
  *   dq = dL/dq, dk = dL/dk, dv = dL/dv
- * of L = sum(dout * out), with the weights recomputed tile by tile (the N x N
- * tables never reach memory).  The gradient of a shared key/value head is the
+ * of L = sum(dout * out), with the weights recomputed tile by tile from lse
+ * (the N x N weights never reach memory; the score gradients dS do, as the
+ * 16-bit table described below).  The gradient of a shared key/value head is the
  * sum over the query heads that read it.  No atomics: the result is
  * bit-identical run to run.
  *   q, out, dout       : 16-bit [B][H][N][d] in in_dtype (out as written by

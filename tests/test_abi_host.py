@@ -102,7 +102,7 @@ def test_status_strings_and_version(lib):
     for code in range(14):
         assert binding.status_string(code) != "unknown status"
     assert binding.status_string(999) == "unknown status"
-    assert binding.fa_version() >= 20000
+    assert binding.fa_version() >= 20100  # 2.1: fa_prefill_backward_ex
 
 
 A = 1 << 20   # an aligned fake address: validation must reject before using it
