@@ -2,7 +2,7 @@
 // step that the flash-attention-cuda README lists under "Future work"), for
 // sm_103a.  Given Q, K, V, the forward output O, its gradient dO and the row
 // log-sum-exp L saved by the forward, it recomputes the weights tile by tile
-// and never stores the N x N tables:
+// and never stores them:
 //   P_ij  = exp(s_ij - L_i),  s_ij = scale q_i.k_j     (2^(c s - L2) with c = scale log2 e)
 //   D_i   = dO_i . O_i
 //   dV_j  = sum_i P_ij dO_i
@@ -10,23 +10,28 @@
 //   dK_j  = scale sum_i dS_ij q_i,    dQ_i = scale sum_j dS_ij k_j
 // (the chain rule through softmax: sum_j P_ij dP_ij = dO_i . O_i).
 //
-// Three kernels, no atomics, so every gradient is bit-identical run to run:
-//   bwd_prep   -D_i and -L2_i = -L_i log2 e for every row (fp32), per head padded
-//              to whole 128-row tiles;
-//   bwd_dkdv   per unit, a 128-key tile of a key/value head: S^T = K Q_i^T and
-//              dP^T = V dO_i^T in TMEM, then P^T and dS^T as 16-bit (over them
-//              at d = 128, in columns of their own at d = 64), then
-//              dV += P^T dO_i and dK += dS^T Q_i accumulate in TMEM over the
-//              query tiles that see the keys, of every query head that reads
-//              this key/value head;
-//   bwd_dq     per unit, a 128-query tile: S = Q K_j^T, dP = dO V_j^T, dS in
-//              columns of its own, dQ += dS K_j over the key tiles the queries see.
-// Both main kernels are persistent (one CTA per SM, units dealt in snake order)
-// and issue the next tile's score products while the elementwise warps still
-// work on the current one, as far as TMEM and the rings allow.
-// Warp roles per CTA (320 threads): warps 0-7 elementwise work, thread = TMEM
-// lane = tile row, two warps per row quadrant taking half of the tile's columns
-// each; warp 8 TMA producer; warp 9 tcgen05 issuer and TMEM owner.
+// Kernels, no atomics, so every gradient is bit-identical run to run:
+//   bwd_prep     -D_i and -L2_i = -L_i log2 e for every row (fp32), per head padded
+//                to whole 128-row tiles;
+//   bwd_dkdv     per unit, a 128-key tile of a key/value head: S^T = K Q_i^T and
+//                dP^T = V dO_i^T in TMEM, then P^T and dS^T as 16-bit (over them
+//                at d = 128, in columns of their own at d = 64), then
+//                dV += P^T dO_i and dK += dS^T Q_i accumulate in TMEM over the
+//                query tiles that see the keys, of every query head that reads
+//                this key/value head.  It also writes each dS block to a table in
+//                HBM (the tensor core's layout for the dQ product);
+//   bwd_dq_gemm  per unit, a 128-query tile: dQ = scale sum_j dS_ij K_j from the
+//                table, one product per key tile;
+//   bwd_dq       (without a table) per unit, a 128-query tile: S = Q K_j^T,
+//                dP = dO V_j^T, dS in columns of its own, dQ += dS K_j over the
+//                key tiles the queries see.
+// The main kernels are persistent (one CTA per SM, units dealt in snake order);
+// bwd_dkdv and bwd_dq issue the next tile's score products while the elementwise
+// warps still work on the current one, as far as TMEM and the rings allow.
+// Warp roles of bwd_dkdv and bwd_dq (320 threads): warps 0-7 elementwise work,
+// thread = TMEM lane = tile row, two warps per row quadrant taking half of the
+// tile's columns each; warp 8 TMA producer; warp 9 tcgen05 issuer and TMEM
+// owner.  bwd_dq_gemm: warps 0-3 epilogue, 4 copies, 5 tcgen05 issuer.
 #include <cfloat>
 
 #include "fa_internal.h"
