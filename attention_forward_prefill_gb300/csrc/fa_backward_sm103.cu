@@ -182,7 +182,7 @@ __device__ __forceinline__ void store_ds_quarter(uint16_t *row, int q, const uin
 // dO in flight; each lane sums its eight products in order, then the row's lanes
 // combine by a fixed butterfly, so D is the same on every run.
 constexpr int kPrepThreads = 256;
-constexpr int kPrepRows = 4;
+constexpr int kPrepRows = 2;
 
 template <int D, bool BF16>
 __device__ __forceinline__ float dot8(const uint4 &a, const uint4 &b) {
