@@ -108,7 +108,7 @@ struct Params {
     // into gridDim.x equal contiguous ranges; a unit cut between two CTAs is
     // finished by the fixup kernel from the partials in ws_o / ws_ml.
     int stream_k;
-    // Causal unit schedule in one round (the kernel's PAIRED instantiation): unit i
+    // Causal unit schedule in one round (the paired instantiation): unit i
     // of a head pairs query tile i with tile T - 1 - i (T = 128-row tiles per
     // sequence), so that no unit holds more than T - i key tiles and its two
     // tiles overlap for the first i + 1.
@@ -122,7 +122,18 @@ struct Params {
     long long sk_s0;
     float *ws_o;           // [gridDim.x][2 slots][256 rows][D]  unnormalised O
     float *ws_ml;          // [gridDim.x][2 slots][256 rows][2]  (m_ref, l)
+    // The ordered schedule (packed batches over more than one round of units):
+    // the (sequence, query block) classes, most key-tile products first (written
+    // by packed_order_kernel just before); unit u is head u % Hq of class
+    // order[u / Hq].
+    const int *order;
 };
+
+// Unit schedules, each its own kernel instantiation so that one's code does not
+// touch the others': plain (round robin, causal heaviest query blocks first),
+// paired (causal tiles i and T - 1 - i in one unit) and ordered (packed batches,
+// heaviest (sequence, block) classes first).
+constexpr int kSchedPlain = 0, kSchedPaired = 1, kSchedOrdered = 2;
 
 // Stream-K: key-tile steps of a head before query block qb.  A kernel argument
 // of its own, so that only this table is indexed at run time and every field
@@ -197,7 +208,7 @@ __device__ __forceinline__ void check_seq(const Params &p, const Work &w) {
     if (bad) atomicCAS(&g_prefill_status, 0, static_cast<int>(FA_ERR_SEQ_LEN));
 }
 
-template <bool PAIRED>
+template <int SCHED>
 __device__ __forceinline__ bool seg_next(const Params &p, const StepTable &tab, SegCursor &c,
                                          Work &w) {
     int bh, qb;
@@ -232,9 +243,13 @@ __device__ __forceinline__ bool seg_next(const Params &p, const StepTable &tab, 
                               : static_cast<int>(blockIdx.x);
         w.u = k * static_cast<int>(gridDim.x) + r;
         if (w.u >= p.n_units) return false;
-        if constexpr (PAIRED) {  // pair i (tiles i and T - 1 - i); pair 0 holds the most keys
+        if constexpr (SCHED == kSchedPaired) {  // pair i (tiles i and T - 1 - i); pair 0 holds the most keys
             qb = w.u / p.BH;
             bh = w.u % p.BH;
+        } else if constexpr (SCHED == kSchedOrdered) {  // heaviest (sequence, block) classes first
+            const int cls = __ldg(p.order + w.u / p.Hq);
+            qb = cls % p.n_qb;
+            bh = (cls / p.n_qb) * p.Hq + w.u % p.Hq;
         } else if (p.causal) {  // heaviest query blocks first
             qb = p.n_qb - 1 - w.u / p.BH;
             bh = w.u % p.BH;
@@ -248,7 +263,7 @@ __device__ __forceinline__ bool seg_next(const Params &p, const StepTable &tab, 
     w.b = bh / p.Hq;
     w.h = bh % p.Hq;
     load_seq(p, w);
-    if constexpr (PAIRED) {  // (dense: every sequence has T tiles)
+    if constexpr (SCHED == kSchedPaired) {  // (dense: every sequence has T tiles)
         const int partner = p.n_tt - 1 - qb;
         w.r0 = qb * kBlockM;
         w.r1 = partner > qb ? partner * kBlockM : w.nq;  // an odd T leaves a middle tile alone
@@ -263,9 +278,8 @@ __device__ __forceinline__ bool seg_next(const Params &p, const StepTable &tab, 
 }
 
 // LSE: also write the row log-sum-exp (a separate instantiation, so that the
-// plain forward keeps its registers).  PAIRED: the paired-tile causal schedule (its
-// own instantiation, so that the other schedules' code is untouched by it).
-template <int D, bool BF16, bool LSE, bool PAIRED>
+// plain forward keeps its registers).  SCHED: the unit schedule (kSched*).
+template <int D, bool BF16, bool LSE, int SCHED>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap map_q,
                    const __grid_constant__ CUtensorMap map_k,
@@ -362,7 +376,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     w.b * p.Hkv + w.hk, pol_kv);
                 }
             };
-            while (ok && seg_next<PAIRED>(p, tab, cur, w)) {
+            while (ok && seg_next<SCHED>(p, tab, cur, w)) {
                 if (packed) check_seq(p, w);
                 if (w.j1 <= w.j0) continue;  // no key tiles: the softmax warps write zeros
                 // query tile t is loaded when it has key tiles in [j0, j1)
@@ -447,7 +461,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (fence) tc_fence_after();
                 return static_cast<int>(st);
             };
-            while (ok && seg_next<PAIRED>(p, tab, cur, w)) {
+            while (ok && seg_next<SCHED>(p, tab, cur, w)) {
                 const int j0 = w.j0, j1 = w.j1;
                 if (j1 <= j0) continue;  // no key tiles: nothing to multiply
                 // key tiles [j0, e_t) for query tile t (empty when e_t <= j0)
@@ -592,7 +606,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         SegCursor cur;
         seg_begin(p, cur);
         Work w;
-        for (int seg = 0; ok && seg_next<PAIRED>(p, tab, cur, w); ++seg) {
+        for (int seg = 0; ok && seg_next<SCHED>(p, tab, cur, w); ++seg) {
             const int j0 = w.j0, j1 = w.j1;
             const int tile_row0 = t ? w.r1 : w.r0;
             const int row = tile_row0 + r;  // query index within the sequence
@@ -1089,6 +1103,57 @@ void make_plan(bool packed, int B, int Hq, int Nq, int Nk, int causal, int no_sk
     }
 }
 
+// The (sequence, 256-row query block) classes of a packed batch, most 128 x 128
+// tile products first (ties by class index), for the unit schedule: its rounds
+// then deal heavy units before light ones across sequences of any length, where
+// the plain order ranks blocks by their index alone.  One CTA sorts the at most
+// kOrderMax classes in shared memory (bitonic, on 64-bit keys: inverted product
+// count above, class index below, so the order is total and the same on every
+// run).  The lengths are clamped as the prefill kernel clamps them.
+constexpr int kOrderMax = 4096;
+constexpr int kOrderThreads = 1024;
+
+__global__ void __launch_bounds__(kOrderThreads)
+    packed_order_kernel(const int *cu_q, const int *cu_k, int B, int n_qb, int Nq, int Nk, int total_q,
+                        int total_k, int causal, int no_skip, int *order) {
+    __shared__ unsigned long long key[kOrderMax];
+    const int n = B * n_qb;
+    int m = 1;
+    while (m < n) m <<= 1;
+    for (int i = threadIdx.x; i < m; i += kOrderThreads) {
+        unsigned long long k = ~0ull;  // padding sorts last
+        if (i < n) {
+            const int b = i / n_qb, qb = i % n_qb;
+            const int q_lo = min(max(cu_q[b], 0), total_q), q_hi = min(max(cu_q[b + 1], q_lo), total_q);
+            const int k_lo = min(max(cu_k[b], 0), total_k), k_hi = min(max(cu_k[b + 1], k_lo), total_k);
+            const int nq = min(q_hi - q_lo, Nq), nk = min(k_hi - k_lo, Nk);
+            const int r0 = qb * kRowsPerUnit;
+            const int c = kv_tiles(causal, no_skip, nq, nk, nk - nq, r0) +
+                          kv_tiles(causal, no_skip, nq, nk, nk - nq, r0 + kBlockM);
+            k = (static_cast<unsigned long long>(0x7fffffff - c) << 32) | static_cast<unsigned>(i);
+        }
+        key[i] = k;
+    }
+    __syncthreads();
+    for (int size = 2; size <= m; size <<= 1) {
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            for (int i = threadIdx.x; i < m; i += kOrderThreads) {
+                const int j = i ^ stride;
+                if (j > i) {
+                    const bool up = (i & size) == 0;
+                    const unsigned long long a = key[i], c = key[j];
+                    if ((a > c) == up) {
+                        key[i] = c;
+                        key[j] = a;
+                    }
+                }
+            }
+            __syncthreads();
+        }
+    }
+    for (int i = threadIdx.x; i < n; i += kOrderThreads) order[i] = static_cast<int>(key[i] & 0xffffffffu);
+}
+
 template <int D, bool BF16, bool LSE>
 int launch_d_lse(const PrefillLaunch &a, const DeviceInfo &dev, cudaStream_t stream) {
     using L = Layout<D>;
@@ -1110,6 +1175,7 @@ int launch_d_lse(const PrefillLaunch &a, const DeviceInfo &dev, cudaStream_t str
     p.lse = a.lse;
     p.cu_q = a.cu_q;
     p.cu_k = a.cu_k;
+    p.order = nullptr;
     p.B = a.B;
     p.Hq = a.Hq;
     p.Hkv = a.Hkv;
@@ -1142,7 +1208,12 @@ int launch_d_lse(const PrefillLaunch &a, const DeviceInfo &dev, cudaStream_t str
     make_plan(packed, a.B, a.Hq, a.Nq, a.Nk, p.causal, p.no_skip, a.schedule, dev.num_sms, pl);
     p.stream_k = pl.stream_k;
     p.n_tt = (a.Nq + kBlockM - 1) / kBlockM;
-    const auto kernel = pl.paired ? prefill_kernel<D, BF16, LSE, true> : prefill_kernel<D, BF16, LSE, false>;
+    // the ordered schedule for a packed batch over more than one round of units
+    const long long n_cls = static_cast<long long>(a.B) * p.n_qb;
+    const bool ordered = packed && !pl.stream_k && p.n_units > pl.grid && n_cls <= kOrderMax;
+    const auto kernel = pl.paired ? prefill_kernel<D, BF16, LSE, kSchedPaired>
+                                  : (ordered ? prefill_kernel<D, BF16, LSE, kSchedOrdered>
+                                             : prefill_kernel<D, BF16, LSE, kSchedPlain>);
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
     if (e != cudaSuccess) return cuda_fail(e);
     // The setmaxnreg split inside the kernel draws on the launch allocation:
@@ -1191,6 +1262,27 @@ int launch_d_lse(const PrefillLaunch &a, const DeviceInfo &dev, cudaStream_t str
             f.ws_ml = p.ws_ml;
         }
     }
+    // A packed batch over more than one round of units takes its classes heaviest
+    // first (the order comes from the device-resident offsets, so a small kernel
+    // computes it on the stream just before).
+    void *ord = nullptr;
+    if (ordered) {
+        if ((e = scratch_alloc(&ord, static_cast<size_t>(n_cls) * sizeof(int), stream)) != cudaSuccess) {
+            cuda_fail(e);
+            if (ws) scratch_free(ws, stream);
+            return FA_ERR_WORKSPACE;
+        }
+        packed_order_kernel<<<1, kOrderThreads, 0, stream>>>(a.cu_q, a.cu_k, a.B, p.n_qb, a.Nq, a.Nk, a.total_q,
+                                                             a.total_k, p.causal, p.no_skip,
+                                                             static_cast<int *>(ord));
+        e = cudaGetLastError();
+        if (e != cudaSuccess) {
+            scratch_free(ord, stream);
+            if (ws) scratch_free(ws, stream);
+            return cuda_fail(e);
+        }
+        p.order = static_cast<const int *>(ord);
+    }
     const StepTable &tab = pl.tab;
     kernel<<<grid, kThreads, L::kSmemBytes, stream>>>(mq, mk, mv, p, tab);
     e = cudaGetLastError();
@@ -1209,6 +1301,10 @@ int launch_d_lse(const PrefillLaunch &a, const DeviceInfo &dev, cudaStream_t str
     }
     if (ws) {
         const cudaError_t e2 = scratch_free(ws, stream);
+        if (e == cudaSuccess) e = e2;
+    }
+    if (ord) {
+        const cudaError_t e2 = scratch_free(ord, stream);
         if (e == cudaSuccess) e = e2;
     }
     if (e != cudaSuccess) return cuda_fail(e);

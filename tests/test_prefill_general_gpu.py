@@ -154,6 +154,37 @@ def test_packed_batch_equals_dense_batch_when_lengths_agree(fa):
     del torch
 
 
+@pytest.mark.parametrize("d,dtype", [(64, "f16"), (128, "bf16")])
+@pytest.mark.parametrize("causal", [True, False])
+def test_packed_batch_over_several_rounds_equals_its_sequences_alone(fa, oracle_mod, d, dtype, causal):
+    # 21 sequences of 0 to 1500 tokens, 8 query heads over 2 key/value heads:
+    # about 1000 units, several rounds on 152 SMs, dealt heaviest (sequence,
+    # block) class first from an order computed on the device.  Every unit is
+    # whole in one CTA, so each sequence's rows must be bit-identical to the same
+    # sequence run alone as a dense batch under the unit schedule.
+    rng = np.random.default_rng(1300 + d + causal)
+    lens = [int(x) for x in rng.integers(1, 1500, 20)] + [0]
+    rng.shuffle(lens)
+    Hq, Hkv = 8, 2
+    q, k, v, cu_q, cu_k = pack(lens, lens, Hq, Hkv, d, dtype, 1310 + d)
+    scale = 1.0 / np.sqrt(d)
+    got = run_varlen(fa, q, k, v, cu_q, cu_k, dtype, causal, scale)
+    for b, n in enumerate(lens):
+        if n == 0:
+            continue
+        sl = slice(int(cu_q[b]), int(cu_q[b + 1]))
+        qs, ks, vs = (np.ascontiguousarray(x[sl].transpose(1, 0, 2)[None]) for x in (q, k, v))
+        alone = run_dense(fa, qs, ks, vs, dtype, causal, scale, "f32", flags=fa.FA_FLAG_SCHEDULE_UNITS)
+        assert np.array_equal(got[sl].transpose(1, 0, 2)[None], alone), f"sequence {b} ({n} tokens)"
+    b = int(np.argmax(lens))
+    sl = slice(int(cu_q[b]), int(cu_q[b + 1]))
+    qs, ks, vs = (np.ascontiguousarray(x[sl].transpose(1, 0, 2)[None]) for x in (q, k, v))
+    rows = G.sample_rows(lens[b], 5)
+    want = oracle_dense(oracle_mod, qs, ks, vs, dtype, causal, scale, rows=rows)
+    G.assert_close(got[sl].transpose(1, 0, 2)[None][:, :, rows], want, dtype, "f32",
+                   f"packed sequence {b} d={d} causal={causal}")
+
+
 # ------------------------------------------------------------ stream-K, causal
 @pytest.mark.parametrize("shape", [(1, 12, 12, 2048, 2048, 64), (2, 3, 3, 1000, 1000, 128),
                                    (1, 4, 2, 700, 1500, 64), (1, 2, 2, 300, 300, 64)])
