@@ -45,8 +45,8 @@ NCU_TRAFFIC = {
     # d=128, bf16): --set full at N=8192, the two DRAM counters alone at 4096 and
     # 16384 (one pass each, on the full-size problem).
     "prefill": {"src": ["fa_prefill_sm103.cu", "fa_tiles.cuh", "sm103_ptx.cuh"],
-                "src_sha": "530f2202b99ec8b5",
-                "bytes_per_launch": {"4096": 50.44e6, "8192": 114.70e6, "16384": 254.23e6}},
+                "src_sha": "e952fd9eb477dd27",
+                "bytes_per_launch": {"4096": 50.46e6, "8192": 114.69e6, "16384": 253.71e6}},
     # one decode_split_kernel<64> launch of the step's decode problem (B=32, H=14)
     "decode": {"src": ["fa_decode_sm103.cu", "sm103_ptx.cuh"], "src_sha": "9066595177c6f87f",
                "bytes_per_launch": 263.58e6},
