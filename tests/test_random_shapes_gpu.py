@@ -195,6 +195,53 @@ def test_random_backward(fa, oracle_mod, case):
                           f"causal={causal} scale={scale:.3f}: {e:.3e} > {tol:.3e}")
 
 
+# Packed batches over several rounds of units (8 to 40 sequences of 0 to 1500
+# tokens, up to 16 query heads), which the kernel deals heaviest (sequence, block)
+# class first in an order computed on the device: every sequence's rows must be
+# bit-identical to that sequence run alone as a dense batch under the unit
+# schedule, and one sequence is checked against the oracle on sampled rows.
+@pytest.mark.parametrize("case", range(8))
+def test_random_large_packed_batch(fa, oracle_mod, case):
+    import torch
+    rng = np.random.default_rng(70000 + case)
+    nseq = int(rng.integers(8, 41))
+    Hkv = int(rng.integers(1, 5))
+    Hq = Hkv * int(rng.choice([1, 2, 4]))
+    d = int(rng.choice([64, 128]))
+    dt = "bf16" if d == 128 else "f16"
+    causal = bool(rng.integers(0, 2))
+    lens = rng.integers(0, 1501, size=nseq)
+    lens[int(rng.integers(0, nseq))] = max(int(lens.max()), 1)
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    T = int(cu[-1])
+    scale = 1.0 / np.sqrt(d)
+    q = inputs.normal_bits((T, Hq, d), 71000 + case, dt)
+    k = inputs.normal_bits((T, Hkv, d), 72000 + case, dt)
+    v = inputs.normal_bits((T, Hkv, d), 73000 + case, dt)
+    cu_d = torch.from_numpy(cu).cuda()
+    out = fa.prefill_varlen(*(G.bits_to_device(x, dt) for x in (q, k, v)), cu_d, cu_d, int(lens.max()),
+                            int(lens.max()), causal=causal, scale=scale, out_dtype=torch.float32)
+    got = G.device_to_f64(out)
+    for b, n in enumerate(lens):
+        if n == 0:
+            continue
+        sl = slice(int(cu[b]), int(cu[b + 1]))
+        alone = fa.prefill(*(G.bits_to_device(np.ascontiguousarray(x[sl].transpose(1, 0, 2)[None]), dt)
+                             for x in (q, k, v)), causal=causal, scale=scale, out_dtype=torch.float32,
+                           flags=fa.FA_FLAG_SCHEDULE_UNITS)
+        assert np.array_equal(got[sl].transpose(1, 0, 2)[None], G.device_to_f64(alone)), (
+            f"packed case {case}: sequence {b} of {nseq} ({n} tokens), Hq={Hq} Hkv={Hkv} d={d} causal={causal}")
+    b = int(rng.integers(0, nseq))
+    while lens[b] == 0:
+        b = (b + 1) % nseq
+    sl = slice(int(cu[b]), int(cu[b + 1]))
+    rows = G.sample_rows(int(lens[b]), case)
+    want = oracle_mod.attention(*(oracle_mod.bits_to_f64(np.ascontiguousarray(x[sl].transpose(1, 0, 2)[None]), dt)
+                                  for x in (q, k, v)), causal, scale, rows=rows, threads=G.THREADS)
+    G.assert_close(got[sl].transpose(1, 0, 2)[None][:, :, rows], want, dt, "f32",
+                   f"packed case {case}: sequence {b} against the oracle")
+
+
 # Larger shapes: 700 to 6000 keys and up to 32 heads, so that stream-K cuts units
 # between CTAs and the persistent grids run several units per CTA; the forward is
 # checked on sampled rows (tile edges, the middle, the end and seeded rows), the
