@@ -263,8 +263,14 @@ int fa_prefill_plan(int B, int Hq, int Nq, int Nk, int causal, unsigned flags,
  *   causal      : per sequence, as fa_prefill_gqa (queries are the last
  *                 positions of their sequence).
  * A sequence with no keys gives zero rows; total_q == 0 returns FA_OK at once.
- * Always scheduled unit by unit (no scratch memory).  The lengths stay on the
- * device: nothing is copied back to the host.
+ * Always scheduled unit by unit.  When the units take more than one round of
+ * the SMs (and the batch has at most 4096 (sequence, 256-query block) pairs), a
+ * one-CTA kernel on `stream` first sorts those pairs by their work, from the
+ * device-resident offsets, into 4 bytes per pair of scratch from the library's
+ * pool (FA_ERR_WORKSPACE if that allocation fails), and the units are dealt
+ * heaviest first; otherwise no scratch is used.  Either way every unit is
+ * computed whole by one CTA, so the output does not depend on the order.  The
+ * lengths stay on the device: nothing is copied back to the host.
  */
 int fa_prefill_varlen(const void *q, const void *k, const void *v, void *out,
                       const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
