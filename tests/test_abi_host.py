@@ -238,6 +238,22 @@ def test_backward_argument_errors(lib):
     assert call(dv=B_ + 16) == binding.FA_ERR_ALIAS    # dv over dq
 
 
+@pytest.mark.parametrize("flags", [binding.FA_BWD_FLAG_NONE, binding.FA_BWD_RECOMPUTE_DQ, 0x80])
+def test_backward_ex_argument_errors_match_the_plain_call(lib, flags):
+    # the flags only pick the dQ pass: every argument error is the plain call's
+    args = dict(q=A, k=A + 4096, v=A + 8192, out=A + 12288, dout=A + 16384, lse=A + 20480,
+                dq=B_, dk=B_ + (1 << 20), dv=B_ + (2 << 20), B=1, H=6, Hkv=2, N=8, d=64, causal=1,
+                scale=0.125, it=0, gt=2)
+    order = ("q", "k", "v", "out", "dout", "lse", "dq", "dk", "dv", "B", "H", "Hkv", "N", "d", "causal",
+             "scale", "it", "gt")
+    for bad in (dict(lse=None), dict(Hkv=4), dict(N=0), dict(d=96), dict(gt=7), dict(lse=A + 20482),
+                dict(scale=float("nan")), dict(dk=A), dict(dv=B_ + 16), dict(q=A + 8)):
+        a = {**args, **bad}
+        plain = binding.fa_prefill_backward(*(a[x] for x in order), None)
+        ex = binding.fa_prefill_backward_ex(*(a[x] for x in order), flags, None)
+        assert plain == ex != binding.FA_OK, bad
+
+
 def test_plain_prefill_checks_too(lib):
     assert binding.fa_prefill(None, A, A, B_, 1, 1, 1, 64, 0, 1.0, None) == 1
     assert binding.fa_prefill(A, A, A, B_, 1, 1, 1, 80, 0, 1.0, None) == 3

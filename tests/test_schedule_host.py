@@ -179,3 +179,57 @@ def test_units_flag_and_packed_rows_never_cut(lib):
     # rows that see no key (Nq > Nk, causal) rule stream-K out
     _, info, _ = binding.fa_prefill_plan(1, 16, 8192, 4096, 1, 4, 152)
     assert info[0] == 0
+
+
+# ---------------------------------------------------------------------------
+# The ordered schedule of packed batches (packed_order_kernel and the ordered
+# instantiation's unit mapping in fa_prefill_sm103.cu), restated: the classes
+# (sequence b, 256-row block qb) are sorted by their 128 x 128 tile products,
+# most first, ties by class index; unit u of the grid's round-robin deal is head
+# u % Hq of class order[u // Hq].
+
+def packed_order(lens_q, lens_k, n_qb, causal):
+    keys = []
+    for b, (nq, nk) in enumerate(zip(lens_q, lens_k)):
+        for qb in range(n_qb):
+            c = kv_tiles(causal, 0, nq, nk, qb * R) + kv_tiles(causal, 0, nq, nk, qb * R + BM)
+            keys.append((0x7fffffff - c, b * n_qb + qb))
+    return [cls for _, cls in sorted(keys)], {cls: 0x7fffffff - k for k, cls in keys}
+
+
+def ordered_units(lens_q, lens_k, Hq, causal, G):
+    n_qb = (max(lens_q) + R - 1) // R
+    order, cost = packed_order(lens_q, lens_k, n_qb, causal)
+    B = len(lens_q)
+    n_units = B * Hq * n_qb
+    per_cta = [[] for _ in range(G)]
+    for u in range(n_units):
+        k, r = divmod(u, G)
+        c = G - 1 - r if k & 1 else r               # the snake deal of the unit schedule
+        cls = order[u // Hq]
+        per_cta[c].append((cls // n_qb, u % Hq, cls % n_qb, cost[cls]))
+    return per_cta, n_units
+
+
+@pytest.mark.parametrize("seed", range(6))
+@pytest.mark.parametrize("causal", [0, 1])
+def test_ordered_packed_schedule_deals_every_unit_once_heaviest_first(seed, causal):
+    rng = random.Random(seed)
+    B = rng.randint(8, 40)
+    Hq = rng.choice([1, 2, 6, 16])
+    lens = [rng.randint(0, 4096) for _ in range(B)]
+    lens[rng.randrange(B)] = max(max(lens), 1)
+    G = 152
+    per_cta, n_units = ordered_units(lens, lens, Hq, causal, G)
+    n_qb = (max(lens) + R - 1) // R
+    dealt = sorted((b, h, qb) for units in per_cta for b, h, qb, _ in units)
+    assert dealt == sorted((b, h, qb) for b in range(B) for h in range(Hq) for qb in range(n_qb))
+    # the deal's rounds never go from a lighter class to a heavier one
+    flat = []
+    for u in range(n_units):
+        k, r = divmod(u, G)
+        flat.append(per_cta[G - 1 - r if k & 1 else r][k][3])
+    assert all(a >= b for a, b in zip(flat, flat[1:]))
+    # and the busiest CTA is within one heaviest unit of the average
+    loads = [sum(x[3] for x in units) for units in per_cta]
+    assert max(loads) <= sum(loads) / G + max(flat)
